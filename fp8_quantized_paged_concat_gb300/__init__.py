@@ -1,0 +1,216 @@
+"""GB300 quantized paged KV-cache write and gather-upconvert.
+
+Thin Python binding over libkvq.so (include/kvq.h): each function has the
+name of the C entry point, checks dtypes / devices / shapes of the torch
+tensors it is given, passes their data pointers and strides and the current
+CUDA stream, and raises RuntimeError on a non-OK status.  Every step of the
+computation runs in the library's sm_103a kernels; there is no fallback.  The
+library is built by ``__graft_entry__.build()`` (or
+``python -m fp8_quantized_paged_concat_gb300._build``); importing this
+package does not load it, the first call does, and fails loudly if it is
+missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "kvq_write_nvfp4_ds_mla", "kvq_write_fp8_ds_mla", "kvq_gather_upconvert_nvfp4_ds_mla",
+    "kvq_gather_upconvert_fp8_ds_mla", "kvq_reshape_and_cache_nvfp4", "kvq_selftest_convert",
+    "kvq_last_error_string", "kvq_version", "library_path", "load_library",
+    "NVFP4_DS_MLA_ENTRY_BYTES", "FP8_DS_MLA_ENTRY_BYTES", "STATUS_BAD_INDEX", "STATUS_BAD_BATCH",
+    "nvfp4_full_dim",
+]
+
+NVFP4_DS_MLA_ENTRY_BYTES = 352
+FP8_DS_MLA_ENTRY_BYTES = 656
+STATUS_BAD_INDEX = 0x1
+STATUS_BAD_BATCH = 0x2
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+_U32 = ctypes.c_uint32
+
+_SIGNATURES = {
+    "kvq_write_nvfp4_ds_mla": [_P, _I64, _P, _I64, _P, _I64, _P, _I64, _I32, _I64, _I64, _P, _P],
+    "kvq_write_fp8_ds_mla": [_P, _I64, _P, _I64, _P, _I64, _P, _I64, _I32, _I64, _I64, _P, _P],
+    "kvq_gather_upconvert_nvfp4_ds_mla": [_P, _I64, _I32, _I64, _I64, _P, _I64, _I64, _P, _I64,
+                                          _I32, _P, _P, _I32, _P, _P],
+    "kvq_gather_upconvert_fp8_ds_mla": [_P, _I64, _I32, _I64, _I64, _P, _I64, _I64, _P, _I64,
+                                        _I32, _P, _P, _I32, _P, _P],
+    "kvq_reshape_and_cache_nvfp4": [_P, _P, _I64, _I64, _I64, _I64, _P, _I64, _I32, _I32, _P, _I64,
+                                    _I32, _P, _P, _P, _P],
+    "kvq_selftest_convert": [_U32, _I64, _P, _P, _P, _P, _P, _P],
+}
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "_lib", "libkvq.so")
+
+
+def load_library():
+    """Loads libkvq.so (once).  Raises RuntimeError if it has not been built."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
+                               "(there is no CPU fallback)")
+        handle = ctypes.CDLL(path)
+        for name, argtypes in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.argtypes = argtypes
+            fn.restype = _I32
+        handle.kvq_last_error_string.restype = ctypes.c_char_p
+        handle.kvq_last_error_string.argtypes = []
+        handle.kvq_version.restype = _I32
+        handle.kvq_version.argtypes = []
+        _lib = handle
+    return _lib
+
+
+def kvq_last_error_string() -> str:
+    return load_library().kvq_last_error_string().decode()
+
+
+def kvq_version() -> int:
+    return load_library().kvq_version()
+
+
+def nvfp4_full_dim(head_size: int) -> int:
+    """Last dimension of the per-head NVFP4 cache: head_size/2 + head_size/16."""
+    return head_size // 2 + head_size // 16
+
+
+def _call(name: str, *args):
+    status = getattr(load_library(), name)(*args)
+    if status != 0:
+        raise RuntimeError(f"{name} failed (status {status}): {kvq_last_error_string()}")
+
+
+def _stream(stream, device) -> int:
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def _status_ptr(status):
+    if status is None:
+        return None
+    if status.dtype != torch.int32 or not status.is_cuda or status.numel() < 1:
+        raise ValueError("status must be a CUDA int32 tensor with at least one element")
+    return status.data_ptr()
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _bf16_rows(name, t, width):
+    _need(t.dtype == torch.bfloat16 and t.is_cuda and t.dim() == 2 and t.shape[1] >= width
+          and t.stride(1) == 1, f"{name}: expected a CUDA bf16 [T, >={width}] tensor with unit inner stride")
+
+
+def _mla_cache(name, t, entry):
+    _need(t.dtype == torch.uint8 and t.is_cuda and t.dim() == 3 and t.shape[2] >= entry
+          and t.stride(2) == 1, f"{name}: expected a CUDA uint8 [num_blocks, block_size, >={entry}] tensor")
+
+
+def _write(cname, entry, kv_c, k_pe, kv_cache, slot_mapping, status, stream):
+    _bf16_rows("kv_c", kv_c, 512)
+    _bf16_rows("k_pe", k_pe, 64)
+    _mla_cache("kv_cache", kv_cache, entry)
+    _need(slot_mapping.dtype == torch.int64 and slot_mapping.is_cuda and slot_mapping.dim() == 1
+          and slot_mapping.is_contiguous(), "slot_mapping: expected a contiguous CUDA int64 vector")
+    T = slot_mapping.shape[0]
+    _need(kv_c.shape[0] >= T and k_pe.shape[0] >= T, "kv_c / k_pe have fewer rows than slot_mapping")
+    _call(cname, kv_c.data_ptr(), kv_c.stride(0), k_pe.data_ptr(), k_pe.stride(0),
+          slot_mapping.data_ptr(), T, kv_cache.data_ptr(), kv_cache.shape[0], kv_cache.shape[1],
+          kv_cache.stride(0), kv_cache.stride(1), _status_ptr(status), _stream(stream, kv_cache.device))
+
+
+def kvq_write_nvfp4_ds_mla(kv_c, k_pe, kv_cache, slot_mapping, status=None, stream=None):
+    """Writes 352-byte nvfp4_ds_mla entries: kv_c bf16 [T, 512], k_pe bf16
+    [T, 64], kv_cache uint8 [num_blocks, block_size, >=352], slot_mapping
+    int64 [T] (negative = padding).  Asynchronous on ``stream``."""
+    _write("kvq_write_nvfp4_ds_mla", 352, kv_c, k_pe, kv_cache, slot_mapping, status, stream)
+
+
+def kvq_write_fp8_ds_mla(kv_c, k_pe, kv_cache, slot_mapping, status=None, stream=None):
+    """Writes 656-byte fp8_ds_mla entries (arguments as kvq_write_nvfp4_ds_mla)."""
+    _write("kvq_write_fp8_ds_mla", 656, kv_c, k_pe, kv_cache, slot_mapping, status, stream)
+
+
+def _gather(cname, entry, src_cache, dst, block_table, workspace_starts, seq_starts, batch_size,
+            status, stream):
+    _mla_cache("src_cache", src_cache, entry)
+    _bf16_rows("dst", dst, 576)
+    for name, t in (("block_table", block_table), ("workspace_starts", workspace_starts),
+                    ("seq_starts", seq_starts)):
+        _need(t.dtype == torch.int32 and t.is_cuda, f"{name}: expected a CUDA int32 tensor")
+    _need(block_table.dim() == 2 and block_table.stride(1) == 1, "block_table: expected [B, W] rows")
+    _need(workspace_starts.is_contiguous() and seq_starts.is_contiguous(),
+          "workspace_starts / seq_starts must be contiguous")
+    B = int(seq_starts.shape[0]) if batch_size is None else int(batch_size)
+    _need(B <= seq_starts.shape[0] and B <= workspace_starts.shape[0] and B <= block_table.shape[0],
+          "batch_size exceeds the metadata tensors")
+    _call(cname, src_cache.data_ptr(), src_cache.shape[0], src_cache.shape[1], src_cache.stride(0),
+          src_cache.stride(1), dst.data_ptr(), dst.stride(0), dst.shape[0], block_table.data_ptr(),
+          block_table.stride(0), block_table.shape[1], workspace_starts.data_ptr(),
+          seq_starts.data_ptr(), B, _status_ptr(status), _stream(stream, dst.device))
+
+
+def kvq_gather_upconvert_nvfp4_ds_mla(src_cache, dst, block_table, workspace_starts, seq_starts,
+                                      batch_size=None, status=None, stream=None):
+    """Gathers nvfp4_ds_mla pages into dst bf16 [T, 576] (T = dst rows):
+    block_table int32 [B, W], workspace_starts / seq_starts int32 [B]."""
+    _gather("kvq_gather_upconvert_nvfp4_ds_mla", 352, src_cache, dst, block_table,
+            workspace_starts, seq_starts, batch_size, status, stream)
+
+
+def kvq_gather_upconvert_fp8_ds_mla(src_cache, dst, block_table, workspace_starts, seq_starts,
+                                    batch_size=None, status=None, stream=None):
+    """Gathers fp8_ds_mla pages into dst bf16 [T, 576] (as the nvfp4 gather)."""
+    _gather("kvq_gather_upconvert_fp8_ds_mla", 656, src_cache, dst, block_table,
+            workspace_starts, seq_starts, batch_size, status, stream)
+
+
+def kvq_reshape_and_cache_nvfp4(key, value, kv_cache, slot_mapping, k_scale, v_scale,
+                                status=None, stream=None):
+    """Writes the per-head NVFP4 cache uint8 [P, 2, block_size, H, full_dim]
+    from key / value bf16 [T, H, D]; k_scale / v_scale CUDA fp32 scalars."""
+    for name, t in (("key", key), ("value", value)):
+        _need(t.dtype == torch.bfloat16 and t.is_cuda and t.dim() == 3 and t.stride(2) == 1,
+              f"{name}: expected a CUDA bf16 [T, H, D] tensor with unit inner stride")
+    _need(key.shape == value.shape, "key and value shapes differ")
+    T, H, D = key.shape
+    _need(kv_cache.dtype == torch.uint8 and kv_cache.is_cuda and kv_cache.dim() == 5
+          and kv_cache.is_contiguous() and kv_cache.shape[1] == 2 and kv_cache.shape[3] == H
+          and kv_cache.shape[4] == nvfp4_full_dim(D),
+          "kv_cache: expected a contiguous CUDA uint8 [P, 2, block_size, H, D/2 + D/16] tensor")
+    _need(slot_mapping.dtype == torch.int64 and slot_mapping.is_cuda and slot_mapping.is_contiguous()
+          and slot_mapping.shape[0] == T, "slot_mapping: expected a contiguous CUDA int64 [T]")
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        _need(t.dtype == torch.float32 and t.is_cuda and t.numel() >= 1, f"{name}: CUDA fp32 scalar")
+    _call("kvq_reshape_and_cache_nvfp4", key.data_ptr(), value.data_ptr(), key.stride(0),
+          key.stride(1), value.stride(0), value.stride(1), slot_mapping.data_ptr(), T, H, D,
+          kv_cache.data_ptr(), kv_cache.shape[0], kv_cache.shape[2], k_scale.data_ptr(),
+          v_scale.data_ptr(), _status_ptr(status), _stream(stream, kv_cache.device))
+
+
+def kvq_selftest_convert(first_bits: int, count: int, device="cuda", stream=None):
+    """Device converters over float32 bit patterns first_bits..+count-1:
+    returns (e4m3_lo, e4m3_hi, e2m1_lo, e2m1_hi, bf16) CUDA tensors."""
+    outs = [torch.empty(count, dtype=torch.uint8, device=device) for _ in range(4)]
+    bf16 = torch.empty(count, dtype=torch.int16, device=device)
+    _call("kvq_selftest_convert", first_bits & 0xFFFFFFFF, count, *(o.data_ptr() for o in outs),
+          bf16.data_ptr(), _stream(stream, outs[0].device))
+    return (*outs, bf16)

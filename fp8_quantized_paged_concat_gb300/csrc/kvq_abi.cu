@@ -1,0 +1,249 @@
+// kvq_abi.cu -- the extern "C" entry points declared in include/kvq.h:
+// host-side validation, device check, launch on the caller's stream, status.
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "kvq.h"
+#include "kvq_launch.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kvq_status fail(kvq_status code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+kvq_status ok() {
+  g_last_error.clear();
+  return KVQ_OK;
+}
+
+bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+// The kernels are built for sm_103a only (GB300); the pages gate the NVFP4
+// DS-MLA format on compute capability 10.x.
+kvq_status check_device(const char* fn, int* num_sms = nullptr) {
+  int dev = 0, major = 0, minor = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e == cudaSuccess && num_sms != nullptr)
+    e = cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+  if (major != 10 || minor != 3)
+    return fail(KVQ_ERR_UNSUPPORTED_DEVICE,
+                "%s: this library is built for sm_103a (GB300); device %d is sm_%d%d", fn, dev,
+                major, minor);
+  return KVQ_OK;
+}
+
+kvq_status launched(const char* fn, cudaError_t e) {
+  if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+  return ok();
+}
+
+#define KVQ_REQUIRE(cond, ...) \
+  do {                         \
+    if (!(cond)) return fail(KVQ_ERR_INVALID_ARG, __VA_ARGS__); \
+  } while (0)
+
+// Shared checks of a [num_blocks, block_size, entry] cache.
+kvq_status check_mla_cache(const char* fn, const void* cache, int64_t num_blocks,
+                           int32_t block_size, int64_t block_stride, int64_t entry_stride,
+                           int64_t entry_bytes) {
+  KVQ_REQUIRE(cache != nullptr, "%s: cache is NULL", fn);
+  KVQ_REQUIRE(aligned(cache, 16), "%s: cache base must be 16-byte aligned", fn);
+  KVQ_REQUIRE(num_blocks > 0 && block_size > 0, "%s: num_blocks and block_size must be positive", fn);
+  KVQ_REQUIRE(num_blocks <= INT64_MAX / block_size, "%s: num_blocks * block_size overflows", fn);
+  KVQ_REQUIRE(entry_stride >= entry_bytes && entry_stride % 16 == 0,
+              "%s: entry_stride must be >= %lld and a multiple of 16 (got %lld)", fn,
+              static_cast<long long>(entry_bytes), static_cast<long long>(entry_stride));
+  KVQ_REQUIRE(block_stride > 0 && block_stride % 16 == 0,
+              "%s: block_stride must be a positive multiple of 16 (got %lld)", fn,
+              static_cast<long long>(block_stride));
+  return KVQ_OK;
+}
+
+kvq_status check_bf16_rows(const char* fn, const char* name, const void* p, int64_t stride,
+                           int64_t width) {
+  KVQ_REQUIRE(p != nullptr, "%s: %s is NULL", fn, name);
+  KVQ_REQUIRE(aligned(p, 16), "%s: %s must be 16-byte aligned", fn, name);
+  KVQ_REQUIRE(stride >= width && stride % 8 == 0,
+              "%s: %s row stride must be >= %lld and a multiple of 8 elements (got %lld)", fn, name,
+              static_cast<long long>(width), static_cast<long long>(stride));
+  return KVQ_OK;
+}
+
+kvq_status write_common(const char* fn, int64_t entry_bytes,
+                        cudaError_t (*launch)(const kvq::WriteArgs&, cudaStream_t),
+                        const void* kv_c, int64_t kv_c_stride, const void* k_pe,
+                        int64_t k_pe_stride, const int64_t* slot_mapping, int64_t num_tokens,
+                        uint8_t* kv_cache, int64_t num_blocks, int32_t block_size,
+                        int64_t block_stride, int64_t entry_stride, int32_t* d_status,
+                        kvq_stream_t stream) {
+  KVQ_REQUIRE(num_tokens >= 0, "%s: num_tokens < 0", fn);
+  if (num_tokens == 0) return ok();
+  KVQ_REQUIRE(num_tokens <= (int64_t{1} << 36), "%s: num_tokens too large", fn);
+  if (kvq_status s = check_bf16_rows(fn, "kv_c", kv_c, kv_c_stride, KVQ_MLA_NOPE_DIM)) return s;
+  if (kvq_status s = check_bf16_rows(fn, "k_pe", k_pe, k_pe_stride, KVQ_MLA_ROPE_DIM)) return s;
+  KVQ_REQUIRE(slot_mapping != nullptr, "%s: slot_mapping is NULL", fn);
+  KVQ_REQUIRE(aligned(slot_mapping, 8), "%s: slot_mapping must be 8-byte aligned", fn);
+  KVQ_REQUIRE(d_status == nullptr || aligned(d_status, 4), "%s: d_status misaligned", fn);
+  if (kvq_status s = check_mla_cache(fn, kv_cache, num_blocks, block_size, block_stride,
+                                     entry_stride, entry_bytes))
+    return s;
+  if (kvq_status s = check_device(fn)) return s;
+  const kvq::WriteArgs a{kv_c,      kv_c_stride, k_pe,       k_pe_stride,  slot_mapping,
+                         num_tokens, kv_cache,   num_blocks * block_size, block_size,
+                         block_stride, entry_stride, d_status};
+  return launched(fn, launch(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvq_status gather_common(const char* fn, int64_t entry_bytes,
+                         cudaError_t (*launch)(const kvq::GatherArgs&, cudaStream_t),
+                         const uint8_t* src_cache, int64_t num_blocks, int32_t block_size,
+                         int64_t block_stride, int64_t entry_stride, void* dst, int64_t dst_stride,
+                         int64_t num_out_tokens, const int32_t* block_table,
+                         int64_t block_table_stride, int32_t block_table_width,
+                         const int32_t* workspace_starts, const int32_t* seq_starts,
+                         int32_t batch_size, int32_t* d_status, kvq_stream_t stream) {
+  KVQ_REQUIRE(num_out_tokens >= 0, "%s: num_out_tokens < 0", fn);
+  if (num_out_tokens == 0) return ok();
+  KVQ_REQUIRE(num_out_tokens <= INT32_MAX, "%s: num_out_tokens exceeds int32 workspace_starts", fn);
+  if (kvq_status s = check_mla_cache(fn, src_cache, num_blocks, block_size, block_stride,
+                                     entry_stride, entry_bytes))
+    return s;
+  if (kvq_status s = check_bf16_rows(fn, "dst", dst, dst_stride, KVQ_WORKSPACE_DIM)) return s;
+  KVQ_REQUIRE(batch_size > 0, "%s: batch_size must be positive", fn);
+  KVQ_REQUIRE(block_table != nullptr && workspace_starts != nullptr && seq_starts != nullptr,
+              "%s: block_table, workspace_starts and seq_starts must be non-NULL", fn);
+  KVQ_REQUIRE(aligned(block_table, 4) && aligned(workspace_starts, 4) && aligned(seq_starts, 4),
+              "%s: int32 arrays must be 4-byte aligned", fn);
+  KVQ_REQUIRE(block_table_width > 0 && block_table_stride >= block_table_width,
+              "%s: need block_table_width > 0 and block_table_stride >= block_table_width", fn);
+  KVQ_REQUIRE(d_status == nullptr || aligned(d_status, 4), "%s: d_status misaligned", fn);
+  if (kvq_status s = check_device(fn)) return s;
+  const kvq::GatherArgs a{src_cache,        num_blocks,       block_size,        block_stride,
+                          entry_stride,     dst,              dst_stride,        num_out_tokens,
+                          block_table,      block_table_stride, block_table_width, workspace_starts,
+                          seq_starts,       batch_size,       d_status};
+  return launched(fn, launch(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_write_nvfp4_ds_mla(const void* kv_c, int64_t kv_c_stride, const void* k_pe,
+                                  int64_t k_pe_stride, const int64_t* slot_mapping,
+                                  int64_t num_tokens, uint8_t* kv_cache, int64_t num_blocks,
+                                  int32_t block_size, int64_t block_stride, int64_t entry_stride,
+                                  int32_t* d_status, kvq_stream_t stream) {
+  return write_common("kvq_write_nvfp4_ds_mla", KVQ_NVFP4_DS_MLA_ENTRY_BYTES,
+                      kvq::launch_write_nvfp4_ds_mla, kv_c, kv_c_stride, k_pe, k_pe_stride,
+                      slot_mapping, num_tokens, kv_cache, num_blocks, block_size, block_stride,
+                      entry_stride, d_status, stream);
+}
+
+kvq_status kvq_write_fp8_ds_mla(const void* kv_c, int64_t kv_c_stride, const void* k_pe,
+                                int64_t k_pe_stride, const int64_t* slot_mapping,
+                                int64_t num_tokens, uint8_t* kv_cache, int64_t num_blocks,
+                                int32_t block_size, int64_t block_stride, int64_t entry_stride,
+                                int32_t* d_status, kvq_stream_t stream) {
+  return write_common("kvq_write_fp8_ds_mla", KVQ_FP8_DS_MLA_ENTRY_BYTES,
+                      kvq::launch_write_fp8_ds_mla, kv_c, kv_c_stride, k_pe, k_pe_stride,
+                      slot_mapping, num_tokens, kv_cache, num_blocks, block_size, block_stride,
+                      entry_stride, d_status, stream);
+}
+
+kvq_status kvq_gather_upconvert_nvfp4_ds_mla(
+    const uint8_t* src_cache, int64_t num_blocks, int32_t block_size, int64_t block_stride,
+    int64_t entry_stride, void* dst, int64_t dst_stride, int64_t num_out_tokens,
+    const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width,
+    const int32_t* workspace_starts, const int32_t* seq_starts, int32_t batch_size,
+    int32_t* d_status, kvq_stream_t stream) {
+  return gather_common("kvq_gather_upconvert_nvfp4_ds_mla", KVQ_NVFP4_DS_MLA_ENTRY_BYTES,
+                       kvq::launch_gather_nvfp4_ds_mla, src_cache, num_blocks, block_size,
+                       block_stride, entry_stride, dst, dst_stride, num_out_tokens, block_table,
+                       block_table_stride, block_table_width, workspace_starts, seq_starts,
+                       batch_size, d_status, stream);
+}
+
+kvq_status kvq_gather_upconvert_fp8_ds_mla(
+    const uint8_t* src_cache, int64_t num_blocks, int32_t block_size, int64_t block_stride,
+    int64_t entry_stride, void* dst, int64_t dst_stride, int64_t num_out_tokens,
+    const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width,
+    const int32_t* workspace_starts, const int32_t* seq_starts, int32_t batch_size,
+    int32_t* d_status, kvq_stream_t stream) {
+  return gather_common("kvq_gather_upconvert_fp8_ds_mla", KVQ_FP8_DS_MLA_ENTRY_BYTES,
+                       kvq::launch_gather_fp8_ds_mla, src_cache, num_blocks, block_size,
+                       block_stride, entry_stride, dst, dst_stride, num_out_tokens, block_table,
+                       block_table_stride, block_table_width, workspace_starts, seq_starts,
+                       batch_size, d_status, stream);
+}
+
+kvq_status kvq_reshape_and_cache_nvfp4(const void* key, const void* value, int64_t key_stride_t,
+                                       int64_t key_stride_h, int64_t value_stride_t,
+                                       int64_t value_stride_h, const int64_t* slot_mapping,
+                                       int64_t num_tokens, int32_t num_heads, int32_t head_size,
+                                       uint8_t* kv_cache, int64_t num_pages, int32_t block_size,
+                                       const float* k_scale, const float* v_scale,
+                                       int32_t* d_status, kvq_stream_t stream) {
+  const char* fn = "kvq_reshape_and_cache_nvfp4";
+  KVQ_REQUIRE(num_tokens >= 0, "%s: num_tokens < 0", fn);
+  if (num_tokens == 0) return ok();
+  KVQ_REQUIRE(num_heads > 0 && head_size >= 16 && head_size % 16 == 0,
+              "%s: need num_heads > 0 and head_size a positive multiple of 16", fn);
+  KVQ_REQUIRE(num_tokens * 2 * num_heads * (head_size / 16) < (int64_t{1} << 40),
+              "%s: problem too large", fn);
+  KVQ_REQUIRE(key != nullptr && value != nullptr, "%s: key / value is NULL", fn);
+  KVQ_REQUIRE(aligned(key, 16) && aligned(value, 16), "%s: key / value must be 16-byte aligned", fn);
+  KVQ_REQUIRE(key_stride_t % 8 == 0 && key_stride_h % 8 == 0 && value_stride_t % 8 == 0 &&
+                  value_stride_h % 8 == 0 && key_stride_t >= 0 && key_stride_h >= 0 &&
+                  value_stride_t >= 0 && value_stride_h >= 0,
+              "%s: key / value strides must be non-negative multiples of 8 elements", fn);
+  KVQ_REQUIRE(slot_mapping != nullptr && aligned(slot_mapping, 8), "%s: bad slot_mapping", fn);
+  KVQ_REQUIRE(k_scale != nullptr && v_scale != nullptr && aligned(k_scale, 4) && aligned(v_scale, 4),
+              "%s: k_scale / v_scale must be device fp32 scalars", fn);
+  KVQ_REQUIRE(kv_cache != nullptr && aligned(kv_cache, 16), "%s: kv_cache must be 16-byte aligned", fn);
+  KVQ_REQUIRE(num_pages > 0 && block_size > 0, "%s: num_pages and block_size must be positive", fn);
+  KVQ_REQUIRE(num_pages <= INT64_MAX / block_size, "%s: num_pages * block_size overflows", fn);
+  const int64_t full_dim = head_size / 2 + head_size / 16;
+  KVQ_REQUIRE((int64_t{block_size} * num_heads * full_dim) % 8 == 0 &&
+                  (int64_t{block_size} * num_heads * (head_size / 2)) % 8 == 0,
+              "%s: block_size * num_heads * full_dim must be a multiple of 8", fn);
+  KVQ_REQUIRE(d_status == nullptr || aligned(d_status, 4), "%s: d_status misaligned", fn);
+  if (kvq_status s = check_device(fn)) return s;
+  const kvq::PerHeadArgs a{key,          value,     key_stride_t, key_stride_h, value_stride_t,
+                           value_stride_h, slot_mapping, num_tokens, num_heads, head_size,
+                           kv_cache,     num_pages * block_size, block_size, k_scale, v_scale,
+                           d_status};
+  return launched(fn, kvq::launch_reshape_and_cache_nvfp4(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_selftest_convert(uint32_t first_bits, int64_t count, uint8_t* e4m3_lo,
+                                uint8_t* e4m3_hi, uint8_t* e2m1_lo, uint8_t* e2m1_hi,
+                                uint16_t* bf16_out, kvq_stream_t stream) {
+  const char* fn = "kvq_selftest_convert";
+  KVQ_REQUIRE(count >= 0 && count <= (int64_t{1} << 32), "%s: count out of range", fn);
+  if (count == 0) return ok();
+  int num_sms = 0;
+  if (kvq_status s = check_device(fn, &num_sms)) return s;
+  return launched(fn, kvq::launch_selftest_convert(first_bits, count, e4m3_lo, e4m3_hi, e2m1_lo,
+                                                   e2m1_hi, bf16_out, num_sms,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* kvq_last_error_string(void) { return g_last_error.c_str(); }
+
+int32_t kvq_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,142 @@
+// kvq_device.cuh -- device helpers shared by the sm_103a kernels: the
+// number-format conversions (hand-written PTX from the public ISA) and the
+// vector memory accesses.  Nothing here is visible outside the library.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr int kNopeDim = KVQ_MLA_NOPE_DIM;       // 512
+constexpr int kRopeDim = KVQ_MLA_ROPE_DIM;       // 64
+constexpr int kGroup = 16;                       // NVFP4 values per e4m3 scale
+constexpr int kNvEntry = KVQ_NVFP4_DS_MLA_ENTRY_BYTES;  // 352
+constexpr int kNvRopeOff = kNopeDim / 2;                 // 256
+constexpr int kNvSfOff = kNvRopeOff + kRopeDim;          // 320
+constexpr int kF8Entry = KVQ_FP8_DS_MLA_ENTRY_BYTES;     // 656
+constexpr int kF8Tile = 128;                             // NoPE values per fp32 scale
+constexpr int kF8ScaleOff = kNopeDim;                    // 512
+constexpr int kF8RopeOff = kF8ScaleOff + 4 * (kNopeDim / kF8Tile);  // 528
+constexpr int kWorkspaceDim = KVQ_WORKSPACE_DIM;         // 576
+constexpr unsigned kFull = 0xffffffffu;
+
+static_assert(kNvSfOff + kNopeDim / kGroup == kNvEntry, "352-byte entry");
+static_assert(kF8RopeOff + 2 * kRopeDim == kF8Entry, "656-byte entry");
+
+// ---------------------------------------------------------------------------
+// number formats
+// ---------------------------------------------------------------------------
+
+// Two fp32 -> two e2m1 codes, round to nearest even, satfinite
+// (cvt.rn.satfinite.e2m1x2.f32, the conversion the NVFP4 DS-MLA page's write
+// kernel names).  Returns lo's code in bits 3:0 and hi's in bits 7:4: the
+// instruction packs its first source operand into the upper nibble.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b;\n\tcvt.rn.satfinite.e2m1x2.f32 b, %1, %2;\n\tcvt.u32.u8 %0, b;\n\t}"
+      : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two fp32 -> two e4m3 codes, round to nearest even, satfinite.  lo's code in
+// bits 7:0, hi's in bits 15:8.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two e4m3 codes (bits 7:0 and 15:8) -> f16x2 holding the same two values
+// (exact: every e4m3 value is an f16 normal or zero).
+__device__ __forceinline__ __half2 e4m3x2_to_half2(uint32_t two_codes) {
+  uint32_t r;
+  const uint16_t v = static_cast<uint16_t>(two_codes);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return *reinterpret_cast<__half2*>(&r);
+}
+
+// Two e2m1 codes (bits 3:0 and 7:4 of the low byte) -> f16x2 (exact).
+__device__ __forceinline__ __half2 e2m1x2_to_half2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
+      : "=r"(r) : "r"(byte));
+  return *reinterpret_cast<__half2*>(&r);
+}
+
+__device__ __forceinline__ float e4m3_to_float(uint32_t code) {
+  return __low2float(e4m3x2_to_half2(code & 0xffu));
+}
+
+// Two fp32 -> bf16x2 bits (round to nearest even; lo in bits 15:0).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// The bf16 value held in bits 15:0 / 31:16 of a packed word, as fp32 (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// max(|a|, |b|) over the bf16 pairs of a packed word, kept packed.
+__device__ __forceinline__ __nv_bfloat162 abs_bf16x2(uint32_t w) {
+  uint32_t a = w & 0x7fff7fffu;
+  return *reinterpret_cast<__nv_bfloat162*>(&a);
+}
+
+// NVFP4 group of 16 fp32 values (already scaled): sf = e4m3(amax / 6),
+// inv = 1 / sf (0 when sf is 0), codes e2m1(x * inv) packed 2 per byte,
+// value 2k in the low nibble of byte k.  Divisions are IEEE round-to-nearest
+// (the library is built without fast-math), products single fp32 roundings.
+__device__ __forceinline__ uint32_t nvfp4_scale_code(float amax) {
+  return cvt_e4m3x2(amax / 6.0f, 0.0f) & 0xffu;
+}
+
+__device__ __forceinline__ float nvfp4_inverse_scale(uint32_t sf_code) {
+  const float sf = e4m3_to_float(sf_code);
+  return sf == 0.0f ? 0.0f : 1.0f / sf;
+}
+
+__device__ __forceinline__ uint2 nvfp4_pack16(const float (&x)[16], float inv) {
+  uint2 out;
+  uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    w0 |= cvt_e2m1x2(__fmul_rn(x[2 * k], inv), __fmul_rn(x[2 * k + 1], inv)) << (8 * k);
+    w1 |= cvt_e2m1x2(__fmul_rn(x[8 + 2 * k], inv), __fmul_rn(x[8 + 2 * k + 1], inv)) << (8 * k);
+  }
+  out.x = w0;
+  out.y = w1;
+  return out;
+}
+
+// ---------------------------------------------------------------------------
+// memory
+// ---------------------------------------------------------------------------
+
+// Read-once streaming loads (evict-first in L1 and L2).
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ uint2 ld_stream8(const void* p) {
+  return __ldcs(reinterpret_cast<const uint2*>(p));
+}
+__device__ __forceinline__ uint32_t ld_stream4(const void* p) {
+  return __ldcs(reinterpret_cast<const unsigned int*>(p));
+}
+__device__ __forceinline__ uint32_t ld_byte(const uint8_t* p) {
+  return __ldg(p);
+}
+
+__device__ __forceinline__ void st16(void* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
+__device__ __forceinline__ void st8(void* p, uint2 v) { *reinterpret_cast<uint2*>(p) = v; }
+__device__ __forceinline__ void st4(void* p, uint32_t v) { *reinterpret_cast<uint32_t*>(p) = v; }
+
+__device__ __forceinline__ void report(int32_t* status, int32_t bits) {
+  if (status != nullptr) atomicOr(status, bits);
+}
+
+}  // namespace kvq

@@ -1,0 +1,69 @@
+// kvq_launch.h -- host launchers of the kernels (one per .cu file), called by
+// the C ABI in kvq_abi.cu after it has validated the arguments.  Each returns
+// the cudaError_t of its launch.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace kvq {
+
+struct WriteArgs {
+  const void* kv_c;
+  int64_t kv_c_stride;
+  const void* k_pe;
+  int64_t k_pe_stride;
+  const int64_t* slot_mapping;
+  int64_t num_tokens;
+  uint8_t* cache;
+  int64_t num_slots;     // num_blocks * block_size
+  int32_t block_size;
+  int64_t block_stride;
+  int64_t entry_stride;
+  int32_t* status;
+};
+
+struct GatherArgs {
+  const uint8_t* cache;
+  int64_t num_blocks;
+  int32_t block_size;
+  int64_t block_stride;
+  int64_t entry_stride;
+  void* dst;
+  int64_t dst_stride;
+  int64_t num_out;
+  const int32_t* block_table;
+  int64_t block_table_stride;
+  int32_t block_table_width;
+  const int32_t* workspace_starts;
+  const int32_t* seq_starts;
+  int32_t batch_size;
+  int32_t* status;
+};
+
+struct PerHeadArgs {
+  const void* key;
+  const void* value;
+  int64_t key_stride_t, key_stride_h, value_stride_t, value_stride_h;
+  const int64_t* slot_mapping;
+  int64_t num_tokens;
+  int32_t num_heads;
+  int32_t head_size;
+  uint8_t* cache;
+  int64_t num_slots;
+  int32_t block_size;
+  const float* k_scale;
+  const float* v_scale;
+  int32_t* status;
+};
+
+cudaError_t launch_write_nvfp4_ds_mla(const WriteArgs& a, cudaStream_t stream);
+cudaError_t launch_write_fp8_ds_mla(const WriteArgs& a, cudaStream_t stream);
+cudaError_t launch_gather_nvfp4_ds_mla(const GatherArgs& a, cudaStream_t stream);
+cudaError_t launch_gather_fp8_ds_mla(const GatherArgs& a, cudaStream_t stream);
+cudaError_t launch_reshape_and_cache_nvfp4(const PerHeadArgs& a, cudaStream_t stream);
+cudaError_t launch_selftest_convert(uint32_t first_bits, int64_t count, uint8_t* e4m3_lo,
+                                    uint8_t* e4m3_hi, uint8_t* e2m1_lo, uint8_t* e2m1_hi,
+                                    uint16_t* bf16_out, int num_sms, cudaStream_t stream);
+
+}  // namespace kvq

@@ -1,0 +1,171 @@
+// kvq_write.cu -- MLA cache writes (concat_and_cache) for the 352-byte
+// nvfp4_ds_mla entry and the 656-byte fp8_ds_mla entry.
+//
+// Design (GB300): one warp per token, kTokensPerWarp tokens per warp with all
+// of their loads issued before any conversion, so each resident warp keeps
+// kTokensPerWarp x 1152 bytes of HBM reads in flight.  Lane l owns the 16
+// NoPE values of group l (32 contiguous bytes: one e4m3 scale, 8 output
+// bytes), so the group amax needs no shuffle.  Stores are warp-contiguous:
+// 256 B of packed NoPE, 64 B of RoPE and 32 B of scales per 352-byte entry,
+// each a whole number of 32-byte sectors when the entry is 32-byte aligned,
+// so L2 never has to read the line before writing it.
+#include "kvq_device.cuh"
+#include "kvq_launch.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+constexpr int kTokensPerWarp = 4;
+
+// The 8 packed bf16 pairs of one lane's 16 NoPE values, as fp32.
+__device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float (&x)[16]) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = bf16_lo(w[i]);
+    x[2 * i + 1] = bf16_hi(w[i]);
+  }
+}
+
+// amax over 16 bf16 values held as 8 packed words: exact, in bf16 pairs.
+__device__ __forceinline__ float amax16(const uint4& a, const uint4& b) {
+  __nv_bfloat162 m = __hmax2(__hmax2(abs_bf16x2(a.x), abs_bf16x2(a.y)),
+                             __hmax2(abs_bf16x2(a.z), abs_bf16x2(a.w)));
+  m = __hmax2(m, __hmax2(__hmax2(abs_bf16x2(b.x), abs_bf16x2(b.y)),
+                         __hmax2(abs_bf16x2(b.z), abs_bf16x2(b.w))));
+  return fmaxf(__low2float(m), __high2float(m));
+}
+
+// Slot -> entry pointer, or nullptr for padding / out-of-range slots.
+__device__ __forceinline__ uint8_t* entry_of(int64_t slot, const WriteArgs& a) {
+  if (slot < 0 || slot >= a.num_slots) return nullptr;
+  return a.cache + (slot / a.block_size) * a.block_stride + (slot % a.block_size) * a.entry_stride;
+}
+
+// ---------------------------------------------------------------------------
+// nvfp4_ds_mla: 352-byte entries
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+write_nvfp4_ds_mla_kernel(const WriteArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t0 =
+      (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5)) * kTokensPerWarp;
+  if (t0 >= a.num_tokens) return;
+
+  // One coalesced load of this warp's slots; lane j holds token t0 + j's.
+  int64_t my_slot = -1;
+  if (lane < kTokensPerWarp && t0 + lane < a.num_tokens) my_slot = __ldg(a.slot_mapping + t0 + lane);
+  if (lane < kTokensPerWarp && my_slot >= a.num_slots) report(a.status, KVQ_STATUS_BAD_INDEX);
+
+  const __nv_bfloat16* kv_c = static_cast<const __nv_bfloat16*>(a.kv_c);
+  const __nv_bfloat16* k_pe = static_cast<const __nv_bfloat16*>(a.k_pe);
+
+  uint8_t* entry[kTokensPerWarp];
+  uint4 na[kTokensPerWarp], nb[kTokensPerWarp];
+  uint2 rp[kTokensPerWarp];
+#pragma unroll
+  for (int j = 0; j < kTokensPerWarp; ++j) {
+    entry[j] = entry_of(__shfl_sync(kFull, my_slot, j), a);   // warp-uniform
+    if (entry[j] != nullptr) {
+      const __nv_bfloat16* row = kv_c + (t0 + j) * a.kv_c_stride + lane * kGroup;
+      na[j] = ld_stream16(row);
+      nb[j] = ld_stream16(row + 8);
+      if (lane < 16) rp[j] = ld_stream8(k_pe + (t0 + j) * a.k_pe_stride + lane * 4);
+    }
+  }
+
+#pragma unroll
+  for (int j = 0; j < kTokensPerWarp; ++j) {
+    if (entry[j] == nullptr) continue;
+    // NoPE group `lane`: scale, inverse, 8 packed bytes at 8 * lane.
+    const uint32_t sf = nvfp4_scale_code(amax16(na[j], nb[j]));
+    float x[16];
+    unpack16(na[j], nb[j], x);
+    st8(entry[j] + 8 * lane, nvfp4_pack16(x, nvfp4_inverse_scale(sf)));
+    // RoPE: lanes 0..15 convert 4 values each into bytes 256 + 4 * lane.
+    if (lane < 16) {
+      const uint32_t lo = cvt_e4m3x2(bf16_lo(rp[j].x), bf16_hi(rp[j].x));
+      const uint32_t hi = cvt_e4m3x2(bf16_lo(rp[j].y), bf16_hi(rp[j].y));
+      st4(entry[j] + kNvRopeOff + 4 * lane, lo | (hi << 16));
+    }
+    // Scale bytes: gather four per word; lanes 0, 4, ..., 28 store 32 bytes.
+    uint32_t w = sf;
+    w |= __shfl_down_sync(kFull, sf, 1) << 8;
+    w |= __shfl_down_sync(kFull, sf, 2) << 16;
+    w |= __shfl_down_sync(kFull, sf, 3) << 24;
+    if ((lane & 3) == 0) st4(entry[j] + kNvSfOff + lane, w);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// fp8_ds_mla: 656-byte entries
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+write_fp8_ds_mla_kernel(const WriteArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t0 =
+      (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5)) * kTokensPerWarp;
+  if (t0 >= a.num_tokens) return;
+
+  int64_t my_slot = -1;
+  if (lane < kTokensPerWarp && t0 + lane < a.num_tokens) my_slot = __ldg(a.slot_mapping + t0 + lane);
+  if (lane < kTokensPerWarp && my_slot >= a.num_slots) report(a.status, KVQ_STATUS_BAD_INDEX);
+
+  const __nv_bfloat16* kv_c = static_cast<const __nv_bfloat16*>(a.kv_c);
+  const __nv_bfloat16* k_pe = static_cast<const __nv_bfloat16*>(a.k_pe);
+
+  uint8_t* entry[kTokensPerWarp];
+  uint4 na[kTokensPerWarp], nb[kTokensPerWarp], rp[kTokensPerWarp];
+#pragma unroll
+  for (int j = 0; j < kTokensPerWarp; ++j) {
+    entry[j] = entry_of(__shfl_sync(kFull, my_slot, j), a);
+    if (entry[j] != nullptr) {
+      const __nv_bfloat16* row = kv_c + (t0 + j) * a.kv_c_stride + lane * 16;
+      na[j] = ld_stream16(row);
+      nb[j] = ld_stream16(row + 8);
+      if (lane < 8) rp[j] = ld_stream16(k_pe + (t0 + j) * a.k_pe_stride + lane * 8);
+    }
+  }
+
+#pragma unroll
+  for (int j = 0; j < kTokensPerWarp; ++j) {
+    if (entry[j] == nullptr) continue;
+    // Tile lane / 8 of 128 values: reduce the amax over its 8 lanes.
+    float amax = amax16(na[j], nb[j]);
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
+    const float s = amax == 0.0f ? 1.0f : amax / 448.0f;
+    float x[16];
+    unpack16(na[j], nb[j], x);
+    uint32_t q[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      q[k] = cvt_e4m3x2(__fdiv_rn(x[4 * k], s), __fdiv_rn(x[4 * k + 1], s)) |
+             (cvt_e4m3x2(__fdiv_rn(x[4 * k + 2], s), __fdiv_rn(x[4 * k + 3], s)) << 16);
+    }
+    st16(entry[j] + 16 * lane, make_uint4(q[0], q[1], q[2], q[3]));
+    if ((lane & 7) == 0) st4(entry[j] + kF8ScaleOff + 4 * (lane >> 3), __float_as_uint(s));
+    if (lane < 8) st16(entry[j] + kF8RopeOff + 16 * lane, rp[j]);
+  }
+}
+
+cudaError_t launch_write(void (*kernel)(WriteArgs), const WriteArgs& a, cudaStream_t stream) {
+  const int64_t tokens_per_block = int64_t{kWarpsPerBlock} * kTokensPerWarp;
+  const int64_t blocks = (a.num_tokens + tokens_per_block - 1) / tokens_per_block;
+  kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_write_nvfp4_ds_mla(const WriteArgs& a, cudaStream_t stream) {
+  return launch_write(write_nvfp4_ds_mla_kernel, a, stream);
+}
+
+cudaError_t launch_write_fp8_ds_mla(const WriteArgs& a, cudaStream_t stream) {
+  return launch_write(write_fp8_ds_mla_kernel, a, stream);
+}
+
+}  // namespace kvq

@@ -1,0 +1,218 @@
+/*
+ * kvq.h -- C ABI of the GB300 (sm_103a) quantized paged KV-cache library.
+ *
+ * The library writes bf16 key/value activations into quantized paged caches
+ * and gathers quantized pages back into contiguous bf16 workspaces, for
+ * DeepSeek-style sparse MLA (352-byte nvfp4_ds_mla and 656-byte fp8_ds_mla
+ * entries) and for a per-head NVFP4 K/V cache.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named by a tensor are DEVICE pointers owned by the caller.  The
+ *     library allocates and frees nothing and keeps no state between calls.
+ *   - Calls are asynchronous and stream-ordered: the kernel is launched on
+ *     `stream` (a cudaStream_t; NULL = the legacy default stream) and the call
+ *     returns without synchronising.
+ *   - bf16 tensors are row-major with strides in ELEMENTS; caches are uint8
+ *     with strides in BYTES.
+ *   - Alignment: every bf16 row must start on a 16-byte boundary (base
+ *     pointer 16-byte aligned, row strides multiples of 8 elements); cache base
+ *     pointers 16-byte aligned and cache strides multiples of 16 bytes.  Cache
+ *     entries that start on 32-byte boundaries are written in whole 32-byte
+ *     sectors (352 = 11 x 32, 656 = 20.5 x 32).
+ *   - Sizes of zero are valid no-ops (KVQ_OK, nothing launched, no device
+ *     query).
+ *   - Every index read from device memory is bounds-checked by the kernels:
+ *     an out-of-range slot, block id or position is skipped (nothing is
+ *     written for that token / row).  When `d_status` (a device int32, may be
+ *     NULL) is given, the kernel ORs the KVQ_STATUS_* bits below into it; the
+ *     caller zeroes it beforehand and reads it back when convenient.
+ *   - Host-side argument errors return before anything is launched.  The text
+ *     of the last error on the calling thread is kvq_last_error_string().
+ *   - Duplicate non-negative slots within one write race (last writer wins,
+ *     per byte); bytes of slots not named by a call are never touched.
+ *
+ * Sources, cited by page title and section:
+ *   [P1] vLLM PR #51724 "Enable W4A16 DSA: NVFP4 DS-MLA KV cache format for
+ *        the FlashMLA Sparse backend"
+ *   [P2] vLLM PR #37332 "Add NVFP4 quantization to the KV cache, extending
+ *        reshape_and_cache_flash"
+ *   [P3] vLLM PR #48642 "[Bugfix] Sparse MLA: enable fp8_ds_mla dense
+ *        prefill"
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t kvq_status;
+#define KVQ_OK                      0
+#define KVQ_ERR_INVALID_ARG         1  /* null pointer, negative size, misalignment, ... */
+#define KVQ_ERR_UNSUPPORTED_DEVICE  2  /* current device is not compute capability 10.3  */
+#define KVQ_ERR_CUDA                3  /* a CUDA runtime call or launch failed           */
+
+/* Bits a kernel ORs into *d_status. */
+#define KVQ_STATUS_BAD_INDEX   0x1  /* slot, block id or position out of range (skipped) */
+#define KVQ_STATUS_BAD_BATCH   0x2  /* workspace_starts not non-decreasing within [0, T],
+                                       or a row before the first request (skipped)       */
+
+/* Entry geometry ([P1] "Implementation breakdown" items 2-3). */
+#define KVQ_MLA_NOPE_DIM               512
+#define KVQ_MLA_ROPE_DIM               64
+#define KVQ_NVFP4_DS_MLA_ENTRY_BYTES   352  /* [0,256) e2m1 NoPE | [256,320) e4m3 RoPE |
+                                               [320,352) e4m3 scale of NoPE group g at 320+g */
+#define KVQ_FP8_DS_MLA_ENTRY_BYTES     656  /* [0,512) e4m3 NoPE | [512,528) 4 fp32 scales,
+                                               one per 128 NoPE values | [528,656) bf16 RoPE */
+#define KVQ_WORKSPACE_DIM              576  /* gathered row: NoPE 0..511, RoPE 512..575      */
+
+typedef struct CUstream_st* kvq_stream_t;   /* identical to cudaStream_t */
+
+/*
+ * kvq_write_nvfp4_ds_mla -- concat_and_cache for the 352-byte nvfp4_ds_mla
+ * cache.  [P1] "Key source snippets" (concat_and_cache_nvfp4_ds_mla_kernel)
+ * and "Implementation breakdown" item 3.
+ *
+ * For each token t < num_tokens with slot s = slot_mapping[t]:
+ *   s < 0                        padding: skipped, nothing read or written;
+ *   s >= num_blocks*block_size   out of range: skipped, KVQ_STATUS_BAD_INDEX;
+ *   otherwise the entry at kv_cache + (s / block_size) * block_stride +
+ *   (s % block_size) * entry_stride receives
+ *     bytes [8g, 8g+8)  the 16 NoPE values of group g (g = 0..31) as e2m1
+ *                       codes of x * (1 / sf_g), value 2k in the low nibble
+ *                       of byte k, round-to-nearest-even, saturating;
+ *     bytes [256, 320)  the 64 RoPE values as e4m3 (RN, saturating, unscaled);
+ *     byte  320 + g     sf_g = e4m3_rn_sat(max|x| over group g / 6), computed
+ *                       in fp32 (1/sf taken as 0 when sf is 0).
+ * kv_c: bf16 [num_tokens, >=512], row stride kv_c_stride elements.
+ * k_pe: bf16 [num_tokens, >=64],  row stride k_pe_stride elements.
+ * slot_mapping: int64 [num_tokens].
+ * kv_cache: uint8, num_blocks blocks of block_size entries; entry_stride >=
+ *   352 bytes; strides in bytes.
+ */
+kvq_status kvq_write_nvfp4_ds_mla(
+    const void* kv_c, int64_t kv_c_stride,
+    const void* k_pe, int64_t k_pe_stride,
+    const int64_t* slot_mapping, int64_t num_tokens,
+    uint8_t* kv_cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride,
+    int32_t* d_status, kvq_stream_t stream);
+
+/*
+ * kvq_gather_upconvert_nvfp4_ds_mla -- cp_gather_and_upconvert for the
+ * 352-byte cache.  [P1] "Key source snippets"
+ * (cp_gather_and_upconvert_nvfp4_kv_cache_kernel) with the seq_starts /
+ * workspace_starts interface of [P3] "Implementation breakdown" item 2 and
+ * "Key source snippets" (_compute_prefill_context).
+ *
+ * Output row w (0 <= w < num_out_tokens) belongs to request b, the largest b
+ * with workspace_starts[b] <= w (request b owns rows [ws[b], ws[b+1]), the
+ * last one up to num_out_tokens; zero-length requests are allowed).  Its
+ * position is p = seq_starts[b] + (w - ws[b]); the source entry is at block
+ * block_table[b * block_table_stride + p / block_size], offset p %
+ * block_size.  Row w of dst receives bf16(e2m1 * sf) for the 512 NoPE values
+ * and bf16(e4m3) for the 64 RoPE values -- both exact.  Rows whose source
+ * cannot be resolved (p / block_size >= block_table_width, a block id outside
+ * [0, num_blocks), a row before the first request) are skipped.
+ * dst: bf16 [num_out_tokens, >=576], row stride dst_stride elements.
+ * block_table: int32 [batch_size, >= block_table_width], row stride
+ *   block_table_stride elements.
+ * workspace_starts, seq_starts: int32 [batch_size] (a cu_seq_lens array of
+ *   batch_size + 1 entries may be passed; its last entry is not read).
+ */
+kvq_status kvq_gather_upconvert_nvfp4_ds_mla(
+    const uint8_t* src_cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride,
+    void* dst, int64_t dst_stride, int64_t num_out_tokens,
+    const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width,
+    const int32_t* workspace_starts, const int32_t* seq_starts, int32_t batch_size,
+    int32_t* d_status, kvq_stream_t stream);
+
+/*
+ * kvq_gather_upconvert_fp8_ds_mla -- cp_gather_and_upconvert_fp8_kv_cache
+ * with seq_starts (seq_lens removed).  [P3] "Implementation breakdown"
+ * items 2 and 4, "Key source snippets".  Same index walk and arguments as
+ * kvq_gather_upconvert_nvfp4_ds_mla; entry_stride >= 656.  NoPE value k =
+ * bf16_rn(fp32(e4m3(byte k)) * scale[k / 128]) with one fp32 rounding; RoPE
+ * bf16 copied bit for bit.
+ */
+kvq_status kvq_gather_upconvert_fp8_ds_mla(
+    const uint8_t* src_cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride,
+    void* dst, int64_t dst_stride, int64_t num_out_tokens,
+    const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width,
+    const int32_t* workspace_starts, const int32_t* seq_starts, int32_t batch_size,
+    int32_t* d_status, kvq_stream_t stream);
+
+/*
+ * kvq_write_fp8_ds_mla -- concat_and_cache for the 656-byte fp8_ds_mla cache
+ * ([P1] "Implementation breakdown" item 2 gives the size; the recipe is the
+ * format spec's).  Same slot rules and arguments as kvq_write_nvfp4_ds_mla;
+ * entry_stride >= 656.  Per 128-value tile j: s_j = max|x| / 448 in fp32 (1
+ * when the tile is all zero), NoPE byte = e4m3_rn_sat(x / s_j) with IEEE
+ * division, scale j stored as fp32 at 512 + 4j, RoPE bf16 bits at 528.
+ */
+kvq_status kvq_write_fp8_ds_mla(
+    const void* kv_c, int64_t kv_c_stride,
+    const void* k_pe, int64_t k_pe_stride,
+    const int64_t* slot_mapping, int64_t num_tokens,
+    uint8_t* kv_cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride,
+    int32_t* d_status, kvq_stream_t stream);
+
+/*
+ * kvq_reshape_and_cache_nvfp4 -- reshape_and_cache_flash into a per-head
+ * NVFP4 K/V cache.  [P2] "Function and motivation" and "Implementation
+ * breakdown" item 4 (layout [K_data | K_scale | V_data | V_scale], per-tensor
+ * scale), "Key source snippets" (cache shape (num_pages, 2, block_size,
+ * num_kv_heads, full_dim) with full_dim = head_size/2 + head_size/16, data_dim
+ * = full_dim*8/9).
+ *
+ * kv_cache is a contiguous uint8 [num_pages, 2, block_size, num_heads,
+ * full_dim] allocation.  Inside page p and side s (K = 0, V = 1) its
+ * block_size*num_heads*full_dim bytes hold the data [block_size][num_heads]
+ * [head_size/2] followed by the scales [block_size][num_heads][head_size/16].
+ * Token t with slot s = slot_mapping[t] >= 0 goes to page s / block_size,
+ * offset s % block_size: each 16-value group of y = x * (1 / scale) (fp32;
+ * scale = *k_scale or *v_scale, device fp32 scalars) is quantized exactly as
+ * an nvfp4_ds_mla NoPE group.  head_size must be a multiple of 16.
+ * key, value: bf16 [num_tokens, num_heads, head_size] with token and head
+ * strides in elements (unit inner stride).
+ */
+kvq_status kvq_reshape_and_cache_nvfp4(
+    const void* key, const void* value,
+    int64_t key_stride_t, int64_t key_stride_h,
+    int64_t value_stride_t, int64_t value_stride_h,
+    const int64_t* slot_mapping, int64_t num_tokens,
+    int32_t num_heads, int32_t head_size,
+    uint8_t* kv_cache, int64_t num_pages, int32_t block_size,
+    const float* k_scale, const float* v_scale,
+    int32_t* d_status, kvq_stream_t stream);
+
+/*
+ * kvq_selftest_convert -- exposes the device number-format converters the
+ * kernels above use, for exhaustive testing.  For i < count and f the float
+ * whose bit pattern is first_bits + i (mod 2^32):
+ *   e4m3_lo[i] / e4m3_hi[i]  e4m3 code of f placed in the low / high lane of
+ *                            the packed two-value conversion;
+ *   e2m1_lo[i] / e2m1_hi[i]  the same for e2m1 (code in the low 4 bits);
+ *   bf16_out[i]              bf16 bits of f rounded to nearest even.
+ * Any output pointer may be NULL.  Not part of the cache path.
+ */
+kvq_status kvq_selftest_convert(
+    uint32_t first_bits, int64_t count,
+    uint8_t* e4m3_lo, uint8_t* e4m3_hi, uint8_t* e2m1_lo, uint8_t* e2m1_hi,
+    uint16_t* bf16_out, kvq_stream_t stream);
+
+/* Text of the last error returned on the calling thread ("" if none). */
+const char* kvq_last_error_string(void);
+
+/* Library ABI version (major * 100 + minor). */
+int32_t kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVQ_H */

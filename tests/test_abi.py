@@ -1,0 +1,172 @@
+"""The C ABI library on a host without a GPU: it builds, loads, exports every
+entry point include/kvq.h declares, and rejects bad arguments on the host
+before any CUDA call.  No kernel is launched here.
+
+The argument-rejection tests pass fake device addresses; they are skipped
+where a GPU is visible, so that a validation gap could never turn into a
+launch on a real device.
+"""
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvq.h")
+
+no_gpu_only = pytest.mark.skipif(torch.cuda.is_available(),
+                                 reason="fake-pointer validation tests run only on GPU-less hosts")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_quantized_paged_concat_gb300 import _build
+    import fp8_quantized_paged_concat_gb300 as kvq
+    _build.build()
+    return kvq.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_hot_path_calls():
+    names = declared_functions()
+    for n in ("kvq_write_nvfp4_ds_mla", "kvq_gather_upconvert_nvfp4_ds_mla",
+              "kvq_gather_upconvert_fp8_ds_mla", "kvq_reshape_and_cache_nvfp4"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from fp8_quantized_paged_concat_gb300 import library_path
+    out = subprocess.run(["nm", "-D", "--defined-only", library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (kvq_[a-z0-9_]+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+    assert lib.kvq_version() == 100
+
+
+def test_library_is_built_for_sm_103a_only():
+    from fp8_quantized_paged_concat_gb300 import _build
+    assert "arch=compute_103a,code=sm_103a" in _build.ARCH
+    assert not any("fast-math" in f or "fast_math" in f for f in _build.NVCC_FLAGS)
+
+
+A = 0x10000000          # a 256-byte-aligned fake device address, never dereferenced
+
+
+def err(lib):
+    return lib.kvq_last_error_string().decode()
+
+
+def write_args(entry=352, **over):
+    args = dict(kv_c=A, kv_c_stride=512, k_pe=A, k_pe_stride=64, slot_mapping=A, num_tokens=16,
+                kv_cache=A, num_blocks=4, block_size=64, block_stride=64 * entry,
+                entry_stride=entry, d_status=None, stream=None)
+    args.update(over)
+    return list(args.values())
+
+
+@no_gpu_only
+@pytest.mark.parametrize("fn,entry", [("kvq_write_nvfp4_ds_mla", 352), ("kvq_write_fp8_ds_mla", 656)])
+@pytest.mark.parametrize("over,needle", [
+    (dict(num_tokens=-1), "num_tokens < 0"),
+    (dict(kv_c=None), "kv_c is NULL"),
+    (dict(kv_c=A + 8), "kv_c must be 16-byte aligned"),
+    (dict(kv_c_stride=500), "row stride"),
+    (dict(kv_c_stride=516), "row stride"),
+    (dict(k_pe_stride=60), "row stride"),
+    (dict(slot_mapping=None), "slot_mapping is NULL"),
+    (dict(kv_cache=A + 4), "16-byte aligned"),
+    (dict(entry_stride=336), "entry_stride"),
+    (dict(entry_stride=664), "entry_stride"),
+    (dict(block_stride=100), "block_stride"),
+    (dict(num_blocks=0), "positive"),
+    (dict(block_size=0), "positive"),
+])
+def test_write_rejects_bad_arguments_on_host(lib, fn, entry, over, needle):
+    assert getattr(lib, fn)(*write_args(entry, **over)) == 1
+    assert needle in err(lib), err(lib)
+
+
+def gather_args(**over):
+    args = dict(src_cache=A, num_blocks=4, block_size=64, block_stride=64 * 352, entry_stride=352,
+                dst=A, dst_stride=576, num_out_tokens=100, block_table=A, block_table_stride=3,
+                block_table_width=3, workspace_starts=A, seq_starts=A, batch_size=2,
+                d_status=None, stream=None)
+    args.update(over)
+    return list(args.values())
+
+
+@no_gpu_only
+@pytest.mark.parametrize("over,needle", [
+    (dict(num_out_tokens=-5), "num_out_tokens < 0"),
+    (dict(num_out_tokens=1 << 31), "int32"),
+    (dict(src_cache=None), "cache is NULL"),
+    (dict(dst=A + 2), "dst must be 16-byte aligned"),
+    (dict(dst_stride=575), "row stride"),
+    (dict(batch_size=0), "batch_size"),
+    (dict(block_table=None), "non-NULL"),
+    (dict(seq_starts=None), "non-NULL"),
+    (dict(workspace_starts=A + 2), "4-byte aligned"),
+    (dict(block_table_width=0), "block_table_width"),
+    (dict(block_table_stride=2), "block_table_stride"),
+    (dict(entry_stride=336), "entry_stride"),
+])
+def test_gather_rejects_bad_arguments_on_host(lib, over, needle):
+    assert lib.kvq_gather_upconvert_nvfp4_ds_mla(*gather_args(**over)) == 1
+    assert needle in err(lib), err(lib)
+
+
+@no_gpu_only
+def test_fp8_gather_requires_656_byte_entries(lib):
+    args = gather_args(entry_stride=352)
+    assert lib.kvq_gather_upconvert_fp8_ds_mla(*args) == 1
+    assert "656" in err(lib)
+
+
+def per_head_args(**over):
+    args = dict(key=A, value=A, kst=1024, ksh=128, vst=1024, vsh=128, slot_mapping=A,
+                num_tokens=8, num_heads=8, head_size=128, kv_cache=A, num_pages=4, block_size=16,
+                k_scale=A, v_scale=A, d_status=None, stream=None)
+    args.update(over)
+    return list(args.values())
+
+
+@no_gpu_only
+@pytest.mark.parametrize("over,needle", [
+    (dict(num_tokens=-1), "num_tokens < 0"),
+    (dict(head_size=72), "multiple of 16"),
+    (dict(num_heads=0), "num_heads"),
+    (dict(key=None), "NULL"),
+    (dict(value=A + 8), "16-byte aligned"),
+    (dict(ksh=100), "multiples of 8"),
+    (dict(k_scale=None), "fp32 scalars"),
+    (dict(kv_cache=A + 8), "16-byte aligned"),
+    (dict(num_pages=0), "positive"),
+    (dict(head_size=16, num_heads=1, block_size=1), "multiple of 8"),
+])
+def test_per_head_rejects_bad_arguments_on_host(lib, over, needle):
+    assert lib.kvq_reshape_and_cache_nvfp4(*per_head_args(**over)) == 1
+    assert needle in err(lib), err(lib)
+
+
+@no_gpu_only
+def test_zero_sized_calls_are_noops_without_device(lib):
+    assert lib.kvq_write_nvfp4_ds_mla(*write_args(num_tokens=0, kv_c=None)) == 0
+    assert lib.kvq_gather_upconvert_fp8_ds_mla(*gather_args(num_out_tokens=0, dst=None)) == 0
+    assert lib.kvq_reshape_and_cache_nvfp4(*per_head_args(num_tokens=0)) == 0
+    assert lib.kvq_selftest_convert(0, 0, None, None, None, None, None, None) == 0
+
+
+@no_gpu_only
+def test_valid_arguments_without_a_gpu_report_a_cuda_error(lib):
+    """With no device the call fails cleanly at the device query."""
+    assert lib.kvq_write_nvfp4_ds_mla(*write_args()) == 3
+    assert "kvq_write_nvfp4_ds_mla" in err(lib)
