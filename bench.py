@@ -1,0 +1,549 @@
+"""Benchmark: the quantized paged KV-cache hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+  1. nvfp4_ds_mla write of 4,194,304 tokens (fills the 65536 x 64 x 352 cache)
+  2. fp8_ds_mla gather-upconvert: 16 requests x 16384 rows (32768 x 64 x 656 cache)
+  3. nvfp4_ds_mla gather-upconvert: 32 requests, 4k-32k rows each, from cache 1
+  4. per-head NVFP4 reshape_and_cache: K, V bf16 [16384, 8, 128]
+Inputs are resident in HBM before timing starts and exceed the 129 MB L2
+(about 7.8 GB move per step), so no L2 flush is needed between steps.
+
+value = algorithmic bytes of the step / device time of the step (GB/s);
+tokens_per_s counts written tokens + gathered rows + per-head tokens.
+--impl reference times the CPU oracle (the only reference that exists for
+this path) on bounded samples of the same workloads, on the host cores.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch one process per GPU with torch.distributed.run; each rank
+runs an independent replica of the step (no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "write & gather-upconvert HBM GB/s (fraction of GB300 peak) and tokens/s"
+WORKLOAD = ("nvfp4_ds_mla write 4,194,304 tok (65536x64x352 fill) + fp8_ds_mla gather 16x16384 rows "
+            "(32768x64x656) + nvfp4_ds_mla gather 32 req U[4k,32k] rows + per-head NVFP4 "
+            "reshape_and_cache K,V [16384,8,128] (16384x2x16x8x72)")
+
+# Algorithmic bytes per unit of work (inputs read once + outputs written once).
+BYTES_WRITE_NVFP4 = 1024 + 128 + 8 + 352       # per valid token; 8 per padding token
+BYTES_WRITE_FP8 = 1024 + 128 + 8 + 656
+BYTES_GATHER_NVFP4 = 352 + 1152                # per output row
+BYTES_GATHER_FP8 = 656 + 1152
+
+
+def per_head_bytes_per_token(H, D):
+    return 2 * H * (2 * D + D // 2 + D // 16) + 8
+
+
+KERNEL_ORDER = ["write_nvfp4_ds_mla", "gather_fp8_ds_mla", "gather_nvfp4_ds_mla",
+                "reshape_and_cache_nvfp4"]
+
+
+# --------------------------------------------------------------------------
+# distributed helpers (one process per GPU, replicas)
+# --------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# clocks
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 20 ms, timestamped."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index: str):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + ",".join(self.FIELDS),
+               "--format=csv,noheader,nounits", "-lms", "20"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        window = "timed region"
+        if len(inside) < 3:          # very short timed region: widen to the loaded span around it
+            inside = [p for (t, p) in self.samples if t0 - 0.5 <= t <= t1 + 0.5]
+            window = "timed region +-0.5 s"
+        if not inside:
+            return None
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        mx = [num(p[1]) for p in inside if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for p in inside for n, v in zip(names, p[4:8]) if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+def measured_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def committed_traffic():
+    """DRAM bytes per unit of work per kernel from the committed ncu summary
+    (profiles/dram_traffic.txt), keyed by the source hash of the kernel file;
+    a kernel whose source changed since the capture gets None."""
+    import hashlib
+    out = {}
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return out
+    for line in open(path):
+        if line.startswith("#") or "=" not in line:
+            continue
+        kv = dict(item.split("=", 1) for item in line.split())
+        src = os.path.join(ROOT, "fp8_quantized_paged_concat_gb300", "csrc", kv.get("source", ""))
+        if not os.path.exists(src):
+            continue
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:12]
+        if sha == kv.get("source_sha"):
+            out[kv["kernel"]] = float(kv["dram_bytes_per_unit"])
+    return out
+
+
+# --------------------------------------------------------------------------
+# GPU path
+# --------------------------------------------------------------------------
+
+class GpuStep:
+    """Device-resident inputs and outputs of one step, and its launches."""
+
+    def __init__(self, device):
+        import fp8_quantized_paged_concat_gb300 as kvq
+        kvq.load_library()
+        self.kvq = kvq
+        self.device = device
+        self.g3 = wl.prefill_gather(device)
+        self.g4 = wl.fp8_gather(device)
+        self.ph = wl.per_head(device)
+        f3, f4 = self.g3.fill, self.g4.fill
+        self.cache3 = torch.zeros((f3.num_blocks, f3.block_size, 352), dtype=torch.uint8, device=device)
+        self.cache4 = torch.zeros((f4.num_blocks, f4.block_size, 656), dtype=torch.uint8, device=device)
+        kvq.kvq_write_fp8_ds_mla(f4.kv_c, f4.k_pe, self.cache4, f4.slot_mapping)      # setup fill
+        self.ws3 = torch.empty((self.g3.num_out_tokens, 576), dtype=torch.bfloat16, device=device)
+        self.ws4 = torch.empty((self.g4.num_out_tokens, 576), dtype=torch.bfloat16, device=device)
+        T, H, D = self.ph.key.shape
+        self.phc = torch.zeros((self.ph.num_pages, 2, self.ph.block_size, H, kvq.nvfp4_full_dim(D)),
+                               dtype=torch.uint8, device=device)
+        self.ks = torch.tensor([self.ph.k_scale], dtype=torch.float32, device=device)
+        self.vs = torch.tensor([self.ph.v_scale], dtype=torch.float32, device=device)
+        self.units = {
+            "write_nvfp4_ds_mla": (f3.num_tokens, "tokens", BYTES_WRITE_NVFP4 * f3.num_tokens),
+            "gather_fp8_ds_mla": (self.g4.num_out_tokens, "rows", BYTES_GATHER_FP8 * self.g4.num_out_tokens),
+            "gather_nvfp4_ds_mla": (self.g3.num_out_tokens, "rows", BYTES_GATHER_NVFP4 * self.g3.num_out_tokens),
+            "reshape_and_cache_nvfp4": (T, "tokens", per_head_bytes_per_token(H, D) * T),
+        }
+        torch.cuda.synchronize(device)
+
+    def bytes_per_step(self):
+        return sum(b for _, _, b in self.units.values())
+
+    def tokens_per_step(self):
+        return sum(n for n, _, _ in self.units.values())
+
+    def launches(self):
+        k, f3, g3, g4, ph = self.kvq, self.g3.fill, self.g3, self.g4, self.ph
+        return [
+            lambda: k.kvq_write_nvfp4_ds_mla(f3.kv_c, f3.k_pe, self.cache3, f3.slot_mapping),
+            lambda: k.kvq_gather_upconvert_fp8_ds_mla(self.cache4, self.ws4, g4.block_table,
+                                                      g4.workspace_starts, g4.seq_starts),
+            lambda: k.kvq_gather_upconvert_nvfp4_ds_mla(self.cache3, self.ws3, g3.block_table,
+                                                        g3.workspace_starts, g3.seq_starts),
+            lambda: k.kvq_reshape_and_cache_nvfp4(ph.key, ph.value, self.phc, ph.slot_mapping,
+                                                  self.ks, self.vs),
+        ]
+
+
+def time_device(step: GpuStep, K: int, W: int, world: int, clocks: ClockSampler | None):
+    """W untimed steps, then K steps bracketed by barrier + synchronize, with
+    an event between consecutive kernels (same stream)."""
+    launches = step.launches()
+    for _ in range(W):
+        for fn in launches:
+            fn()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    h0 = time.time()
+    start.record()
+    for k in range(K):
+        for i, fn in enumerate(launches):
+            evs[k][i].record()
+            fn()
+        evs[k][-1].record()
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    h1 = time.time()
+    total_ms = start.elapsed_time(end)
+    per_kernel = {name: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K))
+                  for i, name in enumerate(KERNEL_ORDER)}
+    return total_ms, per_kernel, (h0, h1), K * len(launches)
+
+
+def time_e2e(step: GpuStep, K: int):
+    """Same step through the public API with host buffers: pinned host ->
+    device copies of every per-step input, the four launches, and device ->
+    pinned host copies of every result, all on the launching stream."""
+    g3, g4, ph = step.g3, step.g4, step.ph
+    dev_inputs = [g3.fill.kv_c, g3.fill.k_pe, g3.fill.slot_mapping, g3.block_table, g3.workspace_starts,
+                  g3.seq_starts, g4.block_table, g4.workspace_starts, g4.seq_starts, ph.key, ph.value,
+                  ph.slot_mapping]
+    dev_outputs = [step.cache3, step.ws4, step.ws3, step.phc]
+    host_in = [t.cpu().pin_memory() for t in dev_inputs]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_outputs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    launches = step.launches()
+
+    def one():
+        for d, h in zip(dev_inputs, host_in):
+            d.copy_(h, non_blocking=True)
+        for fn in launches:
+            fn()
+        for h, d in zip(host_out, dev_outputs):
+            h.copy_(d, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(K):
+        one()
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / K
+    return ms, h2d, d2h
+
+
+def time_extra(step: GpuStep, reps: int = 10):
+    """Kernels measured outside the step: the decode-step write (8192 tokens,
+    L2 flushed before each launch) and the fp8_ds_mla cache fill."""
+    kvq = step.kvq
+    d = wl.decode_write(step.device)
+    cache2 = torch.zeros((d.num_blocks, d.block_size, 352), dtype=torch.uint8, device=step.device)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=step.device)
+    f4 = step.g4.fill
+    out = {}
+    for name, fn, units, nbytes, flush_l2 in (
+            ("write_nvfp4_ds_mla decode T=8192", lambda: kvq.kvq_write_nvfp4_ds_mla(
+                d.kv_c, d.k_pe, cache2, d.slot_mapping), d.num_tokens,
+             BYTES_WRITE_NVFP4 * int((d.slot_mapping >= 0).sum()) + 8 * int((d.slot_mapping < 0).sum()), True),
+            ("write_fp8_ds_mla fill 2,097,152 tok", lambda: kvq.kvq_write_fp8_ds_mla(
+                f4.kv_c, f4.k_pe, step.cache4, f4.slot_mapping), f4.num_tokens,
+             BYTES_WRITE_FP8 * f4.num_tokens, False)):
+        times = []
+        for r in range(reps + 3):
+            if flush_l2:
+                flush.fill_(r & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            if r >= 3:
+                times.append(a.elapsed_time(b))
+        ms = statistics.median(times)
+        out[name] = {"units": units, "us": round(ms * 1e3, 2), "gbs": round(nbytes / ms / 1e6, 1),
+                     "l2_flushed": flush_l2}
+    del flush
+    return out
+
+
+# --------------------------------------------------------------------------
+# CPU oracle (reference arm and cpu_baseline)
+# --------------------------------------------------------------------------
+
+class CpuSample:
+    """Bounded host samples of the four workloads, for the oracle."""
+
+    def __init__(self, threads):
+        import oracle
+        self.oracle = oracle
+        self.threads = threads
+        g = np.random.Generator(np.random.PCG64(2003))
+        # write: 262,144 tokens of the fill, into a 4096 x 64 cache
+        w = wl.make_fill("cpu write sample", 4096, 64, 2003)
+        self.w = (wl.bf16_bits(w.kv_c), wl.bf16_bits(w.k_pe), wl.host(w.slot_mapping))
+        self.c_w = np.zeros((4096, 64, 352), np.uint8)
+        # nvfp4 gather: 8 requests with the prefill length / start mix
+        lens = g.integers(4096, 32768, size=8, endpoint=True)
+        starts = g.integers(1, 4095, size=8, endpoint=True)
+        nb = int(sum(-(-(s + n) // 64) for s, n in zip(starts, lens))) + 8
+        f = wl.make_fill("cpu nvfp4 cache", nb, 64, 2004)
+        self.c3 = np.zeros((nb, 64, 352), np.uint8)
+        oracle.write_nvfp4_ds_mla(wl.bf16_bits(f.kv_c), wl.bf16_bits(f.k_pe), wl.host(f.slot_mapping),
+                                  self.c3, threads=threads)
+        self.b3 = wl.make_gather_batch(nb, 64, lens, starts, 2005)
+        # fp8 gather: 8 requests x 16384 rows
+        starts4 = g.integers(1, 4095, size=8, endpoint=True)
+        nb4 = int(sum(-(-(s + 16384) // 64) for s in starts4)) + 8
+        f4 = wl.make_fill("cpu fp8 cache", nb4, 64, 2006, entry_bytes=656)
+        self.c4 = np.zeros((nb4, 64, 656), np.uint8)
+        oracle.write_fp8_ds_mla(wl.bf16_bits(f4.kv_c), wl.bf16_bits(f4.k_pe), wl.host(f4.slot_mapping),
+                                self.c4, threads=threads)
+        self.b4 = wl.make_gather_batch(nb4, 64, [16384] * 8, starts4, 2007)
+        # per-head: 8192 tokens of the [T, 8, 128] workload
+        p = wl.make_per_head("cpu per-head sample", 8192, 8, 128, 16384, 16, 0, 2008)
+        self.p = (wl.bf16_bits(p.key), wl.bf16_bits(p.value), wl.host(p.slot_mapping))
+        self.pc = np.zeros((16384, 2, 16, 8, 72), np.uint8)
+        self.units = {
+            "write_nvfp4_ds_mla": (self.w[2].size, BYTES_WRITE_NVFP4 * self.w[2].size),
+            "gather_fp8_ds_mla": (self.b4[3], BYTES_GATHER_FP8 * self.b4[3]),
+            "gather_nvfp4_ds_mla": (self.b3[3], BYTES_GATHER_NVFP4 * self.b3[3]),
+            "reshape_and_cache_nvfp4": (8192, per_head_bytes_per_token(8, 128) * 8192),
+        }
+        self.description = (f"oracle on {threads} host threads: write {self.w[2].size} tokens, "
+                            f"fp8 gather {self.b4[3]} rows, nvfp4 gather {self.b3[3]} rows, "
+                            f"per-head {8192} tokens per step")
+
+    def bytes_per_step(self):
+        return sum(b for _, b in self.units.values())
+
+    def tokens_per_step(self):
+        return sum(n for n, _ in self.units.values())
+
+    def step(self):
+        o, t = self.oracle, self.threads
+        times = {}
+        a = time.perf_counter()
+        o.write_nvfp4_ds_mla(*self.w, self.c_w, threads=t)
+        b = time.perf_counter()
+        times["write_nvfp4_ds_mla"] = b - a
+        tbl, ws, st, T = self.b4
+        o.gather_fp8_ds_mla(self.c4, tbl, ws, st, T, threads=t)
+        c = time.perf_counter()
+        times["gather_fp8_ds_mla"] = c - b
+        tbl, ws, st, T = self.b3
+        o.gather_nvfp4_ds_mla(self.c3, tbl, ws, st, T, threads=t)
+        d = time.perf_counter()
+        times["gather_nvfp4_ds_mla"] = d - c
+        o.reshape_and_cache_nvfp4(*self.p, self.pc, threads=t)
+        times["reshape_and_cache_nvfp4"] = time.perf_counter() - d
+        return times
+
+
+def cpu_baseline(threads):
+    s = CpuSample(threads)
+    times = s.step()
+    total = sum(times.values())
+    return {"value": round(s.bytes_per_step() / total / 1e9, 3), "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "sample": s.description,
+            "tokens_per_s": round(s.tokens_per_step() / total, 1), "seconds": round(total, 2)}
+
+
+# --------------------------------------------------------------------------
+# entry points
+# --------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0                          # rank 0 alone times the oracle
+    import oracle
+    threads = oracle.default_threads()
+    s = CpuSample(threads)
+    for _ in range(args.warmup):
+        s.step()
+    per = {k: 0.0 for k in KERNEL_ORDER}
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for k, v in s.step().items():
+            per[k] += v
+    sec = (time.perf_counter() - t0) / args.steps
+    value = s.bytes_per_step() / sec / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": s.description},
+        "tokens_per_s": round(s.tokens_per_step() / sec, 1),
+        "kernels": {k: {"units": s.units[k][0], "gbs": round(s.units[k][1] * args.steps / per[k] / 1e9, 3)}
+                    for k in KERNEL_ORDER},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": s.description},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    step = GpuStep(device)
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [v.strip() for v in visible.split(",") if v.strip()]
+    clocks = ClockSampler(ids[local] if local < len(ids) else str(local))
+    clocks.start()
+    time.sleep(0.3)
+    total_ms, per_kernel, (h0, h1), launches = time_device(step, args.steps, args.warmup, world, clocks)
+    clocks.stop()
+    clock_summary = clocks.summary(h0, h1)
+    max_ms = max_over_ranks(total_ms, world, device)
+    ms_per_step = max_ms / args.steps
+    bytes_step = step.bytes_per_step()
+    value = world * bytes_step / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peak_gbs()
+    traffic = committed_traffic()
+
+    kernels = {}
+    for name in KERNEL_ORDER:
+        units, unit_name, nbytes = step.units[name]
+        ms = per_kernel[name]
+        gbs = nbytes / ms / 1e6
+        kernels[name] = {"units": units, "unit": unit_name, "us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+                         "frac": round(gbs / peak, 4), "units_per_s": round(units / ms * 1e3, 1)}
+    dom = "write_nvfp4_ds_mla"
+    d_units, _, d_bytes = step.units[dom]
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["gbs"], "peak": peak,
+                "unit": "GB/s", "frac": kernels[dom]["frac"], "peak_source": peak_kind,
+                "traffic": (round(traffic[dom] * d_units) if dom in traffic else None),
+                "algorithmic_bytes": d_bytes}
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "bytes_per_step": bytes_step,
+                   "l2": "no flush: every step moves ~7.8 GB, inputs exceed the 129 MB L2"},
+        "frac_of_peak": round(value / world / peak, 4),
+        "tokens_per_s": round(world * step.tokens_per_step() / (ms_per_step * 1e-3), 1),
+        "kernels": kernels, "roofline": roofline, "gpu_launches": launches,
+        "clocks": clock_summary,
+    }
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, 10))
+        ms, h2d, d2h = time_e2e(step, e2e_steps)
+        ms = max_over_ranks(ms, world, device)
+        line["e2e"] = {"value": round(world * bytes_step / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
+                       "steps": e2e_steps}
+    if not args.no_extra:
+        line["kernels_extra"] = time_extra(step)
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        line["cpu_baseline"] = cpu_baseline(oracle.default_threads())
+    barrier(world)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-extra", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -91,7 +91,7 @@ kvq_status write_common(const char* fn, int64_t entry_bytes,
                         kvq_stream_t stream) {
   KVQ_REQUIRE(num_tokens >= 0, "%s: num_tokens < 0", fn);
   if (num_tokens == 0) return ok();
-  KVQ_REQUIRE(num_tokens <= (int64_t{1} << 36), "%s: num_tokens too large", fn);
+  KVQ_REQUIRE(num_tokens < (int64_t{1} << 35), "%s: num_tokens too large", fn);  // grid.x < 2^31
   if (kvq_status s = check_bf16_rows(fn, "kv_c", kv_c, kv_c_stride, KVQ_MLA_NOPE_DIM)) return s;
   if (kvq_status s = check_bf16_rows(fn, "k_pe", k_pe, k_pe_stride, KVQ_MLA_ROPE_DIM)) return s;
   KVQ_REQUIRE(slot_mapping != nullptr, "%s: slot_mapping is NULL", fn);
@@ -202,7 +202,8 @@ kvq_status kvq_reshape_and_cache_nvfp4(const void* key, const void* value, int64
   if (num_tokens == 0) return ok();
   KVQ_REQUIRE(num_heads > 0 && head_size >= 16 && head_size % 16 == 0,
               "%s: need num_heads > 0 and head_size a positive multiple of 16", fn);
-  KVQ_REQUIRE(num_tokens * 2 * num_heads * (head_size / 16) < (int64_t{1} << 40),
+  KVQ_REQUIRE(num_tokens < (int64_t{1} << 31) &&
+                  num_tokens * 2 * num_heads * (head_size / 16) < (int64_t{1} << 38),
               "%s: problem too large", fn);
   KVQ_REQUIRE(key != nullptr && value != nullptr, "%s: key / value is NULL", fn);
   KVQ_REQUIRE(aligned(key, 16) && aligned(value, 16), "%s: key / value must be 16-byte aligned", fn);

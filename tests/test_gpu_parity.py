@@ -1,0 +1,382 @@
+"""GPU parity: every CUDA entry point against the CPU oracle, element by
+element, on the same seeded inputs.  Integer / byte outputs (cache bytes) and
+the bf16 gathers (exact or single-rounding results) must match bit for bit.
+
+Small cases cover several CTAs and ragged tails plus edge cases (padding,
+out-of-range indices, zero-length requests, padded strides, extreme values);
+the full-size cases run the workloads the benchmark times, completely.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    from fp8_quantized_paged_concat_gb300 import _build
+    _build.build()
+    import fp8_quantized_paged_concat_gb300 as m
+    m.load_library()
+    return m
+
+
+@pytest.fixture(scope="module")
+def threads(oracle_mod):
+    return oracle_mod.default_threads()
+
+
+def dev(x):
+    return x.to(DEV) if isinstance(x, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
+
+
+def finite_bf16_bits(shape, seed):
+    """Random finite bf16 bit patterns over the whole exponent range (zeros,
+    subnormals, huge values, both signs)."""
+    b = wl.random_bytes(tuple(shape) + (2,), seed).view(np.uint16).reshape(shape)
+    exp_all_ones = (b & 0x7F80) == 0x7F80
+    b[exp_all_ones] &= 0xBFFF            # clear an exponent bit: finite
+    return b
+
+
+def bits_to_bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+# --------------------------------------------------------------------------
+# device converters, exhaustively over the exponent window that matters
+# --------------------------------------------------------------------------
+
+def sweep_ranges():
+    """(first_bits, count) pieces: every pattern with |f| in [2^-12, 2^10),
+    both signs (the window where e4m3 and e2m1 rounding decisions happen)."""
+    lo = int(np.float32(2.0 ** -12).view(np.uint32))
+    hi = int(np.float32(2.0 ** 10).view(np.uint32))
+    return [(lo, hi - lo), (lo | 0x80000000, hi - lo)]
+
+
+def test_device_converters_match_oracle_in_rounding_window(kvq, oracle_mod, threads):
+    chunk = 1 << 26
+    for first, count in sweep_ranges():
+        for s in range(0, count, chunk):
+            f0, n = first + s, min(chunk, count - s)
+            e4l, e4h, e2l, e2h, bf = (t.cpu().numpy() for t in kvq.kvq_selftest_convert(f0, n))
+            o4, o2 = oracle_mod.encode_bits_range(f0, n, threads=threads)
+            ob = oracle_mod.bf16_rn_bits_range(f0, n, threads=threads)
+            np.testing.assert_array_equal(e4l, o4)
+            np.testing.assert_array_equal(e4h, o4)
+            np.testing.assert_array_equal(e2l, o2)
+            np.testing.assert_array_equal(e2h, o2)
+            np.testing.assert_array_equal(bf.view(np.uint16), ob)
+
+
+def test_device_converters_strided_full_range(kvq, oracle_mod, threads):
+    """Every 509th float32 pattern of all 2^32 (zeros, subnormals,
+    saturation, infinities); NaN inputs only have to stay NaN in e4m3."""
+    chunk, stride = 1 << 28, 509
+    for first in range(0, 1 << 32, chunk):
+        e4l, e4h, e2l, e2h, bf = kvq.kvq_selftest_convert(first, chunk)
+        off = (-first) % stride
+        idx = torch.arange(off, chunk, stride, device=DEV)
+        got = [t[idx].cpu().numpy() for t in (e4l, e4h, e2l, e2h, bf)]
+        del e4l, e4h, e2l, e2h, bf
+        bits = (first + idx.cpu().numpy()).astype(np.uint32)
+        f = bits.view(np.float32)
+        keep = ~np.isnan(f)
+        o4, o2, ob = oracle_mod.e4m3_rn_sat(f), oracle_mod.e2m1_rn_sat(f), oracle_mod.bf16_rn(f)
+        for g, o in ((got[0], o4), (got[1], o4), (got[2], o2), (got[3], o2),
+                     (got[4].view(np.uint16), ob)):
+            np.testing.assert_array_equal(g[keep], o[keep])
+        assert np.all((got[0][~keep] & 0x7F) == 0x7F)
+
+
+# --------------------------------------------------------------------------
+# nvfp4_ds_mla / fp8_ds_mla writes
+# --------------------------------------------------------------------------
+
+def run_write(kvq, oracle_mod, w, entry, init_seed=3, pad_entry=0, pad_block=0, kv_view=False,
+              threads=1, status_expected=0):
+    """GPU vs oracle write into a pre-filled cache with optional padded
+    entries / blocks; returns the GPU cache (host)."""
+    es = entry + pad_entry
+    buf0 = wl.random_bytes((w.num_blocks, w.block_size + pad_block, es), init_seed)
+    kv_bits, pe_bits = wl.bf16_bits(w.kv_c), wl.bf16_bits(w.k_pe)
+    slots = wl.host(w.slot_mapping)
+    if kv_view:            # kv_c and k_pe as column slices of one [T, 576] tensor
+        both = torch.cat([w.kv_c, w.k_pe], dim=1).to(DEV)
+        kv_c, k_pe = both[:, :512], both[:, 512:]
+    else:
+        kv_c, k_pe = dev(w.kv_c), dev(w.k_pe)
+    gbuf = dev(buf0.copy())
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    fn = kvq.kvq_write_nvfp4_ds_mla if entry == 352 else kvq.kvq_write_fp8_ds_mla
+    fn(kv_c, k_pe, gbuf[:, :w.block_size, :], dev(slots), status=status)
+    want = buf0.copy()
+    ofn = oracle_mod.write_nvfp4_ds_mla if entry == 352 else oracle_mod.write_fp8_ds_mla
+    ofn(kv_bits, pe_bits, slots, want[:, :w.block_size, :entry], threads=threads)
+    got = gbuf.cpu().numpy()
+    assert int(status.item()) == status_expected
+    np.testing.assert_array_equal(got, want)
+    return got
+
+
+WRITE_CASES = [
+    ("smoke T=256", lambda: wl.smoke_write(), {}),
+    ("decode T=8192 outliers", lambda: wl.decode_write(), {}),
+    ("single token", lambda: wl.make_write("t1", 1, 1, 64, 0, 61), {}),
+    ("ragged T=37", lambda: wl.make_write("t37", 37, 2, 64, 5, 62), {}),
+    ("all padding", lambda: wl.make_write("pad", 40, 1, 64, 40, 63), {}),
+    ("block_size 1", lambda: wl.make_write("bs1", 250, 300, 1, 3, 64), {}),
+    ("block_size 16 padded strides", lambda: wl.make_write("bs16", 333, 40, 16, 9, 65),
+     dict(pad_entry=16, pad_block=3)),
+    ("kv_c / k_pe slices of one tensor", lambda: wl.make_write("view", 129, 4, 64, 2, 66),
+     dict(kv_view=True)),
+]
+
+
+@pytest.mark.parametrize("entry", [352, 656])
+@pytest.mark.parametrize("name,make,kw", WRITE_CASES, ids=[c[0] for c in WRITE_CASES])
+def test_write_parity(kvq, oracle_mod, threads, entry, name, make, kw):
+    run_write(kvq, oracle_mod, make(), entry, threads=threads, **kw)
+
+
+@pytest.mark.parametrize("entry", [352, 656])
+def test_write_parity_extreme_values(kvq, oracle_mod, entry):
+    """Random finite bf16 bit patterns (subnormals, zeros, huge values), plus
+    all-zero and negative-zero groups and tiles."""
+    T = 300
+    kv = finite_bf16_bits((T, 512), 71)
+    pe = finite_bf16_bits((T, 64), 72)
+    kv[5, :] = 0
+    kv[6, :] = 0x8000
+    kv[7, :128] = 0x0001                       # smallest subnormal
+    kv[8, 16:32] = 0x7F7F                      # largest finite
+    slots = wl.slot_mapping(T, 8 * 64, 7, 73)
+    w = wl.WriteWorkload("extreme", bits_to_bf16(kv), bits_to_bf16(pe), torch.from_numpy(slots), 8, 64, entry)
+    run_write(kvq, oracle_mod, w, entry)
+
+
+@pytest.mark.parametrize("entry", [352, 656])
+def test_write_out_of_range_slots_are_skipped_and_reported(kvq, oracle_mod, entry):
+    w = wl.make_write("oob", 100, 2, 64, 4, 74)
+    slots = wl.host(w.slot_mapping).copy()
+    slots[[3, 50, 99]] = [128, 10 ** 12, 129]
+    w.slot_mapping = torch.from_numpy(slots)
+    run_write(kvq, oracle_mod, w, entry, status_expected=kvq.STATUS_BAD_INDEX)
+
+
+def test_write_prefill_fill_full_size(kvq, oracle_mod, threads):
+    """The 65536 x 64 x 352 cache written over all 4,194,304 slots."""
+    g = wl.prefill_gather(DEV)
+    w = g.fill
+    cache = torch.zeros((w.num_blocks, w.block_size, 352), dtype=torch.uint8, device=DEV)
+    kvq.kvq_write_nvfp4_ds_mla(w.kv_c, w.k_pe, cache, w.slot_mapping)
+    want = np.zeros((w.num_blocks, w.block_size, 352), np.uint8)
+    oracle_mod.write_nvfp4_ds_mla(wl.bf16_bits(w.kv_c), wl.bf16_bits(w.k_pe), wl.host(w.slot_mapping),
+                                  want, threads=threads)
+    got = cache.cpu().numpy()
+    assert np.array_equal(got, want), f"{int((got != want).sum())} bytes differ"
+
+
+# --------------------------------------------------------------------------
+# gathers
+# --------------------------------------------------------------------------
+
+def run_gather(kvq, oracle_mod, entry, cache_host, table, ws, starts, T, batch_size=None,
+               dst_pad=0, pad_entry=0, pad_block=0, status_expected=0, threads=1):
+    nb, bs, _ = cache_host.shape
+    buf = np.zeros((nb, bs + pad_block, entry + pad_entry), np.uint8)
+    buf[:, :bs, :entry] = cache_host
+    gbuf = dev(buf)
+    dst = torch.full((T, 576 + dst_pad), -7.0, dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    fn = kvq.kvq_gather_upconvert_nvfp4_ds_mla if entry == 352 else kvq.kvq_gather_upconvert_fp8_ds_mla
+    fn(gbuf[:, :bs, :], dst[:, :576] if dst_pad else dst, dev(table), dev(ws), dev(starts),
+       batch_size=batch_size, status=status)
+    guard = wl.bf16_bits(torch.tensor([-7.0], dtype=torch.bfloat16))[0]
+    want = np.full((T, 576), guard, np.uint16)
+    ofn = oracle_mod.gather_nvfp4_ds_mla if entry == 352 else oracle_mod.gather_fp8_ds_mla
+    B = len(starts) if batch_size is None else batch_size
+    ofn(cache_host, table, np.asarray(ws)[:B], np.asarray(starts)[:B], T, dst=want, threads=threads)
+    got = wl.bf16_bits(dst)
+    assert int(status.item()) == status_expected
+    np.testing.assert_array_equal(got[:, :576], want)
+    if dst_pad:
+        assert np.all(got[:, 576:] == guard)
+
+
+def oracle_cache(oracle_mod, w, threads=1):
+    c = np.zeros((w.num_blocks, w.block_size, w.entry_bytes), np.uint8)
+    fn = oracle_mod.write_nvfp4_ds_mla if w.entry_bytes == 352 else oracle_mod.write_fp8_ds_mla
+    fn(wl.bf16_bits(w.kv_c), wl.bf16_bits(w.k_pe), wl.host(w.slot_mapping), c, threads=threads)
+    return c
+
+
+def random_nvfp4_cache(nb, bs, seed):
+    c = wl.random_bytes((nb, bs, 352), seed)
+    wl.nan_free_e4m3_bytes(c[..., 256:352])
+    return c
+
+
+def random_fp8_cache(nb, bs, seed):
+    g = np.random.Generator(np.random.PCG64(seed))
+    c = wl.random_bytes((nb, bs, 656), seed + 1)
+    wl.nan_free_e4m3_bytes(c[..., :512])
+    s = (np.exp2(g.integers(-20, 12, size=(nb, bs, 4))) *
+         np.where(g.random((nb, bs, 4)) < 0.5, 1.0, 1.0 + g.random((nb, bs, 4)))).astype("<f4")
+    c[..., 512:528] = s.view(np.uint8).reshape(nb, bs, 16)
+    return c
+
+
+GATHER_CASES = [
+    # name, (nb, bs), lens, starts, extra
+    ("two requests", (8, 64), [100, 120], [0, 17], {}),
+    ("zero-length and block-edge starts", (16, 64), [0, 64, 1, 0, 130], [0, 64, 63, 5, 0], {}),
+    ("ragged rows T=130", (8, 64), [130], [1], {}),
+    ("block_size 16, padded strides", (64, 16), [77, 5, 200], [15, 16, 31],
+     dict(pad_entry=32, pad_block=1, dst_pad=64)),
+    ("300 short requests", (600, 16), list(range(1, 301)), [i % 40 for i in range(300)], {}),
+]
+
+
+@pytest.mark.parametrize("entry", [352, 656])
+@pytest.mark.parametrize("name,geom,lens,starts,kw", GATHER_CASES, ids=[c[0] for c in GATHER_CASES])
+def test_gather_parity_random_cache(kvq, oracle_mod, entry, name, geom, lens, starts, kw):
+    nb, bs = geom
+    cache = random_nvfp4_cache(nb, bs, 81) if entry == 352 else random_fp8_cache(nb, bs, 82)
+    table, ws, st, T = wl.make_gather_batch(nb, bs, lens, starts, 83)
+    run_gather(kvq, oracle_mod, entry, cache, table, ws, st, T, **kw)
+
+
+@pytest.mark.parametrize("entry", [352, 656])
+def test_gather_of_written_cache(kvq, oracle_mod, entry):
+    fill = wl.make_fill("f", 8, 64, 84, entry_bytes=entry)
+    cache = oracle_cache(oracle_mod, fill)
+    table, ws, st, T = wl.make_gather_batch(8, 64, [100, 120], [0, 17], 85)
+    run_gather(kvq, oracle_mod, entry, cache, table, ws, st, T)
+
+
+@pytest.mark.parametrize("entry", [352, 656])
+def test_gather_accepts_cu_seq_lens(kvq, oracle_mod, entry):
+    cache = random_nvfp4_cache(8, 64, 86) if entry == 352 else random_fp8_cache(8, 64, 86)
+    table, ws, st, T = wl.make_gather_batch(8, 64, [50, 70, 30], [3, 0, 9], 87)
+    cu = np.concatenate([ws, [T]]).astype(np.int32)
+    run_gather(kvq, oracle_mod, entry, cache, table, cu, st, T, batch_size=3)
+
+
+@pytest.mark.parametrize("entry", [352, 656])
+def test_gather_bad_block_ids_skip_rows_and_report(kvq, oracle_mod, entry):
+    cache = random_nvfp4_cache(8, 64, 88) if entry == 352 else random_fp8_cache(8, 64, 88)
+    table, ws, st, T = wl.make_gather_batch(8, 64, [100, 120], [0, 17], 89)
+    table = table.copy()
+    table[0, 1] = 8            # one past the last block
+    table[1, 0] = -1
+    run_gather(kvq, oracle_mod, entry, cache, table, ws, st, T, status_expected=kvq.STATUS_BAD_INDEX)
+
+
+def test_gather_non_monotone_workspace_starts_reported(kvq):
+    cache = dev(random_nvfp4_cache(8, 64, 90))
+    table, _, st, _ = wl.make_gather_batch(8, 64, [50, 50], [0, 0], 91)
+    dst = torch.zeros((100, 576), dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kvq.kvq_gather_upconvert_nvfp4_ds_mla(cache, dst, dev(table), dev(np.array([60, 10], np.int32)),
+                                          dev(st), status=status)
+    assert int(status.item()) & kvq.STATUS_BAD_BATCH
+
+
+def test_gather_prefill_full_size(kvq, oracle_mod, threads):
+    """32 requests of 4k-32k rows over the 65536 x 64 cache written by the
+    GPU fill: cache and every gathered row against the oracle."""
+    g = wl.prefill_gather(DEV)
+    w = g.fill
+    cache = torch.zeros((w.num_blocks, w.block_size, 352), dtype=torch.uint8, device=DEV)
+    kvq.kvq_write_nvfp4_ds_mla(w.kv_c, w.k_pe, cache, w.slot_mapping)
+    dst = torch.empty((g.num_out_tokens, 576), dtype=torch.bfloat16, device=DEV)
+    kvq.kvq_gather_upconvert_nvfp4_ds_mla(cache, dst, g.block_table, g.workspace_starts, g.seq_starts)
+    ocache = oracle_cache(oracle_mod, w, threads)
+    got_cache = cache.cpu().numpy()
+    assert np.array_equal(got_cache, ocache)
+    del got_cache
+    want, skipped = oracle_mod.gather_nvfp4_ds_mla(ocache, wl.host(g.block_table), wl.host(g.workspace_starts),
+                                                   wl.host(g.seq_starts), g.num_out_tokens, threads=threads)
+    assert skipped == 0
+    got = wl.bf16_bits(dst)
+    assert np.array_equal(got, want), f"{int((got != want).sum())} values differ"
+
+
+def test_gather_fp8_full_size(kvq, oracle_mod, threads):
+    """16 requests x 16384 rows over the 32768 x 64 x 656 cache written by the
+    GPU fp8 fill: cache and every gathered row against the oracle."""
+    g = wl.fp8_gather(DEV)
+    w = g.fill
+    cache = torch.zeros((w.num_blocks, w.block_size, 656), dtype=torch.uint8, device=DEV)
+    kvq.kvq_write_fp8_ds_mla(w.kv_c, w.k_pe, cache, w.slot_mapping)
+    dst = torch.empty((g.num_out_tokens, 576), dtype=torch.bfloat16, device=DEV)
+    kvq.kvq_gather_upconvert_fp8_ds_mla(cache, dst, g.block_table, g.workspace_starts, g.seq_starts)
+    ocache = oracle_cache(oracle_mod, w, threads)
+    got_cache = cache.cpu().numpy()
+    assert np.array_equal(got_cache, ocache)
+    del got_cache
+    want, skipped = oracle_mod.gather_fp8_ds_mla(ocache, wl.host(g.block_table), wl.host(g.workspace_starts),
+                                                 wl.host(g.seq_starts), g.num_out_tokens, threads=threads)
+    assert skipped == 0
+    got = wl.bf16_bits(dst)
+    assert np.array_equal(got, want), f"{int((got != want).sum())} values differ"
+
+
+# --------------------------------------------------------------------------
+# per-head NVFP4 cache
+# --------------------------------------------------------------------------
+
+def run_per_head(kvq, oracle_mod, w, strided=False, status_expected=0, threads=1):
+    T, H, D = w.key.shape
+    fd = kvq.nvfp4_full_dim(D)
+    init = wl.random_bytes((w.num_pages, 2, w.block_size, H, fd), 5)
+    cache = dev(init.copy())
+    if strided:            # key and value as interleaved halves of one [T, H, 2D] tensor
+        both = torch.cat([w.key, w.value], dim=2).to(DEV)
+        key, value = both[:, :, :D], both[:, :, D:]
+    else:
+        key, value = dev(w.key), dev(w.value)
+    ks = torch.tensor([w.k_scale], dtype=torch.float32, device=DEV)
+    vs = torch.tensor([w.v_scale], dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kvq.kvq_reshape_and_cache_nvfp4(key, value, cache, dev(w.slot_mapping), ks, vs, status=status)
+    want = init.copy()
+    oracle_mod.reshape_and_cache_nvfp4(wl.bf16_bits(w.key), wl.bf16_bits(w.value), wl.host(w.slot_mapping),
+                                       want, w.k_scale, w.v_scale, threads=threads)
+    assert int(status.item()) == status_expected
+    got = cache.cpu().numpy()
+    assert np.array_equal(got, want), f"{int((got != want).sum())} bytes differ"
+
+
+PER_HEAD_CASES = [
+    ("H8 D128", lambda: wl.make_per_head("a", 333, 8, 128, 64, 16, 11, 101), {}),
+    ("H1 D64 scales", lambda: wl.make_per_head("b", 100, 1, 64, 16, 16, 3, 102, k_scale=0.75,
+                                               v_scale=3.0), {}),
+    ("H4 D256", lambda: wl.make_per_head("c", 77, 4, 256, 8, 16, 0, 103, k_scale=2.0), {}),
+    ("H8 D128 strided", lambda: wl.make_per_head("d", 129, 8, 128, 32, 16, 4, 104), dict(strided=True)),
+    ("block_size 1", lambda: wl.make_per_head("e", 50, 8, 128, 64, 1, 2, 105), {}),
+]
+
+
+@pytest.mark.parametrize("name,make,kw", PER_HEAD_CASES, ids=[c[0] for c in PER_HEAD_CASES])
+def test_per_head_parity(kvq, oracle_mod, name, make, kw):
+    run_per_head(kvq, oracle_mod, make(), **kw)
+
+
+def test_per_head_out_of_range_slots(kvq, oracle_mod):
+    w = wl.make_per_head("oob", 40, 8, 128, 4, 16, 2, 106)
+    s = wl.host(w.slot_mapping).copy()
+    s[[0, 7]] = [64, 1000]
+    w.slot_mapping = torch.from_numpy(s)
+    run_per_head(kvq, oracle_mod, w, status_expected=kvq.STATUS_BAD_INDEX)
+
+
+def test_per_head_full_size(kvq, oracle_mod, threads):
+    run_per_head(kvq, oracle_mod, wl.per_head(), threads=threads)
