@@ -240,7 +240,7 @@ GATHER_CASES = [
     ("ragged rows T=130", (8, 64), [130], [1], {}),
     ("block_size 16, padded strides", (64, 16), [77, 5, 200], [15, 16, 31],
      dict(pad_entry=32, pad_block=1, dst_pad=64)),
-    ("300 short requests", (600, 16), list(range(1, 301)), [i % 40 for i in range(300)], {}),
+    ("300 short requests", (4096, 16), list(range(1, 301)), [i % 40 for i in range(300)], {}),
 ]
 
 
