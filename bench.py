@@ -197,13 +197,22 @@ def committed_traffic():
 class GpuStep:
     """Device-resident inputs and outputs of one step, and its launches."""
 
-    def __init__(self, device):
+    def __init__(self, device, size: str = "full"):
         import fp8_quantized_paged_concat_gb300 as kvq
         kvq.load_library()
         self.kvq = kvq
         self.device = device
-        self.g3 = wl.prefill_gather(device)
-        self.g4 = wl.fp8_gather(device)
+        if size == "full":
+            self.g3 = wl.prefill_gather(device)
+            self.g4 = wl.fp8_gather(device)
+        else:    # profiling case: same kernels, a few hundred MB (still above the 129 MB L2)
+            g = np.random.Generator(np.random.PCG64(3003))
+            f3 = wl.make_fill("small fill 4096x64", 4096, 64, 3003, device, rng="device")
+            self.g3 = wl.make_gather("small nvfp4 gather", f3, g.integers(4096, 16384, 8, endpoint=True),
+                                     g.integers(1, 4095, 8, endpoint=True), 3003, device)
+            f4 = wl.make_fill("small fp8 fill 4096x64", 4096, 64, 3004, device, entry_bytes=656, rng="device")
+            self.g4 = wl.make_gather("small fp8 gather", f4, [16384] * 4,
+                                     g.integers(1, 4095, 4, endpoint=True), 3004, device)
         self.ph = wl.per_head(device)
         f3, f4 = self.g3.fill, self.g4.fill
         self.cache3 = torch.zeros((f3.num_blocks, f3.block_size, 352), dtype=torch.uint8, device=device)
@@ -415,12 +424,16 @@ class CpuSample:
 
 
 def cpu_baseline(threads):
+    """The oracle on all host cores over the bounded sample, repeated until
+    about 1.5 s of wall time (at most 8 passes)."""
     s = CpuSample(threads)
-    times = s.step()
-    total = sum(times.values())
-    return {"value": round(s.bytes_per_step() / total / 1e9, 3), "unit": "GB/s", "cores": threads,
-            "kind": "oracle", "sample": s.description,
-            "tokens_per_s": round(s.tokens_per_step() / total, 1), "seconds": round(total, 2)}
+    total, passes = 0.0, 0
+    while passes < 8 and (passes == 0 or total < 1.5):
+        total += sum(s.step().values())
+        passes += 1
+    return {"value": round(passes * s.bytes_per_step() / total / 1e9, 3), "unit": "GB/s",
+            "cores": threads, "kind": "oracle", "sample": f"{passes} passes of: {s.description}",
+            "tokens_per_s": round(passes * s.tokens_per_step() / total, 1), "seconds": round(total, 2)}
 
 
 # --------------------------------------------------------------------------
@@ -467,7 +480,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     init_dist(world, "nccl")
-    step = GpuStep(device)
+    step = GpuStep(device, args.size)
     visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     ids = [v.strip() for v in visible.split(",") if v.strip()]
     clocks = ClockSampler(ids[local] if local < len(ids) else str(local))
@@ -537,6 +550,8 @@ def main(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-extra", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--size", choices=["full", "small"], default="full",
+                   help="small: the same kernels on ~0.4 GB inputs, for profiler captures")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
