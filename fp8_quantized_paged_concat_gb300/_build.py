@@ -40,16 +40,19 @@ def _headers_mtime() -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compiles and links libkvq.so if any source is newer; returns its path."""
-    os.makedirs(OBJDIR, exist_ok=True)
-    os.makedirs(os.path.dirname(LIBRARY), exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), library: str = LIBRARY,
+          objdir: str = OBJDIR) -> str:
+    """Compiles and links libkvq.so if any source is newer; returns its path.
+    ``extra_flags`` / ``library`` / ``objdir`` build a variant elsewhere (for
+    example with -D tuning knobs) without touching the default library."""
+    os.makedirs(objdir, exist_ok=True)
+    os.makedirs(os.path.dirname(library), exist_ok=True)
     hdr = _headers_mtime()
     compiler = nvcc()
 
     def compile_one(src: str) -> str:
         s = os.path.join(CSRC, src)
-        o = os.path.join(OBJDIR, src.replace(".cu", ".o"))
+        o = os.path.join(objdir, src.replace(".cu", ".o"))
         if force or not os.path.exists(o) or os.path.getmtime(o) < max(hdr, os.path.getmtime(s)):
             cmd = [compiler, *NVCC_FLAGS, *extra_flags, "-c", s, "-o", o]
             if verbose:
@@ -63,15 +66,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as pool:
         objs = list(pool.map(compile_one, SOURCES))
-    if force or not os.path.exists(LIBRARY) or os.path.getmtime(LIBRARY) < max(map(os.path.getmtime, objs)):
-        tmp = LIBRARY + ".tmp.%d" % os.getpid()
+    if force or not os.path.exists(library) or os.path.getmtime(library) < max(map(os.path.getmtime, objs)):
+        tmp = library + ".tmp.%d" % os.getpid()
         cmd = [compiler, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
                "-Xlinker", "-rpath," + os.path.join(os.path.dirname(os.path.dirname(compiler)), "lib64")]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"linking libkvq.so failed:\n{r.stderr}")
-        os.replace(tmp, LIBRARY)
-    return LIBRARY
+        os.replace(tmp, library)
+    return library
 
 
 if __name__ == "__main__":

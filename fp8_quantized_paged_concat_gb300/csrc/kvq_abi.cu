@@ -62,7 +62,8 @@ kvq_status check_mla_cache(const char* fn, const void* cache, int64_t num_blocks
   KVQ_REQUIRE(cache != nullptr, "%s: cache is NULL", fn);
   KVQ_REQUIRE(aligned(cache, 16), "%s: cache base must be 16-byte aligned", fn);
   KVQ_REQUIRE(num_blocks > 0 && block_size > 0, "%s: num_blocks and block_size must be positive", fn);
-  KVQ_REQUIRE(num_blocks <= INT64_MAX / block_size, "%s: num_blocks * block_size overflows", fn);
+  KVQ_REQUIRE(num_blocks <= (int64_t{1} << 32) / block_size,
+              "%s: num_blocks * block_size must not exceed 2^32 slots", fn);
   KVQ_REQUIRE(entry_stride >= entry_bytes && entry_stride % 16 == 0,
               "%s: entry_stride must be >= %lld and a multiple of 16 (got %lld)", fn,
               static_cast<long long>(entry_bytes), static_cast<long long>(entry_stride));
@@ -101,8 +102,9 @@ kvq_status write_common(const char* fn, int64_t entry_bytes,
                                      entry_stride, entry_bytes))
     return s;
   if (kvq_status s = check_device(fn)) return s;
-  const kvq::WriteArgs a{kv_c,      kv_c_stride, k_pe,       k_pe_stride,  slot_mapping,
-                         num_tokens, kv_cache,   num_blocks * block_size, block_size,
+  const kvq::WriteArgs a{kv_c,       kv_c_stride,  k_pe,         k_pe_stride,
+                         slot_mapping, num_tokens, kv_cache,   num_blocks * block_size,
+                         block_size, kvq::FastDiv::make(static_cast<uint32_t>(block_size)),
                          block_stride, entry_stride, d_status};
   return launched(fn, launch(a, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -134,7 +136,8 @@ kvq_status gather_common(const char* fn, int64_t entry_bytes,
   const kvq::GatherArgs a{src_cache,        num_blocks,       block_size,        block_stride,
                           entry_stride,     dst,              dst_stride,        num_out_tokens,
                           block_table,      block_table_stride, block_table_width, workspace_starts,
-                          seq_starts,       batch_size,       d_status};
+                          seq_starts,       batch_size,       d_status,
+                          kvq::FastDiv::make(static_cast<uint32_t>(block_size))};
   return launched(fn, launch(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -202,9 +205,8 @@ kvq_status kvq_reshape_and_cache_nvfp4(const void* key, const void* value, int64
   if (num_tokens == 0) return ok();
   KVQ_REQUIRE(num_heads > 0 && head_size >= 16 && head_size % 16 == 0,
               "%s: need num_heads > 0 and head_size a positive multiple of 16", fn);
-  KVQ_REQUIRE(num_tokens < (int64_t{1} << 31) &&
-                  num_tokens * 2 * num_heads * (head_size / 16) < (int64_t{1} << 38),
-              "%s: problem too large", fn);
+  KVQ_REQUIRE(num_tokens * 2 * num_heads * (head_size / 16) < (int64_t{1} << 32) - 256,
+              "%s: num_tokens * 2 * num_heads * head_size / 16 must stay below 2^32 - 256", fn);
   KVQ_REQUIRE(key != nullptr && value != nullptr, "%s: key / value is NULL", fn);
   KVQ_REQUIRE(aligned(key, 16) && aligned(value, 16), "%s: key / value must be 16-byte aligned", fn);
   KVQ_REQUIRE(key_stride_t % 8 == 0 && key_stride_h % 8 == 0 && value_stride_t % 8 == 0 &&
@@ -216,17 +218,23 @@ kvq_status kvq_reshape_and_cache_nvfp4(const void* key, const void* value, int64
               "%s: k_scale / v_scale must be device fp32 scalars", fn);
   KVQ_REQUIRE(kv_cache != nullptr && aligned(kv_cache, 16), "%s: kv_cache must be 16-byte aligned", fn);
   KVQ_REQUIRE(num_pages > 0 && block_size > 0, "%s: num_pages and block_size must be positive", fn);
-  KVQ_REQUIRE(num_pages <= INT64_MAX / block_size, "%s: num_pages * block_size overflows", fn);
+  KVQ_REQUIRE(num_pages <= (int64_t{1} << 32) / block_size,
+              "%s: num_pages * block_size must not exceed 2^32 slots", fn);
   const int64_t full_dim = head_size / 2 + head_size / 16;
   KVQ_REQUIRE((int64_t{block_size} * num_heads * full_dim) % 8 == 0 &&
                   (int64_t{block_size} * num_heads * (head_size / 2)) % 8 == 0,
               "%s: block_size * num_heads * full_dim must be a multiple of 8", fn);
   KVQ_REQUIRE(d_status == nullptr || aligned(d_status, 4), "%s: d_status misaligned", fn);
   if (kvq_status s = check_device(fn)) return s;
+  const int32_t groups = head_size / 16;
   const kvq::PerHeadArgs a{key,          value,     key_stride_t, key_stride_h, value_stride_t,
                            value_stride_h, slot_mapping, num_tokens, num_heads, head_size,
                            kv_cache,     num_pages * block_size, block_size, k_scale, v_scale,
-                           d_status};
+                           d_status,
+                           kvq::FastDiv::make(static_cast<uint32_t>(block_size)),
+                           kvq::FastDiv::make(static_cast<uint32_t>(2 * num_heads * groups)),
+                           kvq::FastDiv::make(static_cast<uint32_t>(num_heads * groups)),
+                           kvq::FastDiv::make(static_cast<uint32_t>(groups))};
   return launched(fn, kvq::launch_reshape_and_cache_nvfp4(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

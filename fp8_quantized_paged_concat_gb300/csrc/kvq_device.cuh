@@ -28,6 +28,34 @@ static_assert(kNvSfOff + kNopeDim / kGroup == kNvEntry, "352-byte entry");
 static_assert(kF8RopeOff + 2 * kRopeDim == kF8Entry, "656-byte entry");
 
 // ---------------------------------------------------------------------------
+// division by a run-time invariant
+// ---------------------------------------------------------------------------
+
+// Unsigned 32-bit n / d for a divisor fixed at launch (1 <= d < 2^31), by a
+// multiply-high and two shifts: the round-up method of Granlund and
+// Montgomery, "Division by Invariant Integers using Multiplication" (PLDI
+// 1994), figure 4.1.  Exact for every 32-bit n.
+struct FastDiv {
+  uint32_t d, m, s1, s2;
+
+  static FastDiv make(uint32_t divisor) {
+    FastDiv f;
+    f.d = divisor;
+    uint32_t l = 0;
+    while ((uint64_t{1} << l) < divisor) ++l;          // l = ceil(log2 d)
+    f.m = static_cast<uint32_t>(((uint64_t{1} << 32) * ((uint64_t{1} << l) - divisor)) / divisor + 1);
+    f.s1 = l < 1 ? l : 1;
+    f.s2 = l > 0 ? l - 1 : 0;
+    return f;
+  }
+
+  __device__ __forceinline__ uint32_t div(uint32_t n) const {
+    const uint32_t t = __umulhi(m, n);
+    return (t + ((n - t) >> s1)) >> s2;
+  }
+};
+
+// ---------------------------------------------------------------------------
 // number formats
 // ---------------------------------------------------------------------------
 

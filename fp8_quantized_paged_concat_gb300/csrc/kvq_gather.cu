@@ -38,8 +38,14 @@ __device__ __forceinline__ int64_t resolve_row(int64_t w, const GatherArgs& a) {
   }
   const int64_t p = static_cast<int64_t>(__ldg(a.seq_starts + b)) +
                     (w - static_cast<int64_t>(__ldg(a.workspace_starts + b)));
-  const int64_t col = p / a.block_size;
-  if (p < 0 || col >= a.block_table_width) {
+  // 0 <= p < 2^32: an int32 start plus a row offset below 2^31
+  if (p < 0) {
+    report(a.status, KVQ_STATUS_BAD_INDEX);
+    return -1;
+  }
+  const uint32_t col = a.block_div.div(static_cast<uint32_t>(p));
+  const uint32_t off = static_cast<uint32_t>(p) - col * static_cast<uint32_t>(a.block_size);
+  if (col >= static_cast<uint32_t>(a.block_table_width)) {
     report(a.status, KVQ_STATUS_BAD_INDEX);
     return -1;
   }
@@ -48,7 +54,7 @@ __device__ __forceinline__ int64_t resolve_row(int64_t w, const GatherArgs& a) {
     report(a.status, KVQ_STATUS_BAD_INDEX);
     return -1;
   }
-  return blk * a.block_stride + (p % a.block_size) * a.entry_stride;
+  return blk * a.block_stride + static_cast<int64_t>(off) * a.entry_stride;
 }
 
 // Fills s_off for this CTA's rows; CTA 0 also checks that workspace_starts is

@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "kvq_device.cuh"
+
 namespace kvq {
 
 struct WriteArgs {
@@ -16,8 +18,9 @@ struct WriteArgs {
   const int64_t* slot_mapping;
   int64_t num_tokens;
   uint8_t* cache;
-  int64_t num_slots;     // num_blocks * block_size
+  int64_t num_slots;     // num_blocks * block_size, < 2^32
   int32_t block_size;
+  FastDiv block_div;     // divides a slot by block_size
   int64_t block_stride;
   int64_t entry_stride;
   int32_t* status;
@@ -39,6 +42,7 @@ struct GatherArgs {
   const int32_t* seq_starts;
   int32_t batch_size;
   int32_t* status;
+  FastDiv block_div;     // divides a position by block_size
 };
 
 struct PerHeadArgs {
@@ -55,6 +59,10 @@ struct PerHeadArgs {
   const float* k_scale;
   const float* v_scale;
   int32_t* status;
+  FastDiv block_div;     // slot -> page
+  FastDiv unit_div;      // flat index -> token (2 * H * D/16 groups per token)
+  FastDiv side_div;      // group within token -> side (H * D/16)
+  FastDiv head_div;      // group within side -> head (D/16)
 };
 
 cudaError_t launch_write_nvfp4_ds_mla(const WriteArgs& a, cudaStream_t stream);

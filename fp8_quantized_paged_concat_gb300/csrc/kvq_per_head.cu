@@ -17,16 +17,15 @@ namespace {
 constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads) reshape_and_cache_nvfp4_kernel(const PerHeadArgs a) {
-  const int groups = a.head_size / kGroup;                 // per head
-  const int64_t per_token = 2LL * a.num_heads * groups;
-  const int64_t idx = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-  const int64_t t = idx / per_token;
+  // flat index = ((t * 2 + side) * H + h) * groups + g, below 2^32 (host check)
+  const uint32_t idx = blockIdx.x * kThreads + threadIdx.x;
+  const uint32_t t = a.unit_div.div(idx);
   if (t >= a.num_tokens) return;
-  int rem = static_cast<int>(idx - t * per_token);
-  const int side = rem / (a.num_heads * groups);
-  rem -= side * a.num_heads * groups;
-  const int h = rem / groups;
-  const int g = rem - h * groups;
+  const uint32_t u = idx - t * a.unit_div.d;
+  const uint32_t side = a.side_div.div(u);
+  const uint32_t r = u - side * a.side_div.d;
+  const uint32_t h = a.head_div.div(r);
+  const uint32_t g = r - h * a.head_div.d;
 
   const int64_t slot = __ldg(a.slot_mapping + t);
   if (slot < 0) return;
@@ -36,8 +35,9 @@ __global__ void __launch_bounds__(kThreads) reshape_and_cache_nvfp4_kernel(const
   }
 
   const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(side ? a.value : a.key) +
-                             t * (side ? a.value_stride_t : a.key_stride_t) +
-                             h * (side ? a.value_stride_h : a.key_stride_h) + g * kGroup;
+                             static_cast<int64_t>(t) * (side ? a.value_stride_t : a.key_stride_t) +
+                             static_cast<int64_t>(h) * (side ? a.value_stride_h : a.key_stride_h) +
+                             g * kGroup;
   const uint4 lo = ld_stream16(src);
   const uint4 hi = ld_stream16(src + 8);
   const float inv_scale = 1.0f / __ldg(side ? a.v_scale : a.k_scale);
@@ -53,13 +53,13 @@ __global__ void __launch_bounds__(kThreads) reshape_and_cache_nvfp4_kernel(const
   }
   const uint32_t sf = nvfp4_scale_code(amax);
 
-  const int64_t page = slot / a.block_size;
-  const int64_t off = slot - page * a.block_size;
+  const uint32_t page = a.block_div.div(static_cast<uint32_t>(slot));
+  const uint32_t off = static_cast<uint32_t>(slot) - page * static_cast<uint32_t>(a.block_size);
   const int64_t data_dim = a.head_size / 2;
   const int64_t scale_dim = a.head_size / kGroup;
   const int64_t region = static_cast<int64_t>(a.block_size) * a.num_heads * (data_dim + scale_dim);
-  uint8_t* base = a.cache + (page * 2 + side) * region;
-  const int64_t row = off * a.num_heads + h;
+  uint8_t* base = a.cache + (static_cast<int64_t>(page) * 2 + side) * region;
+  const int64_t row = static_cast<int64_t>(off) * a.num_heads + h;
   st8(base + row * data_dim + 8 * g, nvfp4_pack16(y, nvfp4_inverse_scale(sf)));
   base[static_cast<int64_t>(a.block_size) * a.num_heads * data_dim + row * scale_dim + g] =
       static_cast<uint8_t>(sf);

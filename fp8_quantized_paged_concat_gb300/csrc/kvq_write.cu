@@ -15,8 +15,19 @@
 namespace kvq {
 namespace {
 
-constexpr int kWarpsPerBlock = 8;
-constexpr int kTokensPerWarp = 4;
+// Launch shape (compile-time tuning knobs; the defaults are the measured best).
+#ifndef KVQ_WRITE_WARPS_PER_BLOCK
+#define KVQ_WRITE_WARPS_PER_BLOCK 8
+#endif
+#ifndef KVQ_WRITE_TOKENS_PER_WARP
+#define KVQ_WRITE_TOKENS_PER_WARP 4
+#endif
+#ifndef KVQ_WRITE_MIN_BLOCKS
+#define KVQ_WRITE_MIN_BLOCKS 1
+#endif
+constexpr int kWarpsPerBlock = KVQ_WRITE_WARPS_PER_BLOCK;
+constexpr int kTokensPerWarp = KVQ_WRITE_TOKENS_PER_WARP;
+constexpr int kMinBlocks = KVQ_WRITE_MIN_BLOCKS;
 
 // The 8 packed bf16 pairs of one lane's 16 NoPE values, as fp32.
 __device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float (&x)[16]) {
@@ -37,16 +48,20 @@ __device__ __forceinline__ float amax16(const uint4& a, const uint4& b) {
   return fmaxf(__low2float(m), __high2float(m));
 }
 
-// Slot -> entry pointer, or nullptr for padding / out-of-range slots.
+// Slot -> entry pointer, or nullptr for padding / out-of-range slots.  Slots
+// in range are below 2^32 (checked on the host), so 32-bit division applies.
 __device__ __forceinline__ uint8_t* entry_of(int64_t slot, const WriteArgs& a) {
   if (slot < 0 || slot >= a.num_slots) return nullptr;
-  return a.cache + (slot / a.block_size) * a.block_stride + (slot % a.block_size) * a.entry_stride;
+  const uint32_t s = static_cast<uint32_t>(slot);
+  const uint32_t blk = a.block_div.div(s);
+  const uint32_t off = s - blk * static_cast<uint32_t>(a.block_size);
+  return a.cache + static_cast<int64_t>(blk) * a.block_stride + static_cast<int64_t>(off) * a.entry_stride;
 }
 
 // ---------------------------------------------------------------------------
 // nvfp4_ds_mla: 352-byte entries
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, kMinBlocks)
 write_nvfp4_ds_mla_kernel(const WriteArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t t0 =
@@ -101,7 +116,7 @@ write_nvfp4_ds_mla_kernel(const WriteArgs a) {
 // ---------------------------------------------------------------------------
 // fp8_ds_mla: 656-byte entries
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, kMinBlocks)
 write_fp8_ds_mla_kernel(const WriteArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t t0 =

@@ -136,6 +136,8 @@ WRITE_CASES = [
      dict(pad_entry=16, pad_block=3)),
     ("kv_c / k_pe slices of one tensor", lambda: wl.make_write("view", 129, 4, 64, 2, 66),
      dict(kv_view=True)),
+    ("block_size 7", lambda: wl.make_write("bs7", 300, 50, 7, 5, 67), {}),
+    ("block_size 33", lambda: wl.make_write("bs33", 301, 12, 33, 6, 68), {}),
 ]
 
 
@@ -241,6 +243,8 @@ GATHER_CASES = [
     ("block_size 16, padded strides", (64, 16), [77, 5, 200], [15, 16, 31],
      dict(pad_entry=32, pad_block=1, dst_pad=64)),
     ("300 short requests", (4096, 16), list(range(1, 301)), [i % 40 for i in range(300)], {}),
+    ("block_size 7", (200, 7), [90, 0, 300, 17], [6, 3, 0, 13], {}),
+    ("block_size 48", (40, 48), [500, 333], [47, 1], {}),
 ]
 
 
@@ -362,6 +366,7 @@ PER_HEAD_CASES = [
     ("H4 D256", lambda: wl.make_per_head("c", 77, 4, 256, 8, 16, 0, 103, k_scale=2.0), {}),
     ("H8 D128 strided", lambda: wl.make_per_head("d", 129, 8, 128, 32, 16, 4, 104), dict(strided=True)),
     ("block_size 1", lambda: wl.make_per_head("e", 50, 8, 128, 64, 1, 2, 105), {}),
+    ("H3 D48 block_size 24", lambda: wl.make_per_head("f", 90, 3, 48, 12, 24, 4, 107, v_scale=1.5), {}),
 ]
 
 
