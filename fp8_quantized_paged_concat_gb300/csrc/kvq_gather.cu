@@ -1,43 +1,64 @@
 // kvq_gather.cu -- prefill gather-upconvert of quantized MLA pages into a
 // contiguous bf16 [T, 576] workspace (nvfp4_ds_mla and fp8_ds_mla).
 //
-// Design (GB300): a CTA owns kRowsPerBlock consecutive workspace rows.  First
-// kRowsPerBlock threads resolve one row each (binary search of
-// workspace_starts, then seq_starts and block_table) into the byte offset of
-// its source entry, kept in shared memory; the whole CTA then streams the
-// entries.  NoPE: one warp per row, lane l converts 16 values (one NVFP4
-// group / a 16-byte fp8 slice) and stores 32 contiguous bytes, so a warp
-// writes a 1024-byte row segment.  RoPE: 8 lanes per row.  Each warp issues
-// the loads of all its rows before converting any of them.  Consecutive rows
-// of one request read consecutive entries of a page, so reads stay in runs of
-// up to block_size entries.
+// Design (GB300): small CTAs, warps independent of each other.  A CTA first
+// stages workspace_starts in shared memory (one coalesced load; batches
+// larger than kMaxSmemBatch search global memory instead) -- the only CTA
+// barrier.  Each warp then owns kRowsPerWarp consecutive workspace rows: lane
+// r < kRowsPerWarp resolves row r (binary search over the staged starts, then
+// seq_starts and block_table) into the byte offset of its source entry and
+// the warp shares the offsets by shuffle.  NoPE: one row at a time across the
+// warp, lane l converting 16 values (one NVFP4 group / a 16-byte fp8 slice)
+// and storing 32 contiguous bytes, so each row is one 1024-byte segment; the
+// loads of all the warp's rows are issued before any conversion.  RoPE: 8
+// lanes per row.  Consecutive rows of a request read consecutive entries of a
+// page, so reads stay in runs of up to block_size entries.
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
 
 namespace kvq {
 namespace {
 
-constexpr int kRowsPerBlock = 64;
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kRowsPerWarp = kRowsPerBlock / kWarps;   // NoPE rows per warp
-constexpr int kRopeItems = kRowsPerBlock * 8 / kThreads;  // RoPE pieces per thread
+#ifndef KVQ_GATHER_WARPS_PER_BLOCK
+#define KVQ_GATHER_WARPS_PER_BLOCK 4
+#endif
+#ifndef KVQ_GATHER_ROWS_PER_WARP
+#define KVQ_GATHER_ROWS_PER_WARP 8
+#endif
+#ifndef KVQ_GATHER_MIN_BLOCKS
+#define KVQ_GATHER_MIN_BLOCKS 8
+#endif
+constexpr int kWarps = KVQ_GATHER_WARPS_PER_BLOCK;
+constexpr int kThreads = kWarps * 32;
+constexpr int kRowsPerWarp = KVQ_GATHER_ROWS_PER_WARP;
+constexpr int kRowsPerBlock = kWarps * kRowsPerWarp;
+constexpr int kMinBlocks = KVQ_GATHER_MIN_BLOCKS;
+constexpr int kRopeItems = kRowsPerWarp * 8 / 32;          // RoPE pieces per lane (4 rows each)
+constexpr int kMaxSmemBatch = 1024;                         // starts staged in smem
+static_assert(kRowsPerWarp <= 32 && (kRowsPerWarp * 8) % 32 == 0, "row tiling");
 
-// Byte offset of the source entry of workspace row w, or -1.
-__device__ __forceinline__ int64_t resolve_row(int64_t w, const GatherArgs& a) {
-  // largest b with workspace_starts[b] <= w (binary search; ws non-decreasing)
-  int lo = 0, hi = a.batch_size;
+// Largest b with starts[b] <= w (starts non-decreasing), or -1.
+template <typename Load>
+__device__ __forceinline__ int find_request(int64_t w, int batch, Load starts) {
+  int lo = 0, hi = batch;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    if (static_cast<int64_t>(__ldg(a.workspace_starts + mid)) <= w) lo = mid + 1; else hi = mid;
+    if (static_cast<int64_t>(starts(mid)) <= w) lo = mid + 1; else hi = mid;
   }
-  const int b = lo - 1;
+  return lo - 1;
+}
+
+// Byte offset of the source entry of workspace row w, or -1.
+__device__ __forceinline__ int64_t resolve_row(int64_t w, const GatherArgs& a, const int32_t* s_ws) {
+  const int b = a.batch_size <= kMaxSmemBatch
+                    ? find_request(w, a.batch_size, [&](int i) { return s_ws[i]; })
+                    : find_request(w, a.batch_size, [&](int i) { return __ldg(a.workspace_starts + i); });
   if (b < 0) {
     report(a.status, KVQ_STATUS_BAD_BATCH);
     return -1;
   }
-  const int64_t p = static_cast<int64_t>(__ldg(a.seq_starts + b)) +
-                    (w - static_cast<int64_t>(__ldg(a.workspace_starts + b)));
+  const int64_t ws_b = a.batch_size <= kMaxSmemBatch ? s_ws[b] : __ldg(a.workspace_starts + b);
+  const int64_t p = static_cast<int64_t>(__ldg(a.seq_starts + b)) + (w - ws_b);
   // 0 <= p < 2^32: an int32 start plus a row offset below 2^31
   if (p < 0) {
     report(a.status, KVQ_STATUS_BAD_INDEX);
@@ -57,13 +78,14 @@ __device__ __forceinline__ int64_t resolve_row(int64_t w, const GatherArgs& a) {
   return blk * a.block_stride + static_cast<int64_t>(off) * a.entry_stride;
 }
 
-// Fills s_off for this CTA's rows; CTA 0 also checks that workspace_starts is
-// non-decreasing inside [0, num_out] when a status word is given.
-__device__ __forceinline__ void resolve_rows(const GatherArgs& a, int64_t w0, int64_t* s_off) {
-  if (threadIdx.x < kRowsPerBlock) {
-    const int64_t w = w0 + threadIdx.x;
-    s_off[threadIdx.x] = w < a.num_out ? resolve_row(w, a) : -1;
-  }
+// Stages workspace_starts in shared memory (CTA 0 also validates them when a
+// status word is given), then gives every lane the source offsets of its
+// warp's rows: offs[k] is row w0 + k's offset (or -1), also held by lane k in
+// `mine`.  Returns w0.
+__device__ __forceinline__ int64_t resolve_warp_rows(const GatherArgs& a, int32_t* s_ws,
+                                                     int64_t (&offs)[kRowsPerWarp], int64_t& mine) {
+  if (a.batch_size <= kMaxSmemBatch)
+    for (int b = threadIdx.x; b < a.batch_size; b += kThreads) s_ws[b] = __ldg(a.workspace_starts + b);
   if (a.status != nullptr && blockIdx.x == 0) {
     for (int b = threadIdx.x; b < a.batch_size; b += kThreads) {
       const int32_t v = __ldg(a.workspace_starts + b);
@@ -73,6 +95,13 @@ __device__ __forceinline__ void resolve_rows(const GatherArgs& a, int64_t w0, in
     }
   }
   __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5)) * kRowsPerWarp;
+  mine = -1;
+  if (lane < kRowsPerWarp && w0 + lane < a.num_out) mine = resolve_row(w0 + lane, a, s_ws);
+#pragma unroll
+  for (int k = 0; k < kRowsPerWarp; ++k) offs[k] = __shfl_sync(kFull, mine, k);
+  return w0;
 }
 
 // 8 e4m3 codes -> 8 bf16 (exact), as 4 packed words.
@@ -88,30 +117,36 @@ __device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint2 c) {
 // ---------------------------------------------------------------------------
 // nvfp4_ds_mla
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) gather_nvfp4_ds_mla_kernel(const GatherArgs a) {
-  __shared__ int64_t s_off[kRowsPerBlock];
-  const int64_t w0 = static_cast<int64_t>(blockIdx.x) * kRowsPerBlock;
-  resolve_rows(a, w0, s_off);
-
+__global__ void __launch_bounds__(kThreads, kMinBlocks) gather_nvfp4_ds_mla_kernel(const GatherArgs a) {
+  __shared__ int32_t s_ws[kMaxSmemBatch];
+  int64_t offs[kRowsPerWarp], mine;
+  const int64_t w0 = resolve_warp_rows(a, s_ws, offs, mine);
+  // RoPE piece k of this lane: row (lane / 8) + 4k, piece lane % 8
+  int64_t roff[kRopeItems];
+#pragma unroll
+  for (int k = 0; k < kRopeItems; ++k) roff[k] = __shfl_sync(kFull, mine, ((threadIdx.x & 31) >> 3) + 4 * k);
   const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
   __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dst);
 
-  // NoPE: warp handles rows warp, warp + 8, ...; lane = NVFP4 group.
+  // Issue every load of the warp's rows first: NoPE group `lane` (8 bytes and
+  // its scale byte) and RoPE pieces (8 bytes each).
   uint2 q[kRowsPerWarp];
   uint32_t sf[kRowsPerWarp];
+  uint2 rp[kRopeItems];
 #pragma unroll
   for (int k = 0; k < kRowsPerWarp; ++k) {
-    const int64_t off = s_off[warp + kWarps * k];
-    if (off >= 0) {
-      q[k] = ld_stream8(a.cache + off + 8 * lane);
-      sf[k] = ld_byte(a.cache + off + kNvSfOff + lane);
+    if (offs[k] >= 0) {
+      q[k] = ld_stream8(a.cache + offs[k] + 8 * lane);
+      sf[k] = ld_byte(a.cache + offs[k] + kNvSfOff + lane);
     }
   }
 #pragma unroll
+  for (int k = 0; k < kRopeItems; ++k)
+    if (roff[k] >= 0) rp[k] = ld_stream8(a.cache + roff[k] + kNvRopeOff + 8 * (lane & 7));
+
+#pragma unroll
   for (int k = 0; k < kRowsPerWarp; ++k) {
-    const int r = warp + kWarps * k;
-    if (s_off[r] < 0) continue;
+    if (offs[k] < 0) continue;
     const float scale = e4m3_to_float(sf[k]);
     uint32_t o[8];
 #pragma unroll
@@ -120,51 +155,52 @@ __global__ void __launch_bounds__(kThreads) gather_nvfp4_ds_mla_kernel(const Gat
       const float2 v = __half22float2(e2m1x2_to_half2(byte));
       o[i] = pack_bf16x2(v.x * scale, v.y * scale);     // exact products
     }
-    __nv_bfloat16* out = dst + (w0 + r) * a.dst_stride + 16 * lane;
+    __nv_bfloat16* out = dst + (w0 + k) * a.dst_stride + 16 * lane;
     st16(out, make_uint4(o[0], o[1], o[2], o[3]));
     st16(out + 8, make_uint4(o[4], o[5], o[6], o[7]));
   }
-
-  // RoPE: 8 pieces of 8 values per row.
 #pragma unroll
   for (int k = 0; k < kRopeItems; ++k) {
-    const int item = threadIdx.x + kThreads * k;
-    const int r = item >> 3, piece = item & 7;
-    const int64_t off = s_off[r];
-    if (off < 0) continue;
-    const uint2 c = ld_stream8(a.cache + off + kNvRopeOff + 8 * piece);
-    st16(dst + (w0 + r) * a.dst_stride + kNopeDim + 8 * piece, e4m3x8_to_bf16x8(c));
+    if (roff[k] < 0) continue;
+    const int r = (lane >> 3) + 4 * k;
+    st16(dst + (w0 + r) * a.dst_stride + kNopeDim + 8 * (lane & 7), e4m3x8_to_bf16x8(rp[k]));
   }
 }
 
 // ---------------------------------------------------------------------------
 // fp8_ds_mla
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) gather_fp8_ds_mla_kernel(const GatherArgs a) {
-  __shared__ int64_t s_off[kRowsPerBlock];
-  const int64_t w0 = static_cast<int64_t>(blockIdx.x) * kRowsPerBlock;
-  resolve_rows(a, w0, s_off);
-
+__global__ void __launch_bounds__(kThreads, kMinBlocks) gather_fp8_ds_mla_kernel(const GatherArgs a) {
+  __shared__ int32_t s_ws[kMaxSmemBatch];
+  int64_t offs[kRowsPerWarp], mine;
+  const int64_t w0 = resolve_warp_rows(a, s_ws, offs, mine);
+  // RoPE piece k of this lane: row (lane / 8) + 4k, piece lane % 8
+  int64_t roff[kRopeItems];
+#pragma unroll
+  for (int k = 0; k < kRopeItems; ++k) roff[k] = __shfl_sync(kFull, mine, ((threadIdx.x & 31) >> 3) + 4 * k);
   const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
   __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dst);
 
-  // NoPE: lane converts bytes [16 lane, 16 lane + 16), scale lane / 8.
+  // NoPE: lane converts bytes [16 lane, 16 lane + 16) with scale lane / 8;
+  // RoPE: bf16 bits copied, 8 pieces of 16 bytes per row.
   uint4 q[kRowsPerWarp];
   float s[kRowsPerWarp];
+  uint4 rp[kRopeItems];
 #pragma unroll
   for (int k = 0; k < kRowsPerWarp; ++k) {
-    const int64_t off = s_off[warp + kWarps * k];
-    if (off >= 0) {
-      q[k] = ld_stream16(a.cache + off + 16 * lane);
+    if (offs[k] >= 0) {
+      q[k] = ld_stream16(a.cache + offs[k] + 16 * lane);
       s[k] = __uint_as_float(__ldg(reinterpret_cast<const unsigned int*>(
-          a.cache + off + kF8ScaleOff + 4 * (lane >> 3))));
+          a.cache + offs[k] + kF8ScaleOff + 4 * (lane >> 3))));
     }
   }
 #pragma unroll
+  for (int k = 0; k < kRopeItems; ++k)
+    if (roff[k] >= 0) rp[k] = ld_stream16(a.cache + roff[k] + kF8RopeOff + 16 * (lane & 7));
+
+#pragma unroll
   for (int k = 0; k < kRowsPerWarp; ++k) {
-    const int r = warp + kWarps * k;
-    if (s_off[r] < 0) continue;
+    if (offs[k] < 0) continue;
     const uint32_t w[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
     uint32_t o[8];
 #pragma unroll
@@ -174,20 +210,15 @@ __global__ void __launch_bounds__(kThreads) gather_fp8_ds_mla_kernel(const Gathe
       o[2 * i] = pack_bf16x2(__fmul_rn(v0.x, s[k]), __fmul_rn(v0.y, s[k]));
       o[2 * i + 1] = pack_bf16x2(__fmul_rn(v1.x, s[k]), __fmul_rn(v1.y, s[k]));
     }
-    __nv_bfloat16* out = dst + (w0 + r) * a.dst_stride + 16 * lane;
+    __nv_bfloat16* out = dst + (w0 + k) * a.dst_stride + 16 * lane;
     st16(out, make_uint4(o[0], o[1], o[2], o[3]));
     st16(out + 8, make_uint4(o[4], o[5], o[6], o[7]));
   }
-
-  // RoPE: bf16 bits copied, 8 pieces of 16 bytes per row.
 #pragma unroll
   for (int k = 0; k < kRopeItems; ++k) {
-    const int item = threadIdx.x + kThreads * k;
-    const int r = item >> 3, piece = item & 7;
-    const int64_t off = s_off[r];
-    if (off < 0) continue;
-    st16(dst + (w0 + r) * a.dst_stride + kNopeDim + 8 * piece,
-         ld_stream16(a.cache + off + kF8RopeOff + 16 * piece));
+    if (roff[k] < 0) continue;
+    const int r = (lane >> 3) + 4 * k;
+    st16(dst + (w0 + r) * a.dst_stride + kNopeDim + 8 * (lane & 7), rp[k]);
   }
 }
 

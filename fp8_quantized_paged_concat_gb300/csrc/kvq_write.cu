@@ -17,13 +17,13 @@ namespace {
 
 // Launch shape (compile-time tuning knobs; the defaults are the measured best).
 #ifndef KVQ_WRITE_WARPS_PER_BLOCK
-#define KVQ_WRITE_WARPS_PER_BLOCK 8
+#define KVQ_WRITE_WARPS_PER_BLOCK 4
 #endif
 #ifndef KVQ_WRITE_TOKENS_PER_WARP
 #define KVQ_WRITE_TOKENS_PER_WARP 4
 #endif
 #ifndef KVQ_WRITE_MIN_BLOCKS
-#define KVQ_WRITE_MIN_BLOCKS 1
+#define KVQ_WRITE_MIN_BLOCKS 8
 #endif
 constexpr int kWarpsPerBlock = KVQ_WRITE_WARPS_PER_BLOCK;
 constexpr int kTokensPerWarp = KVQ_WRITE_TOKENS_PER_WARP;
