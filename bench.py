@@ -514,7 +514,9 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "bytes_per_step": bytes_step,
+        "config": {"workload": WORKLOAD if args.size == "full" else "profiling case (--size small): " +
+                   "nvfp4 fill 4096x64, nvfp4 gather 8 req U[4k,16k], fp8 gather 4x16384, per-head as full",
+                   "bytes_per_step": bytes_step,
                    "l2": "no flush: every step moves ~7.8 GB, inputs exceed the 129 MB L2"},
         "frac_of_peak": round(value / world / peak, 4),
         "tokens_per_s": round(world * step.tokens_per_step() / (ms_per_step * 1e-3), 1),

@@ -23,10 +23,10 @@ namespace {
 #define KVQ_GATHER_WARPS_PER_BLOCK 4
 #endif
 #ifndef KVQ_GATHER_ROWS_PER_WARP
-#define KVQ_GATHER_ROWS_PER_WARP 8
+#define KVQ_GATHER_ROWS_PER_WARP 4
 #endif
 #ifndef KVQ_GATHER_MIN_BLOCKS
-#define KVQ_GATHER_MIN_BLOCKS 8
+#define KVQ_GATHER_MIN_BLOCKS 12
 #endif
 constexpr int kWarps = KVQ_GATHER_WARPS_PER_BLOCK;
 constexpr int kThreads = kWarps * 32;
