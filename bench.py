@@ -172,7 +172,6 @@ def committed_traffic():
     """DRAM bytes per unit of work per kernel from the committed ncu summary
     (profiles/dram_traffic.txt), keyed by the source hash of the kernel file;
     a kernel whose source changed since the capture gets None."""
-    import hashlib
     out = {}
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
@@ -181,13 +180,24 @@ def committed_traffic():
         if line.startswith("#") or "=" not in line:
             continue
         kv = dict(item.split("=", 1) for item in line.split())
-        src = os.path.join(ROOT, "fp8_quantized_paged_concat_gb300", "csrc", kv.get("source", ""))
-        if not os.path.exists(src):
-            continue
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:12]
-        if sha == kv.get("source_sha"):
+        if kernel_source_sha(kv.get("source", "")) == kv.get("source_sha"):
             out[kv["kernel"]] = float(kv["dram_bytes_per_unit"])
     return out
+
+
+def kernel_source_sha(source: str):
+    """12-hex-digit sha256 of a kernel file together with the headers it
+    includes (kvq_device.cuh, kvq_launch.h, include/kvq.h), or None."""
+    import hashlib
+    csrc = os.path.join(ROOT, "fp8_quantized_paged_concat_gb300", "csrc")
+    paths = [os.path.join(csrc, source), os.path.join(csrc, "kvq_device.cuh"),
+             os.path.join(csrc, "kvq_launch.h"), os.path.join(ROOT, "include", "kvq.h")]
+    if not source or not all(os.path.exists(q) for q in paths):
+        return None
+    h = hashlib.sha256()
+    for q in paths:
+        h.update(open(q, "rb").read())
+    return h.hexdigest()[:12]
 
 
 # --------------------------------------------------------------------------
