@@ -334,8 +334,27 @@ def time_extra(step: GpuStep, reps: int = 10):
     cache2 = torch.zeros((d.num_blocks, d.block_size, 352), dtype=torch.uint8, device=step.device)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=step.device)
     f4 = step.g4.fill
+    # per-head read-back of the step's per-head cache at the step's slots
+    ph = step.ph
+    ko, vo = torch.empty_like(ph.key), torch.empty_like(ph.value)
+    T, H, D = ph.key.shape
+    # sparse-decode index conversion: 4096 decode tokens x 2048 positions over
+    # 64 requests of 4k-32k tokens (synthetic sizes), 10 % unused entries
+    g = np.random.Generator(np.random.PCG64(4001))
+    lens = g.integers(4096, 32768, 64, endpoint=True)
+    table, _, _, _ = wl.make_gather_batch(65536, 64, lens, [0] * 64, 4001)
+    req = g.integers(0, 64, 4096).astype(np.int32)
+    idx = (g.random((4096, 2048)) * lens[req][:, None]).astype(np.int32)
+    idx[g.random((4096, 2048)) < 0.1] = -1
+    req_d, idx_d, table_d = (torch.from_numpy(x).to(step.device) for x in (req, idx, table))
+    slots_d = torch.empty_like(idx_d)
     out = {}
     for name, fn, units, nbytes, flush_l2 in (
+            ("dequant_nvfp4_per_head T=16384 H=8 D=128", lambda: kvq.kvq_dequant_nvfp4_per_head(
+                step.phc, ph.slot_mapping, step.ks, step.vs, ko, vo), T,
+             per_head_bytes_per_token(H, D) * T, True),
+            ("req_index_to_global_slot 4096 x 2048", lambda: kvq.kvq_req_index_to_global_slot(
+                req_d, idx_d, table_d, 64, 65536, out=slots_d), idx.size, 8 * idx.size + 4 * 4096, True),
             ("write_nvfp4_ds_mla decode T=8192", lambda: kvq.kvq_write_nvfp4_ds_mla(
                 d.kv_c, d.k_pe, cache2, d.slot_mapping), d.num_tokens,
              BYTES_WRITE_NVFP4 * int((d.slot_mapping >= 0).sum()) + 8 * int((d.slot_mapping < 0).sum()), True),

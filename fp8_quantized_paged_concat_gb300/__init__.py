@@ -20,6 +20,7 @@ import torch
 __all__ = [
     "kvq_write_nvfp4_ds_mla", "kvq_write_fp8_ds_mla", "kvq_gather_upconvert_nvfp4_ds_mla",
     "kvq_gather_upconvert_fp8_ds_mla", "kvq_reshape_and_cache_nvfp4", "kvq_selftest_convert",
+    "kvq_dequant_nvfp4_per_head", "kvq_req_index_to_global_slot",
     "kvq_last_error_string", "kvq_version", "library_path", "load_library",
     "NVFP4_DS_MLA_ENTRY_BYTES", "FP8_DS_MLA_ENTRY_BYTES", "STATUS_BAD_INDEX", "STATUS_BAD_BATCH",
     "nvfp4_full_dim",
@@ -48,6 +49,10 @@ _SIGNATURES = {
     "kvq_reshape_and_cache_nvfp4": [_P, _P, _I64, _I64, _I64, _I64, _P, _I64, _I32, _I32, _P, _I64,
                                     _I32, _P, _P, _P, _P],
     "kvq_selftest_convert": [_U32, _I64, _P, _P, _P, _P, _P, _P],
+    "kvq_dequant_nvfp4_per_head": [_P, _I64, _I32, _I32, _I32, _P, _I64, _P, _P, _P, _I64, _I64, _P,
+                                   _I64, _I64, _P, _P],
+    "kvq_req_index_to_global_slot": [_P, _I64, _P, _I64, _I32, _I64, _P, _I64, _I32, _I32, _I32, _I64,
+                                     _P, _I64, _P, _P],
 }
 
 
@@ -192,10 +197,7 @@ def kvq_reshape_and_cache_nvfp4(key, value, kv_cache, slot_mapping, k_scale, v_s
               f"{name}: expected a CUDA bf16 [T, H, D] tensor with unit inner stride")
     _need(key.shape == value.shape, "key and value shapes differ")
     T, H, D = key.shape
-    _need(kv_cache.dtype == torch.uint8 and kv_cache.is_cuda and kv_cache.dim() == 5
-          and kv_cache.is_contiguous() and kv_cache.shape[1] == 2 and kv_cache.shape[3] == H
-          and kv_cache.shape[4] == nvfp4_full_dim(D),
-          "kv_cache: expected a contiguous CUDA uint8 [P, 2, block_size, H, D/2 + D/16] tensor")
+    _per_head_cache(kv_cache, H, D)
     _need(slot_mapping.dtype == torch.int64 and slot_mapping.is_cuda and slot_mapping.is_contiguous()
           and slot_mapping.shape[0] == T, "slot_mapping: expected a contiguous CUDA int64 [T]")
     for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
@@ -204,6 +206,55 @@ def kvq_reshape_and_cache_nvfp4(key, value, kv_cache, slot_mapping, k_scale, v_s
           key.stride(1), value.stride(0), value.stride(1), slot_mapping.data_ptr(), T, H, D,
           kv_cache.data_ptr(), kv_cache.shape[0], kv_cache.shape[2], k_scale.data_ptr(),
           v_scale.data_ptr(), _status_ptr(status), _stream(stream, kv_cache.device))
+
+
+def _per_head_cache(kv_cache, H, D):
+    _need(kv_cache.dtype == torch.uint8 and kv_cache.is_cuda and kv_cache.dim() == 5
+          and kv_cache.is_contiguous() and kv_cache.shape[1] == 2 and kv_cache.shape[3] == H
+          and kv_cache.shape[4] == nvfp4_full_dim(D),
+          "kv_cache: expected a contiguous CUDA uint8 [P, 2, block_size, H, D/2 + D/16] tensor")
+
+
+def kvq_dequant_nvfp4_per_head(kv_cache, slot_mapping, k_scale, v_scale, key_out, value_out,
+                               status=None, stream=None):
+    """Reads the per-head NVFP4 cache back at slot_mapping into key_out /
+    value_out bf16 [T, H, D] (rows of padding slots are left untouched)."""
+    for name, t in (("key_out", key_out), ("value_out", value_out)):
+        _need(t.dtype == torch.bfloat16 and t.is_cuda and t.dim() == 3 and t.stride(2) == 1,
+              f"{name}: expected a CUDA bf16 [T, H, D] tensor with unit inner stride")
+    _need(key_out.shape == value_out.shape, "key_out and value_out shapes differ")
+    T, H, D = key_out.shape
+    _per_head_cache(kv_cache, H, D)
+    _need(slot_mapping.dtype == torch.int64 and slot_mapping.is_cuda and slot_mapping.is_contiguous()
+          and slot_mapping.shape[0] == T, "slot_mapping: expected a contiguous CUDA int64 [T]")
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        _need(t.dtype == torch.float32 and t.is_cuda and t.numel() >= 1, f"{name}: CUDA fp32 scalar")
+    _call("kvq_dequant_nvfp4_per_head", kv_cache.data_ptr(), kv_cache.shape[0], kv_cache.shape[2], H, D,
+          slot_mapping.data_ptr(), T, k_scale.data_ptr(), v_scale.data_ptr(), key_out.data_ptr(),
+          key_out.stride(0), key_out.stride(1), value_out.data_ptr(), value_out.stride(0),
+          value_out.stride(1), _status_ptr(status), _stream(stream, kv_cache.device))
+
+
+def kvq_req_index_to_global_slot(req_id, token_indices, block_table, block_size: int, num_blocks: int,
+                                 out=None, status=None, stream=None):
+    """Sparse-decode index conversion: int32 token_indices [N, topk] of
+    requests req_id [N] -> global slots int32 [N, topk] (-1 where unused).
+    Raises RuntimeError when req_id and token_indices lengths differ."""
+    for name, t in (("req_id", req_id), ("token_indices", token_indices), ("block_table", block_table)):
+        _need(t.dtype == torch.int32 and t.is_cuda, f"{name}: expected a CUDA int32 tensor")
+    _need(req_id.dim() == 1 and req_id.is_contiguous(), "req_id: expected a contiguous vector")
+    _need(token_indices.dim() == 2 and token_indices.stride(1) == 1, "token_indices: expected [N, topk] rows")
+    _need(block_table.dim() == 2 and block_table.stride(1) == 1, "block_table: expected [R, W] rows")
+    N, topk = token_indices.shape
+    if out is None:
+        out = torch.empty((N, topk), dtype=torch.int32, device=token_indices.device)
+    _need(out.dtype == torch.int32 and out.is_cuda and out.dim() == 2 and out.stride(1) == 1
+          and tuple(out.shape) == (N, topk), "out: expected a CUDA int32 [N, topk] tensor")
+    _call("kvq_req_index_to_global_slot", req_id.data_ptr(), req_id.shape[0], token_indices.data_ptr(),
+          N, topk, token_indices.stride(0), block_table.data_ptr(), block_table.stride(0),
+          block_table.shape[1], block_table.shape[0], block_size, num_blocks, out.data_ptr(),
+          out.stride(0), _status_ptr(status), _stream(stream, token_indices.device))
+    return out
 
 
 def kvq_selftest_convert(first_bits: int, count: int, device="cuda", stream=None):

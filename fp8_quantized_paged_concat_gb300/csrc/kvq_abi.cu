@@ -141,6 +141,55 @@ kvq_status gather_common(const char* fn, int64_t entry_bytes,
   return launched(fn, launch(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+kvq_status per_head_common(const char* fn, bool read_back,
+                           cudaError_t (*launch)(const kvq::PerHeadArgs&, cudaStream_t),
+                           const void* key, const void* value, int64_t key_stride_t,
+                           int64_t key_stride_h, int64_t value_stride_t, int64_t value_stride_h,
+                           const int64_t* slot_mapping, int64_t num_tokens, int32_t num_heads,
+                           int32_t head_size, const uint8_t* kv_cache, int64_t num_pages,
+                           int32_t block_size, const float* k_scale, const float* v_scale,
+                           int32_t* d_status, kvq_stream_t stream) {
+  KVQ_REQUIRE(num_tokens >= 0, "%s: num_tokens < 0", fn);
+  if (num_tokens == 0) return ok();
+  KVQ_REQUIRE(num_heads > 0 && head_size >= 16 && head_size % 16 == 0,
+              "%s: need num_heads > 0 and head_size a positive multiple of 16", fn);
+  KVQ_REQUIRE(num_tokens * 2 * num_heads * (head_size / 16) < (int64_t{1} << 32) - 256,
+              "%s: num_tokens * 2 * num_heads * head_size / 16 must stay below 2^32 - 256", fn);
+  KVQ_REQUIRE(key != nullptr && value != nullptr, "%s: key / value is NULL", fn);
+  KVQ_REQUIRE(aligned(key, 16) && aligned(value, 16), "%s: key / value must be 16-byte aligned", fn);
+  KVQ_REQUIRE(key_stride_t % 8 == 0 && key_stride_h % 8 == 0 && value_stride_t % 8 == 0 &&
+                  value_stride_h % 8 == 0 && key_stride_t >= 0 && key_stride_h >= 0 &&
+                  value_stride_t >= 0 && value_stride_h >= 0,
+              "%s: key / value strides must be non-negative multiples of 8 elements", fn);
+  if (read_back)
+    KVQ_REQUIRE(key_stride_h >= head_size && key_stride_t >= num_heads * key_stride_h &&
+                    value_stride_h >= head_size && value_stride_t >= num_heads * value_stride_h,
+                "%s: output strides must not overlap rows", fn);
+  KVQ_REQUIRE(slot_mapping != nullptr && aligned(slot_mapping, 8), "%s: bad slot_mapping", fn);
+  KVQ_REQUIRE(k_scale != nullptr && v_scale != nullptr && aligned(k_scale, 4) && aligned(v_scale, 4),
+              "%s: k_scale / v_scale must be device fp32 scalars", fn);
+  KVQ_REQUIRE(kv_cache != nullptr && aligned(kv_cache, 16), "%s: kv_cache must be 16-byte aligned", fn);
+  KVQ_REQUIRE(num_pages > 0 && block_size > 0, "%s: num_pages and block_size must be positive", fn);
+  KVQ_REQUIRE(num_pages <= (int64_t{1} << 32) / block_size,
+              "%s: num_pages * block_size must not exceed 2^32 slots", fn);
+  const int64_t full_dim = head_size / 2 + head_size / 16;
+  KVQ_REQUIRE((int64_t{block_size} * num_heads * full_dim) % 8 == 0 &&
+                  (int64_t{block_size} * num_heads * (head_size / 2)) % 8 == 0,
+              "%s: block_size * num_heads * full_dim must be a multiple of 8", fn);
+  KVQ_REQUIRE(d_status == nullptr || aligned(d_status, 4), "%s: d_status misaligned", fn);
+  if (kvq_status s = check_device(fn)) return s;
+  const int32_t groups = head_size / 16;
+  const kvq::PerHeadArgs a{key,          value,     key_stride_t, key_stride_h, value_stride_t,
+                           value_stride_h, slot_mapping, num_tokens, num_heads, head_size,
+                           const_cast<uint8_t*>(kv_cache), num_pages * block_size, block_size,
+                           k_scale, v_scale, d_status,
+                           kvq::FastDiv::make(static_cast<uint32_t>(block_size)),
+                           kvq::FastDiv::make(static_cast<uint32_t>(2 * num_heads * groups)),
+                           kvq::FastDiv::make(static_cast<uint32_t>(num_heads * groups)),
+                           kvq::FastDiv::make(static_cast<uint32_t>(groups))};
+  return launched(fn, launch(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -200,42 +249,59 @@ kvq_status kvq_reshape_and_cache_nvfp4(const void* key, const void* value, int64
                                        uint8_t* kv_cache, int64_t num_pages, int32_t block_size,
                                        const float* k_scale, const float* v_scale,
                                        int32_t* d_status, kvq_stream_t stream) {
-  const char* fn = "kvq_reshape_and_cache_nvfp4";
-  KVQ_REQUIRE(num_tokens >= 0, "%s: num_tokens < 0", fn);
-  if (num_tokens == 0) return ok();
-  KVQ_REQUIRE(num_heads > 0 && head_size >= 16 && head_size % 16 == 0,
-              "%s: need num_heads > 0 and head_size a positive multiple of 16", fn);
-  KVQ_REQUIRE(num_tokens * 2 * num_heads * (head_size / 16) < (int64_t{1} << 32) - 256,
-              "%s: num_tokens * 2 * num_heads * head_size / 16 must stay below 2^32 - 256", fn);
-  KVQ_REQUIRE(key != nullptr && value != nullptr, "%s: key / value is NULL", fn);
-  KVQ_REQUIRE(aligned(key, 16) && aligned(value, 16), "%s: key / value must be 16-byte aligned", fn);
-  KVQ_REQUIRE(key_stride_t % 8 == 0 && key_stride_h % 8 == 0 && value_stride_t % 8 == 0 &&
-                  value_stride_h % 8 == 0 && key_stride_t >= 0 && key_stride_h >= 0 &&
-                  value_stride_t >= 0 && value_stride_h >= 0,
-              "%s: key / value strides must be non-negative multiples of 8 elements", fn);
-  KVQ_REQUIRE(slot_mapping != nullptr && aligned(slot_mapping, 8), "%s: bad slot_mapping", fn);
-  KVQ_REQUIRE(k_scale != nullptr && v_scale != nullptr && aligned(k_scale, 4) && aligned(v_scale, 4),
-              "%s: k_scale / v_scale must be device fp32 scalars", fn);
-  KVQ_REQUIRE(kv_cache != nullptr && aligned(kv_cache, 16), "%s: kv_cache must be 16-byte aligned", fn);
-  KVQ_REQUIRE(num_pages > 0 && block_size > 0, "%s: num_pages and block_size must be positive", fn);
-  KVQ_REQUIRE(num_pages <= (int64_t{1} << 32) / block_size,
-              "%s: num_pages * block_size must not exceed 2^32 slots", fn);
-  const int64_t full_dim = head_size / 2 + head_size / 16;
-  KVQ_REQUIRE((int64_t{block_size} * num_heads * full_dim) % 8 == 0 &&
-                  (int64_t{block_size} * num_heads * (head_size / 2)) % 8 == 0,
-              "%s: block_size * num_heads * full_dim must be a multiple of 8", fn);
+  return per_head_common("kvq_reshape_and_cache_nvfp4", false, kvq::launch_reshape_and_cache_nvfp4,
+                         key, value, key_stride_t, key_stride_h, value_stride_t, value_stride_h,
+                         slot_mapping, num_tokens, num_heads, head_size, kv_cache, num_pages,
+                         block_size, k_scale, v_scale, d_status, stream);
+}
+
+kvq_status kvq_dequant_nvfp4_per_head(const uint8_t* kv_cache, int64_t num_pages,
+                                      int32_t block_size, int32_t num_heads, int32_t head_size,
+                                      const int64_t* slot_mapping, int64_t num_tokens,
+                                      const float* k_scale, const float* v_scale, void* key_out,
+                                      int64_t key_stride_t, int64_t key_stride_h, void* value_out,
+                                      int64_t value_stride_t, int64_t value_stride_h,
+                                      int32_t* d_status, kvq_stream_t stream) {
+  return per_head_common("kvq_dequant_nvfp4_per_head", true, kvq::launch_dequant_nvfp4_per_head,
+                         key_out, value_out, key_stride_t, key_stride_h, value_stride_t,
+                         value_stride_h, slot_mapping, num_tokens, num_heads, head_size, kv_cache,
+                         num_pages, block_size, k_scale, v_scale, d_status, stream);
+}
+
+kvq_status kvq_req_index_to_global_slot(const int32_t* req_id, int64_t num_req_ids,
+                                        const int32_t* token_indices, int64_t num_tokens,
+                                        int32_t topk, int64_t token_indices_stride,
+                                        const int32_t* block_table, int64_t block_table_stride,
+                                        int32_t block_table_width, int32_t num_requests,
+                                        int32_t block_size, int64_t num_blocks, int32_t* out,
+                                        int64_t out_stride, int32_t* d_status,
+                                        kvq_stream_t stream) {
+  const char* fn = "kvq_req_index_to_global_slot";
+  KVQ_REQUIRE(num_tokens >= 0 && topk >= 0, "%s: num_tokens / topk < 0", fn);
+  KVQ_REQUIRE(num_req_ids == num_tokens,
+              "%s: req_id has %lld entries but token_indices has %lld rows", fn,
+              static_cast<long long>(num_req_ids), static_cast<long long>(num_tokens));
+  if (num_tokens == 0 || topk == 0) return ok();
+  KVQ_REQUIRE(num_tokens * topk < (int64_t{1} << 32) - 256, "%s: num_tokens * topk too large", fn);
+  KVQ_REQUIRE(req_id != nullptr && token_indices != nullptr && out != nullptr && block_table != nullptr,
+              "%s: req_id, token_indices, block_table and out must be non-NULL", fn);
+  KVQ_REQUIRE(aligned(req_id, 4) && aligned(token_indices, 4) && aligned(out, 4) && aligned(block_table, 4),
+              "%s: int32 arrays must be 4-byte aligned", fn);
+  KVQ_REQUIRE(token_indices_stride >= topk && out_stride >= topk,
+              "%s: row strides must be >= topk", fn);
+  KVQ_REQUIRE(num_requests > 0 && block_table_width > 0 && block_table_stride >= block_table_width,
+              "%s: need num_requests > 0, block_table_width > 0, stride >= width", fn);
+  KVQ_REQUIRE(block_size > 0 && num_blocks > 0 && num_blocks <= INT32_MAX / block_size,
+              "%s: num_blocks * block_size must fit an int32 slot", fn);
   KVQ_REQUIRE(d_status == nullptr || aligned(d_status, 4), "%s: d_status misaligned", fn);
   if (kvq_status s = check_device(fn)) return s;
-  const int32_t groups = head_size / 16;
-  const kvq::PerHeadArgs a{key,          value,     key_stride_t, key_stride_h, value_stride_t,
-                           value_stride_h, slot_mapping, num_tokens, num_heads, head_size,
-                           kv_cache,     num_pages * block_size, block_size, k_scale, v_scale,
-                           d_status,
-                           kvq::FastDiv::make(static_cast<uint32_t>(block_size)),
-                           kvq::FastDiv::make(static_cast<uint32_t>(2 * num_heads * groups)),
-                           kvq::FastDiv::make(static_cast<uint32_t>(num_heads * groups)),
-                           kvq::FastDiv::make(static_cast<uint32_t>(groups))};
-  return launched(fn, kvq::launch_reshape_and_cache_nvfp4(a, reinterpret_cast<cudaStream_t>(stream)));
+  const kvq::IndexArgs a{req_id,        token_indices, token_indices_stride, num_tokens,
+                         topk,          block_table,   block_table_stride,   block_table_width,
+                         num_requests,  block_size,    num_blocks,           out,
+                         out_stride,    d_status,
+                         kvq::FastDiv::make(static_cast<uint32_t>(block_size)),
+                         kvq::FastDiv::make(static_cast<uint32_t>(topk))};
+  return launched(fn, kvq::launch_req_index_to_global_slot(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kvq_status kvq_selftest_convert(uint32_t first_bits, int64_t count, uint8_t* e4m3_lo,

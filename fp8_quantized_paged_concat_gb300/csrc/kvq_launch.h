@@ -70,6 +70,28 @@ cudaError_t launch_write_fp8_ds_mla(const WriteArgs& a, cudaStream_t stream);
 cudaError_t launch_gather_nvfp4_ds_mla(const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_gather_fp8_ds_mla(const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_reshape_and_cache_nvfp4(const PerHeadArgs& a, cudaStream_t stream);
+// Read-back: key / value are the bf16 OUTPUTS (written through const_cast).
+cudaError_t launch_dequant_nvfp4_per_head(const PerHeadArgs& a, cudaStream_t stream);
+
+struct IndexArgs {
+  const int32_t* req_id;
+  const int32_t* token_indices;
+  int64_t token_indices_stride;   // elements between rows
+  int64_t num_tokens;
+  int32_t topk;
+  const int32_t* block_table;
+  int64_t block_table_stride;
+  int32_t block_table_width;
+  int32_t num_requests;
+  int32_t block_size;
+  int64_t num_blocks;
+  int32_t* out;
+  int64_t out_stride;
+  int32_t* status;
+  FastDiv block_div;              // position -> table column
+  FastDiv topk_div;               // flat index -> token
+};
+cudaError_t launch_req_index_to_global_slot(const IndexArgs& a, cudaStream_t stream);
 cudaError_t launch_selftest_convert(uint32_t first_bits, int64_t count, uint8_t* e4m3_lo,
                                     uint8_t* e4m3_hi, uint8_t* e2m1_lo, uint8_t* e2m1_hi,
                                     uint16_t* bf16_out, int num_sms, cudaStream_t stream);

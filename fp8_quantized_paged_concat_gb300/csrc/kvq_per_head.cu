@@ -1,4 +1,4 @@
-// kvq_per_head.cu -- reshape_and_cache into the per-head NVFP4 K/V cache
+// kvq_per_head.cu -- reshape_and_cache into (and read-back out of) the per-head NVFP4 K/V cache
 // [num_pages, 2, block_size, H, full_dim] whose side regions hold
 // [data [block_size][H][D/2] | scales [block_size][H][D/16]].
 //
@@ -65,7 +65,60 @@ __global__ void __launch_bounds__(kThreads) reshape_and_cache_nvfp4_kernel(const
       static_cast<uint8_t>(sf);
 }
 
+// Read-back: the same thread-per-group decomposition; each thread reads its
+// group's 8 data bytes and scale byte and writes 16 bf16 values
+// bf16_rn((e2m1 * sf) * scale) -- the first product exact, one fp32 rounding
+// for the per-tensor scale, one bf16 rounding.
+__global__ void __launch_bounds__(kThreads) dequant_nvfp4_per_head_kernel(const PerHeadArgs a) {
+  const uint32_t idx = blockIdx.x * kThreads + threadIdx.x;
+  const uint32_t t = a.unit_div.div(idx);
+  if (t >= a.num_tokens) return;
+  const uint32_t u = idx - t * a.unit_div.d;
+  const uint32_t side = a.side_div.div(u);
+  const uint32_t r = u - side * a.side_div.d;
+  const uint32_t h = a.head_div.div(r);
+  const uint32_t g = r - h * a.head_div.d;
+
+  const int64_t slot = __ldg(a.slot_mapping + t);
+  if (slot < 0) return;
+  if (slot >= a.num_slots) {
+    if (side == 0 && h == 0 && g == 0) report(a.status, KVQ_STATUS_BAD_INDEX);
+    return;
+  }
+  const uint32_t page = a.block_div.div(static_cast<uint32_t>(slot));
+  const uint32_t off = static_cast<uint32_t>(slot) - page * static_cast<uint32_t>(a.block_size);
+  const int64_t data_dim = a.head_size / 2;
+  const int64_t scale_dim = a.head_size / kGroup;
+  const int64_t region = static_cast<int64_t>(a.block_size) * a.num_heads * (data_dim + scale_dim);
+  const uint8_t* base = a.cache + (static_cast<int64_t>(page) * 2 + side) * region;
+  const int64_t row = static_cast<int64_t>(off) * a.num_heads + h;
+  const uint2 q = ld_stream8(base + row * data_dim + 8 * g);
+  const float sf = e4m3_to_float(
+      ld_byte(base + static_cast<int64_t>(a.block_size) * a.num_heads * data_dim + row * scale_dim + g));
+  const float scale = __ldg(side ? a.v_scale : a.k_scale);
+
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t byte = (i < 4 ? q.x : q.y) >> (8 * (i & 3));
+    const float2 v = __half22float2(e2m1x2_to_half2(byte));
+    o[i] = pack_bf16x2(__fmul_rn(v.x * sf, scale), __fmul_rn(v.y * sf, scale));
+  }
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(const_cast<void*>(side ? a.value : a.key)) +
+                       static_cast<int64_t>(t) * (side ? a.value_stride_t : a.key_stride_t) +
+                       static_cast<int64_t>(h) * (side ? a.value_stride_h : a.key_stride_h) + g * kGroup;
+  st16(dst, make_uint4(o[0], o[1], o[2], o[3]));
+  st16(dst + 8, make_uint4(o[4], o[5], o[6], o[7]));
+}
+
 }  // namespace
+
+cudaError_t launch_dequant_nvfp4_per_head(const PerHeadArgs& a, cudaStream_t stream) {
+  const int64_t threads = a.num_tokens * 2 * a.num_heads * (a.head_size / kGroup);
+  const int64_t blocks = (threads + kThreads - 1) / kThreads;
+  dequant_nvfp4_per_head_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_reshape_and_cache_nvfp4(const PerHeadArgs& a, cudaStream_t stream) {
   const int64_t threads = a.num_tokens * 2 * a.num_heads * (a.head_size / kGroup);

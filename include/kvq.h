@@ -192,6 +192,50 @@ kvq_status kvq_reshape_and_cache_nvfp4(
     int32_t* d_status, kvq_stream_t stream);
 
 /*
+ * kvq_dequant_nvfp4_per_head -- reads the per-head NVFP4 cache back into bf16
+ * (the GPU counterpart of [P2] "Implementation breakdown" item 5,
+ * dequant_nvfp4_kv_cache; the decode consumer [P2] leaves unimplemented).
+ * For each token t with slot s = slot_mapping[t] >= 0 (in range), every
+ * 16-value group of head h and side (K -> key_out, V -> value_out) becomes
+ * bf16_rn((e2m1 * sf) * scale): the first product exact, one fp32 rounding
+ * for the per-tensor scale (*k_scale / *v_scale).  Rows of padding and
+ * out-of-range slots are not written.  Cache layout and argument rules as in
+ * kvq_reshape_and_cache_nvfp4; key_out / value_out are bf16 [num_tokens,
+ * num_heads, head_size] outputs with token and head strides in elements.
+ */
+kvq_status kvq_dequant_nvfp4_per_head(
+    const uint8_t* kv_cache, int64_t num_pages, int32_t block_size,
+    int32_t num_heads, int32_t head_size,
+    const int64_t* slot_mapping, int64_t num_tokens,
+    const float* k_scale, const float* v_scale,
+    void* key_out, int64_t key_stride_t, int64_t key_stride_h,
+    void* value_out, int64_t value_stride_t, int64_t value_stride_h,
+    int32_t* d_status, kvq_stream_t stream);
+
+/*
+ * kvq_req_index_to_global_slot -- sparse-decode index conversion feeding the
+ * sparse MLA decode ([P3] "Implementation breakdown" item 1:
+ * triton_convert_req_index_to_global_index and its length check).  For decode
+ * token i < num_tokens of request r = req_id[i] and each k < topk, position
+ * p = token_indices[i * token_indices_stride + k] becomes
+ * out[i * out_stride + k] = block_table[r][p / block_size] * block_size +
+ * p % block_size, or -1 when p < 0 (an unused top-k entry).  An out-of-range
+ * request, column or block id also gives -1 and sets KVQ_STATUS_BAD_INDEX.
+ * As on the page, a call whose req_id length (num_req_ids) differs from the
+ * number of token_indices rows (num_tokens) is rejected with
+ * KVQ_ERR_INVALID_ARG before anything is launched.  All arrays int32;
+ * num_blocks * block_size must fit an int32 slot.
+ */
+kvq_status kvq_req_index_to_global_slot(
+    const int32_t* req_id, int64_t num_req_ids,
+    const int32_t* token_indices, int64_t num_tokens, int32_t topk,
+    int64_t token_indices_stride,
+    const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width,
+    int32_t num_requests, int32_t block_size, int64_t num_blocks,
+    int32_t* out, int64_t out_stride,
+    int32_t* d_status, kvq_stream_t stream);
+
+/*
  * kvq_selftest_convert -- exposes the device number-format converters the
  * kernels above use, for exhaustive testing.  For i < count and f the float
  * whose bit pattern is first_bits + i (mod 2^32):

@@ -170,3 +170,52 @@ def test_valid_arguments_without_a_gpu_report_a_cuda_error(lib):
     """With no device the call fails cleanly at the device query."""
     assert lib.kvq_write_nvfp4_ds_mla(*write_args()) == 3
     assert "kvq_write_nvfp4_ds_mla" in err(lib)
+
+
+def index_args(**over):
+    args = dict(req_id=A, num_req_ids=10, token_indices=A, num_tokens=10, topk=8, ti_stride=8,
+                block_table=A, bt_stride=4, bt_width=4, num_requests=2, block_size=16,
+                num_blocks=64, out=A, out_stride=8, d_status=None, stream=None)
+    args.update(over)
+    return list(args.values())
+
+
+@no_gpu_only
+@pytest.mark.parametrize("over,needle", [
+    (dict(num_req_ids=11), "req_id has 11 entries but token_indices has 10 rows"),
+    (dict(num_req_ids=9), "req_id has 9 entries"),
+    (dict(topk=-1), "< 0"),
+    (dict(out=None), "non-NULL"),
+    (dict(ti_stride=4), "row strides"),
+    (dict(num_requests=0), "num_requests"),
+    (dict(num_blocks=1 << 30, block_size=16), "int32 slot"),
+])
+def test_index_conversion_rejects_bad_arguments_on_host(lib, over, needle):
+    assert lib.kvq_req_index_to_global_slot(*index_args(**over)) == 1
+    assert needle in err(lib), err(lib)
+
+
+@no_gpu_only
+def test_index_conversion_zero_sized_is_noop(lib):
+    assert lib.kvq_req_index_to_global_slot(*index_args(num_tokens=0, num_req_ids=0, req_id=None)) == 0
+
+
+def dequant_args(**over):
+    args = dict(kv_cache=A, num_pages=4, block_size=16, num_heads=8, head_size=128, slot_mapping=A,
+                num_tokens=8, k_scale=A, v_scale=A, key_out=A, kst=1024, ksh=128, value_out=A,
+                vst=1024, vsh=128, d_status=None, stream=None)
+    args.update(over)
+    return list(args.values())
+
+
+@no_gpu_only
+@pytest.mark.parametrize("over,needle", [
+    (dict(head_size=40), "multiple of 16"),
+    (dict(key_out=None), "NULL"),
+    (dict(ksh=64), "overlap"),
+    (dict(vst=512), "overlap"),
+    (dict(kv_cache=A + 4), "16-byte aligned"),
+])
+def test_dequant_rejects_bad_arguments_on_host(lib, over, needle):
+    assert lib.kvq_dequant_nvfp4_per_head(*dequant_args(**over)) == 1
+    assert needle in err(lib), err(lib)

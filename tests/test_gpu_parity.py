@@ -385,3 +385,108 @@ def test_per_head_out_of_range_slots(kvq, oracle_mod):
 
 def test_per_head_full_size(kvq, oracle_mod, threads):
     run_per_head(kvq, oracle_mod, wl.per_head(), threads=threads)
+
+
+# --------------------------------------------------------------------------
+# per-head read-back (next row: the consumer side of the per-head cache)
+# --------------------------------------------------------------------------
+
+def run_dequant(kvq, oracle_mod, w, cache_host, strided=False, status_expected=0, threads=1):
+    T, H, D = w.key.shape
+    if strided:          # outputs as halves of one [T, H, 2D] tensor
+        both = torch.full((T, H, 2 * D), -3.0, dtype=torch.bfloat16, device=DEV)
+        ko, vo = both[:, :, :D], both[:, :, D:]
+    else:
+        ko = torch.full((T, H, D), -3.0, dtype=torch.bfloat16, device=DEV)
+        vo = torch.full((T, H, D), -3.0, dtype=torch.bfloat16, device=DEV)
+    ks = torch.tensor([w.k_scale], dtype=torch.float32, device=DEV)
+    vs = torch.tensor([w.v_scale], dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kvq.kvq_dequant_nvfp4_per_head(dev(cache_host), dev(w.slot_mapping), ks, vs, ko, vo, status=status)
+    guard = wl.bf16_bits(torch.tensor([-3.0], dtype=torch.bfloat16))[0]
+    wk = np.full((T, H, D), guard, np.uint16)
+    wv = np.full((T, H, D), guard, np.uint16)
+    oracle_mod.dequant_nvfp4_per_head(cache_host, wl.host(w.slot_mapping), H, D, w.k_scale, w.v_scale,
+                                      key_out=wk, value_out=wv, threads=threads)
+    assert int(status.item()) == status_expected
+    np.testing.assert_array_equal(wl.bf16_bits(ko), wk)
+    np.testing.assert_array_equal(wl.bf16_bits(vo), wv)
+
+
+@pytest.mark.parametrize("name,make,kw", PER_HEAD_CASES, ids=[c[0] for c in PER_HEAD_CASES])
+def test_dequant_per_head_parity_written_cache(kvq, oracle_mod, name, make, kw):
+    w = make()
+    T, H, D = w.key.shape
+    cache = np.zeros((w.num_pages, 2, w.block_size, H, kvq.nvfp4_full_dim(D)), np.uint8)
+    oracle_mod.reshape_and_cache_nvfp4(wl.bf16_bits(w.key), wl.bf16_bits(w.value), wl.host(w.slot_mapping),
+                                       cache, w.k_scale, w.v_scale)
+    run_dequant(kvq, oracle_mod, w, cache, **kw)
+
+
+def test_dequant_per_head_random_cache_and_bad_slots(kvq, oracle_mod):
+    w = wl.make_per_head("rb", 70, 4, 64, 8, 16, 5, 111, k_scale=0.3, v_scale=7.0)
+    s = wl.host(w.slot_mapping).copy()
+    s[[1, 2]] = [128, 999]
+    w.slot_mapping = torch.from_numpy(s)
+    cache = wl.random_bytes((8, 2, 16, 4, kvq.nvfp4_full_dim(64)), 112)
+    # scale bytes must be finite e4m3: every byte that can be a scale byte
+    wl.nan_free_e4m3_bytes(cache)
+    run_dequant(kvq, oracle_mod, w, cache, status_expected=kvq.STATUS_BAD_INDEX)
+
+
+def test_dequant_per_head_full_size(kvq, oracle_mod, threads):
+    w = wl.per_head()
+    T, H, D = w.key.shape
+    cache = np.zeros((w.num_pages, 2, w.block_size, H, kvq.nvfp4_full_dim(D)), np.uint8)
+    oracle_mod.reshape_and_cache_nvfp4(wl.bf16_bits(w.key), wl.bf16_bits(w.value), wl.host(w.slot_mapping),
+                                       cache, threads=threads)
+    run_dequant(kvq, oracle_mod, w, cache, threads=threads)
+
+
+# --------------------------------------------------------------------------
+# sparse-decode index conversion (next row)
+# --------------------------------------------------------------------------
+
+def index_case(num_req, lens, bs, nb, N, topk, seed, p_unused=0.2):
+    g = np.random.Generator(np.random.PCG64(seed))
+    table, _, _, _ = wl.make_gather_batch(nb, bs, lens, [0] * len(lens), seed)
+    req = g.integers(0, num_req, size=N).astype(np.int32)
+    lens = np.asarray(lens)
+    idx = (g.random((N, topk)) * lens[req][:, None]).astype(np.int32)
+    idx[g.random((N, topk)) < p_unused] = -1
+    return req, idx, table
+
+
+@pytest.mark.parametrize("bs,topk", [(64, 2048), (16, 100), (7, 33), (1, 8)])
+def test_index_conversion_parity(kvq, oracle_mod, bs, topk):
+    req, idx, table = index_case(6, [5000, 1, 300, 2048, 64, 999], bs, 20000, 77, topk, 121 + bs)
+    out = kvq.kvq_req_index_to_global_slot(dev(req), dev(idx), dev(table), bs, 20000)
+    want, skipped = oracle_mod.req_index_to_global_slot(req, idx, table, bs, 20000)
+    assert skipped == 0
+    np.testing.assert_array_equal(out.cpu().numpy(), want)
+
+
+def test_index_conversion_strided_rows_and_bad_entries(kvq, oracle_mod):
+    req, idx, table = index_case(3, [100, 200, 50], 16, 64, 40, 24, 131)
+    req[5] = 7                      # no such request
+    idx[6, 3] = 10 ** 6             # past the block table
+    table = table.copy()
+    table[1, 0] = -1                # unusable block
+    wide = np.full((40, 32), 5, np.int32)
+    wide[:, :24] = idx
+    ti = dev(wide)[:, :24]
+    outbuf = torch.full((40, 30), 99, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kvq.kvq_req_index_to_global_slot(dev(req), ti, dev(table), 16, 64, out=outbuf[:, :24], status=status)
+    want, skipped = oracle_mod.req_index_to_global_slot(req, idx, table, 16, 64)
+    assert skipped > 0 and int(status.item()) == kvq.STATUS_BAD_INDEX
+    got = outbuf.cpu().numpy()
+    np.testing.assert_array_equal(got[:, :24], want)
+    assert np.all(got[:, 24:] == 99)
+
+
+def test_index_conversion_rejects_length_mismatch(kvq):
+    req, idx, table = index_case(2, [10, 10], 16, 8, 12, 4, 141)
+    with pytest.raises(RuntimeError, match="req_id has 13 entries"):
+        kvq.kvq_req_index_to_global_slot(dev(np.concatenate([req, [0]]).astype(np.int32)), dev(idx),
+                                         dev(table), 16, 8)
