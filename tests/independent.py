@@ -59,9 +59,11 @@ def e2m1_encode(x: np.ndarray) -> np.ndarray:
     """Brute-force e2m1 round-to-nearest-even with satfinite (finite x)."""
     x = np.asarray(x, np.float32).ravel()
     mags = e2m1_table()[:8]
-    idx = _nearest_even(x, mags)
-    sign = np.signbit(x).astype(np.uint8) << 3
-    return (idx.astype(np.uint8) | sign)
+    out = np.empty(x.size, np.uint8)
+    for s in range(0, x.size, 1 << 20):      # bound the [n, 8] temporaries
+        xs = x[s:s + (1 << 20)]
+        out[s:s + xs.size] = _nearest_even(xs, mags).astype(np.uint8) | (np.signbit(xs).astype(np.uint8) << 3)
+    return out
 
 
 def e4m3_encode(x: np.ndarray) -> np.ndarray:

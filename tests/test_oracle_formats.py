@@ -44,10 +44,10 @@ def _strided_bits(stride, offset=0):
 
 
 def test_e4m3_encode_matches_torch_cast_strided_sweep(oracle_mod):
-    """Every 61st float32 bit pattern: inside torch's non-saturating range
+    """Every 251st float32 bit pattern: inside torch's non-saturating range
     (|f| < 464) the oracle equals torch's RN-even cast; beyond it the oracle
     saturates to +-448 where torch gives NaN."""
-    bits = _strided_bits(61, 17)
+    bits = _strided_bits(251, 17)
     f = bits.view(np.float32)
     finite = np.isfinite(f)
     ours = oracle_mod.e4m3_rn_sat(f)
@@ -99,11 +99,11 @@ def test_e4m3_encode_bruteforce_random(oracle_mod):
 
 
 def test_e2m1_encode_bruteforce_sweep(oracle_mod):
-    """Every 3rd float32 pattern with |f| in [2^-4, 8), all midpoints +-1 ulp,
+    """Every 13th float32 pattern with |f| in [2^-4, 8), all midpoints +-1 ulp,
     and random magnitudes over a wide range, vs exhaustive search."""
     lo = np.float32(2.0 ** -4).view(np.uint32)
     hi = np.float32(8.0).view(np.uint32)
-    f = np.arange(int(lo), int(hi), 3, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    f = np.arange(int(lo), int(hi), 13, dtype=np.uint64).astype(np.uint32).view(np.float32)
     mags = ind.e2m1_table()[:8]
     g = np.random.Generator(np.random.PCG64(8))
     r = (g.standard_normal(100_000) * np.exp2(g.integers(-30, 30, 100_000))).astype(np.float32)
