@@ -10,6 +10,11 @@
 
 namespace kvq {
 
+// CTAs for a persistent launch: every SM filled to the kernel's occupancy,
+// never more CTAs than there is work for.  The occupancy is queried once per
+// (kernel, device) and cached.
+int persistent_grid(const void* kernel, int threads, int64_t ctas_of_work);
+
 struct WriteArgs {
   const void* kv_c;
   int64_t kv_c_stride;
