@@ -2,7 +2,6 @@
 // host-side validation, device check, launch on the caller's stream, status.
 #include <cstdarg>
 #include <cstdio>
-#include <mutex>
 #include <string>
 
 #include "kvq.h"
@@ -192,35 +191,6 @@ kvq_status per_head_common(const char* fn, bool read_back,
 }
 
 }  // namespace
-
-namespace kvq {
-
-int persistent_grid(const void* kernel, int threads, int64_t ctas_of_work) {
-  struct Entry { const void* kernel; int device; int ctas; };
-  static std::mutex mu;
-  static Entry cache[64];
-  static int used = 0;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  int ctas = 0;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < used; ++i)
-      if (cache[i].kernel == kernel && cache[i].device == dev) ctas = cache[i].ctas;
-    if (ctas == 0) {
-      int sms = 0, per_sm = 0;
-      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess ||
-          per_sm < 1)
-        return 1;
-      ctas = sms * per_sm;
-      if (used < 64) cache[used++] = Entry{kernel, dev, ctas};
-    }
-  }
-  return static_cast<int>(ctas_of_work < ctas ? (ctas_of_work < 1 ? 1 : ctas_of_work) : ctas);
-}
-
-}  // namespace kvq
 
 extern "C" {
 

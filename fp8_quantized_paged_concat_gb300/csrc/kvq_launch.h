@@ -10,10 +10,6 @@
 
 namespace kvq {
 
-// CTAs for a persistent launch: every SM filled to the kernel's occupancy,
-// never more CTAs than there is work for.  The occupancy is queried once per
-// (kernel, device) and cached.
-int persistent_grid(const void* kernel, int threads, int64_t ctas_of_work);
 
 struct WriteArgs {
   const void* kv_c;
