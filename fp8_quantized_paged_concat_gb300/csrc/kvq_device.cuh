@@ -159,6 +159,43 @@ __device__ __forceinline__ uint32_t ld_byte(const uint8_t* p) {
   return __ldg(p);
 }
 
+// 32 contiguous bytes in one access (256-bit vector load / store, sm_100 and
+// later); the address must be 32-byte aligned.  A lane that moves 32 bytes as
+// two 16-byte accesses leaves every 32-byte sector half-covered by each
+// instruction; one 32-byte access covers whole sectors.
+__device__ __forceinline__ void ld_stream32(const void* p, uint4& a, uint4& b) {
+  asm("ld.global.cs.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+      : "l"(p));
+}
+__device__ __forceinline__ void st32(void* p, const uint4& a, const uint4& b) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+               :: "l"(p), "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z),
+                  "r"(b.w)
+               : "memory");
+}
+
+// 32 bytes at a 16-byte aligned address: one access when kWide (the caller
+// has checked 32-byte alignment), else two.
+template <bool kWide>
+__device__ __forceinline__ void load32(const void* p, uint4& a, uint4& b) {
+  if constexpr (kWide) {
+    ld_stream32(p, a, b);
+  } else {
+    a = ld_stream16(p);
+    b = ld_stream16(static_cast<const char*>(p) + 16);
+  }
+}
+template <bool kWide>
+__device__ __forceinline__ void store32(void* p, const uint4& a, const uint4& b) {
+  if constexpr (kWide) {
+    st32(p, a, b);
+  } else {
+    *reinterpret_cast<uint4*>(p) = a;
+    *reinterpret_cast<uint4*>(static_cast<char*>(p) + 16) = b;
+  }
+}
+
 __device__ __forceinline__ void st16(void* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 __device__ __forceinline__ void st8(void* p, uint2 v) { *reinterpret_cast<uint2*>(p) = v; }
 __device__ __forceinline__ void st4(void* p, uint32_t v) { *reinterpret_cast<uint32_t*>(p) = v; }

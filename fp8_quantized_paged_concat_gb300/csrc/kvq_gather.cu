@@ -117,6 +117,7 @@ __device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint2 c) {
 // ---------------------------------------------------------------------------
 // nvfp4_ds_mla
 // ---------------------------------------------------------------------------
+template <bool kWide>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) gather_nvfp4_ds_mla_kernel(const GatherArgs a) {
   __shared__ int32_t s_ws[kMaxSmemBatch];
   int64_t offs[kRowsPerWarp], mine;
@@ -155,9 +156,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gather_nvfp4_ds_mla_kern
       const float2 v = __half22float2(e2m1x2_to_half2(byte));
       o[i] = pack_bf16x2(v.x * scale, v.y * scale);     // exact products
     }
-    __nv_bfloat16* out = dst + (w0 + k) * a.dst_stride + 16 * lane;
-    st16(out, make_uint4(o[0], o[1], o[2], o[3]));
-    st16(out + 8, make_uint4(o[4], o[5], o[6], o[7]));
+    store32<kWide>(dst + (w0 + k) * a.dst_stride + 16 * lane, make_uint4(o[0], o[1], o[2], o[3]),
+                   make_uint4(o[4], o[5], o[6], o[7]));
   }
 #pragma unroll
   for (int k = 0; k < kRopeItems; ++k) {
@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gather_nvfp4_ds_mla_kern
 // ---------------------------------------------------------------------------
 // fp8_ds_mla
 // ---------------------------------------------------------------------------
+template <bool kWide>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) gather_fp8_ds_mla_kernel(const GatherArgs a) {
   __shared__ int32_t s_ws[kMaxSmemBatch];
   int64_t offs[kRowsPerWarp], mine;
@@ -210,9 +211,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gather_fp8_ds_mla_kernel
       o[2 * i] = pack_bf16x2(__fmul_rn(v0.x, s[k]), __fmul_rn(v0.y, s[k]));
       o[2 * i + 1] = pack_bf16x2(__fmul_rn(v1.x, s[k]), __fmul_rn(v1.y, s[k]));
     }
-    __nv_bfloat16* out = dst + (w0 + k) * a.dst_stride + 16 * lane;
-    st16(out, make_uint4(o[0], o[1], o[2], o[3]));
-    st16(out + 8, make_uint4(o[4], o[5], o[6], o[7]));
+    store32<kWide>(dst + (w0 + k) * a.dst_stride + 16 * lane, make_uint4(o[0], o[1], o[2], o[3]),
+                   make_uint4(o[4], o[5], o[6], o[7]));
   }
 #pragma unroll
   for (int k = 0; k < kRopeItems; ++k) {
@@ -220,6 +220,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gather_fp8_ds_mla_kernel
     const int r = (lane >> 3) + 4 * k;
     st16(dst + (w0 + r) * a.dst_stride + kNopeDim + 8 * (lane & 7), rp[k]);
   }
+}
+
+// Workspace rows that start on 32-byte boundaries are written with 32-byte
+// stores.
+bool wide_rows(const GatherArgs& a) {
+  return reinterpret_cast<uintptr_t>(a.dst) % 32 == 0 && (a.dst_stride * 2) % 32 == 0;
 }
 
 cudaError_t launch_gather(void (*kernel)(GatherArgs), const GatherArgs& a, cudaStream_t stream) {
@@ -231,11 +237,13 @@ cudaError_t launch_gather(void (*kernel)(GatherArgs), const GatherArgs& a, cudaS
 }  // namespace
 
 cudaError_t launch_gather_nvfp4_ds_mla(const GatherArgs& a, cudaStream_t stream) {
-  return launch_gather(gather_nvfp4_ds_mla_kernel, a, stream);
+  return launch_gather(wide_rows(a) ? gather_nvfp4_ds_mla_kernel<true> : gather_nvfp4_ds_mla_kernel<false>,
+                       a, stream);
 }
 
 cudaError_t launch_gather_fp8_ds_mla(const GatherArgs& a, cudaStream_t stream) {
-  return launch_gather(gather_fp8_ds_mla_kernel, a, stream);
+  return launch_gather(wide_rows(a) ? gather_fp8_ds_mla_kernel<true> : gather_fp8_ds_mla_kernel<false>,
+                       a, stream);
 }
 
 }  // namespace kvq

@@ -16,6 +16,7 @@ namespace {
 
 constexpr int kThreads = 256;
 
+template <bool kWide>
 __global__ void __launch_bounds__(kThreads) reshape_and_cache_nvfp4_kernel(const PerHeadArgs a) {
   // flat index = ((t * 2 + side) * H + h) * groups + g, below 2^32 (host check)
   const uint32_t idx = blockIdx.x * kThreads + threadIdx.x;
@@ -38,8 +39,8 @@ __global__ void __launch_bounds__(kThreads) reshape_and_cache_nvfp4_kernel(const
                              static_cast<int64_t>(t) * (side ? a.value_stride_t : a.key_stride_t) +
                              static_cast<int64_t>(h) * (side ? a.value_stride_h : a.key_stride_h) +
                              g * kGroup;
-  const uint4 lo = ld_stream16(src);
-  const uint4 hi = ld_stream16(src + 8);
+  uint4 lo, hi;
+  load32<kWide>(src, lo, hi);
   const float inv_scale = 1.0f / __ldg(side ? a.v_scale : a.k_scale);
 
   const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
@@ -69,6 +70,7 @@ __global__ void __launch_bounds__(kThreads) reshape_and_cache_nvfp4_kernel(const
 // group's 8 data bytes and scale byte and writes 16 bf16 values
 // bf16_rn((e2m1 * sf) * scale) -- the first product exact, one fp32 rounding
 // for the per-tensor scale, one bf16 rounding.
+template <bool kWide>
 __global__ void __launch_bounds__(kThreads) dequant_nvfp4_per_head_kernel(const PerHeadArgs a) {
   const uint32_t idx = blockIdx.x * kThreads + threadIdx.x;
   const uint32_t t = a.unit_div.div(idx);
@@ -107,8 +109,14 @@ __global__ void __launch_bounds__(kThreads) dequant_nvfp4_per_head_kernel(const 
   __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(const_cast<void*>(side ? a.value : a.key)) +
                        static_cast<int64_t>(t) * (side ? a.value_stride_t : a.key_stride_t) +
                        static_cast<int64_t>(h) * (side ? a.value_stride_h : a.key_stride_h) + g * kGroup;
-  st16(dst, make_uint4(o[0], o[1], o[2], o[3]));
-  st16(dst + 8, make_uint4(o[4], o[5], o[6], o[7]));
+  store32<kWide>(dst, make_uint4(o[0], o[1], o[2], o[3]), make_uint4(o[4], o[5], o[6], o[7]));
+}
+
+// key / value rows whose 16-value groups all start on 32-byte boundaries.
+bool wide_rows(const PerHeadArgs& a) {
+  return reinterpret_cast<uintptr_t>(a.key) % 32 == 0 && reinterpret_cast<uintptr_t>(a.value) % 32 == 0 &&
+         (a.key_stride_t * 2) % 32 == 0 && (a.key_stride_h * 2) % 32 == 0 &&
+         (a.value_stride_t * 2) % 32 == 0 && (a.value_stride_h * 2) % 32 == 0;
 }
 
 }  // namespace
@@ -116,14 +124,16 @@ __global__ void __launch_bounds__(kThreads) dequant_nvfp4_per_head_kernel(const 
 cudaError_t launch_dequant_nvfp4_per_head(const PerHeadArgs& a, cudaStream_t stream) {
   const int64_t threads = a.num_tokens * 2 * a.num_heads * (a.head_size / kGroup);
   const int64_t blocks = (threads + kThreads - 1) / kThreads;
-  dequant_nvfp4_per_head_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(a);
+  (wide_rows(a) ? dequant_nvfp4_per_head_kernel<true> : dequant_nvfp4_per_head_kernel<false>)
+      <<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_reshape_and_cache_nvfp4(const PerHeadArgs& a, cudaStream_t stream) {
   const int64_t threads = a.num_tokens * 2 * a.num_heads * (a.head_size / kGroup);
   const int64_t blocks = (threads + kThreads - 1) / kThreads;
-  reshape_and_cache_nvfp4_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(a);
+  (wide_rows(a) ? reshape_and_cache_nvfp4_kernel<true> : reshape_and_cache_nvfp4_kernel<false>)
+      <<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

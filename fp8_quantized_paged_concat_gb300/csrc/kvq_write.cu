@@ -61,6 +61,7 @@ __device__ __forceinline__ uint8_t* entry_of(int64_t slot, const WriteArgs& a) {
 // ---------------------------------------------------------------------------
 // nvfp4_ds_mla: 352-byte entries
 // ---------------------------------------------------------------------------
+template <bool kWide>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, kMinBlocks)
 write_nvfp4_ds_mla_kernel(const WriteArgs a) {
   const int lane = threadIdx.x & 31;
@@ -83,9 +84,7 @@ write_nvfp4_ds_mla_kernel(const WriteArgs a) {
   for (int j = 0; j < kTokensPerWarp; ++j) {
     entry[j] = entry_of(__shfl_sync(kFull, my_slot, j), a);   // warp-uniform
     if (entry[j] != nullptr) {
-      const __nv_bfloat16* row = kv_c + (t0 + j) * a.kv_c_stride + lane * kGroup;
-      na[j] = ld_stream16(row);
-      nb[j] = ld_stream16(row + 8);
+      load32<kWide>(kv_c + (t0 + j) * a.kv_c_stride + lane * kGroup, na[j], nb[j]);
       if (lane < 16) rp[j] = ld_stream8(k_pe + (t0 + j) * a.k_pe_stride + lane * 4);
     }
   }
@@ -116,6 +115,7 @@ write_nvfp4_ds_mla_kernel(const WriteArgs a) {
 // ---------------------------------------------------------------------------
 // fp8_ds_mla: 656-byte entries
 // ---------------------------------------------------------------------------
+template <bool kWide>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, kMinBlocks)
 write_fp8_ds_mla_kernel(const WriteArgs a) {
   const int lane = threadIdx.x & 31;
@@ -136,9 +136,7 @@ write_fp8_ds_mla_kernel(const WriteArgs a) {
   for (int j = 0; j < kTokensPerWarp; ++j) {
     entry[j] = entry_of(__shfl_sync(kFull, my_slot, j), a);
     if (entry[j] != nullptr) {
-      const __nv_bfloat16* row = kv_c + (t0 + j) * a.kv_c_stride + lane * 16;
-      na[j] = ld_stream16(row);
-      nb[j] = ld_stream16(row + 8);
+      load32<kWide>(kv_c + (t0 + j) * a.kv_c_stride + lane * 16, na[j], nb[j]);
       if (lane < 8) rp[j] = ld_stream16(k_pe + (t0 + j) * a.k_pe_stride + lane * 8);
     }
   }
@@ -166,6 +164,11 @@ write_fp8_ds_mla_kernel(const WriteArgs a) {
   }
 }
 
+// kv_c rows that start on 32-byte boundaries are read with 32-byte accesses.
+bool wide_rows(const WriteArgs& a) {
+  return reinterpret_cast<uintptr_t>(a.kv_c) % 32 == 0 && (a.kv_c_stride * 2) % 32 == 0;
+}
+
 cudaError_t launch_write(void (*kernel)(WriteArgs), const WriteArgs& a, cudaStream_t stream) {
   const int64_t tokens_per_block = int64_t{kWarpsPerBlock} * kTokensPerWarp;
   const int64_t blocks = (a.num_tokens + tokens_per_block - 1) / tokens_per_block;
@@ -176,11 +179,13 @@ cudaError_t launch_write(void (*kernel)(WriteArgs), const WriteArgs& a, cudaStre
 }  // namespace
 
 cudaError_t launch_write_nvfp4_ds_mla(const WriteArgs& a, cudaStream_t stream) {
-  return launch_write(write_nvfp4_ds_mla_kernel, a, stream);
+  return launch_write(wide_rows(a) ? write_nvfp4_ds_mla_kernel<true> : write_nvfp4_ds_mla_kernel<false>,
+                      a, stream);
 }
 
 cudaError_t launch_write_fp8_ds_mla(const WriteArgs& a, cudaStream_t stream) {
-  return launch_write(write_fp8_ds_mla_kernel, a, stream);
+  return launch_write(wide_rows(a) ? write_fp8_ds_mla_kernel<true> : write_fp8_ds_mla_kernel<false>,
+                      a, stream);
 }
 
 }  // namespace kvq

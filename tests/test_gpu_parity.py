@@ -100,7 +100,7 @@ def test_device_converters_strided_full_range(kvq, oracle_mod, threads):
 # --------------------------------------------------------------------------
 
 def run_write(kvq, oracle_mod, w, entry, init_seed=3, pad_entry=0, pad_block=0, kv_view=False,
-              threads=1, status_expected=0):
+              threads=1, status_expected=0, narrow_rows=False):
     """GPU vs oracle write into a pre-filled cache with optional padded
     entries / blocks; returns the GPU cache (host)."""
     es = entry + pad_entry
@@ -110,6 +110,11 @@ def run_write(kvq, oracle_mod, w, entry, init_seed=3, pad_entry=0, pad_block=0, 
     if kv_view:            # kv_c and k_pe as column slices of one [T, 576] tensor
         both = torch.cat([w.kv_c, w.k_pe], dim=1).to(DEV)
         kv_c, k_pe = both[:, :512], both[:, 512:]
+    elif narrow_rows:      # rows 16-byte but not 32-byte aligned: the two-access path
+        buf = torch.zeros((w.num_tokens, 600), dtype=torch.bfloat16, device=DEV)
+        buf[:, 8:520] = w.kv_c.to(DEV)
+        buf[:, 528:592] = w.k_pe.to(DEV)
+        kv_c, k_pe = buf[:, 8:520], buf[:, 528:592]
     else:
         kv_c, k_pe = dev(w.kv_c), dev(w.k_pe)
     gbuf = dev(buf0.copy())
@@ -137,6 +142,7 @@ WRITE_CASES = [
     ("kv_c / k_pe slices of one tensor", lambda: wl.make_write("view", 129, 4, 64, 2, 66),
      dict(kv_view=True)),
     ("block_size 7", lambda: wl.make_write("bs7", 300, 50, 7, 5, 67), {}),
+    ("16-byte aligned rows", lambda: wl.make_write("narrow", 77, 4, 64, 3, 69), dict(narrow_rows=True)),
     ("block_size 33", lambda: wl.make_write("bs33", 301, 12, 33, 6, 68), {}),
 ]
 
@@ -190,16 +196,17 @@ def test_write_prefill_fill_full_size(kvq, oracle_mod, threads):
 # --------------------------------------------------------------------------
 
 def run_gather(kvq, oracle_mod, entry, cache_host, table, ws, starts, T, batch_size=None,
-               dst_pad=0, pad_entry=0, pad_block=0, status_expected=0, threads=1):
+               dst_pad=0, pad_entry=0, pad_block=0, status_expected=0, threads=1, dst_offset=0):
     nb, bs, _ = cache_host.shape
     buf = np.zeros((nb, bs + pad_block, entry + pad_entry), np.uint8)
     buf[:, :bs, :entry] = cache_host
     gbuf = dev(buf)
-    dst = torch.full((T, 576 + dst_pad), -7.0, dtype=torch.bfloat16, device=DEV)
+    dst = torch.full((T, 576 + dst_pad + dst_offset), -7.0, dtype=torch.bfloat16, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     fn = kvq.kvq_gather_upconvert_nvfp4_ds_mla if entry == 352 else kvq.kvq_gather_upconvert_fp8_ds_mla
-    fn(gbuf[:, :bs, :], dst[:, :576] if dst_pad else dst, dev(table), dev(ws), dev(starts),
-       batch_size=batch_size, status=status)
+    view = dst[:, dst_offset:dst_offset + 576] if (dst_pad or dst_offset) else dst
+    fn(gbuf[:, :bs, :], view, dev(table), dev(ws), dev(starts), batch_size=batch_size, status=status)
+    dst = dst[:, dst_offset:]
     guard = wl.bf16_bits(torch.tensor([-7.0], dtype=torch.bfloat16))[0]
     want = np.full((T, 576), guard, np.uint16)
     ofn = oracle_mod.gather_nvfp4_ds_mla if entry == 352 else oracle_mod.gather_fp8_ds_mla
@@ -245,6 +252,7 @@ GATHER_CASES = [
     ("300 short requests", (4096, 16), list(range(1, 301)), [i % 40 for i in range(300)], {}),
     ("block_size 7", (200, 7), [90, 0, 300, 17], [6, 3, 0, 13], {}),
     ("block_size 48", (40, 48), [500, 333], [47, 1], {}),
+    ("16-byte aligned rows", (16, 64), [130, 70], [5, 64], dict(dst_offset=8, dst_pad=16)),
 ]
 
 
@@ -337,7 +345,7 @@ def test_gather_fp8_full_size(kvq, oracle_mod, threads):
 # per-head NVFP4 cache
 # --------------------------------------------------------------------------
 
-def run_per_head(kvq, oracle_mod, w, strided=False, status_expected=0, threads=1):
+def run_per_head(kvq, oracle_mod, w, strided=False, status_expected=0, threads=1, narrow_rows=False):
     T, H, D = w.key.shape
     fd = kvq.nvfp4_full_dim(D)
     init = wl.random_bytes((w.num_pages, 2, w.block_size, H, fd), 5)
@@ -345,6 +353,12 @@ def run_per_head(kvq, oracle_mod, w, strided=False, status_expected=0, threads=1
     if strided:            # key and value as interleaved halves of one [T, H, 2D] tensor
         both = torch.cat([w.key, w.value], dim=2).to(DEV)
         key, value = both[:, :, :D], both[:, :, D:]
+    elif narrow_rows:      # 16-byte but not 32-byte aligned groups: the two-access path
+        kb = torch.zeros((T, H, D + 24), dtype=torch.bfloat16, device=DEV)
+        vb = torch.zeros((T, H, D + 24), dtype=torch.bfloat16, device=DEV)
+        kb[:, :, 8:8 + D] = w.key.to(DEV)
+        vb[:, :, 8:8 + D] = w.value.to(DEV)
+        key, value = kb[:, :, 8:8 + D], vb[:, :, 8:8 + D]
     else:
         key, value = dev(w.key), dev(w.value)
     ks = torch.tensor([w.k_scale], dtype=torch.float32, device=DEV)
@@ -367,6 +381,7 @@ PER_HEAD_CASES = [
     ("H8 D128 strided", lambda: wl.make_per_head("d", 129, 8, 128, 32, 16, 4, 104), dict(strided=True)),
     ("block_size 1", lambda: wl.make_per_head("e", 50, 8, 128, 64, 1, 2, 105), {}),
     ("H3 D48 block_size 24", lambda: wl.make_per_head("f", 90, 3, 48, 12, 24, 4, 107, v_scale=1.5), {}),
+    ("16-byte aligned rows", lambda: wl.make_per_head("g", 45, 4, 128, 8, 16, 2, 108), dict(narrow_rows=True)),
 ]
 
 
@@ -391,11 +406,16 @@ def test_per_head_full_size(kvq, oracle_mod, threads):
 # per-head read-back (next row: the consumer side of the per-head cache)
 # --------------------------------------------------------------------------
 
-def run_dequant(kvq, oracle_mod, w, cache_host, strided=False, status_expected=0, threads=1):
+def run_dequant(kvq, oracle_mod, w, cache_host, strided=False, status_expected=0, threads=1,
+                narrow_rows=False):
     T, H, D = w.key.shape
     if strided:          # outputs as halves of one [T, H, 2D] tensor
         both = torch.full((T, H, 2 * D), -3.0, dtype=torch.bfloat16, device=DEV)
         ko, vo = both[:, :, :D], both[:, :, D:]
+    elif narrow_rows:    # 16-byte but not 32-byte aligned output groups
+        kb = torch.full((T, H, D + 24), -3.0, dtype=torch.bfloat16, device=DEV)
+        vb = torch.full((T, H, D + 24), -3.0, dtype=torch.bfloat16, device=DEV)
+        ko, vo = kb[:, :, 8:8 + D], vb[:, :, 8:8 + D]
     else:
         ko = torch.full((T, H, D), -3.0, dtype=torch.bfloat16, device=DEV)
         vo = torch.full((T, H, D), -3.0, dtype=torch.bfloat16, device=DEV)
