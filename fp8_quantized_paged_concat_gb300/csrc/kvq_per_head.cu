@@ -28,20 +28,22 @@ __global__ void __launch_bounds__(kThreads) reshape_and_cache_nvfp4_kernel(const
   const uint32_t h = a.head_div.div(r);
   const uint32_t g = r - h * a.head_div.d;
 
-  const int64_t slot = __ldg(a.slot_mapping + t);
-  if (slot < 0) return;
-  if (slot >= a.num_slots) {
-    if (side == 0 && h == 0 && g == 0) report(a.status, KVQ_STATUS_BAD_INDEX);
-    return;
-  }
-
+  // The group is loaded without waiting for the slot (a padding token's
+  // values are read but nothing is written for them).
   const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(side ? a.value : a.key) +
                              static_cast<int64_t>(t) * (side ? a.value_stride_t : a.key_stride_t) +
                              static_cast<int64_t>(h) * (side ? a.value_stride_h : a.key_stride_h) +
                              g * kGroup;
   uint4 lo, hi;
   load32<kWide>(src, lo, hi);
-  const float inv_scale = 1.0f / __ldg(side ? a.v_scale : a.k_scale);
+  const int64_t slot = __ldg(a.slot_mapping + t);
+  const float scale_in = __ldg(side ? a.v_scale : a.k_scale);
+  if (slot < 0) return;
+  if (slot >= a.num_slots) {
+    if (side == 0 && h == 0 && g == 0) report(a.status, KVQ_STATUS_BAD_INDEX);
+    return;
+  }
+  const float inv_scale = 1.0f / scale_in;
 
   const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
   float y[16];

@@ -22,11 +22,15 @@ namespace {
 #ifndef KVQ_WRITE_TOKENS_PER_WARP
 #define KVQ_WRITE_TOKENS_PER_WARP 4
 #endif
+#ifndef KVQ_WRITE_SMALL_BATCH
+#define KVQ_WRITE_SMALL_BATCH 65536   // below this many tokens: one token per warp
+#endif
 #ifndef KVQ_WRITE_MIN_BLOCKS
 #define KVQ_WRITE_MIN_BLOCKS 8
 #endif
 constexpr int kWarpsPerBlock = KVQ_WRITE_WARPS_PER_BLOCK;
 constexpr int kTokensPerWarp = KVQ_WRITE_TOKENS_PER_WARP;
+constexpr int64_t kSmallBatch = KVQ_WRITE_SMALL_BATCH;
 constexpr int kMinBlocks = KVQ_WRITE_MIN_BLOCKS;
 
 // The 8 packed bf16 pairs of one lane's 16 NoPE values, as fp32.
@@ -61,7 +65,7 @@ __device__ __forceinline__ uint8_t* entry_of(int64_t slot, const WriteArgs& a) {
 // ---------------------------------------------------------------------------
 // nvfp4_ds_mla: 352-byte entries
 // ---------------------------------------------------------------------------
-template <bool kWide>
+template <bool kWide, int kTokensPerWarp>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, kMinBlocks)
 write_nvfp4_ds_mla_kernel(const WriteArgs a) {
   const int lane = threadIdx.x & 31;
@@ -77,17 +81,20 @@ write_nvfp4_ds_mla_kernel(const WriteArgs a) {
   const __nv_bfloat16* kv_c = static_cast<const __nv_bfloat16*>(a.kv_c);
   const __nv_bfloat16* k_pe = static_cast<const __nv_bfloat16*>(a.k_pe);
 
+  // The rows are loaded without waiting for the slots (a padding token's row
+  // is read but nothing is written for it), so the slot and row loads overlap.
   uint8_t* entry[kTokensPerWarp];
   uint4 na[kTokensPerWarp], nb[kTokensPerWarp];
   uint2 rp[kTokensPerWarp];
 #pragma unroll
   for (int j = 0; j < kTokensPerWarp; ++j) {
-    entry[j] = entry_of(__shfl_sync(kFull, my_slot, j), a);   // warp-uniform
-    if (entry[j] != nullptr) {
+    if (t0 + j < a.num_tokens) {
       load32<kWide>(kv_c + (t0 + j) * a.kv_c_stride + lane * kGroup, na[j], nb[j]);
       if (lane < 16) rp[j] = ld_stream8(k_pe + (t0 + j) * a.k_pe_stride + lane * 4);
     }
   }
+#pragma unroll
+  for (int j = 0; j < kTokensPerWarp; ++j) entry[j] = entry_of(__shfl_sync(kFull, my_slot, j), a);
 
 #pragma unroll
   for (int j = 0; j < kTokensPerWarp; ++j) {
@@ -115,7 +122,7 @@ write_nvfp4_ds_mla_kernel(const WriteArgs a) {
 // ---------------------------------------------------------------------------
 // fp8_ds_mla: 656-byte entries
 // ---------------------------------------------------------------------------
-template <bool kWide>
+template <bool kWide, int kTokensPerWarp>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, kMinBlocks)
 write_fp8_ds_mla_kernel(const WriteArgs a) {
   const int lane = threadIdx.x & 31;
@@ -134,12 +141,13 @@ write_fp8_ds_mla_kernel(const WriteArgs a) {
   uint4 na[kTokensPerWarp], nb[kTokensPerWarp], rp[kTokensPerWarp];
 #pragma unroll
   for (int j = 0; j < kTokensPerWarp; ++j) {
-    entry[j] = entry_of(__shfl_sync(kFull, my_slot, j), a);
-    if (entry[j] != nullptr) {
+    if (t0 + j < a.num_tokens) {
       load32<kWide>(kv_c + (t0 + j) * a.kv_c_stride + lane * 16, na[j], nb[j]);
       if (lane < 8) rp[j] = ld_stream16(k_pe + (t0 + j) * a.k_pe_stride + lane * 8);
     }
   }
+#pragma unroll
+  for (int j = 0; j < kTokensPerWarp; ++j) entry[j] = entry_of(__shfl_sync(kFull, my_slot, j), a);
 
 #pragma unroll
   for (int j = 0; j < kTokensPerWarp; ++j) {
@@ -169,23 +177,43 @@ bool wide_rows(const WriteArgs& a) {
   return reinterpret_cast<uintptr_t>(a.kv_c) % 32 == 0 && (a.kv_c_stride * 2) % 32 == 0;
 }
 
+template <int kTpw>
 cudaError_t launch_write(void (*kernel)(WriteArgs), const WriteArgs& a, cudaStream_t stream) {
-  const int64_t tokens_per_block = int64_t{kWarpsPerBlock} * kTokensPerWarp;
+  const int64_t tokens_per_block = int64_t{kWarpsPerBlock} * kTpw;
   const int64_t blocks = (a.num_tokens + tokens_per_block - 1) / tokens_per_block;
   kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
+// Large batches: kTokensPerWarp tokens per warp (more bytes in flight per
+// warp).  Small, latency-bound batches (decode steps): one token per warp,
+// four times as many warps.
+template <template <bool, int> class K>
+cudaError_t dispatch_write(const WriteArgs& a, cudaStream_t stream) {
+  const bool wide = wide_rows(a);
+  if (a.num_tokens >= kSmallBatch)
+    return launch_write<kTokensPerWarp>(wide ? K<true, kTokensPerWarp>::fn : K<false, kTokensPerWarp>::fn,
+                                        a, stream);
+  return launch_write<1>(wide ? K<true, 1>::fn : K<false, 1>::fn, a, stream);
+}
+
+template <bool W, int T>
+struct Nvfp4Write {
+  static constexpr void (*fn)(WriteArgs) = write_nvfp4_ds_mla_kernel<W, T>;
+};
+template <bool W, int T>
+struct Fp8Write {
+  static constexpr void (*fn)(WriteArgs) = write_fp8_ds_mla_kernel<W, T>;
+};
+
 }  // namespace
 
 cudaError_t launch_write_nvfp4_ds_mla(const WriteArgs& a, cudaStream_t stream) {
-  return launch_write(wide_rows(a) ? write_nvfp4_ds_mla_kernel<true> : write_nvfp4_ds_mla_kernel<false>,
-                      a, stream);
+  return dispatch_write<Nvfp4Write>(a, stream);
 }
 
 cudaError_t launch_write_fp8_ds_mla(const WriteArgs& a, cudaStream_t stream) {
-  return launch_write(wide_rows(a) ? write_fp8_ds_mla_kernel<true> : write_fp8_ds_mla_kernel<false>,
-                      a, stream);
+  return dispatch_write<Fp8Write>(a, stream);
 }
 
 }  // namespace kvq

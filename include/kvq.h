@@ -76,7 +76,8 @@ typedef struct CUstream_st* kvq_stream_t;   /* identical to cudaStream_t */
  * and "Implementation breakdown" item 3.
  *
  * For each token t < num_tokens with slot s = slot_mapping[t]:
- *   s < 0                        padding: skipped, nothing read or written;
+ *   s < 0                        padding: nothing is written for it (its
+ *                                row may still be read);
  *   s >= num_blocks*block_size   out of range: skipped, KVQ_STATUS_BAD_INDEX;
  *   otherwise the entry at kv_cache + (s / block_size) * block_stride +
  *   (s % block_size) * entry_stride receives

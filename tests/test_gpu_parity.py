@@ -143,6 +143,9 @@ WRITE_CASES = [
      dict(kv_view=True)),
     ("block_size 7", lambda: wl.make_write("bs7", 300, 50, 7, 5, 67), {}),
     ("16-byte aligned rows", lambda: wl.make_write("narrow", 77, 4, 64, 3, 69), dict(narrow_rows=True)),
+    ("4-token warps, ragged T=65573", lambda: wl.make_write("big", 65573, 2048, 64, 300, 70), {}),
+    ("4-token warps, 16-byte aligned rows", lambda: wl.make_write("bign", 65540, 1100, 64, 17, 71),
+     dict(narrow_rows=True)),
     ("block_size 33", lambda: wl.make_write("bs33", 301, 12, 33, 6, 68), {}),
 ]
 
