@@ -2,12 +2,12 @@
 // [num_pages, 2, block_size, H, full_dim] whose side regions hold
 // [data [block_size][H][D/2] | scales [block_size][H][D/16]].
 //
-// Design (GB300): one thread per 16-value group of one (token, side, head):
-// it loads its 32 contiguous input bytes, forms the group scale and writes 8
-// data bytes and 1 scale byte.  Groups are numbered fastest within a head,
-// then heads, then sides, so a warp covers whole heads of one token side and
-// its stores are contiguous (8 x 32 = 256 data bytes and 32 scale bytes at
-// H = 8, D = 128).
+// Design (GB300): one thread per 4 consecutive 16-value groups of one
+// (token, side, head) (2 or 1 when a head's group count is not a multiple of
+// 4): it issues its 4 x 32-byte loads first, forms each group's scale and
+// writes 8 data bytes per group and the groups' scale bytes in one store.
+// Threads are numbered fastest within a head, then heads, then sides, so a
+// warp covers whole heads of one token side and its stores are contiguous.
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
 
@@ -16,102 +16,133 @@ namespace {
 
 constexpr int kThreads = 256;
 
-template <bool kWide>
-__global__ void __launch_bounds__(kThreads) reshape_and_cache_nvfp4_kernel(const PerHeadArgs a) {
-  // flat index = ((t * 2 + side) * H + h) * groups + g, below 2^32 (host check)
-  const uint32_t idx = blockIdx.x * kThreads + threadIdx.x;
-  const uint32_t t = a.unit_div.div(idx);
-  if (t >= a.num_tokens) return;
-  const uint32_t u = idx - t * a.unit_div.d;
-  const uint32_t side = a.side_div.div(u);
-  const uint32_t r = u - side * a.side_div.d;
-  const uint32_t h = a.head_div.div(r);
-  const uint32_t g = r - h * a.head_div.d;
+// A thread owns kGpt consecutive 16-value groups of one (token, side, head):
+// flat index = ((t * 2 + side) * H + h) * (groups / kGpt) + u, with
+// unit_div / side_div / head_div set up by the launcher for that kGpt.
+struct Unit {
+  uint32_t t, side, h, g0;
+};
 
-  // The group is loaded without waiting for the slot (a padding token's
+template <int kGpt>
+__device__ __forceinline__ bool unit_of(const PerHeadArgs& a, Unit& u) {
+  const uint32_t idx = blockIdx.x * kThreads + threadIdx.x;     // < 2^32 - 256 (host check)
+  u.t = a.unit_div.div(idx);
+  if (u.t >= a.num_tokens) return false;
+  const uint32_t r0 = idx - u.t * a.unit_div.d;
+  u.side = a.side_div.div(r0);
+  const uint32_t r1 = r0 - u.side * a.side_div.d;
+  u.h = a.head_div.div(r1);
+  u.g0 = (r1 - u.h * a.head_div.d) * kGpt;
+  return true;
+}
+
+// Base of (page, side) and the row index (offset * H + h) of a slot.
+__device__ __forceinline__ int64_t side_base(const PerHeadArgs& a, int64_t slot, uint32_t side,
+                                             uint32_t h, int64_t& row) {
+  const uint32_t page = a.block_div.div(static_cast<uint32_t>(slot));
+  const uint32_t off = static_cast<uint32_t>(slot) - page * static_cast<uint32_t>(a.block_size);
+  const int64_t region = static_cast<int64_t>(a.block_size) * a.num_heads * (a.head_size / 2 + a.head_size / kGroup);
+  row = static_cast<int64_t>(off) * a.num_heads + h;
+  return (static_cast<int64_t>(page) * 2 + side) * region;
+}
+
+template <bool kWide, int kGpt>
+__global__ void __launch_bounds__(kThreads) reshape_and_cache_nvfp4_kernel(const PerHeadArgs a) {
+  Unit u;
+  if (!unit_of<kGpt>(a, u)) return;
+  // The groups are loaded without waiting for the slot (a padding token's
   // values are read but nothing is written for them).
-  const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(side ? a.value : a.key) +
-                             static_cast<int64_t>(t) * (side ? a.value_stride_t : a.key_stride_t) +
-                             static_cast<int64_t>(h) * (side ? a.value_stride_h : a.key_stride_h) +
-                             g * kGroup;
-  uint4 lo, hi;
-  load32<kWide>(src, lo, hi);
-  const int64_t slot = __ldg(a.slot_mapping + t);
-  const float scale_in = __ldg(side ? a.v_scale : a.k_scale);
+  const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(u.side ? a.value : a.key) +
+                             static_cast<int64_t>(u.t) * (u.side ? a.value_stride_t : a.key_stride_t) +
+                             static_cast<int64_t>(u.h) * (u.side ? a.value_stride_h : a.key_stride_h) +
+                             u.g0 * kGroup;
+  uint4 lo[kGpt], hi[kGpt];
+#pragma unroll
+  for (int j = 0; j < kGpt; ++j) load32<kWide>(src + j * kGroup, lo[j], hi[j]);
+  const int64_t slot = __ldg(a.slot_mapping + u.t);
+  const float scale_in = __ldg(u.side ? a.v_scale : a.k_scale);
   if (slot < 0) return;
   if (slot >= a.num_slots) {
-    if (side == 0 && h == 0 && g == 0) report(a.status, KVQ_STATUS_BAD_INDEX);
+    if (u.side == 0 && u.h == 0 && u.g0 == 0) report(a.status, KVQ_STATUS_BAD_INDEX);
     return;
   }
   const float inv_scale = 1.0f / scale_in;
-
-  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-  float y[16];
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    y[2 * i] = __fmul_rn(bf16_lo(w[i]), inv_scale);
-    y[2 * i + 1] = __fmul_rn(bf16_hi(w[i]), inv_scale);
-    amax = fmaxf(amax, fmaxf(fabsf(y[2 * i]), fabsf(y[2 * i + 1])));
-  }
-  const uint32_t sf = nvfp4_scale_code(amax);
-
-  const uint32_t page = a.block_div.div(static_cast<uint32_t>(slot));
-  const uint32_t off = static_cast<uint32_t>(slot) - page * static_cast<uint32_t>(a.block_size);
+  int64_t row;
+  uint8_t* base = a.cache + side_base(a, slot, u.side, u.h, row);
   const int64_t data_dim = a.head_size / 2;
   const int64_t scale_dim = a.head_size / kGroup;
-  const int64_t region = static_cast<int64_t>(a.block_size) * a.num_heads * (data_dim + scale_dim);
-  uint8_t* base = a.cache + (static_cast<int64_t>(page) * 2 + side) * region;
-  const int64_t row = static_cast<int64_t>(off) * a.num_heads + h;
-  st8(base + row * data_dim + 8 * g, nvfp4_pack16(y, nvfp4_inverse_scale(sf)));
-  base[static_cast<int64_t>(a.block_size) * a.num_heads * data_dim + row * scale_dim + g] =
-      static_cast<uint8_t>(sf);
+  uint8_t* data = base + row * data_dim + 8 * u.g0;
+  uint8_t* scales = base + static_cast<int64_t>(a.block_size) * a.num_heads * data_dim + row * scale_dim + u.g0;
+  uint32_t sf_word = 0;
+#pragma unroll
+  for (int j = 0; j < kGpt; ++j) {
+    const uint32_t w[8] = {lo[j].x, lo[j].y, lo[j].z, lo[j].w, hi[j].x, hi[j].y, hi[j].z, hi[j].w};
+    float y[16];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      y[2 * i] = __fmul_rn(bf16_lo(w[i]), inv_scale);
+      y[2 * i + 1] = __fmul_rn(bf16_hi(w[i]), inv_scale);
+      amax = fmaxf(amax, fmaxf(fabsf(y[2 * i]), fabsf(y[2 * i + 1])));
+    }
+    const uint32_t sf = nvfp4_scale_code(amax);
+    st8(data + 8 * j, nvfp4_pack16(y, nvfp4_inverse_scale(sf)));
+    sf_word |= sf << (8 * j);
+  }
+  // kGpt scale bytes, contiguous
+  if constexpr (kGpt == 4) {
+    st4(scales, sf_word);
+  } else if constexpr (kGpt == 2) {
+    *reinterpret_cast<uint16_t*>(scales) = static_cast<uint16_t>(sf_word);
+  } else {
+    *scales = static_cast<uint8_t>(sf_word);
+  }
 }
 
-// Read-back: the same thread-per-group decomposition; each thread reads its
-// group's 8 data bytes and scale byte and writes 16 bf16 values
-// bf16_rn((e2m1 * sf) * scale) -- the first product exact, one fp32 rounding
-// for the per-tensor scale, one bf16 rounding.
-template <bool kWide>
+// Read-back: the same thread-per-groups decomposition; each group's 8 data
+// bytes and scale byte become 16 bf16 values bf16_rn((e2m1 * sf) * scale) --
+// the first product exact, one fp32 rounding for the per-tensor scale, one
+// bf16 rounding.
+template <bool kWide, int kGpt>
 __global__ void __launch_bounds__(kThreads) dequant_nvfp4_per_head_kernel(const PerHeadArgs a) {
-  const uint32_t idx = blockIdx.x * kThreads + threadIdx.x;
-  const uint32_t t = a.unit_div.div(idx);
-  if (t >= a.num_tokens) return;
-  const uint32_t u = idx - t * a.unit_div.d;
-  const uint32_t side = a.side_div.div(u);
-  const uint32_t r = u - side * a.side_div.d;
-  const uint32_t h = a.head_div.div(r);
-  const uint32_t g = r - h * a.head_div.d;
-
-  const int64_t slot = __ldg(a.slot_mapping + t);
+  Unit u;
+  if (!unit_of<kGpt>(a, u)) return;
+  const int64_t slot = __ldg(a.slot_mapping + u.t);
   if (slot < 0) return;
   if (slot >= a.num_slots) {
-    if (side == 0 && h == 0 && g == 0) report(a.status, KVQ_STATUS_BAD_INDEX);
+    if (u.side == 0 && u.h == 0 && u.g0 == 0) report(a.status, KVQ_STATUS_BAD_INDEX);
     return;
   }
-  const uint32_t page = a.block_div.div(static_cast<uint32_t>(slot));
-  const uint32_t off = static_cast<uint32_t>(slot) - page * static_cast<uint32_t>(a.block_size);
+  int64_t row;
+  const uint8_t* base = a.cache + side_base(a, slot, u.side, u.h, row);
   const int64_t data_dim = a.head_size / 2;
   const int64_t scale_dim = a.head_size / kGroup;
-  const int64_t region = static_cast<int64_t>(a.block_size) * a.num_heads * (data_dim + scale_dim);
-  const uint8_t* base = a.cache + (static_cast<int64_t>(page) * 2 + side) * region;
-  const int64_t row = static_cast<int64_t>(off) * a.num_heads + h;
-  const uint2 q = ld_stream8(base + row * data_dim + 8 * g);
-  const float sf = e4m3_to_float(
-      ld_byte(base + static_cast<int64_t>(a.block_size) * a.num_heads * data_dim + row * scale_dim + g));
-  const float scale = __ldg(side ? a.v_scale : a.k_scale);
-
-  uint32_t o[8];
+  const uint8_t* data = base + row * data_dim + 8 * u.g0;
+  const uint8_t* scales = base + static_cast<int64_t>(a.block_size) * a.num_heads * data_dim + row * scale_dim + u.g0;
+  uint2 q[kGpt];
+  uint32_t sfb[kGpt];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t byte = (i < 4 ? q.x : q.y) >> (8 * (i & 3));
-    const float2 v = __half22float2(e2m1x2_to_half2(byte));
-    o[i] = pack_bf16x2(__fmul_rn(v.x * sf, scale), __fmul_rn(v.y * sf, scale));
+  for (int j = 0; j < kGpt; ++j) {
+    q[j] = ld_stream8(data + 8 * j);
+    sfb[j] = ld_byte(scales + j);
   }
-  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(const_cast<void*>(side ? a.value : a.key)) +
-                       static_cast<int64_t>(t) * (side ? a.value_stride_t : a.key_stride_t) +
-                       static_cast<int64_t>(h) * (side ? a.value_stride_h : a.key_stride_h) + g * kGroup;
-  store32<kWide>(dst, make_uint4(o[0], o[1], o[2], o[3]), make_uint4(o[4], o[5], o[6], o[7]));
+  const float scale = __ldg(u.side ? a.v_scale : a.k_scale);
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(const_cast<void*>(u.side ? a.value : a.key)) +
+                       static_cast<int64_t>(u.t) * (u.side ? a.value_stride_t : a.key_stride_t) +
+                       static_cast<int64_t>(u.h) * (u.side ? a.value_stride_h : a.key_stride_h) +
+                       u.g0 * kGroup;
+#pragma unroll
+  for (int j = 0; j < kGpt; ++j) {
+    const float sf = e4m3_to_float(sfb[j]);
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t byte = (i < 4 ? q[j].x : q[j].y) >> (8 * (i & 3));
+      const float2 v = __half22float2(e2m1x2_to_half2(byte));
+      o[i] = pack_bf16x2(__fmul_rn(v.x * sf, scale), __fmul_rn(v.y * sf, scale));
+    }
+    store32<kWide>(dst + j * kGroup, make_uint4(o[0], o[1], o[2], o[3]), make_uint4(o[4], o[5], o[6], o[7]));
+  }
 }
 
 // key / value rows whose 16-value groups all start on 32-byte boundaries.
@@ -121,22 +152,43 @@ bool wide_rows(const PerHeadArgs& a) {
          (a.value_stride_t * 2) % 32 == 0 && (a.value_stride_h * 2) % 32 == 0;
 }
 
-}  // namespace
-
-cudaError_t launch_dequant_nvfp4_per_head(const PerHeadArgs& a, cudaStream_t stream) {
-  const int64_t threads = a.num_tokens * 2 * a.num_heads * (a.head_size / kGroup);
-  const int64_t blocks = (threads + kThreads - 1) / kThreads;
-  (wide_rows(a) ? dequant_nvfp4_per_head_kernel<true> : dequant_nvfp4_per_head_kernel<false>)
-      <<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(a);
+// Groups per thread: 4 when a head's groups split into fours (more bytes in
+// flight per thread), else 2, else 1.  Sets the index dividers for it.
+template <template <bool, int> class K>
+cudaError_t launch_per_head(PerHeadArgs a, cudaStream_t stream) {
+  const int groups = a.head_size / kGroup;
+  const int gpt = groups % 4 == 0 ? 4 : (groups % 2 == 0 ? 2 : 1);
+  const uint32_t per_head = static_cast<uint32_t>(groups / gpt);
+  a.head_div = FastDiv::make(per_head);
+  a.side_div = FastDiv::make(per_head * static_cast<uint32_t>(a.num_heads));
+  a.unit_div = FastDiv::make(2 * per_head * static_cast<uint32_t>(a.num_heads));
+  const int64_t threads = a.num_tokens * a.unit_div.d;
+  const unsigned blocks = static_cast<unsigned>((threads + kThreads - 1) / kThreads);
+  const bool wide = wide_rows(a);
+  void (*kernel)(PerHeadArgs) =
+      gpt == 4 ? (wide ? K<true, 4>::fn : K<false, 4>::fn)
+               : gpt == 2 ? (wide ? K<true, 2>::fn : K<false, 2>::fn) : (wide ? K<true, 1>::fn : K<false, 1>::fn);
+  kernel<<<blocks, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
+template <bool W, int G>
+struct WriteK {
+  static constexpr void (*fn)(PerHeadArgs) = reshape_and_cache_nvfp4_kernel<W, G>;
+};
+template <bool W, int G>
+struct ReadK {
+  static constexpr void (*fn)(PerHeadArgs) = dequant_nvfp4_per_head_kernel<W, G>;
+};
+
+}  // namespace
+
 cudaError_t launch_reshape_and_cache_nvfp4(const PerHeadArgs& a, cudaStream_t stream) {
-  const int64_t threads = a.num_tokens * 2 * a.num_heads * (a.head_size / kGroup);
-  const int64_t blocks = (threads + kThreads - 1) / kThreads;
-  (wide_rows(a) ? reshape_and_cache_nvfp4_kernel<true> : reshape_and_cache_nvfp4_kernel<false>)
-      <<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_per_head<WriteK>(a, stream);
+}
+
+cudaError_t launch_dequant_nvfp4_per_head(const PerHeadArgs& a, cudaStream_t stream) {
+  return launch_per_head<ReadK>(a, stream);
 }
 
 }  // namespace kvq

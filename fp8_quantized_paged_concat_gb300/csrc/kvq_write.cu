@@ -31,6 +31,7 @@ namespace {
 constexpr int kWarpsPerBlock = KVQ_WRITE_WARPS_PER_BLOCK;
 constexpr int kTokensPerWarp = KVQ_WRITE_TOKENS_PER_WARP;
 constexpr int64_t kSmallBatch = KVQ_WRITE_SMALL_BATCH;
+constexpr int kSmallMinBlocks = 16;       // one token per warp: a decode batch in one wave
 constexpr int kMinBlocks = KVQ_WRITE_MIN_BLOCKS;
 
 // The 8 packed bf16 pairs of one lane's 16 NoPE values, as fp32.
@@ -66,7 +67,7 @@ __device__ __forceinline__ uint8_t* entry_of(int64_t slot, const WriteArgs& a) {
 // nvfp4_ds_mla: 352-byte entries
 // ---------------------------------------------------------------------------
 template <bool kWide, int kTokensPerWarp>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32, kMinBlocks)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, kTokensPerWarp == 1 ? kSmallMinBlocks : kMinBlocks)
 write_nvfp4_ds_mla_kernel(const WriteArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t t0 =
@@ -123,7 +124,7 @@ write_nvfp4_ds_mla_kernel(const WriteArgs a) {
 // fp8_ds_mla: 656-byte entries
 // ---------------------------------------------------------------------------
 template <bool kWide, int kTokensPerWarp>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32, kMinBlocks)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, kTokensPerWarp == 1 ? kSmallMinBlocks : kMinBlocks)
 write_fp8_ds_mla_kernel(const WriteArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t t0 =
