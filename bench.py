@@ -326,56 +326,94 @@ def time_e2e(step: GpuStep, K: int):
     return ms, h2d, d2h
 
 
-def time_extra(step: GpuStep, reps: int = 10):
-    """Kernels measured outside the step: the decode-step write (8192 tokens,
-    L2 flushed before each launch) and the fp8_ds_mla cache fill."""
-    kvq = step.kvq
-    d = wl.decode_write(step.device)
-    cache2 = torch.zeros((d.num_blocks, d.block_size, 352), dtype=torch.uint8, device=step.device)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=step.device)
-    f4 = step.g4.fill
-    # per-head read-back of the step's per-head cache at the step's slots
-    ph = step.ph
-    ko, vo = torch.empty_like(ph.key), torch.empty_like(ph.value)
-    T, H, D = ph.key.shape
-    # sparse-decode index conversion: 4096 decode tokens x 2048 positions over
-    # 64 requests of 4k-32k tokens (synthetic sizes), 10 % unused entries
+def graph_replay_us(launches, reps: int = 20) -> float:
+    """Device time per launch of ``launches`` captured back to back in one
+    CUDA graph (no host launch overhead), median over ``reps`` replays."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for fn in launches:
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for fn in launches:
+            fn()
+    graph.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) / len(launches))
+    return statistics.median(times) * 1e3
+
+
+def time_extra(step: GpuStep):
+    """Kernels measured outside the step.  Small launches are timed as CUDA
+    graph replays over rotated input copies whose total exceeds L2 (no host
+    launch overhead, no warm L2); the fp8_ds_mla fill is one large launch."""
+    kvq, dev = step.kvq, step.device
+    out = {}
+
+    def record(name, us, units, nbytes, copies):
+        out[name] = {"units": units, "us": round(us, 2), "gbs": round(nbytes / us / 1e3, 1),
+                     "method": f"CUDA graph over {copies} input copies" if copies else "CUDA events"}
+
+    # decode-step write: 8192 tokens, 12 copies (144 MB of inputs + caches)
+    ds = [wl.make_write("decode", 8192, 4096, 64, 164, 1002 + 100 * i, dev, outlier_p=0.01) for i in range(12)]
+    caches = [torch.zeros((4096, 64, 352), dtype=torch.uint8, device=dev) for _ in ds]
+    us = graph_replay_us([lambda d=d, c=c: kvq.kvq_write_nvfp4_ds_mla(d.kv_c, d.k_pe, c, d.slot_mapping)
+                          for d, c in zip(ds, caches)])
+    valid = int((ds[0].slot_mapping >= 0).sum())
+    record("write_nvfp4_ds_mla decode T=8192", us, 8192, BYTES_WRITE_NVFP4 * valid + 8 * (8192 - valid), 12)
+    del ds, caches
+    # per-head write and read-back: 16384 tokens x 8 heads x 128, 4 copies
+    T, H, D = step.ph.key.shape
+    phs = [wl.make_per_head("per-head", 16384, 8, 128, 16384, 16, 0, 1005 + 7 * i, dev) for i in range(4)]
+    phcs = [torch.zeros((16384, 2, 16, 8, kvq.nvfp4_full_dim(128)), dtype=torch.uint8, device=dev) for _ in phs]
+    us = graph_replay_us([lambda p=p, c=c: kvq.kvq_reshape_and_cache_nvfp4(p.key, p.value, c, p.slot_mapping,
+                                                                           step.ks, step.vs) for p, c in zip(phs, phcs)])
+    record("reshape_and_cache_nvfp4 T=16384 H=8 D=128", us, T, per_head_bytes_per_token(H, D) * T, 4)
+    outs = [(torch.empty_like(p.key), torch.empty_like(p.value)) for p in phs]
+    us = graph_replay_us([lambda p=p, c=c, o=o: kvq.kvq_dequant_nvfp4_per_head(c, p.slot_mapping, step.ks, step.vs,
+                                                                               o[0], o[1])
+                          for p, c, o in zip(phs, phcs, outs)])
+    record("dequant_nvfp4_per_head T=16384 H=8 D=128", us, T, per_head_bytes_per_token(H, D) * T, 4)
+    del phs, phcs, outs
+    # sparse-decode index conversion: 4096 decode tokens x 2048 positions over 64
+    # requests of 4k-32k tokens (synthetic sizes), 10 % unused entries, 3 copies
     g = np.random.Generator(np.random.PCG64(4001))
     lens = g.integers(4096, 32768, 64, endpoint=True)
-    table, _, _, _ = wl.make_gather_batch(65536, 64, lens, [0] * 64, 4001)
-    req = g.integers(0, 64, 4096).astype(np.int32)
-    idx = (g.random((4096, 2048)) * lens[req][:, None]).astype(np.int32)
-    idx[g.random((4096, 2048)) < 0.1] = -1
-    req_d, idx_d, table_d = (torch.from_numpy(x).to(step.device) for x in (req, idx, table))
-    slots_d = torch.empty_like(idx_d)
-    out = {}
-    for name, fn, units, nbytes, flush_l2 in (
-            ("dequant_nvfp4_per_head T=16384 H=8 D=128", lambda: kvq.kvq_dequant_nvfp4_per_head(
-                step.phc, ph.slot_mapping, step.ks, step.vs, ko, vo), T,
-             per_head_bytes_per_token(H, D) * T, True),
-            ("req_index_to_global_slot 4096 x 2048", lambda: kvq.kvq_req_index_to_global_slot(
-                req_d, idx_d, table_d, 64, 65536, out=slots_d), idx.size, 8 * idx.size + 4 * 4096, True),
-            ("write_nvfp4_ds_mla decode T=8192", lambda: kvq.kvq_write_nvfp4_ds_mla(
-                d.kv_c, d.k_pe, cache2, d.slot_mapping), d.num_tokens,
-             BYTES_WRITE_NVFP4 * int((d.slot_mapping >= 0).sum()) + 8 * int((d.slot_mapping < 0).sum()), True),
-            ("write_fp8_ds_mla fill 2,097,152 tok", lambda: kvq.kvq_write_fp8_ds_mla(
-                f4.kv_c, f4.k_pe, step.cache4, f4.slot_mapping), f4.num_tokens,
-             BYTES_WRITE_FP8 * f4.num_tokens, False)):
-        times = []
-        for r in range(reps + 3):
-            if flush_l2:
-                flush.fill_(r & 0xFF)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            torch.cuda.synchronize()
-            if r >= 3:
-                times.append(a.elapsed_time(b))
-        ms = statistics.median(times)
-        out[name] = {"units": units, "us": round(ms * 1e3, 2), "gbs": round(nbytes / ms / 1e6, 1),
-                     "l2_flushed": flush_l2}
-    del flush
+    table = torch.from_numpy(wl.make_gather_batch(65536, 64, lens, [0] * 64, 4001)[0]).to(dev)
+    sets = []
+    for _ in range(3):
+        req = g.integers(0, 64, 4096).astype(np.int32)
+        idx = (g.random((4096, 2048)) * lens[req][:, None]).astype(np.int32)
+        idx[g.random((4096, 2048)) < 0.1] = -1
+        sets.append((torch.from_numpy(req).to(dev), torch.from_numpy(idx).to(dev),
+                     torch.empty((4096, 2048), dtype=torch.int32, device=dev)))
+    us = graph_replay_us([lambda r=r, i=i, o=o: kvq.kvq_req_index_to_global_slot(r, i, table, 64, 65536, out=o)
+                          for r, i, o in sets])
+    record("req_index_to_global_slot 4096 x 2048", us, 4096 * 2048, 8 * 4096 * 2048 + 4 * 4096, 3)
+    del sets
+    # fp8_ds_mla cache fill: 2,097,152 tokens, one launch
+    f4 = step.g4.fill
+    times = []
+    for r in range(13):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        kvq.kvq_write_fp8_ds_mla(f4.kv_c, f4.k_pe, step.cache4, f4.slot_mapping)
+        b.record()
+        torch.cuda.synchronize()
+        if r >= 3:
+            times.append(a.elapsed_time(b))
+    record("write_fp8_ds_mla fill 2,097,152 tok", statistics.median(times) * 1e3, f4.num_tokens,
+           BYTES_WRITE_FP8 * f4.num_tokens, 0)
     return out
 
 

@@ -73,17 +73,27 @@ __global__ void __launch_bounds__(kThreads) reshape_and_cache_nvfp4_kernel(const
   const int64_t scale_dim = a.head_size / kGroup;
   uint8_t* data = base + row * data_dim + 8 * u.g0;
   uint8_t* scales = base + static_cast<int64_t>(a.block_size) * a.num_heads * data_dim + row * scale_dim + u.g0;
+  // y = x * inv_scale.  amax(|y|) = RN(amax(|x|) * |inv_scale|) exactly, since
+  // rounding is monotone, so the maximum is taken on the packed bf16 pairs;
+  // when the per-tensor scale is 1 (warp-uniform), y = x needs no multiply.
+  const bool unit_scale = inv_scale == 1.0f;
   uint32_t sf_word = 0;
 #pragma unroll
   for (int j = 0; j < kGpt; ++j) {
     const uint32_t w[8] = {lo[j].x, lo[j].y, lo[j].z, lo[j].w, hi[j].x, hi[j].y, hi[j].z, hi[j].w};
+    __nv_bfloat162 m = __hmax2(__hmax2(abs_bf16x2(w[0]), abs_bf16x2(w[1])), __hmax2(abs_bf16x2(w[2]), abs_bf16x2(w[3])));
+    m = __hmax2(m, __hmax2(__hmax2(abs_bf16x2(w[4]), abs_bf16x2(w[5])), __hmax2(abs_bf16x2(w[6]), abs_bf16x2(w[7]))));
+    float amax = fmaxf(__low2float(m), __high2float(m));
     float y[16];
-    float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      y[2 * i] = __fmul_rn(bf16_lo(w[i]), inv_scale);
-      y[2 * i + 1] = __fmul_rn(bf16_hi(w[i]), inv_scale);
-      amax = fmaxf(amax, fmaxf(fabsf(y[2 * i]), fabsf(y[2 * i + 1])));
+      y[2 * i] = bf16_lo(w[i]);
+      y[2 * i + 1] = bf16_hi(w[i]);
+    }
+    if (!unit_scale) {
+      amax = __fmul_rn(amax, fabsf(inv_scale));
+#pragma unroll
+      for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(y[i], inv_scale);
     }
     const uint32_t sf = nvfp4_scale_code(amax);
     st8(data + 8 * j, nvfp4_pack16(y, nvfp4_inverse_scale(sf)));

@@ -393,6 +393,21 @@ def test_per_head_parity(kvq, oracle_mod, name, make, kw):
     run_per_head(kvq, oracle_mod, make(), **kw)
 
 
+@pytest.mark.parametrize("k_scale,v_scale", [(1.0, 1.0), (0.75, 3.0), (2.0 ** -20, 2.0 ** 20)])
+def test_per_head_parity_extreme_values(kvq, oracle_mod, k_scale, v_scale):
+    """Random finite bf16 bit patterns (subnormals, zeros, values up to the bf16
+    maximum, so x / scale can overflow to infinity) and zero groups."""
+    T, H, D = 64, 4, 64
+    kb = finite_bf16_bits((T, H, D), 151)
+    vb = finite_bf16_bits((T, H, D), 152)
+    kb[3] = 0
+    vb[4] = 0x8000
+    slots = wl.slot_mapping(T, 16 * 8, 5, 153)
+    w = wl.PerHeadWorkload("extreme", bits_to_bf16(kb), bits_to_bf16(vb), torch.from_numpy(slots), 8, 16,
+                           k_scale, v_scale)
+    run_per_head(kvq, oracle_mod, w)
+
+
 def test_per_head_out_of_range_slots(kvq, oracle_mod):
     w = wl.make_per_head("oob", 40, 8, 128, 4, 16, 2, 106)
     s = wl.host(w.slot_mapping).copy()
