@@ -528,3 +528,52 @@ def test_index_conversion_rejects_length_mismatch(kvq):
     with pytest.raises(RuntimeError, match="req_id has 13 entries"):
         kvq.kvq_req_index_to_global_slot(dev(np.concatenate([req, [0]]).astype(np.int32)), dev(idx),
                                          dev(table), 16, 8)
+
+
+# --------------------------------------------------------------------------
+# stream capture: the entry points allocate nothing and never synchronise,
+# so a sequence of them can be captured in a CUDA graph and replayed
+# --------------------------------------------------------------------------
+
+def test_entry_points_replay_from_a_cuda_graph(kvq):
+    g = wl.smoke_gather(DEV)
+    f = g.fill
+    ph = wl.make_per_head("graph", 64, 8, 128, 16, 16, 3, 161, DEV, k_scale=0.5)
+    ks = torch.tensor([ph.k_scale], device=DEV)
+    vs = torch.tensor([ph.v_scale], device=DEV)
+
+    def run(c352, c656, ws352, ws656, phc, ko, vo):
+        kvq.kvq_write_nvfp4_ds_mla(f.kv_c, f.k_pe, c352, f.slot_mapping)
+        kvq.kvq_write_fp8_ds_mla(f.kv_c, f.k_pe, c656, f.slot_mapping)
+        kvq.kvq_gather_upconvert_nvfp4_ds_mla(c352, ws352, g.block_table, g.workspace_starts, g.seq_starts)
+        kvq.kvq_gather_upconvert_fp8_ds_mla(c656, ws656, g.block_table, g.workspace_starts, g.seq_starts)
+        kvq.kvq_reshape_and_cache_nvfp4(ph.key, ph.value, phc, ph.slot_mapping, ks, vs)
+        kvq.kvq_dequant_nvfp4_per_head(phc, ph.slot_mapping, ks, vs, ko, vo)
+
+    def buffers():
+        return (torch.zeros((8, 64, 352), dtype=torch.uint8, device=DEV),
+                torch.zeros((8, 64, 656), dtype=torch.uint8, device=DEV),
+                torch.zeros((g.num_out_tokens, 576), dtype=torch.bfloat16, device=DEV),
+                torch.zeros((g.num_out_tokens, 576), dtype=torch.bfloat16, device=DEV),
+                torch.zeros((16, 2, 16, 8, 72), dtype=torch.uint8, device=DEV),
+                torch.zeros_like(ph.key), torch.zeros_like(ph.value))
+
+    direct = buffers()
+    run(*direct)
+    captured = buffers()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run(*captured)                      # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(side)
+    for t in captured:
+        t.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run(*captured)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(direct, captured):
+        assert torch.equal(a.view(torch.uint8) if a.dtype == torch.uint8 else a.view(torch.int16),
+                           b.view(torch.uint8) if b.dtype == torch.uint8 else b.view(torch.int16))
