@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+import independent as ind
 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -170,6 +171,29 @@ def test_write_parity_extreme_values(kvq, oracle_mod, entry):
     slots = wl.slot_mapping(T, 8 * 64, 7, 73)
     w = wl.WriteWorkload("extreme", bits_to_bf16(kv), bits_to_bf16(pe), torch.from_numpy(slots), 8, 64, entry)
     run_write(kvq, oracle_mod, w, entry)
+
+
+@pytest.mark.parametrize("base", [1.0, 1.5, 2.0 ** -7, 1.25 * 2.0 ** 9, 2.0 ** -100])
+def test_fp8_write_quotients_on_e4m3_ties(kvq, oracle_mod, base):
+    """fp8_ds_mla tiles whose values divide by the tile scale exactly onto
+    e4m3 rounding ties (and exact codes): the quotient must be the exact one
+    for round-to-nearest-even to pick the even code."""
+    g = np.random.Generator(np.random.PCG64(171))
+    mags = ind.e4m3_table()[:127]
+    mids = (mags[:-1] + mags[1:]) / 2
+    T = 48
+    x = np.zeros((T, 512))
+    for t in range(T):
+        for j in range(4):
+            vals = g.choice(np.concatenate([mids, mags]), 128) * g.choice([-1.0, 1.0], 128)
+            vals[g.integers(0, 128)] = 448.0            # sets amax = 448 * base, so s = base
+            x[t, 128 * j:128 * (j + 1)] = vals * base
+    xb = ind.torch_bf16_bits(torch.from_numpy(x.astype(np.float32)))
+    assert np.array_equal(ind.bf16_to_f32(xb).astype(np.float64), x)     # exact in bf16
+    pe = finite_bf16_bits((T, 64), 172)
+    w = wl.WriteWorkload("ties", bits_to_bf16(xb), bits_to_bf16(pe),
+                         torch.from_numpy(np.arange(T, dtype=np.int64)), 1, 64, 656)
+    run_write(kvq, oracle_mod, w, 656)
 
 
 @pytest.mark.parametrize("entry", [352, 656])
