@@ -61,11 +61,13 @@ __device__ __forceinline__ float amax16(const uint4& a, const uint4& b) {
 // RN(q0 + remainder * inv_s) is the correctly rounded quotient.  The theorem
 // assumes no underflow; quotients here are at most 448 in magnitude, and any
 // quotient in the subnormal range encodes to an e4m3 zero of the same sign
-// whichever of its neighbours is returned.
+// whichever of its neighbours is returned.  s > 0, so the quotient has the
+// sign of x; copying it back keeps -0 / s = -0, which the correction (a
+// +0 remainder added to -0) would turn into +0.
 __device__ __forceinline__ float quotient(float x, float s, float inv_s) {
   const float q0 = __fmul_rn(x, inv_s);
   const float rem = __fmaf_rn(-q0, s, x);
-  return __fmaf_rn(rem, inv_s, q0);
+  return copysignf(__fmaf_rn(rem, inv_s, q0), x);
 }
 
 // Slot -> entry pointer, or nullptr for padding / out-of-range slots.  Slots
