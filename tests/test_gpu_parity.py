@@ -173,7 +173,7 @@ def test_write_parity_extreme_values(kvq, oracle_mod, entry):
     run_write(kvq, oracle_mod, w, entry)
 
 
-@pytest.mark.parametrize("base", [1.0, 1.5, 2.0 ** -7, 1.25 * 2.0 ** 9, 2.0 ** -100])
+@pytest.mark.parametrize("base", [1.0, 1.5, 2.0 ** -7, 1.25 * 2.0 ** 9, 2.0 ** -64, 1.5 * 2.0 ** -65, 2.0 ** -100])
 def test_fp8_write_quotients_on_e4m3_ties(kvq, oracle_mod, base):
     """fp8_ds_mla tiles whose values divide by the tile scale exactly onto
     e4m3 rounding ties (and exact codes): the quotient must be the exact one
