@@ -53,27 +53,6 @@ __device__ __forceinline__ float amax16(const uint4& a, const uint4& b) {
   return fmaxf(__low2float(m), __high2float(m));
 }
 
-// x / s rounded to nearest even, from the correctly rounded reciprocal
-// inv_s = RN(1/s), by Markstein's correction (P. Markstein, "Computation of
-// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
-// Dev. 34(1), 1990): q0 = RN(x * inv_s) is within an ulp of x / s, the
-// remainder x - q0 * s is then exact in one fused multiply-add, and
-// RN(q0 + remainder * inv_s) is the correctly rounded quotient.  The theorem
-// assumes no overflow or underflow in its intermediates, so it is used only
-// for tile scales s >= 2^-64: 1/s stays finite, and for every quotient that
-// can round to a nonzero e4m3 code (|x / s| >= 2^-11) the remainder is a
-// multiple of at least 2^-122, exactly representable.  Smaller quotients
-// encode to an e4m3 zero of the sign of x whichever neighbour is returned,
-// and smaller scales use IEEE division.  s > 0, so the quotient has the sign
-// of x; copying it back keeps -0 / s = -0, which the correction (a +0
-// remainder added to -0) would turn into +0.
-__device__ __forceinline__ float quotient(float x, float s, float inv_s, bool fast) {
-  if (!fast) return __fdiv_rn(x, s);
-  const float q0 = __fmul_rn(x, inv_s);
-  const float rem = __fmaf_rn(-q0, s, x);
-  return copysignf(__fmaf_rn(rem, inv_s, q0), x);
-}
-
 // Slot -> entry pointer, or nullptr for padding / out-of-range slots.  Slots
 // in range are below 2^32 (checked on the host), so 32-bit division applies.
 __device__ __forceinline__ uint8_t* entry_of(int64_t slot, const WriteArgs& a) {
@@ -180,15 +159,13 @@ write_fp8_ds_mla_kernel(const WriteArgs a) {
     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
     const float s = amax == 0.0f ? 1.0f : amax / 448.0f;
-    const float inv_s = 1.0f / s;                      // correctly rounded reciprocal
-    const bool fast = s >= 0x1p-64f;
     float x[16];
     unpack16(na[j], nb[j], x);
     uint32_t q[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      q[k] = cvt_e4m3x2(quotient(x[4 * k], s, inv_s, fast), quotient(x[4 * k + 1], s, inv_s, fast)) |
-             (cvt_e4m3x2(quotient(x[4 * k + 2], s, inv_s, fast), quotient(x[4 * k + 3], s, inv_s, fast)) << 16);
+      q[k] = cvt_e4m3x2(__fdiv_rn(x[4 * k], s), __fdiv_rn(x[4 * k + 1], s)) |
+             (cvt_e4m3x2(__fdiv_rn(x[4 * k + 2], s), __fdiv_rn(x[4 * k + 3], s)) << 16);
     }
     st16(entry[j] + 16 * lane, make_uint4(q[0], q[1], q[2], q[3]));
     if ((lane & 7) == 0) st4(entry[j] + kF8ScaleOff + 4 * (lane >> 3), __float_as_uint(s));
