@@ -152,9 +152,6 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 __device__ __forceinline__ uint2 ld_stream8(const void* p) {
   return __ldcs(reinterpret_cast<const uint2*>(p));
 }
-__device__ __forceinline__ uint32_t ld_stream4(const void* p) {
-  return __ldcs(reinterpret_cast<const unsigned int*>(p));
-}
 __device__ __forceinline__ uint32_t ld_byte(const uint8_t* p) {
   return __ldg(p);
 }

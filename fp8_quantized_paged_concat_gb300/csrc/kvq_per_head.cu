@@ -14,7 +14,14 @@
 namespace kvq {
 namespace {
 
-constexpr int kThreads = 256;
+#ifndef KVQ_PER_HEAD_THREADS
+#define KVQ_PER_HEAD_THREADS 256
+#endif
+#ifndef KVQ_PER_HEAD_MAX_GROUPS
+#define KVQ_PER_HEAD_MAX_GROUPS 4      // 16-value groups per thread, at most
+#endif
+constexpr int kThreads = KVQ_PER_HEAD_THREADS;
+constexpr int kMaxGpt = KVQ_PER_HEAD_MAX_GROUPS;
 
 // A thread owns kGpt consecutive 16-value groups of one (token, side, head):
 // flat index = ((t * 2 + side) * H + h) * (groups / kGpt) + u, with
@@ -167,7 +174,7 @@ bool wide_rows(const PerHeadArgs& a) {
 template <template <bool, int> class K>
 cudaError_t launch_per_head(PerHeadArgs a, cudaStream_t stream) {
   const int groups = a.head_size / kGroup;
-  const int gpt = groups % 4 == 0 ? 4 : (groups % 2 == 0 ? 2 : 1);
+  const int gpt = (kMaxGpt >= 4 && groups % 4 == 0) ? 4 : ((kMaxGpt >= 2 && groups % 2 == 0) ? 2 : 1);
   const uint32_t per_head = static_cast<uint32_t>(groups / gpt);
   a.head_div = FastDiv::make(per_head);
   a.side_div = FastDiv::make(per_head * static_cast<uint32_t>(a.num_heads));

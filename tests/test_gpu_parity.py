@@ -53,47 +53,27 @@ def bits_to_bf16(bits):
 # device converters, exhaustively over the exponent window that matters
 # --------------------------------------------------------------------------
 
-def sweep_ranges():
-    """(first_bits, count) pieces: every pattern with |f| in [2^-12, 2^10),
-    both signs (the window where e4m3 and e2m1 rounding decisions happen)."""
-    lo = int(np.float32(2.0 ** -12).view(np.uint32))
-    hi = int(np.float32(2.0 ** 10).view(np.uint32))
-    return [(lo, hi - lo), (lo | 0x80000000, hi - lo)]
-
-
-def test_device_converters_match_oracle_in_rounding_window(kvq, oracle_mod, threads):
+def test_device_converters_match_oracle_exhaustively(kvq, oracle_mod, threads):
+    """All 2^32 float32 bit patterns through the device e4m3 / e2m1 / bf16
+    converters (both lanes of the packed conversions) against the oracle.
+    NaN inputs are outside the ops' contract; e4m3 must keep them NaN."""
     chunk = 1 << 26
-    for first, count in sweep_ranges():
-        for s in range(0, count, chunk):
-            f0, n = first + s, min(chunk, count - s)
-            e4l, e4h, e2l, e2h, bf = (t.cpu().numpy() for t in kvq.kvq_selftest_convert(f0, n))
-            o4, o2 = oracle_mod.encode_bits_range(f0, n, threads=threads)
-            ob = oracle_mod.bf16_rn_bits_range(f0, n, threads=threads)
-            np.testing.assert_array_equal(e4l, o4)
-            np.testing.assert_array_equal(e4h, o4)
-            np.testing.assert_array_equal(e2l, o2)
-            np.testing.assert_array_equal(e2h, o2)
-            np.testing.assert_array_equal(bf.view(np.uint16), ob)
-
-
-def test_device_converters_strided_full_range(kvq, oracle_mod, threads):
-    """Every 509th float32 pattern of all 2^32 (zeros, subnormals,
-    saturation, infinities); NaN inputs only have to stay NaN in e4m3."""
-    chunk, stride = 1 << 28, 509
     for first in range(0, 1 << 32, chunk):
-        e4l, e4h, e2l, e2h, bf = kvq.kvq_selftest_convert(first, chunk)
-        off = (-first) % stride
-        idx = torch.arange(off, chunk, stride, device=DEV)
-        got = [t[idx].cpu().numpy() for t in (e4l, e4h, e2l, e2h, bf)]
-        del e4l, e4h, e2l, e2h, bf
-        bits = (first + idx.cpu().numpy()).astype(np.uint32)
-        f = bits.view(np.float32)
-        keep = ~np.isnan(f)
-        o4, o2, ob = oracle_mod.e4m3_rn_sat(f), oracle_mod.e2m1_rn_sat(f), oracle_mod.bf16_rn(f)
-        for g, o in ((got[0], o4), (got[1], o4), (got[2], o2), (got[3], o2),
-                     (got[4].view(np.uint16), ob)):
-            np.testing.assert_array_equal(g[keep], o[keep])
-        assert np.all((got[0][~keep] & 0x7F) == 0x7F)
+        e4l, e4h, e2l, e2h, bf = (t.cpu().numpy() for t in kvq.kvq_selftest_convert(first, chunk))
+        o4, o2 = oracle_mod.encode_bits_range(first, chunk, threads=threads)
+        ob = oracle_mod.bf16_rn_bits_range(first, chunk, threads=threads)
+        f = np.arange(first, first + chunk, dtype=np.uint64).astype(np.uint32).view(np.float32)
+        nan = np.isnan(f)
+        if not nan.any():
+            ok = (np.array_equal(e4l, o4) and np.array_equal(e4h, o4) and np.array_equal(e2l, o2)
+                  and np.array_equal(e2h, o2) and np.array_equal(bf.view(np.uint16), ob))
+        else:
+            keep = ~nan
+            ok = (np.array_equal(e4l[keep], o4[keep]) and np.array_equal(e4h[keep], o4[keep])
+                  and np.array_equal(e2l[keep], o2[keep]) and np.array_equal(e2h[keep], o2[keep])
+                  and np.array_equal(bf.view(np.uint16)[keep], ob[keep])
+                  and np.all((e4l[nan] & 0x7F) == 0x7F) and np.all((e4h[nan] & 0x7F) == 0x7F))
+        assert ok, f"converter mismatch in patterns [{first:#x}, {first + chunk:#x})"
 
 
 # --------------------------------------------------------------------------
