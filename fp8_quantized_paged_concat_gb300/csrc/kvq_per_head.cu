@@ -2,10 +2,11 @@
 // [num_pages, 2, block_size, H, full_dim] whose side regions hold
 // [data [block_size][H][D/2] | scales [block_size][H][D/16]].
 //
-// Design (GB300): one thread per 4 consecutive 16-value groups of one
-// (token, side, head) (2 or 1 when a head's group count is not a multiple of
-// 4): it issues its 4 x 32-byte loads first, forms each group's scale and
-// writes 8 data bytes per group and the groups' scale bytes in one store.
+// Design (GB300): one thread per 2 consecutive 16-value groups of one
+// (token, side, head) (1 when a head's group count is odd; up to 4 with
+// KVQ_PER_HEAD_MAX_GROUPS): it issues its 32-byte loads first, forms each
+// group's scale and writes 8 data bytes per group and the groups' scale
+// bytes in one store.  128-thread CTAs (measured best with 2 groups).
 // Threads are numbered fastest within a head, then heads, then sides, so a
 // warp covers whole heads of one token side and its stores are contiguous.
 #include "kvq_device.cuh"
@@ -15,10 +16,10 @@ namespace kvq {
 namespace {
 
 #ifndef KVQ_PER_HEAD_THREADS
-#define KVQ_PER_HEAD_THREADS 256
+#define KVQ_PER_HEAD_THREADS 128
 #endif
 #ifndef KVQ_PER_HEAD_MAX_GROUPS
-#define KVQ_PER_HEAD_MAX_GROUPS 4      // 16-value groups per thread, at most
+#define KVQ_PER_HEAD_MAX_GROUPS 2      // 16-value groups per thread, at most
 #endif
 constexpr int kThreads = KVQ_PER_HEAD_THREADS;
 constexpr int kMaxGpt = KVQ_PER_HEAD_MAX_GROUPS;
@@ -169,8 +170,8 @@ bool wide_rows(const PerHeadArgs& a) {
          (a.value_stride_t * 2) % 32 == 0 && (a.value_stride_h * 2) % 32 == 0;
 }
 
-// Groups per thread: 4 when a head's groups split into fours (more bytes in
-// flight per thread), else 2, else 1.  Sets the index dividers for it.
+// Groups per thread: the largest of kMaxGpt, 2, 1 that divides a head's group
+// count.  Sets the index dividers for it.
 template <template <bool, int> class K>
 cudaError_t launch_per_head(PerHeadArgs a, cudaStream_t stream) {
   const int groups = a.head_size / kGroup;
