@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(kThreads) reshape_and_cache_nvfp4_kernel(const
   // when the per-tensor scale is 1 (warp-uniform), y = x needs no multiply.
   const bool unit_scale = inv_scale == 1.0f;
   uint32_t sf_word = 0;
+  uint2 packed[kGpt];
 #pragma unroll
   for (int j = 0; j < kGpt; ++j) {
     const uint32_t w[8] = {lo[j].x, lo[j].y, lo[j].z, lo[j].w, hi[j].x, hi[j].y, hi[j].z, hi[j].w};
@@ -104,10 +105,19 @@ __global__ void __launch_bounds__(kThreads) reshape_and_cache_nvfp4_kernel(const
       for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(y[i], inv_scale);
     }
     const uint32_t sf = nvfp4_scale_code(amax);
-    st8(data + 8 * j, nvfp4_pack16(y, nvfp4_inverse_scale(sf)));
+    packed[j] = nvfp4_pack16(y, nvfp4_inverse_scale(sf));
     sf_word |= sf << (8 * j);
   }
-  // kGpt scale bytes, contiguous
+  // The groups' 8 * kGpt data bytes in 16-byte stores (the offset is a
+  // multiple of 8 * kGpt), so one instruction covers whole sectors across the
+  // threads of a head; then the kGpt scale bytes, contiguous.
+  if constexpr (kGpt == 1) {
+    st8(data, packed[0]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < kGpt; j += 2)
+      st16(data + 8 * j, make_uint4(packed[j].x, packed[j].y, packed[j + 1].x, packed[j + 1].y));
+  }
   if constexpr (kGpt == 4) {
     st4(scales, sf_word);
   } else if constexpr (kGpt == 2) {
@@ -139,11 +149,18 @@ __global__ void __launch_bounds__(kThreads) dequant_nvfp4_per_head_kernel(const 
   const uint8_t* scales = base + static_cast<int64_t>(a.block_size) * a.num_heads * data_dim + row * scale_dim + u.g0;
   uint2 q[kGpt];
   uint32_t sfb[kGpt];
+  if constexpr (kGpt == 1) {
+    q[0] = ld_stream8(data);
+  } else {
 #pragma unroll
-  for (int j = 0; j < kGpt; ++j) {
-    q[j] = ld_stream8(data + 8 * j);
-    sfb[j] = ld_byte(scales + j);
+    for (int j = 0; j < kGpt; j += 2) {           // 16-byte loads (offset a multiple of 16)
+      const uint4 v = ld_stream16(data + 8 * j);
+      q[j] = make_uint2(v.x, v.y);
+      q[j + 1] = make_uint2(v.z, v.w);
+    }
   }
+#pragma unroll
+  for (int j = 0; j < kGpt; ++j) sfb[j] = ld_byte(scales + j);
   const float scale = __ldg(u.side ? a.v_scale : a.k_scale);
   __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(const_cast<void*>(u.side ? a.value : a.key)) +
                        static_cast<int64_t>(u.t) * (u.side ? a.value_stride_t : a.key_stride_t) +
@@ -175,7 +192,13 @@ bool wide_rows(const PerHeadArgs& a) {
 template <template <bool, int> class K>
 cudaError_t launch_per_head(PerHeadArgs a, cudaStream_t stream) {
   const int groups = a.head_size / kGroup;
-  const int gpt = (kMaxGpt >= 4 && groups % 4 == 0) ? 4 : ((kMaxGpt >= 2 && groups % 2 == 0) ? 2 : 1);
+  // Several groups per thread move their data bytes in 16-byte accesses; that
+  // needs every (page, side) region, block_size * H * full_dim bytes, to start
+  // on a 16-byte boundary (the host check guarantees only 8).
+  const int64_t region = static_cast<int64_t>(a.block_size) * a.num_heads * (a.head_size / 2 + groups);
+  const bool pairs_ok = region % 16 == 0;
+  const int gpt = (pairs_ok && kMaxGpt >= 4 && groups % 4 == 0) ? 4
+                  : ((pairs_ok && kMaxGpt >= 2 && groups % 2 == 0) ? 2 : 1);
   const uint32_t per_head = static_cast<uint32_t>(groups / gpt);
   a.head_div = FastDiv::make(per_head);
   a.side_div = FastDiv::make(per_head * static_cast<uint32_t>(a.num_heads));

@@ -389,6 +389,7 @@ PER_HEAD_CASES = [
     ("block_size 1", lambda: wl.make_per_head("e", 50, 8, 128, 64, 1, 2, 105), {}),
     ("H3 D48 block_size 24", lambda: wl.make_per_head("f", 90, 3, 48, 12, 24, 4, 107, v_scale=1.5), {}),
     ("16-byte aligned rows", lambda: wl.make_per_head("g", 45, 4, 128, 8, 16, 2, 108), dict(narrow_rows=True)),
+    ("H1 D32 block_size 4 (8-byte aligned regions)", lambda: wl.make_per_head("h", 50, 1, 32, 40, 4, 2, 109), {}),
 ]
 
 
