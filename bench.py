@@ -672,6 +672,12 @@ def main(argv=None):
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # not started by torch.distributed.run: start one process per GPU through it
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+               "--master-addr", "127.0.0.1", "--master-port", os.environ.get("MASTER_PORT", "29517"),
+               os.path.abspath(__file__), *(sys.argv[1:] if argv is None else argv)]
+        return subprocess.call(cmd)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -178,15 +178,12 @@ kvq_status per_head_common(const char* fn, bool read_back,
               "%s: block_size * num_heads * full_dim must be a multiple of 8", fn);
   KVQ_REQUIRE(d_status == nullptr || aligned(d_status, 4), "%s: d_status misaligned", fn);
   if (kvq_status s = check_device(fn)) return s;
-  const int32_t groups = head_size / 16;
+  // the launcher sets the index dividers for the groups-per-thread it picks
   const kvq::PerHeadArgs a{key,          value,     key_stride_t, key_stride_h, value_stride_t,
                            value_stride_h, slot_mapping, num_tokens, num_heads, head_size,
                            const_cast<uint8_t*>(kv_cache), num_pages * block_size, block_size,
                            k_scale, v_scale, d_status,
-                           kvq::FastDiv::make(static_cast<uint32_t>(block_size)),
-                           kvq::FastDiv::make(static_cast<uint32_t>(2 * num_heads * groups)),
-                           kvq::FastDiv::make(static_cast<uint32_t>(num_heads * groups)),
-                           kvq::FastDiv::make(static_cast<uint32_t>(groups))};
+                           kvq::FastDiv::make(static_cast<uint32_t>(block_size)), {}, {}, {}};
   return launched(fn, launch(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -300,7 +297,7 @@ kvq_status kvq_req_index_to_global_slot(const int32_t* req_id, int64_t num_req_i
                          num_requests,  block_size,    num_blocks,           out,
                          out_stride,    d_status,
                          kvq::FastDiv::make(static_cast<uint32_t>(block_size)),
-                         kvq::FastDiv::make(static_cast<uint32_t>(topk))};
+                         {}};   // topk_div: set by the launcher for its positions per thread
   return launched(fn, kvq::launch_req_index_to_global_slot(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

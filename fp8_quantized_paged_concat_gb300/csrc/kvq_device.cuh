@@ -36,7 +36,7 @@ static_assert(kF8RopeOff + 2 * kRopeDim == kF8Entry, "656-byte entry");
 // Montgomery, "Division by Invariant Integers using Multiplication" (PLDI
 // 1994), figure 4.1.  Exact for every 32-bit n.
 struct FastDiv {
-  uint32_t d, m, s1, s2;
+  uint32_t d = 1, m = 1, s1 = 0, s2 = 0;     // default: division by 1
 
   static FastDiv make(uint32_t divisor) {
     FastDiv f;

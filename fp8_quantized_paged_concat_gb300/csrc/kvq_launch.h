@@ -61,9 +61,10 @@ struct PerHeadArgs {
   const float* v_scale;
   int32_t* status;
   FastDiv block_div;     // slot -> page
-  FastDiv unit_div;      // flat index -> token (2 * H * D/16 groups per token)
-  FastDiv side_div;      // group within token -> side (H * D/16)
-  FastDiv head_div;      // group within side -> head (D/16)
+  // Set by the launcher for the groups-per-thread g it picks:
+  FastDiv unit_div;      // flat thread index -> token (2 * H * D/16/g threads per token)
+  FastDiv side_div;      // thread within token -> side (H * D/16/g)
+  FastDiv head_div;      // thread within side -> head (D/16/g)
 };
 
 cudaError_t launch_write_nvfp4_ds_mla(const WriteArgs& a, cudaStream_t stream);

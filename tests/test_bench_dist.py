@@ -53,3 +53,19 @@ def test_warmup_below_three_is_rejected():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "2"],
                        capture_output=True, text=True, timeout=300)
     assert r.returncode != 0 and "warmup" in r.stderr
+
+
+def test_reference_arm_relaunches_itself_with_two_ranks():
+    """--gpus 2 without a launcher: bench.py starts torch.distributed.run with
+    two ranks; rank 0 alone times the oracle and prints one line."""
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    env["MASTER_PORT"] = str(free_port())
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--steps", "1", "--warmup", "3"], env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    import json
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["value"] > 0
