@@ -582,3 +582,28 @@ def test_entry_points_replay_from_a_cuda_graph(kvq):
     for a, b in zip(direct, captured):
         assert torch.equal(a.view(torch.uint8) if a.dtype == torch.uint8 else a.view(torch.int16),
                            b.view(torch.uint8) if b.dtype == torch.uint8 else b.view(torch.int16))
+
+
+# --------------------------------------------------------------------------
+# gather index walk: more than 1024 requests (starts searched in global
+# memory instead of shared memory), rows before the first request
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("entry", [352, 656])
+def test_gather_more_requests_than_staged_in_shared_memory(kvq, oracle_mod, entry):
+    g = np.random.Generator(np.random.PCG64(181))
+    B = 1500
+    lens = g.integers(0, 9, size=B)
+    starts = g.integers(0, 40, size=B)
+    nb, bs = 3200, 16
+    cache = random_nvfp4_cache(nb, bs, 182) if entry == 352 else random_fp8_cache(nb, bs, 182)
+    table, ws, st, T = wl.make_gather_batch(nb, bs, lens, starts, 183)
+    run_gather(kvq, oracle_mod, entry, cache, table, ws, st, T)
+
+
+@pytest.mark.parametrize("entry", [352, 656])
+def test_gather_rows_before_the_first_request_are_skipped(kvq, oracle_mod, entry):
+    cache = random_nvfp4_cache(8, 64, 191) if entry == 352 else random_fp8_cache(8, 64, 191)
+    table, ws, st, T = wl.make_gather_batch(8, 64, [40, 30], [3, 9], 192)
+    ws = ws + 5                      # rows 0..4 belong to no request
+    run_gather(kvq, oracle_mod, entry, cache, table, ws, st, T + 5, status_expected=kvq.STATUS_BAD_BATCH)

@@ -5,6 +5,7 @@ golden tables, torch's own float8 / bfloat16 casts (an independent library),
 and an exhaustive nearest-value search (tests/independent.py).
 """
 import math
+import os
 
 import numpy as np
 import pytest
@@ -150,3 +151,23 @@ def test_bits_range_helpers_agree_with_array_forms(oracle_mod):
     np.testing.assert_array_equal(e4, oracle_mod.e4m3_rn_sat(f))
     np.testing.assert_array_equal(e2, oracle_mod.e2m1_rn_sat(f))
     np.testing.assert_array_equal(oracle_mod.bf16_rn_bits_range(first, n, threads=3), oracle_mod.bf16_rn(f))
+
+
+@pytest.mark.skipif(os.environ.get("KVQ_EXHAUSTIVE_CPU") != "1",
+                    reason="all 2^32 patterns: set KVQ_EXHAUSTIVE_CPU=1 (about 10 minutes on 8 cores)")
+def test_encoders_exhaustive_against_torch_and_bruteforce(oracle_mod):
+    """Every float32 bit pattern: e4m3 against torch's cast inside its
+    non-saturating range (and +-448 beyond), e2m1 against the exhaustive
+    nearest-value search."""
+    chunk = 1 << 24
+    threads = oracle_mod.default_threads()
+    for first in range(0, 1 << 32, chunk):
+        e4, e2 = oracle_mod.encode_bits_range(first, chunk, threads=threads)
+        f = np.arange(first, first + chunk, dtype=np.uint64).astype(np.uint32).view(np.float32)
+        finite = np.isfinite(f)
+        inr = finite & (np.abs(f) < 464)
+        t4 = ind.torch_e4m3_bits(torch.from_numpy(f[inr].copy())).numpy()
+        assert np.array_equal(e4[inr], t4), hex(first)
+        big = ~np.isnan(f) & (np.abs(f) >= 448)
+        assert np.array_equal(e4[big], np.where(np.signbit(f[big]), 0xFE, 0x7E)), hex(first)
+        assert np.array_equal(e2[finite], ind.e2m1_encode(f[finite])), hex(first)
