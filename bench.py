@@ -430,6 +430,16 @@ def time_extra(step: GpuStep):
                                                                                o[0], o[1])
                           for p, c, o in zip(phs, phcs, outs)])
     record("dequant_nvfp4_per_head T=16384 H=8 D=128", us, T, per_head_bytes_per_token(H, D) * T, 4)
+    # the same in the HND layout [pages, 2, heads, block_size, full_dim]
+    phcs = [c.view(16384, 2, 8, 16, -1) for c in phcs]
+    us = graph_replay_us([lambda p=p, c=c: kvq.kvq_reshape_and_cache_nvfp4(p.key, p.value, c, p.slot_mapping,
+                                                                           step.ks, step.vs, layout="HND")
+                          for p, c in zip(phs, phcs)])
+    record("reshape_and_cache_nvfp4 HND T=16384 H=8 D=128", us, T, per_head_bytes_per_token(H, D) * T, 4)
+    us = graph_replay_us([lambda p=p, c=c, o=o: kvq.kvq_dequant_nvfp4_per_head(c, p.slot_mapping, step.ks, step.vs,
+                                                                               o[0], o[1], layout="HND")
+                          for p, c, o in zip(phs, phcs, outs)])
+    record("dequant_nvfp4_per_head HND T=16384 H=8 D=128", us, T, per_head_bytes_per_token(H, D) * T, 4)
     del phs, phcs, outs
     # sparse-decode index conversion: 4096 decode tokens x 2048 positions over 64
     # requests of 4k-32k tokens (synthetic sizes), 10 % unused entries, 3 copies

@@ -47,9 +47,9 @@ _SIGNATURES = {
     "kvq_gather_upconvert_fp8_ds_mla": [_P, _I64, _I32, _I64, _I64, _P, _I64, _I64, _P, _I64,
                                         _I32, _P, _P, _I32, _P, _P],
     "kvq_reshape_and_cache_nvfp4": [_P, _P, _I64, _I64, _I64, _I64, _P, _I64, _I32, _I32, _P, _I64,
-                                    _I32, _P, _P, _P, _P],
+                                    _I32, _I32, _P, _P, _P, _P],
     "kvq_selftest_convert": [_U32, _I64, _P, _P, _P, _P, _P, _P],
-    "kvq_dequant_nvfp4_per_head": [_P, _I64, _I32, _I32, _I32, _P, _I64, _P, _P, _P, _I64, _I64, _P,
+    "kvq_dequant_nvfp4_per_head": [_P, _I64, _I32, _I32, _I32, _I32, _P, _I64, _P, _P, _P, _I64, _I64, _P,
                                    _I64, _I64, _P, _P],
     "kvq_req_index_to_global_slot": [_P, _I64, _P, _I64, _I32, _I64, _P, _I64, _I32, _I32, _I32, _I64,
                                      _P, _I64, _P, _P],
@@ -189,47 +189,58 @@ def kvq_gather_upconvert_fp8_ds_mla(src_cache, dst, block_table, workspace_start
 
 
 def kvq_reshape_and_cache_nvfp4(key, value, kv_cache, slot_mapping, k_scale, v_scale,
-                                status=None, stream=None):
+                                status=None, stream=None, layout="NHD"):
     """Writes the per-head NVFP4 cache uint8 [P, 2, block_size, H, full_dim]
-    from key / value bf16 [T, H, D]; k_scale / v_scale CUDA fp32 scalars."""
+    (layout "NHD") or [P, 2, H, block_size, full_dim] ("HND") from key / value
+    bf16 [T, H, D]; k_scale / v_scale CUDA fp32 scalars."""
     for name, t in (("key", key), ("value", value)):
         _need(t.dtype == torch.bfloat16 and t.is_cuda and t.dim() == 3 and t.stride(2) == 1,
               f"{name}: expected a CUDA bf16 [T, H, D] tensor with unit inner stride")
     _need(key.shape == value.shape, "key and value shapes differ")
     T, H, D = key.shape
-    _per_head_cache(kv_cache, H, D)
+    code, block_size = _per_head_cache(kv_cache, H, D, layout)
     _need(slot_mapping.dtype == torch.int64 and slot_mapping.is_cuda and slot_mapping.is_contiguous()
           and slot_mapping.shape[0] == T, "slot_mapping: expected a contiguous CUDA int64 [T]")
     for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
         _need(t.dtype == torch.float32 and t.is_cuda and t.numel() >= 1, f"{name}: CUDA fp32 scalar")
     _call("kvq_reshape_and_cache_nvfp4", key.data_ptr(), value.data_ptr(), key.stride(0),
           key.stride(1), value.stride(0), value.stride(1), slot_mapping.data_ptr(), T, H, D,
-          kv_cache.data_ptr(), kv_cache.shape[0], kv_cache.shape[2], k_scale.data_ptr(),
+          kv_cache.data_ptr(), kv_cache.shape[0], block_size, code, k_scale.data_ptr(),
           v_scale.data_ptr(), _status_ptr(status), _stream(stream, kv_cache.device))
 
 
-def _per_head_cache(kv_cache, H, D):
+LAYOUTS = {"NHD": 0, "HND": 1}
+
+
+def _per_head_cache(kv_cache, H, D, layout):
+    """Checks the per-head cache tensor; returns (layout code, block_size)."""
+    _need(layout in LAYOUTS, f"layout: expected one of {sorted(LAYOUTS)}, got {layout!r}")
+    code = LAYOUTS[layout]
+    head_axis = 3 if code == 0 else 2
+    shape = "[P, 2, block_size, H, D/2 + D/16]" if code == 0 else "[P, 2, H, block_size, D/2 + D/16]"
     _need(kv_cache.dtype == torch.uint8 and kv_cache.is_cuda and kv_cache.dim() == 5
-          and kv_cache.is_contiguous() and kv_cache.shape[1] == 2 and kv_cache.shape[3] == H
+          and kv_cache.is_contiguous() and kv_cache.shape[1] == 2 and kv_cache.shape[head_axis] == H
           and kv_cache.shape[4] == nvfp4_full_dim(D),
-          "kv_cache: expected a contiguous CUDA uint8 [P, 2, block_size, H, D/2 + D/16] tensor")
+          f"kv_cache: expected a contiguous CUDA uint8 {shape} tensor for layout {layout}")
+    return code, kv_cache.shape[5 - head_axis]
 
 
 def kvq_dequant_nvfp4_per_head(kv_cache, slot_mapping, k_scale, v_scale, key_out, value_out,
-                               status=None, stream=None):
-    """Reads the per-head NVFP4 cache back at slot_mapping into key_out /
-    value_out bf16 [T, H, D] (rows of padding slots are left untouched)."""
+                               status=None, stream=None, layout="NHD"):
+    """Reads the per-head NVFP4 cache (layout "NHD" or "HND") back at
+    slot_mapping into key_out / value_out bf16 [T, H, D] (rows of padding
+    slots are left untouched)."""
     for name, t in (("key_out", key_out), ("value_out", value_out)):
         _need(t.dtype == torch.bfloat16 and t.is_cuda and t.dim() == 3 and t.stride(2) == 1,
               f"{name}: expected a CUDA bf16 [T, H, D] tensor with unit inner stride")
     _need(key_out.shape == value_out.shape, "key_out and value_out shapes differ")
     T, H, D = key_out.shape
-    _per_head_cache(kv_cache, H, D)
+    code, block_size = _per_head_cache(kv_cache, H, D, layout)
     _need(slot_mapping.dtype == torch.int64 and slot_mapping.is_cuda and slot_mapping.is_contiguous()
           and slot_mapping.shape[0] == T, "slot_mapping: expected a contiguous CUDA int64 [T]")
     for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
         _need(t.dtype == torch.float32 and t.is_cuda and t.numel() >= 1, f"{name}: CUDA fp32 scalar")
-    _call("kvq_dequant_nvfp4_per_head", kv_cache.data_ptr(), kv_cache.shape[0], kv_cache.shape[2], H, D,
+    _call("kvq_dequant_nvfp4_per_head", kv_cache.data_ptr(), kv_cache.shape[0], block_size, code, H, D,
           slot_mapping.data_ptr(), T, k_scale.data_ptr(), v_scale.data_ptr(), key_out.data_ptr(),
           key_out.stride(0), key_out.stride(1), value_out.data_ptr(), value_out.stride(0),
           value_out.stride(1), _status_ptr(status), _stream(stream, kv_cache.device))

@@ -147,9 +147,11 @@ kvq_status per_head_common(const char* fn, bool read_back,
                            int64_t key_stride_h, int64_t value_stride_t, int64_t value_stride_h,
                            const int64_t* slot_mapping, int64_t num_tokens, int32_t num_heads,
                            int32_t head_size, const uint8_t* kv_cache, int64_t num_pages,
-                           int32_t block_size, const float* k_scale, const float* v_scale,
-                           int32_t* d_status, kvq_stream_t stream) {
+                           int32_t block_size, int32_t layout, const float* k_scale,
+                           const float* v_scale, int32_t* d_status, kvq_stream_t stream) {
   KVQ_REQUIRE(num_tokens >= 0, "%s: num_tokens < 0", fn);
+  KVQ_REQUIRE(layout == KVQ_LAYOUT_NHD || layout == KVQ_LAYOUT_HND,
+              "%s: layout must be KVQ_LAYOUT_NHD (0) or KVQ_LAYOUT_HND (1)", fn);
   if (num_tokens == 0) return ok();
   KVQ_REQUIRE(num_heads > 0 && head_size >= 16 && head_size % 16 == 0,
               "%s: need num_heads > 0 and head_size a positive multiple of 16", fn);
@@ -182,7 +184,7 @@ kvq_status per_head_common(const char* fn, bool read_back,
   const kvq::PerHeadArgs a{key,          value,     key_stride_t, key_stride_h, value_stride_t,
                            value_stride_h, slot_mapping, num_tokens, num_heads, head_size,
                            const_cast<uint8_t*>(kv_cache), num_pages * block_size, block_size,
-                           k_scale, v_scale, d_status,
+                           layout, k_scale, v_scale, d_status,
                            kvq::FastDiv::make(static_cast<uint32_t>(block_size)), {}, {}, {}};
   return launched(fn, launch(a, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -244,17 +246,17 @@ kvq_status kvq_reshape_and_cache_nvfp4(const void* key, const void* value, int64
                                        int64_t value_stride_h, const int64_t* slot_mapping,
                                        int64_t num_tokens, int32_t num_heads, int32_t head_size,
                                        uint8_t* kv_cache, int64_t num_pages, int32_t block_size,
-                                       const float* k_scale, const float* v_scale,
+                                       int32_t layout, const float* k_scale, const float* v_scale,
                                        int32_t* d_status, kvq_stream_t stream) {
   return per_head_common("kvq_reshape_and_cache_nvfp4", false, kvq::launch_reshape_and_cache_nvfp4,
                          key, value, key_stride_t, key_stride_h, value_stride_t, value_stride_h,
                          slot_mapping, num_tokens, num_heads, head_size, kv_cache, num_pages,
-                         block_size, k_scale, v_scale, d_status, stream);
+                         block_size, layout, k_scale, v_scale, d_status, stream);
 }
 
 kvq_status kvq_dequant_nvfp4_per_head(const uint8_t* kv_cache, int64_t num_pages,
-                                      int32_t block_size, int32_t num_heads, int32_t head_size,
-                                      const int64_t* slot_mapping, int64_t num_tokens,
+                                      int32_t block_size, int32_t layout, int32_t num_heads,
+                                      int32_t head_size, const int64_t* slot_mapping, int64_t num_tokens,
                                       const float* k_scale, const float* v_scale, void* key_out,
                                       int64_t key_stride_t, int64_t key_stride_h, void* value_out,
                                       int64_t value_stride_t, int64_t value_stride_h,
@@ -262,7 +264,7 @@ kvq_status kvq_dequant_nvfp4_per_head(const uint8_t* kv_cache, int64_t num_pages
   return per_head_common("kvq_dequant_nvfp4_per_head", true, kvq::launch_dequant_nvfp4_per_head,
                          key_out, value_out, key_stride_t, key_stride_h, value_stride_t,
                          value_stride_h, slot_mapping, num_tokens, num_heads, head_size, kv_cache,
-                         num_pages, block_size, k_scale, v_scale, d_status, stream);
+                         num_pages, block_size, layout, k_scale, v_scale, d_status, stream);
 }
 
 kvq_status kvq_req_index_to_global_slot(const int32_t* req_id, int64_t num_req_ids,

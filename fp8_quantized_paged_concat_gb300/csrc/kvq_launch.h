@@ -57,6 +57,7 @@ struct PerHeadArgs {
   uint8_t* cache;
   int64_t num_slots;
   int32_t block_size;
+  int32_t layout;        // KVQ_LAYOUT_NHD or KVQ_LAYOUT_HND
   const float* k_scale;
   const float* v_scale;
   int32_t* status;

@@ -1,6 +1,7 @@
 // kvq_per_head.cu -- reshape_and_cache into (and read-back out of) the per-head NVFP4 K/V cache
-// [num_pages, 2, block_size, H, full_dim] whose side regions hold
-// [data [block_size][H][D/2] | scales [block_size][H][D/16]].
+// [num_pages, 2, block_size, H, full_dim] (NHD) or [num_pages, 2, H, block_size, full_dim] (HND)
+// whose side regions hold [data rows of D/2 bytes | scale rows of D/16 bytes], rows in the
+// layout's (offset, head) order.
 //
 // Design (GB300): one thread per 2 consecutive 16-value groups of one
 // (token, side, head) (1 when a head's group count is odd; up to 4 with
@@ -44,13 +45,16 @@ __device__ __forceinline__ bool unit_of(const PerHeadArgs& a, Unit& u) {
   return true;
 }
 
-// Base of (page, side) and the row index (offset * H + h) of a slot.
+// Base of (page, side) and the row index of (offset, head) in it: offset * H
+// + h for NHD (a token's heads together), h * block_size + offset for HND (a
+// head's tokens together).
 __device__ __forceinline__ int64_t side_base(const PerHeadArgs& a, int64_t slot, uint32_t side,
                                              uint32_t h, int64_t& row) {
   const uint32_t page = a.block_div.div(static_cast<uint32_t>(slot));
   const uint32_t off = static_cast<uint32_t>(slot) - page * static_cast<uint32_t>(a.block_size);
   const int64_t region = static_cast<int64_t>(a.block_size) * a.num_heads * (a.head_size / 2 + a.head_size / kGroup);
-  row = static_cast<int64_t>(off) * a.num_heads + h;
+  row = a.layout == KVQ_LAYOUT_HND ? static_cast<int64_t>(h) * a.block_size + off
+                                   : static_cast<int64_t>(off) * a.num_heads + h;
   return (static_cast<int64_t>(page) * 2 + side) * region;
 }
 

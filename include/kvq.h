@@ -68,6 +68,11 @@ typedef int32_t kvq_status;
                                                one per 128 NoPE values | [528,656) bf16 RoPE */
 #define KVQ_WORKSPACE_DIM              576  /* gathered row: NoPE 0..511, RoPE 512..575      */
 
+/* Per-head cache layouts ([P2] "Key source snippets", _nvfp4_split_data_scale:
+ * the split views keep the cache's NHD or HND layout). */
+#define KVQ_LAYOUT_NHD   0  /* [num_pages, 2, block_size, num_heads, full_dim] */
+#define KVQ_LAYOUT_HND   1  /* [num_pages, 2, num_heads, block_size, full_dim] */
+
 typedef struct CUstream_st* kvq_stream_t;   /* identical to cudaStream_t */
 
 /*
@@ -172,9 +177,12 @@ kvq_status kvq_write_fp8_ds_mla(
  * = full_dim*8/9).
  *
  * kv_cache is a contiguous uint8 [num_pages, 2, block_size, num_heads,
- * full_dim] allocation.  Inside page p and side s (K = 0, V = 1) its
- * block_size*num_heads*full_dim bytes hold the data [block_size][num_heads]
- * [head_size/2] followed by the scales [block_size][num_heads][head_size/16].
+ * full_dim] allocation (layout KVQ_LAYOUT_NHD) or [num_pages, 2, num_heads,
+ * block_size, full_dim] (KVQ_LAYOUT_HND).  Inside page p and side s (K = 0,
+ * V = 1) its block_size*num_heads*full_dim bytes hold one head_size/2-byte
+ * data row per (offset, head), then one head_size/16-byte scale row per
+ * (offset, head); rows in the layout's order: offset * num_heads + head
+ * (NHD) or head * block_size + offset (HND).
  * Token t with slot s = slot_mapping[t] >= 0 goes to page s / block_size,
  * offset s % block_size: each 16-value group of y = x * (1 / scale) (fp32;
  * scale = *k_scale or *v_scale, device fp32 scalars) is quantized exactly as
@@ -188,7 +196,7 @@ kvq_status kvq_reshape_and_cache_nvfp4(
     int64_t value_stride_t, int64_t value_stride_h,
     const int64_t* slot_mapping, int64_t num_tokens,
     int32_t num_heads, int32_t head_size,
-    uint8_t* kv_cache, int64_t num_pages, int32_t block_size,
+    uint8_t* kv_cache, int64_t num_pages, int32_t block_size, int32_t layout,
     const float* k_scale, const float* v_scale,
     int32_t* d_status, kvq_stream_t stream);
 
@@ -200,12 +208,12 @@ kvq_status kvq_reshape_and_cache_nvfp4(
  * 16-value group of head h and side (K -> key_out, V -> value_out) becomes
  * bf16_rn((e2m1 * sf) * scale): the first product exact, one fp32 rounding
  * for the per-tensor scale (*k_scale / *v_scale).  Rows of padding and
- * out-of-range slots are not written.  Cache layout and argument rules as in
+ * out-of-range slots are not written.  Cache layouts and argument rules as in
  * kvq_reshape_and_cache_nvfp4; key_out / value_out are bf16 [num_tokens,
  * num_heads, head_size] outputs with token and head strides in elements.
  */
 kvq_status kvq_dequant_nvfp4_per_head(
-    const uint8_t* kv_cache, int64_t num_pages, int32_t block_size,
+    const uint8_t* kv_cache, int64_t num_pages, int32_t block_size, int32_t layout,
     int32_t num_heads, int32_t head_size,
     const int64_t* slot_mapping, int64_t num_tokens,
     const float* k_scale, const float* v_scale,

@@ -53,8 +53,9 @@ _SIGNATURES = {
     "kvqo_gather_fp8_ds_mla": (_I64, [_P, _I64, _I32, _I64, _I64, _P, _I64, _I64, _P, _I64, _I32,
                                       _P, _P, _I32, _P, _I64]),
     "kvqo_reshape_and_cache_nvfp4": (_I64, [_P, _P, _I64, _I64, _I64, _I64, _P, _I64, _I64, _I32, _I32,
-                                            _P, _I64, _I32, _F32, _F32]),
-    "kvqo_dequant_nvfp4_per_head": (_I64, [_P, _I64, _I32, _I32, _I32, _P, _I64, _I64, _F32, _F32, _P, _P]),
+                                            _P, _I64, _I32, _F32, _F32, _I32]),
+    "kvqo_dequant_nvfp4_per_head": (_I64, [_P, _I64, _I32, _I32, _I32, _P, _I64, _I64, _F32, _F32, _I32,
+                                           _P, _P]),
     "kvqo_req_index_to_global_slot": (_I64, [_P, _P, _I64, _I32, _P, _I64, _I32, _I32, _I32, _I64, _P]),
     "kvqo_decode_nvfp4_ds_mla_entry": (None, [_P, _P]),
 }
@@ -274,36 +275,51 @@ def _check_khd(name, a):
         raise ValueError(f"{name}: expected uint16 [T, H, D] with unit inner stride")
 
 
+LAYOUTS = {"NHD": 0, "HND": 1}
+
+
+def _per_head_geometry(cache, H, D, layout):
+    """(num_pages, block_size) of a contiguous per-head cache: uint8
+    [P, 2, block_size, H, full_dim] for NHD, [P, 2, H, block_size, full_dim]
+    for HND."""
+    if layout not in LAYOUTS:
+        raise ValueError("layout must be 'NHD' or 'HND'")
+    if cache.dtype != np.uint8 or cache.ndim != 5 or not cache.flags.c_contiguous:
+        raise ValueError("cache: expected a contiguous uint8 5-d per-head cache")
+    P, two, d2, d3, fd = cache.shape
+    bs, Hc = (d2, d3) if layout == "NHD" else (d3, d2)
+    if two != 2 or Hc != H or fd != nvfp4_full_dim(D):
+        raise ValueError("cache shape does not match key / value")
+    return P, bs
+
+
 def reshape_and_cache_nvfp4(key, value, slot_mapping, cache, k_scale: float = 1.0,
-                            v_scale: float = 1.0, threads: int = 1) -> int:
-    """In-place oracle write of the per-head NVFP4 cache uint8
-    [num_pages, 2, block_size, H, full_dim]; returns out-of-range slots."""
+                            v_scale: float = 1.0, threads: int = 1, layout: str = "NHD") -> int:
+    """In-place oracle write of the per-head NVFP4 cache (uint8
+    [num_pages, 2, block_size, H, full_dim] for NHD, [.., H, block_size, ..]
+    for HND); returns out-of-range slots."""
     _check_khd("key", key)
     _check_khd("value", value)
     T, H, D = key.shape
     if value.shape != key.shape:
         raise ValueError("key / value shapes differ")
-    if cache.dtype != np.uint8 or cache.ndim != 5 or not cache.flags.c_contiguous:
-        raise ValueError("cache: expected contiguous uint8 [P, 2, bs, H, full_dim]")
-    P, two, bs, Hc, fd = cache.shape
-    if two != 2 or Hc != H or fd != nvfp4_full_dim(D):
-        raise ValueError("cache shape does not match key / value")
+    P, bs = _per_head_geometry(cache, H, D, layout)
     slot_mapping = np.ascontiguousarray(slot_mapping, dtype=np.int64)
     fn = lib().kvqo_reshape_and_cache_nvfp4
 
     def run(b, e):
         return fn(_ptr(key), _ptr(value), key.strides[0] // 2, key.strides[1] // 2,
                   value.strides[0] // 2, value.strides[1] // 2, _ptr(slot_mapping), b, e,
-                  H, D, _ptr(cache), P, bs, k_scale, v_scale)
+                  H, D, _ptr(cache), P, bs, k_scale, v_scale, LAYOUTS[layout])
 
     return _run_chunks(run, slot_mapping.shape[0], threads)
 
 
 def dequant_nvfp4_per_head(cache, slot_mapping, num_heads: int, head_size: int,
                            k_scale: float = 1.0, v_scale: float = 1.0,
-                           key_out=None, value_out=None, threads: int = 1):
+                           key_out=None, value_out=None, threads: int = 1, layout: str = "NHD"):
     """Reads the per-head cache back at slot_mapping into bf16 [T, H, D]."""
-    P, _, bs, H, fd = cache.shape
+    P, bs = _per_head_geometry(cache, num_heads, head_size, layout)
     slot_mapping = np.ascontiguousarray(slot_mapping, dtype=np.int64)
     T = slot_mapping.shape[0]
     if key_out is None:
@@ -314,7 +330,7 @@ def dequant_nvfp4_per_head(cache, slot_mapping, num_heads: int, head_size: int,
 
     def run(b, e):
         return fn(_ptr(cache), P, bs, num_heads, head_size, _ptr(slot_mapping), b, e,
-                  k_scale, v_scale, _ptr(key_out), _ptr(value_out))
+                  k_scale, v_scale, LAYOUTS[layout], _ptr(key_out), _ptr(value_out))
 
     skipped = _run_chunks(run, T, threads)
     return key_out, value_out, skipped

@@ -452,26 +452,34 @@ int64_t kvqo_gather_fp8_ds_mla(
  * [P2] "Function and motivation" / "Implementation breakdown" item 4: layout
  * [K_data | K_scale | V_data | V_scale], each contiguous.  Format-spec
  * reading: inside page p and side s (K = 0, V = 1) the block_size * H *
- * full_dim bytes hold first the data [block_size][H][data_dim], then the
- * scales [block_size][H][scale_dim], with data_dim and scale_dim from the
- * split-view formula. */
+ * full_dim bytes hold first the data (one data_dim row per (offset, head)),
+ * then the scales (one scale_dim row each), rows in the cache's layout order,
+ * with data_dim and scale_dim from the split-view formula. */
 static int64_t perhead_side_base(int64_t page, int side, int32_t block_size,
                                  int32_t num_heads, int32_t head_size) {
     int64_t region = (int64_t)block_size * num_heads * kvqo_nvfp4_full_dim(head_size);
     return page * 2 * region + side * region;
 }
 
-static int64_t perhead_data_off(int32_t off, int32_t h, int32_t num_heads, int32_t head_size) {
-    int32_t data_dim = kvqo_nvfp4_data_dim(kvqo_nvfp4_full_dim(head_size));
-    return ((int64_t)off * num_heads + h) * data_dim;
+/* Row of (offset, head) inside a side region: NHD keeps a token's heads
+ * together (row = offset * H + h, the shape's (block_size, num_kv_heads)
+ * order); HND keeps a head's tokens together (row = h * block_size + offset).
+ * [P2] "Key source snippets" (torch_utils.py _nvfp4_split_data_scale): the
+ * split views keep the cache's own layout, NHD or HND. */
+static int64_t perhead_row(int32_t off, int32_t h, int32_t block_size, int32_t num_heads, int32_t layout) {
+    return layout == 1 ? (int64_t)h * block_size + off : (int64_t)off * num_heads + h;
 }
 
-static int64_t perhead_scale_off(int32_t off, int32_t h, int32_t block_size,
-                                 int32_t num_heads, int32_t head_size) {
+static int64_t perhead_data_off(int64_t row, int32_t head_size) {
+    int32_t data_dim = kvqo_nvfp4_data_dim(kvqo_nvfp4_full_dim(head_size));
+    return row * data_dim;
+}
+
+static int64_t perhead_scale_off(int64_t row, int32_t block_size, int32_t num_heads, int32_t head_size) {
     int32_t full_dim = kvqo_nvfp4_full_dim(head_size);
     int32_t data_dim = kvqo_nvfp4_data_dim(full_dim);
     int32_t scale_dim = kvqo_nvfp4_scale_dim(full_dim);
-    return (int64_t)block_size * num_heads * data_dim + ((int64_t)off * num_heads + h) * scale_dim;
+    return (int64_t)block_size * num_heads * data_dim + row * scale_dim;
 }
 
 /* [P2] "Implementation breakdown" item 4: reshape_and_cache_nvfp4_kernel
@@ -485,7 +493,7 @@ int64_t kvqo_reshape_and_cache_nvfp4(
     const int64_t* slot_mapping, int64_t t_begin, int64_t t_end,
     int32_t num_heads, int32_t head_size,
     uint8_t* cache, int64_t num_pages, int32_t block_size,
-    float k_scale, float v_scale) {
+    float k_scale, float v_scale, int32_t layout) {
     int64_t t, skipped = 0;
     for (t = t_begin; t < t_end; ++t) {
         int64_t slot = slot_mapping[t], page;
@@ -502,8 +510,9 @@ int64_t kvqo_reshape_and_cache_nvfp4(
             uint8_t* base = cache + perhead_side_base(page, side, block_size, num_heads, head_size);
             for (h = 0; h < num_heads; ++h) {
                 int32_t g;
-                uint8_t* data = base + perhead_data_off(off, h, num_heads, head_size);
-                uint8_t* scales = base + perhead_scale_off(off, h, block_size, num_heads, head_size);
+                int64_t row = perhead_row(off, h, block_size, num_heads, layout);
+                uint8_t* data = base + perhead_data_off(row, head_size);
+                uint8_t* scales = base + perhead_scale_off(row, block_size, num_heads, head_size);
                 for (g = 0; g < head_size / NV_GROUP; ++g) {
                     float y[NV_GROUP];
                     int i;
@@ -525,7 +534,7 @@ int64_t kvqo_dequant_nvfp4_per_head(
     const uint8_t* cache, int64_t num_pages, int32_t block_size,
     int32_t num_heads, int32_t head_size,
     const int64_t* slot_mapping, int64_t t_begin, int64_t t_end,
-    float k_scale, float v_scale, uint16_t* key_out, uint16_t* value_out) {
+    float k_scale, float v_scale, int32_t layout, uint16_t* key_out, uint16_t* value_out) {
     int64_t t, skipped = 0;
     for (t = t_begin; t < t_end; ++t) {
         int64_t slot = slot_mapping[t], page;
@@ -539,8 +548,9 @@ int64_t kvqo_dequant_nvfp4_per_head(
             float scale = side ? v_scale : k_scale;
             const uint8_t* base = cache + perhead_side_base(page, side, block_size, num_heads, head_size);
             for (h = 0; h < num_heads; ++h) {
-                const uint8_t* data = base + perhead_data_off(off, h, num_heads, head_size);
-                const uint8_t* scales = base + perhead_scale_off(off, h, block_size, num_heads, head_size);
+                int64_t row = perhead_row(off, h, block_size, num_heads, layout);
+                const uint8_t* data = base + perhead_data_off(row, head_size);
+                const uint8_t* scales = base + perhead_scale_off(row, block_size, num_heads, head_size);
                 for (d = 0; d < head_size; ++d) {
                     uint8_t byte = data[d / 2];
                     uint8_t nib = (d % 2 == 0) ? (byte & 0xF) : (byte >> 4);

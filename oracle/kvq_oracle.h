@@ -110,7 +110,7 @@ int64_t kvqo_reshape_and_cache_nvfp4(
     const int64_t* slot_mapping, int64_t t_begin, int64_t t_end,
     int32_t num_heads, int32_t head_size,
     uint8_t* cache, int64_t num_pages, int32_t block_size,
-    float k_scale, float v_scale);
+    float k_scale, float v_scale, int32_t layout);   /* layout: 0 = NHD, 1 = HND */
 
 /* Reads K and V back out of the per-head cache at slot_mapping[t] into bf16
  * [T, H, D] (contiguous); rows for padding / out-of-range slots untouched. */
@@ -118,7 +118,7 @@ int64_t kvqo_dequant_nvfp4_per_head(
     const uint8_t* cache, int64_t num_pages, int32_t block_size,
     int32_t num_heads, int32_t head_size,
     const int64_t* slot_mapping, int64_t t_begin, int64_t t_end,
-    float k_scale, float v_scale, uint16_t* key_out, uint16_t* value_out);
+    float k_scale, float v_scale, int32_t layout, uint16_t* key_out, uint16_t* value_out);
 
 /* Sparse-decode index conversion: out[i*topk+k] = global slot of position
  * token_indices[i*topk+k] of request req_id[i], or -1. */

@@ -134,7 +134,7 @@ def test_fp8_gather_requires_656_byte_entries(lib):
 def per_head_args(**over):
     args = dict(key=A, value=A, kst=1024, ksh=128, vst=1024, vsh=128, slot_mapping=A,
                 num_tokens=8, num_heads=8, head_size=128, kv_cache=A, num_pages=4, block_size=16,
-                k_scale=A, v_scale=A, d_status=None, stream=None)
+                layout=0, k_scale=A, v_scale=A, d_status=None, stream=None)
     args.update(over)
     return list(args.values())
 
@@ -151,6 +151,8 @@ def per_head_args(**over):
     (dict(kv_cache=A + 8), "16-byte aligned"),
     (dict(num_pages=0), "positive"),
     (dict(head_size=16, num_heads=1, block_size=1), "multiple of 8"),
+    (dict(layout=2), "KVQ_LAYOUT_NHD (0) or KVQ_LAYOUT_HND (1)"),
+    (dict(layout=-1), "layout must be"),
 ])
 def test_per_head_rejects_bad_arguments_on_host(lib, over, needle):
     assert lib.kvq_reshape_and_cache_nvfp4(*per_head_args(**over)) == 1
@@ -201,7 +203,7 @@ def test_index_conversion_zero_sized_is_noop(lib):
 
 
 def dequant_args(**over):
-    args = dict(kv_cache=A, num_pages=4, block_size=16, num_heads=8, head_size=128, slot_mapping=A,
+    args = dict(kv_cache=A, num_pages=4, block_size=16, layout=1, num_heads=8, head_size=128, slot_mapping=A,
                 num_tokens=8, k_scale=A, v_scale=A, key_out=A, kst=1024, ksh=128, value_out=A,
                 vst=1024, vsh=128, d_status=None, stream=None)
     args.update(over)
@@ -215,6 +217,7 @@ def dequant_args(**over):
     (dict(ksh=64), "overlap"),
     (dict(vst=512), "overlap"),
     (dict(kv_cache=A + 4), "16-byte aligned"),
+    (dict(layout=7), "layout must be"),
 ])
 def test_dequant_rejects_bad_arguments_on_host(lib, over, needle):
     assert lib.kvq_dequant_nvfp4_per_head(*dequant_args(**over)) == 1

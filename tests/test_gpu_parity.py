@@ -352,10 +352,18 @@ def test_gather_fp8_full_size(kvq, oracle_mod, threads):
 # per-head NVFP4 cache
 # --------------------------------------------------------------------------
 
-def run_per_head(kvq, oracle_mod, w, strided=False, status_expected=0, threads=1, narrow_rows=False):
+def per_head_shape(w, kvq, layout):
     T, H, D = w.key.shape
     fd = kvq.nvfp4_full_dim(D)
-    init = wl.random_bytes((w.num_pages, 2, w.block_size, H, fd), 5)
+    if layout == "HND":
+        return (w.num_pages, 2, H, w.block_size, fd)
+    return (w.num_pages, 2, w.block_size, H, fd)
+
+
+def run_per_head(kvq, oracle_mod, w, strided=False, status_expected=0, threads=1, narrow_rows=False,
+                 layout="NHD"):
+    T, H, D = w.key.shape
+    init = wl.random_bytes(per_head_shape(w, kvq, layout), 5)
     cache = dev(init.copy())
     if strided:            # key and value as interleaved halves of one [T, H, 2D] tensor
         both = torch.cat([w.key, w.value], dim=2).to(DEV)
@@ -371,10 +379,11 @@ def run_per_head(kvq, oracle_mod, w, strided=False, status_expected=0, threads=1
     ks = torch.tensor([w.k_scale], dtype=torch.float32, device=DEV)
     vs = torch.tensor([w.v_scale], dtype=torch.float32, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    kvq.kvq_reshape_and_cache_nvfp4(key, value, cache, dev(w.slot_mapping), ks, vs, status=status)
+    kvq.kvq_reshape_and_cache_nvfp4(key, value, cache, dev(w.slot_mapping), ks, vs, status=status,
+                                    layout=layout)
     want = init.copy()
     oracle_mod.reshape_and_cache_nvfp4(wl.bf16_bits(w.key), wl.bf16_bits(w.value), wl.host(w.slot_mapping),
-                                       want, w.k_scale, w.v_scale, threads=threads)
+                                       want, w.k_scale, w.v_scale, threads=threads, layout=layout)
     assert int(status.item()) == status_expected
     got = cache.cpu().numpy()
     assert np.array_equal(got, want), f"{int((got != want).sum())} bytes differ"
@@ -393,9 +402,10 @@ PER_HEAD_CASES = [
 ]
 
 
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
 @pytest.mark.parametrize("name,make,kw", PER_HEAD_CASES, ids=[c[0] for c in PER_HEAD_CASES])
-def test_per_head_parity(kvq, oracle_mod, name, make, kw):
-    run_per_head(kvq, oracle_mod, make(), **kw)
+def test_per_head_parity(kvq, oracle_mod, name, make, kw, layout):
+    run_per_head(kvq, oracle_mod, make(), layout=layout, **kw)
 
 
 @pytest.mark.parametrize("k_scale,v_scale", [(1.0, 1.0), (0.75, 3.0), (2.0 ** -20, 2.0 ** 20)])
@@ -421,8 +431,9 @@ def test_per_head_out_of_range_slots(kvq, oracle_mod):
     run_per_head(kvq, oracle_mod, w, status_expected=kvq.STATUS_BAD_INDEX)
 
 
-def test_per_head_full_size(kvq, oracle_mod, threads):
-    run_per_head(kvq, oracle_mod, wl.per_head(), threads=threads)
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_per_head_full_size(kvq, oracle_mod, threads, layout):
+    run_per_head(kvq, oracle_mod, wl.per_head(), threads=threads, layout=layout)
 
 
 # --------------------------------------------------------------------------
@@ -430,7 +441,7 @@ def test_per_head_full_size(kvq, oracle_mod, threads):
 # --------------------------------------------------------------------------
 
 def run_dequant(kvq, oracle_mod, w, cache_host, strided=False, status_expected=0, threads=1,
-                narrow_rows=False):
+                narrow_rows=False, layout="NHD"):
     T, H, D = w.key.shape
     if strided:          # outputs as halves of one [T, H, 2D] tensor
         both = torch.full((T, H, 2 * D), -3.0, dtype=torch.bfloat16, device=DEV)
@@ -445,36 +456,38 @@ def run_dequant(kvq, oracle_mod, w, cache_host, strided=False, status_expected=0
     ks = torch.tensor([w.k_scale], dtype=torch.float32, device=DEV)
     vs = torch.tensor([w.v_scale], dtype=torch.float32, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    kvq.kvq_dequant_nvfp4_per_head(dev(cache_host), dev(w.slot_mapping), ks, vs, ko, vo, status=status)
+    kvq.kvq_dequant_nvfp4_per_head(dev(cache_host), dev(w.slot_mapping), ks, vs, ko, vo, status=status,
+                                   layout=layout)
     guard = wl.bf16_bits(torch.tensor([-3.0], dtype=torch.bfloat16))[0]
     wk = np.full((T, H, D), guard, np.uint16)
     wv = np.full((T, H, D), guard, np.uint16)
     oracle_mod.dequant_nvfp4_per_head(cache_host, wl.host(w.slot_mapping), H, D, w.k_scale, w.v_scale,
-                                      key_out=wk, value_out=wv, threads=threads)
+                                      key_out=wk, value_out=wv, threads=threads, layout=layout)
     assert int(status.item()) == status_expected
     np.testing.assert_array_equal(wl.bf16_bits(ko), wk)
     np.testing.assert_array_equal(wl.bf16_bits(vo), wv)
 
 
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
 @pytest.mark.parametrize("name,make,kw", PER_HEAD_CASES, ids=[c[0] for c in PER_HEAD_CASES])
-def test_dequant_per_head_parity_written_cache(kvq, oracle_mod, name, make, kw):
+def test_dequant_per_head_parity_written_cache(kvq, oracle_mod, name, make, kw, layout):
     w = make()
-    T, H, D = w.key.shape
-    cache = np.zeros((w.num_pages, 2, w.block_size, H, kvq.nvfp4_full_dim(D)), np.uint8)
+    cache = np.zeros(per_head_shape(w, kvq, layout), np.uint8)
     oracle_mod.reshape_and_cache_nvfp4(wl.bf16_bits(w.key), wl.bf16_bits(w.value), wl.host(w.slot_mapping),
-                                       cache, w.k_scale, w.v_scale)
-    run_dequant(kvq, oracle_mod, w, cache, **kw)
+                                       cache, w.k_scale, w.v_scale, layout=layout)
+    run_dequant(kvq, oracle_mod, w, cache, layout=layout, **kw)
 
 
-def test_dequant_per_head_random_cache_and_bad_slots(kvq, oracle_mod):
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_dequant_per_head_random_cache_and_bad_slots(kvq, oracle_mod, layout):
     w = wl.make_per_head("rb", 70, 4, 64, 8, 16, 5, 111, k_scale=0.3, v_scale=7.0)
     s = wl.host(w.slot_mapping).copy()
     s[[1, 2]] = [128, 999]
     w.slot_mapping = torch.from_numpy(s)
-    cache = wl.random_bytes((8, 2, 16, 4, kvq.nvfp4_full_dim(64)), 112)
+    cache = wl.random_bytes(per_head_shape(w, kvq, layout), 112)
     # scale bytes must be finite e4m3: every byte that can be a scale byte
     wl.nan_free_e4m3_bytes(cache)
-    run_dequant(kvq, oracle_mod, w, cache, status_expected=kvq.STATUS_BAD_INDEX)
+    run_dequant(kvq, oracle_mod, w, cache, status_expected=kvq.STATUS_BAD_INDEX, layout=layout)
 
 
 def test_dequant_per_head_full_size(kvq, oracle_mod, threads):

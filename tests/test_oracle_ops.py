@@ -460,3 +460,29 @@ def test_req_index_conversion_bruteforce(oracle_mod):
             assert out[i, k] == want
     with pytest.raises(ValueError):
         oracle_mod.req_index_to_global_slot(req[:-1], idx, table, 16, 64)
+
+
+def test_per_head_hnd_is_the_nhd_rows_permuted(oracle_mod):
+    """The two layouts hold the same data and scale rows per (page, side):
+    row (offset, head) sits at offset * H + head (NHD) or head * block_size
+    + offset (HND)."""
+    P, bs, H, D = 6, 16, 4, 128
+    w = wl.make_per_head("lay", 70, H, D, P, bs, 4, 45, k_scale=0.5, v_scale=2.0)
+    key, val, slots = wl.bf16_bits(w.key), wl.bf16_bits(w.value), wl.host(w.slot_mapping)
+    fd = oracle_mod.nvfp4_full_dim(D)
+    nhd = np.zeros((P, 2, bs, H, fd), np.uint8)
+    hnd = np.zeros((P, 2, H, bs, fd), np.uint8)
+    oracle_mod.reshape_and_cache_nvfp4(key, val, slots, nhd, 0.5, 2.0, layout="NHD")
+    oracle_mod.reshape_and_cache_nvfp4(key, val, slots, hnd, 0.5, 2.0, layout="HND")
+    dd, sd = D // 2, D // 16
+    for p in range(P):
+        for side in range(2):
+            a, b = nhd[p, side].reshape(-1), hnd[p, side].reshape(-1)
+            ad, as_ = a[:bs * H * dd].reshape(bs, H, dd), a[bs * H * dd:].reshape(bs, H, sd)
+            bd, bs_ = b[:bs * H * dd].reshape(H, bs, dd), b[bs * H * dd:].reshape(H, bs, sd)
+            np.testing.assert_array_equal(ad, bd.transpose(1, 0, 2))
+            np.testing.assert_array_equal(as_, bs_.transpose(1, 0, 2))
+    k1, v1, _ = oracle_mod.dequant_nvfp4_per_head(nhd, slots, H, D, 0.5, 2.0, layout="NHD")
+    k2, v2, _ = oracle_mod.dequant_nvfp4_per_head(hnd, slots, H, D, 0.5, 2.0, layout="HND")
+    np.testing.assert_array_equal(k1, k2)
+    np.testing.assert_array_equal(v1, v2)
