@@ -57,6 +57,9 @@ _SIGNATURES = {
     "kvqo_dequant_nvfp4_per_head": (_I64, [_P, _I64, _I32, _I32, _I32, _P, _I64, _I64, _F32, _F32, _I32,
                                            _P, _P]),
     "kvqo_req_index_to_global_slot": (_I64, [_P, _P, _I64, _I32, _P, _I64, _I32, _I32, _I32, _I64, _P]),
+    "kvqo_sparse_mla_attention_nvfp4_ds_mla": (_I64, [_P, _I64, _I64, _I64, _I64, _I32, _P, _I64, _I32,
+                                                      _P, _I64, _I32, _I64, _I64, ctypes.c_double,
+                                                      _P, _I64, _I64, _P, _I64]),
     "kvqo_decode_nvfp4_ds_mla_entry": (None, [_P, _P]),
 }
 
@@ -349,6 +352,33 @@ def req_index_to_global_slot(req_id, token_indices, block_table, block_size: int
         _ptr(req_id), _ptr(token_indices), N, topk, _ptr(block_table), block_table.shape[1],
         block_table.shape[1], block_table.shape[0], block_size, num_blocks, _ptr(out))
     return out, skipped
+
+
+def sparse_mla_attention_nvfp4_ds_mla(q, indices, cache, softmax_scale: float, threads: int = 1):
+    """Oracle sparse MLA attention (MQA form) of q uint16 bf16 bits [T, H, 576]
+    over the global slots indices int32 [T, topk] of the nvfp4_ds_mla cache;
+    returns (o float64 [T, H, 512], lse float64 [T, H], slots skipped)."""
+    if q.dtype != np.uint16 or q.ndim != 3 or q.shape[2] != 576 or q.strides[2] != 2:
+        raise ValueError("q: expected uint16 [T, H, 576] with unit inner stride")
+    indices = np.ascontiguousarray(indices, dtype=np.int32)
+    T, H = q.shape[0], q.shape[1]
+    if indices.ndim != 2 or indices.shape[0] != T:
+        raise ValueError("indices: expected int32 [T, topk]")
+    nb, bs, bstride, estride = _cache_geometry(cache, 352)
+    out = np.zeros((T, H, 512), np.float64)
+    lse = np.zeros((T, H), np.float64)
+    fn = lib().kvqo_sparse_mla_attention_nvfp4_ds_mla
+
+    def run(b, e):
+        r = fn(_ptr(q), q.strides[0] // 2, q.strides[1] // 2, b, e, H, _ptr(indices), indices.shape[1],
+               indices.shape[1], _ptr(cache), nb, bs, bstride, estride, float(softmax_scale),
+               _ptr(out), H * 512, 512, _ptr(lse), H)
+        if r < 0:
+            raise MemoryError("oracle attention: scratch allocation failed")
+        return r
+
+    skipped = _run_chunks(run, T, threads)
+    return out, lse, skipped
 
 
 def decode_nvfp4_ds_mla_entry(entry) -> np.ndarray:

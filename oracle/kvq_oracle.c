@@ -19,6 +19,7 @@
 #include "kvq_oracle.h"
 
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 /* ========================================================================== */
@@ -594,5 +595,74 @@ int64_t kvqo_req_index_to_global_slot(
             out[i * topk + k] = (int32_t)(block * block_size + p % block_size);
         }
     }
+    return skipped;
+}
+
+/* ========================================================================== */
+/* Sparse MLA attention straight from the nvfp4_ds_mla cache                  */
+/* ========================================================================== */
+
+/* The consumer of the cache: [P1] "Key source snippets" (flashmla_sparse.py:
+ * the quantized DS-MLA formats are served by the sparse decode kernel path,
+ * which reads the cache itself and infers the format from the bytes per
+ * token) and [P3] "Implementation breakdown" item 3 (the decode side runs as
+ * MQA over the latent cache).  Reading of the MQA step: every head h of
+ * token t holds one 576-wide query q[t,h] (512 latent + 64 RoPE) and attends
+ * over the token's top-k list of global slots; the key of slot j is its whole
+ * decoded entry k_j (576 values), the value its 512 NoPE values.
+ *   s_j = softmax_scale * (q[t,h] . k_j)
+ *   o[t,h] = sum_j exp(s_j - m) k_j[0:512] / sum_j exp(s_j - m),  m = max_j s_j
+ *   lse[t,h] = m + log(sum_j exp(s_j - m))            (natural logarithm)
+ * over the valid entries of indices[t] (negative entries are unused; a slot
+ * beyond the cache is skipped and counted).  A token with no valid entry
+ * gets o = 0 and lse = -inf.  Everything in double, entries decoded exactly. */
+int64_t kvqo_sparse_mla_attention_nvfp4_ds_mla(
+    const uint16_t* q, int64_t q_stride_t, int64_t q_stride_h,
+    int64_t t_begin, int64_t t_end, int32_t num_heads,
+    const int32_t* indices, int64_t indices_stride, int32_t topk,
+    const uint8_t* cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride, double softmax_scale,
+    double* out, int64_t out_stride_t, int64_t out_stride_h,
+    double* lse, int64_t lse_stride_t) {
+    const int dim = NV_NOPE_DIM + NV_ROPE_DIM;
+    int64_t t, skipped = 0;
+    double* keys = (double*)malloc(sizeof(double) * (size_t)(topk > 0 ? topk : 1) * dim);
+    double* s = (double*)malloc(sizeof(double) * (size_t)(topk > 0 ? topk : 1));
+    if (!keys || !s) { free(keys); free(s); return -1; }
+    for (t = t_begin; t < t_end; ++t) {
+        int32_t n = 0, k, h;
+        for (k = 0; k < topk; ++k) {
+            int64_t slot = indices[t * indices_stride + k];
+            if (slot < 0) continue;
+            if (slot >= num_blocks * (int64_t)block_size) { ++skipped; continue; }
+            kvqo_decode_nvfp4_ds_mla_entry(
+                cache + (slot / block_size) * block_stride + (slot % block_size) * entry_stride,
+                keys + (int64_t)n * dim);
+            ++n;
+        }
+        for (h = 0; h < num_heads; ++h) {
+            const uint16_t* qh = q + t * q_stride_t + (int64_t)h * q_stride_h;
+            double* oh = out + t * out_stride_t + (int64_t)h * out_stride_h;
+            double m = -INFINITY, l = 0.0;
+            int d, j;
+            for (d = 0; d < NV_NOPE_DIM; ++d) oh[d] = 0.0;
+            for (j = 0; j < n; ++j) {
+                double dot = 0.0;
+                for (d = 0; d < dim; ++d) dot += (double)kvqo_bf16_value(qh[d]) * keys[(int64_t)j * dim + d];
+                s[j] = softmax_scale * dot;
+                if (s[j] > m) m = s[j];
+            }
+            for (j = 0; j < n; ++j) {
+                double w = exp(s[j] - m);
+                l += w;
+                for (d = 0; d < NV_NOPE_DIM; ++d) oh[d] += w * keys[(int64_t)j * dim + d];
+            }
+            if (n > 0)
+                for (d = 0; d < NV_NOPE_DIM; ++d) oh[d] /= l;
+            if (lse) lse[t * lse_stride_t + h] = (n > 0) ? m + log(l) : -INFINITY;
+        }
+    }
+    free(keys);
+    free(s);
     return skipped;
 }

@@ -128,6 +128,20 @@ int64_t kvqo_req_index_to_global_slot(
     int32_t block_table_width, int32_t num_requests, int32_t block_size,
     int64_t num_blocks, int32_t* out);
 
+/* Sparse MLA attention (MQA form) of queries q bf16 [T, H, 576] over the
+ * top-k global slots indices[t][0..topk) of the nvfp4_ds_mla cache: o[t,h]
+ * [512] and lse[t,h] (natural log; may be NULL) in double.  Negative entries
+ * are unused; out-of-range slots are skipped and counted; no valid entry
+ * gives o = 0, lse = -inf.  Returns -1 if scratch memory runs out. */
+int64_t kvqo_sparse_mla_attention_nvfp4_ds_mla(
+    const uint16_t* q, int64_t q_stride_t, int64_t q_stride_h,
+    int64_t t_begin, int64_t t_end, int32_t num_heads,
+    const int32_t* indices, int64_t indices_stride, int32_t topk,
+    const uint8_t* cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride, double softmax_scale,
+    double* out, int64_t out_stride_t, int64_t out_stride_h,
+    double* lse, int64_t lse_stride_t);
+
 /* Decodes one 352-byte nvfp4_ds_mla entry to 576 values (NoPE then RoPE). */
 void kvqo_decode_nvfp4_ds_mla_entry(const uint8_t* entry, double* out576);
 
