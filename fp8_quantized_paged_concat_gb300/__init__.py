@@ -21,8 +21,9 @@ __all__ = [
     "kvq_write_nvfp4_ds_mla", "kvq_write_fp8_ds_mla", "kvq_gather_upconvert_nvfp4_ds_mla",
     "kvq_gather_upconvert_fp8_ds_mla", "kvq_reshape_and_cache_nvfp4", "kvq_selftest_convert",
     "kvq_dequant_nvfp4_per_head", "kvq_req_index_to_global_slot",
-    "kvq_last_error_string", "kvq_version", "library_path", "load_library",
+    "kvq_sparse_mla_attention_nvfp4_ds_mla", "kvq_last_error_string", "kvq_version", "library_path", "load_library",
     "NVFP4_DS_MLA_ENTRY_BYTES", "FP8_DS_MLA_ENTRY_BYTES", "STATUS_BAD_INDEX", "STATUS_BAD_BATCH",
+    "STATUS_TIMEOUT",
     "nvfp4_full_dim",
 ]
 
@@ -30,6 +31,7 @@ NVFP4_DS_MLA_ENTRY_BYTES = 352
 FP8_DS_MLA_ENTRY_BYTES = 656
 STATUS_BAD_INDEX = 0x1
 STATUS_BAD_BATCH = 0x2
+STATUS_TIMEOUT = 0x4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lib = None
@@ -53,6 +55,9 @@ _SIGNATURES = {
                                    _I64, _I64, _P, _P],
     "kvq_req_index_to_global_slot": [_P, _I64, _P, _I64, _I32, _I64, _P, _I64, _I32, _I32, _I32, _I64,
                                      _P, _I64, _P, _P],
+    "kvq_sparse_mla_attention_nvfp4_ds_mla": [_P, _I64, _I64, _I64, _I32, _P, _I64, _I32, _P, _I64, _I32,
+                                              _I64, _I64, ctypes.c_float, _P, _I64, _I64, _P, _I64,
+                                              _P, _P],
 }
 
 
@@ -266,6 +271,35 @@ def kvq_req_index_to_global_slot(req_id, token_indices, block_table, block_size:
           block_table.shape[1], block_table.shape[0], block_size, num_blocks, out.data_ptr(),
           out.stride(0), _status_ptr(status), _stream(stream, token_indices.device))
     return out
+
+
+def kvq_sparse_mla_attention_nvfp4_ds_mla(q, indices, kv_cache, softmax_scale: float, out=None, lse=None,
+                                          status=None, stream=None):
+    """Sparse MLA attention (MQA form) straight from the nvfp4_ds_mla cache:
+    q bf16 [T, H, 576] (H <= 128), indices int32 [T, topk] global slots (< 0
+    unused), kv_cache uint8 [num_blocks, block_size, >=352].  Returns (out
+    bf16 [T, H, 512], lse fp32 [T, H]); lse=False skips the lse output."""
+    _need(q.dtype == torch.bfloat16 and q.is_cuda and q.dim() == 3 and q.shape[2] == 576
+          and q.stride(2) == 1, "q: expected a CUDA bf16 [T, H, 576] tensor with unit inner stride")
+    T, H = q.shape[0], q.shape[1]
+    _need(indices.dtype == torch.int32 and indices.is_cuda and indices.dim() == 2
+          and indices.shape[0] == T and indices.stride(1) == 1, "indices: expected CUDA int32 [T, topk] rows")
+    _mla_cache("kv_cache", kv_cache, 352)
+    if out is None:
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=q.device)
+    _need(out.dtype == torch.bfloat16 and out.is_cuda and tuple(out.shape) == (T, H, 512)
+          and out.stride(2) == 1, "out: expected a CUDA bf16 [T, H, 512] tensor with unit inner stride")
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    if lse is not False:
+        _need(lse.dtype == torch.float32 and lse.is_cuda and tuple(lse.shape) == (T, H) and lse.stride(1) == 1,
+              "lse: expected a CUDA fp32 [T, H] tensor with unit inner stride")
+    _call("kvq_sparse_mla_attention_nvfp4_ds_mla", q.data_ptr(), q.stride(0), q.stride(1), T, H,
+          indices.data_ptr(), indices.stride(0), indices.shape[1], kv_cache.data_ptr(), kv_cache.shape[0],
+          kv_cache.shape[1], kv_cache.stride(0), kv_cache.stride(1), float(softmax_scale), out.data_ptr(),
+          out.stride(0), out.stride(1), None if lse is False else lse.data_ptr(),
+          0 if lse is False else lse.stride(0), _status_ptr(status), _stream(stream, q.device))
+    return out, (None if lse is False else lse)
 
 
 def kvq_selftest_convert(first_bits: int, count: int, device="cuda", stream=None):

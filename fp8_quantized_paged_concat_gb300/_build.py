@@ -21,7 +21,7 @@ OBJDIR = os.path.join(ROOT, "_build", "kvq")
 LIBRARY = os.path.join(PKG, "_lib", "libkvq.so")
 
 SOURCES = ["kvq_abi.cu", "kvq_write.cu", "kvq_gather.cu", "kvq_per_head.cu", "kvq_index.cu",
-           "kvq_selftest.cu"]
+           "kvq_attention.cu", "kvq_selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                      "-prec-div=true", "-prec-sqrt=true", "-ftz=false", "-I" + INCLUDE, "-I" + CSRC]

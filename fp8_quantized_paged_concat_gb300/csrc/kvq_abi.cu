@@ -303,6 +303,63 @@ kvq_status kvq_req_index_to_global_slot(const int32_t* req_id, int64_t num_req_i
   return launched(fn, kvq::launch_req_index_to_global_slot(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+kvq_status kvq_sparse_mla_attention_nvfp4_ds_mla(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h, int64_t num_tokens, int32_t num_heads,
+    const int32_t* indices, int64_t indices_stride, int32_t topk, const uint8_t* kv_cache,
+    int64_t num_blocks, int32_t block_size, int64_t block_stride, int64_t entry_stride,
+    float softmax_scale, void* out, int64_t out_stride_t, int64_t out_stride_h, float* lse,
+    int64_t lse_stride_t, int32_t* d_status, kvq_stream_t stream) {
+  const char* fn = "kvq_sparse_mla_attention_nvfp4_ds_mla";
+  KVQ_REQUIRE(num_tokens >= 0 && topk >= 0, "%s: num_tokens / topk < 0", fn);
+  if (num_tokens == 0) return ok();
+  KVQ_REQUIRE(num_tokens < (int64_t{1} << 30), "%s: num_tokens too large", fn);   // 2 CTAs each
+  KVQ_REQUIRE(num_heads >= 1 && num_heads <= 128, "%s: num_heads must be in [1, 128] (got %d)", fn,
+              num_heads);
+  KVQ_REQUIRE(q != nullptr && out != nullptr, "%s: q and out must be non-NULL", fn);
+  KVQ_REQUIRE(aligned(q, 16) && aligned(out, 16), "%s: q and out must be 16-byte aligned", fn);
+  KVQ_REQUIRE(q_stride_h >= KVQ_WORKSPACE_DIM && q_stride_h % 8 == 0 && q_stride_t % 8 == 0 &&
+                  q_stride_t >= 0,
+              "%s: q strides must be multiples of 8 elements with head stride >= 576", fn);
+  KVQ_REQUIRE(out_stride_h >= KVQ_MLA_NOPE_DIM && out_stride_h % 8 == 0 && out_stride_t % 8 == 0 &&
+                  out_stride_t >= (num_heads - 1) * out_stride_h + KVQ_MLA_NOPE_DIM,
+              "%s: out strides must be multiples of 8 elements and rows must not overlap "
+              "(head stride >= 512, token stride >= (num_heads - 1) * head stride + 512)", fn);
+  KVQ_REQUIRE(lse == nullptr || (aligned(lse, 4) && lse_stride_t >= num_heads),
+              "%s: lse must be 4-byte aligned with token stride >= num_heads", fn);
+  KVQ_REQUIRE(topk == 0 || (indices != nullptr && aligned(indices, 4) && indices_stride >= topk),
+              "%s: indices must be non-NULL, 4-byte aligned, with stride >= topk", fn);
+  KVQ_REQUIRE(softmax_scale == softmax_scale && softmax_scale > -3.0e38f && softmax_scale < 3.0e38f,
+              "%s: softmax_scale must be finite", fn);
+  if (kvq_status s = check_mla_cache(fn, kv_cache, num_blocks, block_size, block_stride,
+                                     entry_stride, KVQ_NVFP4_DS_MLA_ENTRY_BYTES))
+    return s;
+  KVQ_REQUIRE(d_status == nullptr || aligned(d_status, 4), "%s: d_status misaligned", fn);
+  if (kvq_status s = check_device(fn)) return s;
+  kvq::AttentionArgs a{};
+  a.q = q;
+  a.q_stride_t = q_stride_t;
+  a.q_stride_h = q_stride_h;
+  a.num_tokens = num_tokens;
+  a.num_heads = num_heads;
+  a.indices = indices;
+  a.indices_stride = indices_stride;
+  a.topk = topk;
+  a.cache = kv_cache;
+  a.num_slots = num_blocks * block_size;
+  a.block_size = block_size;
+  a.block_div = kvq::FastDiv::make(static_cast<uint32_t>(block_size));
+  a.block_stride = block_stride;
+  a.entry_stride = entry_stride;
+  a.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634074);
+  a.out = out;
+  a.out_stride_t = out_stride_t;
+  a.out_stride_h = out_stride_h;
+  a.lse = lse;
+  a.lse_stride_t = lse_stride_t;
+  a.status = d_status;
+  return launched(fn, kvq::launch_sparse_mla_attention_nvfp4(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kvq_status kvq_selftest_convert(uint32_t first_bits, int64_t count, uint8_t* e4m3_lo,
                                 uint8_t* e4m3_hi, uint8_t* e2m1_lo, uint8_t* e2m1_hi,
                                 uint16_t* bf16_out, kvq_stream_t stream) {

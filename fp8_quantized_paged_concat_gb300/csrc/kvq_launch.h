@@ -68,6 +68,27 @@ struct PerHeadArgs {
   FastDiv head_div;      // thread within side -> head (D/16/g)
 };
 
+struct AttentionArgs {
+  const void* q;                 // bf16 [num_tokens, num_heads, 576]
+  int64_t q_stride_t, q_stride_h;
+  int64_t num_tokens;
+  int32_t num_heads;             // 1 .. 128
+  const int32_t* indices;        // global slots [num_tokens, topk], < 0 unused
+  int64_t indices_stride;
+  int32_t topk;
+  const uint8_t* cache;
+  int64_t num_slots;
+  int32_t block_size;
+  FastDiv block_div;             // slot -> block
+  int64_t block_stride, entry_stride;
+  float scale_log2;              // softmax_scale * log2(e)
+  void* out;                     // bf16 [num_tokens, num_heads, 512]
+  int64_t out_stride_t, out_stride_h;
+  float* lse;                    // fp32 [num_tokens, num_heads] or nullptr
+  int64_t lse_stride_t;
+  int32_t* status;
+};
+
 cudaError_t launch_write_nvfp4_ds_mla(const WriteArgs& a, cudaStream_t stream);
 cudaError_t launch_write_fp8_ds_mla(const WriteArgs& a, cudaStream_t stream);
 cudaError_t launch_gather_nvfp4_ds_mla(const GatherArgs& a, cudaStream_t stream);
@@ -75,6 +96,7 @@ cudaError_t launch_gather_fp8_ds_mla(const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_reshape_and_cache_nvfp4(const PerHeadArgs& a, cudaStream_t stream);
 // Read-back: key / value are the bf16 OUTPUTS (written through const_cast).
 cudaError_t launch_dequant_nvfp4_per_head(const PerHeadArgs& a, cudaStream_t stream);
+cudaError_t launch_sparse_mla_attention_nvfp4(const AttentionArgs& a, cudaStream_t stream);
 
 struct IndexArgs {
   const int32_t* req_id;

@@ -58,6 +58,8 @@ typedef int32_t kvq_status;
 #define KVQ_STATUS_BAD_INDEX   0x1  /* slot, block id or position out of range (skipped) */
 #define KVQ_STATUS_BAD_BATCH   0x2  /* workspace_starts not non-decreasing within [0, T],
                                        or a row before the first request (skipped)       */
+#define KVQ_STATUS_TIMEOUT     0x4  /* a kernel's bounded wait on its own tensor-core work
+                                       expired; that CTA's outputs were not written      */
 
 /* Entry geometry ([P1] "Implementation breakdown" items 2-3). */
 #define KVQ_MLA_NOPE_DIM               512
@@ -219,6 +221,46 @@ kvq_status kvq_dequant_nvfp4_per_head(
     const float* k_scale, const float* v_scale,
     void* key_out, int64_t key_stride_t, int64_t key_stride_h,
     void* value_out, int64_t value_stride_t, int64_t value_stride_h,
+    int32_t* d_status, kvq_stream_t stream);
+
+/*
+ * kvq_sparse_mla_attention_nvfp4_ds_mla -- sparse MLA attention read straight
+ * from the 352-byte nvfp4_ds_mla cache, the consumer that makes the bf16
+ * workspace unnecessary.  [P1] "Key source snippets" (flashmla_sparse.py: the
+ * sparse decode path serves the quantized DS-MLA formats and reads the cache
+ * itself) and [P3] "Implementation breakdown" item 3 (that decode is MQA over
+ * the latent cache).  For token t < num_tokens, head h < num_heads and the
+ * valid entries j of indices[t * indices_stride + 0 .. topk) (global slots as
+ * kvq_req_index_to_global_slot produces them; < 0 = unused, >= num_blocks *
+ * block_size = out of range: skipped, KVQ_STATUS_BAD_INDEX):
+ *   s_j = softmax_scale * (q[t,h] . k_j)     k_j = the slot's 576 decoded
+ *                                            values (NoPE then RoPE, exact)
+ *   out[t,h] = sum_j exp(s_j - m) k_j[0:512] / sum_j exp(s_j - m)
+ *   lse[t,h] = m + ln(sum_j exp(s_j - m)),   m = max_j s_j
+ * A token with no valid entry gets out = 0 and lse = -inf.
+ * Arithmetic: q . k on the tensor cores (bf16 products, fp32 accumulation);
+ * exp in base 2 in fp32; the weights rounded to bf16 for the weighted sum
+ * (fp32 accumulation), and the denominator summed from those rounded
+ * weights; out rounded once to bf16.
+ * q: bf16 [num_tokens, num_heads, 576] (token / head strides in elements,
+ * multiples of 8, head stride >= 576, unit inner stride); 1 <= num_heads <=
+ * 128.  out: bf16 [num_tokens, num_heads, 512] (strides multiples of 8, head
+ * stride >= 512, token stride >= (num_heads - 1) * head stride + 512).  lse:
+ * fp32 [num_tokens, num_heads] with token stride lse_stride_t >= num_heads,
+ * or NULL.  indices: int32, indices_stride >= topk.  The cache follows the
+ * nvfp4 gather's rules.  If a bounded wait of the kernel on its own tensor
+ * work expires (not expected), KVQ_STATUS_TIMEOUT is set and that token's
+ * outputs are left unwritten.
+ */
+kvq_status kvq_sparse_mla_attention_nvfp4_ds_mla(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h,
+    int64_t num_tokens, int32_t num_heads,
+    const int32_t* indices, int64_t indices_stride, int32_t topk,
+    const uint8_t* kv_cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride,
+    float softmax_scale,
+    void* out, int64_t out_stride_t, int64_t out_stride_h,
+    float* lse, int64_t lse_stride_t,
     int32_t* d_status, kvq_stream_t stream);
 
 /*

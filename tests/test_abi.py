@@ -222,3 +222,37 @@ def dequant_args(**over):
 def test_dequant_rejects_bad_arguments_on_host(lib, over, needle):
     assert lib.kvq_dequant_nvfp4_per_head(*dequant_args(**over)) == 1
     assert needle in err(lib), err(lib)
+
+
+def attention_args(**over):
+    args = dict(q=A, qst=128 * 576, qsh=576, num_tokens=4, num_heads=128, indices=A, istride=64,
+                topk=64, kv_cache=A, num_blocks=8, block_size=64, block_stride=64 * 352,
+                entry_stride=352, scale=0.05, out=A, ost=128 * 512, osh=512, lse=A, lst=128,
+                d_status=None, stream=None)
+    args.update(over)
+    return list(args.values())
+
+
+@no_gpu_only
+@pytest.mark.parametrize("over,needle", [
+    (dict(num_heads=0), "num_heads must be in [1, 128]"),
+    (dict(num_heads=129), "num_heads must be in [1, 128]"),
+    (dict(q=None), "non-NULL"),
+    (dict(out=A + 8), "16-byte aligned"),
+    (dict(qsh=512), "head stride >= 576"),
+    (dict(osh=512, ost=500), "must not overlap"),
+    (dict(lst=100), "lse"),
+    (dict(istride=32), "stride >= topk"),
+    (dict(scale=float("inf")), "finite"),
+    (dict(scale=float("nan")), "finite"),
+    (dict(entry_stride=336), "entry_stride"),
+    (dict(topk=-1), "< 0"),
+])
+def test_attention_rejects_bad_arguments_on_host(lib, over, needle):
+    assert lib.kvq_sparse_mla_attention_nvfp4_ds_mla(*attention_args(**over)) == 1
+    assert needle in err(lib), err(lib)
+
+
+@no_gpu_only
+def test_attention_zero_tokens_is_noop(lib):
+    assert lib.kvq_sparse_mla_attention_nvfp4_ds_mla(*attention_args(num_tokens=0, q=None)) == 0

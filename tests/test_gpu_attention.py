@@ -1,0 +1,184 @@
+"""GPU parity of the sparse MLA attention read straight from the nvfp4_ds_mla
+cache, against the oracle's float64 evaluation.
+
+The output is floating point, so the bar is a tolerance derived from the
+kernel's arithmetic (the decoded keys are exact in both):
+  * scores: fp32 accumulation of 576 exact bf16 products, error at most
+    e_s = 576 * 2^-24 * scale * max_j sum_d |q_d| |k_jd|  (per token and head);
+  * weights: exp in fp32 then rounded to bf16 (relative 2^-9), and the
+    denominator sums the rounded weights, so each normalised weight carries a
+    relative error of at most eps = 2^-9 + e_s + 2^-20;
+  * a convex combination whose weights move by a relative eps moves by at
+    most 2 eps / (1 - eps) * max_j |v_j|; the fp32 accumulation of P V adds
+    far less, and the bf16 output rounding adds 2^-9 |o|;
+  * lse moves by at most eps + e_s, plus fp32 rounding of the result.
+The bound is checked per element with vmax = max_j |v_j| of the token's
+valid slots.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    from fp8_quantized_paged_concat_gb300 import _build
+    _build.build()
+    import fp8_quantized_paged_concat_gb300 as m
+    m.load_library()
+    return m
+
+
+@pytest.fixture(scope="module")
+def threads(oracle_mod):
+    return oracle_mod.default_threads()
+
+
+def host_cache(oracle_mod, fill, threads=1):
+    cache = np.zeros((fill.num_blocks, fill.block_size, 352), np.uint8)
+    assert oracle_mod.write_nvfp4_ds_mla(wl.bf16_bits(fill.kv_c), wl.bf16_bits(fill.k_pe),
+                                         wl.host(fill.slot_mapping), cache, threads=threads) == 0
+    return cache
+
+
+def decoded_keys(oracle_mod, cache, slots):
+    """float64 [n, 576] decoded entries of the given slots (oracle decode)."""
+    bs = cache.shape[1]
+    uniq, inv = np.unique(slots, return_inverse=True)
+    table = np.stack([oracle_mod.decode_nvfp4_ds_mla_entry(cache[s // bs, s % bs]) for s in uniq])
+    return table[inv]
+
+
+def q_values(q):
+    bits = wl.bf16_bits(q).astype(np.uint32) << 16
+    return bits.view(np.float32).astype(np.float64)
+
+
+def check(oracle_mod, cache, q, idx, scale, out, lse, threads=1, tokens=None):
+    """Compares GPU out / lse with the oracle on the given tokens (all by default)."""
+    qb = wl.bf16_bits(q)
+    idx = np.asarray(idx, np.int32)
+    tokens = np.arange(q.shape[0]) if tokens is None else np.asarray(tokens)
+    want_o, want_lse, _ = oracle_mod.sparse_mla_attention_nvfp4_ds_mla(
+        np.ascontiguousarray(qb[tokens]), idx[tokens], cache, scale, threads=threads)
+    got_o = out.float().cpu().numpy()[tokens].astype(np.float64)
+    got_lse = lse.cpu().numpy()[tokens].astype(np.float64)
+    qv = q_values(q)[tokens]
+    n_slots = cache.shape[0] * cache.shape[1]
+    for i, t in enumerate(tokens):
+        valid = idx[t][(idx[t] >= 0) & (idx[t] < n_slots)]
+        if valid.size == 0:
+            assert not np.any(got_o[i]), f"token {t}: no valid slot but nonzero output"
+            assert np.all(np.isneginf(got_lse[i])), f"token {t}: lse {got_lse[i]}"
+            continue
+        keys = decoded_keys(oracle_mod, cache, valid)
+        vmax = np.abs(keys[:, :512]).max()
+        e_s = 576 * 2.0 ** -24 * abs(scale) * (np.abs(qv[i]) @ np.abs(keys).T).max(axis=1)   # [H]
+        eps = 2.0 ** -9 + e_s + 2.0 ** -20
+        tol_o = (2 * eps / (1 - eps))[:, None] * vmax + 2.0 ** -9 * np.abs(want_o[i]) + 1e-30
+        err_o = np.abs(got_o[i] - want_o[i])
+        bad = err_o > tol_o
+        assert not bad.any(), (f"token {t}: {int(bad.sum())} outputs beyond the bound; worst "
+                               f"{float((err_o / tol_o).max()):.3f} x bound")
+        tol_l = eps + e_s + 2.0 ** -22 * np.abs(want_lse[i])
+        err_l = np.abs(got_lse[i] - want_lse[i])
+        assert np.all(err_l <= tol_l), f"token {t}: lse error {err_l.max()} > {tol_l.min()}"
+
+
+def run(kvq, oracle_mod, w, cache=None, threads=1, tokens=None, strided=False):
+    if cache is None:
+        cache = host_cache(oracle_mod, w.fill, threads)
+    dcache = torch.from_numpy(cache).to(DEV)
+    q = w.q.to(DEV)
+    T, H = q.shape[0], q.shape[1]
+    if strided:      # q rows and out rows inside wider buffers
+        qbig = torch.zeros((T, H, 640), dtype=torch.bfloat16, device=DEV)
+        qbig[:, :, 32:608] = q
+        q = qbig[:, :, 32:608]
+        obig = torch.full((T, H, 520), -7.0, dtype=torch.bfloat16, device=DEV)
+        out = obig[:, :, 8:520]
+        lbig = torch.full((T, H + 5), -7.0, dtype=torch.float32, device=DEV)
+        lse = lbig[:, :H]
+    else:
+        out = torch.full((T, H, 512), -7.0, dtype=torch.bfloat16, device=DEV)
+        lse = torch.full((T, H), -7.0, dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    idx = w.indices.to(DEV)
+    kvq.kvq_sparse_mla_attention_nvfp4_ds_mla(q, idx, dcache, w.softmax_scale, out=out, lse=lse,
+                                              status=status)
+    torch.cuda.synchronize()
+    check(oracle_mod, cache, w.q, wl.host(w.indices), w.softmax_scale, out, lse, threads, tokens)
+    if strided:
+        assert torch.all(obig[:, :, :8] == -7.0) and torch.all(lbig[:, H:] == -7.0)
+    return int(status.item())
+
+
+CASES = [
+    ("H128 top64", dict(num_tokens=3, num_heads=128, topk=64, num_blocks=8, block_size=64, seed=301)),
+    ("H16 top100 ragged", dict(num_tokens=5, num_heads=16, topk=100, num_blocks=8, block_size=64, seed=302,
+                               p_unused=0.2)),
+    ("H1 top33", dict(num_tokens=4, num_heads=1, topk=33, num_blocks=4, block_size=16, seed=303)),
+    ("H64 top256 sharp", dict(num_tokens=3, num_heads=64, topk=256, num_blocks=16, block_size=64, seed=304,
+                              softmax_scale=0.25)),
+    ("H128 top512 q x4", dict(num_tokens=2, num_heads=128, topk=512, num_blocks=16, block_size=64, seed=305,
+                              q_scale=4.0, p_unused=0.5)),
+    ("H96 top31", dict(num_tokens=6, num_heads=96, topk=31, num_blocks=4, block_size=32, seed=306)),
+]
+
+
+@pytest.mark.parametrize("name,kw", CASES, ids=[c[0] for c in CASES])
+def test_attention_parity(kvq, oracle_mod, name, kw):
+    w = wl.make_attention(name, **kw)
+    assert run(kvq, oracle_mod, w) == 0
+
+
+def test_attention_strided_q_out_lse(kvq, oracle_mod):
+    w = wl.make_attention("strided", 3, 20, 70, 8, 64, 311, p_unused=0.1)
+    assert run(kvq, oracle_mod, w, strided=True) == 0
+
+
+def test_attention_empty_and_bad_slots(kvq, oracle_mod):
+    """Token 0: every entry unused; token 1: only out-of-range slots; token 2:
+    a mix; topk = 40.  Out-of-range slots set the status bit and are skipped."""
+    w = wl.make_attention("edge", 3, 8, 40, 4, 16, 312)
+    idx = wl.host(w.indices).copy()
+    idx[0] = -1
+    idx[1] = 64 + np.arange(40)
+    idx[2, ::3] = 1 << 30
+    w.indices = torch.from_numpy(idx)
+    assert run(kvq, oracle_mod, w) == kvq.STATUS_BAD_INDEX
+
+
+def test_attention_topk_zero(kvq, oracle_mod):
+    w = wl.make_attention("topk0", 4, 8, 0, 4, 16, 313)
+    assert run(kvq, oracle_mod, w) == 0
+
+
+def test_attention_duplicate_slots(kvq, oracle_mod):
+    w = wl.make_attention("dup", 2, 32, 64, 4, 16, 314)
+    idx = wl.host(w.indices).copy()
+    idx[:, 32:] = idx[:, :32]
+    w.indices = torch.from_numpy(idx)
+    assert run(kvq, oracle_mod, w) == 0
+
+
+def test_attention_full_size_sampled(kvq, oracle_mod, threads):
+    """The benchmark's decode workload (4096 tokens x 128 heads, top-2048 over
+    a 65536 x 64 cache, 10 % unused) in one launch; 48 sampled tokens (first,
+    last, random) against the oracle."""
+    fill = wl.make_fill("attention fill", 65536, 64, 1006, DEV, rng="device")
+    cache_host = host_cache(oracle_mod, fill, threads)       # the oracle's own write
+    cache = torch.from_numpy(cache_host).to(DEV)
+    w = wl.sparse_attention(DEV, fill=fill)
+    del fill
+    out, lse = kvq.kvq_sparse_mla_attention_nvfp4_ds_mla(w.q, w.indices, cache, w.softmax_scale)
+    torch.cuda.synchronize()
+    g = np.random.Generator(np.random.PCG64(77))
+    tokens = np.unique(np.concatenate([[0, w.num_tokens - 1], g.choice(w.num_tokens, 46, replace=False)]))
+    check(oracle_mod, cache_host, w.q, wl.host(w.indices), w.softmax_scale, out, lse, threads, tokens)

@@ -146,6 +146,21 @@ class PerHeadWorkload:
         return int(self.slot_mapping.shape[0])
 
 
+@dataclass
+class AttentionWorkload:
+    """Sparse MLA attention (MQA form) of T decode tokens over a filled
+    nvfp4_ds_mla cache."""
+    name: str
+    fill: WriteWorkload           # writes every slot of the cache
+    q: torch.Tensor               # bf16 [T, H, 576]
+    indices: torch.Tensor         # int32 [T, topk] global slots, -1 = unused
+    softmax_scale: float
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.q.shape[0])
+
+
 # --------------------------------------------------------------------------
 # builders
 # --------------------------------------------------------------------------
@@ -211,6 +226,31 @@ def make_per_head(name: str, num_tokens: int, num_heads: int, head_size: int, nu
                            block_size, k_scale, v_scale)
 
 
+def attention_indices(num_tokens: int, topk: int, num_slots: int, p_unused: float, seed: int) -> np.ndarray:
+    """int32 [T, topk] slots drawn uniformly from the cache (a token's top-k
+    positions land on scattered pages); entries set to -1 with p_unused."""
+    g = _rng(seed)
+    idx = g.integers(0, num_slots, size=(num_tokens, topk), dtype=np.int64).astype(np.int32)
+    if p_unused > 0:
+        idx[g.random((num_tokens, topk)) < p_unused] = -1
+    return idx
+
+
+def make_attention(name: str, num_tokens: int, num_heads: int, topk: int, num_blocks: int,
+                   block_size: int, seed: int, device="cpu", p_unused: float = 0.0,
+                   softmax_scale: float = 576 ** -0.5, q_scale: float = 1.0, fill: WriteWorkload = None,
+                   rng: str = "numpy") -> AttentionWorkload:
+    """Queries ~ q_scale * N(0, 1) in bf16 and top-k slot lists over a cache
+    whose every slot is written (``fill``, or a fresh seeded fill)."""
+    if fill is None:
+        fill = make_fill(name + " fill", num_blocks, block_size, seed, device, rng=rng)
+    q = normal_bf16((num_tokens, num_heads, NOPE_DIM + ROPE_DIM), seed * 7 + 5, device, rng=rng)
+    if q_scale != 1.0:
+        q = (q.float() * q_scale).to(torch.bfloat16)
+    idx = attention_indices(num_tokens, topk, fill.num_slots, p_unused, seed * 7 + 6)
+    return AttentionWorkload(name, fill, q, torch.from_numpy(idx).to(device), float(softmax_scale))
+
+
 # --------------------------------------------------------------------------
 # the five named workloads
 # --------------------------------------------------------------------------
@@ -265,6 +305,15 @@ def per_head(device="cpu") -> PerHeadWorkload:
     distinct slots of 262,144; scales 1.0."""
     return make_per_head("per-head nvfp4 T=16384 H=8 D=128 (16384 pages x 16)", 16384, 8, 128,
                          16384, 16, 0, 1005, device)
+
+
+def sparse_attention(device="cpu", fill: WriteWorkload = None) -> AttentionWorkload:
+    """Sparse MLA decode over the nvfp4_ds_mla cache: 4096 tokens x 128
+    heads, top-2048 slots each (10 % unused) drawn over a 65536 x 64 cache
+    (the prefill fill when given), softmax scale 576^-0.5."""
+    return make_attention("sparse MLA attention T=4096 H=128 top-2048", 4096, 128, 2048, 65536, 64, 1006,
+                          device, p_unused=0.1, fill=fill,
+                          rng="device" if str(device).startswith("cuda") else "numpy")
 
 
 # --------------------------------------------------------------------------
