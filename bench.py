@@ -46,6 +46,7 @@ BYTES_WRITE_NVFP4 = 1024 + 128 + 8 + 352       # per valid token; 8 per padding 
 BYTES_WRITE_FP8 = 1024 + 128 + 8 + 656
 BYTES_GATHER_NVFP4 = 352 + 1152                # per output row
 BYTES_GATHER_FP8 = 656 + 1152
+ATTN_FLOPS_PER_SLOT_HEAD = 2 * 576 + 2 * 512    # q . k and the weighted sum of v, per valid slot and head
 
 
 def per_head_bytes_per_token(H, D):
@@ -159,6 +160,15 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside), "window": window}
 
 
+def measured_peak_tflops():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
 def measured_peak_gbs():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -212,6 +222,7 @@ class GpuStep:
         kvq.load_library()
         self.kvq = kvq
         self.device = device
+        self.size = size
         if size == "full":
             self.g3 = wl.prefill_gather(device)
             self.g4 = wl.fp8_gather(device)
@@ -457,6 +468,34 @@ def time_extra(step: GpuStep):
                           for r, i, o in sets])
     record("req_index_to_global_slot 4096 x 2048", us, 4096 * 2048, 8 * 4096 * 2048 + 4 * 4096, 3)
     del sets
+    # sparse MLA attention straight from the nvfp4_ds_mla cache (tensor
+    # cores): 4096 decode tokens x 128 heads, top-2048 slots over the step's
+    # 65536 x 64 cache (filled by the step's write), 10 % unused
+    if step.size == "full":
+        aw = wl.sparse_attention(dev, fill=step.g3.fill)
+        ao = torch.empty((aw.num_tokens, 128, 512), dtype=torch.bfloat16, device=dev)
+        al = torch.empty((aw.num_tokens, 128), dtype=torch.float32, device=dev)
+        times = []
+        for r in range(8):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            kvq.kvq_sparse_mla_attention_nvfp4_ds_mla(aw.q, aw.indices, step.cache3, aw.softmax_scale,
+                                                      out=ao, lse=al)
+            b.record()
+            torch.cuda.synchronize()
+            if r >= 2:
+                times.append(a.elapsed_time(b))
+        us = statistics.median(times) * 1e3
+        n_valid = int((aw.indices >= 0).sum())
+        flops = ATTN_FLOPS_PER_SLOT_HEAD * 128 * n_valid
+        peak_tf, peak_src = measured_peak_tflops()
+        nbytes = 352 * n_valid + aw.q.numel() * 2 + ao.numel() * 2 + al.numel() * 4 + aw.indices.numel() * 4
+        out["sparse_mla_attention_nvfp4_ds_mla T=4096 H=128 top-2048"] = {
+            "units": aw.num_tokens, "us": round(us, 2), "tflops": round(flops / us / 1e6, 1),
+            "bound": "tensor", "peak_tflops": peak_tf, "peak": f"{peak_src} bf16 burst",
+            "frac": round(flops / us / 1e6 / peak_tf, 4), "gbs": round(nbytes / us / 1e3, 1),
+            "valid_slots": n_valid, "method": "CUDA events"}
+        del aw, ao, al
     # fp8_ds_mla cache fill: 2,097,152 tokens, one launch
     f4 = step.g4.fill
     times = []

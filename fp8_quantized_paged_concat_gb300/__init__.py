@@ -283,7 +283,8 @@ def kvq_sparse_mla_attention_nvfp4_ds_mla(q, indices, kv_cache, softmax_scale: f
           and q.stride(2) == 1, "q: expected a CUDA bf16 [T, H, 576] tensor with unit inner stride")
     T, H = q.shape[0], q.shape[1]
     _need(indices.dtype == torch.int32 and indices.is_cuda and indices.dim() == 2
-          and indices.shape[0] == T and indices.stride(1) == 1, "indices: expected CUDA int32 [T, topk] rows")
+          and indices.shape[0] == T and (indices.shape[1] == 0 or indices.stride(1) == 1),
+          "indices: expected CUDA int32 [T, topk] rows")
     _mla_cache("kv_cache", kv_cache, 352)
     if out is None:
         out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=q.device)
@@ -295,7 +296,7 @@ def kvq_sparse_mla_attention_nvfp4_ds_mla(q, indices, kv_cache, softmax_scale: f
         _need(lse.dtype == torch.float32 and lse.is_cuda and tuple(lse.shape) == (T, H) and lse.stride(1) == 1,
               "lse: expected a CUDA fp32 [T, H] tensor with unit inner stride")
     _call("kvq_sparse_mla_attention_nvfp4_ds_mla", q.data_ptr(), q.stride(0), q.stride(1), T, H,
-          indices.data_ptr(), indices.stride(0), indices.shape[1], kv_cache.data_ptr(), kv_cache.shape[0],
+          indices.data_ptr(), max(indices.stride(0), indices.shape[1]), indices.shape[1], kv_cache.data_ptr(), kv_cache.shape[0],
           kv_cache.shape[1], kv_cache.stride(0), kv_cache.stride(1), float(softmax_scale), out.data_ptr(),
           out.stride(0), out.stride(1), None if lse is False else lse.data_ptr(),
           0 if lse is False else lse.stride(0), _status_ptr(status), _stream(stream, q.device))
