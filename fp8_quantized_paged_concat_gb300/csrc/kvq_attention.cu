@@ -11,27 +11,32 @@
 //   s_j = scale * (q[t,h] . k_j)        k_j = the entry's 576 decoded values
 //   o[t,h] = sum_j softmax(s)_j * k_j[0:512],   lse[t,h] = log sum_j exp(s_j)
 //
-// Design (one CTA per (token, half of the 512 value dimensions)):
-//   - the token's 128 query rows (heads, zero-padded) sit in shared memory
-//     for the whole kernel as the A operand of S = Q K^T (K-major, 128-byte
-//     swizzle, 9 blocks of 64 dimensions);
-//   - per tile of 32 slots, all warps decode the 32 entries to bf16 (exact:
-//     e2m1 x e4m3 products) into a swizzled shared tile that is both the B
-//     operand of Q K^T (K-major) and, read MN-major, the V operand of P V;
-//   - one thread issues the MMAs: S (128 x 32, fp32) into TMEM columns
-//     [256, 288), the half of O (128 x 256, fp32) into TMEM columns [0, 256);
-//   - warps 0-3 own TMEM lanes 0-127 (one query row per thread): they read S,
-//     run the online softmax in the base-2 domain, round P to bf16 into
-//     shared memory (the A operand of P V) and rescale their O row in TMEM
-//     when the running maximum grows;
-//   - the denominator sums the bf16-rounded P, the values the tensor cores
-//     multiply, so the normalisation matches the weights used.
-// Both halves compute the same S: the 128 x 512 fp32 O of a full token would
-// fill all 512 TMEM columns and leave none for S.
+// Design: a cluster of two CTAs per token, one per half of the 512 value
+// dimensions.  CTA c (c = 0, 1) owns the query / key dimensions
+// [256c, 256c + 256) of the NoPE part plus the RoPE part (64 dimensions, of
+// which it multiplies the half [32c, 32c + 32)), so the 128 x 576 query block
+// is split 80 KB / 80 KB and the 36 K-steps of Q K^T split 18 / 18:
+//   - producers (8 warps) decode the CTA's share of each entry of a 64-slot
+//     tile to bf16 (exact: e2m1 x e4m3 products) into a double-buffered,
+//     128-byte-swizzled tile: the B operand of Q K^T (K-major) and, read
+//     MN-major, the V operand of P V (the CTA's 256 value columns);
+//   - one thread issues the MMAs: the partial S (128 x 64, fp32) into a TMEM
+//     double buffer, O (128 x 256, fp32) into TMEM columns [0, 256);
+//   - the softmax warps (TMEM lanes 0-127, one query row per thread) send the
+//     partial S to the peer CTA through distributed shared memory
+//     (st.async with transaction-counted mbarriers), add the peer's partial
+//     (a + b == b + a in IEEE arithmetic: both CTAs hold bit-identical
+//     scores), run the online softmax in base 2 with lazy rescaling (the
+//     reference maximum moves only when a tile exceeds it by 2^8), round P
+//     to bf16 into shared memory (the A operand of P V) and rescale their O
+//     row in TMEM when the reference moved;
+//   - the denominator sums the bf16-rounded P, the weights the tensor cores
+//     multiply.
 //
-// Every mbarrier wait is bounded; on expiry the CTA records
-// KVQ_STATUS_TIMEOUT, stops issuing work, waits (bounded) for the MMAs it has
-// in flight and frees its TMEM before it exits.
+// Every mbarrier wait is bounded; on expiry (or when another role of the CTA
+// gave up) the CTA records KVQ_STATUS_TIMEOUT, stops issuing work, waits
+// (bounded) for the MMAs in flight, frees its TMEM and meets its peer at the
+// final cluster barrier, which every path reaches exactly once.
 #include <cuda_bf16.h>
 
 #include "kvq.h"
@@ -40,27 +45,34 @@
 namespace kvq {
 namespace {
 
-constexpr int kDim = KVQ_MLA_NOPE_DIM + KVQ_MLA_ROPE_DIM;   // 576
-constexpr int kNope = KVQ_MLA_NOPE_DIM;                      // 512
-constexpr int kHalf = kNope / 2;                             // 256 value columns per CTA
+constexpr int kHalf = KVQ_MLA_NOPE_DIM / 2;                  // 256 value columns per CTA
 constexpr int kRows = 128;                                   // query rows (heads) per CTA
-constexpr int kTile = 32;                                    // slots per tile (N of Q K^T)
-constexpr int kThreads = 256;
-constexpr int kKBlocks = kDim / 64;                          // 9 swizzle blocks of 64 bf16
+constexpr int kTile = 64;                                    // slots per tile (N of Q K^T)
+constexpr int kBlocks = 5;                                   // 4 NoPE blocks + the RoPE block
+constexpr int kSoftmaxWarps = 4;                             // TMEM lanes 0-127
+constexpr int kProducerWarps = 8;
+constexpr int kRowsPerProducer = kTile / kProducerWarps;     // 8
+constexpr int kThreads = (kSoftmaxWarps + kProducerWarps + 1) * 32;   // + the MMA warp: 416
+constexpr int kMmaThread = (kSoftmaxWarps + kProducerWarps) * 32;
 constexpr int kNvRopeOff = 256, kNvSfOff = 320;
+constexpr float kRescaleLog2 = 8.0f;                         // lazy rescale threshold (base 2)
 
 // Shared memory (offsets from a 1024-byte aligned base).
 constexpr uint32_t kQBlock = kRows * 128;                    // 16 KB per 64-dim block
-constexpr uint32_t kQBytes = kKBlocks * kQBlock;             // 144 KB
-constexpr uint32_t kKBlock = kTile * 128;                    // 4 KB per 64-dim block
-constexpr uint32_t kKOff = kQBytes;
-constexpr uint32_t kKBytes = kKBlocks * kKBlock;             // 36 KB
-constexpr uint32_t kPOff = kKOff + kKBytes;
-constexpr uint32_t kPBytes = kRows * 128;                    // 16 KB (64 columns, 32 used)
-constexpr uint32_t kMiscOff = kPOff + kPBytes;
+constexpr uint32_t kKBlock = kTile * 128;                    // 8 KB per 64-dim block
+constexpr uint32_t kKBytes = kBlocks * kKBlock;              // 40 KB per buffer, 2 buffers
+constexpr uint32_t kRecvPitch = 64 * 4 + 16;                 // one row of the peer's partial S
+constexpr uint32_t kKOff = kBlocks * kQBlock;                // 80 KB of Q first
+constexpr uint32_t kPOff = kKOff + 2 * kKBytes;
+constexpr uint32_t kRecvOff = kPOff + kRows * 128;           // P: 128 x 64 bf16, 128-byte swizzle
+constexpr uint32_t kMiscOff = kRecvOff + kRows * kRecvPitch;
 constexpr uint32_t kSmemBytes = kMiscOff + 128 + 1024;       // + barriers, flags, alignment
+static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
+static_assert(kPOff % 1024 == 0 && kKOff % 1024 == 0, "swizzle atoms must be 1024-byte aligned");
 
-// TMEM columns.
+constexpr uint32_t kRecvTxBytes = kRows * 64 * 4;            // one partial S: 32 KB
+
+// TMEM columns: O [0, 256), partial S double buffer [256, 384).
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 0;
 constexpr uint32_t kSCol = 256;
@@ -68,7 +80,7 @@ constexpr uint32_t kSCol = 256;
 constexpr long long kWaitCycles = 4000000000LL;              // about 2 s at 2 GHz
 
 // ---------------------------------------------------------------------------
-// tcgen05 / mbarrier helpers (inline PTX, PTX ISA 8.7+ for sm_100a-family)
+// tcgen05 / mbarrier / cluster helpers (inline PTX, sm_100a family)
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -119,23 +131,71 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
 }
 
-// Waits for the phase with the given parity; false when the wait expired.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+               :: "r"(bar), "r"(bytes) : "memory");
+}
+
+// Arrive on a barrier of the peer CTA (address from mapa).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+               :: "r"(cluster_bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+  return done != 0;
+}
+
+// Bounded wait that also gives up when another role of the CTA has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   const long long start = clock64();
-  while (true) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done) : "r"(bar), "r"(parity) : "memory");
-    if (done) return true;
-    if (clock64() - start > kWaitCycles) return false;
-    __nanosleep(20);
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag || clock64() - start > kWaitCycles) {
+      *abort_flag = 1;
+      return false;
+    }
   }
+  return true;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
+// 16 bytes into the peer's shared memory; completes 16 bytes on its mbarrier.
+__device__ __forceinline__ void st_async16(uint32_t cluster_addr, const float* v, uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+      :: "r"(cluster_addr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
+         "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(cluster_bar)
+      : "memory");
 }
 
 // 32 consecutive fp32 TMEM columns of this warp's 32 lanes (one per thread).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   uint32_t r[32];
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -152,7 +212,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
       "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -183,6 +243,13 @@ __device__ __forceinline__ void st_shared16(uint32_t addr, const uint4& v) {
                :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
+__device__ __forceinline__ float4 ld_shared16(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
 // 8 e4m3 codes -> 8 bf16 (exact).
 __device__ __forceinline__ uint4 e4m3x8_bf16(uint2 c) {
   const float2 f0 = __half22float2(e4m3x2_to_half2(c.x));
@@ -204,21 +271,99 @@ __device__ __forceinline__ uint4 e2m1x8_bf16(uint32_t four_bytes, float scale) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// ---------------------------------------------------------------------------
+// producers: the CTA's share of a 64-slot tile
+// ---------------------------------------------------------------------------
+
+// Lane `lane` of producer warp w handles NoPE group g = lane % 16 of rows
+// 8w + lane / 16 + 2i (i < 4) and RoPE piece k = lane % 8 of rows
+// 8w + lane / 8 + 4i (i < 2).
+struct TileRegs {
+  uint2 nib[4];
+  uint32_t sf[4];
+  uint2 rope[2];
+  uint32_t valid;                        // bits 0-3: NoPE rows, bits 4-5: RoPE rows
+};
+
+__device__ __forceinline__ const uint8_t* entry_of(const AttentionArgs& a, int32_t slot) {
+  const uint32_t blk = a.block_div.div(static_cast<uint32_t>(slot));
+  const uint32_t off = static_cast<uint32_t>(slot) - blk * static_cast<uint32_t>(a.block_size);
+  return a.cache + static_cast<int64_t>(blk) * a.block_stride + static_cast<int64_t>(off) * a.entry_stride;
+}
+
+__device__ __forceinline__ void load_tile(const AttentionArgs& a, const int32_t* idx, int tile, int row0,
+                                          int lane, uint32_t half, TileRegs& e, bool& bad_index) {
+  e.valid = 0;
+  const int g = lane & 15, k = lane & 7;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int j = tile * kTile + row0 + (lane >> 4) + 2 * i;
+    const int32_t slot = j < a.topk ? __ldg(idx + j) : -1;
+    if (slot >= a.num_slots) bad_index = true;
+    if (slot >= 0 && slot < a.num_slots) {
+      const uint8_t* p = entry_of(a, slot);
+      e.valid |= 1u << i;
+      e.nib[i] = __ldg(reinterpret_cast<const uint2*>(p + 128 * half + 8 * g));
+      e.sf[i] = __ldg(p + kNvSfOff + 16 * half + g);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int j = tile * kTile + row0 + (lane >> 3) + 4 * i;
+    const int32_t slot = j < a.topk ? __ldg(idx + j) : -1;
+    if (slot >= 0 && slot < a.num_slots) {
+      e.valid |= 16u << i;
+      e.rope[i] = __ldg(reinterpret_cast<const uint2*>(entry_of(a, slot) + kNvRopeOff + 8 * k));
+    }
+  }
+}
+
+__device__ __forceinline__ void store_tile(uint32_t kbuf, int row0, int lane, const TileRegs& e) {
+  const int g = lane & 15, k = lane & 7;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t r = row0 + (lane >> 4) + 2 * i;
+    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+    if (e.valid & (1u << i)) {
+      const float scale = e4m3_to_float(e.sf[i]);
+      lo = e2m1x8_bf16(e.nib[i].x, scale);
+      hi = e2m1x8_bf16(e.nib[i].y, scale);
+    }
+    // group g: local dims 16g .. 16g+15 = block g/4, chunks 2(g%4) + {0, 1}
+    const uint32_t blk = kbuf + (g >> 2) * kKBlock;
+    st_shared16(blk + sw128_offset(r, 2 * (g & 3)), lo);
+    st_shared16(blk + sw128_offset(r, 2 * (g & 3) + 1), hi);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t r = row0 + (lane >> 3) + 4 * i;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (e.valid & (16u << i)) v = e4m3x8_bf16(e.rope[i]);
+    st_shared16(kbuf + 4 * kKBlock + sw128_offset(r, k), v);
+  }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t base = smem_u32(smem);
-  const uint32_t q_base = base, k_base = base + kKOff, p_base = base + kPOff;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kMiscOff);
-  const uint32_t bar_s = smem_u32(&bars[0]), bar_o = smem_u32(&bars[1]), bar_d = smem_u32(&bars[2]);
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kMiscOff + 24);
-  uint8_t* s_valid = smem + kMiscOff + 32;                  // [kTile]
+  const uint32_t q_base = base, p_base = base + kPOff, recv_base = base + kRecvOff;
+  const uint32_t k_base[2] = {base + kKOff, base + kKOff + kKBytes};
+  const uint32_t bar0 = base + kMiscOff;
+  const uint32_t k_full[2] = {bar0, bar0 + 8}, k_empty[2] = {bar0 + 16, bar0 + 24};
+  const uint32_t s_full[2] = {bar0 + 32, bar0 + 40};
+  const uint32_t p_full = bar0 + 48, o_done = bar0 + 56, drain = bar0 + 64;
+  const uint32_t x_full = bar0 + 72;     // the peer's partial S has landed here
+  const uint32_t x_empty = bar0 + 80;    // the peer has read the partial S sent to it
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kMiscOff + 96);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kMiscOff + 100);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t token = blockIdx.x >> 1;
-  const int half = blockIdx.x & 1;
+  const uint32_t half = cluster_rank();
+  const uint32_t peer = half ^ 1u;
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -226,124 +371,109 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (threadIdx.x == 32) {
-    mbar_init(bar_s, 1);
-    mbar_init(bar_o, 1);
-    mbar_init(bar_d, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(k_full[b], kProducerWarps);
+      mbar_init(k_empty[b], 1);
+      mbar_init(s_full[b], 1);
+    }
+    mbar_init(p_full, kSoftmaxWarps);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    mbar_init(x_full, 1);
+    mbar_init(x_empty, kSoftmaxWarps);
+    *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
 
-  // Query rows -> swizzled K-major blocks (rows >= num_heads are zero).
+  // The CTA's query dimensions -> swizzled K-major blocks: blocks 0-3 = NoPE
+  // [256 half, +256), block 4 = RoPE; rows >= num_heads are zero.
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + token * a.q_stride_t;
-  for (int i = threadIdx.x; i < kRows * (kDim / 8); i += kThreads) {
-    const int row = i / (kDim / 8), c = i % (kDim / 8);
+  for (int i = threadIdx.x; i < kRows * kBlocks * 8; i += kThreads) {
+    const int row = i / (kBlocks * 8), c = i % (kBlocks * 8);
+    const int blk = c >> 3;
+    const int dim = (blk < 4 ? static_cast<int>(kHalf * half) + 64 * blk : KVQ_MLA_NOPE_DIM) + 8 * (c & 7);
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (row < a.num_heads) v = __ldg(reinterpret_cast<const uint4*>(q + row * a.q_stride_h + 8 * c));
-    st_shared16(q_base + (c >> 3) * kQBlock + sw128_offset(row, c & 7), v);
+    if (row < a.num_heads) v = __ldg(reinterpret_cast<const uint4*>(q + row * a.q_stride_h + dim));
+    st_shared16(q_base + blk * kQBlock + sw128_offset(row, c & 7), v);
   }
   fence_async_smem();
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *s_tmem;
+  cluster_sync();                        // the peer's barriers are initialised from here on
 
   const int32_t* idx = a.indices + token * a.indices_stride;
   const int n_tiles = (a.topk + kTile - 1) / kTile;
-  constexpr uint32_t kIdescQK = idesc_bf16(kRows, kTile, false);
-  constexpr uint32_t kIdescPV = idesc_bf16(kRows, kHalf, true);
+  bool bad_index = false;
+  int mma_issued = 0;                    // MMA thread: any MMA issued
+  float m = -INFINITY, l = 0.0f;         // softmax rows: reference max (base 2) and sum
 
-  float m = -INFINITY, l = 0.0f;           // running max (base 2) and sum of row threadIdx.x
-  const uint32_t row_lane = static_cast<uint32_t>(warp & 3) * 32u << 16;
-  int mma_tiles = 0;                       // tiles whose S MMAs were issued (block-uniform)
-  int pv_tiles = 0;                        // tiles whose P V MMAs were issued (block-uniform)
-  bool bad_index = false, aborted = false;
-
-  for (int tile = 0; tile < n_tiles; ++tile) {
-    int expired = 0;
-    // The previous P V must be done before its operands are overwritten.
-    if (tile > 0 && !mbar_wait(bar_o, (tile - 1) & 1)) expired = 1;
-
-    // Decode this tile's entries: warp w takes rows 4w .. 4w+3.
-    {
-      uint2 nib[4];
-      uint32_t sf[4];
-      uint2 rope[4];
-      bool valid[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int r = warp * 4 + k, j = tile * kTile + r;
-        const int32_t slot = j < a.topk ? __ldg(idx + j) : -1;
-        valid[k] = slot >= 0 && slot < a.num_slots;
-        if (slot >= a.num_slots) bad_index = true;
-        if (valid[k]) {
-          const uint32_t blk = a.block_div.div(static_cast<uint32_t>(slot));
-          const uint32_t off = static_cast<uint32_t>(slot) - blk * static_cast<uint32_t>(a.block_size);
-          const uint8_t* e = a.cache + static_cast<int64_t>(blk) * a.block_stride +
-                             static_cast<int64_t>(off) * a.entry_stride;
-          nib[k] = __ldg(reinterpret_cast<const uint2*>(e + 8 * lane));
-          sf[k] = __ldg(e + kNvSfOff + lane);
-          if (lane < 8) rope[k] = __ldg(reinterpret_cast<const uint2*>(e + kNvRopeOff + 8 * lane));
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t r = warp * 4 + k;
-        uint4 lo = make_uint4(0, 0, 0, 0), hi = lo, rp = lo;
-        if (valid[k]) {
-          const float scale = e4m3_to_float(sf[k]);
-          lo = e2m1x8_bf16(nib[k].x, scale);
-          hi = e2m1x8_bf16(nib[k].y, scale);
-          if (lane < 8) rp = e4m3x8_bf16(rope[k]);
-        }
-        // NoPE group `lane`: dims 16*lane .. 16*lane+15 = block lane/4, chunks 2*(lane%4) + {0,1}
-        const uint32_t blk = k_base + (lane >> 2) * kKBlock;
-        st_shared16(blk + sw128_offset(r, 2 * (lane & 3)), lo);
-        st_shared16(blk + sw128_offset(r, 2 * (lane & 3) + 1), hi);
-        if (lane < 8) st_shared16(k_base + 8 * kKBlock + sw128_offset(r, lane), rp);
-        if (lane == 0) s_valid[r] = valid[k] ? 1 : 0;
-      }
-    }
-    fence_async_smem();
-    fence_before_sync();
-    if (__syncthreads_or(expired)) { aborted = true; break; }
-    mma_tiles = tile + 1;
-
-    // S = Q K^T over 576 dims: 36 MMAs of K = 16.
-    if (threadIdx.x == 0) {
+  if (warp < kSoftmaxWarps) {
+    // ---- softmax: thread = query row ------------------------------------
+    const uint32_t row_lane = static_cast<uint32_t>(warp) * 32u << 16;
+    const uint32_t row = threadIdx.x;
+    const uint32_t my_recv = recv_base + row * kRecvPitch;
+    const uint32_t peer_recv = map_to_rank(my_recv, peer);
+    const uint32_t peer_x_full = map_to_rank(x_full, peer);
+    const uint32_t peer_x_empty = map_to_rank(x_empty, peer);
+    // x_full is armed for a tile's 32 KB before the peer can send it: tile 0
+    // here, tile t + 1 once tile t has landed and before the peer is told it
+    // may send again.
+    if (row == 0 && n_tiles > 0) mbar_arrive_expect_tx(x_full, kRecvTxBytes);
+    for (int t = 0; t < n_tiles; ++t) {
+      // validity of the tile's 64 slots, two per lane
+      const int j = t * kTile + lane;
+      const int32_t s0 = j < a.topk ? __ldg(idx + j) : -1;
+      const int32_t s1 = j + 32 < a.topk ? __ldg(idx + j + 32) : -1;
+      const uint32_t vm0 = __ballot_sync(0xffffffffu, s0 >= 0 && s0 < a.num_slots);
+      const uint32_t vm1 = __ballot_sync(0xffffffffu, s1 >= 0 && s1 < a.num_slots);
+      if (!wait_or_abort(s_full[t & 1], (t >> 1) & 1, s_abort)) break;
       fence_after_sync();
-#pragma unroll 4
-      for (int k = 0; k < kDim / 16; ++k) {
-        const uint32_t kb = k >> 2, kk = (k & 3) * 32;
-        mma_bf16(tmem + kSCol, sw128_desc(q_base + kb * kQBlock + kk, 16, 1024),
-                 sw128_desc(k_base + kb * kKBlock + kk, 16, 1024), kIdescQK, k > 0);
+      float s[64];
+      tmem_ld32(tmem + row_lane + kSCol + kTile * (t & 1), s);
+      tmem_ld32(tmem + row_lane + kSCol + kTile * (t & 1) + 32, s + 32);
+      // partial S -> the peer (its previous one must have been read)
+      if (t > 0 && !wait_or_abort(x_empty, (t - 1) & 1, s_abort)) break;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) st_async16(peer_recv + 16 * c, s + 4 * c, peer_x_full);
+      if (!wait_or_abort(x_full, t & 1, s_abort)) break;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float4 v = ld_shared16(my_recv + 16 * c);
+        s[4 * c] += v.x;
+        s[4 * c + 1] += v.y;
+        s[4 * c + 2] += v.z;
+        s[4 * c + 3] += v.w;
       }
-      mma_commit(bar_s);
-    }
-
-    if (warp < 4) {
-      if (!mbar_wait(bar_s, tile & 1)) expired = 1;
-      fence_after_sync();
-      float s[32];
-      tmem_ld32(tmem + row_lane + kSCol, s);
+      if (row == 0 && t + 1 < n_tiles) mbar_arrive_expect_tx(x_full, kRecvTxBytes);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(peer_x_empty);
       float tmax = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        s[j] = s_valid[j] ? s[j] * a.scale_log2 : -INFINITY;
-        tmax = fmaxf(tmax, s[j]);
+      for (int i = 0; i < 64; ++i) {
+        const bool ok = ((i < 32 ? vm0 : vm1) >> (i & 31)) & 1u;
+        s[i] = ok ? s[i] * a.scale_log2 : -INFINITY;
+        tmax = fmaxf(tmax, s[i]);
       }
-      const float m_new = fmaxf(m, tmax);
-      const float m_use = m_new == -INFINITY ? 0.0f : m_new;
-      const float alpha = exp2f(m - m_use);             // 0 while m is -inf
-      uint32_t pk[16];
+      // Lazy rescaling: the reference max moves only when the tile's max
+      // exceeds it by more than 2^8 (weights stay below 256 otherwise).
+      const bool grow = tmax > m + kRescaleLog2;
+      const float alpha = grow ? exp2f(m - tmax) : 1.0f;          // 0 while m is -inf
+      if (grow) m = tmax;
+      const float m_use = m == -INFINITY ? 0.0f : m;
+      uint32_t pk[32];
       float psum = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        pk[j] = pack_bf16x2(exp2f(s[2 * j] - m_use), exp2f(s[2 * j + 1] - m_use));
-        psum += bf16_lo(pk[j]) + bf16_hi(pk[j]);
+      for (int i = 0; i < 32; ++i) {
+        pk[i] = pack_bf16x2(exp2f(s[2 * i] - m_use), exp2f(s[2 * i + 1] - m_use));
+        psum += bf16_lo(pk[i]) + bf16_hi(pk[i]);
       }
       l = l * alpha + psum;
-      m = m_new;
-      // Rescale this row's O when the maximum grew (warp-wide TMEM access).
-      if (tile > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+      // P V of the previous tile must be done: it reads P, and O is rescaled.
+      if (t > 0 && !wait_or_abort(o_done, (t - 1) & 1, s_abort)) break;
+      if (t > 0 && __any_sync(0xffffffffu, grow)) {
+        fence_after_sync();
 #pragma unroll 1
         for (int c = 0; c < kHalf / 32; ++c) {
           float o[32];
@@ -353,53 +483,96 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
           tmem_st32(tmem + row_lane + kOCol + 32 * c, o);
         }
       }
-      const uint32_t row = threadIdx.x;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        st_shared16(p_base + sw128_offset(row, c),
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
+      for (int c = 0; c < 8; ++c)
+        st_shared16(p_base + sw128_offset(row, c), make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                                                              pk[4 * c + 3]));
       fence_async_smem();
       fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
     }
-    if (__syncthreads_or(expired)) { aborted = true; break; }
-
-    // O[:, half] += P V: 2 MMAs of K = 16 slots, N = 256 value columns.
-    if (threadIdx.x == 0) {
+    if (n_tiles > 0) wait_or_abort(o_done, (n_tiles - 1) & 1, s_abort);
+  } else if (warp < kSoftmaxWarps + kProducerWarps) {
+    // ---- producers: decode tiles into the double-buffered K tile ---------
+    const int row0 = (warp - kSoftmaxWarps) * kRowsPerProducer;
+    TileRegs cur, nxt;
+    if (n_tiles > 0) load_tile(a, idx, 0, row0, lane, half, cur, bad_index);
+    for (int t = 0; t < n_tiles; ++t) {
+      if (t + 1 < n_tiles) load_tile(a, idx, t + 1, row0, lane, half, nxt, bad_index);
+      if (t >= 2 && !wait_or_abort(k_empty[t & 1], ((t - 2) >> 1) & 1, s_abort)) break;
+      store_tile(k_base[t & 1], row0, lane, cur);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(k_full[t & 1]);
+      cur = nxt;
+    }
+  } else if (lane == 0) {
+    // ---- MMA issue (one thread) -------------------------------------------
+    constexpr uint32_t kIdescQK = idesc_bf16(kRows, kTile, false);
+    constexpr uint32_t kIdescPV = idesc_bf16(kRows, kHalf, true);
+    for (int t = 0; t < n_tiles; ++t) {
+      for (int u = (t == 0 ? 0 : t + 1); u <= t + 1 && u < n_tiles; ++u) {
+        // partial S[u & 1] = Q_c K_c(u)^T: 16 NoPE K-steps + 2 RoPE K-steps
+        if (!wait_or_abort(k_full[u & 1], (u >> 1) & 1, s_abort)) goto mma_done;
+        fence_after_sync();
+        const uint32_t d = tmem + kSCol + kTile * (u & 1);
+#pragma unroll
+        for (int k = 0; k < 18; ++k) {
+          const uint32_t blk = k < 16 ? k >> 2 : 4;
+          const uint32_t kk = (k < 16 ? (k & 3) : 2 * half + (k - 16)) * 32;
+          mma_bf16(d, sw128_desc(q_base + blk * kQBlock + kk, 16, 1024),
+                   sw128_desc(k_base[u & 1] + blk * kKBlock + kk, 16, 1024), kIdescQK, k > 0);
+        }
+        mma_commit(s_full[u & 1]);
+        mma_issued = 1;
+      }
+      // O += P(t) V(t): 4 MMAs of K = 16 slots, N = 256 value columns
+      if (!wait_or_abort(p_full, t & 1, s_abort)) break;
       fence_after_sync();
 #pragma unroll
       for (int k = 0; k < kTile / 16; ++k)
         mma_bf16(tmem + kOCol, sw128_desc(p_base + 32 * k, 16, 1024),
-                 sw128_desc(k_base + (4 * half) * kKBlock + 2048 * k, kKBlock, 1024), kIdescPV,
-                 (tile > 0 || k > 0) ? 1u : 0u);
-      mma_commit(bar_o);
+                 sw128_desc(k_base[t & 1] + 2048 * k, kKBlock, 1024), kIdescPV,
+                 (t > 0 || k > 0) ? 1u : 0u);
+      mma_commit(k_empty[t & 1]);
+      mma_commit(o_done);
     }
-    pv_tiles = tile + 1;
+  mma_done:;
   }
 
   // Drain every MMA still in flight: one more commit tracks all of them.
-  if (mma_tiles > 0) {
-    if (threadIdx.x == 0) mma_commit(bar_d);
-    if (!mbar_wait(bar_d, 0)) aborted = true;
+  fence_before_sync();
+  const bool any_mma = __syncthreads_or(mma_issued) != 0;
+  fence_after_sync();
+  bool aborted = *s_abort != 0;
+  if (any_mma) {
+    if (threadIdx.x == kMmaThread) mma_commit(drain);
+    const long long start = clock64();
+    while (!mbar_try_wait(drain, 0)) {     // bounded, ignores the abort flag
+      if (clock64() - start > kWaitCycles) { aborted = true; break; }
+    }
   }
   fence_after_sync();
   if (bad_index && a.status) atomicOr(a.status, KVQ_STATUS_BAD_INDEX);
   aborted = __syncthreads_or(aborted) != 0;
   if (aborted && threadIdx.x == 0 && a.status) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
 
-  if (warp < 4 && !aborted) {
+  if (warp < kSoftmaxWarps && !aborted) {
+    const uint32_t row_lane = static_cast<uint32_t>(warp) * 32u << 16;
     const int row = threadIdx.x;
     const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + token * a.out_stride_t +
-                         static_cast<int64_t>(row) * a.out_stride_h + half * kHalf;
+                         static_cast<int64_t>(row) * a.out_stride_h + kHalf * half;
 #pragma unroll 1
     for (int c = 0; c < kHalf / 32; ++c) {
       float o[32];
-      if (pv_tiles > 0) tmem_ld32(tmem + row_lane + kOCol + 32 * c, o);
+      if (n_tiles > 0) tmem_ld32(tmem + row_lane + kOCol + 32 * c, o);
       if (row < a.num_heads) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           uint4 v = make_uint4(0, 0, 0, 0);
-          if (pv_tiles > 0)
+          if (n_tiles > 0)
             v = make_uint4(pack_bf16x2(o[8 * i] * inv_l, o[8 * i + 1] * inv_l),
                            pack_bf16x2(o[8 * i + 2] * inv_l, o[8 * i + 3] * inv_l),
                            pack_bf16x2(o[8 * i + 4] * inv_l, o[8 * i + 5] * inv_l),
@@ -420,6 +593,9 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
                  :: "r"(tmem), "r"(kTmemCols) : "memory");
   }
+  // Neither CTA leaves while the peer may still write into its shared memory
+  // or arrive on its barriers.
+  cluster_sync();
 }
 
 }  // namespace
