@@ -49,33 +49,42 @@ constexpr int kHalf = KVQ_MLA_NOPE_DIM / 2;                  // 256 value column
 constexpr int kRows = 128;                                   // query rows (heads) per CTA
 constexpr int kTile = 64;                                    // slots per tile (N of Q K^T)
 constexpr int kBlocks = 5;                                   // 4 NoPE blocks + the RoPE block
-constexpr int kSoftmaxWarps = 4;                             // TMEM lanes 0-127
-constexpr int kProducerWarps = 8;
-constexpr int kRowsPerProducer = kTile / kProducerWarps;     // 8
+// Warp roles: 0-3 softmax (columns 0-31), 4-7 producers, 8-11 softmax
+// (columns 32-63), 12 MMA.  Softmax warp w reads TMEM lanes 32 (w % 4) ..
+// +31, so warps w and w + 8 share the query rows 32 (w % 4) .. +31.
+constexpr int kSoftmaxWarps = 8;
+constexpr int kProducerWarps = 4;
+constexpr int kProducerWarp0 = 4;
+constexpr int kRowsPerProducer = kTile / kProducerWarps;     // 16
 constexpr int kThreads = (kSoftmaxWarps + kProducerWarps + 1) * 32;   // + the MMA warp: 416
-constexpr int kMmaThread = (kSoftmaxWarps + kProducerWarps) * 32;
+constexpr int kMmaThread = 12 * 32;
 constexpr int kNvRopeOff = 256, kNvSfOff = 320;
 constexpr float kRescaleLog2 = 8.0f;                         // lazy rescale threshold (base 2)
 
 // Shared memory (offsets from a 1024-byte aligned base).
-constexpr uint32_t kQBlock = kRows * 128;                    // 16 KB per 64-dim block
+constexpr int kKStages = 3;                                  // K tiles in flight
+constexpr uint32_t kQBlock = kRows * 128;                    // the RoPE query block: 16 KB
 constexpr uint32_t kKBlock = kTile * 128;                    // 8 KB per 64-dim block
-constexpr uint32_t kKBytes = kBlocks * kKBlock;              // 40 KB per buffer, 2 buffers
+constexpr uint32_t kKBytes = kBlocks * kKBlock;              // 40 KB per K stage
 constexpr uint32_t kRecvPitch = 64 * 4 + 16;                 // one row of the peer's partial S
-constexpr uint32_t kKOff = kBlocks * kQBlock;                // 80 KB of Q first
-constexpr uint32_t kPOff = kKOff + 2 * kKBytes;
+constexpr uint32_t kKOff = kQBlock;
+constexpr uint32_t kPOff = kKOff + kKStages * kKBytes;
 constexpr uint32_t kRecvOff = kPOff + kRows * 128;           // P: 128 x 64 bf16, 128-byte swizzle
-constexpr uint32_t kMiscOff = kRecvOff + kRows * kRecvPitch;
+constexpr uint32_t kPairOff = kRecvOff + kRows * kRecvPitch; // per-row maxima of the two column halves
+constexpr uint32_t kMiscOff = kPairOff + 2 * 2 * kRows * 4;  // [tile parity][half][row]
 constexpr uint32_t kSmemBytes = kMiscOff + 128 + 1024;       // + barriers, flags, alignment
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
 static_assert(kPOff % 1024 == 0 && kKOff % 1024 == 0, "swizzle atoms must be 1024-byte aligned");
 
 constexpr uint32_t kRecvTxBytes = kRows * 64 * 4;            // one partial S: 32 KB
 
-// TMEM columns: O [0, 256), partial S double buffer [256, 384).
+// TMEM columns: O [0, 256), the CTA's 256 NoPE query dimensions as bf16
+// pairs [256, 384) (the A operand of the NoPE K-steps), partial S double
+// buffer [384, 512).
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 0;
-constexpr uint32_t kSCol = 256;
+constexpr uint32_t kQCol = 256;
+constexpr uint32_t kSCol = 384;
 
 constexpr long long kWaitCycles = 4000000000LL;              // about 2 s at 2 GHz
 
@@ -109,6 +118,16 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
       :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// The same with A in TMEM: row i in lane i, element pairs (2c, 2c+1) of its
+// 16 K-elements in columns a_tmem + c (the lower-indexed element in the low half).
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      :: "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -250,6 +269,27 @@ __device__ __forceinline__ float4 ld_shared16(uint32_t addr) {
   return v;
 }
 
+// 2^x for x <= 0 (0 for -inf): the hardware approximation, relative error
+// below 2^-22, flushed to zero below 2^-126 (weights that small vanish next
+// to the largest weight, which is at least 2^-8).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a), y = *reinterpret_cast<__nv_bfloat162*>(&b);
+  __nv_bfloat162 r = __hmul2(x, y);
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
 // 8 e4m3 codes -> 8 bf16 (exact).
 __device__ __forceinline__ uint4 e4m3x8_bf16(uint2 c) {
   const float2 f0 = __half22float2(e4m3x2_to_half2(c.x));
@@ -260,13 +300,42 @@ __device__ __forceinline__ uint4 e4m3x8_bf16(uint2 c) {
                     pack_bf16x2(f3.x, f3.y));
 }
 
-// 4 bytes of e2m1 pairs times one scale -> 8 bf16 (exact products).
-__device__ __forceinline__ uint4 e2m1x8_bf16(uint32_t four_bytes, float scale) {
+// One NVFP4 group as bf16 without conversion instructions.  The eight
+// products m * sf (m = 0, 0.5, 1, 1.5, 2, 3, 4, 6) are exact in bf16 (at most
+// 6 significant bits, inside e4m3's range), so they are formed once per group
+// with four bf16x2 multiplies; each code then selects its product's low and
+// high byte with byte permutes (the code's magnitude is the byte index) and
+// its sign bit is copied to bit 15.
+struct GroupTable {
+  uint32_t lo_a, lo_b, hi_a, hi_b;       // low / high bytes of products 0-3 and 4-7
+};
+
+__device__ __forceinline__ GroupTable group_table(uint32_t sf_code) {
+  const uint32_t sf = __float_as_uint(e4m3_to_float(sf_code)) >> 16;   // exact bf16
+  const uint32_t sf2 = sf | (sf << 16);
+  const uint32_t t0 = bf16x2_mul(0x3F000000u, sf2);   // (0, 0.5) * sf
+  const uint32_t t1 = bf16x2_mul(0x3FC03F80u, sf2);   // (1, 1.5) * sf
+  const uint32_t t2 = bf16x2_mul(0x40404000u, sf2);   // (2, 3) * sf
+  const uint32_t t3 = bf16x2_mul(0x40C04080u, sf2);   // (4, 6) * sf
+  return {prmt(t0, t1, 0x6420), prmt(t2, t3, 0x6420), prmt(t0, t1, 0x7531), prmt(t2, t3, 0x7531)};
+}
+
+// 4 bytes of codes (8 values, value 2k in the low nibble of byte k) -> 8 bf16.
+__device__ __forceinline__ uint4 e2m1x8_lut(uint32_t x, const GroupTable& t) {
+  const uint32_t mag_even = x & 0x07070707u, mag_odd = (x >> 4) & 0x07070707u;
+  const uint32_t sign = x & 0x88888888u;
   uint32_t o[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 v = __half22float2(e2m1x2_to_half2(four_bytes >> (8 * i)));
-    o[i] = pack_bf16x2(v.x * scale, v.y * scale);
+  for (int k = 0; k < 4; ++k) {
+    // selector: magnitude of value 2k in nibble 0, of value 2k+1 in nibble 2
+    const uint32_t sel = prmt(mag_even, mag_odd, static_cast<uint32_t>(k | ((4 + k) << 4)));
+    const uint32_t lo = prmt(t.lo_a, t.lo_b, sel);          // bytes 0, 2: low bytes
+    const uint32_t hi = prmt(t.hi_a, t.hi_b, sel << 4);     // bytes 1, 3: high bytes
+    // byte k of the sign bits into bytes 1 and 3 (zeros elsewhere): bit 11
+    // (value 2k) moves to bit 15, bit 31 (value 2k+1) stays; XOR, so that a
+    // negative scale byte gives the product's sign
+    const uint32_t sg = prmt(sign, 0, static_cast<uint32_t>(0x0404 | (k << 4) | (k << 12)));
+    o[k] = ((lo & 0x00FF00FFu) | (hi & 0xFF00FF00u)) ^ (((sg << 4) & 0x00008000u) | (sg & 0x80000000u));
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
@@ -275,14 +344,15 @@ __device__ __forceinline__ uint4 e2m1x8_bf16(uint32_t four_bytes, float scale) {
 // producers: the CTA's share of a 64-slot tile
 // ---------------------------------------------------------------------------
 
-// Lane `lane` of producer warp w handles NoPE group g = lane % 16 of rows
-// 8w + lane / 16 + 2i (i < 4) and RoPE piece k = lane % 8 of rows
-// 8w + lane / 8 + 4i (i < 2).
+// Producer warp w (rows 16w .. 16w+15 of the tile): lane `lane` handles NoPE
+// group g = lane % 16 of rows 16w + lane / 16 + 2i (i < 8) and RoPE piece
+// k = lane % 4 (the CTA's 32 RoPE values are pieces 4 half + k) of rows
+// 16w + lane / 4 + 8i (i < 2).
 struct TileRegs {
-  uint2 nib[4];
-  uint32_t sf[4];
+  uint2 nib[8];
+  uint32_t sf[8];
   uint2 rope[2];
-  uint32_t valid;                        // bits 0-3: NoPE rows, bits 4-5: RoPE rows
+  uint32_t valid;                        // bits 0-7: NoPE rows, bits 8-9: RoPE rows
 };
 
 __device__ __forceinline__ const uint8_t* entry_of(const AttentionArgs& a, int32_t slot) {
@@ -291,15 +361,23 @@ __device__ __forceinline__ const uint8_t* entry_of(const AttentionArgs& a, int32
   return a.cache + static_cast<int64_t>(blk) * a.block_stride + static_cast<int64_t>(off) * a.entry_stride;
 }
 
-__device__ __forceinline__ void load_tile(const AttentionArgs& a, const int32_t* idx, int tile, int row0,
-                                          int lane, uint32_t half, TileRegs& e, bool& bad_index) {
+// Slot of row row0 + lane % 16 of a tile (-1 past top-k).
+__device__ __forceinline__ int32_t tile_slot(const AttentionArgs& a, const int32_t* idx, int tile, int row0,
+                                             int lane) {
+  const int j = tile * kTile + row0 + (lane & 15);
+  return j < a.topk ? __ldg(idx + j) : -1;
+}
+
+// Issues the tile's entry loads; `mine` = tile_slot(...) of this lane, read
+// a tile earlier so that the loads need not wait for it.
+__device__ __forceinline__ void load_tile(const AttentionArgs& a, int32_t mine, int lane, uint32_t half,
+                                          TileRegs& e, bool& bad_index) {
+  if (mine >= a.num_slots) bad_index = true;
   e.valid = 0;
-  const int g = lane & 15, k = lane & 7;
+  const int g = lane & 15, k = lane & 3;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int j = tile * kTile + row0 + (lane >> 4) + 2 * i;
-    const int32_t slot = j < a.topk ? __ldg(idx + j) : -1;
-    if (slot >= a.num_slots) bad_index = true;
+  for (int i = 0; i < 8; ++i) {
+    const int32_t slot = __shfl_sync(0xffffffffu, mine, (lane >> 4) + 2 * i);
     if (slot >= 0 && slot < a.num_slots) {
       const uint8_t* p = entry_of(a, slot);
       e.valid |= 1u << i;
@@ -309,25 +387,24 @@ __device__ __forceinline__ void load_tile(const AttentionArgs& a, const int32_t*
   }
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const int j = tile * kTile + row0 + (lane >> 3) + 4 * i;
-    const int32_t slot = j < a.topk ? __ldg(idx + j) : -1;
+    const int32_t slot = __shfl_sync(0xffffffffu, mine, (lane >> 2) + 8 * i);
     if (slot >= 0 && slot < a.num_slots) {
-      e.valid |= 16u << i;
-      e.rope[i] = __ldg(reinterpret_cast<const uint2*>(entry_of(a, slot) + kNvRopeOff + 8 * k));
+      e.valid |= 256u << i;
+      e.rope[i] = __ldg(reinterpret_cast<const uint2*>(entry_of(a, slot) + kNvRopeOff + 32 * half + 8 * k));
     }
   }
 }
 
-__device__ __forceinline__ void store_tile(uint32_t kbuf, int row0, int lane, const TileRegs& e) {
-  const int g = lane & 15, k = lane & 7;
+__device__ __forceinline__ void store_tile(uint32_t kbuf, int row0, int lane, uint32_t half, const TileRegs& e) {
+  const int g = lane & 15, k = lane & 3;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < 8; ++i) {
     const uint32_t r = row0 + (lane >> 4) + 2 * i;
     uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
     if (e.valid & (1u << i)) {
-      const float scale = e4m3_to_float(e.sf[i]);
-      lo = e2m1x8_bf16(e.nib[i].x, scale);
-      hi = e2m1x8_bf16(e.nib[i].y, scale);
+      const GroupTable t = group_table(e.sf[i]);
+      lo = e2m1x8_lut(e.nib[i].x, t);
+      hi = e2m1x8_lut(e.nib[i].y, t);
     }
     // group g: local dims 16g .. 16g+15 = block g/4, chunks 2(g%4) + {0, 1}
     const uint32_t blk = kbuf + (g >> 2) * kKBlock;
@@ -336,10 +413,10 @@ __device__ __forceinline__ void store_tile(uint32_t kbuf, int row0, int lane, co
   }
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const uint32_t r = row0 + (lane >> 3) + 4 * i;
+    const uint32_t r = row0 + (lane >> 2) + 8 * i;
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (e.valid & (16u << i)) v = e4m3x8_bf16(e.rope[i]);
-    st_shared16(kbuf + 4 * kKBlock + sw128_offset(r, k), v);
+    if (e.valid & (256u << i)) v = e4m3x8_bf16(e.rope[i]);
+    st_shared16(kbuf + 4 * kKBlock + sw128_offset(r, 4 * half + k), v);
   }
 }
 
@@ -349,21 +426,23 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t base = smem_u32(smem);
-  const uint32_t q_base = base, p_base = base + kPOff, recv_base = base + kRecvOff;
-  const uint32_t k_base[2] = {base + kKOff, base + kKOff + kKBytes};
+  const uint32_t qr_base = base, p_base = base + kPOff, recv_base = base + kRecvOff;
+  float* s_pair = reinterpret_cast<float*>(smem + kPairOff);        // [2][2][kRows]
   const uint32_t bar0 = base + kMiscOff;
-  const uint32_t k_full[2] = {bar0, bar0 + 8}, k_empty[2] = {bar0 + 16, bar0 + 24};
-  const uint32_t s_full[2] = {bar0 + 32, bar0 + 40};
-  const uint32_t p_full = bar0 + 48, o_done = bar0 + 56, drain = bar0 + 64;
-  const uint32_t x_full = bar0 + 72;     // the peer's partial S has landed here
-  const uint32_t x_empty = bar0 + 80;    // the peer has read the partial S sent to it
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kMiscOff + 96);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kMiscOff + 100);
+  // k_full[3], k_empty[3], s_full[2], p_full, o_done, drain, x_full, x_empty
+  const uint32_t k_full0 = bar0, k_empty0 = bar0 + 24;
+  const uint32_t s_full[2] = {bar0 + 48, bar0 + 56};
+  const uint32_t p_full = bar0 + 64, o_done = bar0 + 72, drain = bar0 + 80;
+  const uint32_t x_full = bar0 + 88;     // the peer's partial S has landed here
+  const uint32_t x_empty = bar0 + 96;    // the peer has read the partial S sent to it
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kMiscOff + 112);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kMiscOff + 116);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t token = blockIdx.x >> 1;
   const uint32_t half = cluster_rank();
   const uint32_t peer = half ^ 1u;
+  const bool is_softmax = warp < 4 || (warp >= 8 && warp < 12);
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -371,11 +450,11 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (threadIdx.x == 32) {
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(k_full[b], kProducerWarps);
-      mbar_init(k_empty[b], 1);
-      mbar_init(s_full[b], 1);
+    for (int b = 0; b < kKStages; ++b) {
+      mbar_init(k_full0 + 8 * b, kProducerWarps);
+      mbar_init(k_empty0 + 8 * b, 1);
     }
+    for (int b = 0; b < 2; ++b) mbar_init(s_full[b], 1);
     mbar_init(p_full, kSoftmaxWarps);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
@@ -385,88 +464,115 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
 
-  // The CTA's query dimensions -> swizzled K-major blocks: blocks 0-3 = NoPE
-  // [256 half, +256), block 4 = RoPE; rows >= num_heads are zero.
+  // The CTA's 32 RoPE query dimensions -> chunks 4 half .. 4 half + 3 of a
+  // swizzled K-major block (rows >= num_heads are zero).
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + token * a.q_stride_t;
-  for (int i = threadIdx.x; i < kRows * kBlocks * 8; i += kThreads) {
-    const int row = i / (kBlocks * 8), c = i % (kBlocks * 8);
-    const int blk = c >> 3;
-    const int dim = (blk < 4 ? static_cast<int>(kHalf * half) + 64 * blk : KVQ_MLA_NOPE_DIM) + 8 * (c & 7);
+  for (int i = threadIdx.x; i < kRows * 4; i += kThreads) {
+    const int row = i >> 2, c = i & 3;
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (row < a.num_heads) v = __ldg(reinterpret_cast<const uint4*>(q + row * a.q_stride_h + dim));
-    st_shared16(q_base + blk * kQBlock + sw128_offset(row, c & 7), v);
+    if (row < a.num_heads)
+      v = __ldg(reinterpret_cast<const uint4*>(q + row * a.q_stride_h + KVQ_MLA_NOPE_DIM + 32 * half + 8 * c));
+    st_shared16(qr_base + sw128_offset(row, 4 * half + c), v);
   }
   fence_async_smem();
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *s_tmem;
+  // The CTA's 256 NoPE query dimensions -> TMEM (softmax warps: lane = row,
+  // warp w < 4 dims 0-127, warp w + 8 dims 128-255 of the half).
+  if (is_softmax) {
+    const uint32_t quad = warp & 3, ch = warp >> 3;
+    const int row = quad * 32 + lane;
+    const uint4* src = reinterpret_cast<const uint4*>(q + row * a.q_stride_h + kHalf * half + 128 * ch);
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {            // 64 dims = 32 columns per part
+      float w[32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = row < a.num_heads ? __ldg(src + 8 * part + i) : make_uint4(0, 0, 0, 0);
+        w[4 * i] = __uint_as_float(v.x);
+        w[4 * i + 1] = __uint_as_float(v.y);
+        w[4 * i + 2] = __uint_as_float(v.z);
+        w[4 * i + 3] = __uint_as_float(v.w);
+      }
+      tmem_st32(tmem + (quad * 32u << 16) + kQCol + 64 * ch + 32 * part, w);
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
   cluster_sync();                        // the peer's barriers are initialised from here on
 
   const int32_t* idx = a.indices + token * a.indices_stride;
   const int n_tiles = (a.topk + kTile - 1) / kTile;
   bool bad_index = false;
   int mma_issued = 0;                    // MMA thread: any MMA issued
-  float m = -INFINITY, l = 0.0f;         // softmax rows: reference max (base 2) and sum
+  float m = -INFINITY, l = 0.0f;         // softmax: reference max (base 2), partial sum of the row
 
-  if (warp < kSoftmaxWarps) {
-    // ---- softmax: thread = query row ------------------------------------
-    const uint32_t row_lane = static_cast<uint32_t>(warp) * 32u << 16;
-    const uint32_t row = threadIdx.x;
-    const uint32_t my_recv = recv_base + row * kRecvPitch;
+  if (is_softmax) {
+    // ---- softmax: thread = (query row, column half) ------------------------
+    const uint32_t quad = warp & 3, ch = warp >> 3;         // column half: 0 = cols 0-31
+    const uint32_t row_lane = quad * 32u << 16;
+    const uint32_t row = quad * 32 + lane;
+    const uint32_t my_recv = recv_base + row * kRecvPitch + 128 * ch;
     const uint32_t peer_recv = map_to_rank(my_recv, peer);
     const uint32_t peer_x_full = map_to_rank(x_full, peer);
     const uint32_t peer_x_empty = map_to_rank(x_empty, peer);
+    const uint32_t pair_bar = 1 + quad;                      // named barrier of warps quad, quad + 8
     // x_full is armed for a tile's 32 KB before the peer can send it: tile 0
     // here, tile t + 1 once tile t has landed and before the peer is told it
     // may send again.
-    if (row == 0 && n_tiles > 0) mbar_arrive_expect_tx(x_full, kRecvTxBytes);
+    if (threadIdx.x == 0 && n_tiles > 0) mbar_arrive_expect_tx(x_full, kRecvTxBytes);
+    // validity of this thread's 32 slots of the next tile (one per lane)
+    int32_t next_slot = lane + 32 * ch < a.topk ? __ldg(idx + lane + 32 * ch) : -1;
     for (int t = 0; t < n_tiles; ++t) {
-      // validity of the tile's 64 slots, two per lane
-      const int j = t * kTile + lane;
-      const int32_t s0 = j < a.topk ? __ldg(idx + j) : -1;
-      const int32_t s1 = j + 32 < a.topk ? __ldg(idx + j + 32) : -1;
-      const uint32_t vm0 = __ballot_sync(0xffffffffu, s0 >= 0 && s0 < a.num_slots);
-      const uint32_t vm1 = __ballot_sync(0xffffffffu, s1 >= 0 && s1 < a.num_slots);
+      const uint32_t vm = __ballot_sync(0xffffffffu, next_slot >= 0 && next_slot < a.num_slots);
+      {
+        const int j = (t + 1) * kTile + 32 * ch + lane;
+        next_slot = j < a.topk ? __ldg(idx + j) : -1;
+      }
       if (!wait_or_abort(s_full[t & 1], (t >> 1) & 1, s_abort)) break;
       fence_after_sync();
-      float s[64];
-      tmem_ld32(tmem + row_lane + kSCol + kTile * (t & 1), s);
-      tmem_ld32(tmem + row_lane + kSCol + kTile * (t & 1) + 32, s + 32);
+      float s[32];
+      tmem_ld32(tmem + row_lane + kSCol + kTile * (t & 1) + 32 * ch, s);
       // partial S -> the peer (its previous one must have been read)
       if (t > 0 && !wait_or_abort(x_empty, (t - 1) & 1, s_abort)) break;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) st_async16(peer_recv + 16 * c, s + 4 * c, peer_x_full);
+      for (int c = 0; c < 8; ++c) st_async16(peer_recv + 16 * c, s + 4 * c, peer_x_full);
       if (!wait_or_abort(x_full, t & 1, s_abort)) break;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
+      for (int c = 0; c < 8; ++c) {
         const float4 v = ld_shared16(my_recv + 16 * c);
         s[4 * c] += v.x;
         s[4 * c + 1] += v.y;
         s[4 * c + 2] += v.z;
         s[4 * c + 3] += v.w;
       }
-      if (row == 0 && t + 1 < n_tiles) mbar_arrive_expect_tx(x_full, kRecvTxBytes);
+      if (threadIdx.x == 0 && t + 1 < n_tiles) mbar_arrive_expect_tx(x_full, kRecvTxBytes);
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(peer_x_empty);
-      float tmax = -INFINITY;
+      float hmax = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const bool ok = ((i < 32 ? vm0 : vm1) >> (i & 31)) & 1u;
-        s[i] = ok ? s[i] * a.scale_log2 : -INFINITY;
-        tmax = fmaxf(tmax, s[i]);
+      for (int i = 0; i < 32; ++i) {
+        s[i] = (vm >> i) & 1u ? s[i] * a.scale_log2 : -INFINITY;
+        hmax = fmaxf(hmax, s[i]);
       }
+      // row max over both column halves
+      s_pair[((t & 1) * 2 + ch) * kRows + row] = hmax;
+      asm volatile("bar.sync %0, 64;" :: "r"(pair_bar) : "memory");
+      const float tmax = fmaxf(hmax, s_pair[((t & 1) * 2 + (ch ^ 1)) * kRows + row]);
       // Lazy rescaling: the reference max moves only when the tile's max
       // exceeds it by more than 2^8 (weights stay below 256 otherwise).
       const bool grow = tmax > m + kRescaleLog2;
-      const float alpha = grow ? exp2f(m - tmax) : 1.0f;          // 0 while m is -inf
+      const float alpha = grow ? ex2(m - tmax) : 1.0f;          // 0 while m is -inf
       if (grow) m = tmax;
       const float m_use = m == -INFINITY ? 0.0f : m;
-      uint32_t pk[32];
+      uint32_t pk[16];
       float psum = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        pk[i] = pack_bf16x2(exp2f(s[2 * i] - m_use), exp2f(s[2 * i + 1] - m_use));
+      for (int i = 0; i < 16; ++i) {
+        pk[i] = pack_bf16x2(ex2(s[2 * i] - m_use), ex2(s[2 * i + 1] - m_use));
         psum += bf16_lo(pk[i]) + bf16_hi(pk[i]);
       }
       l = l * alpha + psum;
@@ -475,68 +581,83 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
       if (t > 0 && __any_sync(0xffffffffu, grow)) {
         fence_after_sync();
 #pragma unroll 1
-        for (int c = 0; c < kHalf / 32; ++c) {
+        for (int c = 0; c < kHalf / 64; ++c) {          // this half's 128 O columns
           float o[32];
-          tmem_ld32(tmem + row_lane + kOCol + 32 * c, o);
+          const uint32_t col = kOCol + 128 * ch + 32 * c;
+          tmem_ld32(tmem + row_lane + col, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(tmem + row_lane + kOCol + 32 * c, o);
+          tmem_st32(tmem + row_lane + col, o);
         }
       }
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_shared16(p_base + sw128_offset(row, c), make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                                                              pk[4 * c + 3]));
+      for (int c = 0; c < 4; ++c)
+        st_shared16(p_base + sw128_offset(row, 4 * ch + c),
+                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
       fence_async_smem();
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
     if (n_tiles > 0) wait_or_abort(o_done, (n_tiles - 1) & 1, s_abort);
-  } else if (warp < kSoftmaxWarps + kProducerWarps) {
+  } else if (warp < kProducerWarp0 + kProducerWarps) {
     // ---- producers: decode tiles into the double-buffered K tile ---------
-    const int row0 = (warp - kSoftmaxWarps) * kRowsPerProducer;
+    const int row0 = (warp - kProducerWarp0) * kRowsPerProducer;
     TileRegs cur, nxt;
-    if (n_tiles > 0) load_tile(a, idx, 0, row0, lane, half, cur, bad_index);
+    if (n_tiles > 0) load_tile(a, tile_slot(a, idx, 0, row0, lane), lane, half, cur, bad_index);
+    int32_t slot_next = tile_slot(a, idx, 1, row0, lane);        // slots one tile ahead of the loads
+    uint32_t stage = 0, phase = 0;                               // ring position of tile t
     for (int t = 0; t < n_tiles; ++t) {
-      if (t + 1 < n_tiles) load_tile(a, idx, t + 1, row0, lane, half, nxt, bad_index);
-      if (t >= 2 && !wait_or_abort(k_empty[t & 1], ((t - 2) >> 1) & 1, s_abort)) break;
-      store_tile(k_base[t & 1], row0, lane, cur);
+      if (t + 1 < n_tiles) {
+        load_tile(a, slot_next, lane, half, nxt, bad_index);
+        slot_next = tile_slot(a, idx, t + 2, row0, lane);
+      }
+      // stage reuse: P V of tile t - kKStages must be done
+      if (t >= kKStages && !wait_or_abort(k_empty0 + 8 * stage, phase ^ 1, s_abort)) break;
+      store_tile(base + kKOff + stage * kKBytes, row0, lane, half, cur);
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(k_full[t & 1]);
+      if (lane == 0) mbar_arrive(k_full0 + 8 * stage);
       cur = nxt;
+      if (++stage == kKStages) { stage = 0; phase ^= 1; }
     }
-  } else if (lane == 0) {
+  } else if (warp == kMmaThread / 32 && lane == 0) {
     // ---- MMA issue (one thread) -------------------------------------------
     constexpr uint32_t kIdescQK = idesc_bf16(kRows, kTile, false);
     constexpr uint32_t kIdescPV = idesc_bf16(kRows, kHalf, true);
+    uint32_t qk_stage = 0, qk_phase = 0, pv_stage = 0;           // ring positions of u and t
     for (int t = 0; t < n_tiles; ++t) {
       for (int u = (t == 0 ? 0 : t + 1); u <= t + 1 && u < n_tiles; ++u) {
-        // partial S[u & 1] = Q_c K_c(u)^T: 16 NoPE K-steps + 2 RoPE K-steps
-        if (!wait_or_abort(k_full[u & 1], (u >> 1) & 1, s_abort)) goto mma_done;
+        // partial S[u & 1] = Q_c K_c(u)^T: 16 NoPE K-steps (A in TMEM) + 2 RoPE K-steps
+        if (!wait_or_abort(k_full0 + 8 * qk_stage, qk_phase, s_abort)) goto mma_done;
         fence_after_sync();
         const uint32_t d = tmem + kSCol + kTile * (u & 1);
+        const uint32_t kb = base + kKOff + qk_stage * kKBytes;
 #pragma unroll
-        for (int k = 0; k < 18; ++k) {
-          const uint32_t blk = k < 16 ? k >> 2 : 4;
-          const uint32_t kk = (k < 16 ? (k & 3) : 2 * half + (k - 16)) * 32;
-          mma_bf16(d, sw128_desc(q_base + blk * kQBlock + kk, 16, 1024),
-                   sw128_desc(k_base[u & 1] + blk * kKBlock + kk, 16, 1024), kIdescQK, k > 0);
+        for (int k = 0; k < 16; ++k)
+          mma_bf16_ta(d, tmem + kQCol + 8 * k, sw128_desc(kb + (k >> 2) * kKBlock + (k & 3) * 32, 16, 1024),
+                      kIdescQK, k > 0);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const uint32_t kk = (2 * half + k) * 32;
+          mma_bf16(d, sw128_desc(qr_base + kk, 16, 1024), sw128_desc(kb + 4 * kKBlock + kk, 16, 1024),
+                   kIdescQK, 1u);
         }
         mma_commit(s_full[u & 1]);
         mma_issued = 1;
+        if (++qk_stage == kKStages) { qk_stage = 0; qk_phase ^= 1; }
       }
       // O += P(t) V(t): 4 MMAs of K = 16 slots, N = 256 value columns
       if (!wait_or_abort(p_full, t & 1, s_abort)) break;
       fence_after_sync();
+      const uint32_t kb = base + kKOff + pv_stage * kKBytes;
 #pragma unroll
       for (int k = 0; k < kTile / 16; ++k)
-        mma_bf16(tmem + kOCol, sw128_desc(p_base + 32 * k, 16, 1024),
-                 sw128_desc(k_base[t & 1] + 2048 * k, kKBlock, 1024), kIdescPV,
-                 (t > 0 || k > 0) ? 1u : 0u);
-      mma_commit(k_empty[t & 1]);
+        mma_bf16(tmem + kOCol, sw128_desc(p_base + 32 * k, 16, 1024), sw128_desc(kb + 2048 * k, kKBlock, 1024),
+                 kIdescPV, (t > 0 || k > 0) ? 1u : 0u);
+      mma_commit(k_empty0 + 8 * pv_stage);
       mma_commit(o_done);
+      if (++pv_stage == kKStages) pv_stage = 0;
     }
   mma_done:;
   }
@@ -555,19 +676,23 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
   }
   fence_after_sync();
   if (bad_index && a.status) atomicOr(a.status, KVQ_STATUS_BAD_INDEX);
+  // the row sums of the two column halves
+  if (is_softmax) s_pair[(warp >> 3) * kRows + (warp & 3) * 32 + lane] = l;
   aborted = __syncthreads_or(aborted) != 0;
   if (aborted && threadIdx.x == 0 && a.status) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
 
-  if (warp < kSoftmaxWarps && !aborted) {
-    const uint32_t row_lane = static_cast<uint32_t>(warp) * 32u << 16;
-    const int row = threadIdx.x;
-    const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+  if (is_softmax && !aborted) {
+    const uint32_t quad = warp & 3, ch = warp >> 3;
+    const uint32_t row_lane = quad * 32u << 16;
+    const int row = quad * 32 + lane;
+    const float l_row = s_pair[row] + s_pair[kRows + row];
+    const float inv_l = l_row > 0.0f ? 1.0f / l_row : 0.0f;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + token * a.out_stride_t +
-                         static_cast<int64_t>(row) * a.out_stride_h + kHalf * half;
+                         static_cast<int64_t>(row) * a.out_stride_h + kHalf * half + 128 * ch;
 #pragma unroll 1
-    for (int c = 0; c < kHalf / 32; ++c) {
+    for (int c = 0; c < 4; ++c) {
       float o[32];
-      if (n_tiles > 0) tmem_ld32(tmem + row_lane + kOCol + 32 * c, o);
+      if (n_tiles > 0) tmem_ld32(tmem + row_lane + kOCol + 128 * ch + 32 * c, o);
       if (row < a.num_heads) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -581,9 +706,9 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
         }
       }
     }
-    if (half == 0 && a.lse != nullptr && row < a.num_heads)
+    if (half == 0 && ch == 0 && a.lse != nullptr && row < a.num_heads)
       a.lse[token * a.lse_stride_t + row] =
-          l > 0.0f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+          l_row > 0.0f ? (m + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
   }
 
   fence_before_sync();

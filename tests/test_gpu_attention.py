@@ -182,3 +182,12 @@ def test_attention_full_size_sampled(kvq, oracle_mod, threads):
     g = np.random.Generator(np.random.PCG64(77))
     tokens = np.unique(np.concatenate([[0, w.num_tokens - 1], g.choice(w.num_tokens, 46, replace=False)]))
     check(oracle_mod, cache_host, w.q, wl.host(w.indices), w.softmax_scale, out, lse, threads, tokens)
+
+
+def test_attention_random_cache_bytes(kvq, oracle_mod):
+    """Every e2m1 code, negative and subnormal scale bytes and large RoPE
+    values: a cache of random bytes (the two e4m3 NaN codes replaced)."""
+    cache = wl.random_bytes((16, 64, 352), 321)
+    wl.nan_free_e4m3_bytes(cache[:, :, 256:])          # RoPE and scale bytes
+    w = wl.make_attention("random bytes", 4, 128, 192, 16, 64, 322, p_unused=0.1, softmax_scale=0.01)
+    assert run(kvq, oracle_mod, w, cache=cache) == 0
