@@ -70,7 +70,8 @@ constexpr uint32_t kRecvPitch = 64 * 4 + 16;                 // one row of the p
 constexpr uint32_t kKOff = kQBlock;
 constexpr uint32_t kPOff = kKOff + kKStages * kKBytes;
 constexpr uint32_t kRecvOff = kPOff + kRows * 128;           // P: 128 x 64 bf16, 128-byte swizzle
-constexpr uint32_t kPairOff = kRecvOff + kRows * kRecvPitch; // per-row maxima of the two column halves
+constexpr uint32_t kRecvBytes = kRows * kRecvPitch;          // one receive buffer; 2 buffers
+constexpr uint32_t kPairOff = kRecvOff + 2 * kRecvBytes;     // per-row maxima of the two column halves
 constexpr uint32_t kMiscOff = kPairOff + 2 * 2 * kRows * 4;  // [tile parity][half][row]
 constexpr uint32_t kSmemBytes = kMiscOff + 128 + 1024;       // + barriers, flags, alignment
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
@@ -165,12 +166,14 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
                :: "r"(cluster_bar) : "memory");
 }
 
+// One bounded wait step: the thread sleeps in the barrier (up to about 1 ms,
+// woken when the phase completes) instead of spinning on issue slots.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+      : "=r"(done) : "r"(bar), "r"(parity), "r"(1000000u) : "memory");
   return done != 0;
 }
 
@@ -429,14 +432,14 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
   const uint32_t qr_base = base, p_base = base + kPOff, recv_base = base + kRecvOff;
   float* s_pair = reinterpret_cast<float*>(smem + kPairOff);        // [2][2][kRows]
   const uint32_t bar0 = base + kMiscOff;
-  // k_full[3], k_empty[3], s_full[2], p_full, o_done, drain, x_full, x_empty
+  // k_full[3], k_empty[3], s_full[2], p_full, o_done, drain, x_full[2], x_empty[2]
   const uint32_t k_full0 = bar0, k_empty0 = bar0 + 24;
   const uint32_t s_full[2] = {bar0 + 48, bar0 + 56};
   const uint32_t p_full = bar0 + 64, o_done = bar0 + 72, drain = bar0 + 80;
-  const uint32_t x_full = bar0 + 88;     // the peer's partial S has landed here
-  const uint32_t x_empty = bar0 + 96;    // the peer has read the partial S sent to it
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kMiscOff + 112);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kMiscOff + 116);
+  const uint32_t x_full0 = bar0 + 88;    // [b]: the peer's partial S has landed in receive buffer b
+  const uint32_t x_empty0 = bar0 + 104;  // [b]: the peer has read what was sent to its buffer b
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kMiscOff + 120);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kMiscOff + 124);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t token = blockIdx.x >> 1;
@@ -458,10 +461,16 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
     mbar_init(p_full, kSoftmaxWarps);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
-    mbar_init(x_full, 1);
-    mbar_init(x_empty, kSoftmaxWarps);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(x_full0 + 8 * b, 1);
+      mbar_init(x_empty0 + 8 * b, kSoftmaxWarps);
+    }
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // Receive buffers 0 and 1 expect tiles 0 and 1 (32 KB each) before the
+    // cluster barrier below, i.e. before the peer can send anything.
+    const int n = (a.topk + kTile - 1) / kTile;
+    for (int b = 0; b < 2 && b < n; ++b) mbar_arrive_expect_tx(x_full0 + 8 * b, kRecvTxBytes);
   }
 
   // The CTA's 32 RoPE query dimensions -> chunks 4 half .. 4 half + 3 of a
@@ -515,43 +524,47 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
     const uint32_t quad = warp & 3, ch = warp >> 3;         // column half: 0 = cols 0-31
     const uint32_t row_lane = quad * 32u << 16;
     const uint32_t row = quad * 32 + lane;
-    const uint32_t my_recv = recv_base + row * kRecvPitch + 128 * ch;
+    const uint32_t my_recv = recv_base + row * kRecvPitch + 128 * ch;   // + b * kRecvBytes
     const uint32_t peer_recv = map_to_rank(my_recv, peer);
-    const uint32_t peer_x_full = map_to_rank(x_full, peer);
-    const uint32_t peer_x_empty = map_to_rank(x_empty, peer);
+    const uint32_t peer_x_full0 = map_to_rank(x_full0, peer);
+    const uint32_t peer_x_empty0 = map_to_rank(x_empty0, peer);
     const uint32_t pair_bar = 1 + quad;                      // named barrier of warps quad, quad + 8
-    // x_full is armed for a tile's 32 KB before the peer can send it: tile 0
-    // here, tile t + 1 once tile t has landed and before the peer is told it
-    // may send again.
-    if (threadIdx.x == 0 && n_tiles > 0) mbar_arrive_expect_tx(x_full, kRecvTxBytes);
+    // Software pipeline over the exchange: tile t + 1's partial scores are
+    // read from TMEM once tile t's weights are formed (the MMAs for t + 1 run
+    // meanwhile) and sent to the peer's other receive buffer after tile t's P
+    // is handed over.  Receive buffer b holds tiles t with t % 2 == b; it is
+    // re-armed for tile t + 2 once tile t is read and before the peer is told
+    // (x_empty) that it may send there again.
+    float cur[32], nxt[32];
+    if (n_tiles > 0) {
+      if (wait_or_abort(s_full[0], 0, s_abort)) {
+        fence_after_sync();
+        tmem_ld32(tmem + row_lane + kSCol + 32 * ch, cur);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) st_async16(peer_recv + 16 * c, cur + 4 * c, peer_x_full0);
+      }
+    }
     // validity of this thread's 32 slots of the next tile (one per lane)
     int32_t next_slot = lane + 32 * ch < a.topk ? __ldg(idx + lane + 32 * ch) : -1;
-    for (int t = 0; t < n_tiles; ++t) {
+    for (int t = 0; t < n_tiles && !*s_abort; ++t) {
       const uint32_t vm = __ballot_sync(0xffffffffu, next_slot >= 0 && next_slot < a.num_slots);
-      {
-        const int j = (t + 1) * kTile + 32 * ch + lane;
-        next_slot = j < a.topk ? __ldg(idx + j) : -1;
-      }
-      if (!wait_or_abort(s_full[t & 1], (t >> 1) & 1, s_abort)) break;
-      fence_after_sync();
-      float s[32];
-      tmem_ld32(tmem + row_lane + kSCol + kTile * (t & 1) + 32 * ch, s);
-      // partial S -> the peer (its previous one must have been read)
-      if (t > 0 && !wait_or_abort(x_empty, (t - 1) & 1, s_abort)) break;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) st_async16(peer_recv + 16 * c, s + 4 * c, peer_x_full);
-      if (!wait_or_abort(x_full, t & 1, s_abort)) break;
+      const bool more = t + 1 < n_tiles;
+      const uint32_t nb = (t + 1) & 1;
+      // tile t: the peer's partial scores
+      const uint32_t cb = t & 1;
+      if (!wait_or_abort(x_full0 + 8 * cb, (t >> 1) & 1, s_abort)) break;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const float4 v = ld_shared16(my_recv + 16 * c);
-        s[4 * c] += v.x;
-        s[4 * c + 1] += v.y;
-        s[4 * c + 2] += v.z;
-        s[4 * c + 3] += v.w;
+        const float4 v = ld_shared16(my_recv + cb * kRecvBytes + 16 * c);
+        cur[4 * c] += v.x;
+        cur[4 * c + 1] += v.y;
+        cur[4 * c + 2] += v.z;
+        cur[4 * c + 3] += v.w;
       }
-      if (threadIdx.x == 0 && t + 1 < n_tiles) mbar_arrive_expect_tx(x_full, kRecvTxBytes);
+      if (threadIdx.x == 0 && t + 2 < n_tiles) mbar_arrive_expect_tx(x_full0 + 8 * cb, kRecvTxBytes);
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote(peer_x_empty);
+      if (lane == 0) mbar_arrive_remote(peer_x_empty0 + 8 * cb);
+      float* s = cur;
       float hmax = -INFINITY;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
@@ -576,6 +589,12 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
         psum += bf16_lo(pk[i]) + bf16_hi(pk[i]);
       }
       l = l * alpha + psum;
+      // Tile t + 1's partial scores (their MMAs ran during this tile's work).
+      if (more) {
+        if (!wait_or_abort(s_full[nb], ((t + 1) >> 1) & 1, s_abort)) break;
+        fence_after_sync();
+        tmem_ld32(tmem + row_lane + kSCol + kTile * nb + 32 * ch, nxt);
+      }
       // P V of the previous tile must be done: it reads P, and O is rescaled.
       if (t > 0 && !wait_or_abort(o_done, (t - 1) & 1, s_abort)) break;
       if (t > 0 && __any_sync(0xffffffffu, grow)) {
@@ -598,6 +617,21 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
+      // After the arrive (a release waits for accesses in flight): tile
+      // t + 1's partial scores to the peer once its buffer there is free,
+      // and the next slots' indices.
+      if (more) {
+        if (t + 1 >= 2 && !wait_or_abort(x_empty0 + 8 * nb, ((t - 1) >> 1) & 1, s_abort)) break;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) st_async16(peer_recv + nb * kRecvBytes + 16 * c, nxt + 4 * c,
+                                               peer_x_full0 + 8 * nb);
+      }
+      {
+        const int j = (t + 1) * kTile + 32 * ch + lane;
+        next_slot = j < a.topk ? __ldg(idx + j) : -1;
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) cur[i] = nxt[i];
     }
     if (n_tiles > 0) wait_or_abort(o_done, (n_tiles - 1) & 1, s_abort);
   } else if (warp < kProducerWarp0 + kProducerWarps) {
@@ -607,17 +641,19 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
     if (n_tiles > 0) load_tile(a, tile_slot(a, idx, 0, row0, lane), lane, half, cur, bad_index);
     int32_t slot_next = tile_slot(a, idx, 1, row0, lane);        // slots one tile ahead of the loads
     uint32_t stage = 0, phase = 0;                               // ring position of tile t
+    // The next tile's loads are issued after each arrive: a release waits for
+    // every memory access of the thread still in flight, loads included.
     for (int t = 0; t < n_tiles; ++t) {
-      if (t + 1 < n_tiles) {
-        load_tile(a, slot_next, lane, half, nxt, bad_index);
-        slot_next = tile_slot(a, idx, t + 2, row0, lane);
-      }
       // stage reuse: P V of tile t - kKStages must be done
       if (t >= kKStages && !wait_or_abort(k_empty0 + 8 * stage, phase ^ 1, s_abort)) break;
       store_tile(base + kKOff + stage * kKBytes, row0, lane, half, cur);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(k_full0 + 8 * stage);
+      if (t + 1 < n_tiles) {
+        load_tile(a, slot_next, lane, half, nxt, bad_index);
+        slot_next = tile_slot(a, idx, t + 2, row0, lane);
+      }
       cur = nxt;
       if (++stage == kKStages) { stage = 0; phase ^= 1; }
     }
