@@ -50,14 +50,13 @@ constexpr int kRows = 128;                                   // query rows (head
 constexpr int kTile = 64;                                    // slots per tile (N of Q K^T)
 constexpr int kBlocks = 5;                                   // 4 NoPE blocks + the RoPE block
 // Warp roles: 0-3 softmax (columns 0-31), 4-7 producers, 8-11 softmax
-// (columns 32-63), 12 MMA.  Softmax warp w reads TMEM lanes 32 (w % 4) ..
-// +31, so warps w and w + 8 share the query rows 32 (w % 4) .. +31.
+// (columns 32-63), 12-15 producers, 16 MMA.  Softmax warp w reads TMEM lanes
+// 32 (w % 4) .. +31, so warps w and w + 8 share the query rows 32 (w % 4) .. +31.
 constexpr int kSoftmaxWarps = 8;
-constexpr int kProducerWarps = 4;
-constexpr int kProducerWarp0 = 4;
-constexpr int kRowsPerProducer = kTile / kProducerWarps;     // 16
-constexpr int kThreads = (kSoftmaxWarps + kProducerWarps + 1) * 32;   // + the MMA warp: 416
-constexpr int kMmaThread = 12 * 32;
+constexpr int kProducerWarps = 8;
+constexpr int kRowsPerProducer = kTile / kProducerWarps;     // 8
+constexpr int kThreads = (kSoftmaxWarps + kProducerWarps + 1) * 32;   // + the MMA warp: 544
+constexpr int kMmaThread = 16 * 32;
 constexpr int kNvRopeOff = 256, kNvSfOff = 320;
 constexpr float kRescaleLog2 = 8.0f;                         // lazy rescale threshold (base 2)
 
@@ -347,15 +346,15 @@ __device__ __forceinline__ uint4 e2m1x8_lut(uint32_t x, const GroupTable& t) {
 // producers: the CTA's share of a 64-slot tile
 // ---------------------------------------------------------------------------
 
-// Producer warp w (rows 16w .. 16w+15 of the tile): lane `lane` handles NoPE
-// group g = lane % 16 of rows 16w + lane / 16 + 2i (i < 8) and RoPE piece
-// k = lane % 4 (the CTA's 32 RoPE values are pieces 4 half + k) of rows
-// 16w + lane / 4 + 8i (i < 2).
+// Producer p (rows 8p .. 8p+7 of the tile): lane `lane` handles NoPE group
+// g = lane % 16 of rows 8p + lane / 16 + 2i (i < 4) and RoPE piece
+// k = lane % 4 (the CTA's 32 RoPE values are pieces 4 half + k) of row
+// 8p + lane / 4.
 struct TileRegs {
-  uint2 nib[8];
-  uint32_t sf[8];
-  uint2 rope[2];
-  uint32_t valid;                        // bits 0-7: NoPE rows, bits 8-9: RoPE rows
+  uint2 nib[4];
+  uint32_t sf[4];
+  uint2 rope;
+  uint32_t valid;                        // bits 0-3: NoPE rows, bit 4: RoPE row
 };
 
 __device__ __forceinline__ const uint8_t* entry_of(const AttentionArgs& a, int32_t slot) {
@@ -364,10 +363,10 @@ __device__ __forceinline__ const uint8_t* entry_of(const AttentionArgs& a, int32
   return a.cache + static_cast<int64_t>(blk) * a.block_stride + static_cast<int64_t>(off) * a.entry_stride;
 }
 
-// Slot of row row0 + lane % 16 of a tile (-1 past top-k).
+// Slot of row row0 + lane % 8 of a tile (-1 past top-k).
 __device__ __forceinline__ int32_t tile_slot(const AttentionArgs& a, const int32_t* idx, int tile, int row0,
                                              int lane) {
-  const int j = tile * kTile + row0 + (lane & 15);
+  const int j = tile * kTile + row0 + (lane & 7);
   return j < a.topk ? __ldg(idx + j) : -1;
 }
 
@@ -379,7 +378,7 @@ __device__ __forceinline__ void load_tile(const AttentionArgs& a, int32_t mine, 
   e.valid = 0;
   const int g = lane & 15, k = lane & 3;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < 4; ++i) {
     const int32_t slot = __shfl_sync(0xffffffffu, mine, (lane >> 4) + 2 * i);
     if (slot >= 0 && slot < a.num_slots) {
       const uint8_t* p = entry_of(a, slot);
@@ -388,12 +387,11 @@ __device__ __forceinline__ void load_tile(const AttentionArgs& a, int32_t mine, 
       e.sf[i] = __ldg(p + kNvSfOff + 16 * half + g);
     }
   }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int32_t slot = __shfl_sync(0xffffffffu, mine, (lane >> 2) + 8 * i);
+  {
+    const int32_t slot = __shfl_sync(0xffffffffu, mine, lane >> 2);
     if (slot >= 0 && slot < a.num_slots) {
-      e.valid |= 256u << i;
-      e.rope[i] = __ldg(reinterpret_cast<const uint2*>(entry_of(a, slot) + kNvRopeOff + 32 * half + 8 * k));
+      e.valid |= 16u;
+      e.rope = __ldg(reinterpret_cast<const uint2*>(entry_of(a, slot) + kNvRopeOff + 32 * half + 8 * k));
     }
   }
 }
@@ -401,7 +399,7 @@ __device__ __forceinline__ void load_tile(const AttentionArgs& a, int32_t mine, 
 __device__ __forceinline__ void store_tile(uint32_t kbuf, int row0, int lane, uint32_t half, const TileRegs& e) {
   const int g = lane & 15, k = lane & 3;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < 4; ++i) {
     const uint32_t r = row0 + (lane >> 4) + 2 * i;
     uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
     if (e.valid & (1u << i)) {
@@ -414,11 +412,10 @@ __device__ __forceinline__ void store_tile(uint32_t kbuf, int row0, int lane, ui
     st_shared16(blk + sw128_offset(r, 2 * (g & 3)), lo);
     st_shared16(blk + sw128_offset(r, 2 * (g & 3) + 1), hi);
   }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const uint32_t r = row0 + (lane >> 2) + 8 * i;
+  {
+    const uint32_t r = row0 + (lane >> 2);
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (e.valid & (256u << i)) v = e4m3x8_bf16(e.rope[i]);
+    if (e.valid & 16u) v = e4m3x8_bf16(e.rope);
     st_shared16(kbuf + 4 * kKBlock + sw128_offset(r, 4 * half + k), v);
   }
 }
@@ -634,9 +631,9 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
       for (int i = 0; i < 32; ++i) cur[i] = nxt[i];
     }
     if (n_tiles > 0) wait_or_abort(o_done, (n_tiles - 1) & 1, s_abort);
-  } else if (warp < kProducerWarp0 + kProducerWarps) {
-    // ---- producers: decode tiles into the double-buffered K tile ---------
-    const int row0 = (warp - kProducerWarp0) * kRowsPerProducer;
+  } else if (warp < 16) {
+    // ---- producers: decode tiles into the K ring ----------------------------
+    const int row0 = (warp < 8 ? warp - 4 : warp - 8) * kRowsPerProducer;
     TileRegs cur, nxt;
     if (n_tiles > 0) load_tile(a, tile_slot(a, idx, 0, row0, lane), lane, half, cur, bad_index);
     int32_t slot_next = tile_slot(a, idx, 1, row0, lane);        // slots one tile ahead of the loads
