@@ -707,6 +707,26 @@ def run_ours(args):
     return 0
 
 
+def run_attention_only(tokens: int) -> int:
+    """Profiler hook: the attention alone on a small cache (a few hundred MB)."""
+    import fp8_quantized_paged_concat_gb300 as kvq
+    kvq.load_library()
+    dev = torch.device("cuda:0")
+    fill = wl.make_fill("attention profiling fill 8192x64", 8192, 64, 1006, dev, rng="device")
+    cache = torch.zeros((8192, 64, 352), dtype=torch.uint8, device=dev)
+    kvq.kvq_write_nvfp4_ds_mla(fill.kv_c, fill.k_pe, cache, fill.slot_mapping)
+    w = wl.make_attention("attention profiling case", tokens, 128, 2048, 8192, 64, 1006, dev, p_unused=0.1,
+                          fill=fill, rng="device")
+    for r in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        kvq.kvq_sparse_mla_attention_nvfp4_ds_mla(w.q, w.indices, cache, w.softmax_scale)
+        b.record()
+        torch.cuda.synchronize()
+        print(f"sparse_mla_attention T={tokens}: {a.elapsed_time(b) * 1e3:.1f} us", flush=True)
+    return 0
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -718,7 +738,12 @@ def main(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--size", choices=["full", "small"], default="full",
                    help="small: the same kernels on ~0.4 GB inputs, for profiler captures")
+    p.add_argument("--attention-only", type=int, default=0, metavar="T",
+                   help="profiler hook: T decode tokens of the sparse MLA attention (128 heads, top-2048 "
+                        "over an 8192 x 64 cache), 3 launches, times printed; nothing else runs")
     args = p.parse_args(argv)
+    if args.attention_only > 0:
+        return run_attention_only(args.attention_only)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
