@@ -665,17 +665,17 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
         if (!wait_or_abort(k_full0 + 8 * qk_stage, qk_phase, s_abort)) goto mma_done;
         fence_after_sync();
         const uint32_t d = tmem + kSCol + kTile * (u & 1);
-        const uint32_t kb = base + kKOff + qk_stage * kKBytes;
+        // descriptors built once; a K-step adds its byte offset / 16 to the
+        // start-address field (addresses stay below 256 KB: no carry out)
+        const uint64_t kdesc = sw128_desc(base + kKOff + qk_stage * kKBytes, 16, 1024);
 #pragma unroll
         for (int k = 0; k < 16; ++k)
-          mma_bf16_ta(d, tmem + kQCol + 8 * k, sw128_desc(kb + (k >> 2) * kKBlock + (k & 3) * 32, 16, 1024),
-                      kIdescQK, k > 0);
+          mma_bf16_ta(d, tmem + kQCol + 8 * k, kdesc + (((k >> 2) * kKBlock + (k & 3) * 32) >> 4), kIdescQK,
+                      k > 0);
+        const uint64_t qrdesc = sw128_desc(qr_base + 64 * half, 16, 1024);
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const uint32_t kk = (2 * half + k) * 32;
-          mma_bf16(d, sw128_desc(qr_base + kk, 16, 1024), sw128_desc(kb + 4 * kKBlock + kk, 16, 1024),
-                   kIdescQK, 1u);
-        }
+        for (int k = 0; k < 2; ++k)
+          mma_bf16(d, qrdesc + 2 * k, kdesc + ((4 * kKBlock + 64 * half + 32 * k) >> 4), kIdescQK, 1u);
         mma_commit(s_full[u & 1]);
         mma_issued = 1;
         if (++qk_stage == kKStages) { qk_stage = 0; qk_phase ^= 1; }
@@ -683,11 +683,11 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
       // O += P(t) V(t): 4 MMAs of K = 16 slots, N = 256 value columns
       if (!wait_or_abort(p_full, t & 1, s_abort)) break;
       fence_after_sync();
-      const uint32_t kb = base + kKOff + pv_stage * kKBytes;
+      const uint64_t pdesc = sw128_desc(p_base, 16, 1024);
+      const uint64_t vdesc = sw128_desc(base + kKOff + pv_stage * kKBytes, kKBlock, 1024);
 #pragma unroll
       for (int k = 0; k < kTile / 16; ++k)
-        mma_bf16(tmem + kOCol, sw128_desc(p_base + 32 * k, 16, 1024), sw128_desc(kb + 2048 * k, kKBlock, 1024),
-                 kIdescPV, (t > 0 || k > 0) ? 1u : 0u);
+        mma_bf16(tmem + kOCol, pdesc + 2 * k, vdesc + 128 * k, kIdescPV, (t > 0 || k > 0) ? 1u : 0u);
       mma_commit(k_empty0 + 8 * pv_stage);
       mma_commit(o_done);
       if (++pv_stage == kKStages) pv_stage = 0;
