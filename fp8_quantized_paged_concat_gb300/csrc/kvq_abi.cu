@@ -281,7 +281,8 @@ kvq_status kvq_req_index_to_global_slot(const int32_t* req_id, int64_t num_req_i
               "%s: req_id has %lld entries but token_indices has %lld rows", fn,
               static_cast<long long>(num_req_ids), static_cast<long long>(num_tokens));
   if (num_tokens == 0 || topk == 0) return ok();
-  KVQ_REQUIRE(num_tokens * topk < (int64_t{1} << 32) - 256, "%s: num_tokens * topk too large", fn);
+  KVQ_REQUIRE(num_tokens < (int64_t{1} << 31) && topk <= (1 << 24),
+              "%s: num_tokens must be below 2^31 and topk at most 2^24", fn);   // grid x / y
   KVQ_REQUIRE(req_id != nullptr && token_indices != nullptr && out != nullptr && block_table != nullptr,
               "%s: req_id, token_indices, block_table and out must be non-NULL", fn);
   KVQ_REQUIRE(aligned(req_id, 4) && aligned(token_indices, 4) && aligned(out, 4) && aligned(block_table, 4),
@@ -298,8 +299,7 @@ kvq_status kvq_req_index_to_global_slot(const int32_t* req_id, int64_t num_req_i
                          topk,          block_table,   block_table_stride,   block_table_width,
                          num_requests,  block_size,    num_blocks,           out,
                          out_stride,    d_status,
-                         kvq::FastDiv::make(static_cast<uint32_t>(block_size)),
-                         {}};   // topk_div: set by the launcher for its positions per thread
+                         kvq::FastDiv::make(static_cast<uint32_t>(block_size))};
   return launched(fn, kvq::launch_req_index_to_global_slot(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -3,24 +3,31 @@
 // cache slot block_table[r][p / block_size] * block_size + p % block_size,
 // -1 for unused (negative) positions and for anything out of range.
 //
-// One thread per 4 consecutive (token, k) pairs (16-byte loads and stores;
-// one per pair when rows are not 16-byte aligned): int32 reads and writes,
-// coalesced along k; the block-table read is a gather into a small,
-// L2-resident table.
+// One CTA per (token, chunk of 2048 positions): every position of a token
+// belongs to the same request, so the CTA stages that request's block-table
+// row in shared memory once and resolves its positions there (a 4-byte
+// gather per position from L2 would move a 32-byte sector each).  Threads
+// take 4 x 4 consecutive positions (16-byte loads and stores, all four loads
+// in flight together; 4 x 1 position when rows are not 16-byte aligned).
+// Rows wider than the staging limit read the table from global memory.
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
 
 namespace kvq {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;
+constexpr int kLoads = 4;                     // independent accesses per thread
+constexpr int kMaxStagedWidth = 12288;        // 48 KB of int32: no opt-in shared memory needed
 
-// Slot of position p of request r, or -1 (with a status bit when out of range).
-__device__ __forceinline__ int32_t global_slot(const IndexArgs& a, int32_t r, int32_t p) {
+// Slot of position p given the request's table row (or -1, with a status
+// bit when out of range; row == nullptr marks an out-of-range request).
+template <typename Row>
+__device__ __forceinline__ int32_t global_slot(const IndexArgs& a, Row row, int32_t p) {
   if (p < 0) return -1;
   const uint32_t col = a.block_div.div(static_cast<uint32_t>(p));
-  if (r >= 0 && r < a.num_requests && col < static_cast<uint32_t>(a.block_table_width)) {
-    const int32_t blk = __ldg(a.block_table + static_cast<int64_t>(r) * a.block_table_stride + col);
+  if (row != nullptr && col < static_cast<uint32_t>(a.block_table_width)) {
+    const int32_t blk = row[col];
     if (blk >= 0 && blk < a.num_blocks)
       return blk * a.block_size + static_cast<int32_t>(static_cast<uint32_t>(p) - col * a.block_div.d);
   }
@@ -28,23 +35,64 @@ __device__ __forceinline__ int32_t global_slot(const IndexArgs& a, int32_t r, in
   return -1;
 }
 
-// kVec consecutive positions per thread (16-byte loads and stores when 4).
-template <int kVec>
+template <int kVec, bool kStaged>
 __global__ void __launch_bounds__(kThreads) req_index_to_global_slot_kernel(const IndexArgs a) {
-  const uint32_t idx = blockIdx.x * kThreads + threadIdx.x;      // < 2^32 - 256 (host check)
-  const uint32_t i = a.topk_div.div(idx);                        // topk_div divides by topk / kVec
-  if (i >= a.num_tokens) return;
-  const uint32_t k = (idx - i * a.topk_div.d) * kVec;
+  extern __shared__ int32_t s_row[];
+  const int64_t i = blockIdx.x;                                   // token
   const int32_t r = __ldg(a.req_id + i);
-  const int32_t* src = a.token_indices + static_cast<int64_t>(i) * a.token_indices_stride + k;
-  int32_t* dst = a.out + static_cast<int64_t>(i) * a.out_stride + k;
-  if constexpr (kVec == 4) {
-    const int4 p = __ldcs(reinterpret_cast<const int4*>(src));
-    *reinterpret_cast<int4*>(dst) =
-        make_int4(global_slot(a, r, p.x), global_slot(a, r, p.y), global_slot(a, r, p.z), global_slot(a, r, p.w));
-  } else {
-    *dst = global_slot(a, r, __ldg(src));
+  const bool valid_req = r >= 0 && r < a.num_requests;
+  const int32_t* g_row = valid_req ? a.block_table + static_cast<int64_t>(r) * a.block_table_stride : nullptr;
+  if constexpr (kStaged) {
+    if (valid_req)
+      for (int c = threadIdx.x; c < a.block_table_width; c += kThreads) s_row[c] = __ldg(g_row + c);
+    __syncthreads();
   }
+  // kLoads accesses of kVec positions per thread, kThreads * kVec apart
+  // (coalesced), all loads issued before any use
+  const int64_t k0 = (static_cast<int64_t>(blockIdx.y) * kThreads * kLoads + threadIdx.x) * kVec;
+  const int32_t* src = a.token_indices + i * a.token_indices_stride;
+  int32_t* dst = a.out + i * a.out_stride;
+  const int32_t* row = valid_req ? (kStaged ? s_row : g_row) : nullptr;
+  if constexpr (kVec == 4) {
+    int4 p[kLoads];
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      const int64_t k = k0 + u * kThreads * kVec;
+      if (k < a.topk) p[u] = __ldcs(reinterpret_cast<const int4*>(src + k));
+    }
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      const int64_t k = k0 + u * kThreads * kVec;
+      if (k < a.topk)
+        __stcs(reinterpret_cast<int4*>(dst + k),
+               make_int4(global_slot(a, row, p[u].x), global_slot(a, row, p[u].y), global_slot(a, row, p[u].z),
+                         global_slot(a, row, p[u].w)));
+    }
+  } else {
+    int32_t p[kLoads];
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      const int64_t k = k0 + u * kThreads;
+      if (k < a.topk) p[u] = __ldcs(src + k);
+    }
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      const int64_t k = k0 + u * kThreads;
+      if (k < a.topk) __stcs(dst + k, global_slot(a, row, p[u]));
+    }
+  }
+}
+
+template <int kVec>
+cudaError_t launch(const IndexArgs& a, cudaStream_t stream) {
+  const int64_t per_cta = static_cast<int64_t>(kThreads) * kLoads * kVec;
+  const dim3 grid(static_cast<unsigned>(a.num_tokens), static_cast<unsigned>((a.topk + per_cta - 1) / per_cta));
+  if (a.block_table_width <= kMaxStagedWidth)
+    req_index_to_global_slot_kernel<kVec, true>
+        <<<grid, kThreads, a.block_table_width * sizeof(int32_t), stream>>>(a);
+  else
+    req_index_to_global_slot_kernel<kVec, false><<<grid, kThreads, 0, stream>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -54,16 +102,7 @@ cudaError_t launch_req_index_to_global_slot(const IndexArgs& a, cudaStream_t str
   const bool vec = a.topk % 4 == 0 && a.token_indices_stride % 4 == 0 && a.out_stride % 4 == 0 &&
                    reinterpret_cast<uintptr_t>(a.token_indices) % 16 == 0 &&
                    reinterpret_cast<uintptr_t>(a.out) % 16 == 0;
-  IndexArgs b = a;
-  const int per_thread = vec ? 4 : 1;
-  b.topk_div = FastDiv::make(static_cast<uint32_t>(a.topk / per_thread));
-  const int64_t threads = a.num_tokens * (a.topk / per_thread);
-  const int64_t blocks = (threads + kThreads - 1) / kThreads;
-  if (vec)
-    req_index_to_global_slot_kernel<4><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(b);
-  else
-    req_index_to_global_slot_kernel<1><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(b);
-  return cudaGetLastError();
+  return vec ? launch<4>(a, stream) : launch<1>(a, stream);
 }
 
 }  // namespace kvq
