@@ -28,8 +28,8 @@
 //     (a + b == b + a in IEEE arithmetic: both CTAs hold bit-identical
 //     scores), run the online softmax in base 2 with lazy rescaling (the
 //     reference maximum moves only when a tile exceeds it by 2^8), round P
-//     to bf16 into shared memory (the A operand of P V) and rescale their O
-//     row in TMEM when the reference moved;
+//     to bf16 into TMEM (the A operand of P V) and rescale their O row in
+//     TMEM when the reference moved;
 //   - the denominator sums the bf16-rounded P, the weights the tensor cores
 //     multiply.
 //
@@ -67,20 +67,22 @@ constexpr uint32_t kKBlock = kTile * 128;                    // 8 KB per 64-dim 
 constexpr uint32_t kKBytes = kBlocks * kKBlock;              // 40 KB per K stage
 constexpr uint32_t kRecvPitch = 64 * 4 + 16;                 // one row of the peer's partial S
 constexpr uint32_t kKOff = kQBlock;
-constexpr uint32_t kPOff = kKOff + kKStages * kKBytes;
-constexpr uint32_t kRecvOff = kPOff + kRows * 128;           // P: 128 x 64 bf16, 128-byte swizzle
+constexpr uint32_t kRecvOff = kKOff + kKStages * kKBytes;
 constexpr uint32_t kRecvBytes = kRows * kRecvPitch;          // one receive buffer; 2 buffers
 constexpr uint32_t kPairOff = kRecvOff + 2 * kRecvBytes;     // per-row maxima of the two column halves
 constexpr uint32_t kMiscOff = kPairOff + 2 * 2 * kRows * 4;  // [tile parity][half][row]
 constexpr uint32_t kSmemBytes = kMiscOff + 128 + 1024;       // + barriers, flags, alignment
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
-static_assert(kPOff % 1024 == 0 && kKOff % 1024 == 0, "swizzle atoms must be 1024-byte aligned");
+static_assert(kKOff % 1024 == 0 && kKBytes % 1024 == 0, "swizzle atoms must be 1024-byte aligned");
 
 constexpr uint32_t kRecvTxBytes = kRows * 64 * 4;            // one partial S: 32 KB
 
 // TMEM columns: O [0, 256), the CTA's 256 NoPE query dimensions as bf16
 // pairs [256, 384) (the A operand of the NoPE K-steps), partial S double
-// buffer [384, 512).
+// buffer [384, 512).  A tile's P (bf16 pairs, 32 columns) is written over
+// the first half of its own S buffer, once its scores are in registers, and
+// is the A operand of P V: the MMAs of one thread run in order, so the Q K^T
+// two tiles later cannot overwrite it before P V has read it.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 0;
 constexpr uint32_t kQCol = 256;
@@ -231,6 +233,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+         "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
@@ -426,7 +438,7 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t base = smem_u32(smem);
-  const uint32_t qr_base = base, p_base = base + kPOff, recv_base = base + kRecvOff;
+  const uint32_t qr_base = base, recv_base = base + kRecvOff;
   float* s_pair = reinterpret_cast<float*>(smem + kPairOff);        // [2][2][kRows]
   const uint32_t bar0 = base + kMiscOff;
   // k_full[3], k_empty[3], s_full[2], p_full, o_done, drain, x_full[2], x_empty[2]
@@ -586,13 +598,19 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
         psum += bf16_lo(pk[i]) + bf16_hi(pk[i]);
       }
       l = l * alpha + psum;
-      // Tile t + 1's partial scores (their MMAs ran during this tile's work).
+      // Tile t + 1's partial scores (their MMAs ran during this tile's work),
+      // straight on to the peer once its buffer there is free.
       if (more) {
         if (!wait_or_abort(s_full[nb], ((t + 1) >> 1) & 1, s_abort)) break;
         fence_after_sync();
         tmem_ld32(tmem + row_lane + kSCol + kTile * nb + 32 * ch, nxt);
+        if (t + 1 >= 2 && !wait_or_abort(x_empty0 + 8 * nb, ((t - 1) >> 1) & 1, s_abort)) break;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) st_async16(peer_recv + nb * kRecvBytes + 16 * c, nxt + 4 * c,
+                                               peer_x_full0 + 8 * nb);
       }
-      // P V of the previous tile must be done: it reads P, and O is rescaled.
+      // P V of the previous tile must be done before O is rescaled (it
+      // normally is by now; the wait also keeps the barrier's phases in step).
       if (t > 0 && !wait_or_abort(o_done, (t - 1) & 1, s_abort)) break;
       if (t > 0 && __any_sync(0xffffffffu, grow)) {
         fence_after_sync();
@@ -606,23 +624,13 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
           tmem_st32(tmem + row_lane + col, o);
         }
       }
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        st_shared16(p_base + sw128_offset(row, 4 * ch + c),
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
-      fence_async_smem();
+      // P (32 values = 16 bf16 pairs of this column half) over tile t's S.
+      tmem_st16(tmem + row_lane + kSCol + kTile * cb + 16 * ch, pk);
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
-      // After the arrive (a release waits for accesses in flight): tile
-      // t + 1's partial scores to the peer once its buffer there is free,
-      // and the next slots' indices.
-      if (more) {
-        if (t + 1 >= 2 && !wait_or_abort(x_empty0 + 8 * nb, ((t - 1) >> 1) & 1, s_abort)) break;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) st_async16(peer_recv + nb * kRecvBytes + 16 * c, nxt + 4 * c,
-                                               peer_x_full0 + 8 * nb);
-      }
+      // the next slots' indices, after the arrive (a release waits for
+      // accesses in flight)
       {
         const int j = (t + 1) * kTile + 32 * ch + lane;
         next_slot = j < a.topk ? __ldg(idx + j) : -1;
@@ -683,11 +691,11 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
       // O += P(t) V(t): 4 MMAs of K = 16 slots, N = 256 value columns
       if (!wait_or_abort(p_full, t & 1, s_abort)) break;
       fence_after_sync();
-      const uint64_t pdesc = sw128_desc(p_base, 16, 1024);
       const uint64_t vdesc = sw128_desc(base + kKOff + pv_stage * kKBytes, kKBlock, 1024);
 #pragma unroll
       for (int k = 0; k < kTile / 16; ++k)
-        mma_bf16(tmem + kOCol, pdesc + 2 * k, vdesc + 128 * k, kIdescPV, (t > 0 || k > 0) ? 1u : 0u);
+        mma_bf16_ta(tmem + kOCol, tmem + kSCol + kTile * (t & 1) + 8 * k, vdesc + 128 * k, kIdescPV,
+                    (t > 0 || k > 0) ? 1u : 0u);
       mma_commit(k_empty0 + 8 * pv_stage);
       mma_commit(o_done);
       if (++pv_stage == kKStages) pv_stage = 0;
