@@ -60,6 +60,10 @@ _SIGNATURES = {
     "kvqo_sparse_mla_attention_nvfp4_ds_mla": (_I64, [_P, _I64, _I64, _I64, _I64, _I32, _P, _I64, _I32,
                                                       _P, _I64, _I32, _I64, _I64, ctypes.c_double,
                                                       _P, _I64, _I64, _P, _I64]),
+    "kvqo_sparse_mla_attention_fp8_ds_mla": (_I64, [_P, _I64, _I64, _I64, _I64, _I32, _P, _I64, _I32,
+                                                    _P, _I64, _I32, _I64, _I64, ctypes.c_double,
+                                                    _P, _I64, _I64, _P, _I64]),
+    "kvqo_decode_fp8_ds_mla_entry": (None, [_P, _P]),
     "kvqo_decode_nvfp4_ds_mla_entry": (None, [_P, _P]),
 }
 
@@ -358,16 +362,25 @@ def sparse_mla_attention_nvfp4_ds_mla(q, indices, cache, softmax_scale: float, t
     """Oracle sparse MLA attention (MQA form) of q uint16 bf16 bits [T, H, 576]
     over the global slots indices int32 [T, topk] of the nvfp4_ds_mla cache;
     returns (o float64 [T, H, 512], lse float64 [T, H], slots skipped)."""
+    return _attention("kvqo_sparse_mla_attention_nvfp4_ds_mla", 352, q, indices, cache, softmax_scale, threads)
+
+
+def sparse_mla_attention_fp8_ds_mla(q, indices, cache, softmax_scale: float, threads: int = 1):
+    """The same over the 656-byte fp8_ds_mla cache."""
+    return _attention("kvqo_sparse_mla_attention_fp8_ds_mla", 656, q, indices, cache, softmax_scale, threads)
+
+
+def _attention(fn_name, entry_bytes, q, indices, cache, softmax_scale, threads):
     if q.dtype != np.uint16 or q.ndim != 3 or q.shape[2] != 576 or q.strides[2] != 2:
         raise ValueError("q: expected uint16 [T, H, 576] with unit inner stride")
     indices = np.ascontiguousarray(indices, dtype=np.int32)
     T, H = q.shape[0], q.shape[1]
     if indices.ndim != 2 or indices.shape[0] != T:
         raise ValueError("indices: expected int32 [T, topk]")
-    nb, bs, bstride, estride = _cache_geometry(cache, 352)
+    nb, bs, bstride, estride = _cache_geometry(cache, entry_bytes)
     out = np.zeros((T, H, 512), np.float64)
     lse = np.zeros((T, H), np.float64)
-    fn = lib().kvqo_sparse_mla_attention_nvfp4_ds_mla
+    fn = getattr(lib(), fn_name)
 
     def run(b, e):
         r = fn(_ptr(q), q.strides[0] // 2, q.strides[1] // 2, b, e, H, _ptr(indices), indices.shape[1],
@@ -379,6 +392,16 @@ def sparse_mla_attention_nvfp4_ds_mla(q, indices, cache, softmax_scale: float, t
 
     skipped = _run_chunks(run, T, threads)
     return out, lse, skipped
+
+
+def decode_fp8_ds_mla_entry(entry) -> np.ndarray:
+    """The 576 bf16 values (as float64) one 656-byte fp8_ds_mla entry upconverts to."""
+    entry = np.ascontiguousarray(entry, dtype=np.uint8)
+    if entry.shape != (656,):
+        raise ValueError("entry must be 656 bytes")
+    out = np.empty(576, np.float64)
+    lib().kvqo_decode_fp8_ds_mla_entry(_ptr(entry), _ptr(out))
+    return out
 
 
 def decode_nvfp4_ds_mla_entry(entry) -> np.ndarray:

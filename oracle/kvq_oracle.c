@@ -616,7 +616,8 @@ int64_t kvqo_req_index_to_global_slot(
  * over the valid entries of indices[t] (negative entries are unused; a slot
  * beyond the cache is skipped and counted).  A token with no valid entry
  * gets o = 0 and lse = -inf.  Everything in double, entries decoded exactly. */
-int64_t kvqo_sparse_mla_attention_nvfp4_ds_mla(
+static int64_t sparse_mla_attention(
+    void (*decode)(const uint8_t*, double*),
     const uint16_t* q, int64_t q_stride_t, int64_t q_stride_h,
     int64_t t_begin, int64_t t_end, int32_t num_heads,
     const int32_t* indices, int64_t indices_stride, int32_t topk,
@@ -635,9 +636,8 @@ int64_t kvqo_sparse_mla_attention_nvfp4_ds_mla(
             int64_t slot = indices[t * indices_stride + k];
             if (slot < 0) continue;
             if (slot >= num_blocks * (int64_t)block_size) { ++skipped; continue; }
-            kvqo_decode_nvfp4_ds_mla_entry(
-                cache + (slot / block_size) * block_stride + (slot % block_size) * entry_stride,
-                keys + (int64_t)n * dim);
+            decode(cache + (slot / block_size) * block_stride + (slot % block_size) * entry_stride,
+                   keys + (int64_t)n * dim);
             ++n;
         }
         for (h = 0; h < num_heads; ++h) {
@@ -665,4 +665,48 @@ int64_t kvqo_sparse_mla_attention_nvfp4_ds_mla(
     free(keys);
     free(s);
     return skipped;
+}
+
+int64_t kvqo_sparse_mla_attention_nvfp4_ds_mla(
+    const uint16_t* q, int64_t q_stride_t, int64_t q_stride_h,
+    int64_t t_begin, int64_t t_end, int32_t num_heads,
+    const int32_t* indices, int64_t indices_stride, int32_t topk,
+    const uint8_t* cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride, double softmax_scale,
+    double* out, int64_t out_stride_t, int64_t out_stride_h,
+    double* lse, int64_t lse_stride_t) {
+    return sparse_mla_attention(kvqo_decode_nvfp4_ds_mla_entry, q, q_stride_t, q_stride_h, t_begin, t_end,
+                                num_heads, indices, indices_stride, topk, cache, num_blocks, block_size,
+                                block_stride, entry_stride, softmax_scale, out, out_stride_t, out_stride_h,
+                                lse, lse_stride_t);
+}
+
+/* The same consumer over the 656-byte fp8_ds_mla cache ([P1] "Key source
+ * snippets": the sparse decode path serves both quantized DS-MLA formats).
+ * A slot's key is the fp8 gather's upconvert of its entry: NoPE value k =
+ * bf16_rn(fp32(e4m3(n_k)) * s_{k/128}), RoPE bf16 as stored. */
+void kvqo_decode_fp8_ds_mla_entry(const uint8_t* entry, double* out576) {
+    int k;
+    for (k = 0; k < NV_NOPE_DIM; ++k) {
+        float s;
+        memcpy(&s, &entry[F8_SCALE_OFF + 4 * (k / F8_TILE)], 4);
+        out576[k] = kvqo_bf16_value(kvqo_bf16_rn((float)kvqo_e4m3_value(entry[k]) * s));
+    }
+    for (k = 0; k < NV_ROPE_DIM; ++k)
+        out576[NV_NOPE_DIM + k] = kvqo_bf16_value(
+            (uint16_t)(entry[F8_ROPE_OFF + 2 * k] | (entry[F8_ROPE_OFF + 2 * k + 1] << 8)));
+}
+
+int64_t kvqo_sparse_mla_attention_fp8_ds_mla(
+    const uint16_t* q, int64_t q_stride_t, int64_t q_stride_h,
+    int64_t t_begin, int64_t t_end, int32_t num_heads,
+    const int32_t* indices, int64_t indices_stride, int32_t topk,
+    const uint8_t* cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride, double softmax_scale,
+    double* out, int64_t out_stride_t, int64_t out_stride_h,
+    double* lse, int64_t lse_stride_t) {
+    return sparse_mla_attention(kvqo_decode_fp8_ds_mla_entry, q, q_stride_t, q_stride_h, t_begin, t_end,
+                                num_heads, indices, indices_stride, topk, cache, num_blocks, block_size,
+                                block_stride, entry_stride, softmax_scale, out, out_stride_t, out_stride_h,
+                                lse, lse_stride_t);
 }

@@ -142,6 +142,20 @@ int64_t kvqo_sparse_mla_attention_nvfp4_ds_mla(
     double* out, int64_t out_stride_t, int64_t out_stride_h,
     double* lse, int64_t lse_stride_t);
 
+/* The same over the 656-byte fp8_ds_mla cache (keys as the fp8 gather
+ * upconverts them). */
+int64_t kvqo_sparse_mla_attention_fp8_ds_mla(
+    const uint16_t* q, int64_t q_stride_t, int64_t q_stride_h,
+    int64_t t_begin, int64_t t_end, int32_t num_heads,
+    const int32_t* indices, int64_t indices_stride, int32_t topk,
+    const uint8_t* cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride, double softmax_scale,
+    double* out, int64_t out_stride_t, int64_t out_stride_h,
+    double* lse, int64_t lse_stride_t);
+
+/* Decodes one 656-byte fp8_ds_mla entry to its 576 bf16 values (as doubles). */
+void kvqo_decode_fp8_ds_mla_entry(const uint8_t* entry, double* out576);
+
 /* Decodes one 352-byte nvfp4_ds_mla entry to 576 values (NoPE then RoPE). */
 void kvqo_decode_nvfp4_ds_mla_entry(const uint8_t* entry, double* out576);
 

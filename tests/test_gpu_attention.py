@@ -191,3 +191,21 @@ def test_attention_random_cache_bytes(kvq, oracle_mod):
     wl.nan_free_e4m3_bytes(cache[:, :, 256:])          # RoPE and scale bytes
     w = wl.make_attention("random bytes", 4, 128, 192, 16, 64, 322, p_unused=0.1, softmax_scale=0.01)
     assert run(kvq, oracle_mod, w, cache=cache) == 0
+
+
+def test_attention_single_token_strided_indices_no_lse(kvq, oracle_mod):
+    """One token (one cluster), top-k slots taken from a wider index tensor,
+    and no lse output (the output alone is still checked)."""
+    w = wl.make_attention("one token", 1, 128, 160, 8, 64, 331, p_unused=0.15)
+    cache = host_cache(oracle_mod, w.fill)
+    wide = torch.full((1, 160 + 24), 5, dtype=torch.int32)
+    wide[:, :160] = w.indices
+    idx = wide.to(DEV)[:, :160]
+    out = torch.full((1, 128, 512), -7.0, dtype=torch.bfloat16, device=DEV)
+    kvq.kvq_sparse_mla_attention_nvfp4_ds_mla(w.q.to(DEV), idx, torch.from_numpy(cache).to(DEV), w.softmax_scale,
+                                              out=out, lse=False)
+    torch.cuda.synchronize()
+    _, lse_ref, _ = oracle_mod.sparse_mla_attention_nvfp4_ds_mla(wl.bf16_bits(w.q), wl.host(w.indices), cache,
+                                                                 w.softmax_scale)
+    check(oracle_mod, cache, w.q, wl.host(w.indices), w.softmax_scale, out,
+          torch.from_numpy(lse_ref.astype(np.float32)))

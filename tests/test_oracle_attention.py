@@ -1,4 +1,5 @@
-"""Pins for the oracle's sparse MLA attention over the nvfp4_ds_mla cache.
+"""Pins for the oracle's sparse MLA attention over the nvfp4_ds_mla and
+fp8_ds_mla caches.
 
 The attention is a plain definition (softmax-weighted sum of the cached latent
 rows, MQA form), so the oracle is pinned against an independent float64
@@ -151,3 +152,54 @@ def test_large_scores_do_not_overflow(oracle_mod):
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)) and np.abs(want_lse).max() > 1000
     np.testing.assert_allclose(o[0], want_o, rtol=1e-9, atol=1e-9 * np.abs(keys).max())
     np.testing.assert_allclose(lse[0], want_lse, rtol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# the same consumer over the 656-byte fp8_ds_mla cache
+# --------------------------------------------------------------------------
+
+def exact_fp8_cache(oracle_mod, n_slots, seed, num_blocks=8):
+    """Entries built byte by byte whose upconvert is exact: e4m3 NoPE codes
+    with power-of-two tile scales, bf16 RoPE.  Returns (cache, slots, keys)."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    cache = np.zeros((num_blocks, BS, 656), np.uint8)
+    slots = g.permutation(num_blocks * BS)[:n_slots]
+    keys = np.zeros((n_slots, 576))
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    for i, s in enumerate(slots):
+        e = cache[s // BS, s % BS]
+        codes = finite[g.integers(0, len(finite), 512)]
+        scales = (2.0 ** g.integers(-6, 4, 4)).astype(np.float32)
+        e[:512] = codes
+        e[512:528] = np.frombuffer(scales.astype("<f4").tobytes(), np.uint8)
+        rope_bits, rope = bf16_bits_of(g.standard_normal(64).astype(np.float32))
+        e[528:656] = np.frombuffer(rope_bits.astype("<u2").tobytes(), np.uint8)
+        keys[i, :512] = [oracle_mod.e4m3_value(int(c)) * float(scales[k // 128]) for k, c in enumerate(codes)]
+        keys[i, 512:] = rope
+    return cache, slots, keys
+
+
+def test_fp8_entry_decode_is_exact_on_constructed_entries(oracle_mod):
+    cache, slots, keys = exact_fp8_cache(oracle_mod, 6, 71)
+    for i, s in enumerate(slots):
+        np.testing.assert_array_equal(oracle_mod.decode_fp8_ds_mla_entry(cache[s // BS, s % BS]), keys[i])
+
+
+@pytest.mark.parametrize("scale", [1.0 / 24.0, 0.15])
+def test_fp8_attention_matches_numpy_definition(oracle_mod, scale):
+    cache, slots, keys = exact_fp8_cache(oracle_mod, 40, 72)
+    T, H, topk = 4, 5, 20
+    qb, qv = random_q(T, H, 73)
+    g = np.random.Generator(np.random.PCG64(74))
+    idx = np.full((T, topk), -1, np.int32)
+    for t in range(T):
+        pick = g.choice(40, size=topk - 2 * t, replace=False)
+        idx[t, :len(pick)] = slots[pick]
+    o, lse, skipped = oracle_mod.sparse_mla_attention_fp8_ds_mla(qb, idx, cache, scale)
+    assert skipped == 0
+    slot_row = {int(s): i for i, s in enumerate(slots)}
+    for t in range(T):
+        rows = [slot_row[int(s)] for s in idx[t] if s >= 0]
+        want_o, want_lse = numpy_attention(qv[t], keys[rows], scale)
+        np.testing.assert_allclose(o[t], want_o, rtol=1e-11, atol=1e-11 * np.abs(keys).max())
+        np.testing.assert_allclose(lse[t], want_lse, rtol=1e-12, atol=1e-12)
