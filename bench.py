@@ -471,31 +471,34 @@ def time_extra(step: GpuStep):
     # sparse MLA attention straight from the nvfp4_ds_mla cache (tensor
     # cores): 4096 decode tokens x 128 heads, top-2048 slots over the step's
     # 65536 x 64 cache (filled by the step's write), 10 % unused
+    # (the same over the step's 32768 x 64 fp8_ds_mla cache)
     if step.size == "full":
-        aw = wl.sparse_attention(dev, fill=step.g3.fill)
-        ao = torch.empty((aw.num_tokens, 128, 512), dtype=torch.bfloat16, device=dev)
-        al = torch.empty((aw.num_tokens, 128), dtype=torch.float32, device=dev)
-        times = []
-        for r in range(8):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            kvq.kvq_sparse_mla_attention_nvfp4_ds_mla(aw.q, aw.indices, step.cache3, aw.softmax_scale,
-                                                      out=ao, lse=al)
-            b.record()
-            torch.cuda.synchronize()
-            if r >= 2:
-                times.append(a.elapsed_time(b))
-        us = statistics.median(times) * 1e3
-        n_valid = int((aw.indices >= 0).sum())
-        flops = ATTN_FLOPS_PER_SLOT_HEAD * 128 * n_valid
-        peak_tf, peak_src = measured_peak_tflops()
-        nbytes = 352 * n_valid + aw.q.numel() * 2 + ao.numel() * 2 + al.numel() * 4 + aw.indices.numel() * 4
-        out["sparse_mla_attention_nvfp4_ds_mla T=4096 H=128 top-2048"] = {
-            "units": aw.num_tokens, "us": round(us, 2), "tflops": round(flops / us / 1e6, 1),
-            "bound": "tensor", "peak_tflops": peak_tf, "peak": f"{peak_src} bf16 burst",
-            "frac": round(flops / us / 1e6 / peak_tf, 4), "gbs": round(nbytes / us / 1e3, 1),
-            "valid_slots": n_valid, "method": "CUDA events"}
-        del aw, ao, al
+        for fmt, fill, cache, entry, fn in (
+                ("nvfp4_ds_mla", step.g3.fill, step.cache3, 352, kvq.kvq_sparse_mla_attention_nvfp4_ds_mla),
+                ("fp8_ds_mla", step.g4.fill, step.cache4, 656, kvq.kvq_sparse_mla_attention_fp8_ds_mla)):
+            aw = wl.sparse_attention(dev, fill=fill)
+            ao = torch.empty((aw.num_tokens, 128, 512), dtype=torch.bfloat16, device=dev)
+            al = torch.empty((aw.num_tokens, 128), dtype=torch.float32, device=dev)
+            times = []
+            for r in range(8):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn(aw.q, aw.indices, cache, aw.softmax_scale, out=ao, lse=al)
+                b.record()
+                torch.cuda.synchronize()
+                if r >= 2:
+                    times.append(a.elapsed_time(b))
+            us = statistics.median(times) * 1e3
+            n_valid = int((aw.indices >= 0).sum())
+            flops = ATTN_FLOPS_PER_SLOT_HEAD * 128 * n_valid
+            peak_tf, peak_src = measured_peak_tflops()
+            nbytes = entry * n_valid + aw.q.numel() * 2 + ao.numel() * 2 + al.numel() * 4 + aw.indices.numel() * 4
+            out[f"sparse_mla_attention_{fmt} T=4096 H=128 top-2048"] = {
+                "units": aw.num_tokens, "us": round(us, 2), "tflops": round(flops / us / 1e6, 1),
+                "bound": "tensor", "peak_tflops": peak_tf, "peak": f"{peak_src} bf16 burst",
+                "frac": round(flops / us / 1e6 / peak_tf, 4), "gbs": round(nbytes / us / 1e3, 1),
+                "valid_slots": n_valid, "method": "CUDA events"}
+            del aw, ao, al
     # fp8_ds_mla cache fill: 2,097,152 tokens, one launch
     f4 = step.g4.fill
     times = []

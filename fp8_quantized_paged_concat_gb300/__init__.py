@@ -21,7 +21,7 @@ __all__ = [
     "kvq_write_nvfp4_ds_mla", "kvq_write_fp8_ds_mla", "kvq_gather_upconvert_nvfp4_ds_mla",
     "kvq_gather_upconvert_fp8_ds_mla", "kvq_reshape_and_cache_nvfp4", "kvq_selftest_convert",
     "kvq_dequant_nvfp4_per_head", "kvq_req_index_to_global_slot",
-    "kvq_sparse_mla_attention_nvfp4_ds_mla", "kvq_last_error_string", "kvq_version", "library_path", "load_library",
+    "kvq_sparse_mla_attention_nvfp4_ds_mla", "kvq_sparse_mla_attention_fp8_ds_mla", "kvq_last_error_string", "kvq_version", "library_path", "load_library",
     "NVFP4_DS_MLA_ENTRY_BYTES", "FP8_DS_MLA_ENTRY_BYTES", "STATUS_BAD_INDEX", "STATUS_BAD_BATCH",
     "STATUS_TIMEOUT",
     "nvfp4_full_dim",
@@ -58,6 +58,9 @@ _SIGNATURES = {
     "kvq_sparse_mla_attention_nvfp4_ds_mla": [_P, _I64, _I64, _I64, _I32, _P, _I64, _I32, _P, _I64, _I32,
                                               _I64, _I64, ctypes.c_float, _P, _I64, _I64, _P, _I64,
                                               _P, _P],
+    "kvq_sparse_mla_attention_fp8_ds_mla": [_P, _I64, _I64, _I64, _I32, _P, _I64, _I32, _P, _I64, _I32,
+                                            _I64, _I64, ctypes.c_float, _P, _I64, _I64, _P, _I64,
+                                            _P, _P],
 }
 
 
@@ -279,13 +282,25 @@ def kvq_sparse_mla_attention_nvfp4_ds_mla(q, indices, kv_cache, softmax_scale: f
     q bf16 [T, H, 576] (H <= 128), indices int32 [T, topk] global slots (< 0
     unused), kv_cache uint8 [num_blocks, block_size, >=352].  Returns (out
     bf16 [T, H, 512], lse fp32 [T, H]); lse=False skips the lse output."""
+    return _attention("kvq_sparse_mla_attention_nvfp4_ds_mla", 352, q, indices, kv_cache, softmax_scale, out,
+                      lse, status, stream)
+
+
+def kvq_sparse_mla_attention_fp8_ds_mla(q, indices, kv_cache, softmax_scale: float, out=None, lse=None,
+                                        status=None, stream=None):
+    """The same attention straight from the 656-byte fp8_ds_mla cache."""
+    return _attention("kvq_sparse_mla_attention_fp8_ds_mla", 656, q, indices, kv_cache, softmax_scale, out,
+                      lse, status, stream)
+
+
+def _attention(cname, entry, q, indices, kv_cache, softmax_scale, out, lse, status, stream):
     _need(q.dtype == torch.bfloat16 and q.is_cuda and q.dim() == 3 and q.shape[2] == 576
           and q.stride(2) == 1, "q: expected a CUDA bf16 [T, H, 576] tensor with unit inner stride")
     T, H = q.shape[0], q.shape[1]
     _need(indices.dtype == torch.int32 and indices.is_cuda and indices.dim() == 2
           and indices.shape[0] == T and (indices.shape[1] == 0 or indices.stride(1) == 1),
           "indices: expected CUDA int32 [T, topk] rows")
-    _mla_cache("kv_cache", kv_cache, 352)
+    _mla_cache("kv_cache", kv_cache, entry)
     if out is None:
         out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=q.device)
     _need(out.dtype == torch.bfloat16 and out.is_cuda and tuple(out.shape) == (T, H, 512)
@@ -295,7 +310,7 @@ def kvq_sparse_mla_attention_nvfp4_ds_mla(q, indices, kv_cache, softmax_scale: f
     if lse is not False:
         _need(lse.dtype == torch.float32 and lse.is_cuda and tuple(lse.shape) == (T, H) and lse.stride(1) == 1,
               "lse: expected a CUDA fp32 [T, H] tensor with unit inner stride")
-    _call("kvq_sparse_mla_attention_nvfp4_ds_mla", q.data_ptr(), q.stride(0), q.stride(1), T, H,
+    _call(cname, q.data_ptr(), q.stride(0), q.stride(1), T, H,
           indices.data_ptr(), max(indices.stride(0), indices.shape[1]), indices.shape[1], kv_cache.data_ptr(), kv_cache.shape[0],
           kv_cache.shape[1], kv_cache.stride(0), kv_cache.stride(1), float(softmax_scale), out.data_ptr(),
           out.stride(0), out.stride(1), None if lse is False else lse.data_ptr(),

@@ -303,13 +303,15 @@ kvq_status kvq_req_index_to_global_slot(const int32_t* req_id, int64_t num_req_i
   return launched(fn, kvq::launch_req_index_to_global_slot(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-kvq_status kvq_sparse_mla_attention_nvfp4_ds_mla(
+namespace {
+
+kvq_status attention_common(
+    const char* fn, int64_t entry_bytes, cudaError_t (*launch)(const kvq::AttentionArgs&, cudaStream_t),
     const void* q, int64_t q_stride_t, int64_t q_stride_h, int64_t num_tokens, int32_t num_heads,
     const int32_t* indices, int64_t indices_stride, int32_t topk, const uint8_t* kv_cache,
     int64_t num_blocks, int32_t block_size, int64_t block_stride, int64_t entry_stride,
     float softmax_scale, void* out, int64_t out_stride_t, int64_t out_stride_h, float* lse,
     int64_t lse_stride_t, int32_t* d_status, kvq_stream_t stream) {
-  const char* fn = "kvq_sparse_mla_attention_nvfp4_ds_mla";
   KVQ_REQUIRE(num_tokens >= 0 && topk >= 0, "%s: num_tokens / topk < 0", fn);
   if (num_tokens == 0) return ok();
   KVQ_REQUIRE(num_tokens < (int64_t{1} << 30), "%s: num_tokens too large", fn);   // 2 CTAs each
@@ -331,7 +333,7 @@ kvq_status kvq_sparse_mla_attention_nvfp4_ds_mla(
   KVQ_REQUIRE(softmax_scale == softmax_scale && softmax_scale > -3.0e38f && softmax_scale < 3.0e38f,
               "%s: softmax_scale must be finite", fn);
   if (kvq_status s = check_mla_cache(fn, kv_cache, num_blocks, block_size, block_stride,
-                                     entry_stride, KVQ_NVFP4_DS_MLA_ENTRY_BYTES))
+                                     entry_stride, entry_bytes))
     return s;
   KVQ_REQUIRE(d_status == nullptr || aligned(d_status, 4), "%s: d_status misaligned", fn);
   if (kvq_status s = check_device(fn)) return s;
@@ -357,7 +359,35 @@ kvq_status kvq_sparse_mla_attention_nvfp4_ds_mla(
   a.lse = lse;
   a.lse_stride_t = lse_stride_t;
   a.status = d_status;
-  return launched(fn, kvq::launch_sparse_mla_attention_nvfp4(a, reinterpret_cast<cudaStream_t>(stream)));
+  return launched(fn, launch(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+kvq_status kvq_sparse_mla_attention_nvfp4_ds_mla(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h, int64_t num_tokens, int32_t num_heads,
+    const int32_t* indices, int64_t indices_stride, int32_t topk, const uint8_t* kv_cache,
+    int64_t num_blocks, int32_t block_size, int64_t block_stride, int64_t entry_stride,
+    float softmax_scale, void* out, int64_t out_stride_t, int64_t out_stride_h, float* lse,
+    int64_t lse_stride_t, int32_t* d_status, kvq_stream_t stream) {
+  return attention_common("kvq_sparse_mla_attention_nvfp4_ds_mla", KVQ_NVFP4_DS_MLA_ENTRY_BYTES,
+                          kvq::launch_sparse_mla_attention_nvfp4, q, q_stride_t, q_stride_h, num_tokens,
+                          num_heads, indices, indices_stride, topk, kv_cache, num_blocks, block_size,
+                          block_stride, entry_stride, softmax_scale, out, out_stride_t, out_stride_h, lse,
+                          lse_stride_t, d_status, stream);
+}
+
+kvq_status kvq_sparse_mla_attention_fp8_ds_mla(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h, int64_t num_tokens, int32_t num_heads,
+    const int32_t* indices, int64_t indices_stride, int32_t topk, const uint8_t* kv_cache,
+    int64_t num_blocks, int32_t block_size, int64_t block_stride, int64_t entry_stride,
+    float softmax_scale, void* out, int64_t out_stride_t, int64_t out_stride_h, float* lse,
+    int64_t lse_stride_t, int32_t* d_status, kvq_stream_t stream) {
+  return attention_common("kvq_sparse_mla_attention_fp8_ds_mla", KVQ_FP8_DS_MLA_ENTRY_BYTES,
+                          kvq::launch_sparse_mla_attention_fp8, q, q_stride_t, q_stride_h, num_tokens,
+                          num_heads, indices, indices_stride, topk, kv_cache, num_blocks, block_size,
+                          block_stride, entry_stride, softmax_scale, out, out_stride_t, out_stride_h, lse,
+                          lse_stride_t, d_status, stream);
 }
 
 kvq_status kvq_selftest_convert(uint32_t first_bits, int64_t count, uint8_t* e4m3_lo,

@@ -57,7 +57,8 @@ constexpr int kProducerWarps = 8;
 constexpr int kRowsPerProducer = kTile / kProducerWarps;     // 8
 constexpr int kThreads = (kSoftmaxWarps + kProducerWarps + 1) * 32;   // + the MMA warp: 544
 constexpr int kMmaThread = 16 * 32;
-constexpr int kNvRopeOff = 256, kNvSfOff = 320;
+constexpr int kNvRopeOff = 256, kNvSfOff = 320;                  // nvfp4_ds_mla entry
+constexpr int kF8ScaleOff = 512, kF8RopeOff = 528;                // fp8_ds_mla entry
 constexpr float kRescaleLog2 = 8.0f;                         // lazy rescale threshold (base 2)
 
 // Shared memory (offsets from a 1024-byte aligned base).
@@ -358,15 +359,26 @@ __device__ __forceinline__ uint4 e2m1x8_lut(uint32_t x, const GroupTable& t) {
 // producers: the CTA's share of a 64-slot tile
 // ---------------------------------------------------------------------------
 
-// Producer p (rows 8p .. 8p+7 of the tile): lane `lane` handles NoPE group
-// g = lane % 16 of rows 8p + lane / 16 + 2i (i < 4) and RoPE piece
-// k = lane % 4 (the CTA's 32 RoPE values are pieces 4 half + k) of row
-// 8p + lane / 4.
-struct TileRegs {
-  uint2 nib[4];
-  uint32_t sf[4];
-  uint2 rope;
+// The two entry formats the producers decode (the rest of the kernel is the
+// same): 352-byte nvfp4_ds_mla and 656-byte fp8_ds_mla.
+enum class Entry { kNvfp4, kFp8 };
+
+// Producer p (rows 8p .. 8p+7 of the tile): lane `lane` handles NoPE piece
+// g = lane % 16 (local values 16g .. 16g+15 of the CTA's 256) of rows
+// 8p + lane / 16 + 2i (i < 4) and RoPE piece k = lane % 4 (values
+// 32 half + 8k .. +7) of row 8p + lane / 4.
+template <Entry F> struct TileRegs;
+template <> struct TileRegs<Entry::kNvfp4> {
+  uint2 nib[4];                          // 16 e2m1 codes
+  uint32_t sf[4];                        // their e4m3 scale
+  uint2 rope;                            // 8 e4m3 RoPE values
   uint32_t valid;                        // bits 0-3: NoPE rows, bit 4: RoPE row
+};
+template <> struct TileRegs<Entry::kFp8> {
+  uint4 code[4];                         // 16 e4m3 codes
+  float sc[4];                           // their 128-value tile's fp32 scale
+  uint4 rope;                            // 8 bf16 RoPE values
+  uint32_t valid;
 };
 
 __device__ __forceinline__ const uint8_t* entry_of(const AttentionArgs& a, int32_t slot) {
@@ -384,8 +396,9 @@ __device__ __forceinline__ int32_t tile_slot(const AttentionArgs& a, const int32
 
 // Issues the tile's entry loads; `mine` = tile_slot(...) of this lane, read
 // a tile earlier so that the loads need not wait for it.
+template <Entry F>
 __device__ __forceinline__ void load_tile(const AttentionArgs& a, int32_t mine, int lane, uint32_t half,
-                                          TileRegs& e, bool& bad_index) {
+                                          TileRegs<F>& e, bool& bad_index) {
   if (mine >= a.num_slots) bad_index = true;
   e.valid = 0;
   const int g = lane & 15, k = lane & 3;
@@ -395,31 +408,59 @@ __device__ __forceinline__ void load_tile(const AttentionArgs& a, int32_t mine, 
     if (slot >= 0 && slot < a.num_slots) {
       const uint8_t* p = entry_of(a, slot);
       e.valid |= 1u << i;
-      e.nib[i] = __ldg(reinterpret_cast<const uint2*>(p + 128 * half + 8 * g));
-      e.sf[i] = __ldg(p + kNvSfOff + 16 * half + g);
+      if constexpr (F == Entry::kNvfp4) {
+        e.nib[i] = __ldg(reinterpret_cast<const uint2*>(p + 128 * half + 8 * g));
+        e.sf[i] = __ldg(p + kNvSfOff + 16 * half + g);
+      } else {
+        e.code[i] = __ldg(reinterpret_cast<const uint4*>(p + kHalf * half + 16 * g));
+        e.sc[i] = __ldg(reinterpret_cast<const float*>(p + kF8ScaleOff) + 2 * half + (g >> 3));
+      }
     }
   }
   {
     const int32_t slot = __shfl_sync(0xffffffffu, mine, lane >> 2);
     if (slot >= 0 && slot < a.num_slots) {
       e.valid |= 16u;
-      e.rope = __ldg(reinterpret_cast<const uint2*>(entry_of(a, slot) + kNvRopeOff + 32 * half + 8 * k));
+      if constexpr (F == Entry::kNvfp4)
+        e.rope = __ldg(reinterpret_cast<const uint2*>(entry_of(a, slot) + kNvRopeOff + 32 * half + 8 * k));
+      else
+        e.rope = __ldg(reinterpret_cast<const uint4*>(entry_of(a, slot) + kF8RopeOff + 64 * half + 16 * k));
     }
   }
 }
 
-__device__ __forceinline__ void store_tile(uint32_t kbuf, int row0, int lane, uint32_t half, const TileRegs& e) {
+// 16 e4m3 codes times their tile's fp32 scale -> 16 bf16, as the fp8 gather
+// upconverts them: one fp32 product rounding, one bf16 rounding.
+__device__ __forceinline__ void e4m3x16_scaled(const uint4& c, float s, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 v = __half22float2(e4m3x2_to_half2(w[i >> 1] >> (16 * (i & 1))));
+    o[i] = pack_bf16x2(__fmul_rn(v.x, s), __fmul_rn(v.y, s));
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+template <Entry F>
+__device__ __forceinline__ void store_tile(uint32_t kbuf, int row0, int lane, uint32_t half,
+                                           const TileRegs<F>& e) {
   const int g = lane & 15, k = lane & 3;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t r = row0 + (lane >> 4) + 2 * i;
     uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
     if (e.valid & (1u << i)) {
-      const GroupTable t = group_table(e.sf[i]);
-      lo = e2m1x8_lut(e.nib[i].x, t);
-      hi = e2m1x8_lut(e.nib[i].y, t);
+      if constexpr (F == Entry::kNvfp4) {
+        const GroupTable t = group_table(e.sf[i]);
+        lo = e2m1x8_lut(e.nib[i].x, t);
+        hi = e2m1x8_lut(e.nib[i].y, t);
+      } else {
+        e4m3x16_scaled(e.code[i], e.sc[i], lo, hi);
+      }
     }
-    // group g: local dims 16g .. 16g+15 = block g/4, chunks 2(g%4) + {0, 1}
+    // piece g: local dims 16g .. 16g+15 = block g/4, chunks 2(g%4) + {0, 1}
     const uint32_t blk = kbuf + (g >> 2) * kKBlock;
     st_shared16(blk + sw128_offset(r, 2 * (g & 3)), lo);
     st_shared16(blk + sw128_offset(r, 2 * (g & 3) + 1), hi);
@@ -427,13 +468,19 @@ __device__ __forceinline__ void store_tile(uint32_t kbuf, int row0, int lane, ui
   {
     const uint32_t r = row0 + (lane >> 2);
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (e.valid & 16u) v = e4m3x8_bf16(e.rope);
+    if (e.valid & 16u) {
+      if constexpr (F == Entry::kNvfp4)
+        v = e4m3x8_bf16(e.rope);
+      else
+        v = e.rope;                      // bf16 as stored
+    }
     st_shared16(kbuf + 4 * kKBlock + sw128_offset(r, 4 * half + k), v);
   }
 }
 
+template <Entry F>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
+sparse_mla_attention_kernel(const AttentionArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -642,8 +689,8 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
   } else if (warp < 16) {
     // ---- producers: decode tiles into the K ring ----------------------------
     const int row0 = (warp < 8 ? warp - 4 : warp - 8) * kRowsPerProducer;
-    TileRegs cur, nxt;
-    if (n_tiles > 0) load_tile(a, tile_slot(a, idx, 0, row0, lane), lane, half, cur, bad_index);
+    TileRegs<F> cur, nxt;
+    if (n_tiles > 0) load_tile<F>(a, tile_slot(a, idx, 0, row0, lane), lane, half, cur, bad_index);
     int32_t slot_next = tile_slot(a, idx, 1, row0, lane);        // slots one tile ahead of the loads
     uint32_t stage = 0, phase = 0;                               // ring position of tile t
     // The next tile's loads are issued after each arrive: a release waits for
@@ -651,12 +698,12 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
     for (int t = 0; t < n_tiles; ++t) {
       // stage reuse: P V of tile t - kKStages must be done
       if (t >= kKStages && !wait_or_abort(k_empty0 + 8 * stage, phase ^ 1, s_abort)) break;
-      store_tile(base + kKOff + stage * kKBytes, row0, lane, half, cur);
+      store_tile<F>(base + kKOff + stage * kKBytes, row0, lane, half, cur);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(k_full0 + 8 * stage);
       if (t + 1 < n_tiles) {
-        load_tile(a, slot_next, lane, half, nxt, bad_index);
+        load_tile<F>(a, slot_next, lane, half, nxt, bad_index);
         slot_next = tile_slot(a, idx, t + 2, row0, lane);
       }
       cur = nxt;
@@ -766,13 +813,21 @@ sparse_mla_attention_nvfp4_kernel(const AttentionArgs a) {
 
 }  // namespace
 
-cudaError_t launch_sparse_mla_attention_nvfp4(const AttentionArgs& a, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(sparse_mla_attention_nvfp4_kernel,
+template <Entry F>
+cudaError_t launch_attention(const AttentionArgs& a, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(sparse_mla_attention_kernel<F>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  sparse_mla_attention_nvfp4_kernel<<<static_cast<unsigned>(a.num_tokens * 2), kThreads, kSmemBytes,
-                                      stream>>>(a);
+  sparse_mla_attention_kernel<F><<<static_cast<unsigned>(a.num_tokens * 2), kThreads, kSmemBytes, stream>>>(a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_mla_attention_nvfp4(const AttentionArgs& a, cudaStream_t stream) {
+  return launch_attention<Entry::kNvfp4>(a, stream);
+}
+
+cudaError_t launch_sparse_mla_attention_fp8(const AttentionArgs& a, cudaStream_t stream) {
+  return launch_attention<Entry::kFp8>(a, stream);
 }
 
 }  // namespace kvq

@@ -97,6 +97,7 @@ cudaError_t launch_reshape_and_cache_nvfp4(const PerHeadArgs& a, cudaStream_t st
 // Read-back: key / value are the bf16 OUTPUTS (written through const_cast).
 cudaError_t launch_dequant_nvfp4_per_head(const PerHeadArgs& a, cudaStream_t stream);
 cudaError_t launch_sparse_mla_attention_nvfp4(const AttentionArgs& a, cudaStream_t stream);
+cudaError_t launch_sparse_mla_attention_fp8(const AttentionArgs& a, cudaStream_t stream);
 
 struct IndexArgs {
   const int32_t* req_id;

@@ -264,6 +264,26 @@ kvq_status kvq_sparse_mla_attention_nvfp4_ds_mla(
     int32_t* d_status, kvq_stream_t stream);
 
 /*
+ * kvq_sparse_mla_attention_fp8_ds_mla -- the same attention read straight
+ * from the 656-byte fp8_ds_mla cache ([P1] "Key source snippets": the sparse
+ * decode path serves both quantized DS-MLA formats; [P3] is about this
+ * cache).  The key of a slot is what kvq_gather_upconvert_fp8_ds_mla writes
+ * for it: NoPE value k = bf16_rn(fp32(e4m3) * s_{k/128}) (one fp32 product
+ * rounding), RoPE the stored bf16.  Arguments, arithmetic, outputs and status
+ * as kvq_sparse_mla_attention_nvfp4_ds_mla; entry_stride >= 656.
+ */
+kvq_status kvq_sparse_mla_attention_fp8_ds_mla(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h,
+    int64_t num_tokens, int32_t num_heads,
+    const int32_t* indices, int64_t indices_stride, int32_t topk,
+    const uint8_t* kv_cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride,
+    float softmax_scale,
+    void* out, int64_t out_stride_t, int64_t out_stride_h,
+    float* lse, int64_t lse_stride_t,
+    int32_t* d_status, kvq_stream_t stream);
+
+/*
  * kvq_req_index_to_global_slot -- sparse-decode index conversion feeding the
  * sparse MLA decode ([P3] "Implementation breakdown" item 1:
  * triton_convert_req_index_to_global_index and its length check).  For decode

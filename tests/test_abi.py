@@ -256,3 +256,9 @@ def test_attention_rejects_bad_arguments_on_host(lib, over, needle):
 @no_gpu_only
 def test_attention_zero_tokens_is_noop(lib):
     assert lib.kvq_sparse_mla_attention_nvfp4_ds_mla(*attention_args(num_tokens=0, q=None)) == 0
+
+
+@no_gpu_only
+def test_fp8_attention_requires_656_byte_entries(lib):
+    assert lib.kvq_sparse_mla_attention_fp8_ds_mla(*attention_args(entry_stride=352, block_stride=64 * 352)) == 1
+    assert "656" in err(lib), err(lib)

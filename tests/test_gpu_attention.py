@@ -40,18 +40,30 @@ def threads(oracle_mod):
     return oracle_mod.default_threads()
 
 
-def host_cache(oracle_mod, fill, threads=1):
-    cache = np.zeros((fill.num_blocks, fill.block_size, 352), np.uint8)
-    assert oracle_mod.write_nvfp4_ds_mla(wl.bf16_bits(fill.kv_c), wl.bf16_bits(fill.k_pe),
-                                         wl.host(fill.slot_mapping), cache, threads=threads) == 0
+# entry format -> (entry bytes, oracle write, oracle decode, oracle attention, kernel entry point)
+FORMATS = {
+    "nvfp4": (352, "write_nvfp4_ds_mla", "decode_nvfp4_ds_mla_entry", "sparse_mla_attention_nvfp4_ds_mla",
+              "kvq_sparse_mla_attention_nvfp4_ds_mla"),
+    "fp8": (656, "write_fp8_ds_mla", "decode_fp8_ds_mla_entry", "sparse_mla_attention_fp8_ds_mla",
+            "kvq_sparse_mla_attention_fp8_ds_mla"),
+}
+
+
+def host_cache(oracle_mod, fill, threads=1, fmt="nvfp4"):
+    entry, write = FORMATS[fmt][:2]
+    cache = np.zeros((fill.num_blocks, fill.block_size, entry), np.uint8)
+    assert getattr(oracle_mod, write)(wl.bf16_bits(fill.kv_c), wl.bf16_bits(fill.k_pe),
+                                      wl.host(fill.slot_mapping), cache, threads=threads) == 0
     return cache
 
 
 def decoded_keys(oracle_mod, cache, slots):
     """float64 [n, 576] decoded entries of the given slots (oracle decode)."""
     bs = cache.shape[1]
+    decode = getattr(oracle_mod, "decode_fp8_ds_mla_entry" if cache.shape[2] == 656 else
+                     "decode_nvfp4_ds_mla_entry")
     uniq, inv = np.unique(slots, return_inverse=True)
-    table = np.stack([oracle_mod.decode_nvfp4_ds_mla_entry(cache[s // bs, s % bs]) for s in uniq])
+    table = np.stack([decode(cache[s // bs, s % bs]) for s in uniq])
     return table[inv]
 
 
@@ -65,8 +77,8 @@ def check(oracle_mod, cache, q, idx, scale, out, lse, threads=1, tokens=None):
     qb = wl.bf16_bits(q)
     idx = np.asarray(idx, np.int32)
     tokens = np.arange(q.shape[0]) if tokens is None else np.asarray(tokens)
-    want_o, want_lse, _ = oracle_mod.sparse_mla_attention_nvfp4_ds_mla(
-        np.ascontiguousarray(qb[tokens]), idx[tokens], cache, scale, threads=threads)
+    attention = getattr(oracle_mod, FORMATS["fp8" if cache.shape[2] == 656 else "nvfp4"][3])
+    want_o, want_lse, _ = attention(np.ascontiguousarray(qb[tokens]), idx[tokens], cache, scale, threads=threads)
     got_o = out.float().cpu().numpy()[tokens].astype(np.float64)
     got_lse = lse.cpu().numpy()[tokens].astype(np.float64)
     qv = q_values(q)[tokens]
@@ -91,9 +103,9 @@ def check(oracle_mod, cache, q, idx, scale, out, lse, threads=1, tokens=None):
         assert np.all(err_l <= tol_l), f"token {t}: lse error {err_l.max()} > {tol_l.min()}"
 
 
-def run(kvq, oracle_mod, w, cache=None, threads=1, tokens=None, strided=False):
+def run(kvq, oracle_mod, w, cache=None, threads=1, tokens=None, strided=False, fmt="nvfp4"):
     if cache is None:
-        cache = host_cache(oracle_mod, w.fill, threads)
+        cache = host_cache(oracle_mod, w.fill, threads, fmt)
     dcache = torch.from_numpy(cache).to(DEV)
     q = w.q.to(DEV)
     T, H = q.shape[0], q.shape[1]
@@ -110,8 +122,7 @@ def run(kvq, oracle_mod, w, cache=None, threads=1, tokens=None, strided=False):
         lse = torch.full((T, H), -7.0, dtype=torch.float32, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     idx = w.indices.to(DEV)
-    kvq.kvq_sparse_mla_attention_nvfp4_ds_mla(q, idx, dcache, w.softmax_scale, out=out, lse=lse,
-                                              status=status)
+    getattr(kvq, FORMATS[fmt][4])(q, idx, dcache, w.softmax_scale, out=out, lse=lse, status=status)
     torch.cuda.synchronize()
     check(oracle_mod, cache, w.q, wl.host(w.indices), w.softmax_scale, out, lse, threads, tokens)
     if strided:
@@ -132,18 +143,21 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("fmt", sorted(FORMATS))
 @pytest.mark.parametrize("name,kw", CASES, ids=[c[0] for c in CASES])
-def test_attention_parity(kvq, oracle_mod, name, kw):
+def test_attention_parity(kvq, oracle_mod, name, kw, fmt):
     w = wl.make_attention(name, **kw)
-    assert run(kvq, oracle_mod, w) == 0
+    assert run(kvq, oracle_mod, w, fmt=fmt) == 0
 
 
-def test_attention_strided_q_out_lse(kvq, oracle_mod):
+@pytest.mark.parametrize("fmt", sorted(FORMATS))
+def test_attention_strided_q_out_lse(kvq, oracle_mod, fmt):
     w = wl.make_attention("strided", 3, 20, 70, 8, 64, 311, p_unused=0.1)
-    assert run(kvq, oracle_mod, w, strided=True) == 0
+    assert run(kvq, oracle_mod, w, strided=True, fmt=fmt) == 0
 
 
-def test_attention_empty_and_bad_slots(kvq, oracle_mod):
+@pytest.mark.parametrize("fmt", sorted(FORMATS))
+def test_attention_empty_and_bad_slots(kvq, oracle_mod, fmt):
     """Token 0: every entry unused; token 1: only out-of-range slots; token 2:
     a mix; topk = 40.  Out-of-range slots set the status bit and are skipped."""
     w = wl.make_attention("edge", 3, 8, 40, 4, 16, 312)
@@ -152,7 +166,7 @@ def test_attention_empty_and_bad_slots(kvq, oracle_mod):
     idx[1] = 64 + np.arange(40)
     idx[2, ::3] = 1 << 30
     w.indices = torch.from_numpy(idx)
-    assert run(kvq, oracle_mod, w) == kvq.STATUS_BAD_INDEX
+    assert run(kvq, oracle_mod, w, fmt=fmt) == kvq.STATUS_BAD_INDEX
 
 
 def test_attention_topk_zero(kvq, oracle_mod):
@@ -209,3 +223,36 @@ def test_attention_single_token_strided_indices_no_lse(kvq, oracle_mod):
                                                                  w.softmax_scale)
     check(oracle_mod, cache, w.q, wl.host(w.indices), w.softmax_scale, out,
           torch.from_numpy(lse_ref.astype(np.float32)))
+
+
+def test_attention_fp8_random_codes_and_scales(kvq, oracle_mod):
+    """fp8_ds_mla entries of random bytes: every e4m3 code (NaN codes
+    replaced), power-of-two tile scales from 2^-8 to 2^8 and bf16 RoPE values
+    of magnitudes 2^-8 .. 2^8 (scores must fit the fp32 accumulator, as
+    for any input of the kernel)."""
+    g = np.random.Generator(np.random.PCG64(341))
+    cache = wl.random_bytes((16, 64, 656), 342)
+    wl.nan_free_e4m3_bytes(cache[:, :, :512])
+    scales = (2.0 ** g.integers(-8, 9, (16, 64, 4))).astype("<f4")
+    cache[:, :, 512:528] = scales.view(np.uint8).reshape(16, 64, 16)
+    rope = (g.standard_normal((16, 64, 64)) * 2.0 ** g.integers(-8, 9, (16, 64, 64))).astype(np.float32)
+    rope_bits = (rope.view(np.uint32) >> 16).astype("<u2")
+    cache[:, :, 528:656] = rope_bits.view(np.uint8).reshape(16, 64, 128)
+    w = wl.make_attention("fp8 random bytes", 4, 128, 192, 16, 64, 343, p_unused=0.1, softmax_scale=1e-4)
+    assert run(kvq, oracle_mod, w, cache=cache, fmt="fp8") == 0
+
+
+def test_attention_fp8_full_size_sampled(kvq, oracle_mod, threads):
+    """4096 tokens x 128 heads, top-2048 over a 32768 x 64 fp8_ds_mla cache
+    filled by the oracle's write; 32 sampled tokens against the oracle."""
+    fill = wl.make_fill("fp8 attention fill", 32768, 64, 1004, DEV, entry_bytes=656, rng="device")
+    cache_host = host_cache(oracle_mod, fill, threads, "fp8")
+    cache = torch.from_numpy(cache_host).to(DEV)
+    w = wl.make_attention("fp8 attention", 4096, 128, 2048, 32768, 64, 1008, DEV, p_unused=0.1, fill=fill,
+                          rng="device")
+    del fill
+    out, lse = kvq.kvq_sparse_mla_attention_fp8_ds_mla(w.q, w.indices, cache, w.softmax_scale)
+    torch.cuda.synchronize()
+    g = np.random.Generator(np.random.PCG64(78))
+    tokens = np.unique(np.concatenate([[0, w.num_tokens - 1], g.choice(w.num_tokens, 30, replace=False)]))
+    check(oracle_mod, cache_host, w.q, wl.host(w.indices), w.softmax_scale, out, lse, threads, tokens)

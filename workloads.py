@@ -308,9 +308,9 @@ def per_head(device="cpu") -> PerHeadWorkload:
 
 
 def sparse_attention(device="cpu", fill: WriteWorkload = None) -> AttentionWorkload:
-    """Sparse MLA decode over the nvfp4_ds_mla cache: 4096 tokens x 128
-    heads, top-2048 slots each (10 % unused) drawn over a 65536 x 64 cache
-    (the prefill fill when given), softmax scale 576^-0.5."""
+    """Sparse MLA decode: 4096 tokens x 128 heads, top-2048 slots each (10 %
+    unused) drawn over the given cache fill (else a fresh 65536 x 64
+    nvfp4_ds_mla fill), softmax scale 576^-0.5."""
     return make_attention("sparse MLA attention T=4096 H=128 top-2048", 4096, 128, 2048, 65536, 64, 1006,
                           device, p_unused=0.1, fill=fill,
                           rng="device" if str(device).startswith("cuda") else "numpy")
