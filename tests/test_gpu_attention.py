@@ -256,3 +256,13 @@ def test_attention_fp8_full_size_sampled(kvq, oracle_mod, threads):
     g = np.random.Generator(np.random.PCG64(78))
     tokens = np.unique(np.concatenate([[0, w.num_tokens - 1], g.choice(w.num_tokens, 30, replace=False)]))
     check(oracle_mod, cache_host, w.q, wl.host(w.indices), w.softmax_scale, out, lse, threads, tokens)
+
+
+@pytest.mark.parametrize("fmt", sorted(FORMATS))
+@pytest.mark.parametrize("heads", [2, 32, 127])
+@pytest.mark.parametrize("topk", [1, 65, 257])
+def test_attention_shape_sweep(kvq, oracle_mod, fmt, heads, topk):
+    """Head counts that are not a warp multiple and top-k lengths of one
+    slot, one slot past a tile and one past four tiles."""
+    w = wl.make_attention(f"sweep H{heads} k{topk}", 2, heads, topk, 8, 64, 400 + heads + topk, p_unused=0.05)
+    assert run(kvq, oracle_mod, w, fmt=fmt) == 0
