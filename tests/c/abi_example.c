@@ -1,9 +1,13 @@
 /*
  * abi_example.c -- the C ABI used from plain C (no Python, no torch): write
- * 64 tokens into a 2 x 64 x 352 nvfp4_ds_mla cache, gather 40 rows back, and
- * compare both with the CPU oracle linked beside it.  Exit status 0 on a
- * bit-exact match.  Built and run by tests/test_c_abi.py on a GPU host.
+ * 64 tokens into a 2 x 64 x 352 nvfp4_ds_mla cache, gather 40 rows back, run
+ * the sparse MLA attention of 2 tokens x 16 heads over 48 of its slots, and
+ * compare all three with the CPU oracle linked beside it (bit for bit for the
+ * write and the gather, within the bound derived from the attention's
+ * arithmetic for the attention).  Exit status 0 on success.  Built and run by
+ * tests/test_c_abi.py on a GPU host.
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -90,6 +94,69 @@ int main(void) {
   if (status != 0) { fprintf(stderr, "device status %d\n", status); return 5; }
   if (memcmp(cache, want_cache, sizeof cache) != 0) { fprintf(stderr, "cache differs\n"); return 6; }
   if (memcmp(rows, want_rows, sizeof rows) != 0) { fprintf(stderr, "rows differ\n"); return 7; }
-  printf("C ABI: write (64 tokens) and gather (40 rows) match the oracle bit for bit\n");
+
+  /* attention: 2 tokens x 16 heads, 48 slots each (every 7th unused) */
+  enum { AT = 2, AH = 16, AK = 48 };
+  static uint16_t q[AT * AH * 576], o_bits[AT * AH * 512];
+  static int32_t aidx[AT * AK];
+  static float lse[AT * AH];
+  static double want_o[AT * AH * 512], want_lse[AT * AH], keys[AK * 576];
+  const float scale = 0.0416667f;
+  for (i = 0; i < AT * AH * 576; ++i) q[i] = rand_bf16();
+  for (i = 0; i < AT * AK; ++i) aidx[i] = (i % 7 == 3) ? -1 : (int32_t)((i * 29 + 3) % (NB * BS));
+  kvqo_sparse_mla_attention_nvfp4_ds_mla(q, AH * 576, 576, 0, AT, AH, aidx, AK, AK, want_cache, NB, BS, BS * 352,
+                                         352, scale, want_o, AH * 512, 512, want_lse, AH);
+  void *d_q, *d_idx, *d_o, *d_lse;
+  CHECK(cudaMalloc(&d_q, sizeof q));
+  CHECK(cudaMalloc(&d_idx, sizeof aidx));
+  CHECK(cudaMalloc(&d_o, sizeof o_bits));
+  CHECK(cudaMalloc(&d_lse, sizeof lse));
+  CHECK(cudaMemcpy(d_q, q, sizeof q, cudaMemcpyHostToDevice));
+  CHECK(cudaMemcpy(d_idx, aidx, sizeof aidx, cudaMemcpyHostToDevice));
+  st = kvq_sparse_mla_attention_nvfp4_ds_mla(d_q, AH * 576, 576, AT, AH, (const int32_t*)d_idx, AK, AK,
+                                             (const uint8_t*)d_cache, NB, BS, BS * 352, 352, scale, d_o,
+                                             AH * 512, 512, (float*)d_lse, AH, (int32_t*)d_status, NULL);
+  if (st != KVQ_OK) { fprintf(stderr, "attention: %s\n", kvq_last_error_string()); return 3; }
+  CHECK(cudaMemcpy(o_bits, d_o, sizeof o_bits, cudaMemcpyDeviceToHost));
+  CHECK(cudaMemcpy(lse, d_lse, sizeof lse, cudaMemcpyDeviceToHost));
+  CHECK(cudaMemcpy(&status, d_status, sizeof status, cudaMemcpyDeviceToHost));
+  if (status != 0) { fprintf(stderr, "attention device status %d\n", status); return 5; }
+  for (int t = 0; t < AT; ++t) {
+    int n = 0;
+    double vmax = 0.0;
+    for (int k = 0; k < AK; ++k) {
+      const int32_t sl = aidx[t * AK + k];
+      if (sl < 0) continue;
+      kvqo_decode_nvfp4_ds_mla_entry(want_cache + (int64_t)sl * 352, keys + (int64_t)n * 576);
+      for (int d = 0; d < 512; ++d) vmax = fmax(vmax, fabs(keys[(int64_t)n * 576 + d]));
+      ++n;
+    }
+    for (int h = 0; h < AH; ++h) {
+      /* the bound of the Python parity tests: score error e_s, weight error eps */
+      double dmax = 0.0;
+      for (int j = 0; j < n; ++j) {
+        double acc = 0.0;
+        for (int d = 0; d < 576; ++d)
+          acc += fabs((double)kvqo_bf16_value(q[(t * AH + h) * 576 + d])) * fabs(keys[(int64_t)j * 576 + d]);
+        dmax = fmax(dmax, acc);
+      }
+      const double e_s = 576.0 * ldexp(1.0, -24) * scale * dmax;
+      const double eps = ldexp(1.0, -9) + e_s + ldexp(1.0, -20);
+      for (int d = 0; d < 512; ++d) {
+        const double w = want_o[(t * AH + h) * 512 + d];
+        const double got = kvqo_bf16_value(o_bits[(t * AH + h) * 512 + d]);
+        if (fabs(got - w) > 2 * eps / (1 - eps) * vmax + ldexp(1.0, -9) * fabs(w)) {
+          fprintf(stderr, "attention t%d h%d d%d: %g vs %g\n", t, h, d, got, w);
+          return 8;
+        }
+      }
+      if (fabs(lse[t * AH + h] - want_lse[t * AH + h]) > eps + e_s + ldexp(1.0, -22) * fabs(want_lse[t * AH + h])) {
+        fprintf(stderr, "attention lse t%d h%d: %g vs %g\n", t, h, lse[t * AH + h], want_lse[t * AH + h]);
+        return 9;
+      }
+    }
+  }
+  printf("C ABI: write (64 tokens) and gather (40 rows) match the oracle bit for bit; attention (2 x 16 x 48) "
+         "within its bound\n");
   return 0;
 }
