@@ -22,11 +22,14 @@
 //     MN-major, the V operand of P V (the CTA's 256 value columns);
 //   - one thread issues the MMAs: the partial S (128 x 64, fp32) into a TMEM
 //     double buffer, O (128 x 256, fp32) into TMEM columns [0, 256);
-//   - the softmax warps (TMEM lanes 0-127, one query row per thread) send the
-//     partial S to the peer CTA through distributed shared memory
-//     (st.async with transaction-counted mbarriers), add the peer's partial
-//     (a + b == b + a in IEEE arithmetic: both CTAs hold bit-identical
-//     scores), run the online softmax in base 2 with lazy rescaling (the
+//   - four exchange warps (one per TMEM lane quadrant) read each partial S
+//     as soon as its MMAs complete and send it to the peer CTA through
+//     distributed shared memory (st.async with transaction-counted
+//     mbarriers), so the transfer overlaps the softmax of the tile before;
+//   - the softmax warps (TMEM lanes 0-127, one query row per thread) add the
+//     peer's partial to their own (a + b == b + a in IEEE arithmetic: both
+//     CTAs hold bit-identical scores), run the online softmax in base 2 with
+//     lazy rescaling (the
 //     reference maximum moves only when a tile exceeds it by 2^8), round P
 //     to bf16 into TMEM (the A operand of P V) and rescale their O row in
 //     TMEM when the reference moved;
@@ -50,13 +53,19 @@ constexpr int kRows = 128;                                   // query rows (head
 constexpr int kTile = 64;                                    // slots per tile (N of Q K^T)
 constexpr int kBlocks = 5;                                   // 4 NoPE blocks + the RoPE block
 // Warp roles: 0-3 softmax (columns 0-31), 4-7 producers, 8-11 softmax
-// (columns 32-63), 12-15 producers, 16 MMA.  Softmax warp w reads TMEM lanes
-// 32 (w % 4) .. +31, so warps w and w + 8 share the query rows 32 (w % 4) .. +31.
+// (columns 32-63), 12-15 producers, 16 MMA, 17-20 exchange, 21 forwarder
+// (one thread).  A warp w that
+// touches TMEM reads lanes 32 (w % 4) .. +31: softmax warps w and w + 8 share
+// the query rows 32 (w % 4) .. +31, and the exchange warps cover all four
+// quadrants (17 % 4 = 1, ..., 20 % 4 = 0).
 constexpr int kSoftmaxWarps = 8;
 constexpr int kProducerWarps = 8;
+constexpr int kExchangeWarps = 4;
 constexpr int kRowsPerProducer = kTile / kProducerWarps;     // 8
-constexpr int kThreads = (kSoftmaxWarps + kProducerWarps + 1) * 32;   // + the MMA warp: 544
+constexpr int kThreads = (kSoftmaxWarps + kProducerWarps + 1 + kExchangeWarps + 1) * 32;   // 704
 constexpr int kMmaThread = 16 * 32;
+constexpr int kFirstExchangeWarp = 17;
+constexpr int kForwardWarp = 21;
 constexpr int kNvRopeOff = 256, kNvSfOff = 320;                  // nvfp4_ds_mla entry
 constexpr int kF8ScaleOff = 512, kF8RopeOff = 528;                // fp8_ds_mla entry
 constexpr float kRescaleLog2 = 8.0f;                         // lazy rescale threshold (base 2)
@@ -72,7 +81,7 @@ constexpr uint32_t kRecvOff = kKOff + kKStages * kKBytes;
 constexpr uint32_t kRecvBytes = kRows * kRecvPitch;          // one receive buffer; 2 buffers
 constexpr uint32_t kPairOff = kRecvOff + 2 * kRecvBytes;     // per-row maxima of the two column halves
 constexpr uint32_t kMiscOff = kPairOff + 2 * 2 * kRows * 4;  // [tile parity][half][row]
-constexpr uint32_t kSmemBytes = kMiscOff + 128 + 1024;       // + barriers, flags, alignment
+constexpr uint32_t kSmemBytes = kMiscOff + 256 + 1024;       // + barriers, flags, alignment
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
 static_assert(kKOff % 1024 == 0 && kKBytes % 1024 == 0, "swizzle atoms must be 1024-byte aligned");
 
@@ -170,19 +179,29 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
 
 // One bounded wait step: the thread sleeps in the barrier (up to about 1 ms,
 // woken when the phase completes) instead of spinning on issue slots.
+// Acquire at CTA scope for the barriers only this CTA arrives on, at
+// cluster scope for those that order the peer's accesses.
+template <bool kCluster>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done) : "r"(bar), "r"(parity), "r"(1000000u) : "memory");
+  if constexpr (kCluster)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done) : "r"(bar), "r"(parity), "r"(1000000u) : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done) : "r"(bar), "r"(parity), "r"(1000000u) : "memory");
   return done != 0;
 }
 
 // Bounded wait that also gives up when another role of the CTA has aborted.
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   const long long start = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait<kCluster>(bar, parity)) {
     if (*abort_flag || clock64() - start > kWaitCycles) {
       *abort_flag = 1;
       return false;
@@ -488,14 +507,17 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
   const uint32_t qr_base = base, recv_base = base + kRecvOff;
   float* s_pair = reinterpret_cast<float*>(smem + kPairOff);        // [2][2][kRows]
   const uint32_t bar0 = base + kMiscOff;
-  // k_full[3], k_empty[3], s_full[2], p_full, o_done, drain, x_full[2], x_empty[2]
+  // k_full[3], k_empty[3], s_full[2], p_full, o_done, drain, x_full[2], x_empty[2], s_read[2],
+  // recv_done[2]
   const uint32_t k_full0 = bar0, k_empty0 = bar0 + 24;
   const uint32_t s_full[2] = {bar0 + 48, bar0 + 56};
   const uint32_t p_full = bar0 + 64, o_done = bar0 + 72, drain = bar0 + 80;
   const uint32_t x_full0 = bar0 + 88;    // [b]: the peer's partial S has landed in receive buffer b
   const uint32_t x_empty0 = bar0 + 104;  // [b]: the peer has read what was sent to its buffer b
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kMiscOff + 120);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kMiscOff + 124);
+  const uint32_t s_read0 = bar0 + 120;   // [b]: the exchange warps have read partial S buffer b
+  const uint32_t recv_done0 = bar0 + 136;  // [b]: the softmax warps have read receive buffer b
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kMiscOff + 152);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kMiscOff + 156);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t token = blockIdx.x >> 1;
@@ -519,7 +541,9 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
     mbar_init(drain, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(x_full0 + 8 * b, 1);
-      mbar_init(x_empty0 + 8 * b, kSoftmaxWarps);
+      mbar_init(x_empty0 + 8 * b, 1);
+      mbar_init(s_read0 + 8 * b, kExchangeWarps);
+      mbar_init(recv_done0 + 8 * b, kSoftmaxWarps);
     }
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -581,53 +605,41 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
     const uint32_t row_lane = quad * 32u << 16;
     const uint32_t row = quad * 32 + lane;
     const uint32_t my_recv = recv_base + row * kRecvPitch + 128 * ch;   // + b * kRecvBytes
-    const uint32_t peer_recv = map_to_rank(my_recv, peer);
-    const uint32_t peer_x_full0 = map_to_rank(x_full0, peer);
-    const uint32_t peer_x_empty0 = map_to_rank(x_empty0, peer);
     const uint32_t pair_bar = 1 + quad;                      // named barrier of warps quad, quad + 8
-    // Software pipeline over the exchange: tile t + 1's partial scores are
-    // read from TMEM once tile t's weights are formed (the MMAs for t + 1 run
-    // meanwhile) and sent to the peer's other receive buffer after tile t's P
-    // is handed over.  Receive buffer b holds tiles t with t % 2 == b; it is
-    // re-armed for tile t + 2 once tile t is read and before the peer is told
-    // (x_empty) that it may send there again.
-    float cur[32], nxt[32];
-    if (n_tiles > 0) {
-      if (wait_or_abort(s_full[0], 0, s_abort)) {
-        fence_after_sync();
-        tmem_ld32(tmem + row_lane + kSCol + 32 * ch, cur);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) st_async16(peer_recv + 16 * c, cur + 4 * c, peer_x_full0);
-      }
-    }
+    // Receive buffer b holds the peer's partial scores of the tiles t with
+    // t % 2 == b; it is re-armed for tile t + 2 once tile t is read and
+    // before the forwarder tells the peer (x_empty) that it may send there
+    // again.
     // validity of this thread's 32 slots of the next tile (one per lane)
     int32_t next_slot = lane + 32 * ch < a.topk ? __ldg(idx + lane + 32 * ch) : -1;
     for (int t = 0; t < n_tiles && !*s_abort; ++t) {
       const uint32_t vm = __ballot_sync(0xffffffffu, next_slot >= 0 && next_slot < a.num_slots);
-      const bool more = t + 1 < n_tiles;
-      const uint32_t nb = (t + 1) & 1;
-      // tile t: the peer's partial scores
-      const uint32_t cb = t & 1;
-      if (!wait_or_abort(x_full0 + 8 * cb, (t >> 1) & 1, s_abort)) break;
+      const uint32_t cb = t & 1, par = (t >> 1) & 1;
+      // tile t: this CTA's partial scores, then the peer's
+      float s[32];
+      if (!wait_or_abort(s_full[cb], par, s_abort)) break;
+      fence_after_sync();
+      tmem_ld32(tmem + row_lane + kSCol + kTile * cb + 32 * ch, s);
+      if (!wait_or_abort<true>(x_full0 + 8 * cb, par, s_abort)) break;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const float4 v = ld_shared16(my_recv + cb * kRecvBytes + 16 * c);
-        cur[4 * c] += v.x;
-        cur[4 * c + 1] += v.y;
-        cur[4 * c + 2] += v.z;
-        cur[4 * c + 3] += v.w;
+        s[4 * c] += v.x;
+        s[4 * c + 1] += v.y;
+        s[4 * c + 2] += v.z;
+        s[4 * c + 3] += v.w;
       }
       if (threadIdx.x == 0 && t + 2 < n_tiles) mbar_arrive_expect_tx(x_full0 + 8 * cb, kRecvTxBytes);
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote(peer_x_empty0 + 8 * cb);
-      float* s = cur;
+      if (lane == 0) mbar_arrive(recv_done0 + 8 * cb);
       float hmax = -INFINITY;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         s[i] = (vm >> i) & 1u ? s[i] * a.scale_log2 : -INFINITY;
         hmax = fmaxf(hmax, s[i]);
       }
-      // row max over both column halves
+      // row max over both column halves (the barrier also orders both
+      // warps' reads of the scores before either writes P over them)
       s_pair[((t & 1) * 2 + ch) * kRows + row] = hmax;
       asm volatile("bar.sync %0, 64;" :: "r"(pair_bar) : "memory");
       const float tmax = fmaxf(hmax, s_pair[((t & 1) * 2 + (ch ^ 1)) * kRows + row]);
@@ -645,19 +657,11 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
         psum += bf16_lo(pk[i]) + bf16_hi(pk[i]);
       }
       l = l * alpha + psum;
-      // Tile t + 1's partial scores (their MMAs ran during this tile's work),
-      // straight on to the peer once its buffer there is free.
-      if (more) {
-        if (!wait_or_abort(s_full[nb], ((t + 1) >> 1) & 1, s_abort)) break;
-        fence_after_sync();
-        tmem_ld32(tmem + row_lane + kSCol + kTile * nb + 32 * ch, nxt);
-        if (t + 1 >= 2 && !wait_or_abort(x_empty0 + 8 * nb, ((t - 1) >> 1) & 1, s_abort)) break;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) st_async16(peer_recv + nb * kRecvBytes + 16 * c, nxt + 4 * c,
-                                               peer_x_full0 + 8 * nb);
-      }
-      // P V of the previous tile must be done before O is rescaled (it
-      // normally is by now; the wait also keeps the barrier's phases in step).
+      // The exchange warps must have read tile t's partial scores before P
+      // overwrites them (normally long done), and P V of the previous tile
+      // must be done before O is rescaled (the wait also keeps the
+      // barrier's phases in step).
+      if (!wait_or_abort(s_read0 + 8 * cb, par, s_abort)) break;
       if (t > 0 && !wait_or_abort(o_done, (t - 1) & 1, s_abort)) break;
       if (t > 0 && __any_sync(0xffffffffu, grow)) {
         fence_after_sync();
@@ -682,32 +686,37 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
         const int j = (t + 1) * kTile + 32 * ch + lane;
         next_slot = j < a.topk ? __ldg(idx + j) : -1;
       }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) cur[i] = nxt[i];
     }
     if (n_tiles > 0) wait_or_abort(o_done, (n_tiles - 1) & 1, s_abort);
   } else if (warp < 16) {
     // ---- producers: decode tiles into the K ring ----------------------------
     const int row0 = (warp < 8 ? warp - 4 : warp - 8) * kRowsPerProducer;
-    TileRegs<F> cur, nxt;
-    if (n_tiles > 0) load_tile<F>(a, tile_slot(a, idx, 0, row0, lane), lane, half, cur, bad_index);
-    int32_t slot_next = tile_slot(a, idx, 1, row0, lane);        // slots one tile ahead of the loads
-    uint32_t stage = 0, phase = 0;                               // ring position of tile t
-    // The next tile's loads are issued after each arrive: a release waits for
-    // every memory access of the thread still in flight, loads included.
-    for (int t = 0; t < n_tiles; ++t) {
+    // Two register sets alternate: a tile's loads are issued right after the
+    // tile two before it is handed over and decoded a whole tile later, so
+    // their latency hides behind the decode in between.  (Loads go after
+    // the arrive: a release waits for every access of the thread in flight.)
+    uint32_t stage = 0, phase = 0;                               // ring position of the next tile
+    int32_t slot_next = tile_slot(a, idx, 2, row0, lane);        // slots of the next tile to load
+    auto produce = [&](int t, TileRegs<F>& r) -> bool {
       // stage reuse: P V of tile t - kKStages must be done
-      if (t >= kKStages && !wait_or_abort(k_empty0 + 8 * stage, phase ^ 1, s_abort)) break;
-      store_tile<F>(base + kKOff + stage * kKBytes, row0, lane, half, cur);
+      if (t >= kKStages && !wait_or_abort(k_empty0 + 8 * stage, phase ^ 1, s_abort)) return false;
+      store_tile<F>(base + kKOff + stage * kKBytes, row0, lane, half, r);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(k_full0 + 8 * stage);
-      if (t + 1 < n_tiles) {
-        load_tile<F>(a, slot_next, lane, half, nxt, bad_index);
-        slot_next = tile_slot(a, idx, t + 2, row0, lane);
-      }
-      cur = nxt;
       if (++stage == kKStages) { stage = 0; phase ^= 1; }
+      if (t + 2 < n_tiles) {
+        load_tile<F>(a, slot_next, lane, half, r, bad_index);
+        slot_next = tile_slot(a, idx, t + 3, row0, lane);
+      }
+      return true;
+    };
+    TileRegs<F> ra, rb;
+    if (n_tiles > 0) load_tile<F>(a, tile_slot(a, idx, 0, row0, lane), lane, half, ra, bad_index);
+    if (n_tiles > 1) load_tile<F>(a, tile_slot(a, idx, 1, row0, lane), lane, half, rb, bad_index);
+    for (int t = 0; t < n_tiles; t += 2) {
+      if (!produce(t, ra)) break;
+      if (t + 1 < n_tiles && !produce(t + 1, rb)) break;
     }
   } else if (warp == kMmaThread / 32 && lane == 0) {
     // ---- MMA issue (one thread) -------------------------------------------
@@ -748,6 +757,42 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
       if (++pv_stage == kKStages) pv_stage = 0;
     }
   mma_done:;
+  } else if (warp >= kFirstExchangeWarp && warp < kFirstExchangeWarp + kExchangeWarps) {
+    // ---- exchange: each partial S to the peer as soon as it is complete ----
+    const uint32_t quad = warp & 3;
+    const uint32_t row_lane = quad * 32u << 16;
+    const uint32_t row = quad * 32 + lane;
+    const uint32_t peer_recv = map_to_rank(recv_base + row * kRecvPitch, peer);   // + b * kRecvBytes
+    const uint32_t peer_x_full0 = map_to_rank(x_full0, peer);
+    for (int u = 0; u < n_tiles; ++u) {
+      const uint32_t b = u & 1, par = (u >> 1) & 1;
+      if (!wait_or_abort(s_full[b], par, s_abort)) break;
+      fence_after_sync();
+      float v[64];
+      tmem_ld32(tmem + row_lane + kSCol + kTile * b, v);
+      tmem_ld32(tmem + row_lane + kSCol + kTile * b + 32, v + 32);
+      // released before the sends: an arrive with release semantics would
+      // wait for the stores in flight
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_read0 + 8 * b);
+      // the peer has read what this CTA sent to its buffer b two tiles ago
+      if (u >= 2 && !wait_or_abort<true>(x_empty0 + 8 * b, par ^ 1u, s_abort)) break;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        st_async16(peer_recv + b * kRecvBytes + 16 * c, v + 4 * c, peer_x_full0 + 8 * b);
+    }
+  } else if (warp == kForwardWarp && lane == 0) {
+    // ---- forwarder: "receive buffer b is free" to the peer ------------------
+    // Off the softmax warps' path: a cluster-scope release stalls the thread
+    // that issues it.  The softmax warps' local release, this thread's
+    // acquire and its cluster-scope release order their reads of the buffer
+    // before the peer's next writes into it.
+    const uint32_t peer_x_empty0 = map_to_rank(x_empty0, peer);
+    for (int t = 0; t + 2 < n_tiles; ++t) {
+      if (!wait_or_abort(recv_done0 + 8 * (t & 1), (t >> 1) & 1, s_abort)) break;
+      mbar_arrive_remote(peer_x_empty0 + 8 * (t & 1));
+    }
   }
 
   // Drain every MMA still in flight: one more commit tracks all of them.
@@ -758,7 +803,7 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
   if (any_mma) {
     if (threadIdx.x == kMmaThread) mma_commit(drain);
     const long long start = clock64();
-    while (!mbar_try_wait(drain, 0)) {     // bounded, ignores the abort flag
+    while (!mbar_try_wait<false>(drain, 0)) {     // bounded, ignores the abort flag
       if (clock64() - start > kWaitCycles) { aborted = true; break; }
     }
   }
