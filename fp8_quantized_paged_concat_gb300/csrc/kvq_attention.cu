@@ -17,15 +17,16 @@
 // which it multiplies the half [32c, 32c + 32)), so the 128 x 576 query block
 // is split 80 KB / 80 KB and the 36 K-steps of Q K^T split 18 / 18:
 //   - producers (8 warps) decode the CTA's share of each entry of a 64-slot
-//     tile to bf16 (exact: e2m1 x e4m3 products) into a double-buffered,
-//     128-byte-swizzled tile: the B operand of Q K^T (K-major) and, read
-//     MN-major, the V operand of P V (the CTA's 256 value columns);
+//     tile to bf16 (exact: e2m1 x e4m3 products) into a 3-stage ring of
+//     swizzled tiles: the B operand of Q K^T (K-major) and, read MN-major,
+//     the V operand of P V (the CTA's 256 value columns);
 //   - one thread issues the MMAs: the partial S (128 x 64, fp32) into a TMEM
 //     double buffer, O (128 x 256, fp32) into TMEM columns [0, 256);
 //   - four exchange warps (one per TMEM lane quadrant) read each partial S
-//     as soon as its MMAs complete and send it to the peer CTA through
-//     distributed shared memory (st.async with transaction-counted
-//     mbarriers), so the transfer overlaps the softmax of the tile before;
+//     as soon as its MMAs complete and stage it in shared memory; one thread
+//     hands it to the copy engine (cp.async.bulk into the peer CTA's
+//     shared memory, completed on a transaction-counted mbarrier there), so
+//     the transfer overlaps the softmax of the tile before;
 //   - the softmax warps (TMEM lanes 0-127, one query row per thread) add the
 //     peer's partial to their own (a + b == b + a in IEEE arithmetic: both
 //     CTAs hold bit-identical scores), run the online softmax in base 2 with
@@ -51,7 +52,6 @@ namespace {
 constexpr int kHalf = KVQ_MLA_NOPE_DIM / 2;                  // 256 value columns per CTA
 constexpr int kRows = 128;                                   // query rows (heads) per CTA
 constexpr int kTile = 64;                                    // slots per tile (N of Q K^T)
-constexpr int kBlocks = 5;                                   // 4 NoPE blocks + the RoPE block
 // Warp roles: 0-3 softmax (columns 0-31), 4-7 producers, 8-11 softmax
 // (columns 32-63), 12-15 producers, 16 MMA, 17-20 exchange, 21 forwarder
 // (one thread).  A warp w that
@@ -72,20 +72,23 @@ constexpr float kRescaleLog2 = 8.0f;                         // lazy rescale thr
 
 // Shared memory (offsets from a 1024-byte aligned base).
 constexpr int kKStages = 3;                                  // K tiles in flight
-constexpr uint32_t kQBlock = kRows * 128;                    // the RoPE query block: 16 KB
-constexpr uint32_t kKBlock = kTile * 128;                    // 8 KB per 64-dim block
-constexpr uint32_t kKBytes = kBlocks * kKBlock;              // 40 KB per K stage
-constexpr uint32_t kRecvPitch = 64 * 4 + 16;                 // one row of the peer's partial S
-constexpr uint32_t kKOff = kQBlock;
-constexpr uint32_t kRecvOff = kKOff + kKStages * kKBytes;
-constexpr uint32_t kRecvBytes = kRows * kRecvPitch;          // one receive buffer; 2 buffers
-constexpr uint32_t kPairOff = kRecvOff + 2 * kRecvBytes;     // per-row maxima of the two column halves
+// The CTA's 32 RoPE dimensions are 64 bytes per row: those blocks use the
+// 64-byte swizzle (atoms of 8 rows x 64 bytes), the NoPE blocks (64
+// dimensions, 128 bytes per row) the 128-byte swizzle.
+constexpr uint32_t kQRope = kRows * 64;                      // the CTA's RoPE query dims: 8 KB
+constexpr uint32_t kKBlock = kTile * 128;                    // 8 KB per 64-dim NoPE block
+constexpr uint32_t kKRope = kTile * 64;                      // the tile's RoPE dims of the CTA: 4 KB
+constexpr uint32_t kKBytes = 4 * kKBlock + kKRope;           // 36 KB per K stage
+constexpr uint32_t kSBytes = kRows * kTile * 4;              // one partial S tile (fp32): 32 KB
+constexpr uint32_t kKOff = kQRope;
+constexpr uint32_t kRecvOff = kKOff + kKStages * kKBytes;    // 2 receive buffers (the peer's partial S)
+constexpr uint32_t kSendOff = kRecvOff + 2 * kSBytes;        // this CTA's partial S, staged for the copy
+constexpr uint32_t kPairOff = kSendOff + kSBytes;            // per-row maxima of the two column halves
 constexpr uint32_t kMiscOff = kPairOff + 2 * 2 * kRows * 4;  // [tile parity][half][row]
 constexpr uint32_t kSmemBytes = kMiscOff + 256 + 1024;       // + barriers, flags, alignment
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
 static_assert(kKOff % 1024 == 0 && kKBytes % 1024 == 0, "swizzle atoms must be 1024-byte aligned");
-
-constexpr uint32_t kRecvTxBytes = kRows * 64 * 4;            // one partial S: 32 KB
+static_assert(kRecvOff % 16 == 0 && kSendOff % 16 == 0, "bulk copies move 16-byte aligned data");
 
 // TMEM columns: O [0, 256), the CTA's 256 NoPE query dimensions as bf16
 // pairs [256, 384) (the A operand of the NoPE K-steps), partial S double
@@ -108,14 +111,21 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// Shared-memory matrix descriptor: 128-byte swizzle, 1024-byte aligned atoms
-// of 8 rows x 128 bytes.  lbo / sbo in bytes.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptor: lbo / sbo in bytes; swizzle mode 2 =
+// 128-byte (1024-byte atoms of 8 rows x 128 bytes), 4 = 64-byte (512-byte
+// atoms of 8 rows x 64 bytes).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t mode) {
   return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) |
          (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) |
          (uint64_t{1} << 46) |                 // descriptor version of tcgen05
-         (uint64_t{2} << 61);                  // 128-byte swizzle
+         (static_cast<uint64_t>(mode) << 61);
+}
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return smem_desc(addr, lbo, sbo, 2);
+}
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t addr) {
+  return smem_desc(addr, 16, 512, 4);
 }
 
 // Instruction descriptor of kind::f16: bf16 A and B, fp32 D, A K-major.
@@ -228,13 +238,12 @@ __device__ __forceinline__ void cluster_sync() {
                ::: "memory");
 }
 
-// 16 bytes into the peer's shared memory; completes 16 bytes on its mbarrier.
-__device__ __forceinline__ void st_async16(uint32_t cluster_addr, const float* v, uint32_t cluster_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
-      :: "r"(cluster_addr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
-         "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(cluster_bar)
-      : "memory");
+// `bytes` (a multiple of 16) from this CTA's shared memory into the peer's
+// (address from mapa); the copy engine completes them on the peer's mbarrier.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                                  uint32_t cluster_bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(dst_cluster), "r"(src), "r"(bytes), "r"(cluster_bar) : "memory");
 }
 
 // 32 consecutive fp32 TMEM columns of this warp's 32 lanes (one per thread).
@@ -289,6 +298,19 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
 // 128-byte-swizzled block: chunks are permuted by XOR with row % 8.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
   return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+// The same for 64-byte rows (chunk 0..3) under the 64-byte swizzle: the
+// chunk index is XORed with address bits 7-8, i.e. with (row / 2) % 4.
+__device__ __forceinline__ uint32_t sw64_offset(uint32_t row, uint32_t chunk) {
+  return row * 64u + ((chunk ^ ((row >> 1) & 3u)) << 4);
+}
+
+// A partial S tile (128 rows x 64 fp32 = 256 bytes per row) in a receive or
+// send buffer: 16-byte chunk c of row r moves to chunk c ^ (r % 16), so that
+// 32 threads reading the same chunk of 32 rows spread over all banks.
+__device__ __forceinline__ uint32_t s_offset(uint32_t row, uint32_t chunk) {
+  return row * 256u + ((chunk ^ (row & 15u)) << 4);
 }
 
 __device__ __forceinline__ void st_shared16(uint32_t addr, const uint4& v) {
@@ -493,7 +515,7 @@ __device__ __forceinline__ void store_tile(uint32_t kbuf, int row0, int lane, ui
       else
         v = e.rope;                      // bf16 as stored
     }
-    st_shared16(kbuf + 4 * kKBlock + sw128_offset(r, 4 * half + k), v);
+    st_shared16(kbuf + 4 * kKBlock + sw64_offset(r, k), v);
   }
 }
 
@@ -508,7 +530,7 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
   float* s_pair = reinterpret_cast<float*>(smem + kPairOff);        // [2][2][kRows]
   const uint32_t bar0 = base + kMiscOff;
   // k_full[3], k_empty[3], s_full[2], p_full, o_done, drain, x_full[2], x_empty[2], s_read[2],
-  // recv_done[2]
+  // recv_done[2], send_free, staged
   const uint32_t k_full0 = bar0, k_empty0 = bar0 + 24;
   const uint32_t s_full[2] = {bar0 + 48, bar0 + 56};
   const uint32_t p_full = bar0 + 64, o_done = bar0 + 72, drain = bar0 + 80;
@@ -516,8 +538,10 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
   const uint32_t x_empty0 = bar0 + 104;  // [b]: the peer has read what was sent to its buffer b
   const uint32_t s_read0 = bar0 + 120;   // [b]: the exchange warps have read partial S buffer b
   const uint32_t recv_done0 = bar0 + 136;  // [b]: the softmax warps have read receive buffer b
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kMiscOff + 152);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kMiscOff + 156);
+  const uint32_t send_free = bar0 + 152;   // the last copy out of the send buffer has landed
+  const uint32_t staged = bar0 + 160;      // the exchange warps have filled the send buffer
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kMiscOff + 168);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kMiscOff + 172);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t token = blockIdx.x >> 1;
@@ -545,23 +569,25 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
       mbar_init(s_read0 + 8 * b, kExchangeWarps);
       mbar_init(recv_done0 + 8 * b, kSoftmaxWarps);
     }
+    mbar_init(send_free, 1);
+    mbar_init(staged, kExchangeWarps);
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     // Receive buffers 0 and 1 expect tiles 0 and 1 (32 KB each) before the
     // cluster barrier below, i.e. before the peer can send anything.
     const int n = (a.topk + kTile - 1) / kTile;
-    for (int b = 0; b < 2 && b < n; ++b) mbar_arrive_expect_tx(x_full0 + 8 * b, kRecvTxBytes);
+    for (int b = 0; b < 2 && b < n; ++b) mbar_arrive_expect_tx(x_full0 + 8 * b, kSBytes);
   }
 
-  // The CTA's 32 RoPE query dimensions -> chunks 4 half .. 4 half + 3 of a
-  // swizzled K-major block (rows >= num_heads are zero).
+  // The CTA's 32 RoPE query dimensions -> a 64-byte-swizzled K-major block
+  // (rows >= num_heads are zero).
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + token * a.q_stride_t;
   for (int i = threadIdx.x; i < kRows * 4; i += kThreads) {
     const int row = i >> 2, c = i & 3;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (row < a.num_heads)
       v = __ldg(reinterpret_cast<const uint4*>(q + row * a.q_stride_h + KVQ_MLA_NOPE_DIM + 32 * half + 8 * c));
-    st_shared16(qr_base + sw128_offset(row, 4 * half + c), v);
+    st_shared16(qr_base + sw64_offset(row, c), v);
   }
   fence_async_smem();
   fence_before_sync();
@@ -604,7 +630,6 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
     const uint32_t quad = warp & 3, ch = warp >> 3;         // column half: 0 = cols 0-31
     const uint32_t row_lane = quad * 32u << 16;
     const uint32_t row = quad * 32 + lane;
-    const uint32_t my_recv = recv_base + row * kRecvPitch + 128 * ch;   // + b * kRecvBytes
     const uint32_t pair_bar = 1 + quad;                      // named barrier of warps quad, quad + 8
     // Receive buffer b holds the peer's partial scores of the tiles t with
     // t % 2 == b; it is re-armed for tile t + 2 once tile t is read and
@@ -623,13 +648,13 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
       if (!wait_or_abort<true>(x_full0 + 8 * cb, par, s_abort)) break;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const float4 v = ld_shared16(my_recv + cb * kRecvBytes + 16 * c);
+        const float4 v = ld_shared16(recv_base + cb * kSBytes + s_offset(row, 8 * ch + c));
         s[4 * c] += v.x;
         s[4 * c + 1] += v.y;
         s[4 * c + 2] += v.z;
         s[4 * c + 3] += v.w;
       }
-      if (threadIdx.x == 0 && t + 2 < n_tiles) mbar_arrive_expect_tx(x_full0 + 8 * cb, kRecvTxBytes);
+      if (threadIdx.x == 0 && t + 2 < n_tiles) mbar_arrive_expect_tx(x_full0 + 8 * cb, kSBytes);
       __syncwarp();
       if (lane == 0) mbar_arrive(recv_done0 + 8 * cb);
       float hmax = -INFINITY;
@@ -736,10 +761,10 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
         for (int k = 0; k < 16; ++k)
           mma_bf16_ta(d, tmem + kQCol + 8 * k, kdesc + (((k >> 2) * kKBlock + (k & 3) * 32) >> 4), kIdescQK,
                       k > 0);
-        const uint64_t qrdesc = sw128_desc(qr_base + 64 * half, 16, 1024);
+        const uint64_t qrdesc = sw64_desc(qr_base);
+        const uint64_t krdesc = sw64_desc(base + kKOff + qk_stage * kKBytes + 4 * kKBlock);
 #pragma unroll
-        for (int k = 0; k < 2; ++k)
-          mma_bf16(d, qrdesc + 2 * k, kdesc + ((4 * kKBlock + 64 * half + 32 * k) >> 4), kIdescQK, 1u);
+        for (int k = 0; k < 2; ++k) mma_bf16(d, qrdesc + 2 * k, krdesc + 2 * k, kIdescQK, 1u);
         mma_commit(s_full[u & 1]);
         mma_issued = 1;
         if (++qk_stage == kKStages) { qk_stage = 0; qk_phase ^= 1; }
@@ -759,39 +784,68 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
   mma_done:;
   } else if (warp >= kFirstExchangeWarp && warp < kFirstExchangeWarp + kExchangeWarps) {
     // ---- exchange: each partial S to the peer as soon as it is complete ----
+    // Each warp stages its 32 rows in the send buffer; one thread then hands
+    // the whole tile to the copy engine, which moves it into the peer's
+    // receive buffer without holding up this SM's load / store pipeline.
+    // Every decision to stop is taken by the whole warp (the TMEM loads are
+    // warp-collective), and the warps meet only on bounded mbarrier waits.
     const uint32_t quad = warp & 3;
     const uint32_t row_lane = quad * 32u << 16;
     const uint32_t row = quad * 32 + lane;
-    const uint32_t peer_recv = map_to_rank(recv_base + row * kRecvPitch, peer);   // + b * kRecvBytes
+    const uint32_t send = base + kSendOff;
+    const bool issuer = warp == kFirstExchangeWarp && lane == 0;
+    const uint32_t peer_recv0 = map_to_rank(recv_base, peer);
     const uint32_t peer_x_full0 = map_to_rank(x_full0, peer);
     for (int u = 0; u < n_tiles; ++u) {
       const uint32_t b = u & 1, par = (u >> 1) & 1;
-      if (!wait_or_abort(s_full[b], par, s_abort)) break;
+      if (!__all_sync(0xffffffffu, wait_or_abort(s_full[b], par, s_abort))) break;
       fence_after_sync();
       float v[64];
       tmem_ld32(tmem + row_lane + kSCol + kTile * b, v);
       tmem_ld32(tmem + row_lane + kSCol + kTile * b + 32, v + 32);
-      // released before the sends: an arrive with release semantics would
-      // wait for the stores in flight
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_read0 + 8 * b);
-      // the peer has read what this CTA sent to its buffer b two tiles ago
-      if (u >= 2 && !wait_or_abort<true>(x_empty0 + 8 * b, par ^ 1u, s_abort)) break;
+      // the copy of tile u - 1 has landed in the peer: the send buffer is free
+      if (u >= 1 && !__all_sync(0xffffffffu, wait_or_abort<true>(send_free, (u - 1) & 1, s_abort))) break;
 #pragma unroll
       for (int c = 0; c < 16; ++c)
-        st_async16(peer_recv + b * kRecvBytes + 16 * c, v + 4 * c, peer_x_full0 + 8 * b);
+        st_shared16(send + s_offset(row, c), make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
+                                                       __float_as_uint(v[4 * c + 2]),
+                                                       __float_as_uint(v[4 * c + 3])));
+      fence_async_smem();                // the stores, visible to the copy engine
+      __syncwarp();
+      if (lane == 0) mbar_arrive(staged);
+      if (warp == kFirstExchangeWarp) {
+        bool ok = true;
+        if (issuer) {
+          // all four warps have staged; the peer has read (and re-armed) its
+          // buffer b, which held tile u - 2
+          ok = wait_or_abort(staged, u & 1, s_abort) &&
+               (u < 2 || wait_or_abort<true>(x_empty0 + 8 * b, par ^ 1u, s_abort));
+          if (ok) bulk_copy_to_peer(peer_recv0 + b * kSBytes, send, kSBytes, peer_x_full0 + 8 * b);
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
     }
   } else if (warp == kForwardWarp && lane == 0) {
-    // ---- forwarder: "receive buffer b is free" to the peer ------------------
+    // ---- forwarder: the peer's copies and this CTA's reads, to the peer -----
+    // For tile t: once the peer's copy has landed here, the peer's send
+    // buffer is free again (send_free); once the softmax warps have read
+    // receive buffer t % 2, the peer may copy tile t + 2 into it (x_empty).
     // Off the softmax warps' path: a cluster-scope release stalls the thread
     // that issues it.  The softmax warps' local release, this thread's
     // acquire and its cluster-scope release order their reads of the buffer
     // before the peer's next writes into it.
     const uint32_t peer_x_empty0 = map_to_rank(x_empty0, peer);
-    for (int t = 0; t + 2 < n_tiles; ++t) {
-      if (!wait_or_abort(recv_done0 + 8 * (t & 1), (t >> 1) & 1, s_abort)) break;
-      mbar_arrive_remote(peer_x_empty0 + 8 * (t & 1));
+    const uint32_t peer_send_free = map_to_rank(send_free, peer);
+    for (int t = 0; t + 1 < n_tiles; ++t) {
+      if (!wait_or_abort<true>(x_full0 + 8 * (t & 1), (t >> 1) & 1, s_abort)) break;
+      mbar_arrive_remote(peer_send_free);
+      if (t + 2 < n_tiles) {
+        if (!wait_or_abort(recv_done0 + 8 * (t & 1), (t >> 1) & 1, s_abort)) break;
+        mbar_arrive_remote(peer_x_empty0 + 8 * (t & 1));
+      }
     }
   }
 
