@@ -530,7 +530,7 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
   float* s_pair = reinterpret_cast<float*>(smem + kPairOff);        // [2][2][kRows]
   const uint32_t bar0 = base + kMiscOff;
   // k_full[3], k_empty[3], s_full[2], p_full, o_done, drain, x_full[2], x_empty[2], s_read[2],
-  // recv_done[2], send_free, staged
+  // recv_done[2], send_free
   const uint32_t k_full0 = bar0, k_empty0 = bar0 + 24;
   const uint32_t s_full[2] = {bar0 + 48, bar0 + 56};
   const uint32_t p_full = bar0 + 64, o_done = bar0 + 72, drain = bar0 + 80;
@@ -539,7 +539,6 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
   const uint32_t s_read0 = bar0 + 120;   // [b]: the exchange warps have read partial S buffer b
   const uint32_t recv_done0 = bar0 + 136;  // [b]: the softmax warps have read receive buffer b
   const uint32_t send_free = bar0 + 152;   // the last copy out of the send buffer has landed
-  const uint32_t staged = bar0 + 160;      // the exchange warps have filled the send buffer
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kMiscOff + 168);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kMiscOff + 172);
 
@@ -570,7 +569,6 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
       mbar_init(recv_done0 + 8 * b, kSoftmaxWarps);
     }
     mbar_init(send_free, 1);
-    mbar_init(staged, kExchangeWarps);
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     // Receive buffers 0 and 1 expect tiles 0 and 1 (32 KB each) before the
@@ -784,16 +782,16 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
   mma_done:;
   } else if (warp >= kFirstExchangeWarp && warp < kFirstExchangeWarp + kExchangeWarps) {
     // ---- exchange: each partial S to the peer as soon as it is complete ----
-    // Each warp stages its 32 rows in the send buffer; one thread then hands
-    // the whole tile to the copy engine, which moves it into the peer's
-    // receive buffer without holding up this SM's load / store pipeline.
+    // Each warp stages its 32 rows (8 KB, contiguous) in the send buffer and
+    // hands them to the copy engine, which moves them into the peer's
+    // receive buffer without holding up this SM's load / store pipeline; the
+    // four copies of a tile complete its 32 KB on the peer's x_full.
     // Every decision to stop is taken by the whole warp (the TMEM loads are
     // warp-collective), and the warps meet only on bounded mbarrier waits.
     const uint32_t quad = warp & 3;
     const uint32_t row_lane = quad * 32u << 16;
     const uint32_t row = quad * 32 + lane;
     const uint32_t send = base + kSendOff;
-    const bool issuer = warp == kFirstExchangeWarp && lane == 0;
     const uint32_t peer_recv0 = map_to_rank(recv_base, peer);
     const uint32_t peer_x_full0 = map_to_rank(x_full0, peer);
     for (int u = 0; u < n_tiles; ++u) {
@@ -815,18 +813,14 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
                                                        __float_as_uint(v[4 * c + 3])));
       fence_async_smem();                // the stores, visible to the copy engine
       __syncwarp();
-      if (lane == 0) mbar_arrive(staged);
-      if (warp == kFirstExchangeWarp) {
-        bool ok = true;
-        if (issuer) {
-          // all four warps have staged; the peer has read (and re-armed) its
-          // buffer b, which held tile u - 2
-          ok = wait_or_abort(staged, u & 1, s_abort) &&
-               (u < 2 || wait_or_abort<true>(x_empty0 + 8 * b, par ^ 1u, s_abort));
-          if (ok) bulk_copy_to_peer(peer_recv0 + b * kSBytes, send, kSBytes, peer_x_full0 + 8 * b);
-        }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      bool ok = true;
+      if (lane == 0) {
+        // the peer has read (and re-armed) its buffer b, which held tile u - 2
+        ok = u < 2 || wait_or_abort<true>(x_empty0 + 8 * b, par ^ 1u, s_abort);
+        const uint32_t part = quad * 32 * 256;   // this warp's rows
+        if (ok) bulk_copy_to_peer(peer_recv0 + b * kSBytes + part, send + part, kSBytes / 4, peer_x_full0 + 8 * b);
       }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
     }
   } else if (warp == kForwardWarp && lane == 0) {
     // ---- forwarder: the peer's copies and this CTA's reads, to the peer -----
