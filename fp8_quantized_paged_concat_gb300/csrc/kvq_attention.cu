@@ -714,12 +714,13 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
   } else if (warp < 16) {
     // ---- producers: decode tiles into the K ring ----------------------------
     const int row0 = (warp < 8 ? warp - 4 : warp - 8) * kRowsPerProducer;
-    // Two register sets alternate: a tile's loads are issued right after the
-    // tile two before it is handed over and decoded a whole tile later, so
-    // their latency hides behind the decode in between.  (Loads go after
-    // the arrive: a release waits for every access of the thread in flight.)
+    // A tile's loads are issued right after the tile before it is handed
+    // over, and their latency hides behind the wait for the next free
+    // stage.  (Loads go after the arrive: a release waits for every access
+    // of the thread in flight.  Loading two tiles ahead, in a second
+    // register set, measured slower: the producers are short of registers.)
     uint32_t stage = 0, phase = 0;                               // ring position of the next tile
-    int32_t slot_next = tile_slot(a, idx, 2, row0, lane);        // slots of the next tile to load
+    int32_t slot_next = tile_slot(a, idx, 1, row0, lane);        // slots of the next tile to load
     auto produce = [&](int t, TileRegs<F>& r) -> bool {
       // stage reuse: P V of tile t - kKStages must be done
       if (t >= kKStages && !wait_or_abort(k_empty0 + 8 * stage, phase ^ 1, s_abort)) return false;
@@ -728,19 +729,16 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
       __syncwarp();
       if (lane == 0) mbar_arrive(k_full0 + 8 * stage);
       if (++stage == kKStages) { stage = 0; phase ^= 1; }
-      if (t + 2 < n_tiles) {
+      if (t + 1 < n_tiles) {
         load_tile<F>(a, slot_next, lane, half, r, bad_index);
-        slot_next = tile_slot(a, idx, t + 3, row0, lane);
+        slot_next = tile_slot(a, idx, t + 2, row0, lane);
       }
       return true;
     };
-    TileRegs<F> ra, rb;
-    if (n_tiles > 0) load_tile<F>(a, tile_slot(a, idx, 0, row0, lane), lane, half, ra, bad_index);
-    if (n_tiles > 1) load_tile<F>(a, tile_slot(a, idx, 1, row0, lane), lane, half, rb, bad_index);
-    for (int t = 0; t < n_tiles; t += 2) {
-      if (!produce(t, ra)) break;
-      if (t + 1 < n_tiles && !produce(t + 1, rb)) break;
-    }
+    TileRegs<F> regs;
+    if (n_tiles > 0) load_tile<F>(a, tile_slot(a, idx, 0, row0, lane), lane, half, regs, bad_index);
+    for (int t = 0; t < n_tiles; ++t)
+      if (!produce(t, regs)) break;
   } else if (warp == kMmaThread / 32 && lane == 0) {
     // ---- MMA issue (one thread) -------------------------------------------
     constexpr uint32_t kIdescQK = idesc_bf16(kRows, kTile, false);
