@@ -404,11 +404,17 @@ __device__ __forceinline__ uint4 e2m1x8_lut(uint32_t x, const GroupTable& t) {
 // same): 352-byte nvfp4_ds_mla and 656-byte fp8_ds_mla.
 enum class Entry { kNvfp4, kFp8 };
 
-// Producer p (rows 8p .. 8p+7 of the tile): lane `lane` handles row
-// 8p + lane / 4 and, with k = lane % 4, the CTA's NoPE values 64k .. 64k+63
-// (four 16-value groups: one 64-dim block of the tile) and RoPE values
-// 32 half + 8k .. +7.  One entry address per lane, and the four lanes of a
-// row read its NoPE half, scales and RoPE half as contiguous runs.
+// Producer p handles rows 8p .. 8p+7 of the tile; the lanes split them by
+// format (each mapping measured fastest for its format):
+//  - nvfp4: lane `lane` takes row 8p + lane / 4 and, with k = lane % 4, the
+//    CTA's NoPE values 64k .. 64k+63 (four 16-value groups, one 64-dim block
+//    of the tile: 32 contiguous code bytes and 4 scale bytes), one entry
+//    address per lane;
+//  - fp8: lane `lane` takes the 16-value piece g = lane % 16 (local values
+//    16g .. 16g+15) of rows 8p + lane / 16 + 2i (i < 4): every 16-byte load
+//    covers 256 contiguous bytes of two rows;
+//  - both: RoPE piece k = lane % 4 (values 32 half + 8k .. +7) of row
+//    8p + lane / 4.
 template <Entry F> struct TileRegs;
 template <> struct TileRegs<Entry::kNvfp4> {
   uint4 nib[2];                          // 64 e2m1 codes (groups 4k .. 4k+3)
@@ -417,10 +423,10 @@ template <> struct TileRegs<Entry::kNvfp4> {
   uint32_t valid;
 };
 template <> struct TileRegs<Entry::kFp8> {
-  uint4 code[4];                         // 64 e4m3 codes
-  float sc;                              // their 128-value tile's fp32 scale
+  uint4 code[4];                         // 16 e4m3 codes of row i
+  float sc[4];                           // their 128-value tile's fp32 scale
   uint4 rope;                            // 8 bf16 RoPE values
-  uint32_t valid;
+  uint32_t valid;                        // bits 0-3: NoPE rows, bit 4: RoPE row
 };
 
 __device__ __forceinline__ const uint8_t* entry_of(const AttentionArgs& a, int32_t slot) {
@@ -429,10 +435,12 @@ __device__ __forceinline__ const uint8_t* entry_of(const AttentionArgs& a, int32
   return a.cache + static_cast<int64_t>(blk) * a.block_stride + static_cast<int64_t>(off) * a.entry_stride;
 }
 
-// Slot of this lane's row row0 + lane / 4 of a tile (-1 past top-k).
+// The slot this lane reads for its mapping: row row0 + lane / 4 (nvfp4) or
+// row0 + lane % 8 (fp8, passed on by shuffles) of a tile; -1 past top-k.
+template <Entry F>
 __device__ __forceinline__ int32_t tile_slot(const AttentionArgs& a, const int32_t* idx, int tile, int row0,
                                              int lane) {
-  const int j = tile * kTile + row0 + (lane >> 2);
+  const int j = tile * kTile + row0 + (F == Entry::kNvfp4 ? lane >> 2 : lane & 7);
   return j < a.topk ? __ldg(idx + j) : -1;
 }
 
@@ -442,22 +450,34 @@ template <Entry F>
 __device__ __forceinline__ void load_tile(const AttentionArgs& a, int32_t mine, int lane, uint32_t half,
                                           TileRegs<F>& e, bool& bad_index) {
   if (mine >= a.num_slots) bad_index = true;
-  e.valid = mine >= 0 && mine < a.num_slots;
-  if (!e.valid) return;
   const int k = lane & 3;
-  const uint8_t* p = entry_of(a, mine);
   if constexpr (F == Entry::kNvfp4) {
+    e.valid = mine >= 0 && mine < a.num_slots;
+    if (!e.valid) return;
+    const uint8_t* p = entry_of(a, mine);
     const uint4* c = reinterpret_cast<const uint4*>(p + 128 * half + 32 * k);
     e.nib[0] = __ldg(c);
     e.nib[1] = __ldg(c + 1);
     e.sf = __ldg(reinterpret_cast<const uint32_t*>(p + kNvSfOff + 16 * half + 4 * k));
     e.rope = __ldg(reinterpret_cast<const uint2*>(p + kNvRopeOff + 32 * half + 8 * k));
   } else {
-    const uint4* c = reinterpret_cast<const uint4*>(p + kHalf * half + 64 * k);
+    e.valid = 0;
+    const int g = lane & 15;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) e.code[j] = __ldg(c + j);
-    e.sc = __ldg(reinterpret_cast<const float*>(p + kF8ScaleOff) + 2 * half + (k >> 1));
-    e.rope = __ldg(reinterpret_cast<const uint4*>(p + kF8RopeOff + 64 * half + 16 * k));
+    for (int i = 0; i < 4; ++i) {
+      const int32_t slot = __shfl_sync(0xffffffffu, mine, (lane >> 4) + 2 * i);
+      if (slot >= 0 && slot < a.num_slots) {
+        const uint8_t* p = entry_of(a, slot);
+        e.valid |= 1u << i;
+        e.code[i] = __ldg(reinterpret_cast<const uint4*>(p + kHalf * half + 16 * g));
+        e.sc[i] = __ldg(reinterpret_cast<const float*>(p + kF8ScaleOff) + 2 * half + (g >> 3));
+      }
+    }
+    const int32_t slot = __shfl_sync(0xffffffffu, mine, lane >> 2);
+    if (slot >= 0 && slot < a.num_slots) {
+      e.valid |= 16u;
+      e.rope = __ldg(reinterpret_cast<const uint4*>(entry_of(a, slot) + kF8RopeOff + 64 * half + 16 * k));
+    }
   }
 }
 
@@ -478,32 +498,38 @@ __device__ __forceinline__ void e4m3x16_scaled(const uint4& c, float s, uint4& l
 template <Entry F>
 __device__ __forceinline__ void store_tile(uint32_t kbuf, int row0, int lane, const TileRegs<F>& e) {
   const int k = lane & 3;
-  const uint32_t r = row0 + (lane >> 2);
-  const uint32_t blk = kbuf + k * kKBlock;             // this lane's 64 dims: a whole block row
+  const uint32_t rr = row0 + (lane >> 2);              // the RoPE row (and the nvfp4 row)
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if constexpr (F == Entry::kNvfp4) {
+    const uint32_t blk = kbuf + k * kKBlock;           // this lane's 64 dims: a whole block row
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {                        // group 4k + j -> chunks 2j, 2j + 1
-    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-    if (e.valid) {
-      if constexpr (F == Entry::kNvfp4) {
+    for (int j = 0; j < 4; ++j) {                      // group 4k + j -> chunks 2j, 2j + 1
+      uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+      if (e.valid) {
         const GroupTable t = group_table((e.sf >> (8 * j)) & 0xffu);
         const uint4& c = e.nib[j >> 1];
         lo = e2m1x8_lut((j & 1) ? c.z : c.x, t);
         hi = e2m1x8_lut((j & 1) ? c.w : c.y, t);
-      } else {
-        e4m3x16_scaled(e.code[j], e.sc, lo, hi);
       }
+      st_shared16(blk + sw128_offset(rr, 2 * j), lo);
+      st_shared16(blk + sw128_offset(rr, 2 * j + 1), hi);
     }
-    st_shared16(blk + sw128_offset(r, 2 * j), lo);
-    st_shared16(blk + sw128_offset(r, 2 * j + 1), hi);
+    if (e.valid) v = e4m3x8_bf16(e.rope);
+  } else {
+    const int g = lane & 15;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t r = row0 + (lane >> 4) + 2 * i;
+      uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+      if (e.valid & (1u << i)) e4m3x16_scaled(e.code[i], e.sc[i], lo, hi);
+      // piece g: local dims 16g .. 16g+15 = block g/4, chunks 2(g%4) + {0, 1}
+      const uint32_t blk = kbuf + (g >> 2) * kKBlock;
+      st_shared16(blk + sw128_offset(r, 2 * (g & 3)), lo);
+      st_shared16(blk + sw128_offset(r, 2 * (g & 3) + 1), hi);
+    }
+    if (e.valid & 16u) v = e.rope;       // bf16 as stored
   }
-  uint4 v = make_uint4(0, 0, 0, 0);
-  if (e.valid) {
-    if constexpr (F == Entry::kNvfp4)
-      v = e4m3x8_bf16(e.rope);
-    else
-      v = e.rope;                        // bf16 as stored
-  }
-  st_shared16(kbuf + 4 * kKBlock + sw64_offset(r, k), v);
+  st_shared16(kbuf + 4 * kKBlock + sw64_offset(rr, k), v);
 }
 
 template <Entry F>
@@ -707,7 +733,7 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
     // of the thread in flight.  Loading two tiles ahead, in a second
     // register set, measured slower: the producers are short of registers.)
     uint32_t stage = 0, phase = 0;                               // ring position of the next tile
-    int32_t slot_next = tile_slot(a, idx, 1, row0, lane);        // slots of the next tile to load
+    int32_t slot_next = tile_slot<F>(a, idx, 1, row0, lane);        // slots of the next tile to load
     auto produce = [&](int t, TileRegs<F>& r) -> bool {
       // stage reuse: P V of tile t - kKStages must be done
       if (t >= kKStages && !wait_or_abort(k_empty0 + 8 * stage, phase ^ 1, s_abort)) return false;
@@ -718,12 +744,12 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
       if (++stage == kKStages) { stage = 0; phase ^= 1; }
       if (t + 1 < n_tiles) {
         load_tile<F>(a, slot_next, lane, half, r, bad_index);
-        slot_next = tile_slot(a, idx, t + 2, row0, lane);
+        slot_next = tile_slot<F>(a, idx, t + 2, row0, lane);
       }
       return true;
     };
     TileRegs<F> regs;
-    if (n_tiles > 0) load_tile<F>(a, tile_slot(a, idx, 0, row0, lane), lane, half, regs, bad_index);
+    if (n_tiles > 0) load_tile<F>(a, tile_slot<F>(a, idx, 0, row0, lane), lane, half, regs, bad_index);
     for (int t = 0; t < n_tiles; ++t)
       if (!produce(t, regs)) break;
   } else if (warp == kMmaThread / 32 && lane == 0) {
