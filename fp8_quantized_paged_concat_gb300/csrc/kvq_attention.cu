@@ -23,17 +23,18 @@
 //   - one thread issues the MMAs: the partial S (128 x 64, fp32) into a TMEM
 //     double buffer, O (128 x 256, fp32) into TMEM columns [0, 256);
 //   - four exchange warps (one per TMEM lane quadrant) read each partial S
-//     as soon as its MMAs complete and stage it in shared memory; one thread
-//     hands it to the copy engine (cp.async.bulk into the peer CTA's
-//     shared memory, completed on a transaction-counted mbarrier there), so
-//     the transfer overlaps the softmax of the tile before;
+//     as soon as its MMAs complete, stage their 32 rows in shared memory and
+//     hand them to the copy engine (cp.async.bulk into the peer CTA's shared
+//     memory, completed on a transaction-counted mbarrier there), so the
+//     transfer overlaps the softmax of the tile before; a forwarder thread
+//     tells the peer when its copies have landed and when the receive
+//     buffers have been read;
 //   - the softmax warps (TMEM lanes 0-127, one query row per thread) add the
 //     peer's partial to their own (a + b == b + a in IEEE arithmetic: both
 //     CTAs hold bit-identical scores), run the online softmax in base 2 with
-//     lazy rescaling (the
-//     reference maximum moves only when a tile exceeds it by 2^8), round P
-//     to bf16 into TMEM (the A operand of P V) and rescale their O row in
-//     TMEM when the reference moved;
+//     lazy rescaling (the reference maximum moves only when a tile exceeds
+//     it by 2^8), round P to bf16 into TMEM (the A operand of P V) and
+//     rescale their O row in TMEM when the reference moved;
 //   - the denominator sums the bf16-rounded P, the weights the tensor cores
 //     multiply.
 //
@@ -54,10 +55,9 @@ constexpr int kRows = 128;                                   // query rows (head
 constexpr int kTile = 64;                                    // slots per tile (N of Q K^T)
 // Warp roles: 0-3 softmax (columns 0-31), 4-7 producers, 8-11 softmax
 // (columns 32-63), 12-15 producers, 16 MMA, 17-20 exchange, 21 forwarder
-// (one thread).  A warp w that
-// touches TMEM reads lanes 32 (w % 4) .. +31: softmax warps w and w + 8 share
-// the query rows 32 (w % 4) .. +31, and the exchange warps cover all four
-// quadrants (17 % 4 = 1, ..., 20 % 4 = 0).
+// (one thread).  A warp w that touches TMEM reads lanes 32 (w % 4) .. +31:
+// softmax warps w and w + 8 share the query rows 32 (w % 4) .. +31, and the
+// exchange warps cover all four quadrants (17 % 4 = 1, ..., 20 % 4 = 0).
 constexpr int kSoftmaxWarps = 8;
 constexpr int kProducerWarps = 8;
 constexpr int kExchangeWarps = 4;
