@@ -619,10 +619,10 @@ class CpuSample:
 
 def cpu_baseline(threads):
     """The oracle on all host cores over the bounded sample, repeated until
-    about 1.5 s of wall time (at most 8 passes)."""
+    about 10 s of wall time (at most 64 passes)."""
     s = CpuSample(threads)
     total, passes = 0.0, 0
-    while passes < 8 and (passes == 0 or total < 1.5):
+    while passes < 64 and (passes == 0 or total < 10.0):
         total += sum(s.step().values())
         passes += 1
     return {"value": round(passes * s.bytes_per_step() / total / 1e9, 3), "unit": "GB/s",
