@@ -334,6 +334,23 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Two fp32 operations in one instruction (each rounded to nearest even, as
+// the scalar ones).
+__device__ __forceinline__ float2 fmul2(float2 x, float2 y) {
+  float2 r;
+  asm("{\n\t.reg .b64 a, b, c;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mul.rn.f32x2 c, a, b;\n\tmov.b64 {%0, %1}, c;\n\t}"
+      : "=f"(r.x), "=f"(r.y) : "f"(x.x), "f"(x.y), "f"(y.x), "f"(y.y));
+  return r;
+}
+__device__ __forceinline__ float2 fadd2(float2 x, float2 y) {
+  float2 r;
+  asm("{\n\t.reg .b64 a, b, c;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "add.rn.f32x2 c, a, b;\n\tmov.b64 {%0, %1}, c;\n\t}"
+      : "=f"(r.x), "=f"(r.y) : "f"(x.x), "f"(x.y), "f"(y.x), "f"(y.y));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -488,8 +505,8 @@ __device__ __forceinline__ void e4m3x16_scaled(const uint4& c, float s, uint4& l
   uint32_t o[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float2 v = __half22float2(e4m3x2_to_half2(w[i >> 1] >> (16 * (i & 1))));
-    o[i] = pack_bf16x2(__fmul_rn(v.x, s), __fmul_rn(v.y, s));
+    const float2 v = fmul2(__half22float2(e4m3x2_to_half2(w[i >> 1] >> (16 * (i & 1)))), make_float2(s, s));
+    o[i] = pack_bf16x2(v.x, v.y);
   }
   lo = make_uint4(o[0], o[1], o[2], o[3]);
   hi = make_uint4(o[4], o[5], o[6], o[7]);
@@ -660,19 +677,23 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const float4 v = ld_shared16(recv_base + cb * kSBytes + s_offset(row, 8 * ch + c));
-        s[4 * c] += v.x;
-        s[4 * c + 1] += v.y;
-        s[4 * c + 2] += v.z;
-        s[4 * c + 3] += v.w;
+        const float2 a = fadd2(make_float2(s[4 * c], s[4 * c + 1]), make_float2(v.x, v.y));
+        const float2 b = fadd2(make_float2(s[4 * c + 2], s[4 * c + 3]), make_float2(v.z, v.w));
+        s[4 * c] = a.x;
+        s[4 * c + 1] = a.y;
+        s[4 * c + 2] = b.x;
+        s[4 * c + 3] = b.y;
       }
       if (threadIdx.x == 0 && t + 2 < n_tiles) mbar_arrive_expect_tx(x_full0 + 8 * cb, kSBytes);
       __syncwarp();
       if (lane == 0) mbar_arrive(recv_done0 + 8 * cb);
       float hmax = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        s[i] = (vm >> i) & 1u ? s[i] * a.scale_log2 : -INFINITY;
-        hmax = fmaxf(hmax, s[i]);
+      for (int i = 0; i < 32; i += 2) {
+        const float2 y = fmul2(make_float2(s[i], s[i + 1]), make_float2(a.scale_log2, a.scale_log2));
+        s[i] = (vm >> i) & 1u ? y.x : -INFINITY;
+        s[i + 1] = (vm >> (i + 1)) & 1u ? y.y : -INFINITY;
+        hmax = fmaxf(hmax, fmaxf(s[i], s[i + 1]));
       }
       // row max over both column halves (the barrier also orders both
       // warps' reads of the scores before either writes P over them)
@@ -686,12 +707,14 @@ sparse_mla_attention_kernel(const AttentionArgs a) {
       if (grow) m = tmax;
       const float m_use = m == -INFINITY ? 0.0f : m;
       uint32_t pk[16];
-      float psum = 0.0f;
+      float2 psum2 = make_float2(0.0f, 0.0f);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        pk[i] = pack_bf16x2(ex2(s[2 * i] - m_use), ex2(s[2 * i + 1] - m_use));
-        psum += bf16_lo(pk[i]) + bf16_hi(pk[i]);
+        const float2 d = fadd2(make_float2(s[2 * i], s[2 * i + 1]), make_float2(-m_use, -m_use));
+        pk[i] = pack_bf16x2(ex2(d.x), ex2(d.y));
+        psum2 = fadd2(psum2, make_float2(bf16_lo(pk[i]), bf16_hi(pk[i])));
       }
+      const float psum = psum2.x + psum2.y;
       l = l * alpha + psum;
       // The exchange warps must have read tile t's partial scores before P
       // overwrites them (normally long done), and P V of the previous tile
