@@ -140,6 +140,8 @@ CASES = [
     ("H128 top512 q x4", dict(num_tokens=2, num_heads=128, topk=512, num_blocks=16, block_size=64, seed=305,
                               q_scale=4.0, p_unused=0.5)),
     ("H96 top31", dict(num_tokens=6, num_heads=96, topk=31, num_blocks=4, block_size=32, seed=306)),
+    # three full tiles: the score and receive double buffers wrap, the K ring fills
+    ("H128 top192", dict(num_tokens=2, num_heads=128, topk=192, num_blocks=8, block_size=64, seed=307)),
 ]
 
 
