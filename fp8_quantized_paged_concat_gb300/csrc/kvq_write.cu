@@ -53,6 +53,25 @@ __device__ __forceinline__ float amax16(const uint4& a, const uint4& b) {
   return fmaxf(__low2float(m), __high2float(m));
 }
 
+// x / s rounded to nearest even, for |x| <= 448 s (a value of its own tile),
+// from s2 = s * f and inv = RN(1 / s2), f a power of two that keeps s2 at or
+// above 2^-64 (x * f is exact).  Markstein's theorem (P. Markstein, IBM J.
+// Res. Dev. 34(1), 1990): q0 = RN(x * inv) is within an ulp of the quotient,
+// the remainder x - q0 * s2 is exact in one fused multiply-add, and
+// RN(q0 + remainder * inv) is the correctly rounded quotient (no overflow
+// or harmful underflow here: s2 >= 2^-64 and |quotient| <= 448; quotients
+// below 2^-11, where the remainder might not be exact, encode to an e4m3
+// zero of the sign of x whichever neighbour is returned).  The sign is
+// copied back so that -0 / s stays -0.  An exhaustive comparison with IEEE
+// division over every pair of bf16 values x, amax with |x| <= amax is in
+// tests/c/fp8_quotient_check.c.
+__device__ __forceinline__ float quotient(float x, float f, float s2, float inv) {
+  const float x2 = __fmul_rn(x, f);
+  const float q0 = __fmul_rn(x2, inv);
+  const float rem = __fmaf_rn(-q0, s2, x2);
+  return copysignf(__fmaf_rn(rem, inv, q0), x);
+}
+
 // Slot -> entry pointer, or nullptr for padding / out-of-range slots.  Slots
 // in range are below 2^32 (checked on the host), so 32-bit division applies.
 __device__ __forceinline__ uint8_t* entry_of(int64_t slot, const WriteArgs& a) {
@@ -159,13 +178,20 @@ write_fp8_ds_mla_kernel(const WriteArgs a) {
     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
     const float s = amax == 0.0f ? 1.0f : amax / 448.0f;
+    // x / s, correctly rounded, without a division per value: tile scales
+    // below 2^-64 are first brought up by 2^96 together with the values
+    // (exact, the quotient is unchanged), then Markstein's correction of a
+    // product with the correctly rounded reciprocal applies (see quotient()).
+    const float f = s < 0x1p-64f ? 0x1p96f : 1.0f;
+    const float s2 = __fmul_rn(s, f);
+    const float inv = __frcp_rn(s2);
     float x[16];
     unpack16(na[j], nb[j], x);
     uint32_t q[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      q[k] = cvt_e4m3x2(__fdiv_rn(x[4 * k], s), __fdiv_rn(x[4 * k + 1], s)) |
-             (cvt_e4m3x2(__fdiv_rn(x[4 * k + 2], s), __fdiv_rn(x[4 * k + 3], s)) << 16);
+      q[k] = cvt_e4m3x2(quotient(x[4 * k], f, s2, inv), quotient(x[4 * k + 1], f, s2, inv)) |
+             (cvt_e4m3x2(quotient(x[4 * k + 2], f, s2, inv), quotient(x[4 * k + 3], f, s2, inv)) << 16);
     }
     st16(entry[j] + 16 * lane, make_uint4(q[0], q[1], q[2], q[3]));
     if ((lane & 7) == 0) st4(entry[j] + kF8ScaleOff + 4 * (lane >> 3), __float_as_uint(s));

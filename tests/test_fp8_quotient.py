@@ -1,0 +1,23 @@
+"""The fp8_ds_mla write kernel's division-free quotient (Markstein's
+correction after a correctly rounded reciprocal, tile scales below 2^-64
+rescaled by 2^96) against IEEE division, for every pair of bf16 values
+x, amax with |x| <= amax: the e4m3 code it feeds is the oracle's.  Host
+code only (tests/c/fp8_quotient_check.c); about half a minute on one core."""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+def test_fp8_quotient_matches_ieee_division_exhaustively(tmp_path):
+    exe = tmp_path / "fp8_quotient_check"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-o", str(exe),
+                           os.path.join(HERE, "c", "fp8_quotient_check.c"), "-lm"])
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout
+    assert "mismatches 0" in r.stdout
+    assert "pairs 1065402238" in r.stdout
