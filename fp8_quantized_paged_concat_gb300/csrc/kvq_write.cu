@@ -62,14 +62,16 @@ __device__ __forceinline__ float amax16(const uint4& a, const uint4& b) {
 // or harmful underflow here: s2 >= 2^-64 and |quotient| <= 448; quotients
 // below 2^-11, where the remainder might not be exact, encode to an e4m3
 // zero of the sign of x whichever neighbour is returned).  The sign is
-// copied back so that -0 / s stays -0.  An exhaustive comparison with IEEE
-// division over every pair of bf16 values x, amax with |x| <= amax is in
-// tests/c/fp8_quotient_check.c.
-__device__ __forceinline__ float quotient(float x, float f, float s2, float inv) {
-  const float x2 = __fmul_rn(x, f);
-  const float q0 = __fmul_rn(x2, inv);
-  const float rem = __fmaf_rn(-q0, s2, x2);
-  return copysignf(__fmaf_rn(rem, inv, q0), x);
+// copied back so that -0 / s stays -0.  Two values per call (packed fp32
+// pairs, each half rounded as the scalar operation).  An exhaustive
+// comparison with IEEE division over every pair of bf16 values x, amax with
+// |x| <= amax is in tests/c/fp8_quotient_check.c.
+__device__ __forceinline__ float2 quotient2(float2 x, float f, float s2, float inv) {
+  const float2 x2 = fmul2(x, make_float2(f, f));
+  const float2 q0 = fmul2(x2, make_float2(inv, inv));
+  const float2 rem = ffma2(q0, make_float2(-s2, -s2), x2);
+  const float2 q = ffma2(rem, make_float2(inv, inv), q0);
+  return make_float2(copysignf(q.x, x.x), copysignf(q.y, x.y));
 }
 
 // Slot -> entry pointer, or nullptr for padding / out-of-range slots.  Slots
@@ -181,7 +183,7 @@ write_fp8_ds_mla_kernel(const WriteArgs a) {
     // x / s, correctly rounded, without a division per value: tile scales
     // below 2^-64 are first brought up by 2^96 together with the values
     // (exact, the quotient is unchanged), then Markstein's correction of a
-    // product with the correctly rounded reciprocal applies (see quotient()).
+    // product with the correctly rounded reciprocal applies (see quotient2()).
     const float f = s < 0x1p-64f ? 0x1p96f : 1.0f;
     const float s2 = __fmul_rn(s, f);
     const float inv = __frcp_rn(s2);
@@ -190,8 +192,9 @@ write_fp8_ds_mla_kernel(const WriteArgs a) {
     uint32_t q[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      q[k] = cvt_e4m3x2(quotient(x[4 * k], f, s2, inv), quotient(x[4 * k + 1], f, s2, inv)) |
-             (cvt_e4m3x2(quotient(x[4 * k + 2], f, s2, inv), quotient(x[4 * k + 3], f, s2, inv)) << 16);
+      const float2 lo = quotient2(make_float2(x[4 * k], x[4 * k + 1]), f, s2, inv);
+      const float2 hi = quotient2(make_float2(x[4 * k + 2], x[4 * k + 3]), f, s2, inv);
+      q[k] = cvt_e4m3x2(lo.x, lo.y) | (cvt_e4m3x2(hi.x, hi.y) << 16);
     }
     st16(entry[j] + 16 * lane, make_uint4(q[0], q[1], q[2], q[3]));
     if ((lane & 7) == 0) st4(entry[j] + kF8ScaleOff + 4 * (lane >> 3), __float_as_uint(s));
