@@ -115,32 +115,6 @@ __device__ __forceinline__ __nv_bfloat162 abs_bf16x2(uint32_t w) {
   return *reinterpret_cast<__nv_bfloat162*>(&a);
 }
 
-// NVFP4 group of 16 fp32 values (already scaled): sf = e4m3(amax / 6),
-// inv = 1 / sf (0 when sf is 0), codes e2m1(x * inv) packed 2 per byte,
-// value 2k in the low nibble of byte k.  Divisions are IEEE round-to-nearest
-// (the library is built without fast-math), products single fp32 roundings.
-__device__ __forceinline__ uint32_t nvfp4_scale_code(float amax) {
-  return cvt_e4m3x2(amax / 6.0f, 0.0f) & 0xffu;
-}
-
-__device__ __forceinline__ float nvfp4_inverse_scale(uint32_t sf_code) {
-  const float sf = e4m3_to_float(sf_code);
-  return sf == 0.0f ? 0.0f : 1.0f / sf;
-}
-
-__device__ __forceinline__ uint2 nvfp4_pack16(const float (&x)[16], float inv) {
-  uint2 out;
-  uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    w0 |= cvt_e2m1x2(__fmul_rn(x[2 * k], inv), __fmul_rn(x[2 * k + 1], inv)) << (8 * k);
-    w1 |= cvt_e2m1x2(__fmul_rn(x[8 + 2 * k], inv), __fmul_rn(x[8 + 2 * k + 1], inv)) << (8 * k);
-  }
-  out.x = w0;
-  out.y = w1;
-  return out;
-}
-
 // Two fp32 operations in one instruction (sm_100 and later; each half rounded
 // to nearest even exactly as the scalar operation).
 __device__ __forceinline__ float2 fmul2(float2 x, float2 y) {
@@ -164,6 +138,46 @@ __device__ __forceinline__ float2 ffma2(float2 x, float2 y, float2 z) {
       "mov.b64 c, {%6, %7};\n\tfma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
       : "=f"(r.x), "=f"(r.y) : "f"(x.x), "f"(x.y), "f"(y.x), "f"(y.y), "f"(z.x), "f"(z.y));
   return r;
+}
+
+// NVFP4 group of 16 fp32 values (already scaled): sf = e4m3(amax / 6),
+// inv = 1 / sf (0 when sf is 0), codes e2m1(x * inv) packed 2 per byte,
+// value 2k in the low nibble of byte k.  Quotients are IEEE round-to-nearest
+// (the library is built without fast-math), products single fp32 roundings.
+//
+// amax / 6 without a division: q0 = RN(amax * RN(1/6)) is within an ulp of
+// the quotient, the remainder amax - 6 q0 is exact in one fused
+// multiply-add, and RN(q0 + remainder * RN(1/6)) is the correctly rounded
+// quotient (Markstein's theorem, P. Markstein, IBM J. Res. Dev. 34(1),
+// 1990); +inf is passed through.  tests/c/nvfp4_scale_check.c compares it
+// with IEEE division for every non-negative fp32 amax: equal wherever the
+// e4m3 code can depend on it (quotients of 2^-11 and above).
+__device__ __forceinline__ uint32_t nvfp4_scale_code(float amax) {
+  constexpr float kInv6 = 1.0f / 6.0f;
+  const float q0 = __fmul_rn(amax, kInv6);
+  const float r = __fmaf_rn(-q0, 6.0f, amax);
+  const float q = isinf(amax) ? amax : __fmaf_rn(r, kInv6, q0);
+  return cvt_e4m3x2(q, 0.0f) & 0xffu;
+}
+
+__device__ __forceinline__ float nvfp4_inverse_scale(uint32_t sf_code) {
+  const float sf = e4m3_to_float(sf_code);
+  return sf == 0.0f ? 0.0f : 1.0f / sf;
+}
+
+__device__ __forceinline__ uint2 nvfp4_pack16(const float (&x)[16], float inv) {
+  uint2 out;
+  uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 a = fmul2(make_float2(x[2 * k], x[2 * k + 1]), make_float2(inv, inv));
+    const float2 b = fmul2(make_float2(x[8 + 2 * k], x[8 + 2 * k + 1]), make_float2(inv, inv));
+    w0 |= cvt_e2m1x2(a.x, a.y) << (8 * k);
+    w1 |= cvt_e2m1x2(b.x, b.y) << (8 * k);
+  }
+  out.x = w0;
+  out.y = w1;
+  return out;
 }
 
 // ---------------------------------------------------------------------------
