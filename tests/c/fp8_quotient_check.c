@@ -12,7 +12,7 @@
  * (x of the tile whose maximum magnitude is amax): the fp32 bits must agree,
  * except where both magnitudes are below 2^-11 -- those encode to an e4m3
  * zero -- and there the signs must agree.  Exit status 0 when every pair
- * passes.  Build: gcc -O2 -std=c11 -ffp-contract=off ... -lm.
+ * passes.  Build: gcc -O2 -std=c11 -ffp-contract=off [-fopenmp] ... -lm.
  */
 #include <math.h>
 #include <stdint.h>
@@ -34,6 +34,7 @@ static uint32_t float_bits(float f) {
 
 int main(void) {
   long long pairs = 0, mismatches = 0;
+#pragma omp parallel for schedule(dynamic, 64) reduction(+ : pairs, mismatches)
   for (uint32_t ab = 1; ab < 0x7f80u; ++ab) {          /* every positive finite bf16 amax */
     const float amax = bf16_value((uint16_t)ab);
     const float s = amax / 448.0f;
