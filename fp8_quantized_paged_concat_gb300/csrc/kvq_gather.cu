@@ -208,8 +208,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) gather_fp8_ds_mla_kernel
     for (int i = 0; i < 4; ++i) {
       const float2 v0 = __half22float2(e4m3x2_to_half2(w[i]));
       const float2 v1 = __half22float2(e4m3x2_to_half2(w[i] >> 16));
-      o[2 * i] = pack_bf16x2(__fmul_rn(v0.x, s[k]), __fmul_rn(v0.y, s[k]));
-      o[2 * i + 1] = pack_bf16x2(__fmul_rn(v1.x, s[k]), __fmul_rn(v1.y, s[k]));
+      const float2 p0 = fmul2(v0, make_float2(s[k], s[k]));   // packed pairs, each rounded as __fmul_rn
+      const float2 p1 = fmul2(v1, make_float2(s[k], s[k]));
+      o[2 * i] = pack_bf16x2(p0.x, p0.y);
+      o[2 * i + 1] = pack_bf16x2(p1.x, p1.y);
     }
     store32<kWide>(dst + (w0 + k) * a.dst_stride + 16 * lane, make_uint4(o[0], o[1], o[2], o[3]),
                    make_uint4(o[4], o[5], o[6], o[7]));

@@ -106,7 +106,11 @@ __global__ void __launch_bounds__(kThreads) reshape_and_cache_nvfp4_kernel(const
     if (!unit_scale) {
       amax = __fmul_rn(amax, fabsf(inv_scale));
 #pragma unroll
-      for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(y[i], inv_scale);
+      for (int i = 0; i < 16; i += 2) {
+        const float2 p = fmul2(make_float2(y[i], y[i + 1]), make_float2(inv_scale, inv_scale));
+        y[i] = p.x;
+        y[i + 1] = p.y;
+      }
     }
     const uint32_t sf = nvfp4_scale_code(amax);
     packed[j] = nvfp4_pack16(y, nvfp4_inverse_scale(sf));
@@ -178,7 +182,8 @@ __global__ void __launch_bounds__(kThreads) dequant_nvfp4_per_head_kernel(const 
     for (int i = 0; i < 8; ++i) {
       const uint32_t byte = (i < 4 ? q[j].x : q[j].y) >> (8 * (i & 3));
       const float2 v = __half22float2(e2m1x2_to_half2(byte));
-      o[i] = pack_bf16x2(__fmul_rn(v.x * sf, scale), __fmul_rn(v.y * sf, scale));
+      const float2 y = fmul2(fmul2(v, make_float2(sf, sf)), make_float2(scale, scale));   // (v sf) scale, each RN
+      o[i] = pack_bf16x2(y.x, y.y);
     }
     store32<kWide>(dst + j * kGroup, make_uint4(o[0], o[1], o[2], o[3]), make_uint4(o[4], o[5], o[6], o[7]));
   }

@@ -11,8 +11,11 @@
  * quotient x / s for every pair of bf16 values x, amax with |x| <= amax
  * (x of the tile whose maximum magnitude is amax): the fp32 bits must agree,
  * except where both magnitudes are below 2^-11 -- those encode to an e4m3
- * zero -- and there the signs must agree.  Exit status 0 when every pair
- * passes.  Build: gcc -O2 -std=c11 -ffp-contract=off [-fopenmp] ... -lm.
+ * zero -- and there the signs must agree.  It also checks the tile scale
+ * itself, formed as RN(q0 + (amax - 448 q0) * RN(1/448)) with
+ * q0 = RN(amax * RN(1/448)), against amax / 448 for every positive finite
+ * bf16 amax: the bits must agree (the scale is stored).  Exit status 0 when
+ * every pair and every scale passes.  Build: gcc -O2 -std=c11 -ffp-contract=off [-fopenmp] ... -lm.
  */
 #include <math.h>
 #include <stdint.h>
@@ -33,6 +36,19 @@ static uint32_t float_bits(float f) {
 }
 
 int main(void) {
+  long long scales = 0, scale_mismatches = 0;
+  const float inv448 = 1.0f / 448.0f;
+  for (uint32_t ab = 1; ab < 0x7f80u; ++ab) {
+    const float amax = bf16_value((uint16_t)ab);
+    const float q0 = amax * inv448;
+    const float s = fmaf(fmaf(-q0, 448.0f, amax), inv448, q0);
+    ++scales;
+    if (float_bits(s) != float_bits(amax / 448.0f)) {
+      if (scale_mismatches < 10) printf("scale: amax=%a exact=%a s=%a\n", amax, amax / 448.0f, s);
+      ++scale_mismatches;
+    }
+  }
+  printf("scales %lld scale mismatches %lld\n", scales, scale_mismatches);
   long long pairs = 0, mismatches = 0;
 #pragma omp parallel for schedule(dynamic, 64) reduction(+ : pairs, mismatches)
   for (uint32_t ab = 1; ab < 0x7f80u; ++ab) {          /* every positive finite bf16 amax */
@@ -58,5 +74,5 @@ int main(void) {
     }
   }
   printf("pairs %lld mismatches %lld\n", pairs, mismatches);
-  return mismatches != 0;
+  return mismatches != 0 || scale_mismatches != 0;
 }

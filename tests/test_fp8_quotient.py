@@ -1,7 +1,8 @@
-"""The fp8_ds_mla write kernel's division-free quotient (Markstein's
-correction after a correctly rounded reciprocal, tile scales below 2^-64
-rescaled by 2^96) against IEEE division, for every pair of bf16 values
-x, amax with |x| <= amax: the e4m3 code it feeds is the oracle's.  Host
+"""The fp8_ds_mla write kernel's division-free arithmetic against IEEE
+division: the quotient x / s (Markstein's correction after a correctly
+rounded reciprocal, tile scales below 2^-64 rescaled by 2^96) for every pair
+of bf16 values x, amax with |x| <= amax -- the e4m3 code it feeds is the
+oracle's -- and the stored tile scale amax / 448 for every bf16 amax.  Host
 code only (tests/c/fp8_quotient_check.c); a few seconds on several cores (about half a minute on one)."""
 import os
 import shutil
@@ -28,5 +29,5 @@ def test_fp8_quotient_matches_ieee_division_exhaustively(tmp_path):
                            os.path.join(HERE, "c", "fp8_quotient_check.c"), "-lm"])
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout
-    assert "mismatches 0" in r.stdout
-    assert "pairs 1065402238" in r.stdout
+    assert "pairs 1065402238 mismatches 0" in r.stdout
+    assert "scales 32639 scale mismatches 0" in r.stdout
