@@ -268,3 +268,21 @@ def test_attention_shape_sweep(kvq, oracle_mod, fmt, heads, topk):
     slot, one slot past a tile and one past four tiles."""
     w = wl.make_attention(f"sweep H{heads} k{topk}", 2, heads, topk, 8, 64, 400 + heads + topk, p_unused=0.05)
     assert run(kvq, oracle_mod, w, fmt=fmt) == 0
+
+
+@pytest.mark.parametrize("fmt", sorted(FORMATS))
+def test_attention_repeated_launches_bit_identical(kvq, oracle_mod, fmt):
+    """The kernel fixes every accumulation order (the MMAs, the score
+    exchange, the softmax sums), so repeated launches on the same inputs give
+    the same bits; a race in the exchange or the buffer hand-offs would show
+    as launch-to-launch differences.  152 tokens: one wave of clusters."""
+    w = wl.make_attention("repeat", 152, 128, 512, 16, 64, 331, p_unused=0.1)
+    cache = torch.from_numpy(host_cache(oracle_mod, w.fill, fmt=fmt)).to(DEV)
+    q, idx = w.q.to(DEV), w.indices.to(DEV)
+    fn = getattr(kvq, FORMATS[fmt][4])
+    out0, lse0 = fn(q, idx, cache, w.softmax_scale)
+    for _ in range(8):
+        out, lse = fn(q, idx, cache, w.softmax_scale)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), out0.view(torch.int16))
+        assert torch.equal(lse.view(torch.int32), lse0.view(torch.int32))
