@@ -16,8 +16,15 @@
 namespace kvq {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kLoads = 4;                     // independent accesses per thread
+// Launch shape (compile-time tuning knobs; the defaults are the measured best).
+#ifndef KVQ_INDEX_THREADS
+#define KVQ_INDEX_THREADS 128
+#endif
+#ifndef KVQ_INDEX_LOADS
+#define KVQ_INDEX_LOADS 4
+#endif
+constexpr int kThreads = KVQ_INDEX_THREADS;
+constexpr int kLoads = KVQ_INDEX_LOADS;       // independent accesses per thread
 constexpr int kMaxStagedWidth = 12288;        // 48 KB of int32: no opt-in shared memory needed
 
 // Slot of position p given the request's table row (or -1, with a status
