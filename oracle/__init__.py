@@ -63,6 +63,12 @@ _SIGNATURES = {
     "kvqo_sparse_mla_attention_fp8_ds_mla": (_I64, [_P, _I64, _I64, _I64, _I64, _I32, _P, _I64, _I32,
                                                     _P, _I64, _I32, _I64, _I64, ctypes.c_double,
                                                     _P, _I64, _I64, _P, _I64]),
+    "kvqo_prefill_mla_attention_nvfp4_ds_mla": (_I64, [_P, _I64, _I64, _I32, _P, _P, _P, _I64, _I32, _I64, _I64,
+                                                       _P, _I64, _I32, _I64, _I64, ctypes.c_double,
+                                                       _P, _I64, _I64, _P, _I64]),
+    "kvqo_prefill_mla_attention_fp8_ds_mla": (_I64, [_P, _I64, _I64, _I32, _P, _P, _P, _I64, _I32, _I64, _I64,
+                                                     _P, _I64, _I32, _I64, _I64, ctypes.c_double,
+                                                     _P, _I64, _I64, _P, _I64]),
     "kvqo_decode_fp8_ds_mla_entry": (None, [_P, _P]),
     "kvqo_decode_nvfp4_ds_mla_entry": (None, [_P, _P]),
 }
@@ -391,6 +397,53 @@ def _attention(fn_name, entry_bytes, q, indices, cache, softmax_scale, threads):
         return r
 
     skipped = _run_chunks(run, T, threads)
+    return out, lse, skipped
+
+
+def prefill_mla_attention_nvfp4_ds_mla(q, query_start, context_lens, block_table, cache, softmax_scale: float,
+                                       threads: int = 1):
+    """Oracle dense prefill over the nvfp4_ds_mla cache: q uint16 bf16 bits [T,
+    H, 576]; request b's query tokens [query_start[b], query_start[b+1])
+    attend to its context positions [0, context_lens[b]) through block_table
+    int32 [B, W]; returns (o float64 [T, H, 512], lse float64 [T, H],
+    positions skipped)."""
+    return _prefill("kvqo_prefill_mla_attention_nvfp4_ds_mla", 352, q, query_start, context_lens, block_table,
+                    cache, softmax_scale, threads)
+
+
+def prefill_mla_attention_fp8_ds_mla(q, query_start, context_lens, block_table, cache, softmax_scale: float,
+                                     threads: int = 1):
+    """The same over the 656-byte fp8_ds_mla cache."""
+    return _prefill("kvqo_prefill_mla_attention_fp8_ds_mla", 656, q, query_start, context_lens, block_table,
+                    cache, softmax_scale, threads)
+
+
+def _prefill(fn_name, entry_bytes, q, query_start, context_lens, block_table, cache, softmax_scale, threads):
+    if q.dtype != np.uint16 or q.ndim != 3 or q.shape[2] != 576 or q.strides[2] != 2:
+        raise ValueError("q: expected uint16 [T, H, 576] with unit inner stride")
+    query_start = np.ascontiguousarray(query_start, dtype=np.int32)
+    context_lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    block_table = np.ascontiguousarray(block_table, dtype=np.int32)
+    B = context_lens.shape[0]
+    if query_start.shape != (B + 1,) or block_table.ndim != 2 or block_table.shape[0] != B:
+        raise ValueError("query_start [B + 1], context_lens [B] and block_table [B, W] disagree")
+    T, H = q.shape[0], q.shape[1]
+    if query_start[0] < 0 or query_start[-1] > T or np.any(np.diff(query_start) < 0):
+        raise ValueError("query_start must be non-decreasing within [0, T]")
+    nb, bs, bstride, estride = _cache_geometry(cache, entry_bytes)
+    out = np.zeros((T, H, 512), np.float64)
+    lse = np.zeros((T, H), np.float64)
+    fn = getattr(lib(), fn_name)
+
+    def run(b, e):
+        r = fn(_ptr(q), q.strides[0] // 2, q.strides[1] // 2, H, _ptr(query_start), _ptr(context_lens),
+               _ptr(block_table), block_table.shape[1], block_table.shape[1], b, e, _ptr(cache), nb, bs, bstride,
+               estride, float(softmax_scale), _ptr(out), H * 512, 512, _ptr(lse), H)
+        if r < 0:
+            raise MemoryError("oracle prefill attention: scratch allocation failed")
+        return r
+
+    skipped = _run_chunks(run, B, threads)
     return out, lse, skipped
 
 

@@ -616,6 +616,37 @@ int64_t kvqo_req_index_to_global_slot(
  * over the valid entries of indices[t] (negative entries are unused; a slot
  * beyond the cache is skipped and counted).  A token with no valid entry
  * gets o = 0 and lse = -inf.  Everything in double, entries decoded exactly. */
+/* Softmax attention of the heads of one query token over n decoded keys
+ * (576 values each): s_j = scale * q . k_j, o = sum_j exp(s_j - m) k_j[0:512]
+ * / sum_j exp(s_j - m), lse = m + log sum_j exp(s_j - m), all in double;
+ * n = 0 gives o = 0, lse = -inf.  s is scratch for n scores. */
+static void attend_token(const uint16_t* q_t, int64_t q_stride_h, int32_t num_heads, const double* keys, int32_t n,
+                         double softmax_scale, double* s, double* out_t, int64_t out_stride_h, double* lse_t) {
+    const int dim = NV_NOPE_DIM + NV_ROPE_DIM;
+    int32_t h;
+    for (h = 0; h < num_heads; ++h) {
+        const uint16_t* qh = q_t + (int64_t)h * q_stride_h;
+        double* oh = out_t + (int64_t)h * out_stride_h;
+        double m = -INFINITY, l = 0.0;
+        int d, j;
+        for (d = 0; d < NV_NOPE_DIM; ++d) oh[d] = 0.0;
+        for (j = 0; j < n; ++j) {
+            double dot = 0.0;
+            for (d = 0; d < dim; ++d) dot += (double)kvqo_bf16_value(qh[d]) * keys[(int64_t)j * dim + d];
+            s[j] = softmax_scale * dot;
+            if (s[j] > m) m = s[j];
+        }
+        for (j = 0; j < n; ++j) {
+            double w = exp(s[j] - m);
+            l += w;
+            for (d = 0; d < NV_NOPE_DIM; ++d) oh[d] += w * keys[(int64_t)j * dim + d];
+        }
+        if (n > 0)
+            for (d = 0; d < NV_NOPE_DIM; ++d) oh[d] /= l;
+        if (lse_t) lse_t[h] = (n > 0) ? m + log(l) : -INFINITY;
+    }
+}
+
 static int64_t sparse_mla_attention(
     void (*decode)(const uint8_t*, double*),
     const uint16_t* q, int64_t q_stride_t, int64_t q_stride_h,
@@ -631,7 +662,7 @@ static int64_t sparse_mla_attention(
     double* s = (double*)malloc(sizeof(double) * (size_t)(topk > 0 ? topk : 1));
     if (!keys || !s) { free(keys); free(s); return -1; }
     for (t = t_begin; t < t_end; ++t) {
-        int32_t n = 0, k, h;
+        int32_t n = 0, k;
         for (k = 0; k < topk; ++k) {
             int64_t slot = indices[t * indices_stride + k];
             if (slot < 0) continue;
@@ -640,27 +671,8 @@ static int64_t sparse_mla_attention(
                    keys + (int64_t)n * dim);
             ++n;
         }
-        for (h = 0; h < num_heads; ++h) {
-            const uint16_t* qh = q + t * q_stride_t + (int64_t)h * q_stride_h;
-            double* oh = out + t * out_stride_t + (int64_t)h * out_stride_h;
-            double m = -INFINITY, l = 0.0;
-            int d, j;
-            for (d = 0; d < NV_NOPE_DIM; ++d) oh[d] = 0.0;
-            for (j = 0; j < n; ++j) {
-                double dot = 0.0;
-                for (d = 0; d < dim; ++d) dot += (double)kvqo_bf16_value(qh[d]) * keys[(int64_t)j * dim + d];
-                s[j] = softmax_scale * dot;
-                if (s[j] > m) m = s[j];
-            }
-            for (j = 0; j < n; ++j) {
-                double w = exp(s[j] - m);
-                l += w;
-                for (d = 0; d < NV_NOPE_DIM; ++d) oh[d] += w * keys[(int64_t)j * dim + d];
-            }
-            if (n > 0)
-                for (d = 0; d < NV_NOPE_DIM; ++d) oh[d] /= l;
-            if (lse) lse[t * lse_stride_t + h] = (n > 0) ? m + log(l) : -INFINITY;
-        }
+        attend_token(q + t * q_stride_t, q_stride_h, num_heads, keys, n, softmax_scale, s, out + t * out_stride_t,
+                     out_stride_h, lse ? lse + t * lse_stride_t : NULL);
     }
     free(keys);
     free(s);
@@ -709,4 +721,80 @@ int64_t kvqo_sparse_mla_attention_fp8_ds_mla(
                                 num_heads, indices, indices_stride, topk, cache, num_blocks, block_size,
                                 block_stride, entry_stride, softmax_scale, out, out_stride_t, out_stride_h,
                                 lse, lse_stride_t);
+}
+
+/* Dense prefill over the quantized cache ([P3] "Function and motivation" and
+ * "Key source snippets", _compute_prefill_context: a request's whole context
+ * is read through its block-table row and attended densely; the MQA form of
+ * the sparse decode, reading 21 of the build's spec).  Request b (b_begin <=
+ * b < b_end) owns the query tokens [query_start[b], query_start[b+1]); each of
+ * them attends, with every head, to the positions p < context_lens[b] of its
+ * context, position p being entry p % block_size of block
+ * block_table[b][p / block_size].  Positions whose block-table column or block
+ * id is out of range are skipped and counted. */
+static int64_t prefill_mla_attention(
+    void (*decode)(const uint8_t*, double*),
+    const uint16_t* q, int64_t q_stride_t, int64_t q_stride_h, int32_t num_heads,
+    const int32_t* query_start, const int32_t* context_lens,
+    const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width,
+    int64_t b_begin, int64_t b_end,
+    const uint8_t* cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride, double softmax_scale,
+    double* out, int64_t out_stride_t, int64_t out_stride_h,
+    double* lse, int64_t lse_stride_t) {
+    const int dim = NV_NOPE_DIM + NV_ROPE_DIM;
+    int64_t b, skipped = 0;
+    for (b = b_begin; b < b_end; ++b) {
+        const int32_t ctx = context_lens[b] > 0 ? context_lens[b] : 0;
+        double* keys = (double*)malloc(sizeof(double) * (size_t)(ctx > 0 ? ctx : 1) * dim);
+        double* s = (double*)malloc(sizeof(double) * (size_t)(ctx > 0 ? ctx : 1));
+        int32_t n = 0, p;
+        int64_t t;
+        if (!keys || !s) { free(keys); free(s); return -1; }
+        for (p = 0; p < ctx; ++p) {
+            const int32_t col = p / block_size;
+            int64_t id;
+            if (col >= block_table_width) { ++skipped; continue; }
+            id = block_table[b * block_table_stride + col];
+            if (id < 0 || id >= num_blocks) { ++skipped; continue; }
+            decode(cache + id * block_stride + (int64_t)(p % block_size) * entry_stride, keys + (int64_t)n * dim);
+            ++n;
+        }
+        for (t = query_start[b]; t < query_start[b + 1]; ++t)
+            attend_token(q + t * q_stride_t, q_stride_h, num_heads, keys, n, softmax_scale, s,
+                         out + t * out_stride_t, out_stride_h, lse ? lse + t * lse_stride_t : NULL);
+        free(keys);
+        free(s);
+    }
+    return skipped;
+}
+
+int64_t kvqo_prefill_mla_attention_nvfp4_ds_mla(
+    const uint16_t* q, int64_t q_stride_t, int64_t q_stride_h, int32_t num_heads,
+    const int32_t* query_start, const int32_t* context_lens,
+    const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width,
+    int64_t b_begin, int64_t b_end,
+    const uint8_t* cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride, double softmax_scale,
+    double* out, int64_t out_stride_t, int64_t out_stride_h,
+    double* lse, int64_t lse_stride_t) {
+    return prefill_mla_attention(kvqo_decode_nvfp4_ds_mla_entry, q, q_stride_t, q_stride_h, num_heads, query_start,
+                                 context_lens, block_table, block_table_stride, block_table_width, b_begin, b_end,
+                                 cache, num_blocks, block_size, block_stride, entry_stride, softmax_scale, out,
+                                 out_stride_t, out_stride_h, lse, lse_stride_t);
+}
+
+int64_t kvqo_prefill_mla_attention_fp8_ds_mla(
+    const uint16_t* q, int64_t q_stride_t, int64_t q_stride_h, int32_t num_heads,
+    const int32_t* query_start, const int32_t* context_lens,
+    const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width,
+    int64_t b_begin, int64_t b_end,
+    const uint8_t* cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride, double softmax_scale,
+    double* out, int64_t out_stride_t, int64_t out_stride_h,
+    double* lse, int64_t lse_stride_t) {
+    return prefill_mla_attention(kvqo_decode_fp8_ds_mla_entry, q, q_stride_t, q_stride_h, num_heads, query_start,
+                                 context_lens, block_table, block_table_stride, block_table_width, b_begin, b_end,
+                                 cache, num_blocks, block_size, block_stride, entry_stride, softmax_scale, out,
+                                 out_stride_t, out_stride_h, lse, lse_stride_t);
 }

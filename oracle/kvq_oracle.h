@@ -153,6 +153,31 @@ int64_t kvqo_sparse_mla_attention_fp8_ds_mla(
     double* out, int64_t out_stride_t, int64_t out_stride_h,
     double* lse, int64_t lse_stride_t);
 
+/* Dense prefill of the query tokens [query_start[b], query_start[b+1]) of
+ * requests b_begin <= b < b_end over their context positions [0,
+ * context_lens[b]), read through block_table (the same attention as the
+ * sparse form, with every context position listed).  Out-of-range block-table
+ * columns or block ids are skipped and counted.  Returns -1 if scratch memory
+ * runs out. */
+int64_t kvqo_prefill_mla_attention_nvfp4_ds_mla(
+    const uint16_t* q, int64_t q_stride_t, int64_t q_stride_h, int32_t num_heads,
+    const int32_t* query_start, const int32_t* context_lens,
+    const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width,
+    int64_t b_begin, int64_t b_end,
+    const uint8_t* cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride, double softmax_scale,
+    double* out, int64_t out_stride_t, int64_t out_stride_h,
+    double* lse, int64_t lse_stride_t);
+int64_t kvqo_prefill_mla_attention_fp8_ds_mla(
+    const uint16_t* q, int64_t q_stride_t, int64_t q_stride_h, int32_t num_heads,
+    const int32_t* query_start, const int32_t* context_lens,
+    const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width,
+    int64_t b_begin, int64_t b_end,
+    const uint8_t* cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride, double softmax_scale,
+    double* out, int64_t out_stride_t, int64_t out_stride_h,
+    double* lse, int64_t lse_stride_t);
+
 /* Decodes one 656-byte fp8_ds_mla entry to its 576 bf16 values (as doubles). */
 void kvqo_decode_fp8_ds_mla_entry(const uint8_t* entry, double* out576);
 

@@ -203,3 +203,115 @@ def test_fp8_attention_matches_numpy_definition(oracle_mod, scale):
         want_o, want_lse = numpy_attention(qv[t], keys[rows], scale)
         np.testing.assert_allclose(o[t], want_o, rtol=1e-11, atol=1e-11 * np.abs(keys).max())
         np.testing.assert_allclose(lse[t], want_lse, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# dense prefill: every context position of a request, read through its
+# block-table row (vLLM PR #48642, "Function and motivation",
+# _compute_prefill_context)
+# ---------------------------------------------------------------------------
+
+def prefill_case(oracle_mod, seed, ctx_lens, q_lens, H, num_blocks=12):
+    """Requests whose contexts hold exact keys: request b's positions p <
+    ctx_lens[b] live at entry p % BS of block table[b][p // BS] (distinct
+    shuffled blocks).  Returns (cache, table, query_start, keys per request,
+    q bits, q values)."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    n_blk = [(c + BS - 1) // BS for c in ctx_lens]
+    order = g.permutation(num_blocks)
+    assert sum(n_blk) <= num_blocks
+    width = max(1, max(n_blk))
+    table = np.full((len(ctx_lens), width), -1, np.int32)
+    cache = np.zeros((num_blocks, BS, 352), np.uint8)
+    keys, used = [], 0
+    for b, c in enumerate(ctx_lens):
+        table[b, :n_blk[b]] = order[used:used + n_blk[b]]
+        used += n_blk[b]
+        kv_c, k_pe, k = exact_keys(c, seed + 10 + b, oracle_mod)
+        slots = np.array([table[b, p // BS] * BS + p % BS for p in range(c)], np.int64)
+        if c:
+            assert oracle_mod.write_nvfp4_ds_mla(kv_c, k_pe, slots, cache) == 0
+        keys.append(k)
+    qs = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    qb, qv = random_q(int(qs[-1]), H, seed + 5)
+    return cache, table, qs, keys, qb, qv
+
+
+@pytest.mark.parametrize("scale", [1.0 / 24.0, 0.7])
+def test_prefill_matches_numpy_definition(oracle_mod, scale):
+    """Three requests (ragged contexts across block boundaries, 1-3 query
+    tokens each) against numpy's float64 evaluation on the exact keys."""
+    ctx, ql, H = [37, 16, 50], [2, 1, 3], 5
+    cache, table, qs, keys, qb, qv = prefill_case(oracle_mod, 41, ctx, ql, H)
+    o, lse, skipped = oracle_mod.prefill_mla_attention_nvfp4_ds_mla(qb, qs, ctx, table, cache, scale)
+    assert skipped == 0
+    for b in range(3):
+        for t in range(qs[b], qs[b + 1]):
+            want_o, want_lse = numpy_attention(qv[t], keys[b], scale)
+            np.testing.assert_allclose(o[t], want_o, rtol=1e-11, atol=1e-11 * np.abs(keys[b]).max())
+            np.testing.assert_allclose(lse[t], want_lse, rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_is_independent_of_block_placement(oracle_mod):
+    """Moving a request's blocks elsewhere in the cache (the table updated
+    with them) changes nothing: the context is addressed only through the
+    table."""
+    ctx, ql, H = [40, 23], [2, 2], 3
+    cache, table, qs, _, qb, _ = prefill_case(oracle_mod, 51, ctx, ql, H)
+    perm = np.random.Generator(np.random.PCG64(52)).permutation(cache.shape[0])
+    moved = np.empty_like(cache)
+    moved[perm] = cache                              # block i -> perm[i]
+    table2 = np.where(table >= 0, perm[np.maximum(table, 0)], -1).astype(np.int32)
+    o1, l1, _ = oracle_mod.prefill_mla_attention_nvfp4_ds_mla(qb, qs, ctx, table, cache, 0.3)
+    o2, l2, _ = oracle_mod.prefill_mla_attention_nvfp4_ds_mla(qb, qs, ctx, table2, moved, 0.3)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+def test_prefill_empty_context_bad_blocks_and_no_queries(oracle_mod):
+    """A request with no context gives o = 0 and lse = -inf; positions whose
+    block id or table column is out of range are skipped and counted (the
+    rest still attend); a request with no query tokens writes nothing."""
+    ctx, ql, H = [0, 30, 20], [2, 1, 0], 2
+    cache, table, qs, keys, qb, qv = prefill_case(oracle_mod, 61, ctx, ql, H)
+    table = table.copy()
+    table[1, 1] = 99                                 # positions 16..29 of request 1: bad block id
+    ctx2 = np.array([0, 30, 20], np.int32)
+    o, lse, skipped = oracle_mod.prefill_mla_attention_nvfp4_ds_mla(qb, qs, ctx2, table, cache, 0.5)
+    assert skipped == 14
+    assert not o[0:2].any() and np.all(np.isneginf(lse[0:2]))
+    want_o, want_lse = numpy_attention(qv[2], keys[1][:16], 0.5)
+    np.testing.assert_allclose(o[2], want_o, rtol=1e-11, atol=1e-11 * np.abs(keys[1]).max())
+    np.testing.assert_allclose(lse[2], want_lse, rtol=1e-12, atol=1e-12)
+    wide = np.array([0, 40, 20], np.int32)           # 40 positions: columns past the table width
+    _, _, skipped = oracle_mod.prefill_mla_attention_nvfp4_ds_mla(qb, qs, wide, table, cache, 0.5)
+    assert skipped == (32 - 16) + (40 - 32)          # bad block: positions 16..31; past the width: 32..39
+
+
+def test_prefill_fp8_matches_numpy_definition(oracle_mod):
+    """The fp8_ds_mla form: entries of e4m3 codes with power-of-two tile
+    scales and bf16 RoPE (exact by construction), two requests."""
+    g = np.random.Generator(np.random.PCG64(71))
+    nb = 6
+    cache = np.zeros((nb, BS, 656), np.uint8)
+    codes = g.integers(0, 0x7f, (nb, BS, 512)).astype(np.uint8) | (g.integers(0, 2, (nb, BS, 512)) << 7).astype(np.uint8)
+    codes[(codes & 0x7f) == 0x7f] = 0x10
+    cache[:, :, :512] = codes
+    scales = (2.0 ** g.integers(-4, 5, (nb, BS, 4))).astype("<f4")
+    cache[:, :, 512:528] = scales.view(np.uint8).reshape(nb, BS, 16)
+    rope_bits, rope = bf16_bits_of(g.standard_normal((nb, BS, 64)).astype(np.float32))
+    cache[:, :, 528:656] = rope_bits.astype("<u2").view(np.uint8).reshape(nb, BS, 128)
+    e4 = np.array([oracle_mod.e4m3_value(c) for c in range(256)])
+    dec = np.concatenate([e4[codes] * np.repeat(scales.astype(np.float64), 128, axis=2), rope], axis=2)
+    table = np.array([[4, 1, 0], [2, 5, -1]], np.int32)
+    ctx = np.array([40, 17], np.int32)
+    qs = np.array([0, 2, 3], np.int32)
+    qb, qv = random_q(3, 4, 72)
+    o, lse, skipped = oracle_mod.prefill_mla_attention_fp8_ds_mla(qb, qs, ctx, table, cache, 0.02)
+    assert skipped == 0
+    for b in range(2):
+        k = np.stack([dec[table[b, p // BS], p % BS] for p in range(ctx[b])])
+        for t in range(qs[b], qs[b + 1]):
+            want_o, want_lse = numpy_attention(qv[t], k, 0.02)
+            np.testing.assert_allclose(o[t], want_o, rtol=1e-11, atol=1e-11 * np.abs(k).max())
+            np.testing.assert_allclose(lse[t], want_lse, rtol=1e-12, atol=1e-12)
