@@ -248,6 +248,10 @@ struct Fp8Write {
 
 }  // namespace
 
+// The largest batch whose grid stays within 2^31 - 1 CTAs on either launch
+// path (at least one token per warp).
+int64_t write_max_tokens() { return int64_t{INT32_MAX} * kWarpsPerBlock; }
+
 cudaError_t launch_write_nvfp4_ds_mla(const WriteArgs& a, cudaStream_t stream) {
   return dispatch_write<Nvfp4Write>(a, stream);
 }
