@@ -21,7 +21,8 @@ __all__ = [
     "kvq_write_nvfp4_ds_mla", "kvq_write_fp8_ds_mla", "kvq_gather_upconvert_nvfp4_ds_mla",
     "kvq_gather_upconvert_fp8_ds_mla", "kvq_reshape_and_cache_nvfp4", "kvq_selftest_convert",
     "kvq_dequant_nvfp4_per_head", "kvq_req_index_to_global_slot",
-    "kvq_sparse_mla_attention_nvfp4_ds_mla", "kvq_sparse_mla_attention_fp8_ds_mla", "kvq_last_error_string", "kvq_version", "library_path", "load_library",
+    "kvq_sparse_mla_attention_nvfp4_ds_mla", "kvq_sparse_mla_attention_fp8_ds_mla",
+    "kvq_prefill_mla_attention_nvfp4_ds_mla", "kvq_prefill_mla_attention_fp8_ds_mla", "kvq_last_error_string", "kvq_version", "library_path", "load_library",
     "NVFP4_DS_MLA_ENTRY_BYTES", "FP8_DS_MLA_ENTRY_BYTES", "STATUS_BAD_INDEX", "STATUS_BAD_BATCH",
     "STATUS_TIMEOUT",
     "nvfp4_full_dim",
@@ -61,6 +62,12 @@ _SIGNATURES = {
     "kvq_sparse_mla_attention_fp8_ds_mla": [_P, _I64, _I64, _I64, _I32, _P, _I64, _I32, _P, _I64, _I32,
                                             _I64, _I64, ctypes.c_float, _P, _I64, _I64, _P, _I64,
                                             _P, _P],
+    "kvq_prefill_mla_attention_nvfp4_ds_mla": [_P, _I64, _I64, _I64, _I32, _P, _P, _I32, _I32, _P, _I64, _I32,
+                                               _P, _I64, _I32, _I64, _I64, ctypes.c_float, _P, _I64, _I64, _P,
+                                               _I64, _P, _P],
+    "kvq_prefill_mla_attention_fp8_ds_mla": [_P, _I64, _I64, _I64, _I32, _P, _P, _I32, _I32, _P, _I64, _I32,
+                                             _P, _I64, _I32, _I64, _I64, ctypes.c_float, _P, _I64, _I64, _P,
+                                             _I64, _P, _P],
 }
 
 
@@ -315,6 +322,58 @@ def _attention(cname, entry, q, indices, kv_cache, softmax_scale, out, lse, stat
           kv_cache.shape[1], kv_cache.stride(0), kv_cache.stride(1), float(softmax_scale), out.data_ptr(),
           out.stride(0), out.stride(1), None if lse is False else lse.data_ptr(),
           0 if lse is False else lse.stride(0), _status_ptr(status), _stream(stream, q.device))
+    return out, (None if lse is False else lse)
+
+
+def kvq_prefill_mla_attention_nvfp4_ds_mla(q, query_start, context_lens, block_table, kv_cache,
+                                           softmax_scale: float, max_query_len: int, out=None, lse=None,
+                                           status=None, stream=None):
+    """Dense prefill straight from the nvfp4_ds_mla cache: q bf16 [T, H, 576];
+    request b's query tokens [query_start[b], query_start[b+1]) (int32 [B+1],
+    at most max_query_len each) attend to its context positions [0,
+    context_lens[b]) (int32 [B]) through block_table int32 [B, W].  Returns
+    (out bf16 [T, H, 512], lse fp32 [T, H]); lse=False skips the lse output."""
+    return _prefill("kvq_prefill_mla_attention_nvfp4_ds_mla", 352, q, query_start, context_lens, block_table,
+                    kv_cache, softmax_scale, max_query_len, out, lse, status, stream)
+
+
+def kvq_prefill_mla_attention_fp8_ds_mla(q, query_start, context_lens, block_table, kv_cache,
+                                         softmax_scale: float, max_query_len: int, out=None, lse=None,
+                                         status=None, stream=None):
+    """The same dense prefill straight from the 656-byte fp8_ds_mla cache."""
+    return _prefill("kvq_prefill_mla_attention_fp8_ds_mla", 656, q, query_start, context_lens, block_table,
+                    kv_cache, softmax_scale, max_query_len, out, lse, status, stream)
+
+
+def _prefill(cname, entry, q, query_start, context_lens, block_table, kv_cache, softmax_scale, max_query_len,
+             out, lse, status, stream):
+    _need(q.dtype == torch.bfloat16 and q.is_cuda and q.dim() == 3 and q.shape[2] == 576
+          and q.stride(2) == 1, "q: expected a CUDA bf16 [T, H, 576] tensor with unit inner stride")
+    T, H = q.shape[0], q.shape[1]
+    B = context_lens.shape[0] if context_lens.dim() == 1 else -1
+    _need(context_lens.dtype == torch.int32 and context_lens.is_cuda and B >= 0 and context_lens.is_contiguous(),
+          "context_lens: expected a contiguous CUDA int32 [B] tensor")
+    _need(query_start.dtype == torch.int32 and query_start.is_cuda and tuple(query_start.shape) == (B + 1,)
+          and query_start.is_contiguous(), "query_start: expected a contiguous CUDA int32 [B + 1] tensor")
+    _need(block_table.dtype == torch.int32 and block_table.is_cuda and block_table.dim() == 2
+          and block_table.shape[0] == B and block_table.stride(1) == 1,
+          "block_table: expected a CUDA int32 [B, W] tensor with unit inner stride")
+    _mla_cache("kv_cache", kv_cache, entry)
+    if out is None:
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=q.device)
+    _need(out.dtype == torch.bfloat16 and out.is_cuda and tuple(out.shape) == (T, H, 512)
+          and out.stride(2) == 1, "out: expected a CUDA bf16 [T, H, 512] tensor with unit inner stride")
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    if lse is not False:
+        _need(lse.dtype == torch.float32 and lse.is_cuda and tuple(lse.shape) == (T, H) and lse.stride(1) == 1,
+              "lse: expected a CUDA fp32 [T, H] tensor with unit inner stride")
+    _call(cname, q.data_ptr(), q.stride(0), q.stride(1), T, H, query_start.data_ptr(), context_lens.data_ptr(),
+          B, int(max_query_len), block_table.data_ptr(), block_table.stride(0), block_table.shape[1],
+          kv_cache.data_ptr(), kv_cache.shape[0], kv_cache.shape[1], kv_cache.stride(0), kv_cache.stride(1),
+          float(softmax_scale), out.data_ptr(), out.stride(0), out.stride(1),
+          None if lse is False else lse.data_ptr(), 0 if lse is False else lse.stride(0), _status_ptr(status),
+          _stream(stream, q.device))
     return out, (None if lse is False else lse)
 
 

@@ -92,7 +92,8 @@ kvq_status write_common(const char* fn, int64_t entry_bytes,
                         kvq_stream_t stream) {
   KVQ_REQUIRE(num_tokens >= 0, "%s: num_tokens < 0", fn);
   if (num_tokens == 0) return ok();
-  KVQ_REQUIRE(num_tokens < (int64_t{1} << 35), "%s: num_tokens too large", fn);  // grid.x < 2^31
+  KVQ_REQUIRE(num_tokens <= kvq::write_max_tokens(), "%s: num_tokens exceeds %lld (grid limit)", fn,
+              static_cast<long long>(kvq::write_max_tokens()));
   if (kvq_status s = check_bf16_rows(fn, "kv_c", kv_c, kv_c_stride, KVQ_MLA_NOPE_DIM)) return s;
   if (kvq_status s = check_bf16_rows(fn, "k_pe", k_pe, k_pe_stride, KVQ_MLA_ROPE_DIM)) return s;
   KVQ_REQUIRE(slot_mapping != nullptr, "%s: slot_mapping is NULL", fn);
@@ -347,6 +348,77 @@ kvq_status attention_common(
   a.indices_stride = indices_stride;
   a.topk = topk;
   a.cache = kv_cache;
+  a.num_blocks = num_blocks;
+  a.num_slots = num_blocks * block_size;
+  a.block_size = block_size;
+  a.block_div = kvq::FastDiv::make(static_cast<uint32_t>(block_size));
+  a.block_stride = block_stride;
+  a.entry_stride = entry_stride;
+  a.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634074);
+  a.out = out;
+  a.out_stride_t = out_stride_t;
+  a.out_stride_h = out_stride_h;
+  a.lse = lse;
+  a.lse_stride_t = lse_stride_t;
+  a.status = d_status;
+  return launched(fn, launch(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvq_status prefill_common(
+    const char* fn, int64_t entry_bytes, cudaError_t (*launch)(const kvq::AttentionArgs&, cudaStream_t),
+    const void* q, int64_t q_stride_t, int64_t q_stride_h, int64_t num_tokens, int32_t num_heads,
+    const int32_t* query_start, const int32_t* context_lens, int32_t batch_size, int32_t max_query_len,
+    const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width, const uint8_t* kv_cache,
+    int64_t num_blocks, int32_t block_size, int64_t block_stride, int64_t entry_stride, float softmax_scale,
+    void* out, int64_t out_stride_t, int64_t out_stride_h, float* lse, int64_t lse_stride_t, int32_t* d_status,
+    kvq_stream_t stream) {
+  KVQ_REQUIRE(num_tokens >= 0 && batch_size >= 0 && max_query_len >= 0,
+              "%s: num_tokens, batch_size and max_query_len must be >= 0", fn);
+  if (num_tokens == 0 || batch_size == 0 || max_query_len == 0) return ok();
+  KVQ_REQUIRE(num_heads >= 1, "%s: num_heads must be >= 1 (got %d)", fn, num_heads);
+  KVQ_REQUIRE(batch_size <= 65535, "%s: batch_size must be at most 65535 (grid.y)", fn);
+  KVQ_REQUIRE(int64_t{max_query_len} * num_heads < (int64_t{1} << 31) && num_tokens < (int64_t{1} << 31),
+              "%s: max_query_len * num_heads and num_tokens must stay below 2^31", fn);
+  KVQ_REQUIRE(q != nullptr && out != nullptr, "%s: q and out must be non-NULL", fn);
+  KVQ_REQUIRE(aligned(q, 16) && aligned(out, 16), "%s: q and out must be 16-byte aligned", fn);
+  KVQ_REQUIRE(q_stride_h >= KVQ_WORKSPACE_DIM && q_stride_h % 8 == 0 && q_stride_t % 8 == 0 &&
+                  q_stride_t >= 0,
+              "%s: q strides must be multiples of 8 elements with head stride >= 576", fn);
+  KVQ_REQUIRE(out_stride_h >= KVQ_MLA_NOPE_DIM && out_stride_h % 8 == 0 && out_stride_t % 8 == 0 &&
+                  out_stride_t >= (num_heads - 1) * out_stride_h + KVQ_MLA_NOPE_DIM,
+              "%s: out strides must be multiples of 8 elements and rows must not overlap "
+              "(head stride >= 512, token stride >= (num_heads - 1) * head stride + 512)", fn);
+  KVQ_REQUIRE(lse == nullptr || (aligned(lse, 4) && lse_stride_t >= num_heads),
+              "%s: lse must be 4-byte aligned with token stride >= num_heads", fn);
+  KVQ_REQUIRE(query_start != nullptr && context_lens != nullptr && block_table != nullptr,
+              "%s: query_start, context_lens and block_table must be non-NULL", fn);
+  KVQ_REQUIRE(aligned(query_start, 4) && aligned(context_lens, 4) && aligned(block_table, 4),
+              "%s: int32 arrays must be 4-byte aligned", fn);
+  KVQ_REQUIRE(block_table_width > 0 && block_table_stride >= block_table_width,
+              "%s: need block_table_width > 0 and block_table_stride >= block_table_width", fn);
+  KVQ_REQUIRE(softmax_scale == softmax_scale && softmax_scale > -3.0e38f && softmax_scale < 3.0e38f,
+              "%s: softmax_scale must be finite", fn);
+  if (kvq_status s = check_mla_cache(fn, kv_cache, num_blocks, block_size, block_stride,
+                                     entry_stride, entry_bytes))
+    return s;
+  KVQ_REQUIRE(d_status == nullptr || aligned(d_status, 4), "%s: d_status misaligned", fn);
+  if (kvq_status s = check_device(fn)) return s;
+  kvq::AttentionArgs a{};
+  a.q = q;
+  a.q_stride_t = q_stride_t;
+  a.q_stride_h = q_stride_h;
+  a.num_tokens = num_tokens;
+  a.num_heads = num_heads;
+  a.head_div = kvq::FastDiv::make(static_cast<uint32_t>(num_heads));
+  a.query_start = query_start;
+  a.context_lens = context_lens;
+  a.block_table = block_table;
+  a.block_table_stride = block_table_stride;
+  a.block_table_width = block_table_width;
+  a.batch_size = batch_size;
+  a.max_query_len = max_query_len;
+  a.cache = kv_cache;
+  a.num_blocks = num_blocks;
   a.num_slots = num_blocks * block_size;
   a.block_size = block_size;
   a.block_div = kvq::FastDiv::make(static_cast<uint32_t>(block_size));
@@ -363,6 +435,34 @@ kvq_status attention_common(
 }
 
 }  // namespace
+
+kvq_status kvq_prefill_mla_attention_nvfp4_ds_mla(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h, int64_t num_tokens, int32_t num_heads,
+    const int32_t* query_start, const int32_t* context_lens, int32_t batch_size, int32_t max_query_len,
+    const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width, const uint8_t* kv_cache,
+    int64_t num_blocks, int32_t block_size, int64_t block_stride, int64_t entry_stride, float softmax_scale,
+    void* out, int64_t out_stride_t, int64_t out_stride_h, float* lse, int64_t lse_stride_t, int32_t* d_status,
+    kvq_stream_t stream) {
+  return prefill_common("kvq_prefill_mla_attention_nvfp4_ds_mla", KVQ_NVFP4_DS_MLA_ENTRY_BYTES,
+                        kvq::launch_prefill_mla_attention_nvfp4, q, q_stride_t, q_stride_h, num_tokens, num_heads,
+                        query_start, context_lens, batch_size, max_query_len, block_table, block_table_stride,
+                        block_table_width, kv_cache, num_blocks, block_size, block_stride, entry_stride,
+                        softmax_scale, out, out_stride_t, out_stride_h, lse, lse_stride_t, d_status, stream);
+}
+
+kvq_status kvq_prefill_mla_attention_fp8_ds_mla(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h, int64_t num_tokens, int32_t num_heads,
+    const int32_t* query_start, const int32_t* context_lens, int32_t batch_size, int32_t max_query_len,
+    const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width, const uint8_t* kv_cache,
+    int64_t num_blocks, int32_t block_size, int64_t block_stride, int64_t entry_stride, float softmax_scale,
+    void* out, int64_t out_stride_t, int64_t out_stride_h, float* lse, int64_t lse_stride_t, int32_t* d_status,
+    kvq_stream_t stream) {
+  return prefill_common("kvq_prefill_mla_attention_fp8_ds_mla", KVQ_FP8_DS_MLA_ENTRY_BYTES,
+                        kvq::launch_prefill_mla_attention_fp8, q, q_stride_t, q_stride_h, num_tokens, num_heads,
+                        query_start, context_lens, batch_size, max_query_len, block_table, block_table_stride,
+                        block_table_width, kv_cache, num_blocks, block_size, block_stride, entry_stride,
+                        softmax_scale, out, out_stride_t, out_stride_h, lse, lse_stride_t, d_status, stream);
+}
 
 kvq_status kvq_sparse_mla_attention_nvfp4_ds_mla(
     const void* q, int64_t q_stride_t, int64_t q_stride_h, int64_t num_tokens, int32_t num_heads,

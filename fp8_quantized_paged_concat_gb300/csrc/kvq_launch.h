@@ -72,14 +72,26 @@ struct AttentionArgs {
   const void* q;                 // bf16 [num_tokens, num_heads, 576]
   int64_t q_stride_t, q_stride_h;
   int64_t num_tokens;
-  int32_t num_heads;             // 1 .. 128
+  int32_t num_heads;             // 1 .. 128 (sparse decode), >= 1 (dense prefill)
+  FastDiv head_div;              // divides a packed (token, head) row by num_heads
+  // sparse decode: each token's own list of global slots
   const int32_t* indices;        // global slots [num_tokens, topk], < 0 unused
   int64_t indices_stride;
   int32_t topk;
+  // dense prefill: request b's query tokens [query_start[b], query_start[b+1])
+  // attend to its context positions [0, context_lens[b]) through block_table
+  const int32_t* query_start;    // [batch_size + 1]
+  const int32_t* context_lens;   // [batch_size]
+  const int32_t* block_table;    // [batch_size, >= block_table_width]
+  int64_t block_table_stride;
+  int32_t block_table_width;
+  int32_t batch_size;
+  int32_t max_query_len;         // bounds the grid (row blocks per request)
   const uint8_t* cache;
-  int64_t num_slots;
+  int64_t num_blocks;
+  int64_t num_slots;             // num_blocks * block_size
   int32_t block_size;
-  FastDiv block_div;             // slot -> block
+  FastDiv block_div;             // slot (or context position) -> block (or block-table column)
   int64_t block_stride, entry_stride;
   float scale_log2;              // softmax_scale * log2(e)
   void* out;                     // bf16 [num_tokens, num_heads, 512]
@@ -89,6 +101,7 @@ struct AttentionArgs {
   int32_t* status;
 };
 
+int64_t write_max_tokens();     // grid.x bound of the write launches
 cudaError_t launch_write_nvfp4_ds_mla(const WriteArgs& a, cudaStream_t stream);
 cudaError_t launch_write_fp8_ds_mla(const WriteArgs& a, cudaStream_t stream);
 cudaError_t launch_gather_nvfp4_ds_mla(const GatherArgs& a, cudaStream_t stream);
@@ -98,6 +111,8 @@ cudaError_t launch_reshape_and_cache_nvfp4(const PerHeadArgs& a, cudaStream_t st
 cudaError_t launch_dequant_nvfp4_per_head(const PerHeadArgs& a, cudaStream_t stream);
 cudaError_t launch_sparse_mla_attention_nvfp4(const AttentionArgs& a, cudaStream_t stream);
 cudaError_t launch_sparse_mla_attention_fp8(const AttentionArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill_mla_attention_nvfp4(const AttentionArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill_mla_attention_fp8(const AttentionArgs& a, cudaStream_t stream);
 
 struct IndexArgs {
   const int32_t* req_id;

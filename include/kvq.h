@@ -58,8 +58,9 @@ typedef int32_t kvq_status;
 #define KVQ_STATUS_BAD_INDEX   0x1  /* slot, block id or position out of range (skipped) */
 #define KVQ_STATUS_BAD_BATCH   0x2  /* workspace_starts not non-decreasing within [0, T],
                                        or a row before the first request (skipped)       */
-#define KVQ_STATUS_TIMEOUT     0x4  /* a kernel's bounded wait on its own tensor-core work
-                                       expired; that CTA's outputs were not written      */
+#define KVQ_STATUS_TIMEOUT     0x4  /* a bounded wait of the attention kernel (on its own
+                                       tensor-core work or on another of its warp roles)
+                                       expired; the outputs concerned were not written  */
 
 /* Entry geometry ([P1] "Implementation breakdown" items 2-3). */
 #define KVQ_MLA_NOPE_DIM               512
@@ -248,9 +249,11 @@ kvq_status kvq_dequant_nvfp4_per_head(
  * stride >= 512, token stride >= (num_heads - 1) * head stride + 512).  lse:
  * fp32 [num_tokens, num_heads] with token stride lse_stride_t >= num_heads,
  * or NULL.  indices: int32, indices_stride >= topk.  The cache follows the
- * nvfp4 gather's rules.  If a bounded wait of the kernel on its own tensor
- * work expires (not expected), KVQ_STATUS_TIMEOUT is set and that token's
- * outputs are left unwritten.
+ * nvfp4 gather's rules.  Every wait of the kernel is bounded (about 2 s):
+ * if one expires (not expected), the kernel sets KVQ_STATUS_TIMEOUT, leaves
+ * the outputs of the query rows concerned unwritten (each of the two CTAs of
+ * a token writes its own 256 output columns) and still returns, with nothing
+ * of it left running on the device.
  */
 kvq_status kvq_sparse_mla_attention_nvfp4_ds_mla(
     const void* q, int64_t q_stride_t, int64_t q_stride_h,
@@ -276,6 +279,61 @@ kvq_status kvq_sparse_mla_attention_fp8_ds_mla(
     const void* q, int64_t q_stride_t, int64_t q_stride_h,
     int64_t num_tokens, int32_t num_heads,
     const int32_t* indices, int64_t indices_stride, int32_t topk,
+    const uint8_t* kv_cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride,
+    float softmax_scale,
+    void* out, int64_t out_stride_t, int64_t out_stride_h,
+    float* lse, int64_t lse_stride_t,
+    int32_t* d_status, kvq_stream_t stream);
+
+/*
+ * kvq_prefill_mla_attention_nvfp4_ds_mla -- dense prefill over the 352-byte
+ * cache: the query tokens of each request attend to every position of its
+ * context, read straight from the quantized pages through the block table
+ * ([P3] "Function and motivation" and "Key source snippets",
+ * _compute_prefill_context, which otherwise gathers that context into the
+ * bf16 workspace first).  Request b < batch_size owns the query tokens
+ * [query_start[b], query_start[b+1]) (rows of q / out / lse; at most
+ * max_query_len of them) and the context positions p < context_lens[b];
+ * position p is entry p % block_size of block block_table[b *
+ * block_table_stride + p / block_size].  For each of its query tokens t and
+ * heads h, out[t,h] and lse[t,h] are the attention of
+ * kvq_sparse_mla_attention_nvfp4_ds_mla with the key list = all of those
+ * positions, with the same arithmetic.  (token, head) rows of a request are
+ * processed 128 at a time, so a decoded page feeds the heads of every query
+ * token in such a block.  A position whose block-table column is >=
+ * block_table_width or whose block id is outside [0, num_blocks) is skipped
+ * (KVQ_STATUS_BAD_INDEX); a request whose query range is not inside [0,
+ * num_tokens) or is longer than max_query_len is skipped (KVQ_STATUS_BAD_BATCH);
+ * a request with no context position gets out = 0, lse = -inf.
+ * q, out, lse: as kvq_sparse_mla_attention_nvfp4_ds_mla, num_heads >= 1
+ * (max_query_len * num_heads < 2^31).  query_start: int32 [batch_size + 1];
+ * context_lens: int32 [batch_size]; block_table: int32 [batch_size, >=
+ * block_table_width]; batch_size <= 65535.  Waits are bounded as in the
+ * sparse form (KVQ_STATUS_TIMEOUT).
+ */
+kvq_status kvq_prefill_mla_attention_nvfp4_ds_mla(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h,
+    int64_t num_tokens, int32_t num_heads,
+    const int32_t* query_start, const int32_t* context_lens, int32_t batch_size, int32_t max_query_len,
+    const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width,
+    const uint8_t* kv_cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride,
+    float softmax_scale,
+    void* out, int64_t out_stride_t, int64_t out_stride_h,
+    float* lse, int64_t lse_stride_t,
+    int32_t* d_status, kvq_stream_t stream);
+
+/*
+ * kvq_prefill_mla_attention_fp8_ds_mla -- the same dense prefill over the
+ * 656-byte fp8_ds_mla cache (keys as kvq_gather_upconvert_fp8_ds_mla writes
+ * them); entry_stride >= 656.
+ */
+kvq_status kvq_prefill_mla_attention_fp8_ds_mla(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h,
+    int64_t num_tokens, int32_t num_heads,
+    const int32_t* query_start, const int32_t* context_lens, int32_t batch_size, int32_t max_query_len,
+    const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width,
     const uint8_t* kv_cache, int64_t num_blocks, int32_t block_size,
     int64_t block_stride, int64_t entry_stride,
     float softmax_scale,

@@ -286,3 +286,162 @@ def test_attention_repeated_launches_bit_identical(kvq, oracle_mod, fmt):
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int16), out0.view(torch.int16))
         assert torch.equal(lse.view(torch.int32), lse0.view(torch.int32))
+
+
+# ---------------------------------------------------------------------------
+# dense prefill: the query tokens of a request attend to its whole context
+# through the block table; (token, head) rows are packed 128 to a CTA, so a
+# CTA's decoded key tiles feed several query tokens when H < 128
+# ---------------------------------------------------------------------------
+
+PREFILL_FORMATS = {"nvfp4": ("prefill_mla_attention_nvfp4_ds_mla", "kvq_prefill_mla_attention_nvfp4_ds_mla"),
+                   "fp8": ("prefill_mla_attention_fp8_ds_mla", "kvq_prefill_mla_attention_fp8_ds_mla")}
+
+
+def check_prefill(oracle_mod, cache, w, out, lse, threads=1, requests=None):
+    """GPU out / lse against the oracle's dense prefill for the given
+    requests (all by default), within the bound of check()."""
+    fmt = "fp8" if cache.shape[2] == 656 else "nvfp4"
+    qs, ctx, table = wl.host(w.query_start), wl.host(w.context_lens), wl.host(w.block_table)
+    qb = wl.bf16_bits(w.q)
+    qv = q_values(w.q)
+    got_o = out.float().cpu().numpy().astype(np.float64)
+    got_lse = lse.cpu().numpy().astype(np.float64)
+    bs, nb = cache.shape[1], cache.shape[0]
+    requests = range(len(ctx)) if requests is None else requests
+    for b in requests:
+        sub_qs = np.array([0, qs[b + 1] - qs[b]], np.int32)
+        if sub_qs[1] == 0:
+            continue
+        want_o, want_lse, _ = getattr(oracle_mod, PREFILL_FORMATS[fmt][0])(
+            np.ascontiguousarray(qb[qs[b]:qs[b + 1]]), sub_qs, ctx[b:b + 1], table[b:b + 1], cache, w.softmax_scale,
+            threads=threads)
+        slots = [table[b, p // bs] * bs + p % bs for p in range(max(ctx[b], 0))
+                 if p // bs < table.shape[1] and 0 <= table[b, p // bs] < nb]
+        for i, t in enumerate(range(qs[b], qs[b + 1])):
+            if not slots:
+                assert not np.any(got_o[t]), f"request {b} token {t}: no context but nonzero output"
+                assert np.all(np.isneginf(got_lse[t])), f"request {b} token {t}: lse {got_lse[t]}"
+                continue
+            keys = decoded_keys(oracle_mod, cache, np.asarray(slots))
+            vmax = np.abs(keys[:, :512]).max()
+            e_s = 576 * 2.0 ** -24 * abs(w.softmax_scale) * (np.abs(qv[t]) @ np.abs(keys).T).max(axis=1)
+            eps = 2.0 ** -9 + e_s + 2.0 ** -20
+            tol_o = (2 * eps / (1 - eps))[:, None] * vmax + 2.0 ** -9 * np.abs(want_o[i]) + 1e-30
+            err_o = np.abs(got_o[t] - want_o[i])
+            bad = err_o > tol_o
+            assert not bad.any(), (f"request {b} token {t}: {int(bad.sum())} outputs beyond the bound; worst "
+                                   f"{float((err_o / tol_o).max()):.3f} x bound")
+            tol_l = eps + e_s + 2.0 ** -22 * np.abs(want_lse[i])
+            assert np.all(np.abs(got_lse[t] - want_lse[i]) <= tol_l), f"request {b} token {t}: lse"
+
+
+def run_prefill(kvq, oracle_mod, w, fmt="nvfp4", cache=None, threads=1, requests=None):
+    if cache is None:
+        cache = host_cache(oracle_mod, w.fill, threads, fmt)
+    dcache = torch.from_numpy(cache).to(DEV)
+    T, H = w.q.shape[0], w.q.shape[1]
+    out = torch.full((T, H, 512), -7.0, dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((T, H), -7.0, dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    getattr(kvq, PREFILL_FORMATS[fmt][1])(w.q.to(DEV), w.query_start.to(DEV), w.context_lens.to(DEV),
+                                           w.block_table.to(DEV), dcache, w.softmax_scale, w.max_query_len,
+                                           out=out, lse=lse, status=status)
+    torch.cuda.synchronize()
+    check_prefill(oracle_mod, cache, w, out, lse, threads, requests)
+    return int(status.item()), out, lse
+
+
+PREFILL_CASES = [
+    # one query token per row block; ragged contexts across 64-position blocks
+    ("H128 ragged", dict(context_lens=[100, 64, 257], query_lens=[2, 1, 3], num_heads=128, num_blocks=16,
+                         block_size=64, seed=501)),
+    # 8 query tokens share every decoded tile; 20 tokens -> 3 row blocks, the last one partial
+    ("H16 packed", dict(context_lens=[300, 70], query_lens=[9, 20], num_heads=16, num_blocks=16,
+                        block_size=64, seed=502)),
+    # 128 / 20 is not whole: a row block holds parts of tokens; an empty context; block size 16
+    ("H20 straddling, empty context", dict(context_lens=[130, 0, 65], query_lens=[13, 2, 7], num_heads=20,
+                                           num_blocks=24, block_size=16, seed=503)),
+    # one head, 200 query tokens: two row blocks of one request
+    ("H1 200 tokens", dict(context_lens=[33], query_lens=[200], num_heads=1, num_blocks=4, block_size=16,
+                           seed=504)),
+    # a request with no query tokens between two that have some
+    ("no query tokens", dict(context_lens=[80, 90, 70], query_lens=[1, 0, 2], num_heads=64, num_blocks=8,
+                             block_size=64, seed=505)),
+]
+
+
+@pytest.mark.parametrize("fmt", sorted(PREFILL_FORMATS))
+@pytest.mark.parametrize("name,kw", PREFILL_CASES, ids=[c[0] for c in PREFILL_CASES])
+def test_prefill_parity(kvq, oracle_mod, name, kw, fmt):
+    w = wl.make_prefill(name, **kw)
+    status, _, _ = run_prefill(kvq, oracle_mod, w, fmt)
+    assert status == 0
+
+
+@pytest.mark.parametrize("fmt", sorted(PREFILL_FORMATS))
+def test_prefill_4k_contexts(kvq, oracle_mod, threads, fmt):
+    """Contexts of 4096 and 4500 positions (64 and 71 tiles), 128 heads."""
+    w = wl.make_prefill("4k contexts", [4096, 4500], [2, 1], 128, 160, 64, 506)
+    status, _, _ = run_prefill(kvq, oracle_mod, w, fmt, threads=threads)
+    assert status == 0
+
+
+@pytest.mark.parametrize("fmt", sorted(PREFILL_FORMATS))
+def test_prefill_bad_blocks_and_requests(kvq, oracle_mod, fmt):
+    """A block id out of range (its positions skipped, KVQ_STATUS_BAD_INDEX),
+    a context longer than the table (the rest skipped), and a request whose
+    query range runs past num_tokens (skipped whole, KVQ_STATUS_BAD_BATCH,
+    its rows untouched)."""
+    w = wl.make_prefill("bad", [150, 70, 60], [2, 2, 1], 32, 12, 64, 507)
+    table = wl.host(w.block_table).copy()
+    table[0, 1] = 1 << 20                            # positions 64..127 of request 0
+    w.block_table = torch.from_numpy(table)
+    ctx = wl.host(w.context_lens).copy()
+    ctx[1] = 200                                     # request 1 owns 2 blocks: positions 128.. skipped
+    w.context_lens = torch.from_numpy(ctx)
+    qs = wl.host(w.query_start).copy()
+    good_qs = qs.copy()
+    qs[3] = qs[2] + 5                                # request 2 claims 5 tokens, only 1 exists
+    w.query_start = torch.from_numpy(qs)
+    w.max_query_len = 5
+    cache = host_cache(oracle_mod, w.fill, fmt=fmt)
+    dcache = torch.from_numpy(cache).to(DEV)
+    T, H = w.q.shape[0], w.q.shape[1]
+    out = torch.full((T, H, 512), -7.0, dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((T, H), -7.0, dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    getattr(kvq, PREFILL_FORMATS[fmt][1])(w.q.to(DEV), w.query_start.to(DEV), w.context_lens.to(DEV),
+                                           w.block_table.to(DEV), dcache, w.softmax_scale, w.max_query_len,
+                                           out=out, lse=lse, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == kvq.STATUS_BAD_INDEX | kvq.STATUS_BAD_BATCH
+    assert torch.all(out[good_qs[2]:] == -7.0) and torch.all(lse[good_qs[2]:] == -7.0)
+    w.query_start = torch.from_numpy(good_qs)
+    check_prefill(oracle_mod, cache, w, out, lse, requests=[0, 1])
+
+
+@pytest.mark.parametrize("fmt", sorted(PREFILL_FORMATS))
+def test_prefill_matches_sparse_form(kvq, oracle_mod, fmt):
+    """The dense prefill of a request equals the sparse attention of its
+    tokens over the slot list of its whole context (the same arithmetic and
+    tile order), bit for bit."""
+    w = wl.make_prefill("vs sparse", [190, 77], [3, 2], 128, 16, 64, 508)
+    cache = host_cache(oracle_mod, w.fill, fmt=fmt)
+    dcache = torch.from_numpy(cache).to(DEV)
+    q = w.q.to(DEV)
+    out, lse = getattr(kvq, PREFILL_FORMATS[fmt][1])(q, w.query_start.to(DEV), w.context_lens.to(DEV),
+                                                      w.block_table.to(DEV), dcache, w.softmax_scale,
+                                                      w.max_query_len)
+    qs, ctx, table = wl.host(w.query_start), wl.host(w.context_lens), wl.host(w.block_table)
+    idx = np.full((w.num_tokens, int(ctx.max())), -1, np.int32)
+    for b in range(2):
+        for t in range(qs[b], qs[b + 1]):
+            idx[t, :ctx[b]] = [table[b, p // 64] * 64 + p % 64 for p in range(ctx[b])]
+    out2, lse2 = getattr(kvq, FORMATS[fmt][4])(q, torch.from_numpy(idx).to(DEV), dcache, w.softmax_scale)
+    torch.cuda.synchronize()
+    # equal wherever the token's own list covers the same tiles: all of
+    # request 0's tokens (the longest context); request 1's lists are padded
+    # with unused entries to the longest context, which adds only masked tiles
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))

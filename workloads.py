@@ -161,6 +161,24 @@ class AttentionWorkload:
         return int(self.q.shape[0])
 
 
+@dataclass
+class PrefillWorkload:
+    """Dense prefill: the query tokens of each request attend to every
+    position of its context, read through its block-table row."""
+    name: str
+    fill: WriteWorkload           # writes every slot of the cache
+    q: torch.Tensor               # bf16 [T, H, 576]
+    query_start: torch.Tensor     # int32 [B + 1]: request b owns query tokens [qs[b], qs[b+1])
+    context_lens: torch.Tensor    # int32 [B]
+    block_table: torch.Tensor     # int32 [B, W]
+    softmax_scale: float
+    max_query_len: int
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.q.shape[0])
+
+
 # --------------------------------------------------------------------------
 # builders
 # --------------------------------------------------------------------------
@@ -251,6 +269,28 @@ def make_attention(name: str, num_tokens: int, num_heads: int, topk: int, num_bl
     return AttentionWorkload(name, fill, q, torch.from_numpy(idx).to(device), float(softmax_scale))
 
 
+def make_prefill(name: str, context_lens, query_lens, num_heads: int, num_blocks: int, block_size: int,
+                 seed: int, device="cpu", softmax_scale: float = 576 ** -0.5, fill: WriteWorkload = None,
+                 rng: str = "numpy", block_table=None) -> PrefillWorkload:
+    """Queries ~ N(0, 1) in bf16 for requests with the given query-token
+    counts, each attending to its first context_lens[b] positions; each
+    request owns distinct shuffled blocks (or the given block table) of a
+    cache whose every slot is written (``fill``, or a fresh seeded fill)."""
+    context_lens = [int(x) for x in context_lens]
+    query_lens = [int(x) for x in query_lens]
+    if fill is None:
+        fill = make_fill(name + " fill", num_blocks, block_size, seed, device, rng=rng)
+    if block_table is None:
+        block_table = make_gather_batch(num_blocks, block_size, context_lens, [0] * len(context_lens), seed)[0]
+    qs = np.zeros(len(query_lens) + 1, np.int32)
+    qs[1:] = np.cumsum(query_lens)
+    q = normal_bf16((int(qs[-1]), num_heads, NOPE_DIM + ROPE_DIM), seed * 7 + 5, device, rng=rng)
+    return PrefillWorkload(name, fill, q, torch.from_numpy(qs).to(device),
+                           torch.from_numpy(np.asarray(context_lens, np.int32)).to(device),
+                           torch.as_tensor(np.asarray(block_table, np.int32)).to(device), float(softmax_scale),
+                           max(query_lens) if query_lens else 0)
+
+
 # --------------------------------------------------------------------------
 # the five named workloads
 # --------------------------------------------------------------------------
@@ -314,6 +354,18 @@ def sparse_attention(device="cpu", fill: WriteWorkload = None) -> AttentionWorkl
     return make_attention("sparse MLA attention T=4096 H=128 top-2048", 4096, 128, 2048, 65536, 64, 1006,
                           device, p_unused=0.1, fill=fill,
                           rng="device" if str(device).startswith("cuda") else "numpy")
+
+
+def prefill_attention(gather: GatherWorkload, device="cpu", query_len: int = 16) -> PrefillWorkload:
+    """Dense prefill over the prefill gather's cache and batch: each of its 32
+    requests attends with ``query_len`` new tokens x 128 heads to its whole
+    context up to the end of its gathered range (seq_start + length, 4k-36k
+    positions) through the same block table."""
+    ctx = [int(s) + n for s, n in zip(host(gather.seq_starts), gather.seq_lens)]
+    return make_prefill(f"dense prefill B={len(ctx)} q={query_len} H=128 over contexts of 4k-36k", ctx,
+                        [query_len] * len(ctx), 128, gather.fill.num_blocks, gather.fill.block_size, 1007, device,
+                        fill=gather.fill, rng="device" if str(device).startswith("cuda") else "numpy",
+                        block_table=host(gather.block_table))
 
 
 # --------------------------------------------------------------------------
