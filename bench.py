@@ -528,6 +528,36 @@ def time_extra(step: GpuStep):
                 "frac": round(flops / us / 1e6 / peak_tf, 4), "gbs": round(nbytes / us / 1e3, 1),
                 "valid_slots": n_valid, "method": "CUDA events"}
             del aw, ao, al
+        # dense prefill straight from the caches: each request of a gather
+        # batch attends with 16 new tokens x 128 heads to its whole context
+        # (seq_start + length positions) through the same block table
+        for fmt, gather, cache, fn in (
+                ("nvfp4_ds_mla", step.g3, step.cache3, kvq.kvq_prefill_mla_attention_nvfp4_ds_mla),
+                ("fp8_ds_mla", step.g4, step.cache4, kvq.kvq_prefill_mla_attention_fp8_ds_mla)):
+            pw = wl.prefill_attention(gather, dev)
+            po = torch.empty((pw.num_tokens, 128, 512), dtype=torch.bfloat16, device=dev)
+            pl = torch.empty((pw.num_tokens, 128), dtype=torch.float32, device=dev)
+            times = []
+            for r in range(8):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn(pw.q, pw.query_start, pw.context_lens, pw.block_table, cache, pw.softmax_scale,
+                   pw.max_query_len, out=po, lse=pl)
+                b.record()
+                torch.cuda.synchronize()
+                if r >= 2:
+                    times.append(a.elapsed_time(b))
+            us = statistics.median(times) * 1e3
+            ctx = wl.host(pw.context_lens).astype(np.int64)
+            ql = np.diff(wl.host(pw.query_start)).astype(np.int64)
+            flops = ATTN_FLOPS_PER_SLOT_HEAD * 128 * int((ctx * ql).sum())
+            peak_tf, peak_src = measured_peak_tflops()
+            out[f"prefill_mla_attention_{fmt} B={len(ctx)} q=16 H=128 ctx {int(ctx.min())}-{int(ctx.max())}"] = {
+                "units": pw.num_tokens, "us": round(us, 2), "tflops": round(flops / us / 1e6, 1),
+                "bound": "tensor", "peak_tflops": peak_tf, "peak": f"{peak_src} bf16 burst",
+                "frac": round(flops / us / 1e6 / peak_tf, 4), "context_positions": int(ctx.sum()),
+                "method": "CUDA events"}
+            del pw, po, pl
     # fp8_ds_mla cache fill: 2,097,152 tokens, one launch
     f4 = step.g4.fill
     times = []
@@ -745,6 +775,30 @@ def run_ours(args):
     return 0
 
 
+def run_prefill_only(query_len: int) -> int:
+    """Profiler hook: the dense prefill alone on a small cache: 8 requests
+    with contexts of 4k-16k positions over an 8192 x 64 cache, query_len new
+    tokens x 128 heads each, 3 launches."""
+    import fp8_quantized_paged_concat_gb300 as kvq
+    kvq.load_library()
+    dev = torch.device("cuda:0")
+    fill = wl.make_fill("prefill profiling fill 8192x64", 8192, 64, 1007, dev, rng="device")
+    cache = torch.zeros((8192, 64, 352), dtype=torch.uint8, device=dev)
+    kvq.kvq_write_nvfp4_ds_mla(fill.kv_c, fill.k_pe, cache, fill.slot_mapping)
+    g = np.random.Generator(np.random.PCG64(1007))
+    w = wl.make_prefill("prefill profiling case", g.integers(4096, 16384, 8, endpoint=True), [query_len] * 8, 128,
+                        8192, 64, 1007, dev, fill=fill, rng="device")
+    for r in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        kvq.kvq_prefill_mla_attention_nvfp4_ds_mla(w.q, w.query_start, w.context_lens, w.block_table, cache,
+                                                   w.softmax_scale, w.max_query_len)
+        b.record()
+        torch.cuda.synchronize()
+        print(f"prefill_mla_attention q={query_len}: {a.elapsed_time(b) * 1e3:.1f} us", flush=True)
+    return 0
+
+
 def run_attention_only(tokens: int) -> int:
     """Profiler hook: the attention alone on a small cache (a few hundred MB)."""
     import fp8_quantized_paged_concat_gb300 as kvq
@@ -765,6 +819,50 @@ def run_attention_only(tokens: int) -> int:
     return 0
 
 
+KERNEL_ONLY = ["reshape_and_cache_nvfp4", "reshape_and_cache_nvfp4_hnd", "dequant_nvfp4_per_head",
+               "dequant_nvfp4_per_head_hnd", "req_index_to_global_slot"]
+
+
+def run_kernel_only(name: str) -> int:
+    """Profiler hook: one kernel of the bench's extra measurements on its own
+    workload (per-head: K, V [16384, 8, 128] into 16384 x 2 x 16 x 8 x 72;
+    index conversion: 4096 x 2048 positions), 3 launches after one set-up
+    launch, times printed; nothing else runs."""
+    import fp8_quantized_paged_concat_gb300 as kvq
+    kvq.load_library()
+    dev = torch.device("cuda:0")
+    if name.startswith(("reshape", "dequant")):
+        layout = "HND" if name.endswith("_hnd") else "NHD"
+        p = wl.make_per_head("per-head", 16384, 8, 128, 16384, 16, 0, 1005, dev)
+        ks = torch.ones(1, dtype=torch.float32, device=dev)
+        shape = (16384, 2, 16, 8, 72) if layout == "NHD" else (16384, 2, 8, 16, 72)
+        cache = torch.zeros(shape, dtype=torch.uint8, device=dev)
+        ko, vo = torch.empty_like(p.key), torch.empty_like(p.value)
+        write = lambda: kvq.kvq_reshape_and_cache_nvfp4(p.key, p.value, cache, p.slot_mapping, ks, ks, layout=layout)
+        fn = write if name.startswith("reshape") else \
+            (lambda: kvq.kvq_dequant_nvfp4_per_head(cache, p.slot_mapping, ks, ks, ko, vo, layout=layout))
+        write()
+    else:
+        g = np.random.Generator(np.random.PCG64(4001))
+        lens = g.integers(4096, 32768, 64, endpoint=True)
+        table = torch.from_numpy(wl.make_gather_batch(65536, 64, lens, [0] * 64, 4001)[0]).to(dev)
+        req = g.integers(0, 64, 4096).astype(np.int32)
+        idx = (g.random((4096, 2048)) * lens[req][:, None]).astype(np.int32)
+        idx[g.random((4096, 2048)) < 0.1] = -1
+        r, i = torch.from_numpy(req).to(dev), torch.from_numpy(idx).to(dev)
+        o = torch.empty((4096, 2048), dtype=torch.int32, device=dev)
+        fn = lambda: kvq.kvq_req_index_to_global_slot(r, i, table, 64, 65536, out=o)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        print(f"{name}: {a.elapsed_time(b) * 1e3:.1f} us", flush=True)
+    return 0
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -779,9 +877,19 @@ def main(argv=None):
     p.add_argument("--attention-only", type=int, default=0, metavar="T",
                    help="profiler hook: T decode tokens of the sparse MLA attention (128 heads, top-2048 "
                         "over an 8192 x 64 cache), 3 launches, times printed; nothing else runs")
+    p.add_argument("--prefill-only", type=int, default=0, metavar="Q",
+                   help="profiler hook: the dense prefill alone, 8 requests with contexts of 4k-16k, Q new "
+                        "tokens x 128 heads each, over an 8192 x 64 cache, 3 launches; nothing else runs")
+    p.add_argument("--kernel-only", choices=KERNEL_ONLY, default=None,
+                   help="profiler hook: one kernel of the extra measurements, 3 launches on its own "
+                        "workload, times printed; nothing else runs")
     args = p.parse_args(argv)
     if args.attention_only > 0:
         return run_attention_only(args.attention_only)
+    if args.kernel_only:
+        return run_kernel_only(args.kernel_only)
+    if args.prefill_only > 0:
+        return run_prefill_only(args.prefill_only)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:

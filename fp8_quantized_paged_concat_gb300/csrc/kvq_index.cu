@@ -10,6 +10,8 @@
 // take 4 x 4 consecutive positions (16-byte loads and stores, all four loads
 // in flight together; 4 x 1 position when rows are not 16-byte aligned).
 // Rows wider than the staging limit read the table from global memory.
+#include <type_traits>
+
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
 
@@ -46,46 +48,40 @@ template <int kVec, bool kStaged>
 __global__ void __launch_bounds__(kThreads) req_index_to_global_slot_kernel(const IndexArgs a) {
   extern __shared__ int32_t s_row[];
   const int64_t i = blockIdx.x;                                   // token
+  // kLoads accesses of kVec positions per thread, kThreads * kVec apart
+  // (coalesced).  They do not depend on the request, so they are issued
+  // first and their latency overlaps the block-table staging.
+  const int64_t k0 = (static_cast<int64_t>(blockIdx.y) * kThreads * kLoads + threadIdx.x) * kVec;
+  const int32_t* src = a.token_indices + i * a.token_indices_stride;
+  int32_t* dst = a.out + i * a.out_stride;
+  using Vec = typename std::conditional<kVec == 4, int4, int32_t>::type;
+  Vec p[kLoads];
+#pragma unroll
+  for (int u = 0; u < kLoads; ++u) {
+    const int64_t k = k0 + u * kThreads * kVec;
+    if (k < a.topk) p[u] = __ldcs(reinterpret_cast<const Vec*>(src + k));
+  }
   const int32_t r = __ldg(a.req_id + i);
   const bool valid_req = r >= 0 && r < a.num_requests;
   const int32_t* g_row = valid_req ? a.block_table + static_cast<int64_t>(r) * a.block_table_stride : nullptr;
   if constexpr (kStaged) {
-    if (valid_req)
+    if (valid_req) {
+#pragma unroll 4
       for (int c = threadIdx.x; c < a.block_table_width; c += kThreads) s_row[c] = __ldg(g_row + c);
+    }
     __syncthreads();
   }
-  // kLoads accesses of kVec positions per thread, kThreads * kVec apart
-  // (coalesced), all loads issued before any use
-  const int64_t k0 = (static_cast<int64_t>(blockIdx.y) * kThreads * kLoads + threadIdx.x) * kVec;
-  const int32_t* src = a.token_indices + i * a.token_indices_stride;
-  int32_t* dst = a.out + i * a.out_stride;
   const int32_t* row = valid_req ? (kStaged ? s_row : g_row) : nullptr;
-  if constexpr (kVec == 4) {
-    int4 p[kLoads];
 #pragma unroll
-    for (int u = 0; u < kLoads; ++u) {
-      const int64_t k = k0 + u * kThreads * kVec;
-      if (k < a.topk) p[u] = __ldcs(reinterpret_cast<const int4*>(src + k));
-    }
-#pragma unroll
-    for (int u = 0; u < kLoads; ++u) {
-      const int64_t k = k0 + u * kThreads * kVec;
-      if (k < a.topk)
-        __stcs(reinterpret_cast<int4*>(dst + k),
-               make_int4(global_slot(a, row, p[u].x), global_slot(a, row, p[u].y), global_slot(a, row, p[u].z),
-                         global_slot(a, row, p[u].w)));
-    }
-  } else {
-    int32_t p[kLoads];
-#pragma unroll
-    for (int u = 0; u < kLoads; ++u) {
-      const int64_t k = k0 + u * kThreads;
-      if (k < a.topk) p[u] = __ldcs(src + k);
-    }
-#pragma unroll
-    for (int u = 0; u < kLoads; ++u) {
-      const int64_t k = k0 + u * kThreads;
-      if (k < a.topk) __stcs(dst + k, global_slot(a, row, p[u]));
+  for (int u = 0; u < kLoads; ++u) {
+    const int64_t k = k0 + u * kThreads * kVec;
+    if (k >= a.topk) continue;
+    if constexpr (kVec == 4) {
+      __stcs(reinterpret_cast<int4*>(dst + k),
+             make_int4(global_slot(a, row, p[u].x), global_slot(a, row, p[u].y), global_slot(a, row, p[u].z),
+                       global_slot(a, row, p[u].w)));
+    } else {
+      __stcs(dst + k, global_slot(a, row, p[u]));
     }
   }
 }
