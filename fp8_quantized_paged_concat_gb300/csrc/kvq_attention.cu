@@ -36,9 +36,11 @@
 //     of this CTA uses (2 stages, free again once their K-steps are done);
 //     key tile group B, this CTA's own 256 dimensions, which are also the V
 //     operand of P V (2 stages, free once P V is done);
-//   - four producer warps decode group A of each 64-key tile and four decode
-//     group B (e2m1 x e4m3 products formed exactly by byte-permute table
+//   - eight producer warps decode group A of each 64-key tile, then group B,
+//     8 rows each (e2m1 x e4m3 products formed exactly by byte-permute table
 //     lookups; fp8 codes times their tile scale as the fp8 gather does);
+//     group B of tile t is decoded as soon as P V of tile t - 2 is done,
+//     while the 20 group-A K-steps of tile t run;
 //   - one thread issues the MMAs: S(u) = the 20 group-A K-steps and the 16
 //     group-B K-steps of Q K^T, then O += P(t) V(t) (4 K-steps, N = 256), in
 //     the order S(0), S(1), PV(0), S(2), PV(1), ...: the 36 K-steps of the
@@ -65,13 +67,11 @@ constexpr int kHalf = KVQ_MLA_NOPE_DIM / 2;                  // 256 value column
 constexpr int kRows = 128;                                   // query rows per CTA
 constexpr int kTile = 64;                                    // keys per tile (N of Q K^T)
 // Warp roles: 0-3 softmax (warp w: TMEM lanes 32 w .. +31), 4-11 producers,
-// 12 MMA (one thread).  Warp w runs on SM sub-partition w % 4: the group-A
-// producers are warps 4, 5, 8, 9 (sub-partitions 0 and 1) and the group-B
-// producers warps 6, 7, 10, 11 (sub-partitions 2 and 3), so a sub-partition
-// runs the softmax and one decode loop, not both.  13 warps put at most 4 on
-// a sub-partition: 128 registers per thread.
+// 12 MMA (one thread).  13 warps put at most 4 on an SM sub-partition: 128
+// registers per thread.
 constexpr int kSoftmaxWarps = 4;
 constexpr int kFirstProducerWarp = 4;
+constexpr int kProducerWarps = 8;
 constexpr int kMmaWarp = 12;
 constexpr int kThreads = 13 * 32;                            // 416
 constexpr int kNvRopeOff = 256, kNvSfOff = 320;              // nvfp4_ds_mla entry
@@ -464,103 +464,94 @@ __device__ __forceinline__ const uint8_t* key_entry(const AttentionArgs& a, int3
 }
 
 // ---------------------------------------------------------------------------
-// producers: one group of a key tile each
+// producers: both groups of every key tile, 8 rows per warp
 // ---------------------------------------------------------------------------
 //
-// Producer thread (w, lane) of either group takes tile row r = 16 w + lane %
-// 16 and h = lane / 16: the NoPE blocks 2h and 2h + 1 of its group (128
-// dimensions), and in group A also the RoPE dimensions [32 h, 32 h + 32).
-// The 8 lanes of a quarter warp write 8 consecutive rows of one block, whose
-// 128-byte swizzle puts a given 16-byte chunk in 8 different bank groups.
-// Group A's NoPE blocks are the other half's dimensions 256 (1 - c) ..,
-// group B's the CTA's own 256 c .. .
+// Producer thread (w, lane) takes tile row r = 8 w + lane % 8 and k = lane /
+// 8: of group A the other half's NoPE block k (dimensions 256 (1 - c) + 64 k
+// .. +64) and the RoPE dimensions 16 k .. +16, of group B the own NoPE block
+// k (256 c + 64 k .. +64).  All eight warps decode group A of a tile, then
+// group B, so a group's decode is spread over all of them.  The 8 lanes of a
+// quarter warp write 8 consecutive rows of one block, whose 128-byte swizzle
+// puts a given 16-byte chunk in 8 different bank groups.
 
-template <Entry F> struct HalfRegs;
-template <> struct HalfRegs<Entry::kNvfp4> {
-  uint4 code[4];                         // 128 e2m1 codes (8 groups)
-  uint2 sf;                              // their 8 e4m3 scales
-  uint4 rope[2];                         // group A: 32 e4m3 RoPE values
+template <Entry F, bool kRope> struct PartRegs;
+template <bool kRope> struct PartRegs<Entry::kNvfp4, kRope> {
+  uint4 code[2];                         // 64 e2m1 codes (4 groups)
+  uint32_t sf;                           // their 4 e4m3 scales
+  uint4 rope;                            // group A: 16 e4m3 RoPE values
 };
-template <> struct HalfRegs<Entry::kFp8> {
-  uint4 code[8];                         // 128 e4m3 codes
+template <bool kRope> struct PartRegs<Entry::kFp8, kRope> {
+  uint4 code[4];                         // 64 e4m3 codes
   float sc;                              // the scale of their 128-value tile
-  uint4 rope[4];                         // group A: 32 bf16 RoPE values
+  uint4 rope[2];                         // group A: 16 bf16 RoPE values
 };
 
 // Issues the loads of this thread's share of one key's entry (p = nullptr:
-// nothing to load).  `nope0` is the first NoPE dimension of the thread's 128.
+// nothing to load): NoPE dimensions nope0 .. nope0 + 63 and, with kRope, the
+// RoPE dimensions 16 k .. 16 k + 15.
 template <Entry F, bool kRope>
-__device__ __forceinline__ void load_half(const uint8_t* p, int nope0, int h, HalfRegs<F>& e) {
+__device__ __forceinline__ void load_part(const uint8_t* p, int nope0, int k, PartRegs<F, kRope>& e) {
   if (p == nullptr) return;
   if constexpr (F == Entry::kNvfp4) {
     const uint4* c = reinterpret_cast<const uint4*>(p + nope0 / 2);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) e.code[i] = __ldg(c + i);
-    e.sf = __ldg(reinterpret_cast<const uint2*>(p + kNvSfOff + nope0 / 16));
-    if constexpr (kRope) {
-      const uint4* r = reinterpret_cast<const uint4*>(p + kNvRopeOff + 32 * h);
-      e.rope[0] = __ldg(r);
-      e.rope[1] = __ldg(r + 1);
-    }
+    e.code[0] = __ldg(c);
+    e.code[1] = __ldg(c + 1);
+    e.sf = __ldg(reinterpret_cast<const uint32_t*>(p + kNvSfOff + nope0 / 16));
+    if constexpr (kRope) e.rope = __ldg(reinterpret_cast<const uint4*>(p + kNvRopeOff + 16 * k));
   } else {
     const uint4* c = reinterpret_cast<const uint4*>(p + nope0);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) e.code[i] = __ldg(c + i);
+    for (int i = 0; i < 4; ++i) e.code[i] = __ldg(c + i);
     e.sc = __ldg(reinterpret_cast<const float*>(p + kF8ScaleOff) + nope0 / 128);
     if constexpr (kRope) {
-      const uint4* r = reinterpret_cast<const uint4*>(p + kF8RopeOff + 64 * h);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) e.rope[i] = __ldg(r + i);
+      const uint4* r = reinterpret_cast<const uint4*>(p + kF8RopeOff + 32 * k);
+      e.rope[0] = __ldg(r);
+      e.rope[1] = __ldg(r + 1);
     }
   }
 }
 
-// Decodes and stores this thread's share of tile row r: NoPE blocks b0 and
-// b0 + 1 of the buffer at `buf`, and with kRope the RoPE chunks 4h .. 4h + 3
-// of the block at `rope_blk`.  An unused key stores zeros.
+// Decodes and stores this thread's share of tile row r: NoPE block `blk`
+// (chunks 0-7) and, with kRope, RoPE chunks 2k, 2k + 1 of the block at
+// `rope_blk`.  An unused key stores zeros.
 template <Entry F, bool kRope>
-__device__ __forceinline__ void store_half(uint32_t buf, int b0, uint32_t rope_blk, uint32_t r, int h, bool valid,
-                                           const HalfRegs<F>& e) {
+__device__ __forceinline__ void store_part(uint32_t blk, uint32_t rope_blk, uint32_t r, int k, bool valid,
+                                           const PartRegs<F, kRope>& e) {
+  // the four 16-value groups decoded into registers first (they are
+  // independent), then stored: chunks 2g, 2g + 1 hold group g
+  uint4 v[10];
 #pragma unroll
-  for (int blk = 0; blk < 2; ++blk) {
-    const uint32_t base = buf + (b0 + blk) * kKBlock;
-    // the block's four 16-value groups decoded into registers first (they
-    // are independent), then stored: chunks 2g, 2g + 1 hold group g
-    uint4 v[8];
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      v[2 * g] = v[2 * g + 1] = make_uint4(0, 0, 0, 0);
-      if (valid) {
-        if constexpr (F == Entry::kNvfp4) {
-          const int gg = 4 * blk + g;                  // group of the thread's 8
-          const GroupTable t = group_table(((gg < 4 ? e.sf.x : e.sf.y) >> (8 * (gg & 3))) & 0xffu);
-          const uint4& c = e.code[gg >> 1];
-          v[2 * g] = e2m1x8_bf16((gg & 1) ? c.z : c.x, t);
-          v[2 * g + 1] = e2m1x8_bf16((gg & 1) ? c.w : c.y, t);
-        } else {
-          e4m3x16_scaled(e.code[4 * blk + g], e.sc, v[2 * g], v[2 * g + 1]);
-        }
+  for (int g = 0; g < 4; ++g) {
+    v[2 * g] = v[2 * g + 1] = make_uint4(0, 0, 0, 0);
+    if (valid) {
+      if constexpr (F == Entry::kNvfp4) {
+        const GroupTable t = group_table((e.sf >> (8 * g)) & 0xffu);
+        const uint4& c = e.code[g >> 1];
+        v[2 * g] = e2m1x8_bf16((g & 1) ? c.z : c.x, t);
+        v[2 * g + 1] = e2m1x8_bf16((g & 1) ? c.w : c.y, t);
+      } else {
+        e4m3x16_scaled(e.code[g], e.sc, v[2 * g], v[2 * g + 1]);
       }
     }
-#pragma unroll
-    for (int c = 0; c < 8; ++c) st_shared16(base + sw128_offset(r, c), v[c]);
   }
   if constexpr (kRope) {
-    uint4 v[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {                      // RoPE dims 32h + 8i .. +7 = chunk 4h + i
-      v[i] = make_uint4(0, 0, 0, 0);
-      if (valid) {
-        if constexpr (F == Entry::kNvfp4) {
-          const uint4& q = e.rope[i >> 1];
-          v[i] = e4m3x8_bf16((i & 1) ? make_uint2(q.z, q.w) : make_uint2(q.x, q.y));
-        } else {
-          v[i] = e.rope[i];                            // bf16 as stored
-        }
+    v[8] = v[9] = make_uint4(0, 0, 0, 0);
+    if (valid) {
+      if constexpr (F == Entry::kNvfp4) {
+        v[8] = e4m3x8_bf16(make_uint2(e.rope.x, e.rope.y));
+        v[9] = e4m3x8_bf16(make_uint2(e.rope.z, e.rope.w));
+      } else {
+        v[8] = e.rope[0];                              // bf16 as stored
+        v[9] = e.rope[1];
       }
     }
+  }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) st_shared16(rope_blk + sw128_offset(r, 4 * h + i), v[i]);
+  for (int c = 0; c < 8; ++c) st_shared16(blk + sw128_offset(r, c), v[c]);
+  if constexpr (kRope) {
+    st_shared16(rope_blk + sw128_offset(r, 2 * k), v[8]);
+    st_shared16(rope_blk + sw128_offset(r, 2 * k + 1), v[9]);
   }
 }
 
@@ -592,11 +583,11 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
   }
   if (threadIdx.x == 32) {
     for (int s = 0; s < kAStages; ++s) {
-      mbar_init(a_full0 + 8 * s, 4);
+      mbar_init(a_full0 + 8 * s, kProducerWarps);
       mbar_init(a_empty0 + 8 * s, 1);
     }
     for (int s = 0; s < kBStages; ++s) {
-      mbar_init(b_full0 + 8 * s, 4);
+      mbar_init(b_full0 + 8 * s, kProducerWarps);
       mbar_init(b_empty0 + 8 * s, 1);
     }
     for (int s = 0; s < 2; ++s) mbar_init(s_full0 + 8 * s, 1);
@@ -741,54 +732,47 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
       raw2_hi = key_raw<K>(a, blk, (t + 2) * kTile + 32 + lane);
     }
   } else if (warp < kMmaWarp) {
-    // ---- producers: group A (warps 4, 5, 8, 9) or group B (6, 7, 10, 11) ----
-    const bool group_a = (warp & 2) == 0;
-    const int pw = ((warp - kFirstProducerWarp) >> 2) * 2 + (warp & 1);     // 0..3 within the group
-    const uint32_t r = 16 * pw + (lane & 15);
-    const int h = lane >> 4;
-    const int nope0 = (group_a ? other : own) + 128 * h;
-    // A tile's loads are issued right after the tile before it is handed
-    // over, and their latency hides behind the wait for its buffer.  (Loads
-    // go after the arrive: a release waits for every access of the thread in
-    // flight.)
+    // ---- producers: group A, then group B, of every tile ----------------------
+    const int pw = warp - kFirstProducerWarp;
+    const uint32_t r = 8 * pw + (lane & 7);
+    const int k = lane >> 3;
+    const int a_nope0 = other + 64 * k, b_nope0 = own + 64 * k;
     // Row r's raw index is loaded two tiles ahead and becomes an entry
-    // address one tile ahead, when the entry's loads are issued.
-    HalfRegs<F> regs;
+    // address one tile ahead, when the entry's loads are issued: a group's
+    // loads for the next tile right after this tile's group is handed over
+    // (a release waits for every access of the thread in flight, so loads go
+    // after an arrive), so that their latency hides behind the other group's
+    // decode and the waits for free stages.
+    PartRegs<F, true> ra;
+    PartRegs<F, false> rb;
     const uint8_t* cur = key_entry<K>(a, key_raw<K>(a, blk, r), r, bad_index);
     int32_t raw_next = key_raw<K>(a, blk, kTile + r), raw_next2 = key_raw<K>(a, blk, 2 * kTile + r);
     if (n_tiles > 0) {
-      if (group_a) load_half<F, true>(cur, nope0, h, regs);
-      else load_half<F, false>(cur, nope0, h, regs);
+      load_part<F, true>(cur, a_nope0, k, ra);
+      load_part<F, false>(cur, b_nope0, k, rb);
     }
-    const uint8_t* next = nullptr;
     for (int t = 0; t < n_tiles; ++t) {
-      if (group_a) {
-        // stage t % kAStages is free once the group-A K-steps of tile
-        // t - kAStages are done
-        const int sa = t % kAStages;
-        if (t >= kAStages && !warp_wait_or_abort(a_empty0 + 8 * sa, (t / kAStages - 1) & 1, s_abort)) break;
-        store_half<F, true>(base + kAOff + sa * kAStage, 2 * h, base + kAOff + sa * kAStage + 4 * kKBlock, r, h,
-                            cur != nullptr, regs);
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(a_full0 + 8 * sa);
-        if (t + 1 < n_tiles) {
-          next = key_entry<K>(a, raw_next, (t + 1) * kTile + r, bad_index);
-          load_half<F, true>(next, nope0, h, regs);
-        }
-      } else {
-        // stage t % kBStages is free once P V of tile t - kBStages is done
-        const int st = t % kBStages;
-        if (t >= kBStages && !warp_wait_or_abort(b_empty0 + 8 * st, (t / kBStages - 1) & 1, s_abort)) break;
-        store_half<F, false>(base + kBOff + st * kBStage, 2 * h, 0, r, h, cur != nullptr, regs);
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b_full0 + 8 * st);
-        if (t + 1 < n_tiles) {
-          next = key_entry<K>(a, raw_next, (t + 1) * kTile + r, bad_index);
-          load_half<F, false>(next, nope0, h, regs);
-        }
-      }
+      // group A: stage t % kAStages is free once the group-A K-steps of tile
+      // t - kAStages are done
+      const int sa = t % kAStages;
+      if (t >= kAStages && !warp_wait_or_abort(a_empty0 + 8 * sa, (t / kAStages - 1) & 1, s_abort)) break;
+      const uint32_t astage = base + kAOff + sa * kAStage;
+      store_part<F, true>(astage + k * kKBlock, astage + 4 * kKBlock, r, k, cur != nullptr, ra);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(a_full0 + 8 * sa);
+      // the next tile's group-A loads now: they are consumed a whole group-B
+      // decode and one wait later
+      const uint8_t* next = t + 1 < n_tiles ? key_entry<K>(a, raw_next, (t + 1) * kTile + r, bad_index) : nullptr;
+      if (t + 1 < n_tiles) load_part<F, true>(next, a_nope0, k, ra);
+      // group B: stage t % kBStages is free once P V of tile t - kBStages is done
+      const int sb = t % kBStages;
+      if (t >= kBStages && !warp_wait_or_abort(b_empty0 + 8 * sb, (t / kBStages - 1) & 1, s_abort)) break;
+      store_part<F, false>(base + kBOff + sb * kBStage + k * kKBlock, 0, r, k, cur != nullptr, rb);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_full0 + 8 * sb);
+      if (t + 1 < n_tiles) load_part<F, false>(next, b_nope0, k, rb);
       cur = next;
       raw_next = raw_next2;
       raw_next2 = key_raw<K>(a, blk, (t + 3) * kTile + r);
