@@ -130,6 +130,7 @@ struct IndexArgs {
   int64_t out_stride;
   int32_t* status;
   FastDiv block_div;              // position -> table column
+  int32_t block_shift;            // log2(block_size) when it is a power of two (set by the launcher)
 };
 cudaError_t launch_req_index_to_global_slot(const IndexArgs& a, cudaStream_t stream);
 cudaError_t launch_selftest_convert(uint32_t first_bits, int64_t count, uint8_t* e4m3_lo,
