@@ -50,16 +50,16 @@ __device__ __forceinline__ uint32_t column_of(const IndexArgs& a, uint32_t p, ui
 }
 
 // Slot of position p given the request's table row (or -1; row == nullptr
-// marks an out-of-range request).  A position that cannot be resolved sets
-// `bad` (reported once per warp by the caller).
+// marks an out-of-range request).  A position >= 0 that cannot be resolved
+// sets `bad` (reported once per warp by the caller).
 template <bool kPow2, typename Row>
-__device__ __forceinline__ int32_t global_slot(const IndexArgs& a, Row row, int32_t p, bool& bad) {
-  if (p < 0) return -1;
+__device__ __forceinline__ int32_t global_slot(const IndexArgs& a, Row row, int32_t p, int32_t num_blocks, bool& bad) {
+  // branch-free: a negative (unused) position gives -1 and is not an error
   uint32_t off;
-  const uint32_t col = column_of<kPow2>(a, static_cast<uint32_t>(p), off);
+  const uint32_t col = column_of<kPow2>(a, static_cast<uint32_t>(p), off);   // huge for p < 0
   const int32_t blk = (row != nullptr && col < static_cast<uint32_t>(a.block_table_width)) ? row[col] : -1;
-  const bool ok = blk >= 0 && blk < a.num_blocks;
-  bad |= !ok;
+  const bool ok = blk >= 0 && blk < num_blocks;
+  bad |= !ok && p >= 0;
   return ok ? blk * a.block_size + static_cast<int32_t>(off) : -1;
 }
 
@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(kThreads) req_index_to_global_slot_kernel(cons
   }
   if constexpr (kStaged) __syncthreads();
   bool bad = false;
+  const int32_t nb = static_cast<int32_t>(a.num_blocks);         // < 2^31 (host check)
 #pragma unroll
   for (int j = 0; j < kTokens; ++j) {
     if (i0 + j >= a.num_tokens) continue;
@@ -114,10 +115,12 @@ __global__ void __launch_bounds__(kThreads) req_index_to_global_slot_kernel(cons
       if (k >= a.topk) continue;
       if constexpr (kVec == 4) {
         __stcs(reinterpret_cast<int4*>(dst + k),
-               make_int4(global_slot<kPow2>(a, rows[j], p[j][u].x, bad), global_slot<kPow2>(a, rows[j], p[j][u].y, bad),
-                         global_slot<kPow2>(a, rows[j], p[j][u].z, bad), global_slot<kPow2>(a, rows[j], p[j][u].w, bad)));
+               make_int4(global_slot<kPow2>(a, rows[j], p[j][u].x, nb, bad),
+                         global_slot<kPow2>(a, rows[j], p[j][u].y, nb, bad),
+                         global_slot<kPow2>(a, rows[j], p[j][u].z, nb, bad),
+                         global_slot<kPow2>(a, rows[j], p[j][u].w, nb, bad)));
       } else {
-        __stcs(dst + k, global_slot<kPow2>(a, rows[j], p[j][u], bad));
+        __stcs(dst + k, global_slot<kPow2>(a, rows[j], p[j][u], nb, bad));
       }
     }
   }
