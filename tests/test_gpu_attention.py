@@ -445,3 +445,33 @@ def test_prefill_matches_sparse_form(kvq, oracle_mod, fmt):
     # with unused entries to the longest context, which adds only masked tiles
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
     assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
+
+
+@pytest.mark.parametrize("fmt", sorted(PREFILL_FORMATS))
+def test_prefill_full_size_sampled(kvq, oracle_mod, threads, fmt):
+    """The bench's prefill workload (every request of the prefill gather -- or
+    of the fp8 gather -- attends with 16 new tokens x 128 heads to its whole
+    context through the gather's block table) in one launch; the first two
+    tokens of the request with the shortest and of one with a middle-sized
+    context are checked against the oracle."""
+    if fmt == "nvfp4":
+        gather = wl.prefill_gather(DEV)
+    else:
+        gather = wl.fp8_gather(DEV)
+    w = wl.prefill_attention(gather, DEV)
+    cache_host = host_cache(oracle_mod, gather.fill, threads, fmt)
+    cache = torch.from_numpy(cache_host).to(DEV)
+    del gather
+    out, lse = getattr(kvq, PREFILL_FORMATS[fmt][1])(w.q, w.query_start, w.context_lens, w.block_table, cache,
+                                                      w.softmax_scale, w.max_query_len)
+    torch.cuda.synchronize()
+    ctx = wl.host(w.context_lens)
+    order = np.argsort(ctx)
+    picks = [int(order[0]), int(order[len(order) // 2])]
+    # the sampled requests cut down to their first two query tokens
+    qs = wl.host(w.query_start)
+    keep = torch.from_numpy(np.concatenate([np.arange(qs[b], qs[b] + 2) for b in picks])).to(DEV)
+    sub = wl.PrefillWorkload("sampled", None, w.q[keep].cpu(), torch.tensor([0, 2, 4], dtype=torch.int32),
+                             torch.from_numpy(ctx[picks].astype(np.int32)),
+                             torch.from_numpy(wl.host(w.block_table)[picks]), w.softmax_scale, 2)
+    check_prefill(oracle_mod, cache_host, sub, out[keep].cpu(), lse[keep].cpu(), threads)

@@ -5,12 +5,10 @@ The kernel waits only through mbarriers, each wait with an iteration limit.
 A build of the library used only here (KVQ_ATTN_STALL_TILE) makes the MMA
 thread stop issuing at tile 2 of 4, as if its tensor work never completed, and
 shortens the role waits' limit (KVQ_ATTN_WAIT_CYCLES, about 10 ms) so that
-the test is quick; the final waits (for the CTA's own MMAs in flight and for
-the peer CTA's copies still landing in its shared memory) keep their own long
-limit.  Nothing hangs: the waits that nothing will satisfy run out, every role
-takes the abort path, the kernel drains its MMAs and the copies in flight,
-frees its tensor memory, meets its peer at the final cluster barrier and
-returns.
+the test is quick; the final wait (for the CTA's own MMAs in flight) keeps its
+own long limit.  Nothing hangs: the waits that nothing will satisfy run out,
+every role takes the abort path, the kernel drains the MMAs it issued, frees
+its tensor memory and returns.
 
 Checked, in a process of its own: the call returns, KVQ_STATUS_TIMEOUT is set,
 the outputs (out and lse) are untouched, and the normal library then gives a
