@@ -98,6 +98,8 @@ constexpr uint32_t kBStage = 4 * kKBlock;
 constexpr uint32_t kMiscOff = kBOff + kBStages * kBStage;
 constexpr uint32_t kSmemBytes = kMiscOff + 256 + 1024;       // + barriers, flags, alignment
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
+static_assert(kAStages * kAStage >= kRows * 512 && kBStages * kBStage >= 4 * kQBlock,
+              "the output staging fits the group-A stages, the own query staging the group-B stages");
 static_assert(kAOff % 1024 == 0 && kBOff % 1024 == 0 && kAStage % 1024 == 0 && kBStage % 1024 == 0,
               "1024-byte swizzle atoms");
 
@@ -273,6 +275,20 @@ __device__ __forceinline__ void st_shared16(uint32_t addr, const uint4& v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
 }
+
+__device__ __forceinline__ uint4 ld_shared16(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
+// 16 bytes global -> shared without passing through registers; with
+// src_bytes = 0 nothing is read and the 16 bytes are zero-filled.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // 2^x for x <= 0 (0 for -inf): the hardware approximation, relative error
 // below 2^-22, flushed to zero below 2^-126 (weights that small vanish next
@@ -598,44 +614,69 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
 
-  // The other half's 256 NoPE query dimensions and the 64 RoPE dimensions ->
-  // five 128-byte-swizzled K-major blocks (rows past the block's rows are zero).
+  // Query rows -> shared memory by asynchronous copies, all in flight at
+  // once: the other half's 256 NoPE dimensions and the 64 RoPE dimensions as
+  // five 128-byte-swizzled K-major blocks (the A operand of the group-A
+  // K-steps), and the CTA's own 256 NoPE dimensions staged in the same layout
+  // in the group-B stages (idle until the first key tile) on their way to
+  // TMEM.  Rows past the block's rows are zero-filled.
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-  for (int i = threadIdx.x; i < kRows * 5 * 8; i += kThreads) {
-    const int row = i / 40, rem = i % 40, j = rem >> 3, c = rem & 7;
-    uint4 v = make_uint4(0, 0, 0, 0);
+  for (int i = threadIdx.x; i < kRows * 9 * 8; i += kThreads) {
+    const int row = i / 72, rem = i % 72, j = rem >> 3, c = rem & 7;   // block j: 0-3 other, 4 RoPE, 5-8 own
+    const __nv_bfloat16* src = q;
+    uint32_t bytes = 0;
     if (row < blk.rows) {
       int64_t token;
       int32_t head;
       row_of<K>(a, blk, row, token, head);
-      const int dim = j < 4 ? other + 64 * j + 8 * c : KVQ_MLA_NOPE_DIM + 8 * c;
-      v = __ldg(reinterpret_cast<const uint4*>(q + token * a.q_stride_t + head * a.q_stride_h + dim));
+      const int dim = j < 4 ? other + 64 * j : j == 4 ? KVQ_MLA_NOPE_DIM : own + 64 * (j - 5);
+      src = q + token * a.q_stride_t + head * a.q_stride_h + dim + 8 * c;
+      bytes = 16;
     }
-    st_shared16(base + kQOff + j * kQBlock + sw128_offset(row, c), v);
+    const uint32_t blk_base = j < 5 ? base + kQOff + j * kQBlock : base + kBOff + (j - 5) * kQBlock;
+    cp_async16(blk_base + sw128_offset(row, c), src, bytes);
   }
+
+  const int n_tiles = (blk.n_keys + kTile - 1) / kTile;
+  bool bad_index = false;
+  const bool is_softmax = warp < kSoftmaxWarps;
+  const bool is_producer = warp >= kFirstProducerWarp && warp < kMmaWarp;
+  // Producer row r of a tile, dimension block k of its parts (see below).
+  const uint32_t r = 8 * (warp - kFirstProducerWarp) + (lane & 7);
+  const int k = lane >> 3;
+  const int a_nope0 = other + 64 * k, b_nope0 = own + 64 * k;
+  // Row r's raw index is loaded two tiles ahead and becomes an entry address
+  // one tile ahead, when the entry's loads are issued; the first tile's are
+  // issued here, while the query copies land.
+  PartRegs<F, true> ra;
+  PartRegs<F, false> rb;
+  const uint8_t* cur = nullptr;
+  int32_t raw_next = 0, raw_next2 = 0;
+  if (is_producer) {
+    cur = key_entry<K>(a, key_raw<K>(a, blk, r), r, bad_index);
+    raw_next = key_raw<K>(a, blk, kTile + r);
+    raw_next2 = key_raw<K>(a, blk, 2 * kTile + r);
+    if (n_tiles > 0) {
+      load_part<F, true>(cur, a_nope0, k, ra);
+      load_part<F, false>(cur, b_nope0, k, rb);
+    }
+  }
+  cp_async_wait_all();
   fence_async_smem();
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *s_tmem;
-  const bool is_softmax = warp < kSoftmaxWarps;
-  // The CTA's own 256 NoPE query dimensions -> TMEM (softmax warp w: lane =
-  // row 32 w + lane).
+  // The CTA's own 256 NoPE query dimensions: staging -> TMEM (softmax warp w:
+  // lane = row 32 w + lane).
   if (is_softmax) {
-    const int row = warp * 32 + lane;
-    const uint4* src = nullptr;
-    if (row < blk.rows) {
-      int64_t token;
-      int32_t head;
-      row_of<K>(a, blk, row, token, head);
-      src = reinterpret_cast<const uint4*>(q + token * a.q_stride_t + head * a.q_stride_h + own);
-    }
+    const uint32_t row = warp * 32 + lane;
 #pragma unroll 1
     for (int part = 0; part < 4; ++part) {            // 64 dims = 32 columns per part
       float w[32];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const uint4 v = src != nullptr ? __ldg(src + 8 * part + i) : make_uint4(0, 0, 0, 0);
+        const uint4 v = ld_shared16(base + kBOff + part * kQBlock + sw128_offset(row, i));
         w[4 * i] = __uint_as_float(v.x);
         w[4 * i + 1] = __uint_as_float(v.y);
         w[4 * i + 2] = __uint_as_float(v.z);
@@ -648,8 +689,6 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
   __syncthreads();
   fence_after_sync();
 
-  const int n_tiles = (blk.n_keys + kTile - 1) / kTile;
-  bool bad_index = false;
   int mma_issued = 0;                    // MMA thread: any MMA issued
   float m = -INFINITY, l = 0.0f;         // softmax: reference max (base 2), partial sum of the row
 
@@ -733,24 +772,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
     }
   } else if (warp < kMmaWarp) {
     // ---- producers: group A, then group B, of every tile ----------------------
-    const int pw = warp - kFirstProducerWarp;
-    const uint32_t r = 8 * pw + (lane & 7);
-    const int k = lane >> 3;
-    const int a_nope0 = other + 64 * k, b_nope0 = own + 64 * k;
-    // Row r's raw index is loaded two tiles ahead and becomes an entry
-    // address one tile ahead, when the entry's loads are issued: a group's
-    // loads for the next tile right after this tile's group is handed over
-    // (a release waits for every access of the thread in flight, so loads go
-    // after an arrive), so that their latency hides behind the other group's
-    // decode and the waits for free stages.
-    PartRegs<F, true> ra;
-    PartRegs<F, false> rb;
-    const uint8_t* cur = key_entry<K>(a, key_raw<K>(a, blk, r), r, bad_index);
-    int32_t raw_next = key_raw<K>(a, blk, kTile + r), raw_next2 = key_raw<K>(a, blk, 2 * kTile + r);
-    if (n_tiles > 0) {
-      load_part<F, true>(cur, a_nope0, k, ra);
-      load_part<F, false>(cur, b_nope0, k, rb);
-    }
+    // A group's loads for the next tile are issued right after this tile's
+    // group is handed over (a release waits for every access of the thread in
+    // flight, so loads go after an arrive), so that their latency hides
+    // behind the other group's decode and the waits for free stages.
     for (int t = 0; t < n_tiles; ++t) {
       // group A: stage t % kAStages is free once the group-A K-steps of tile
       // t - kAStages are done
@@ -857,33 +882,46 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
   if (aborted && threadIdx.x == 0 && a.status) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
 
   if (is_softmax && !aborted) {
+    // Each thread scales its row's 256 O columns into bf16 and writes them as
+    // a 512-byte row of a staging area in the (now idle) group-A stages, its
+    // 16-byte chunks rotated by XOR with row % 32 so that a warp's stores hit
+    // distinct banks; the warp then writes its 32 rows out one whole row (512
+    // contiguous bytes) per instruction.
     const uint32_t row_lane = warp * 32u << 16;
-    const int row = warp * 32 + lane;
+    const uint32_t row = warp * 32 + lane;
     const float l_row = l;
     const float inv_l = l_row > 0.0f ? 1.0f / l_row : 0.0f;
     int64_t token = 0;
     int32_t head = 0;
-    if (row < blk.rows) row_of<K>(a, blk, row, token, head);
+    const bool live = row < static_cast<uint32_t>(blk.rows);
+    if (live) row_of<K>(a, blk, row, token, head);
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + token * a.out_stride_t +
                          static_cast<int64_t>(head) * a.out_stride_h + own;
+    const uint32_t stage = base + kAOff;
 #pragma unroll 1
     for (int c = 0; c < kHalf / 32; ++c) {
       float o[32];
       if (n_tiles > 0) tmem_ld32(tmem + row_lane + kOCol + 32 * c, o);
-      if (row < blk.rows) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (n_tiles > 0)
-            v = make_uint4(pack_bf16x2(o[8 * i] * inv_l, o[8 * i + 1] * inv_l),
-                           pack_bf16x2(o[8 * i + 2] * inv_l, o[8 * i + 3] * inv_l),
-                           pack_bf16x2(o[8 * i + 4] * inv_l, o[8 * i + 5] * inv_l),
-                           pack_bf16x2(o[8 * i + 6] * inv_l, o[8 * i + 7] * inv_l));
-          *reinterpret_cast<uint4*>(out + 32 * c + 8 * i) = v;
-        }
+      for (int i = 0; i < 4; ++i) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (n_tiles > 0)
+          v = make_uint4(pack_bf16x2(o[8 * i] * inv_l, o[8 * i + 1] * inv_l),
+                         pack_bf16x2(o[8 * i + 2] * inv_l, o[8 * i + 3] * inv_l),
+                         pack_bf16x2(o[8 * i + 4] * inv_l, o[8 * i + 5] * inv_l),
+                         pack_bf16x2(o[8 * i + 6] * inv_l, o[8 * i + 7] * inv_l));
+        st_shared16(stage + row * 512 + (((4 * c + i) ^ (row & 31)) << 4), v);
       }
     }
-    if (half == 0 && a.lse != nullptr && row < blk.rows)
+    __syncwarp();
+#pragma unroll 4
+    for (int i = 0; i < 32; ++i) {
+      const uint32_t src_row = warp * 32 + i;
+      const auto dst = reinterpret_cast<uint4*>(__shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(out), i));
+      if (__shfl_sync(0xffffffffu, static_cast<int>(live), i))
+        dst[lane] = ld_shared16(stage + src_row * 512 + ((lane ^ i) << 4));
+    }
+    if (half == 0 && a.lse != nullptr && live)
       a.lse[token * a.lse_stride_t + head] =
           l_row > 0.0f ? (m + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
   }
