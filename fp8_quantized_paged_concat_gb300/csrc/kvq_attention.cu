@@ -96,10 +96,15 @@ constexpr uint32_t kAStage = 5 * kKBlock;
 constexpr uint32_t kBOff = kAOff + kAStages * kAStage;       // group B: 4 own-NoPE blocks per stage
 constexpr uint32_t kBStage = 4 * kKBlock;
 constexpr uint32_t kMiscOff = kBOff + kBStages * kBStage;
-constexpr uint32_t kSmemBytes = kMiscOff + 256 + 1024;       // + barriers, flags, alignment
+constexpr uint32_t kBiasOff = kMiscOff + 256;                // per softmax warp: 64 fp32 score biases
+constexpr uint32_t kSmemBytes = kBiasOff + kSoftmaxWarps * 256 + 1024;   // + alignment
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
-static_assert(kAStages * kAStage >= kRows * 512 && kBStages * kBStage >= 4 * kQBlock,
-              "the output staging fits the group-A stages, the own query staging the group-B stages");
+// The key stages (group A then group B, contiguous) are idle before the
+// first tile and after the last: they stage the own query dimensions on their
+// way to TMEM and the output rows on their way out.
+constexpr uint32_t kStagingOff = kAOff;
+static_assert(kMiscOff - kStagingOff >= kRows * 512 && kMiscOff - kStagingOff >= 4 * kQBlock,
+              "the staging fits the key stages");
 static_assert(kAOff % 1024 == 0 && kBOff % 1024 == 0 && kAStage % 1024 == 0 && kBStage % 1024 == 0,
               "1024-byte swizzle atoms");
 
@@ -274,6 +279,10 @@ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
 __device__ __forceinline__ void st_shared16(uint32_t addr, const uint4& v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+}
+
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" :: "r"(addr), "f"(v) : "memory");
 }
 
 __device__ __forceinline__ uint4 ld_shared16(uint32_t addr) {
@@ -528,15 +537,11 @@ __device__ __forceinline__ void load_part(const uint8_t* p, int nope0, int k, Pa
   }
 }
 
-// Decodes and stores this thread's share of tile row r: NoPE block `blk`
-// (chunks 0-7) and, with kRope, RoPE chunks 2k, 2k + 1 of the block at
-// `rope_blk`.  An unused key stores zeros.
+// Decodes this thread's share of a key row into registers: chunks 2g, 2g + 1
+// hold NoPE group g and, with kRope, v[8], v[9] the RoPE values.  An unused
+// key decodes to zeros.
 template <Entry F, bool kRope>
-__device__ __forceinline__ void store_part(uint32_t blk, uint32_t rope_blk, uint32_t r, int k, bool valid,
-                                           const PartRegs<F, kRope>& e) {
-  // the four 16-value groups decoded into registers first (they are
-  // independent), then stored: chunks 2g, 2g + 1 hold group g
-  uint4 v[10];
+__device__ __forceinline__ void decode_part(bool valid, const PartRegs<F, kRope>& e, uint4 (&v)[kRope ? 10 : 8]) {
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     v[2 * g] = v[2 * g + 1] = make_uint4(0, 0, 0, 0);
@@ -563,6 +568,13 @@ __device__ __forceinline__ void store_part(uint32_t blk, uint32_t rope_blk, uint
       }
     }
   }
+}
+
+// Stores a decoded share into tile row r: NoPE block `blk` (chunks 0-7) and,
+// with kRope, RoPE chunks 2k, 2k + 1 of the block at `rope_blk`.
+template <bool kRope>
+__device__ __forceinline__ void write_part(uint32_t blk, uint32_t rope_blk, uint32_t r, int k,
+                                           const uint4 (&v)[kRope ? 10 : 8]) {
 #pragma unroll
   for (int c = 0; c < 8; ++c) st_shared16(blk + sw128_offset(r, c), v[c]);
   if constexpr (kRope) {
@@ -618,8 +630,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
   // once: the other half's 256 NoPE dimensions and the 64 RoPE dimensions as
   // five 128-byte-swizzled K-major blocks (the A operand of the group-A
   // K-steps), and the CTA's own 256 NoPE dimensions staged in the same layout
-  // in the group-B stages (idle until the first key tile) on their way to
-  // TMEM.  Rows past the block's rows are zero-filled.
+  // in the key stages on their way to TMEM.  Rows past the block's rows are
+  // zero-filled.
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
   for (int i = threadIdx.x; i < kRows * 9 * 8; i += kThreads) {
     const int row = i / 72, rem = i % 72, j = rem >> 3, c = rem & 7;   // block j: 0-3 other, 4 RoPE, 5-8 own
@@ -633,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
       src = q + token * a.q_stride_t + head * a.q_stride_h + dim + 8 * c;
       bytes = 16;
     }
-    const uint32_t blk_base = j < 5 ? base + kQOff + j * kQBlock : base + kBOff + (j - 5) * kQBlock;
+    const uint32_t blk_base = j < 5 ? base + kQOff + j * kQBlock : base + kStagingOff + (j - 5) * kQBlock;
     cp_async16(blk_base + sw128_offset(row, c), src, bytes);
   }
 
@@ -676,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
       float w[32];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const uint4 v = ld_shared16(base + kBOff + part * kQBlock + sw128_offset(row, i));
+        const uint4 v = ld_shared16(base + kStagingOff + part * kQBlock + sw128_offset(row, i));
         w[4 * i] = __uint_as_float(v.x);
         w[4 * i + 1] = __uint_as_float(v.y);
         w[4 * i + 2] = __uint_as_float(v.z);
@@ -701,9 +713,16 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
     int32_t raw2_lo = key_raw<K>(a, blk, kTile + lane), raw2_hi = key_raw<K>(a, blk, kTile + 32 + lane);
     // Every wait is bounded and taken by the whole warp; a warp that gives up
     // leaves its loop and meets no other warp before the end.
+    // The tile's key validity is the same for every row: each lane writes the
+    // score bias (0, or -inf for an unused or bad key) of keys lane and 32 +
+    // lane to the warp's bias row, and every lane reads the 64 back as
+    // broadcasts, so that masking costs one fused multiply-add per score pair.
+    const uint32_t bias_row = base + kBiasOff + warp * 256;
     for (int t = 0; t < n_tiles; ++t) {
-      const uint32_t vm_lo = __ballot_sync(0xffffffffu, raw_valid<K>(a, raw1_lo));
-      const uint32_t vm_hi = __ballot_sync(0xffffffffu, raw_valid<K>(a, raw1_hi));
+      __syncwarp();                                             // the last tile's bias reads are done
+      st_shared_f32(bias_row + 4 * lane, raw_valid<K>(a, raw1_lo) ? 0.0f : -INFINITY);
+      st_shared_f32(bias_row + 128 + 4 * lane, raw_valid<K>(a, raw1_hi) ? 0.0f : -INFINITY);
+      __syncwarp();
       const uint32_t sb = t & 1;
       if (!warp_wait_or_abort(s_full0 + 8 * sb, (t >> 1) & 1, s_abort)) break;
       fence_after_sync();
@@ -714,12 +733,18 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 64; i += 2) {
-        const uint32_t vm = i < 32 ? vm_lo : vm_hi;
-        const float2 y = fmul2(make_float2(s[i], s[i + 1]), make_float2(a.scale_log2, a.scale_log2));
-        s[i] = (vm >> (i & 31)) & 1u ? y.x : -INFINITY;
-        s[i + 1] = (vm >> ((i + 1) & 31)) & 1u ? y.y : -INFINITY;
-        mx[(i >> 1) & 7] = fmaxf(mx[(i >> 1) & 7], fmaxf(s[i], s[i + 1]));
+      for (int i = 0; i < 64; i += 4) {
+        const uint4 b = ld_shared16(bias_row + 4 * i);
+        const float2 y0 = ffma2(make_float2(s[i], s[i + 1]), make_float2(a.scale_log2, a.scale_log2),
+                                make_float2(__uint_as_float(b.x), __uint_as_float(b.y)));
+        const float2 y1 = ffma2(make_float2(s[i + 2], s[i + 3]), make_float2(a.scale_log2, a.scale_log2),
+                                make_float2(__uint_as_float(b.z), __uint_as_float(b.w)));
+        s[i] = y0.x;
+        s[i + 1] = y0.y;
+        s[i + 2] = y1.x;
+        s[i + 3] = y1.y;
+        mx[(i >> 1) & 7] = fmaxf(mx[(i >> 1) & 7], fmaxf(y0.x, y0.y));
+        mx[((i >> 1) + 1) & 7] = fmaxf(mx[((i >> 1) + 1) & 7], fmaxf(y1.x, y1.y));
       }
       const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
@@ -777,12 +802,14 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
     // flight, so loads go after an arrive), so that their latency hides
     // behind the other group's decode and the waits for free stages.
     for (int t = 0; t < n_tiles; ++t) {
-      // group A: stage t % kAStages is free once the group-A K-steps of tile
-      // t - kAStages are done
+      // group A: decoded into registers, then stored once stage t % kAStages
+      // is free (the group-A K-steps of tile t - kAStages are done)
+      uint4 va[10];
+      decode_part<F, true>(cur != nullptr, ra, va);
       const int sa = t % kAStages;
       if (t >= kAStages && !warp_wait_or_abort(a_empty0 + 8 * sa, (t / kAStages - 1) & 1, s_abort)) break;
       const uint32_t astage = base + kAOff + sa * kAStage;
-      store_part<F, true>(astage + k * kKBlock, astage + 4 * kKBlock, r, k, cur != nullptr, ra);
+      write_part<true>(astage + k * kKBlock, astage + 4 * kKBlock, r, k, va);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(a_full0 + 8 * sa);
@@ -791,9 +818,11 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
       const uint8_t* next = t + 1 < n_tiles ? key_entry<K>(a, raw_next, (t + 1) * kTile + r, bad_index) : nullptr;
       if (t + 1 < n_tiles) load_part<F, true>(next, a_nope0, k, ra);
       // group B: stage t % kBStages is free once P V of tile t - kBStages is done
+      uint4 vb[8];
+      decode_part<F, false>(cur != nullptr, rb, vb);
       const int sb = t % kBStages;
       if (t >= kBStages && !warp_wait_or_abort(b_empty0 + 8 * sb, (t / kBStages - 1) & 1, s_abort)) break;
-      store_part<F, false>(base + kBOff + sb * kBStage + k * kKBlock, 0, r, k, cur != nullptr, rb);
+      write_part<false>(base + kBOff + sb * kBStage + k * kKBlock, 0, r, k, vb);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_full0 + 8 * sb);
@@ -883,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
 
   if (is_softmax && !aborted) {
     // Each thread scales its row's 256 O columns into bf16 and writes them as
-    // a 512-byte row of a staging area in the (now idle) group-A stages, its
+    // a 512-byte row of a staging area in the (now idle) key stages, its
     // 16-byte chunks rotated by XOR with row % 32 so that a warp's stores hit
     // distinct banks; the warp then writes its 32 rows out one whole row (512
     // contiguous bytes) per instruction.
@@ -897,7 +926,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
     if (live) row_of<K>(a, blk, row, token, head);
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + token * a.out_stride_t +
                          static_cast<int64_t>(head) * a.out_stride_h + own;
-    const uint32_t stage = base + kAOff;
+    const uint32_t stage = base + kStagingOff;
 #pragma unroll 1
     for (int c = 0; c < kHalf / 32; ++c) {
       float o[32];
