@@ -55,7 +55,11 @@
 // the CTA records KVQ_STATUS_TIMEOUT, stops issuing work, waits (with its own
 // long limit) for the MMAs in flight, frees its TMEM, leaves its outputs
 // unwritten and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+
+#include <cstring>
 
 #include "kvq.h"
 #include "kvq_launch.h"
@@ -103,7 +107,8 @@ static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
 // first tile and after the last: they stage the own query dimensions on their
 // way to TMEM and the output rows on their way out.
 constexpr uint32_t kStagingOff = kAOff;
-static_assert(kMiscOff - kStagingOff >= kRows * 512 && kMiscOff - kStagingOff >= 4 * kQBlock,
+constexpr uint32_t kStageRowBytes = 528;                     // an output row (512 bytes) + 16
+static_assert(kMiscOff - kStagingOff >= kRows * kStageRowBytes && kMiscOff - kStagingOff >= 4 * kQBlock,
               "the staging fits the key stages");
 static_assert(kAOff % 1024 == 0 && kBOff % 1024 == 0 && kAStage % 1024 == 0 && kBStage % 1024 == 0,
               "1024-byte swizzle atoms");
@@ -188,6 +193,26 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+
+// Tensor-map tile loads into shared memory, completing on an mbarrier
+// (coordinates innermost first; the innermost one times 2 bytes is a multiple
+// of 16 here).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                            int32_t c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar) : "memory");
+}
+
 // One bounded wait step: the thread sleeps in the barrier (up to about 1 ms,
 // woken when the phase completes) instead of spinning on issue slots.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -235,6 +260,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 64 consecutive fp32 TMEM columns of this warp's 32 lanes in one load.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
@@ -298,6 +344,27 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from shared to global memory by the copy engine, tracked by the thread's
+// bulk group; the thread waits only until its source has been read.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+               :: "l"(dst), "r"(src), "r"(bytes) : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// L2 prefetch hints: `bytes` (a multiple of 16, 16-byte aligned) from addr,
+// or the 128-byte line holding addr.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* addr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(addr), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2_line(const void* addr) {
+  asm volatile("prefetch.global.L2 [%0];" :: "l"(addr) : "memory");
+}
 
 // 2^x for x <= 0 (0 for -inf): the hardware approximation, relative error
 // below 2^-22, flushed to zero below 2^-126 (weights that small vanish next
@@ -400,28 +467,30 @@ struct Block {
   const int32_t* idx;         // sparse: the token's slot list
 };
 
+// The block of CTA (bx, by); `report`: record a skipped request in the
+// status word (only the CTA's own block does).
 template <Keys K>
-__device__ __forceinline__ Block block_of(const AttentionArgs& a) {
+__device__ __forceinline__ Block block_of(const AttentionArgs& a, uint32_t bx, uint32_t by, bool report) {
   Block b{};
   if constexpr (K == Keys::kSparse) {
     b.live = true;
-    b.token0 = blockIdx.x >> 1;
+    b.token0 = bx >> 1;
     b.row0 = 0;
     b.rows = a.num_heads;
     b.n_keys = a.topk;
     b.idx = a.indices + b.token0 * a.indices_stride;
   } else {
-    b.request = blockIdx.y;
+    b.request = static_cast<int32_t>(by);
     const int32_t q0 = __ldg(a.query_start + b.request), q1 = __ldg(a.query_start + b.request + 1);
     if (q0 < 0 || q1 < q0 || q1 > a.num_tokens || q1 - q0 > a.max_query_len) {
       // a request whose query tokens are not inside [0, num_tokens) or longer
       // than max_query_len: skipped
-      if (blockIdx.x == 0 && threadIdx.x == 0 && a.status) atomicOr(a.status, KVQ_STATUS_BAD_BATCH);
+      if (report && bx == 0 && threadIdx.x == 0 && a.status) atomicOr(a.status, KVQ_STATUS_BAD_BATCH);
       b.live = false;
       return b;
     }
     const int64_t total = static_cast<int64_t>(q1 - q0) * a.num_heads;
-    b.row0 = static_cast<int32_t>(blockIdx.x >> 1) * kRows;
+    b.row0 = static_cast<int32_t>(bx >> 1) * kRows;
     b.live = q1 > q0 && b.row0 < total;
     b.token0 = q0;
     b.rows = static_cast<int32_t>(min(static_cast<int64_t>(kRows), total - b.row0));
@@ -442,6 +511,33 @@ __device__ __forceinline__ void row_of(const AttentionArgs& a, const Block& b, i
     const uint32_t tk = a.head_div.div(g);
     token = b.token0 + tk;
     head = static_cast<int32_t>(g - tk * a.head_div.d);
+  }
+}
+
+// The CTAs of a launch run in waves of `a.wave` (one per SM, in launch
+// order), every CTA of this kernel taking about as long as the others, so the
+// CTA that follows this one onto some SM is about `a.wave` places later in
+// launch order.  Halfway through its keys a CTA asks L2 for that CTA's query
+// rows (an even CTA) or its slot list (an odd one), so that the next wave's
+// start-up reads come from L2 and not all at once from HBM.  Only a hint: a
+// wrong guess costs an L2 fill and nothing else.
+template <Keys K>
+__device__ __forceinline__ void prefetch_next_wave(const AttentionArgs& a, uint32_t row) {
+  const uint64_t grid = static_cast<uint64_t>(gridDim.x) * gridDim.y;
+  const uint64_t id = static_cast<uint64_t>(blockIdx.y) * gridDim.x + blockIdx.x + static_cast<uint32_t>(a.wave);
+  if (a.wave <= 0 || id >= grid) return;
+  const Block nb = block_of<K>(a, static_cast<uint32_t>(id % gridDim.x), static_cast<uint32_t>(id / gridDim.x), false);
+  if (!nb.live) return;
+  if ((id & 1) == 0) {
+    if (row < static_cast<uint32_t>(nb.rows)) {
+      int64_t token;
+      int32_t head;
+      row_of<K>(a, nb, static_cast<int>(row), token, head);
+      prefetch_l2_bulk(static_cast<const __nv_bfloat16*>(a.q) + token * a.q_stride_t + head * a.q_stride_h,
+                       KVQ_WORKSPACE_DIM * 2);
+    }
+  } else if constexpr (K == Keys::kSparse) {
+    for (int j = static_cast<int>(row) * 32; j < nb.n_keys; j += kRows * 32) prefetch_l2_line(nb.idx + j);
   }
 }
 
@@ -584,8 +680,9 @@ __device__ __forceinline__ void write_part(uint32_t blk, uint32_t rope_blk, uint
 }
 
 template <Entry F, Keys K>
-__global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const AttentionArgs a) {
-  const Block blk = block_of<K>(a);
+__global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const AttentionArgs a,
+                                                                    const __grid_constant__ CUtensorMap qmap) {
+  const Block blk = block_of<K>(a, blockIdx.x, blockIdx.y, true);
   if (!blk.live) return;                 // uniform over the CTA, before any barrier or allocation
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -599,6 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
   static_assert(16 * kAStages + 16 * kBStages + 40 <= 160, "barriers fit below the flags");
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kMiscOff + 160);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kMiscOff + 164);
+  const uint32_t q_full = bar0 + 168;    // the query rows' tensor-map loads
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t half = blockIdx.x & 1;  // value columns [256 half, +256)
@@ -622,18 +720,34 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
     mbar_init(p_full, kSoftmaxWarps);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
+    mbar_init(q_full, 1);
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (a.q_tma) {
+      // Query rows -> shared memory, nine 16 KB tiles by the copy engine: the
+      // other half's 256 NoPE dimensions and the 64 RoPE dimensions as five
+      // 128-byte-swizzled K-major blocks (the A operand of the group-A
+      // K-steps), and the CTA's own 256 NoPE dimensions staged in the same
+      // layout in the key stages on their way to TMEM.  Rows past the tensor
+      // are zero-filled; rows past the block's rows (dense form) hold other
+      // query rows, whose results are never written.
+      mbar_arrive_expect_tx(q_full, 9 * kQBlock);
+#pragma unroll 1
+      for (int j = 0; j < 9; ++j) {
+        const int dim = j < 4 ? other + 64 * j : j == 4 ? KVQ_MLA_NOPE_DIM : own + 64 * (j - 5);
+        const uint32_t dst = j < 5 ? base + kQOff + j * kQBlock : base + kStagingOff + (j - 5) * kQBlock;
+        if constexpr (K == Keys::kSparse)
+          tma_load_3d(dst, &qmap, dim, 0, static_cast<int32_t>(blk.token0), q_full);
+        else
+          tma_load_2d(dst, &qmap, dim, static_cast<int32_t>(blk.token0 * a.num_heads + blk.row0), q_full);
+      }
+    }
   }
 
-  // Query rows -> shared memory by asynchronous copies, all in flight at
-  // once: the other half's 256 NoPE dimensions and the 64 RoPE dimensions as
-  // five 128-byte-swizzled K-major blocks (the A operand of the group-A
-  // K-steps), and the CTA's own 256 NoPE dimensions staged in the same layout
-  // in the key stages on their way to TMEM.  Rows past the block's rows are
-  // zero-filled.
+  // Without a tensor map: the same nine blocks by asynchronous 16-byte copies,
+  // all in flight at once (rows past the block's rows zero-filled).
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-  for (int i = threadIdx.x; i < kRows * 9 * 8; i += kThreads) {
+  for (int i = a.q_tma ? kRows * 72 : threadIdx.x; i < kRows * 9 * 8; i += kThreads) {
     const int row = i / 72, rem = i % 72, j = rem >> 3, c = rem & 7;   // block j: 0-3 other, 4 RoPE, 5-8 own
     const __nv_bfloat16* src = q;
     uint32_t bytes = 0;
@@ -673,15 +787,17 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
       load_part<F, false>(cur, b_nope0, k, rb);
     }
   }
-  cp_async_wait_all();
-  fence_async_smem();
+  if (!a.q_tma) {
+    cp_async_wait_all();
+    fence_async_smem();
+  }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *s_tmem;
   // The CTA's own 256 NoPE query dimensions: staging -> TMEM (softmax warp w:
-  // lane = row 32 w + lane).
-  if (is_softmax) {
+  // lane = row 32 w + lane), once the tensor-map loads have landed.
+  if (is_softmax && (!a.q_tma || warp_wait_or_abort(q_full, 0, s_abort))) {
     const uint32_t row = warp * 32 + lane;
 #pragma unroll 1
     for (int part = 0; part < 4; ++part) {            // 64 dims = 32 columns per part
@@ -794,6 +910,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
       raw1_hi = raw2_hi;
       raw2_lo = key_raw<K>(a, blk, (t + 2) * kTile + lane);
       raw2_hi = key_raw<K>(a, blk, (t + 2) * kTile + 32 + lane);
+      if (t == n_tiles / 2) prefetch_next_wave<K>(a, warp * 32 + lane);
     }
   } else if (warp < kMmaWarp) {
     // ---- producers: group A, then group B, of every tile ----------------------
@@ -865,7 +982,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
       mma_commit(s_full0 + 8 * (u & 1));
       return true;
     };
-    if (n_tiles > 0 && scores(0)) {
+    if (n_tiles > 0 && (!a.q_tma || wait_or_abort(q_full, 0, s_abort)) && scores(0)) {
       for (int t = 0; t < n_tiles; ++t) {
 #ifdef KVQ_ATTN_STALL_TILE
         // Failure-detection build only: from this tile on no MMA is issued, as
@@ -905,6 +1022,13 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
       if (clock64() - start > kDrainCycles) { aborted = true; break; }
     }
   }
+  if (a.q_tma) {
+    // the query tiles have landed before the CTA may leave (normally long ago)
+    const long long start = clock64();
+    while (!mbar_try_wait(q_full, 0)) {
+      if (clock64() - start > kDrainCycles) { aborted = true; break; }
+    }
+  }
   fence_after_sync();
   if (bad_index && a.status) atomicOr(a.status, KVQ_STATUS_BAD_INDEX);
   aborted = __syncthreads_or(aborted) != 0;
@@ -912,10 +1036,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
 
   if (is_softmax && !aborted) {
     // Each thread scales its row's 256 O columns into bf16 and writes them as
-    // a 512-byte row of a staging area in the (now idle) key stages, its
-    // 16-byte chunks rotated by XOR with row % 32 so that a warp's stores hit
-    // distinct banks; the warp then writes its 32 rows out one whole row (512
-    // contiguous bytes) per instruction.
+    // one 512-byte row of a staging area in the (now idle) key stages (rows
+    // 528 bytes apart, so that a warp's 16-byte stores spread over all banks),
+    // then hands the row to the copy engine as one bulk copy to its output row.
     const uint32_t row_lane = warp * 32u << 16;
     const uint32_t row = warp * 32 + lane;
     const float l_row = l;
@@ -924,31 +1047,32 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
     int32_t head = 0;
     const bool live = row < static_cast<uint32_t>(blk.rows);
     if (live) row_of<K>(a, blk, row, token, head);
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + token * a.out_stride_t +
-                         static_cast<int64_t>(head) * a.out_stride_h + own;
-    const uint32_t stage = base + kStagingOff;
+    const uint32_t stage_row = base + kStagingOff + row * kStageRowBytes;
 #pragma unroll 1
-    for (int c = 0; c < kHalf / 32; ++c) {
-      float o[32];
-      if (n_tiles > 0) tmem_ld32(tmem + row_lane + kOCol + 32 * c, o);
+    for (int c = 0; c < kHalf; c += 64) {
+      uint32_t o[64];
+      if (n_tiles > 0) {
+        tmem_ld64(tmem + row_lane + kOCol + c, o);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (n_tiles > 0)
-          v = make_uint4(pack_bf16x2(o[8 * i] * inv_l, o[8 * i + 1] * inv_l),
-                         pack_bf16x2(o[8 * i + 2] * inv_l, o[8 * i + 3] * inv_l),
-                         pack_bf16x2(o[8 * i + 4] * inv_l, o[8 * i + 5] * inv_l),
-                         pack_bf16x2(o[8 * i + 6] * inv_l, o[8 * i + 7] * inv_l));
-        st_shared16(stage + row * 512 + (((4 * c + i) ^ (row & 31)) << 4), v);
+        for (int i = 0; i < 64; ++i) o[i] = 0;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = make_uint4(
+            pack_bf16x2(__uint_as_float(o[8 * i]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l),
+            pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l),
+            pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l),
+            pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l));
+        st_shared16(stage_row + 2 * c + 16 * i, v);
       }
     }
-    __syncwarp();
-#pragma unroll 4
-    for (int i = 0; i < 32; ++i) {
-      const uint32_t src_row = warp * 32 + i;
-      const auto dst = reinterpret_cast<uint4*>(__shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(out), i));
-      if (__shfl_sync(0xffffffffu, static_cast<int>(live), i))
-        dst[lane] = ld_shared16(stage + src_row * 512 + ((lane ^ i) << 4));
+    fence_async_smem();                 // the staged row -> visible to the copy engine
+    if (live) {
+      bulk_store(static_cast<__nv_bfloat16*>(a.out) + token * a.out_stride_t +
+                     static_cast<int64_t>(head) * a.out_stride_h + own,
+                 stage_row, kHalf * 2);
+      bulk_wait_read();                 // the staging area is read before the CTA leaves
     }
     if (half == 0 && a.lse != nullptr && live)
       a.lse[token * a.lse_stride_t + head] =
@@ -966,11 +1090,65 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
 
 }  // namespace
 
+// The driver's tensor-map encoder, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult found{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &found) !=
+            cudaSuccess ||
+        found != cudaDriverEntryPointSuccess)
+      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// Tensor map of the query rows, tiles of 64 dimensions x 128 rows with the
+// 128-byte swizzle: sparse form [tokens][heads][576] (a tile is 128 heads of
+// one token, heads past num_heads zero-filled); dense form [token x head
+// rows][576], which needs the tokens' rows packed (q_stride_t = num_heads x
+// q_stride_h).  false: no map (the kernel copies the rows itself).
+template <Keys K>
+bool query_tensor_map(const AttentionArgs& a, CUtensorMap* map) {
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr || a.num_tokens < 1) return false;
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  CUresult r;
+  if constexpr (K == Keys::kSparse) {
+    const cuuint64_t dims[3] = {KVQ_WORKSPACE_DIM, static_cast<cuuint64_t>(a.num_heads),
+                                static_cast<cuuint64_t>(a.num_tokens)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.q_stride_h) * 2, static_cast<cuuint64_t>(a.q_stride_t) * 2};
+    const cuuint32_t box[3] = {64, kRows, 1};
+    r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides, box, elem_strides,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    const int64_t rows = a.num_tokens * a.num_heads;
+    if (a.q_stride_t != a.num_heads * a.q_stride_h || rows >= (int64_t{1} << 31)) return false;
+    const cuuint64_t dims[2] = {KVQ_WORKSPACE_DIM, static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.q_stride_h) * 2};
+    const cuuint32_t box[2] = {64, kRows};
+    r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.q), dims, strides, box, elem_strides,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  return r == CUDA_SUCCESS;
+}
+
 template <Entry F, Keys K>
 cudaError_t launch_attention(const AttentionArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(mla_attention_kernel<F, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
+  int device = 0, sms = 0;
+  if ((e = cudaGetDevice(&device)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess) return e;
+  AttentionArgs args = a;
+  args.wave = sms;                      // one CTA per SM
+  CUtensorMap qmap;
+  std::memset(&qmap, 0, sizeof(qmap));
+  args.q_tma = query_tensor_map<K>(a, &qmap) ? 1 : 0;
   dim3 grid;
   if constexpr (K == Keys::kSparse) {
     grid = dim3(static_cast<unsigned>(a.num_tokens * 2));
@@ -978,7 +1156,7 @@ cudaError_t launch_attention(const AttentionArgs& a, cudaStream_t stream) {
     const int64_t blocks = (static_cast<int64_t>(a.max_query_len) * a.num_heads + kRows - 1) / kRows;
     grid = dim3(static_cast<unsigned>(blocks * 2), static_cast<unsigned>(a.batch_size));
   }
-  mla_attention_kernel<F, K><<<grid, kThreads, kSmemBytes, stream>>>(a);
+  mla_attention_kernel<F, K><<<grid, kThreads, kSmemBytes, stream>>>(args, qmap);
   return cudaGetLastError();
 }
 

@@ -99,6 +99,8 @@ struct AttentionArgs {
   float* lse;                    // fp32 [num_tokens, num_heads] or nullptr
   int64_t lse_stride_t;
   int32_t* status;
+  int32_t wave;                  // set by the launcher: CTAs resident at once (one per SM)
+  int32_t q_tma;                 // set by the launcher: query rows loaded through its tensor map
 };
 
 int64_t write_max_tokens();     // grid.x bound of the write launches

@@ -475,3 +475,39 @@ def test_prefill_full_size_sampled(kvq, oracle_mod, threads, fmt):
                              torch.from_numpy(ctx[picks].astype(np.int32)),
                              torch.from_numpy(wl.host(w.block_table)[picks]), w.softmax_scale, 2)
     check_prefill(oracle_mod, cache_host, sub, out[keep].cpu(), lse[keep].cpu(), threads)
+
+
+@pytest.mark.parametrize("layout", ["rows in wider buffers", "heads of a wider tensor"])
+def test_query_row_layouts(kvq, oracle_mod, layout):
+    """Query rows that are not a packed [T, H, 576] tensor: each row inside a
+    640-value buffer (token rows still packed: q_stride_t = H q_stride_h), or
+    the first H heads of a tensor with H + 3 heads (token rows not packed).
+    The sparse form reads both through its query tensor map; the dense form
+    reads the first through its tensor map and copies the second row by row
+    itself."""
+    T, H = 5, 20
+
+    def place(q):
+        q = q.to(DEV)
+        if layout == "rows in wider buffers":
+            big = torch.zeros((q.shape[0], H, 640), dtype=torch.bfloat16, device=DEV)
+            big[:, :, 32:608] = q
+            return big[:, :, 32:608]
+        big = torch.zeros((q.shape[0], H + 3, 576), dtype=torch.bfloat16, device=DEV)
+        big[:, :H] = q
+        return big[:, :H]
+
+    w = wl.make_attention("layout sparse", T, H, 128, 8, 64, 521, p_unused=0.1)
+    cache = host_cache(oracle_mod, w.fill)
+    dcache = torch.from_numpy(cache).to(DEV)
+    out, lse = kvq.kvq_sparse_mla_attention_nvfp4_ds_mla(place(w.q), w.indices.to(DEV), dcache, w.softmax_scale)
+    torch.cuda.synchronize()
+    check(oracle_mod, cache, w.q, wl.host(w.indices), w.softmax_scale, out, lse)
+
+    p = wl.make_prefill("layout dense", [150, 90], [3, 4], H, 8, 64, 522)
+    pcache = host_cache(oracle_mod, p.fill)
+    out, lse = kvq.kvq_prefill_mla_attention_nvfp4_ds_mla(place(p.q), p.query_start.to(DEV), p.context_lens.to(DEV),
+                                                          p.block_table.to(DEV), torch.from_numpy(pcache).to(DEV),
+                                                          p.softmax_scale, p.max_query_len)
+    torch.cuda.synchronize()
+    check_prefill(oracle_mod, pcache, p, out, lse)
