@@ -528,6 +528,35 @@ def time_extra(step: GpuStep):
                 "frac": round(flops / us / 1e6 / peak_tf, 4), "gbs": round(nbytes / us / 1e3, 1),
                 "valid_slots": n_valid, "method": "CUDA events"}
             del aw, ao, al
+        # a small decode batch: 8 tokens x 128 heads x top-2048 over the same
+        # nvfp4 cache, one CTA pair per token (16 CTAs on the GPU) against
+        # the split over the keys (default_num_splits ranges, a combine
+        # launch); CUDA-graph replays over 24 index sets (138 MB of entries,
+        # more than L2)
+        sets = [wl.make_attention(f"small decode {i}", 8, 128, 2048, 65536, 64, 600 + i, dev, p_unused=0.1,
+                                  fill=step.g3.fill, rng="device") for i in range(24)]
+        so = torch.empty((8, 128, 512), dtype=torch.bfloat16, device=dev)
+        sl = torch.empty((8, 128), dtype=torch.float32, device=dev)
+        splits = kvq.default_num_splits(8, 2048)
+        ws = torch.empty(kvq.kvq_sparse_mla_attention_split_workspace_bytes(8, 128, splits), dtype=torch.uint8,
+                         device=dev)
+        n_valid = sum(int((s.indices >= 0).sum()) for s in sets) / len(sets)
+        flops = ATTN_FLOPS_PER_SLOT_HEAD * 128 * n_valid
+        peak_tf, peak_src = measured_peak_tflops()
+        for name, fn in (
+                ("sparse_mla_attention_nvfp4_ds_mla T=8 H=128 top-2048 (one range)",
+                 lambda s: kvq.kvq_sparse_mla_attention_nvfp4_ds_mla(s.q, s.indices, step.cache3, s.softmax_scale,
+                                                                     out=so, lse=sl)),
+                (f"sparse_mla_attention_split_nvfp4_ds_mla T=8 H=128 top-2048 ({splits} ranges)",
+                 lambda s: kvq.kvq_sparse_mla_attention_split_nvfp4_ds_mla(s.q, s.indices, step.cache3,
+                                                                           s.softmax_scale, num_splits=splits,
+                                                                           workspace=ws, out=so, lse=sl))):
+            us = graph_replay_us([lambda s=s, fn=fn: fn(s) for s in sets])
+            out[name] = {"units": 8, "us": round(us, 2), "tflops": round(flops / us / 1e6, 1), "bound": "tensor",
+                         "peak_tflops": peak_tf, "peak": f"{peak_src} bf16 burst",
+                         "frac": round(flops / us / 1e6 / peak_tf, 4),
+                         "method": "CUDA graph over 24 index sets"}
+        del sets, so, sl, ws
         # dense prefill straight from the caches: each request of a gather
         # batch attends with 16 new tokens x 128 heads to its whole context
         # (seq_start + length positions) through the same block table

@@ -22,7 +22,10 @@ __all__ = [
     "kvq_gather_upconvert_fp8_ds_mla", "kvq_reshape_and_cache_nvfp4", "kvq_selftest_convert",
     "kvq_dequant_nvfp4_per_head", "kvq_req_index_to_global_slot",
     "kvq_sparse_mla_attention_nvfp4_ds_mla", "kvq_sparse_mla_attention_fp8_ds_mla",
-    "kvq_prefill_mla_attention_nvfp4_ds_mla", "kvq_prefill_mla_attention_fp8_ds_mla", "kvq_last_error_string", "kvq_version", "library_path", "load_library",
+    "kvq_prefill_mla_attention_nvfp4_ds_mla", "kvq_prefill_mla_attention_fp8_ds_mla",
+    "kvq_sparse_mla_attention_split_nvfp4_ds_mla", "kvq_sparse_mla_attention_split_fp8_ds_mla",
+    "kvq_sparse_mla_attention_split_workspace_bytes", "default_num_splits", "ATTN_MAX_SPLITS",
+    "kvq_last_error_string", "kvq_version", "library_path", "load_library",
     "NVFP4_DS_MLA_ENTRY_BYTES", "FP8_DS_MLA_ENTRY_BYTES", "STATUS_BAD_INDEX", "STATUS_BAD_BATCH",
     "STATUS_TIMEOUT",
     "nvfp4_full_dim",
@@ -33,6 +36,7 @@ FP8_DS_MLA_ENTRY_BYTES = 656
 STATUS_BAD_INDEX = 0x1
 STATUS_BAD_BATCH = 0x2
 STATUS_TIMEOUT = 0x4
+ATTN_MAX_SPLITS = 32
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lib = None
@@ -68,6 +72,12 @@ _SIGNATURES = {
     "kvq_prefill_mla_attention_fp8_ds_mla": [_P, _I64, _I64, _I64, _I32, _P, _P, _I32, _I32, _P, _I64, _I32,
                                              _P, _I64, _I32, _I64, _I64, ctypes.c_float, _P, _I64, _I64, _P,
                                              _I64, _P, _P],
+    "kvq_sparse_mla_attention_split_nvfp4_ds_mla": [_P, _I64, _I64, _I64, _I32, _P, _I64, _I32, _P, _I64, _I32,
+                                                    _I64, _I64, ctypes.c_float, _P, _I64, _I64, _P, _I64,
+                                                    _I32, _P, _I64, _P, _P],
+    "kvq_sparse_mla_attention_split_fp8_ds_mla": [_P, _I64, _I64, _I64, _I32, _P, _I64, _I32, _P, _I64, _I32,
+                                                  _I64, _I64, ctypes.c_float, _P, _I64, _I64, _P, _I64,
+                                                  _I32, _P, _I64, _P, _P],
 }
 
 
@@ -92,6 +102,8 @@ def load_library():
         handle.kvq_last_error_string.argtypes = []
         handle.kvq_version.restype = _I32
         handle.kvq_version.argtypes = []
+        handle.kvq_sparse_mla_attention_split_workspace_bytes.restype = _I64
+        handle.kvq_sparse_mla_attention_split_workspace_bytes.argtypes = [_I64, _I32, _I32]
         _lib = handle
     return _lib
 
@@ -300,7 +312,45 @@ def kvq_sparse_mla_attention_fp8_ds_mla(q, indices, kv_cache, softmax_scale: flo
                       lse, status, stream)
 
 
-def _attention(cname, entry, q, indices, kv_cache, softmax_scale, out, lse, status, stream):
+def kvq_sparse_mla_attention_split_workspace_bytes(num_tokens: int, num_heads: int, num_splits: int) -> int:
+    """Bytes of workspace the split-key decode needs (-1 for bad arguments)."""
+    return load_library().kvq_sparse_mla_attention_split_workspace_bytes(num_tokens, num_heads, num_splits)
+
+
+def default_num_splits(num_tokens: int, topk: int, device=None) -> int:
+    """Key ranges per token for a decode batch of num_tokens: as many as one
+    wave of CTAs holds (two CTAs per token and range, one CTA per SM), at
+    most ATTN_MAX_SPLITS and at most one per 64-key tile, the count then
+    trimmed so that no range is left empty."""
+    if num_tokens <= 0:
+        return 1
+    sms = torch.cuda.get_device_properties(device if device is not None else torch.cuda.current_device()
+                                           ).multi_processor_count
+    tiles = (topk + 63) // 64
+    want = max(1, min(ATTN_MAX_SPLITS, tiles, sms // (2 * num_tokens)))
+    per_range = -(-tiles // want) if tiles else 1
+    return max(1, -(-tiles // per_range)) if tiles else 1
+
+
+def kvq_sparse_mla_attention_split_nvfp4_ds_mla(q, indices, kv_cache, softmax_scale: float, num_splits=None,
+                                                workspace=None, out=None, lse=None, status=None, stream=None):
+    """The sparse attention of kvq_sparse_mla_attention_nvfp4_ds_mla with each
+    token's keys split into num_splits ranges (default: default_num_splits)
+    whose partial results a second launch combines.  workspace: a CUDA uint8
+    tensor of at least kvq_sparse_mla_attention_split_workspace_bytes bytes
+    (allocated here when None)."""
+    return _attention("kvq_sparse_mla_attention_split_nvfp4_ds_mla", 352, q, indices, kv_cache, softmax_scale, out,
+                      lse, status, stream, split=(num_splits, workspace))
+
+
+def kvq_sparse_mla_attention_split_fp8_ds_mla(q, indices, kv_cache, softmax_scale: float, num_splits=None,
+                                              workspace=None, out=None, lse=None, status=None, stream=None):
+    """The same split-key decode straight from the 656-byte fp8_ds_mla cache."""
+    return _attention("kvq_sparse_mla_attention_split_fp8_ds_mla", 656, q, indices, kv_cache, softmax_scale, out,
+                      lse, status, stream, split=(num_splits, workspace))
+
+
+def _attention(cname, entry, q, indices, kv_cache, softmax_scale, out, lse, status, stream, split=None):
     _need(q.dtype == torch.bfloat16 and q.is_cuda and q.dim() == 3 and q.shape[2] == 576
           and q.stride(2) == 1, "q: expected a CUDA bf16 [T, H, 576] tensor with unit inner stride")
     T, H = q.shape[0], q.shape[1]
@@ -317,11 +367,23 @@ def _attention(cname, entry, q, indices, kv_cache, softmax_scale, out, lse, stat
     if lse is not False:
         _need(lse.dtype == torch.float32 and lse.is_cuda and tuple(lse.shape) == (T, H) and lse.stride(1) == 1,
               "lse: expected a CUDA fp32 [T, H] tensor with unit inner stride")
-    _call(cname, q.data_ptr(), q.stride(0), q.stride(1), T, H,
-          indices.data_ptr(), max(indices.stride(0), indices.shape[1]), indices.shape[1], kv_cache.data_ptr(), kv_cache.shape[0],
-          kv_cache.shape[1], kv_cache.stride(0), kv_cache.stride(1), float(softmax_scale), out.data_ptr(),
-          out.stride(0), out.stride(1), None if lse is False else lse.data_ptr(),
-          0 if lse is False else lse.stride(0), _status_ptr(status), _stream(stream, q.device))
+    args = [q.data_ptr(), q.stride(0), q.stride(1), T, H,
+            indices.data_ptr(), max(indices.stride(0), indices.shape[1]), indices.shape[1], kv_cache.data_ptr(),
+            kv_cache.shape[0], kv_cache.shape[1], kv_cache.stride(0), kv_cache.stride(1), float(softmax_scale),
+            out.data_ptr(), out.stride(0), out.stride(1), None if lse is False else lse.data_ptr(),
+            0 if lse is False else lse.stride(0)]
+    if split is not None:
+        num_splits, workspace = split
+        if num_splits is None:
+            num_splits = default_num_splits(T, indices.shape[1], q.device)
+        need = kvq_sparse_mla_attention_split_workspace_bytes(T, H, num_splits) if num_splits > 1 else 0
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        if workspace is not None:
+            _need(workspace.is_cuda and workspace.is_contiguous(), "workspace: expected a contiguous CUDA tensor")
+        args += [int(num_splits), None if workspace is None else workspace.data_ptr(),
+                 0 if workspace is None else workspace.numel() * workspace.element_size()]
+    _call(cname, *args, _status_ptr(status), _stream(stream, q.device))
     return out, (None if lse is False else lse)
 
 

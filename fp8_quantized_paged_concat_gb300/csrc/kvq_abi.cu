@@ -312,10 +312,13 @@ kvq_status attention_common(
     const int32_t* indices, int64_t indices_stride, int32_t topk, const uint8_t* kv_cache,
     int64_t num_blocks, int32_t block_size, int64_t block_stride, int64_t entry_stride,
     float softmax_scale, void* out, int64_t out_stride_t, int64_t out_stride_h, float* lse,
-    int64_t lse_stride_t, int32_t* d_status, kvq_stream_t stream) {
+    int64_t lse_stride_t, int32_t* d_status, kvq_stream_t stream, int32_t num_splits = 1,
+    void* workspace = nullptr, int64_t workspace_bytes = 0) {
   KVQ_REQUIRE(num_tokens >= 0 && topk >= 0, "%s: num_tokens / topk < 0", fn);
+  KVQ_REQUIRE(num_splits >= 1 && num_splits <= KVQ_ATTN_MAX_SPLITS, "%s: num_splits must be in [1, %d] (got %d)",
+              fn, KVQ_ATTN_MAX_SPLITS, num_splits);
   if (num_tokens == 0) return ok();
-  KVQ_REQUIRE(num_tokens < (int64_t{1} << 30), "%s: num_tokens too large", fn);   // 2 CTAs each
+  KVQ_REQUIRE(num_tokens * num_splits < (int64_t{1} << 30), "%s: num_tokens x num_splits too large", fn);
   KVQ_REQUIRE(num_heads >= 1 && num_heads <= 128, "%s: num_heads must be in [1, 128] (got %d)", fn,
               num_heads);
   KVQ_REQUIRE(q != nullptr && out != nullptr, "%s: q and out must be non-NULL", fn);
@@ -337,8 +340,23 @@ kvq_status attention_common(
                                      entry_stride, entry_bytes))
     return s;
   KVQ_REQUIRE(d_status == nullptr || aligned(d_status, 4), "%s: d_status misaligned", fn);
+  if (num_splits > 1) {
+    const int64_t need = kvq_sparse_mla_attention_split_workspace_bytes(num_tokens, num_heads, num_splits);
+    KVQ_REQUIRE(workspace != nullptr && aligned(workspace, 16) && workspace_bytes >= need,
+                "%s: workspace must be non-NULL, 16-byte aligned and at least %lld bytes (got %lld)", fn,
+                static_cast<long long>(need), static_cast<long long>(workspace_bytes));
+  }
   if (kvq_status s = check_device(fn)) return s;
   kvq::AttentionArgs a{};
+  a.num_splits = num_splits;
+  if (num_splits > 1) {
+    // whole 64-key tiles per range; ranges past the list are empty
+    const int64_t tiles = (int64_t{topk} + 63) / 64;
+    a.split_keys = static_cast<int32_t>((tiles + num_splits - 1) / num_splits * 64);
+    const int64_t rows = num_tokens * num_heads * num_splits;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_lse = static_cast<float*>(workspace) + rows * KVQ_MLA_NOPE_DIM;
+  }
   a.q = q;
   a.q_stride_t = q_stride_t;
   a.q_stride_h = q_stride_h;
@@ -488,6 +506,40 @@ kvq_status kvq_sparse_mla_attention_fp8_ds_mla(
                           num_heads, indices, indices_stride, topk, kv_cache, num_blocks, block_size,
                           block_stride, entry_stride, softmax_scale, out, out_stride_t, out_stride_h, lse,
                           lse_stride_t, d_status, stream);
+}
+
+int64_t kvq_sparse_mla_attention_split_workspace_bytes(int64_t num_tokens, int32_t num_heads, int32_t num_splits) {
+  if (num_tokens < 0 || num_heads < 1 || num_splits < 1 || num_tokens >= (int64_t{1} << 40)) return -1;
+  const int64_t rows = num_tokens * num_heads * num_splits;
+  return (rows * (KVQ_MLA_NOPE_DIM + 1) * 4 + 15) / 16 * 16;
+}
+
+kvq_status kvq_sparse_mla_attention_split_nvfp4_ds_mla(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h, int64_t num_tokens, int32_t num_heads,
+    const int32_t* indices, int64_t indices_stride, int32_t topk, const uint8_t* kv_cache, int64_t num_blocks,
+    int32_t block_size, int64_t block_stride, int64_t entry_stride, float softmax_scale, void* out,
+    int64_t out_stride_t, int64_t out_stride_h, float* lse, int64_t lse_stride_t, int32_t num_splits,
+    void* workspace, int64_t workspace_bytes, int32_t* d_status, kvq_stream_t stream) {
+  return attention_common("kvq_sparse_mla_attention_split_nvfp4_ds_mla", KVQ_NVFP4_DS_MLA_ENTRY_BYTES,
+                          num_splits > 1 ? kvq::launch_sparse_mla_attention_split_nvfp4
+                                         : kvq::launch_sparse_mla_attention_nvfp4,
+                          q, q_stride_t, q_stride_h, num_tokens, num_heads, indices, indices_stride, topk, kv_cache,
+                          num_blocks, block_size, block_stride, entry_stride, softmax_scale, out, out_stride_t,
+                          out_stride_h, lse, lse_stride_t, d_status, stream, num_splits, workspace, workspace_bytes);
+}
+
+kvq_status kvq_sparse_mla_attention_split_fp8_ds_mla(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h, int64_t num_tokens, int32_t num_heads,
+    const int32_t* indices, int64_t indices_stride, int32_t topk, const uint8_t* kv_cache, int64_t num_blocks,
+    int32_t block_size, int64_t block_stride, int64_t entry_stride, float softmax_scale, void* out,
+    int64_t out_stride_t, int64_t out_stride_h, float* lse, int64_t lse_stride_t, int32_t num_splits,
+    void* workspace, int64_t workspace_bytes, int32_t* d_status, kvq_stream_t stream) {
+  return attention_common("kvq_sparse_mla_attention_split_fp8_ds_mla", KVQ_FP8_DS_MLA_ENTRY_BYTES,
+                          num_splits > 1 ? kvq::launch_sparse_mla_attention_split_fp8
+                                         : kvq::launch_sparse_mla_attention_fp8,
+                          q, q_stride_t, q_stride_h, num_tokens, num_heads, indices, indices_stride, topk, kv_cache,
+                          num_blocks, block_size, block_stride, entry_stride, softmax_scale, out, out_stride_t,
+                          out_stride_h, lse, lse_stride_t, d_status, stream, num_splits, workspace, workspace_bytes);
 }
 
 kvq_status kvq_selftest_convert(uint32_t first_bits, int64_t count, uint8_t* e4m3_lo,

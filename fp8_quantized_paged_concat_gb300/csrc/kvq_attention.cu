@@ -108,7 +108,8 @@ static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
 // way to TMEM and the output rows on their way out.
 constexpr uint32_t kStagingOff = kAOff;
 constexpr uint32_t kStageRowBytes = 528;                     // an output row (512 bytes) + 16
-static_assert(kMiscOff - kStagingOff >= kRows * kStageRowBytes && kMiscOff - kStagingOff >= 4 * kQBlock,
+constexpr uint32_t kPartRowBytes = 1040;                     // a partial fp32 row (1 KB) + 16
+static_assert(kMiscOff - kStagingOff >= kRows * kPartRowBytes && kMiscOff - kStagingOff >= 4 * kQBlock,
               "the staging fits the key stages");
 static_assert(kAOff % 1024 == 0 && kBOff % 1024 == 0 && kAStage % 1024 == 0 && kBStage % 1024 == 0,
               "1024-byte swizzle atoms");
@@ -463,8 +464,9 @@ struct Block {
   int32_t row0;               // dense: first packed (token, head) row of the block
   int32_t rows;               // rows of the block (query rows past it are zero)
   int32_t request;            // dense: the request
-  int32_t n_keys;             // topk (sparse) or the context length (dense)
-  const int32_t* idx;         // sparse: the token's slot list
+  int32_t n_keys;             // keys of the block: topk, or its split's share (sparse), the context (dense)
+  int32_t split;              // sparse, split over the keys: the block's range of the list
+  const int32_t* idx;         // sparse: the block's part of the token's slot list
 };
 
 // The block of CTA (bx, by); `report`: record a skipped request in the
@@ -474,11 +476,21 @@ __device__ __forceinline__ Block block_of(const AttentionArgs& a, uint32_t bx, u
   Block b{};
   if constexpr (K == Keys::kSparse) {
     b.live = true;
-    b.token0 = bx >> 1;
     b.row0 = 0;
     b.rows = a.num_heads;
-    b.n_keys = a.topk;
-    b.idx = a.indices + b.token0 * a.indices_stride;
+    if (a.num_splits > 1) {
+      // CTA pair (token, split): keys [split * split_keys, +split_keys) of the list
+      const uint32_t unit = bx >> 1, splits = static_cast<uint32_t>(a.num_splits);
+      b.token0 = unit / splits;
+      b.split = static_cast<int32_t>(unit - static_cast<uint32_t>(b.token0) * splits);
+      const int32_t key0 = b.split * a.split_keys;
+      b.n_keys = max(0, min(a.topk - key0, a.split_keys));
+      b.idx = a.indices + b.token0 * a.indices_stride + key0;
+    } else {
+      b.token0 = bx >> 1;
+      b.n_keys = a.topk;
+      b.idx = a.indices + b.token0 * a.indices_stride;
+    }
   } else {
     b.request = static_cast<int32_t>(by);
     const int32_t q0 = __ldg(a.query_start + b.request), q1 = __ldg(a.query_start + b.request + 1);
@@ -1035,10 +1047,6 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
   if (aborted && threadIdx.x == 0 && a.status) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
 
   if (is_softmax && !aborted) {
-    // Each thread scales its row's 256 O columns into bf16 and writes them as
-    // one 512-byte row of a staging area in the (now idle) key stages (rows
-    // 528 bytes apart, so that a warp's 16-byte stores spread over all banks),
-    // then hands the row to the copy engine as one bulk copy to its output row.
     const uint32_t row_lane = warp * 32u << 16;
     const uint32_t row = warp * 32 + lane;
     const float l_row = l;
@@ -1047,36 +1055,72 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
     int32_t head = 0;
     const bool live = row < static_cast<uint32_t>(blk.rows);
     if (live) row_of<K>(a, blk, row, token, head);
-    const uint32_t stage_row = base + kStagingOff + row * kStageRowBytes;
+    if (a.part_o != nullptr) {
+      // A key range of a split decode: the normalised fp32 partial row (1 KB,
+      // staged 1040 bytes apart) and the range's base-2 log-sum-exp, for the
+      // combine launch.
+      const uint32_t part_row = base + kStagingOff + row * kPartRowBytes;
 #pragma unroll 1
-    for (int c = 0; c < kHalf; c += 64) {
-      uint32_t o[64];
-      if (n_tiles > 0) {
-        tmem_ld64(tmem + row_lane + kOCol + c, o);
-      } else {
+      for (int c = 0; c < kHalf; c += 64) {
+        uint32_t o[64];
+        if (n_tiles > 0) {
+          tmem_ld64(tmem + row_lane + kOCol + c, o);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) o[i] = 0;
-      }
+          for (int i = 0; i < 64; ++i) o[i] = 0;
+        }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint4 v = make_uint4(
-            pack_bf16x2(__uint_as_float(o[8 * i]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l),
-            pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l),
-            pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l),
-            pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l));
-        st_shared16(stage_row + 2 * c + 16 * i, v);
+        for (int i = 0; i < 16; ++i)
+          st_shared16(part_row + 4 * c + 16 * i,
+                      make_uint4(__float_as_uint(__uint_as_float(o[4 * i]) * inv_l),
+                                 __float_as_uint(__uint_as_float(o[4 * i + 1]) * inv_l),
+                                 __float_as_uint(__uint_as_float(o[4 * i + 2]) * inv_l),
+                                 __float_as_uint(__uint_as_float(o[4 * i + 3]) * inv_l)));
       }
+      fence_async_smem();
+      const int64_t prow = (token * a.num_heads + head) * a.num_splits + blk.split;
+      if (live) {
+        bulk_store(a.part_o + prow * KVQ_MLA_NOPE_DIM + own, part_row, kHalf * 4);
+        bulk_wait_read();
+        if (half == 0) a.part_lse[prow] = l_row > 0.0f ? m + log2f(l_row) : -INFINITY;
+      }
+    } else {
+      // Each thread scales its row's 256 O columns into bf16 and writes them
+      // as one 512-byte row of a staging area in the (now idle) key stages
+      // (rows 528 bytes apart, so that a warp's 16-byte stores spread over all
+      // banks), then hands the row to the copy engine as one bulk copy to its
+      // output row.
+      const uint32_t stage_row = base + kStagingOff + row * kStageRowBytes;
+#pragma unroll 1
+      for (int c = 0; c < kHalf; c += 64) {
+        uint32_t o[64];
+        if (n_tiles > 0) {
+          tmem_ld64(tmem + row_lane + kOCol + c, o);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) o[i] = 0;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = make_uint4(
+              pack_bf16x2(__uint_as_float(o[8 * i]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l),
+              pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l),
+              pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l),
+              pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l));
+          st_shared16(stage_row + 2 * c + 16 * i, v);
+        }
+      }
+      fence_async_smem();                 // the staged row -> visible to the copy engine
+      if (live) {
+        bulk_store(static_cast<__nv_bfloat16*>(a.out) + token * a.out_stride_t +
+                       static_cast<int64_t>(head) * a.out_stride_h + own,
+                   stage_row, kHalf * 2);
+        bulk_wait_read();                 // the staging area is read before the CTA leaves
+      }
+      if (half == 0 && a.lse != nullptr && live)
+        a.lse[token * a.lse_stride_t + head] =
+            l_row > 0.0f ? (m + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
     }
-    fence_async_smem();                 // the staged row -> visible to the copy engine
-    if (live) {
-      bulk_store(static_cast<__nv_bfloat16*>(a.out) + token * a.out_stride_t +
-                     static_cast<int64_t>(head) * a.out_stride_h + own,
-                 stage_row, kHalf * 2);
-      bulk_wait_read();                 // the staging area is read before the CTA leaves
-    }
-    if (half == 0 && a.lse != nullptr && live)
-      a.lse[token * a.lse_stride_t + head] =
-          l_row > 0.0f ? (m + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
   }
 
   fence_before_sync();
@@ -1086,6 +1130,62 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
                  :: "r"(tmem), "r"(kTmemCols) : "memory");
   }
+}
+
+// ---------------------------------------------------------------------------
+// split decode: the key ranges' partial results combined
+// ---------------------------------------------------------------------------
+//
+// One warp per (token, head) row; lane s holds range s's base-2 log-sum-exp
+// L_s (at most 32 ranges).  With M = max L_s and w_s = 2^(L_s - M):
+//   out = sum_s w_s o_s / sum_s w_s,   lse = (M + log2 sum_s w_s) ln 2,
+// o_s being range s's normalised partial output (an empty range: L_s = -inf,
+// weight 0; no valid key at all: out = 0, lse = -inf, as unsplit).
+constexpr int kCombineWarps = 8;
+
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_splits_kernel(const AttentionArgs a) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= a.num_tokens * a.num_heads) return;          // whole warps
+  const int splits = a.num_splits;
+  const float ls = lane < splits ? a.part_lse[row * splits + lane] : -INFINITY;
+  float mx = ls;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float w = ls == -INFINITY ? 0.0f : ex2(ls - mx);
+  float den = w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+  const float* po = a.part_o + row * splits * KVQ_MLA_NOPE_DIM + 16 * lane;
+  for (int sp = 0; sp < splits; ++sp) {
+    const float ws = __shfl_sync(0xffffffffu, w, sp);
+    if (ws == 0.0f) continue;                               // uniform over the warp
+    const float4* src = reinterpret_cast<const float4*>(po + sp * KVQ_MLA_NOPE_DIM);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 v = __ldg(src + i);
+      acc[4 * i] += ws * v.x;
+      acc[4 * i + 1] += ws * v.y;
+      acc[4 * i + 2] += ws * v.z;
+      acc[4 * i + 3] += ws * v.w;
+    }
+  }
+  const float inv = den > 0.0f ? 1.0f / den : 0.0f;
+  const int64_t token = row / a.num_heads;
+  const int64_t head = row - token * a.num_heads;
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + token * a.out_stride_t +
+                                        head * a.out_stride_h + 16 * lane);
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    dst[h] = make_uint4(pack_bf16x2(acc[8 * h] * inv, acc[8 * h + 1] * inv),
+                        pack_bf16x2(acc[8 * h + 2] * inv, acc[8 * h + 3] * inv),
+                        pack_bf16x2(acc[8 * h + 4] * inv, acc[8 * h + 5] * inv),
+                        pack_bf16x2(acc[8 * h + 6] * inv, acc[8 * h + 7] * inv));
+  if (lane == 0 && a.lse != nullptr)
+    a.lse[token * a.lse_stride_t + head] = den > 0.0f ? (mx + log2f(den)) * 0.69314718055994530942f : -INFINITY;
 }
 
 }  // namespace
@@ -1151,7 +1251,7 @@ cudaError_t launch_attention(const AttentionArgs& a, cudaStream_t stream) {
   args.q_tma = query_tensor_map<K>(a, &qmap) ? 1 : 0;
   dim3 grid;
   if constexpr (K == Keys::kSparse) {
-    grid = dim3(static_cast<unsigned>(a.num_tokens * 2));
+    grid = dim3(static_cast<unsigned>(a.num_tokens * 2 * (a.num_splits > 1 ? a.num_splits : 1)));
   } else {
     const int64_t blocks = (static_cast<int64_t>(a.max_query_len) * a.num_heads + kRows - 1) / kRows;
     grid = dim3(static_cast<unsigned>(blocks * 2), static_cast<unsigned>(a.batch_size));
@@ -1165,6 +1265,22 @@ cudaError_t launch_sparse_mla_attention_nvfp4(const AttentionArgs& a, cudaStream
 }
 cudaError_t launch_sparse_mla_attention_fp8(const AttentionArgs& a, cudaStream_t stream) {
   return launch_attention<Entry::kFp8, Keys::kSparse>(a, stream);
+}
+template <Entry F>
+cudaError_t launch_split(const AttentionArgs& a, cudaStream_t stream) {
+  cudaError_t e = launch_attention<F, Keys::kSparse>(a, stream);
+  if (e != cudaSuccess) return e;
+  const int64_t rows = a.num_tokens * a.num_heads;
+  combine_splits_kernel<<<static_cast<unsigned>((rows + kCombineWarps - 1) / kCombineWarps), kCombineWarps * 32, 0,
+                          stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_mla_attention_split_nvfp4(const AttentionArgs& a, cudaStream_t stream) {
+  return launch_split<Entry::kNvfp4>(a, stream);
+}
+cudaError_t launch_sparse_mla_attention_split_fp8(const AttentionArgs& a, cudaStream_t stream) {
+  return launch_split<Entry::kFp8>(a, stream);
 }
 cudaError_t launch_prefill_mla_attention_nvfp4(const AttentionArgs& a, cudaStream_t stream) {
   return launch_attention<Entry::kNvfp4, Keys::kDense>(a, stream);

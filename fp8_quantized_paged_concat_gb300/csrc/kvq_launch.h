@@ -101,6 +101,14 @@ struct AttentionArgs {
   int32_t* status;
   int32_t wave;                  // set by the launcher: CTAs resident at once (one per SM)
   int32_t q_tma;                 // set by the launcher: query rows loaded through its tensor map
+  // sparse decode split over the keys: each token's list cut into num_splits
+  // ranges of split_keys keys (whole 64-key tiles), one CTA pair per range,
+  // each writing its normalised partial output and base-2 lse to part_o /
+  // part_lse (nullptr: no split, num_splits = 1, results straight to out / lse)
+  int32_t num_splits;
+  int32_t split_keys;
+  float* part_o;                 // fp32 [num_tokens, num_heads, num_splits, 512]
+  float* part_lse;               // fp32 [num_tokens, num_heads, num_splits]
 };
 
 int64_t write_max_tokens();     // grid.x bound of the write launches
@@ -114,6 +122,9 @@ cudaError_t launch_dequant_nvfp4_per_head(const PerHeadArgs& a, cudaStream_t str
 cudaError_t launch_sparse_mla_attention_nvfp4(const AttentionArgs& a, cudaStream_t stream);
 cudaError_t launch_sparse_mla_attention_fp8(const AttentionArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_mla_attention_nvfp4(const AttentionArgs& a, cudaStream_t stream);
+// Split-key sparse decode: the partial launch, then the combine into out / lse.
+cudaError_t launch_sparse_mla_attention_split_nvfp4(const AttentionArgs& a, cudaStream_t stream);
+cudaError_t launch_sparse_mla_attention_split_fp8(const AttentionArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_mla_attention_fp8(const AttentionArgs& a, cudaStream_t stream);
 
 struct IndexArgs {

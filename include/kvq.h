@@ -286,6 +286,66 @@ kvq_status kvq_sparse_mla_attention_fp8_ds_mla(
     float* lse, int64_t lse_stride_t,
     int32_t* d_status, kvq_stream_t stream);
 
+#define KVQ_ATTN_MAX_SPLITS 32         /* key ranges per token of the split-key decode */
+
+/*
+ * kvq_sparse_mla_attention_split_workspace_bytes -- bytes of device workspace
+ * the split-key decode below needs for num_tokens x num_heads query rows cut
+ * into num_splits key ranges: num_tokens * num_heads * num_splits * 513 * 4,
+ * rounded up to 16.  -1 for a negative or zero argument.
+ */
+int64_t kvq_sparse_mla_attention_split_workspace_bytes(int64_t num_tokens, int32_t num_heads,
+                                                       int32_t num_splits);
+
+/*
+ * kvq_sparse_mla_attention_split_nvfp4_ds_mla,
+ * kvq_sparse_mla_attention_split_fp8_ds_mla -- the sparse MLA attention of
+ * kvq_sparse_mla_attention_nvfp4_ds_mla / _fp8_ds_mla (the same definition,
+ * [P1] "Key source snippets" and [P3] "Implementation breakdown" item 3; the
+ * same arguments, arithmetic rules, outputs and status), scheduled for decode
+ * batches too small to fill the GPU: no passage of the pages defines the
+ * schedule, which is a split over the keys.  Each token's list is cut into
+ * num_splits ranges of whole 64-key tiles (the last ranges may be empty); a
+ * pair of CTAs per (token, range) writes the range's normalised partial output
+ * o_r (fp32) and its base-2 log-sum-exp L_r into the workspace, and a second
+ * launch on the same stream combines them:
+ *   out = sum_r w_r o_r / sum_r w_r,   lse = (M + log2 sum_r w_r) ln 2,
+ *   w_r = 2^(L_r - M),   M = max_r L_r.
+ * Each range's weights are relative to its own maximum before their bf16
+ * rounding, so the result differs from the one-range result within the same
+ * error bound.  1 <= num_splits <= KVQ_ATTN_MAX_SPLITS; num_splits = 1 is
+ * the plain entry point (the workspace is not used and may be NULL).
+ * workspace: device memory owned by the caller, 16-byte aligned, at least
+ * kvq_sparse_mla_attention_split_workspace_bytes(num_tokens, num_heads,
+ * num_splits) bytes (workspace_bytes says how many there are), overwritten:
+ * fp32 partial rows [num_tokens, num_heads, num_splits, 512], then the fp32
+ * range lse values; no other call may use it while this one runs.  After a
+ * KVQ_STATUS_TIMEOUT the outputs of the tokens concerned are undefined (their
+ * partial rows were not written).
+ */
+kvq_status kvq_sparse_mla_attention_split_nvfp4_ds_mla(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h,
+    int64_t num_tokens, int32_t num_heads,
+    const int32_t* indices, int64_t indices_stride, int32_t topk,
+    const uint8_t* kv_cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride,
+    float softmax_scale,
+    void* out, int64_t out_stride_t, int64_t out_stride_h,
+    float* lse, int64_t lse_stride_t,
+    int32_t num_splits, void* workspace, int64_t workspace_bytes,
+    int32_t* d_status, kvq_stream_t stream);
+kvq_status kvq_sparse_mla_attention_split_fp8_ds_mla(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h,
+    int64_t num_tokens, int32_t num_heads,
+    const int32_t* indices, int64_t indices_stride, int32_t topk,
+    const uint8_t* kv_cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride,
+    float softmax_scale,
+    void* out, int64_t out_stride_t, int64_t out_stride_h,
+    float* lse, int64_t lse_stride_t,
+    int32_t num_splits, void* workspace, int64_t workspace_bytes,
+    int32_t* d_status, kvq_stream_t stream);
+
 /*
  * kvq_prefill_mla_attention_nvfp4_ds_mla -- dense prefill over the 352-byte
  * cache: the query tokens of each request attend to every position of its

@@ -262,3 +262,39 @@ def test_attention_zero_tokens_is_noop(lib):
 def test_fp8_attention_requires_656_byte_entries(lib):
     assert lib.kvq_sparse_mla_attention_fp8_ds_mla(*attention_args(entry_stride=352, block_stride=64 * 352)) == 1
     assert "656" in err(lib), err(lib)
+
+
+def split_args(num_splits=4, workspace=A, workspace_bytes=1 << 30, **over):
+    args = attention_args(**over)
+    return args[:-2] + [num_splits, workspace, workspace_bytes] + args[-2:]
+
+
+@no_gpu_only
+@pytest.mark.parametrize("over,needle", [
+    (dict(num_splits=0), "num_splits must be in [1, 32]"),
+    (dict(num_splits=33), "num_splits must be in [1, 32]"),
+    (dict(workspace=None), "workspace"),
+    (dict(workspace=A + 8), "workspace"),
+    (dict(workspace_bytes=4 * 128 * 4 * 513 * 4 - 16), "at least 4202496 bytes"),
+    (dict(num_heads=129), "num_heads must be in [1, 128]"),
+])
+def test_split_attention_rejects_bad_arguments_on_host(lib, over, needle):
+    assert lib.kvq_sparse_mla_attention_split_nvfp4_ds_mla(*split_args(**over)) == 1
+    assert needle in err(lib), err(lib)
+
+
+def test_split_workspace_bytes(lib):
+    f = lib.kvq_sparse_mla_attention_split_workspace_bytes
+    assert f(4, 128, 4) == 4 * 128 * 4 * 513 * 4
+    assert f(1, 1, 1) == 2064                          # 2052 rounded up to 16
+    assert f(0, 128, 8) == 0
+    assert f(-1, 128, 8) == -1 and f(4, 0, 8) == -1 and f(4, 128, 0) == -1
+
+
+@no_gpu_only
+def test_split_attention_one_range_needs_no_workspace(lib):
+    """One range is the plain entry point: no workspace needed; without a
+    device the call passes the argument checks and fails at the device query."""
+    assert lib.kvq_sparse_mla_attention_split_nvfp4_ds_mla(*split_args(num_splits=1, workspace=None,
+                                                                        workspace_bytes=0)) == 3
+    assert "kvq_sparse_mla_attention_split_nvfp4_ds_mla" in err(lib)

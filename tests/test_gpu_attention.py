@@ -511,3 +511,81 @@ def test_query_row_layouts(kvq, oracle_mod, layout):
                                                           p.softmax_scale, p.max_query_len)
     torch.cuda.synchronize()
     check_prefill(oracle_mod, pcache, p, out, lse)
+
+
+# ---------------------------------------------------------------------------
+# split-key decode: ranges of a token's keys combined by a second launch
+# ---------------------------------------------------------------------------
+
+SPLIT_CASES = [
+    # one token, 128 heads, top-2048 in 8 ranges of 4 tiles
+    ("1 token top2048 x8", dict(num_tokens=1, num_heads=128, topk=2048, num_blocks=64, block_size=64, seed=531,
+                                p_unused=0.1), 8),
+    # a ragged list (not whole tiles) in 5 ranges of 2 tiles, the last one partial
+    ("3 tokens top300 x5", dict(num_tokens=3, num_heads=64, topk=300, num_blocks=16, block_size=64, seed=532,
+                                p_unused=0.2), 5),
+    # more ranges than tiles: ranges 2 and 3 are empty
+    ("2 tokens top100 x4", dict(num_tokens=2, num_heads=16, topk=100, num_blocks=8, block_size=64, seed=533), 4),
+    # the 32-range maximum over a 33-tile list; one head
+    ("4 tokens top2100 x32 H1", dict(num_tokens=4, num_heads=1, topk=2100, num_blocks=64, block_size=64,
+                                     seed=534, p_unused=0.3), 32),
+]
+
+
+@pytest.mark.parametrize("fmt", sorted(FORMATS))
+@pytest.mark.parametrize("name,kw,splits", SPLIT_CASES, ids=[c[0] for c in SPLIT_CASES])
+def test_split_parity(kvq, oracle_mod, name, kw, splits, fmt):
+    w = wl.make_attention(name, **kw)
+    cache = host_cache(oracle_mod, w.fill, fmt=fmt)
+    dcache = torch.from_numpy(cache).to(DEV)
+    T, H = w.q.shape[0], w.q.shape[1]
+    out = torch.full((T, H, 512), -7.0, dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((T, H), -7.0, dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    fn = getattr(kvq, FORMATS[fmt][4].replace("sparse_mla_attention", "sparse_mla_attention_split"))
+    fn(w.q.to(DEV), w.indices.to(DEV), dcache, w.softmax_scale, num_splits=splits, out=out, lse=lse, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    check(oracle_mod, cache, w.q, wl.host(w.indices), w.softmax_scale, out, lse)
+
+
+def test_split_ranges_without_valid_keys(kvq, oracle_mod):
+    """Token 0: its second range (keys 64-127) all unused, weight 0; token 1:
+    no valid key at all (out = 0, lse = -inf, as unsplit); a bad slot in
+    token 2 is skipped and reported."""
+    w = wl.make_attention("split holes", 3, 32, 256, 8, 64, 535)
+    idx = wl.host(w.indices).copy()
+    idx[0, 64:128] = -1
+    idx[1, :] = -1
+    idx[2, 10] = 8 * 64 + 3                           # past the cache
+    w.indices = torch.from_numpy(idx)
+    cache = host_cache(oracle_mod, w.fill)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, lse = kvq.kvq_sparse_mla_attention_split_nvfp4_ds_mla(w.q.to(DEV), w.indices.to(DEV),
+                                                               torch.from_numpy(cache).to(DEV), w.softmax_scale,
+                                                               num_splits=4, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == kvq.STATUS_BAD_INDEX
+    idx[2, 10] = -1                                   # the oracle skips it the same way
+    check(oracle_mod, cache, w.q, idx, w.softmax_scale, out, lse)
+
+
+def test_split_small_batch_full_cache(kvq, oracle_mod, threads):
+    """The small-batch case the split serves: 8 decode tokens x 128 heads,
+    top-2048 over the 65536 x 64 cache, ranges from default_num_splits, the
+    workspace reused by a second call; every token against the oracle."""
+    fill = wl.make_fill("split fill", 65536, 64, 1006, DEV, rng="device")
+    cache_host = host_cache(oracle_mod, fill, threads)
+    cache = torch.from_numpy(cache_host).to(DEV)
+    w = wl.make_attention("split decode", 8, 128, 2048, 65536, 64, 536, DEV, p_unused=0.1, fill=fill,
+                          rng="device")
+    del fill
+    splits = kvq.default_num_splits(8, 2048)
+    assert splits > 1
+    ws = torch.empty(kvq.kvq_sparse_mla_attention_split_workspace_bytes(8, 128, splits), dtype=torch.uint8,
+                     device=DEV)
+    for _ in range(2):
+        out, lse = kvq.kvq_sparse_mla_attention_split_nvfp4_ds_mla(w.q, w.indices, cache, w.softmax_scale,
+                                                                   num_splits=splits, workspace=ws)
+        torch.cuda.synchronize()
+        check(oracle_mod, cache_host, w.q, wl.host(w.indices), w.softmax_scale, out, lse, threads)
