@@ -25,6 +25,7 @@ __all__ = [
     "kvq_prefill_mla_attention_nvfp4_ds_mla", "kvq_prefill_mla_attention_fp8_ds_mla",
     "kvq_sparse_mla_attention_split_nvfp4_ds_mla", "kvq_sparse_mla_attention_split_fp8_ds_mla",
     "kvq_sparse_mla_attention_split_workspace_bytes", "default_num_splits", "ATTN_MAX_SPLITS",
+    "kvq_sparse_mla_attention_split_nvfp4_ds_mla_noalloc", "NOALLOC_SCRATCH_BYTES",
     "kvq_last_error_string", "kvq_version", "library_path", "load_library",
     "NVFP4_DS_MLA_ENTRY_BYTES", "FP8_DS_MLA_ENTRY_BYTES", "STATUS_BAD_INDEX", "STATUS_BAD_BATCH",
     "STATUS_TIMEOUT",
@@ -37,6 +38,7 @@ STATUS_BAD_INDEX = 0x1
 STATUS_BAD_BATCH = 0x2
 STATUS_TIMEOUT = 0x4
 ATTN_MAX_SPLITS = 32
+NOALLOC_SCRATCH_BYTES = 24 << 20
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lib = None
@@ -78,6 +80,9 @@ _SIGNATURES = {
     "kvq_sparse_mla_attention_split_fp8_ds_mla": [_P, _I64, _I64, _I64, _I32, _P, _I64, _I32, _P, _I64, _I32,
                                                   _I64, _I64, ctypes.c_float, _P, _I64, _I64, _P, _I64,
                                                   _I32, _P, _I64, _P, _P],
+    "kvq_sparse_mla_attention_split_nvfp4_ds_mla_noalloc": [_P, _I64, _I64, _I64, _I32, _P, _I64, _I32, _P, _I64,
+                                                            _I32, _I64, _I64, ctypes.c_float, _P, _I64, _I64, _P,
+                                                            _I64, _I32, _P, _P],
 }
 
 
@@ -350,6 +355,16 @@ def kvq_sparse_mla_attention_split_fp8_ds_mla(q, indices, kv_cache, softmax_scal
                       lse, status, stream, split=(num_splits, workspace))
 
 
+def kvq_sparse_mla_attention_split_nvfp4_ds_mla_noalloc(q, indices, kv_cache, softmax_scale: float, num_splits=None,
+                                                        out=None, lse=None, status=None, stream=None):
+    """The split-key decode with its partial results in the library's own
+    fixed array (NOALLOC_SCRATCH_BYTES per GPU) instead of a workspace, for
+    callers that cannot allocate device memory when they call in.  Calls that
+    overlap on the GPU race on that array: order them."""
+    return _attention("kvq_sparse_mla_attention_split_nvfp4_ds_mla_noalloc", 352, q, indices, kv_cache,
+                      softmax_scale, out, lse, status, stream, split=(num_splits, "noalloc"))
+
+
 def _attention(cname, entry, q, indices, kv_cache, softmax_scale, out, lse, status, stream, split=None):
     _need(q.dtype == torch.bfloat16 and q.is_cuda and q.dim() == 3 and q.shape[2] == 576
           and q.stride(2) == 1, "q: expected a CUDA bf16 [T, H, 576] tensor with unit inner stride")
@@ -372,7 +387,10 @@ def _attention(cname, entry, q, indices, kv_cache, softmax_scale, out, lse, stat
             kv_cache.shape[0], kv_cache.shape[1], kv_cache.stride(0), kv_cache.stride(1), float(softmax_scale),
             out.data_ptr(), out.stride(0), out.stride(1), None if lse is False else lse.data_ptr(),
             0 if lse is False else lse.stride(0)]
-    if split is not None:
+    if split is not None and split[1] == "noalloc":
+        num_splits = split[0] if split[0] is not None else default_num_splits(T, indices.shape[1], q.device)
+        args += [int(num_splits)]
+    elif split is not None:
         num_splits, workspace = split
         if num_splits is None:
             num_splits = default_num_splits(T, indices.shape[1], q.device)

@@ -2,6 +2,7 @@
 // host-side validation, device check, launch on the caller's stream, status.
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "kvq.h"
@@ -553,6 +554,82 @@ kvq_status kvq_selftest_convert(uint32_t first_bits, int64_t count, uint8_t* e4m
   return launched(fn, kvq::launch_selftest_convert(first_bits, count, e4m3_lo, e4m3_hi, e2m1_lo,
                                                    e2m1_hi, bf16_out, num_sms,
                                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// The split-key decode without a caller workspace
+// ---------------------------------------------------------------------------
+//
+// Some callers cannot allocate device memory when they call in: a serving
+// engine that reserved the GPU's memory for its own pools at start-up (a
+// cudaMalloc would fail, or take memory its key-value cache counts on), or
+// host code on a latency-critical path, where an allocation can synchronise
+// the device and stall its other streams.  For them the partial results of
+// the split-key decode live in one fixed array that the library holds on
+// every GPU that loads it, for the life of the process.
+
+// Device storage of the partial results; in host code this name is only a
+// stand-in for the symbol, never a device address.
+static __device__ __align__(256) unsigned char g_split_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// The device address of g_split_scratch on the current device, looked up on
+// the first call made with that device current and kept.
+cudaError_t split_scratch(void** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_split_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *ptr = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_sparse_mla_attention_split_nvfp4_ds_mla_noalloc(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h, int64_t num_tokens, int32_t num_heads,
+    const int32_t* indices, int64_t indices_stride, int32_t topk, const uint8_t* kv_cache, int64_t num_blocks,
+    int32_t block_size, int64_t block_stride, int64_t entry_stride, float softmax_scale, void* out,
+    int64_t out_stride_t, int64_t out_stride_h, float* lse, int64_t lse_stride_t, int32_t num_splits,
+    int32_t* d_status, kvq_stream_t stream) {
+  const char* fn = "kvq_sparse_mla_attention_split_nvfp4_ds_mla_noalloc";
+  KVQ_REQUIRE(num_tokens >= 0 && num_heads >= 1 && num_splits >= 1,
+              "%s: num_tokens must be >= 0, num_heads and num_splits >= 1", fn);
+  const int64_t need =
+      num_splits > 1 ? kvq_sparse_mla_attention_split_workspace_bytes(num_tokens, num_heads, num_splits) : 0;
+  KVQ_REQUIRE(need >= 0 && need <= KVQ_NOALLOC_SCRATCH_BYTES,
+              "%s: %lld tokens x %d heads x %d key ranges need %lld bytes of partial results, more than the "
+              "library's fixed %lld-byte array holds (at most %lld (token, head, range) rows); use fewer ranges "
+              "or tokens, or kvq_sparse_mla_attention_split_nvfp4_ds_mla with a workspace",
+              fn, static_cast<long long>(num_tokens), num_heads, num_splits, static_cast<long long>(need),
+              static_cast<long long>(KVQ_NOALLOC_SCRATCH_BYTES),
+              static_cast<long long>(KVQ_NOALLOC_SCRATCH_BYTES / ((KVQ_MLA_NOPE_DIM + 1) * 4)));
+  void* scratch = nullptr;
+  if (need > 0) {
+    if (kvq_status st = check_device(fn)) return st;
+    const cudaError_t e = split_scratch(&scratch);
+    if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "%s: the scratch array's address: %s", fn, cudaGetErrorString(e));
+  }
+  return kvq_sparse_mla_attention_split_nvfp4_ds_mla(
+      q, q_stride_t, q_stride_h, num_tokens, num_heads, indices, indices_stride, topk, kv_cache, num_blocks,
+      block_size, block_stride, entry_stride, softmax_scale, out, out_stride_t, out_stride_h, lse, lse_stride_t,
+      num_splits, scratch, need > 0 ? KVQ_NOALLOC_SCRATCH_BYTES : 0, d_status, stream);
 }
 
 const char* kvq_last_error_string(void) { return g_last_error.c_str(); }

@@ -346,6 +346,42 @@ kvq_status kvq_sparse_mla_attention_split_fp8_ds_mla(
     int32_t num_splits, void* workspace, int64_t workspace_bytes,
     int32_t* d_status, kvq_stream_t stream);
 
+#define KVQ_NOALLOC_SCRATCH_BYTES (24LL << 20)   /* fixed partial-result array, per GPU */
+
+/*
+ * kvq_sparse_mla_attention_split_nvfp4_ds_mla_noalloc -- the split-key decode
+ * of kvq_sparse_mla_attention_split_nvfp4_ds_mla (same arguments except the
+ * workspace, same results bit for bit) for callers that cannot allocate
+ * device memory when they call in: an engine that reserved the GPU's memory
+ * for its own pools at start-up, or host code on a latency-critical path
+ * where an allocation can synchronise the device.  The paper has no
+ * counterpart: this is an addition of this library.  The partial results go
+ * to one array of KVQ_NOALLOC_SCRATCH_BYTES (24 MiB) that the library holds
+ * on every GPU that loads it, until the process exits; a call whose
+ * num_tokens x num_heads x num_splits rows need more
+ * (kvq_sparse_mla_attention_split_workspace_bytes) returns
+ * KVQ_ERR_INVALID_ARG and launches nothing.  num_splits = 1 uses no array.
+ * The first call on a device (with that device current) looks up the array's
+ * device address and keeps it: make that first call before any stream
+ * capture.  Every call shares the array, which keeps the last call's
+ * contents; nothing in it has to start at zero (a call writes every partial
+ * row it reads before reading it), but calls that overlap on the GPU (other
+ * streams, other host threads) race on it, so the caller orders them.  The
+ * call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine.
+ */
+kvq_status kvq_sparse_mla_attention_split_nvfp4_ds_mla_noalloc(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h,
+    int64_t num_tokens, int32_t num_heads,
+    const int32_t* indices, int64_t indices_stride, int32_t topk,
+    const uint8_t* kv_cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride,
+    float softmax_scale,
+    void* out, int64_t out_stride_t, int64_t out_stride_h,
+    float* lse, int64_t lse_stride_t,
+    int32_t num_splits,
+    int32_t* d_status, kvq_stream_t stream);
+
 /*
  * kvq_prefill_mla_attention_nvfp4_ds_mla -- dense prefill over the 352-byte
  * cache: the query tokens of each request attend to every position of its

@@ -298,3 +298,12 @@ def test_split_attention_one_range_needs_no_workspace(lib):
     assert lib.kvq_sparse_mla_attention_split_nvfp4_ds_mla(*split_args(num_splits=1, workspace=None,
                                                                         workspace_bytes=0)) == 3
     assert "kvq_sparse_mla_attention_split_nvfp4_ds_mla" in err(lib)
+
+
+@no_gpu_only
+def test_noalloc_split_refuses_oversized_calls_on_host(lib):
+    """128 heads x 32 ranges x 3 tokens need more than the fixed array holds."""
+    args = attention_args(num_tokens=3, ost=128 * 512)
+    args = args[:-2] + [32] + args[-2:]
+    assert lib.kvq_sparse_mla_attention_split_nvfp4_ds_mla_noalloc(*args) == 1
+    assert "more than the library's fixed 25165824-byte array" in err(lib), err(lib)
