@@ -510,9 +510,12 @@ kvq_status kvq_sparse_mla_attention_fp8_ds_mla(
 }
 
 int64_t kvq_sparse_mla_attention_split_workspace_bytes(int64_t num_tokens, int32_t num_heads, int32_t num_splits) {
-  if (num_tokens < 0 || num_heads < 1 || num_splits < 1 || num_tokens >= (int64_t{1} << 40)) return -1;
+  constexpr int64_t kRowBytes = (KVQ_MLA_NOPE_DIM + 1) * 4;
+  if (num_tokens < 0 || num_heads < 1 || num_splits < 1 ||
+      num_tokens > (INT64_MAX - 15) / kRowBytes / num_heads / num_splits)
+    return -1;
   const int64_t rows = num_tokens * num_heads * num_splits;
-  return (rows * (KVQ_MLA_NOPE_DIM + 1) * 4 + 15) / 16 * 16;
+  return (rows * kRowBytes + 15) / 16 * 16;
 }
 
 kvq_status kvq_sparse_mla_attention_split_nvfp4_ds_mla(

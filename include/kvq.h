@@ -292,7 +292,8 @@ kvq_status kvq_sparse_mla_attention_fp8_ds_mla(
  * kvq_sparse_mla_attention_split_workspace_bytes -- bytes of device workspace
  * the split-key decode below needs for num_tokens x num_heads query rows cut
  * into num_splits key ranges: num_tokens * num_heads * num_splits * 513 * 4,
- * rounded up to 16.  -1 for a negative or zero argument.
+ * rounded up to 16.  -1 for a negative or zero argument or a size past
+ * INT64_MAX.
  */
 int64_t kvq_sparse_mla_attention_split_workspace_bytes(int64_t num_tokens, int32_t num_heads,
                                                        int32_t num_splits);

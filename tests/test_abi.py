@@ -289,6 +289,7 @@ def test_split_workspace_bytes(lib):
     assert f(1, 1, 1) == 2064                          # 2052 rounded up to 16
     assert f(0, 128, 8) == 0
     assert f(-1, 128, 8) == -1 and f(4, 0, 8) == -1 and f(4, 128, 0) == -1
+    assert f(1 << 62, 128, 32) == -1                  # past INT64_MAX
 
 
 @no_gpu_only
