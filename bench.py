@@ -587,6 +587,49 @@ def time_extra(step: GpuStep):
                 "frac": round(flops / us / 1e6 / peak_tf, 4), "context_positions": int(ctx.sum()),
                 "method": "CUDA events"}
             del pw, po, pl
+        # one request with the longest context of the nvfp4 prefill batch, 16
+        # query tokens x 128 heads: 32 CTAs, against the split over its
+        # context (default_prefill_num_splits ranges, a combine launch)
+        pw = wl.prefill_attention(step.g3, dev)
+        b = int(np.argmax(wl.host(pw.context_lens)))
+        qs = wl.host(pw.query_start)
+        one = wl.PrefillWorkload("one request", None, pw.q[int(qs[b]):int(qs[b + 1])].contiguous(),
+                                 torch.tensor([0, 16], dtype=torch.int32, device=dev), pw.context_lens[b:b + 1],
+                                 pw.block_table[b:b + 1], pw.softmax_scale, 16)
+        ctx1 = int(wl.host(one.context_lens)[0])
+        po = torch.empty((16, 128, 512), dtype=torch.bfloat16, device=dev)
+        pl = torch.empty((16, 128), dtype=torch.float32, device=dev)
+        splits = kvq.default_prefill_num_splits(16, 128, 1, ctx1)
+        ws = torch.empty(kvq.kvq_sparse_mla_attention_split_workspace_bytes(16, 128, splits), dtype=torch.uint8,
+                         device=dev)
+        flops = ATTN_FLOPS_PER_SLOT_HEAD * 128 * ctx1 * 16
+        peak_tf, peak_src = measured_peak_tflops()
+        for name, fn in (
+                (f"prefill_mla_attention_nvfp4_ds_mla B=1 q=16 H=128 ctx {ctx1} (one range)",
+                 lambda: kvq.kvq_prefill_mla_attention_nvfp4_ds_mla(one.q, one.query_start, one.context_lens,
+                                                                    one.block_table, step.cache3, one.softmax_scale,
+                                                                    16, out=po, lse=pl)),
+                (f"prefill_mla_attention_split_nvfp4_ds_mla B=1 q=16 H=128 ctx {ctx1} ({splits} ranges)",
+                 lambda: kvq.kvq_prefill_mla_attention_split_nvfp4_ds_mla(one.q, one.query_start, one.context_lens,
+                                                                          one.block_table, step.cache3,
+                                                                          one.softmax_scale, 16,
+                                                                          max_context_len=ctx1, num_splits=splits,
+                                                                          workspace=ws, out=po, lse=pl))):
+            times = []
+            for r in range(8):
+                a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b2.record()
+                torch.cuda.synchronize()
+                if r >= 2:
+                    times.append(a.elapsed_time(b2))
+            us = statistics.median(times) * 1e3
+            out[name] = {"units": 16, "us": round(us, 2), "tflops": round(flops / us / 1e6, 1), "bound": "tensor",
+                         "peak_tflops": peak_tf, "peak": f"{peak_src} bf16 burst",
+                         "frac": round(flops / us / 1e6 / peak_tf, 4),
+                         "method": "CUDA events, repeated launches (its 12 MB of entries stay in L2)"}
+        del pw, one, po, pl, ws
     # fp8_ds_mla cache fill: 2,097,152 tokens, one launch
     f4 = step.g4.fill
     times = []

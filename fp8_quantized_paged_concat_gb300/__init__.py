@@ -26,6 +26,8 @@ __all__ = [
     "kvq_sparse_mla_attention_split_nvfp4_ds_mla", "kvq_sparse_mla_attention_split_fp8_ds_mla",
     "kvq_sparse_mla_attention_split_workspace_bytes", "default_num_splits", "ATTN_MAX_SPLITS",
     "kvq_sparse_mla_attention_split_nvfp4_ds_mla_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "kvq_prefill_mla_attention_split_nvfp4_ds_mla", "kvq_prefill_mla_attention_split_fp8_ds_mla",
+    "default_prefill_num_splits",
     "kvq_last_error_string", "kvq_version", "library_path", "load_library",
     "NVFP4_DS_MLA_ENTRY_BYTES", "FP8_DS_MLA_ENTRY_BYTES", "STATUS_BAD_INDEX", "STATUS_BAD_BATCH",
     "STATUS_TIMEOUT",
@@ -80,6 +82,12 @@ _SIGNATURES = {
     "kvq_sparse_mla_attention_split_fp8_ds_mla": [_P, _I64, _I64, _I64, _I32, _P, _I64, _I32, _P, _I64, _I32,
                                                   _I64, _I64, ctypes.c_float, _P, _I64, _I64, _P, _I64,
                                                   _I32, _P, _I64, _P, _P],
+    "kvq_prefill_mla_attention_split_nvfp4_ds_mla": [_P, _I64, _I64, _I64, _I32, _P, _P, _I32, _I32, _P, _I64,
+                                                     _I32, _P, _I64, _I32, _I64, _I64, ctypes.c_float, _P, _I64,
+                                                     _I64, _P, _I64, _I32, _I32, _P, _I64, _P, _P],
+    "kvq_prefill_mla_attention_split_fp8_ds_mla": [_P, _I64, _I64, _I64, _I32, _P, _P, _I32, _I32, _P, _I64,
+                                                   _I32, _P, _I64, _I32, _I64, _I64, ctypes.c_float, _P, _I64,
+                                                   _I64, _P, _I64, _I32, _I32, _P, _I64, _P, _P],
     "kvq_sparse_mla_attention_split_nvfp4_ds_mla_noalloc": [_P, _I64, _I64, _I64, _I32, _P, _I64, _I32, _P, _I64,
                                                             _I32, _I64, _I64, ctypes.c_float, _P, _I64, _I64, _P,
                                                             _I64, _I32, _P, _P],
@@ -425,8 +433,46 @@ def kvq_prefill_mla_attention_fp8_ds_mla(q, query_start, context_lens, block_tab
                     kv_cache, softmax_scale, max_query_len, out, lse, status, stream)
 
 
+def default_prefill_num_splits(max_query_len: int, num_heads: int, batch_size: int, max_context_len: int,
+                               device=None) -> int:
+    """Context ranges per request for a dense prefill: as many as one wave
+    of CTAs holds (two per 128-row block and range), at most
+    ATTN_MAX_SPLITS and one per 64-position tile of the longest context."""
+    blocks = -(-max_query_len * num_heads // 128) * batch_size
+    if blocks <= 0:
+        return 1
+    sms = torch.cuda.get_device_properties(device if device is not None else torch.cuda.current_device()
+                                           ).multi_processor_count
+    tiles = (max_context_len + 63) // 64
+    return max(1, min(ATTN_MAX_SPLITS, tiles, sms // (2 * blocks)))
+
+
+def kvq_prefill_mla_attention_split_nvfp4_ds_mla(q, query_start, context_lens, block_table, kv_cache,
+                                                 softmax_scale: float, max_query_len: int, max_context_len=None,
+                                                 num_splits=None, workspace=None, out=None, lse=None, status=None,
+                                                 stream=None):
+    """The dense prefill of kvq_prefill_mla_attention_nvfp4_ds_mla with each
+    request's context split into num_splits ranges sized from
+    max_context_len (default: the longest context, read from the device)
+    and combined by a second launch.  workspace as for the split decode
+    (allocated here when None)."""
+    return _prefill("kvq_prefill_mla_attention_split_nvfp4_ds_mla", 352, q, query_start, context_lens, block_table,
+                    kv_cache, softmax_scale, max_query_len, out, lse, status, stream,
+                    split=(max_context_len, num_splits, workspace))
+
+
+def kvq_prefill_mla_attention_split_fp8_ds_mla(q, query_start, context_lens, block_table, kv_cache,
+                                               softmax_scale: float, max_query_len: int, max_context_len=None,
+                                               num_splits=None, workspace=None, out=None, lse=None, status=None,
+                                               stream=None):
+    """The same split dense prefill straight from the 656-byte fp8_ds_mla cache."""
+    return _prefill("kvq_prefill_mla_attention_split_fp8_ds_mla", 656, q, query_start, context_lens, block_table,
+                    kv_cache, softmax_scale, max_query_len, out, lse, status, stream,
+                    split=(max_context_len, num_splits, workspace))
+
+
 def _prefill(cname, entry, q, query_start, context_lens, block_table, kv_cache, softmax_scale, max_query_len,
-             out, lse, status, stream):
+             out, lse, status, stream, split=None):
     _need(q.dtype == torch.bfloat16 and q.is_cuda and q.dim() == 3 and q.shape[2] == 576
           and q.stride(2) == 1, "q: expected a CUDA bf16 [T, H, 576] tensor with unit inner stride")
     T, H = q.shape[0], q.shape[1]
@@ -448,12 +494,25 @@ def _prefill(cname, entry, q, query_start, context_lens, block_table, kv_cache, 
     if lse is not False:
         _need(lse.dtype == torch.float32 and lse.is_cuda and tuple(lse.shape) == (T, H) and lse.stride(1) == 1,
               "lse: expected a CUDA fp32 [T, H] tensor with unit inner stride")
-    _call(cname, q.data_ptr(), q.stride(0), q.stride(1), T, H, query_start.data_ptr(), context_lens.data_ptr(),
-          B, int(max_query_len), block_table.data_ptr(), block_table.stride(0), block_table.shape[1],
-          kv_cache.data_ptr(), kv_cache.shape[0], kv_cache.shape[1], kv_cache.stride(0), kv_cache.stride(1),
-          float(softmax_scale), out.data_ptr(), out.stride(0), out.stride(1),
-          None if lse is False else lse.data_ptr(), 0 if lse is False else lse.stride(0), _status_ptr(status),
-          _stream(stream, q.device))
+    args = [q.data_ptr(), q.stride(0), q.stride(1), T, H, query_start.data_ptr(), context_lens.data_ptr(),
+            B, int(max_query_len), block_table.data_ptr(), block_table.stride(0), block_table.shape[1],
+            kv_cache.data_ptr(), kv_cache.shape[0], kv_cache.shape[1], kv_cache.stride(0), kv_cache.stride(1),
+            float(softmax_scale), out.data_ptr(), out.stride(0), out.stride(1),
+            None if lse is False else lse.data_ptr(), 0 if lse is False else lse.stride(0)]
+    if split is not None:
+        max_context_len, num_splits, workspace = split
+        if max_context_len is None:
+            max_context_len = int(context_lens.max().item()) if B > 0 else 0
+        if num_splits is None:
+            num_splits = default_prefill_num_splits(int(max_query_len), H, B, max_context_len, q.device)
+        need = kvq_sparse_mla_attention_split_workspace_bytes(T, H, num_splits) if num_splits > 1 else 0
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        if workspace is not None:
+            _need(workspace.is_cuda and workspace.is_contiguous(), "workspace: expected a contiguous CUDA tensor")
+        args += [int(max_context_len), int(num_splits), None if workspace is None else workspace.data_ptr(),
+                 0 if workspace is None else workspace.numel() * workspace.element_size()]
+    _call(cname, *args, _status_ptr(status), _stream(stream, q.device))
     return out, (None if lse is False else lse)
 
 

@@ -2,6 +2,7 @@
 // host-side validation, device check, launch on the caller's stream, status.
 #include <cstdarg>
 #include <cstdio>
+#include <algorithm>
 #include <mutex>
 #include <string>
 
@@ -390,7 +391,8 @@ kvq_status prefill_common(
     const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width, const uint8_t* kv_cache,
     int64_t num_blocks, int32_t block_size, int64_t block_stride, int64_t entry_stride, float softmax_scale,
     void* out, int64_t out_stride_t, int64_t out_stride_h, float* lse, int64_t lse_stride_t, int32_t* d_status,
-    kvq_stream_t stream) {
+    kvq_stream_t stream, int32_t num_splits = 1,
+    int32_t max_context_len = 0, void* workspace = nullptr, int64_t workspace_bytes = 0) {
   KVQ_REQUIRE(num_tokens >= 0 && batch_size >= 0 && max_query_len >= 0,
               "%s: num_tokens, batch_size and max_query_len must be >= 0", fn);
   if (num_tokens == 0 || batch_size == 0 || max_query_len == 0) return ok();
@@ -421,8 +423,29 @@ kvq_status prefill_common(
                                      entry_stride, entry_bytes))
     return s;
   KVQ_REQUIRE(d_status == nullptr || aligned(d_status, 4), "%s: d_status misaligned", fn);
+  KVQ_REQUIRE(num_splits >= 1 && num_splits <= KVQ_ATTN_MAX_SPLITS, "%s: num_splits must be in [1, %d] (got %d)",
+              fn, KVQ_ATTN_MAX_SPLITS, num_splits);
+  if (num_splits > 1) {
+    const int64_t need = kvq_sparse_mla_attention_split_workspace_bytes(num_tokens, num_heads, num_splits);
+    KVQ_REQUIRE(max_context_len >= 0, "%s: max_context_len must be >= 0", fn);
+    KVQ_REQUIRE((int64_t{max_query_len} * num_heads + 127) / 128 * 2 * num_splits < (int64_t{1} << 31),
+                "%s: too many CTAs (grid.x)", fn);
+    KVQ_REQUIRE(workspace != nullptr && aligned(workspace, 16) && need >= 0 && workspace_bytes >= need,
+                "%s: workspace must be non-NULL, 16-byte aligned and at least %lld bytes (got %lld)", fn,
+                static_cast<long long>(need), static_cast<long long>(workspace_bytes));
+  }
   if (kvq_status s = check_device(fn)) return s;
   kvq::AttentionArgs a{};
+  a.num_splits = num_splits;
+  if (num_splits > 1) {
+    // whole 64-key tiles per range, sized from max_context_len; the last range
+    // of a request also takes every position past num_splits ranges
+    const int64_t tiles = (int64_t{max_context_len} + 63) / 64;
+    a.split_keys = static_cast<int32_t>(std::max<int64_t>(1, (tiles + num_splits - 1) / num_splits) * 64);
+    const int64_t rows = num_tokens * num_heads * num_splits;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_lse = static_cast<float*>(workspace) + rows * KVQ_MLA_NOPE_DIM;
+  }
   a.q = q;
   a.q_stride_t = q_stride_t;
   a.q_stride_h = q_stride_h;
@@ -483,6 +506,40 @@ kvq_status kvq_prefill_mla_attention_fp8_ds_mla(
                         softmax_scale, out, out_stride_t, out_stride_h, lse, lse_stride_t, d_status, stream);
 }
 
+kvq_status kvq_prefill_mla_attention_split_nvfp4_ds_mla(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h, int64_t num_tokens, int32_t num_heads,
+    const int32_t* query_start, const int32_t* context_lens, int32_t batch_size, int32_t max_query_len,
+    const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width, const uint8_t* kv_cache,
+    int64_t num_blocks, int32_t block_size, int64_t block_stride, int64_t entry_stride, float softmax_scale,
+    void* out, int64_t out_stride_t, int64_t out_stride_h, float* lse, int64_t lse_stride_t,
+    int32_t max_context_len, int32_t num_splits, void* workspace, int64_t workspace_bytes, int32_t* d_status,
+    kvq_stream_t stream) {
+  return prefill_common("kvq_prefill_mla_attention_split_nvfp4_ds_mla", KVQ_NVFP4_DS_MLA_ENTRY_BYTES,
+                        num_splits > 1 ? kvq::launch_prefill_mla_attention_split_nvfp4
+                                       : kvq::launch_prefill_mla_attention_nvfp4,
+                        q, q_stride_t, q_stride_h, num_tokens, num_heads, query_start, context_lens, batch_size,
+                        max_query_len, block_table, block_table_stride, block_table_width, kv_cache, num_blocks,
+                        block_size, block_stride, entry_stride, softmax_scale, out, out_stride_t, out_stride_h, lse,
+                        lse_stride_t, d_status, stream, num_splits, max_context_len, workspace, workspace_bytes);
+}
+
+kvq_status kvq_prefill_mla_attention_split_fp8_ds_mla(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h, int64_t num_tokens, int32_t num_heads,
+    const int32_t* query_start, const int32_t* context_lens, int32_t batch_size, int32_t max_query_len,
+    const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width, const uint8_t* kv_cache,
+    int64_t num_blocks, int32_t block_size, int64_t block_stride, int64_t entry_stride, float softmax_scale,
+    void* out, int64_t out_stride_t, int64_t out_stride_h, float* lse, int64_t lse_stride_t,
+    int32_t max_context_len, int32_t num_splits, void* workspace, int64_t workspace_bytes, int32_t* d_status,
+    kvq_stream_t stream) {
+  return prefill_common("kvq_prefill_mla_attention_split_fp8_ds_mla", KVQ_FP8_DS_MLA_ENTRY_BYTES,
+                        num_splits > 1 ? kvq::launch_prefill_mla_attention_split_fp8
+                                       : kvq::launch_prefill_mla_attention_fp8,
+                        q, q_stride_t, q_stride_h, num_tokens, num_heads, query_start, context_lens, batch_size,
+                        max_query_len, block_table, block_table_stride, block_table_width, kv_cache, num_blocks,
+                        block_size, block_stride, entry_stride, softmax_scale, out, out_stride_t, out_stride_h, lse,
+                        lse_stride_t, d_status, stream, num_splits, max_context_len, workspace, workspace_bytes);
+}
+
 kvq_status kvq_sparse_mla_attention_nvfp4_ds_mla(
     const void* q, int64_t q_stride_t, int64_t q_stride_h, int64_t num_tokens, int32_t num_heads,
     const int32_t* indices, int64_t indices_stride, int32_t topk, const uint8_t* kv_cache,
@@ -510,7 +567,7 @@ kvq_status kvq_sparse_mla_attention_fp8_ds_mla(
 }
 
 int64_t kvq_sparse_mla_attention_split_workspace_bytes(int64_t num_tokens, int32_t num_heads, int32_t num_splits) {
-  constexpr int64_t kRowBytes = (KVQ_MLA_NOPE_DIM + 1) * 4;
+  constexpr int64_t kRowBytes = (KVQ_MLA_NOPE_DIM + 2) * 4;
   if (num_tokens < 0 || num_heads < 1 || num_splits < 1 ||
       num_tokens > (INT64_MAX - 15) / kRowBytes / num_heads / num_splits)
     return -1;
@@ -622,7 +679,7 @@ kvq_status kvq_sparse_mla_attention_split_nvfp4_ds_mla_noalloc(
               "or tokens, or kvq_sparse_mla_attention_split_nvfp4_ds_mla with a workspace",
               fn, static_cast<long long>(num_tokens), num_heads, num_splits, static_cast<long long>(need),
               static_cast<long long>(KVQ_NOALLOC_SCRATCH_BYTES),
-              static_cast<long long>(KVQ_NOALLOC_SCRATCH_BYTES / ((KVQ_MLA_NOPE_DIM + 1) * 4)));
+              static_cast<long long>(KVQ_NOALLOC_SCRATCH_BYTES / ((KVQ_MLA_NOPE_DIM + 2) * 4)));
   void* scratch = nullptr;
   if (need > 0) {
     if (kvq_status st = check_device(fn)) return st;

@@ -464,8 +464,9 @@ struct Block {
   int32_t row0;               // dense: first packed (token, head) row of the block
   int32_t rows;               // rows of the block (query rows past it are zero)
   int32_t request;            // dense: the request
-  int32_t n_keys;             // keys of the block: topk, or its split's share (sparse), the context (dense)
-  int32_t split;              // sparse, split over the keys: the block's range of the list
+  int32_t n_keys;             // keys of the block: topk or the context, or the block's range of them
+  int32_t split;              // split over the keys: the block's range
+  int32_t key0;               // dense: the context position of the block's key 0
   const int32_t* idx;         // sparse: the block's part of the token's slot list
 };
 
@@ -502,11 +503,24 @@ __device__ __forceinline__ Block block_of(const AttentionArgs& a, uint32_t bx, u
       return b;
     }
     const int64_t total = static_cast<int64_t>(q1 - q0) * a.num_heads;
-    b.row0 = static_cast<int32_t>(bx >> 1) * kRows;
+    const int32_t ctx = max(0, __ldg(a.context_lens + b.request));
+    uint32_t unit = bx >> 1;
+    if (a.num_splits > 1) {
+      // CTA pair (row block, split): context positions [split * split_keys,
+      // +split_keys), the last range also every position past the others
+      const uint32_t splits = static_cast<uint32_t>(a.num_splits);
+      const uint32_t rb = unit / splits;
+      b.split = static_cast<int32_t>(unit - rb * splits);
+      unit = rb;
+      b.key0 = b.split * a.split_keys;
+      b.n_keys = b.split == a.num_splits - 1 ? max(0, ctx - b.key0) : max(0, min(ctx - b.key0, a.split_keys));
+    } else {
+      b.n_keys = ctx;
+    }
+    b.row0 = static_cast<int32_t>(unit) * kRows;
     b.live = q1 > q0 && b.row0 < total;
     b.token0 = q0;
     b.rows = static_cast<int32_t>(min(static_cast<int64_t>(kRows), total - b.row0));
-    b.n_keys = max(0, __ldg(a.context_lens + b.request));
   }
   return b;
 }
@@ -563,7 +577,7 @@ __device__ __forceinline__ int32_t key_raw(const AttentionArgs& a, const Block& 
   if constexpr (K == Keys::kSparse) {
     return __ldg(b.idx + j);
   } else {
-    const uint32_t col = a.block_div.div(static_cast<uint32_t>(j));
+    const uint32_t col = a.block_div.div(static_cast<uint32_t>(b.key0 + j));
     if (col >= static_cast<uint32_t>(a.block_table_width)) return INT32_MAX;
     const int32_t id = __ldg(a.block_table + b.request * a.block_table_stride + col);
     return id < 0 ? INT32_MAX : id;
@@ -579,7 +593,8 @@ __device__ __forceinline__ bool raw_valid(const AttentionArgs& a, int32_t raw) {
 // Entry of key j from its raw index, or nullptr when the key is unused or out
 // of range (bad_index set for the latter).
 template <Keys K>
-__device__ __forceinline__ const uint8_t* key_entry(const AttentionArgs& a, int32_t raw, int j, bool& bad_index) {
+__device__ __forceinline__ const uint8_t* key_entry(const AttentionArgs& a, const Block& b, int32_t raw, int j,
+                                                    bool& bad_index) {
   if (raw < 0) return nullptr;
   if (!raw_valid<K>(a, raw)) {
     bad_index = true;
@@ -590,8 +605,9 @@ __device__ __forceinline__ const uint8_t* key_entry(const AttentionArgs& a, int3
     blk = a.block_div.div(static_cast<uint32_t>(raw));
     off = static_cast<uint32_t>(raw) - blk * static_cast<uint32_t>(a.block_size);
   } else {
+    const uint32_t p = static_cast<uint32_t>(b.key0 + j);
     blk = static_cast<uint32_t>(raw);
-    off = static_cast<uint32_t>(j) - a.block_div.div(static_cast<uint32_t>(j)) * static_cast<uint32_t>(a.block_size);
+    off = p - a.block_div.div(p) * static_cast<uint32_t>(a.block_size);
   }
   return a.cache + static_cast<int64_t>(blk) * a.block_stride + static_cast<int64_t>(off) * a.entry_stride;
 }
@@ -791,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
   const uint8_t* cur = nullptr;
   int32_t raw_next = 0, raw_next2 = 0;
   if (is_producer) {
-    cur = key_entry<K>(a, key_raw<K>(a, blk, r), r, bad_index);
+    cur = key_entry<K>(a, blk, key_raw<K>(a, blk, r), r, bad_index);
     raw_next = key_raw<K>(a, blk, kTile + r);
     raw_next2 = key_raw<K>(a, blk, 2 * kTile + r);
     if (n_tiles > 0) {
@@ -944,7 +960,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
       if (lane == 0) mbar_arrive(a_full0 + 8 * sa);
       // the next tile's group-A loads now: they are consumed a whole group-B
       // decode and one wait later
-      const uint8_t* next = t + 1 < n_tiles ? key_entry<K>(a, raw_next, (t + 1) * kTile + r, bad_index) : nullptr;
+      const uint8_t* next =
+          t + 1 < n_tiles ? key_entry<K>(a, blk, raw_next, (t + 1) * kTile + r, bad_index) : nullptr;
       if (t + 1 < n_tiles) load_part<F, true>(next, a_nope0, k, ra);
       // group B: stage t % kBStages is free once P V of tile t - kBStages is done
       uint4 vb[8];
@@ -1082,7 +1099,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
       if (live) {
         bulk_store(a.part_o + prow * KVQ_MLA_NOPE_DIM + own, part_row, kHalf * 4);
         bulk_wait_read();
-        if (half == 0) a.part_lse[prow] = l_row > 0.0f ? m + log2f(l_row) : -INFINITY;
+        // both CTAs of the pair compute the same m and l; each records them,
+        // so that a range one of them did not write is seen by the combine
+        a.part_lse[prow * 2 + half] = l_row > 0.0f ? m + log2f(l_row) : -INFINITY;
       }
     } else {
       // Each thread scales its row's 256 O columns into bf16 and writes them
@@ -1137,18 +1156,30 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
 // ---------------------------------------------------------------------------
 //
 // One warp per (token, head) row; lane s holds range s's base-2 log-sum-exp
-// L_s (at most 32 ranges).  With M = max L_s and w_s = 2^(L_s - M):
+// L_s (at most 32 ranges; both CTAs of a range record it).  With M = max L_s
+// and w_s = 2^(L_s - M):
 //   out = sum_s w_s o_s / sum_s w_s,   lse = (M + log2 sum_s w_s) ln 2,
 // o_s being range s's normalised partial output (an empty range: L_s = -inf,
-// weight 0; no valid key at all: out = 0, lse = -inf, as unsplit).
+// weight 0; no valid key at all: out = 0, lse = -inf, as unsplit).  Every L_s
+// is set to NaN before the partial launch: a row with a range that no CTA
+// wrote (a query token of no request, a skipped request, a CTA that timed
+// out) keeps its outputs untouched, as unsplit.
 constexpr int kCombineWarps = 8;
+
+__global__ void fill_nan_kernel(float* p, int64_t n) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    p[i] = __int_as_float(0x7fc00000);
+}
 
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_splits_kernel(const AttentionArgs a) {
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= a.num_tokens * a.num_heads) return;          // whole warps
   const int splits = a.num_splits;
-  const float ls = lane < splits ? a.part_lse[row * splits + lane] : -INFINITY;
+  const float ls = lane < splits ? a.part_lse[(row * splits + lane) * 2] : -INFINITY;
+  const float ls1 = lane < splits ? a.part_lse[(row * splits + lane) * 2 + 1] : -INFINITY;
+  if (__any_sync(0xffffffffu, ls != ls || ls1 != ls1)) return;   // a range half not written
   float mx = ls;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -1254,7 +1285,8 @@ cudaError_t launch_attention(const AttentionArgs& a, cudaStream_t stream) {
     grid = dim3(static_cast<unsigned>(a.num_tokens * 2 * (a.num_splits > 1 ? a.num_splits : 1)));
   } else {
     const int64_t blocks = (static_cast<int64_t>(a.max_query_len) * a.num_heads + kRows - 1) / kRows;
-    grid = dim3(static_cast<unsigned>(blocks * 2), static_cast<unsigned>(a.batch_size));
+    grid = dim3(static_cast<unsigned>(blocks * 2 * (a.num_splits > 1 ? a.num_splits : 1)),
+                static_cast<unsigned>(a.batch_size));
   }
   mla_attention_kernel<F, K><<<grid, kThreads, kSmemBytes, stream>>>(args, qmap);
   return cudaGetLastError();
@@ -1266,21 +1298,31 @@ cudaError_t launch_sparse_mla_attention_nvfp4(const AttentionArgs& a, cudaStream
 cudaError_t launch_sparse_mla_attention_fp8(const AttentionArgs& a, cudaStream_t stream) {
   return launch_attention<Entry::kFp8, Keys::kSparse>(a, stream);
 }
-template <Entry F>
+template <Entry F, Keys K>
 cudaError_t launch_split(const AttentionArgs& a, cudaStream_t stream) {
-  cudaError_t e = launch_attention<F, Keys::kSparse>(a, stream);
-  if (e != cudaSuccess) return e;
   const int64_t rows = a.num_tokens * a.num_heads;
+  const int64_t n = rows * a.num_splits * 2;
+  fill_nan_kernel<<<static_cast<unsigned>(min(int64_t{1024}, (n + 255) / 256)), 256, 0, stream>>>(a.part_lse, n);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_attention<F, K>(a, stream);
+  if (e != cudaSuccess) return e;
   combine_splits_kernel<<<static_cast<unsigned>((rows + kCombineWarps - 1) / kCombineWarps), kCombineWarps * 32, 0,
                           stream>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_sparse_mla_attention_split_nvfp4(const AttentionArgs& a, cudaStream_t stream) {
-  return launch_split<Entry::kNvfp4>(a, stream);
+  return launch_split<Entry::kNvfp4, Keys::kSparse>(a, stream);
 }
 cudaError_t launch_sparse_mla_attention_split_fp8(const AttentionArgs& a, cudaStream_t stream) {
-  return launch_split<Entry::kFp8>(a, stream);
+  return launch_split<Entry::kFp8, Keys::kSparse>(a, stream);
+}
+cudaError_t launch_prefill_mla_attention_split_nvfp4(const AttentionArgs& a, cudaStream_t stream) {
+  return launch_split<Entry::kNvfp4, Keys::kDense>(a, stream);
+}
+cudaError_t launch_prefill_mla_attention_split_fp8(const AttentionArgs& a, cudaStream_t stream) {
+  return launch_split<Entry::kFp8, Keys::kDense>(a, stream);
 }
 cudaError_t launch_prefill_mla_attention_nvfp4(const AttentionArgs& a, cudaStream_t stream) {
   return launch_attention<Entry::kNvfp4, Keys::kDense>(a, stream);

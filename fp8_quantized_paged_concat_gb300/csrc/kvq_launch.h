@@ -101,14 +101,15 @@ struct AttentionArgs {
   int32_t* status;
   int32_t wave;                  // set by the launcher: CTAs resident at once (one per SM)
   int32_t q_tma;                 // set by the launcher: query rows loaded through its tensor map
-  // sparse decode split over the keys: each token's list cut into num_splits
-  // ranges of split_keys keys (whole 64-key tiles), one CTA pair per range,
-  // each writing its normalised partial output and base-2 lse to part_o /
-  // part_lse (nullptr: no split, num_splits = 1, results straight to out / lse)
+  // split over the keys: each token's list (sparse) or each request's context
+  // (dense) cut into num_splits ranges of split_keys keys (whole 64-key
+  // tiles), one CTA pair per range, each writing its normalised partial
+  // output and base-2 lse to part_o / part_lse (nullptr: no split,
+  // num_splits = 1, results straight to out / lse)
   int32_t num_splits;
   int32_t split_keys;
   float* part_o;                 // fp32 [num_tokens, num_heads, num_splits, 512]
-  float* part_lse;               // fp32 [num_tokens, num_heads, num_splits]
+  float* part_lse;               // fp32 [num_tokens, num_heads, num_splits, 2] (one per value half)
 };
 
 int64_t write_max_tokens();     // grid.x bound of the write launches
@@ -125,6 +126,8 @@ cudaError_t launch_prefill_mla_attention_nvfp4(const AttentionArgs& a, cudaStrea
 // Split-key sparse decode: the partial launch, then the combine into out / lse.
 cudaError_t launch_sparse_mla_attention_split_nvfp4(const AttentionArgs& a, cudaStream_t stream);
 cudaError_t launch_sparse_mla_attention_split_fp8(const AttentionArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill_mla_attention_split_nvfp4(const AttentionArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill_mla_attention_split_fp8(const AttentionArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_mla_attention_fp8(const AttentionArgs& a, cudaStream_t stream);
 
 struct IndexArgs {

@@ -291,7 +291,7 @@ kvq_status kvq_sparse_mla_attention_fp8_ds_mla(
 /*
  * kvq_sparse_mla_attention_split_workspace_bytes -- bytes of device workspace
  * the split-key decode below needs for num_tokens x num_heads query rows cut
- * into num_splits key ranges: num_tokens * num_heads * num_splits * 513 * 4,
+ * into num_splits key ranges: num_tokens * num_heads * num_splits * 514 * 4,
  * rounded up to 16.  -1 for a negative or zero argument or a size past
  * INT64_MAX.
  */
@@ -320,9 +320,11 @@ int64_t kvq_sparse_mla_attention_split_workspace_bytes(int64_t num_tokens, int32
  * kvq_sparse_mla_attention_split_workspace_bytes(num_tokens, num_heads,
  * num_splits) bytes (workspace_bytes says how many there are), overwritten:
  * fp32 partial rows [num_tokens, num_heads, num_splits, 512], then the fp32
- * range lse values; no other call may use it while this one runs.  After a
- * KVQ_STATUS_TIMEOUT the outputs of the tokens concerned are undefined (their
- * partial rows were not written).
+ * range lse values (two per row and range, one per value half); no other
+ * call may use it while this one runs.  The range lse values are set to NaN
+ * before the partial launch, and the combine leaves a row untouched if any
+ * of its ranges was not written (as after a KVQ_STATUS_TIMEOUT), as the
+ * plain entry point leaves the rows of a CTA that timed out.
  */
 kvq_status kvq_sparse_mla_attention_split_nvfp4_ds_mla(
     const void* q, int64_t q_stride_t, int64_t q_stride_h,
@@ -345,6 +347,49 @@ kvq_status kvq_sparse_mla_attention_split_fp8_ds_mla(
     void* out, int64_t out_stride_t, int64_t out_stride_h,
     float* lse, int64_t lse_stride_t,
     int32_t num_splits, void* workspace, int64_t workspace_bytes,
+    int32_t* d_status, kvq_stream_t stream);
+
+/*
+ * kvq_prefill_mla_attention_split_nvfp4_ds_mla,
+ * kvq_prefill_mla_attention_split_fp8_ds_mla -- the dense prefill of
+ * kvq_prefill_mla_attention_nvfp4_ds_mla / _fp8_ds_mla (the same definition,
+ * [P3] "Function and motivation" and "Key source snippets",
+ * _compute_prefill_context; the same arguments, arithmetic rules, outputs and
+ * status) split over the context, as the split-key decode above splits a
+ * token's list, for batches with few query rows over long contexts.  Each
+ * request's context is cut into num_splits ranges of whole 64-position
+ * tiles sized from max_context_len (ceil(ceil(max_context_len / 64) /
+ * num_splits) tiles; the last range of a request also takes every position
+ * past the others, so a context longer than max_context_len is still
+ * attended in full, only less evenly split).  workspace as for the split
+ * decode, sized by kvq_sparse_mla_attention_split_workspace_bytes(num_tokens,
+ * num_heads, num_splits) (num_tokens = all query tokens).  Rows of query
+ * tokens that belong to no request, or to a skipped one, are left
+ * untouched, as by the plain entry point.
+ */
+kvq_status kvq_prefill_mla_attention_split_nvfp4_ds_mla(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h,
+    int64_t num_tokens, int32_t num_heads,
+    const int32_t* query_start, const int32_t* context_lens, int32_t batch_size, int32_t max_query_len,
+    const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width,
+    const uint8_t* kv_cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride,
+    float softmax_scale,
+    void* out, int64_t out_stride_t, int64_t out_stride_h,
+    float* lse, int64_t lse_stride_t,
+    int32_t max_context_len, int32_t num_splits, void* workspace, int64_t workspace_bytes,
+    int32_t* d_status, kvq_stream_t stream);
+kvq_status kvq_prefill_mla_attention_split_fp8_ds_mla(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h,
+    int64_t num_tokens, int32_t num_heads,
+    const int32_t* query_start, const int32_t* context_lens, int32_t batch_size, int32_t max_query_len,
+    const int32_t* block_table, int64_t block_table_stride, int32_t block_table_width,
+    const uint8_t* kv_cache, int64_t num_blocks, int32_t block_size,
+    int64_t block_stride, int64_t entry_stride,
+    float softmax_scale,
+    void* out, int64_t out_stride_t, int64_t out_stride_h,
+    float* lse, int64_t lse_stride_t,
+    int32_t max_context_len, int32_t num_splits, void* workspace, int64_t workspace_bytes,
     int32_t* d_status, kvq_stream_t stream);
 
 #define KVQ_NOALLOC_SCRATCH_BYTES (24LL << 20)   /* fixed partial-result array, per GPU */

@@ -275,7 +275,7 @@ def split_args(num_splits=4, workspace=A, workspace_bytes=1 << 30, **over):
     (dict(num_splits=33), "num_splits must be in [1, 32]"),
     (dict(workspace=None), "workspace"),
     (dict(workspace=A + 8), "workspace"),
-    (dict(workspace_bytes=4 * 128 * 4 * 513 * 4 - 16), "at least 4202496 bytes"),
+    (dict(workspace_bytes=4 * 128 * 4 * 514 * 4 - 16), "at least 4210688 bytes"),
     (dict(num_heads=129), "num_heads must be in [1, 128]"),
 ])
 def test_split_attention_rejects_bad_arguments_on_host(lib, over, needle):
@@ -285,8 +285,8 @@ def test_split_attention_rejects_bad_arguments_on_host(lib, over, needle):
 
 def test_split_workspace_bytes(lib):
     f = lib.kvq_sparse_mla_attention_split_workspace_bytes
-    assert f(4, 128, 4) == 4 * 128 * 4 * 513 * 4
-    assert f(1, 1, 1) == 2064                          # 2052 rounded up to 16
+    assert f(4, 128, 4) == 4 * 128 * 4 * 514 * 4
+    assert f(1, 1, 1) == 2064                          # 2056 rounded up to 16
     assert f(0, 128, 8) == 0
     assert f(-1, 128, 8) == -1 and f(4, 0, 8) == -1 and f(4, 128, 0) == -1
     assert f(1 << 62, 128, 32) == -1                  # past INT64_MAX
@@ -308,3 +308,32 @@ def test_noalloc_split_refuses_oversized_calls_on_host(lib):
     args = args[:-2] + [32] + args[-2:]
     assert lib.kvq_sparse_mla_attention_split_nvfp4_ds_mla_noalloc(*args) == 1
     assert "more than the library's fixed 25165824-byte array" in err(lib), err(lib)
+
+
+def prefill_split_args(**over):
+    args = dict(q=A, qst=16 * 576, qsh=576, num_tokens=8, num_heads=16, query_start=A, context_lens=A,
+                batch_size=2, max_query_len=4, block_table=A, bt_stride=8, bt_width=8, kv_cache=A,
+                num_blocks=16, block_size=64, block_stride=64 * 352, entry_stride=352, scale=0.05, out=A,
+                ost=16 * 512, osh=512, lse=A, lst=16, max_context_len=500, num_splits=4, workspace=A,
+                workspace_bytes=1 << 30, d_status=None, stream=None)
+    args.update(over)
+    return list(args.values())
+
+
+@no_gpu_only
+@pytest.mark.parametrize("over,needle", [
+    (dict(num_splits=0), "num_splits must be in [1, 32]"),
+    (dict(num_splits=33), "num_splits must be in [1, 32]"),
+    (dict(workspace=None), "workspace"),
+    (dict(workspace_bytes=8 * 16 * 4 * 514 * 4 - 16), "at least 1052672 bytes"),
+    (dict(max_context_len=-1), "max_context_len"),
+])
+def test_prefill_split_rejects_bad_arguments_on_host(lib, over, needle):
+    assert lib.kvq_prefill_mla_attention_split_nvfp4_ds_mla(*prefill_split_args(**over)) == 1
+    assert needle in err(lib), err(lib)
+
+
+@no_gpu_only
+def test_prefill_split_valid_arguments_reach_the_device_check(lib):
+    assert lib.kvq_prefill_mla_attention_split_fp8_ds_mla(*prefill_split_args(entry_stride=656,
+                                                                              block_stride=64 * 656)) == 3

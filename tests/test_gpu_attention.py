@@ -589,3 +589,95 @@ def test_split_small_batch_full_cache(kvq, oracle_mod, threads):
                                                                    num_splits=splits, workspace=ws)
         torch.cuda.synchronize()
         check(oracle_mod, cache_host, w.q, wl.host(w.indices), w.softmax_scale, out, lse, threads)
+
+
+def run_prefill_split(kvq, oracle_mod, w, fmt, num_splits, max_context_len=None, requests=None):
+    cache = host_cache(oracle_mod, w.fill, fmt=fmt)
+    dcache = torch.from_numpy(cache).to(DEV)
+    T, H = w.q.shape[0], w.q.shape[1]
+    out = torch.full((T, H, 512), -7.0, dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((T, H), -7.0, dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    fn = getattr(kvq, PREFILL_FORMATS[fmt][1].replace("prefill_mla_attention", "prefill_mla_attention_split"))
+    fn(w.q.to(DEV), w.query_start.to(DEV), w.context_lens.to(DEV), w.block_table.to(DEV), dcache, w.softmax_scale,
+       w.max_query_len, max_context_len=max_context_len, num_splits=num_splits, out=out, lse=lse, status=status)
+    torch.cuda.synchronize()
+    check_prefill(oracle_mod, cache, w, out, lse, requests=requests)
+    return int(status.item()), out, lse
+
+
+@pytest.mark.parametrize("fmt", sorted(PREFILL_FORMATS))
+def test_prefill_split_long_context(kvq, oracle_mod, fmt):
+    """One request, 3 query tokens x 128 heads over 4500 positions (71
+    tiles) in 8 ranges of 9 tiles, the last one partial."""
+    w = wl.make_prefill("split long", [4500], [3], 128, 80, 64, 541)
+    status, _, _ = run_prefill_split(kvq, oracle_mod, w, fmt, 8)
+    assert status == 0
+
+
+def test_prefill_split_ragged_requests(kvq, oracle_mod):
+    """Packed rows of 20 heads, an empty context, a request with no query
+    tokens; max_context_len below the longest context (its last range takes
+    the rest); 5 ranges."""
+    w = wl.make_prefill("split ragged", [700, 0, 90, 1300], [5, 3, 0, 7], 20, 160, 16, 542)
+    status, _, _ = run_prefill_split(kvq, oracle_mod, w, "nvfp4", 5, max_context_len=600)
+    assert status == 0
+
+
+def test_prefill_split_untouched_rows(kvq, oracle_mod):
+    """Query tokens of no request (before the first one) and of a skipped
+    request (its range past num_tokens) keep their outputs; a bad block is
+    skipped and reported."""
+    w = wl.make_prefill("split holes", [200, 150], [2, 2], 32, 12, 64, 543)
+    qs = wl.host(w.query_start).copy()
+    table = wl.host(w.block_table).copy()
+    table[0, 1] = 1 << 20                            # positions 64..127 of request 0
+    w.block_table = torch.from_numpy(table)
+    # tokens 0, 1 belong to no request; request 0 = tokens 2-3, request 1 claims 2-7 (only 2-5 exist)
+    T = w.num_tokens + 2
+    q = torch.zeros((T, 32, 576), dtype=torch.bfloat16)
+    q[2:] = w.q
+    w.q = q
+    w.query_start = torch.from_numpy((qs + 2).astype(np.int32))
+    w.query_start[2] = T + 2
+    w.max_query_len = 6
+    cache = host_cache(oracle_mod, w.fill)
+    out = torch.full((T, 32, 512), -7.0, dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((T, 32), -7.0, dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kvq.kvq_prefill_mla_attention_split_nvfp4_ds_mla(w.q.to(DEV), w.query_start.to(DEV), w.context_lens.to(DEV),
+                                                     w.block_table.to(DEV), torch.from_numpy(cache).to(DEV),
+                                                     w.softmax_scale, w.max_query_len, num_splits=3, out=out,
+                                                     lse=lse, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == kvq.STATUS_BAD_INDEX | kvq.STATUS_BAD_BATCH
+    untouched = [0, 1] + list(range(4, T))
+    assert torch.all(out[untouched] == -7.0) and torch.all(lse[untouched] == -7.0)
+    check_prefill(oracle_mod, cache, w, out, lse, requests=[0])
+
+
+@pytest.mark.parametrize("fmt", sorted(PREFILL_FORMATS))
+def test_prefill_split_full_size_sampled(kvq, oracle_mod, threads, fmt):
+    """Two requests of the bench's prefill gather (contexts of the 65536 x 64
+    cache, or of the fp8 cache) with 16 query tokens x 128 heads each, split
+    with the default range count; the first two tokens of each against the
+    oracle."""
+    gather = wl.prefill_gather(DEV) if fmt == "nvfp4" else wl.fp8_gather(DEV)
+    full = wl.prefill_attention(gather, DEV)
+    cache_host = host_cache(oracle_mod, gather.fill, threads, fmt)
+    cache = torch.from_numpy(cache_host).to(DEV)
+    del gather
+    picks = [0, 1]
+    qs = wl.host(full.query_start)
+    rows = torch.from_numpy(np.concatenate([np.arange(qs[b], qs[b + 1]) for b in picks])).to(DEV)
+    sub = wl.PrefillWorkload("split sampled", None, full.q[rows], torch.tensor([0, 16, 32], dtype=torch.int32),
+                             full.context_lens[picks].cpu(), full.block_table[picks].cpu(), full.softmax_scale, 16)
+    fn = getattr(kvq, PREFILL_FORMATS[fmt][1].replace("prefill_mla_attention", "prefill_mla_attention_split"))
+    out, lse = fn(sub.q, sub.query_start.to(DEV), sub.context_lens.to(DEV), sub.block_table.to(DEV), cache,
+                  sub.softmax_scale, 16)
+    torch.cuda.synchronize()
+    keep = torch.tensor([0, 1, 16, 17])
+    check_sub = wl.PrefillWorkload("split sampled rows", None, sub.q[keep.to(DEV)].cpu(),
+                                   torch.tensor([0, 2, 4], dtype=torch.int32), sub.context_lens,
+                                   sub.block_table, sub.softmax_scale, 2)
+    check_prefill(oracle_mod, cache_host, check_sub, out[keep.to(DEV)].cpu(), lse[keep.to(DEV)].cpu(), threads)

@@ -57,7 +57,7 @@ def test_noalloc_split_decode_matches_the_workspace_entry_point(kvq, oracle_mod)
 
 
 def test_noalloc_refuses_more_rows_than_the_array_holds(kvq):
-    rows = kvq.NOALLOC_SCRATCH_BYTES // (513 * 4)
+    rows = kvq.NOALLOC_SCRATCH_BYTES // (514 * 4)
     tokens = rows // (128 * 32) + 1                   # 128 heads x 32 ranges: one token too many
     q = torch.zeros((tokens, 128, 576), dtype=torch.bfloat16, device=DEV)
     idx = torch.full((tokens, 2048), -1, dtype=torch.int32, device=DEV)
