@@ -586,7 +586,36 @@ def time_extra(step: GpuStep):
                 "bound": "tensor", "peak_tflops": peak_tf, "peak": f"{peak_src} bf16 burst",
                 "frac": round(flops / us / 1e6 / peak_tf, 4), "context_positions": int(ctx.sum()),
                 "method": "CUDA events"}
-            del pw, po, pl
+            # the pages' own flow for the same batch: gather every context
+            # into a packed bf16 workspace, then attention over it
+            ctx64 = wl.host(pw.context_lens).astype(np.int64)
+            wstarts = np.zeros(len(ctx64), np.int32)
+            wstarts[1:] = np.cumsum(ctx64)[:-1]
+            wst = torch.from_numpy(wstarts).to(dev)
+            zeros = torch.zeros(len(ctx64), dtype=torch.int32, device=dev)
+            ws = torch.empty((int(ctx64.sum()), 576), dtype=torch.bfloat16, device=dev)
+            gfn = kvq.kvq_gather_upconvert_nvfp4_ds_mla if fmt == "nvfp4_ds_mla" else kvq.kvq_gather_upconvert_fp8_ds_mla
+            times_g, times_a = [], []
+            for r in range(8):
+                e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+                e0.record()
+                gfn(cache, ws, pw.block_table, wst, zeros, batch_size=len(ctx64))
+                e1.record()
+                kvq.kvq_prefill_mla_attention_workspace(pw.q, pw.query_start, pw.context_lens, wst, ws,
+                                                        pw.softmax_scale, pw.max_query_len, out=po, lse=pl)
+                e2.record()
+                torch.cuda.synchronize()
+                if r >= 2:
+                    times_g.append(e0.elapsed_time(e1))
+                    times_a.append(e1.elapsed_time(e2))
+            ug, ua = statistics.median(times_g) * 1e3, statistics.median(times_a) * 1e3
+            out[f"prefill over gathered workspace, {fmt} B={len(ctx)} q=16 H=128"] = {
+                "units": pw.num_tokens, "us": round(ug + ua, 2), "gather_us": round(ug, 2),
+                "attention_us": round(ua, 2), "tflops": round(flops / (ug + ua) / 1e6, 1),
+                "attention_tflops": round(flops / ua / 1e6, 1), "bound": "tensor", "peak_tflops": peak_tf,
+                "peak": f"{peak_src} bf16 burst", "frac": round(flops / (ug + ua) / 1e6 / peak_tf, 4),
+                "attention_frac": round(flops / ua / 1e6 / peak_tf, 4), "method": "CUDA events"}
+            del pw, po, pl, ws
         # one request with the longest context of the nvfp4 prefill batch, 16
         # query tokens x 128 heads: 32 CTAs, against the split over its
         # context (default_prefill_num_splits ranges, a combine launch)

@@ -27,7 +27,7 @@ __all__ = [
     "kvq_sparse_mla_attention_split_workspace_bytes", "default_num_splits", "ATTN_MAX_SPLITS",
     "kvq_sparse_mla_attention_split_nvfp4_ds_mla_noalloc", "NOALLOC_SCRATCH_BYTES",
     "kvq_prefill_mla_attention_split_nvfp4_ds_mla", "kvq_prefill_mla_attention_split_fp8_ds_mla",
-    "default_prefill_num_splits",
+    "default_prefill_num_splits", "kvq_prefill_mla_attention_workspace",
     "kvq_last_error_string", "kvq_version", "library_path", "load_library",
     "NVFP4_DS_MLA_ENTRY_BYTES", "FP8_DS_MLA_ENTRY_BYTES", "STATUS_BAD_INDEX", "STATUS_BAD_BATCH",
     "STATUS_TIMEOUT",
@@ -88,6 +88,8 @@ _SIGNATURES = {
     "kvq_prefill_mla_attention_split_fp8_ds_mla": [_P, _I64, _I64, _I64, _I32, _P, _P, _I32, _I32, _P, _I64,
                                                    _I32, _P, _I64, _I32, _I64, _I64, ctypes.c_float, _P, _I64,
                                                    _I64, _P, _I64, _I32, _I32, _P, _I64, _P, _P],
+    "kvq_prefill_mla_attention_workspace": [_P, _I64, _I64, _I64, _I32, _P, _P, _P, _I32, _I32, _P, _I64, _I64,
+                                            ctypes.c_float, _P, _I64, _I64, _P, _I64, _P, _P],
     "kvq_sparse_mla_attention_split_nvfp4_ds_mla_noalloc": [_P, _I64, _I64, _I64, _I32, _P, _I64, _I32, _P, _I64,
                                                             _I32, _I64, _I64, ctypes.c_float, _P, _I64, _I64, _P,
                                                             _I64, _I32, _P, _P],
@@ -431,6 +433,41 @@ def kvq_prefill_mla_attention_fp8_ds_mla(q, query_start, context_lens, block_tab
     """The same dense prefill straight from the 656-byte fp8_ds_mla cache."""
     return _prefill("kvq_prefill_mla_attention_fp8_ds_mla", 656, q, query_start, context_lens, block_table,
                     kv_cache, softmax_scale, max_query_len, out, lse, status, stream)
+
+
+def kvq_prefill_mla_attention_workspace(q, query_start, context_lens, workspace_starts, workspace,
+                                        softmax_scale: float, max_query_len: int, out=None, lse=None, status=None,
+                                        stream=None):
+    """Dense prefill over a gathered bf16 workspace [R, >=576] (what
+    kvq_gather_upconvert_*_ds_mla writes): request b's context position p is
+    workspace row workspace_starts[b] + p, p < context_lens[b].  Returns
+    (out bf16 [T, H, 512], lse fp32 [T, H]); lse=False skips the lse output."""
+    _need(q.dtype == torch.bfloat16 and q.is_cuda and q.dim() == 3 and q.shape[2] == 576
+          and q.stride(2) == 1, "q: expected a CUDA bf16 [T, H, 576] tensor with unit inner stride")
+    T, H = q.shape[0], q.shape[1]
+    B = context_lens.shape[0] if context_lens.dim() == 1 else -1
+    for name, t, n in (("context_lens", context_lens, B), ("query_start", query_start, B + 1),
+                       ("workspace_starts", workspace_starts, B)):
+        _need(t.dtype == torch.int32 and t.is_cuda and t.dim() == 1 and t.shape[0] == n and t.is_contiguous(),
+              f"{name}: expected a contiguous CUDA int32 vector of {n}")
+    _need(workspace.dtype == torch.bfloat16 and workspace.is_cuda and workspace.dim() == 2
+          and workspace.shape[1] >= 576 and workspace.stride(1) == 1,
+          "workspace: expected a CUDA bf16 [R, >=576] tensor with unit inner stride")
+    if out is None:
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=q.device)
+    _need(out.dtype == torch.bfloat16 and out.is_cuda and tuple(out.shape) == (T, H, 512)
+          and out.stride(2) == 1, "out: expected a CUDA bf16 [T, H, 512] tensor with unit inner stride")
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    if lse is not False:
+        _need(lse.dtype == torch.float32 and lse.is_cuda and tuple(lse.shape) == (T, H) and lse.stride(1) == 1,
+              "lse: expected a CUDA fp32 [T, H] tensor with unit inner stride")
+    _call("kvq_prefill_mla_attention_workspace", q.data_ptr(), q.stride(0), q.stride(1), T, H,
+          query_start.data_ptr(), context_lens.data_ptr(), workspace_starts.data_ptr(), B, int(max_query_len),
+          workspace.data_ptr(), workspace.stride(0), workspace.shape[0], float(softmax_scale), out.data_ptr(),
+          out.stride(0), out.stride(1), None if lse is False else lse.data_ptr(),
+          0 if lse is False else lse.stride(0), _status_ptr(status), _stream(stream, q.device))
+    return out, (None if lse is False else lse)
 
 
 def default_prefill_num_splits(max_query_len: int, num_heads: int, batch_size: int, max_context_len: int,

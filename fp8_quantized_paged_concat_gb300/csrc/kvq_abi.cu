@@ -540,6 +540,67 @@ kvq_status kvq_prefill_mla_attention_split_fp8_ds_mla(
                         lse_stride_t, d_status, stream, num_splits, max_context_len, workspace, workspace_bytes);
 }
 
+kvq_status kvq_prefill_mla_attention_workspace(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h, int64_t num_tokens, int32_t num_heads,
+    const int32_t* query_start, const int32_t* context_lens, const int32_t* workspace_starts, int32_t batch_size,
+    int32_t max_query_len, const void* workspace, int64_t workspace_stride, int64_t workspace_rows,
+    float softmax_scale, void* out, int64_t out_stride_t, int64_t out_stride_h, float* lse, int64_t lse_stride_t,
+    int32_t* d_status, kvq_stream_t stream) {
+  const char* fn = "kvq_prefill_mla_attention_workspace";
+  KVQ_REQUIRE(num_tokens >= 0 && batch_size >= 0 && max_query_len >= 0 && workspace_rows >= 0,
+              "%s: num_tokens, batch_size, max_query_len and workspace_rows must be >= 0", fn);
+  if (num_tokens == 0 || batch_size == 0 || max_query_len == 0) return ok();
+  KVQ_REQUIRE(num_heads >= 1, "%s: num_heads must be >= 1 (got %d)", fn, num_heads);
+  KVQ_REQUIRE(batch_size <= 65535, "%s: batch_size must be at most 65535 (grid.y)", fn);
+  KVQ_REQUIRE(int64_t{max_query_len} * num_heads < (int64_t{1} << 31) && num_tokens < (int64_t{1} << 31),
+              "%s: max_query_len * num_heads and num_tokens must stay below 2^31", fn);
+  KVQ_REQUIRE(q != nullptr && out != nullptr, "%s: q and out must be non-NULL", fn);
+  KVQ_REQUIRE(aligned(q, 16) && aligned(out, 16), "%s: q and out must be 16-byte aligned", fn);
+  KVQ_REQUIRE(q_stride_h >= KVQ_WORKSPACE_DIM && q_stride_h % 8 == 0 && q_stride_t % 8 == 0 && q_stride_t >= 0,
+              "%s: q strides must be multiples of 8 elements with head stride >= 576", fn);
+  KVQ_REQUIRE(out_stride_h >= KVQ_MLA_NOPE_DIM && out_stride_h % 8 == 0 && out_stride_t % 8 == 0 &&
+                  out_stride_t >= (num_heads - 1) * out_stride_h + KVQ_MLA_NOPE_DIM,
+              "%s: out strides must be multiples of 8 elements and rows must not overlap", fn);
+  KVQ_REQUIRE(lse == nullptr || (aligned(lse, 4) && lse_stride_t >= num_heads),
+              "%s: lse must be 4-byte aligned with token stride >= num_heads", fn);
+  KVQ_REQUIRE(query_start != nullptr && context_lens != nullptr && workspace_starts != nullptr,
+              "%s: query_start, context_lens and workspace_starts must be non-NULL", fn);
+  KVQ_REQUIRE(aligned(query_start, 4) && aligned(context_lens, 4) && aligned(workspace_starts, 4),
+              "%s: int32 arrays must be 4-byte aligned", fn);
+  KVQ_REQUIRE(workspace_rows == 0 || (workspace != nullptr && aligned(workspace, 16)),
+              "%s: workspace must be non-NULL and 16-byte aligned", fn);
+  KVQ_REQUIRE(workspace_stride >= KVQ_WORKSPACE_DIM && workspace_stride % 8 == 0 && workspace_rows < (int64_t{1} << 31),
+              "%s: workspace row stride must be >= 576 and a multiple of 8 elements, workspace_rows below 2^31", fn);
+  KVQ_REQUIRE(softmax_scale == softmax_scale && softmax_scale > -3.0e38f && softmax_scale < 3.0e38f,
+              "%s: softmax_scale must be finite", fn);
+  KVQ_REQUIRE(d_status == nullptr || aligned(d_status, 4), "%s: d_status misaligned", fn);
+  if (kvq_status st = check_device(fn)) return st;
+  kvq::AttentionArgs a{};
+  a.q = q;
+  a.q_stride_t = q_stride_t;
+  a.q_stride_h = q_stride_h;
+  a.num_tokens = num_tokens;
+  a.num_heads = num_heads;
+  a.head_div = kvq::FastDiv::make(static_cast<uint32_t>(num_heads));
+  a.query_start = query_start;
+  a.context_lens = context_lens;
+  a.batch_size = batch_size;
+  a.max_query_len = max_query_len;
+  a.ws = workspace;
+  a.ws_stride = workspace_stride;
+  a.ws_rows = workspace_rows;
+  a.ws_starts = workspace_starts;
+  a.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634074);
+  a.out = out;
+  a.out_stride_t = out_stride_t;
+  a.out_stride_h = out_stride_h;
+  a.lse = lse;
+  a.lse_stride_t = lse_stride_t;
+  a.status = d_status;
+  if (workspace_rows == 0) a.ws = q;   // no rows: every context must be empty; the map's one row is never read
+  return launched(fn, kvq::launch_prefill_mla_attention_workspace(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kvq_status kvq_sparse_mla_attention_nvfp4_ds_mla(
     const void* q, int64_t q_stride_t, int64_t q_stride_h, int64_t num_tokens, int32_t num_heads,
     const int32_t* indices, int64_t indices_stride, int32_t topk, const uint8_t* kv_cache,

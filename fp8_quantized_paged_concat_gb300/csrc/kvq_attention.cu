@@ -455,7 +455,9 @@ __device__ __forceinline__ void e4m3x16_scaled(const uint4& c, float s, uint4& l
 // ---------------------------------------------------------------------------
 
 enum class Entry { kNvfp4, kFp8 };          // 352-byte nvfp4_ds_mla, 656-byte fp8_ds_mla
-enum class Keys { kSparse, kDense };        // per-token slot lists, a request's whole context
+// per-token slot lists; a request's whole context through its block table;
+// the same context as rows of a gathered bf16 workspace
+enum class Keys { kSparse, kDense, kWorkspace };
 
 // What one CTA works on: its query rows and its list of keys.
 struct Block {
@@ -467,6 +469,7 @@ struct Block {
   int32_t n_keys;             // keys of the block: topk or the context, or the block's range of them
   int32_t split;              // split over the keys: the block's range
   int32_t key0;               // dense: the context position of the block's key 0
+  int64_t ws_row0;            // workspace: the row of context position 0
   const int32_t* idx;         // sparse: the block's part of the token's slot list
 };
 
@@ -504,6 +507,15 @@ __device__ __forceinline__ Block block_of(const AttentionArgs& a, uint32_t bx, u
     }
     const int64_t total = static_cast<int64_t>(q1 - q0) * a.num_heads;
     const int32_t ctx = max(0, __ldg(a.context_lens + b.request));
+    if constexpr (K == Keys::kWorkspace) {
+      b.ws_row0 = __ldg(a.ws_starts + b.request);
+      if (b.ws_row0 < 0 || b.ws_row0 + ctx > a.ws_rows) {
+        // a context that does not lie inside the workspace: skipped
+        if (report && bx == 0 && threadIdx.x == 0 && a.status) atomicOr(a.status, KVQ_STATUS_BAD_BATCH);
+        b.live = false;
+        return b;
+      }
+    }
     uint32_t unit = bx >> 1;
     if (a.num_splits > 1) {
       // CTA pair (row block, split): context positions [split * split_keys,
@@ -576,6 +588,8 @@ __device__ __forceinline__ int32_t key_raw(const AttentionArgs& a, const Block& 
   if (j >= b.n_keys) return -1;
   if constexpr (K == Keys::kSparse) {
     return __ldg(b.idx + j);
+  } else if constexpr (K == Keys::kWorkspace) {
+    return 0;                                 // every position inside the context is a key
   } else {
     const uint32_t col = a.block_div.div(static_cast<uint32_t>(b.key0 + j));
     if (col >= static_cast<uint32_t>(a.block_table_width)) return INT32_MAX;
@@ -587,6 +601,7 @@ __device__ __forceinline__ int32_t key_raw(const AttentionArgs& a, const Block& 
 // Whether a key with this raw index takes part.
 template <Keys K>
 __device__ __forceinline__ bool raw_valid(const AttentionArgs& a, int32_t raw) {
+  if constexpr (K == Keys::kWorkspace) return raw >= 0;
   return raw >= 0 && (K == Keys::kSparse ? raw < a.num_slots : raw < a.num_blocks);
 }
 
@@ -709,7 +724,8 @@ __device__ __forceinline__ void write_part(uint32_t blk, uint32_t rope_blk, uint
 
 template <Entry F, Keys K>
 __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const AttentionArgs a,
-                                                                    const __grid_constant__ CUtensorMap qmap) {
+                                                                    const __grid_constant__ CUtensorMap qmap,
+                                                                    const __grid_constant__ CUtensorMap kmap) {
   const Block blk = block_of<K>(a, blockIdx.x, blockIdx.y, true);
   if (!blk.live) return;                 // uniform over the CTA, before any barrier or allocation
   extern __shared__ uint8_t smem_raw[];
@@ -736,12 +752,15 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (threadIdx.x == 32) {
+    // a stage is full when the producer warps have stored it, or (workspace
+    // keys) when the copy engine has landed it after its issuer's arrival
+    constexpr uint32_t kFullCount = K == Keys::kWorkspace ? 1 : kProducerWarps;
     for (int s = 0; s < kAStages; ++s) {
-      mbar_init(a_full0 + 8 * s, kProducerWarps);
+      mbar_init(a_full0 + 8 * s, kFullCount);
       mbar_init(a_empty0 + 8 * s, 1);
     }
     for (int s = 0; s < kBStages; ++s) {
-      mbar_init(b_full0 + 8 * s, kProducerWarps);
+      mbar_init(b_full0 + 8 * s, kFullCount);
       mbar_init(b_empty0 + 8 * s, 1);
     }
     for (int s = 0; s < 2; ++s) mbar_init(s_full0 + 8 * s, 1);
@@ -806,7 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
   PartRegs<F, false> rb;
   const uint8_t* cur = nullptr;
   int32_t raw_next = 0, raw_next2 = 0;
-  if (is_producer) {
+  if (K != Keys::kWorkspace && is_producer) {
     cur = key_entry<K>(a, blk, key_raw<K>(a, blk, r), r, bad_index);
     raw_next = key_raw<K>(a, blk, kTile + r);
     raw_next2 = key_raw<K>(a, blk, 2 * kTile + r);
@@ -941,41 +960,84 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
       if (t == n_tiles / 2) prefetch_next_wave<K>(a, warp * 32 + lane);
     }
   } else if (warp < kMmaWarp) {
-    // ---- producers: group A, then group B, of every tile ----------------------
-    // A group's loads for the next tile are issued right after this tile's
-    // group is handed over (a release waits for every access of the thread in
-    // flight, so loads go after an arrive), so that their latency hides
-    // behind the other group's decode and the waits for free stages.
-    for (int t = 0; t < n_tiles; ++t) {
-      // group A: decoded into registers, then stored once stage t % kAStages
-      // is free (the group-A K-steps of tile t - kAStages are done)
-      uint4 va[10];
-      decode_part<F, true>(cur != nullptr, ra, va);
-      const int sa = t % kAStages;
-      if (t >= kAStages && !warp_wait_or_abort(a_empty0 + 8 * sa, (t / kAStages - 1) & 1, s_abort)) break;
-      const uint32_t astage = base + kAOff + sa * kAStage;
-      write_part<true>(astage + k * kKBlock, astage + 4 * kKBlock, r, k, va);
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(a_full0 + 8 * sa);
-      // the next tile's group-A loads now: they are consumed a whole group-B
-      // decode and one wait later
-      const uint8_t* next =
-          t + 1 < n_tiles ? key_entry<K>(a, blk, raw_next, (t + 1) * kTile + r, bad_index) : nullptr;
-      if (t + 1 < n_tiles) load_part<F, true>(next, a_nope0, k, ra);
-      // group B: stage t % kBStages is free once P V of tile t - kBStages is done
-      uint4 vb[8];
-      decode_part<F, false>(cur != nullptr, rb, vb);
-      const int sb = t % kBStages;
-      if (t >= kBStages && !warp_wait_or_abort(b_empty0 + 8 * sb, (t / kBStages - 1) & 1, s_abort)) break;
-      write_part<false>(base + kBOff + sb * kBStage + k * kKBlock, 0, r, k, vb);
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_full0 + 8 * sb);
-      if (t + 1 < n_tiles) load_part<F, false>(next, b_nope0, k, rb);
-      cur = next;
-      raw_next = raw_next2;
-      raw_next2 = key_raw<K>(a, blk, (t + 3) * kTile + r);
+    if constexpr (K == Keys::kWorkspace) {
+      // ---- workspace keys: one thread has the copy engine land every tile --
+      // (the nine 8 KB blocks of a tile as tensor-map loads of 64 rows x 64
+      // dimensions, 128-byte swizzled: group A then group B, each completing
+      // its stage's full barrier).  Rows of a tile past the context (or past
+      // the workspace, zero-filled) are masked by the softmax.
+      if (warp == kFirstProducerWarp && lane == 0) {
+        int last_a[kAStages], last_b[kBStages];     // last tile issued into each stage
+        for (int s2 = 0; s2 < kAStages; ++s2) last_a[s2] = -1;
+        for (int s2 = 0; s2 < kBStages; ++s2) last_b[s2] = -1;
+        for (int t = 0; t < n_tiles; ++t) {
+          const int32_t row = static_cast<int32_t>(blk.ws_row0 + blk.key0 + static_cast<int64_t>(t) * kTile);
+          const int sa = t % kAStages;
+          if (t >= kAStages && !wait_or_abort(a_empty0 + 8 * sa, (t / kAStages - 1) & 1, s_abort)) break;
+          const uint32_t astage = base + kAOff + sa * kAStage;
+          mbar_arrive_expect_tx(a_full0 + 8 * sa, 5 * kKBlock);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) tma_load_2d(astage + j * kKBlock, &kmap, other + 64 * j, row, a_full0 + 8 * sa);
+          tma_load_2d(astage + 4 * kKBlock, &kmap, KVQ_MLA_NOPE_DIM, row, a_full0 + 8 * sa);
+          last_a[sa] = t;
+          const int sb = t % kBStages;
+          if (t >= kBStages && !wait_or_abort(b_empty0 + 8 * sb, (t / kBStages - 1) & 1, s_abort)) break;
+          const uint32_t bstage = base + kBOff + sb * kBStage;
+          mbar_arrive_expect_tx(b_full0 + 8 * sb, 4 * kKBlock);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) tma_load_2d(bstage + j * kKBlock, &kmap, own + 64 * j, row, b_full0 + 8 * sb);
+          last_b[sb] = t;
+        }
+        // Before the CTA may leave, the copies of the last tile issued into
+        // each stage have landed (normally long since consumed).
+        for (int s2 = 0; s2 < kAStages + kBStages; ++s2) {
+          const int t = s2 < kAStages ? last_a[s2] : last_b[s2 - kAStages];
+          if (t < 0) continue;
+          const uint32_t bar = s2 < kAStages ? a_full0 + 8 * s2 : b_full0 + 8 * (s2 - kAStages);
+          const int stages = s2 < kAStages ? kAStages : kBStages;
+          const long long start = clock64();
+          while (!mbar_try_wait(bar, (t / stages) & 1)) {
+            if (clock64() - start > kDrainCycles) { *s_abort = 1; break; }
+          }
+        }
+      }
+    } else {
+      // ---- producers: group A, then group B, of every tile ----------------------
+      // A group's loads for the next tile are issued right after this tile's
+      // group is handed over (a release waits for every access of the thread in
+      // flight, so loads go after an arrive), so that their latency hides
+      // behind the other group's decode and the waits for free stages.
+      for (int t = 0; t < n_tiles; ++t) {
+        // group A: decoded into registers, then stored once stage t % kAStages
+        // is free (the group-A K-steps of tile t - kAStages are done)
+        uint4 va[10];
+        decode_part<F, true>(cur != nullptr, ra, va);
+        const int sa = t % kAStages;
+        if (t >= kAStages && !warp_wait_or_abort(a_empty0 + 8 * sa, (t / kAStages - 1) & 1, s_abort)) break;
+        const uint32_t astage = base + kAOff + sa * kAStage;
+        write_part<true>(astage + k * kKBlock, astage + 4 * kKBlock, r, k, va);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(a_full0 + 8 * sa);
+        // the next tile's group-A loads now: they are consumed a whole group-B
+        // decode and one wait later
+        const uint8_t* next =
+            t + 1 < n_tiles ? key_entry<K>(a, blk, raw_next, (t + 1) * kTile + r, bad_index) : nullptr;
+        if (t + 1 < n_tiles) load_part<F, true>(next, a_nope0, k, ra);
+        // group B: stage t % kBStages is free once P V of tile t - kBStages is done
+        uint4 vb[8];
+        decode_part<F, false>(cur != nullptr, rb, vb);
+        const int sb = t % kBStages;
+        if (t >= kBStages && !warp_wait_or_abort(b_empty0 + 8 * sb, (t / kBStages - 1) & 1, s_abort)) break;
+        write_part<false>(base + kBOff + sb * kBStage + k * kKBlock, 0, r, k, vb);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_full0 + 8 * sb);
+        if (t + 1 < n_tiles) load_part<F, false>(next, b_nope0, k, rb);
+        cur = next;
+        raw_next = raw_next2;
+        raw_next2 = key_raw<K>(a, blk, (t + 3) * kTile + r);
+      }
     }
   } else if (lane == 0) {
     // ---- MMA issue (one thread) -------------------------------------------
@@ -1267,6 +1329,22 @@ bool query_tensor_map(const AttentionArgs& a, CUtensorMap* map) {
   return r == CUDA_SUCCESS;
 }
 
+// Tensor map of a gathered bf16 workspace [ws_rows, 576] (row stride
+// ws_stride elements): tiles of 64 dimensions x 64 rows, 128-byte swizzled,
+// the layout of one key block of a stage; rows past ws_rows read as zeros
+// (with no rows at all, one row of q stands in: no tile is then loaded).
+bool workspace_tensor_map(const AttentionArgs& a, CUtensorMap* map) {
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return false;
+  const cuuint64_t dims[2] = {KVQ_WORKSPACE_DIM, static_cast<cuuint64_t>(a.ws_rows > 0 ? a.ws_rows : 1)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.ws_stride) * 2};
+  const cuuint32_t box[2] = {64, kTile};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.ws), dims, strides, box, elem_strides,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <Entry F, Keys K>
 cudaError_t launch_attention(const AttentionArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(mla_attention_kernel<F, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1277,9 +1355,11 @@ cudaError_t launch_attention(const AttentionArgs& a, cudaStream_t stream) {
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess) return e;
   AttentionArgs args = a;
   args.wave = sms;                      // one CTA per SM
-  CUtensorMap qmap;
+  CUtensorMap qmap, kmap;
   std::memset(&qmap, 0, sizeof(qmap));
+  std::memset(&kmap, 0, sizeof(kmap));
   args.q_tma = query_tensor_map<K>(a, &qmap) ? 1 : 0;
+  if (K == Keys::kWorkspace && !workspace_tensor_map(a, &kmap)) return cudaErrorInvalidValue;
   dim3 grid;
   if constexpr (K == Keys::kSparse) {
     grid = dim3(static_cast<unsigned>(a.num_tokens * 2 * (a.num_splits > 1 ? a.num_splits : 1)));
@@ -1288,7 +1368,7 @@ cudaError_t launch_attention(const AttentionArgs& a, cudaStream_t stream) {
     grid = dim3(static_cast<unsigned>(blocks * 2 * (a.num_splits > 1 ? a.num_splits : 1)),
                 static_cast<unsigned>(a.batch_size));
   }
-  mla_attention_kernel<F, K><<<grid, kThreads, kSmemBytes, stream>>>(args, qmap);
+  mla_attention_kernel<F, K><<<grid, kThreads, kSmemBytes, stream>>>(args, qmap, kmap);
   return cudaGetLastError();
 }
 
@@ -1323,6 +1403,9 @@ cudaError_t launch_prefill_mla_attention_split_nvfp4(const AttentionArgs& a, cud
 }
 cudaError_t launch_prefill_mla_attention_split_fp8(const AttentionArgs& a, cudaStream_t stream) {
   return launch_split<Entry::kFp8, Keys::kDense>(a, stream);
+}
+cudaError_t launch_prefill_mla_attention_workspace(const AttentionArgs& a, cudaStream_t stream) {
+  return launch_attention<Entry::kNvfp4, Keys::kWorkspace>(a, stream);   // keys are bf16: no entry format
 }
 cudaError_t launch_prefill_mla_attention_nvfp4(const AttentionArgs& a, cudaStream_t stream) {
   return launch_attention<Entry::kNvfp4, Keys::kDense>(a, stream);

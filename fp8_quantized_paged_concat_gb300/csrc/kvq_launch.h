@@ -108,6 +108,12 @@ struct AttentionArgs {
   // num_splits = 1, results straight to out / lse)
   int32_t num_splits;
   int32_t split_keys;
+  // dense prefill over a gathered bf16 workspace: request b's context
+  // positions are rows ws_starts[b] .. + context_lens[b] of ws
+  const void* ws;                // bf16 [ws_rows, >= 576], row stride ws_stride elements
+  int64_t ws_stride;
+  int64_t ws_rows;
+  const int32_t* ws_starts;      // [batch_size]
   float* part_o;                 // fp32 [num_tokens, num_heads, num_splits, 512]
   float* part_lse;               // fp32 [num_tokens, num_heads, num_splits, 2] (one per value half)
 };
@@ -127,6 +133,8 @@ cudaError_t launch_prefill_mla_attention_nvfp4(const AttentionArgs& a, cudaStrea
 cudaError_t launch_sparse_mla_attention_split_nvfp4(const AttentionArgs& a, cudaStream_t stream);
 cudaError_t launch_sparse_mla_attention_split_fp8(const AttentionArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_mla_attention_split_nvfp4(const AttentionArgs& a, cudaStream_t stream);
+// Dense prefill whose keys are rows of a gathered bf16 workspace.
+cudaError_t launch_prefill_mla_attention_workspace(const AttentionArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_mla_attention_split_fp8(const AttentionArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_mla_attention_fp8(const AttentionArgs& a, cudaStream_t stream);
 

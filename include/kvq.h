@@ -392,6 +392,37 @@ kvq_status kvq_prefill_mla_attention_split_fp8_ds_mla(
     int32_t max_context_len, int32_t num_splits, void* workspace, int64_t workspace_bytes,
     int32_t* d_status, kvq_stream_t stream);
 
+/*
+ * kvq_prefill_mla_attention_workspace -- the dense prefill attention of
+ * kvq_prefill_mla_attention_nvfp4_ds_mla over the bf16 workspace that
+ * kvq_gather_upconvert_nvfp4_ds_mla / _fp8_ds_mla fill: the pages' own
+ * prefill flow ([P3] "Key source snippets", _compute_prefill_context: the
+ * context gathered into the bf16 workspace, then attention over it).
+ * Request b's context position p is workspace row workspace_starts[b] + p
+ * (576 bf16 values, NoPE then RoPE), p < context_lens[b].  Same definition,
+ * arithmetic, outputs and status as the quantized-cache prefill; over the
+ * workspace that the gather wrote from the same cache the results are equal
+ * bit for bit.  The keys arrive by tensor-map copies (no decode in the
+ * attention), so the pair of calls pays off when many query rows share a
+ * context: the gather decodes it once, the fused prefill once per CTA.
+ * workspace: bf16, 16-byte aligned, workspace_rows rows (< 2^31) of
+ * workspace_stride >= 576 elements (a multiple of 8).  Rows that a tile
+ * reads past a request's context (up to 63 more, or up to the end of the
+ * workspace, past which zeros are read) must hold finite values, as the
+ * gather's packed output does.  A request whose context does not lie inside
+ * the workspace is skipped (KVQ_STATUS_BAD_BATCH, its rows untouched).
+ */
+kvq_status kvq_prefill_mla_attention_workspace(
+    const void* q, int64_t q_stride_t, int64_t q_stride_h,
+    int64_t num_tokens, int32_t num_heads,
+    const int32_t* query_start, const int32_t* context_lens, const int32_t* workspace_starts,
+    int32_t batch_size, int32_t max_query_len,
+    const void* workspace, int64_t workspace_stride, int64_t workspace_rows,
+    float softmax_scale,
+    void* out, int64_t out_stride_t, int64_t out_stride_h,
+    float* lse, int64_t lse_stride_t,
+    int32_t* d_status, kvq_stream_t stream);
+
 #define KVQ_NOALLOC_SCRATCH_BYTES (24LL << 20)   /* fixed partial-result array, per GPU */
 
 /*

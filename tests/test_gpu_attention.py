@@ -681,3 +681,99 @@ def test_prefill_split_full_size_sampled(kvq, oracle_mod, threads, fmt):
                                    torch.tensor([0, 2, 4], dtype=torch.int32), sub.context_lens,
                                    sub.block_table, sub.softmax_scale, 2)
     check_prefill(oracle_mod, cache_host, check_sub, out[keep.to(DEV)].cpu(), lse[keep.to(DEV)].cpu(), threads)
+
+
+# ---------------------------------------------------------------------------
+# dense prefill over a gathered bf16 workspace (gather, then attention)
+# ---------------------------------------------------------------------------
+
+def gather_workspace(kvq, w, dcache, fmt, pad_rows=0):
+    """The gather of every request's context into one packed bf16 workspace:
+    returns (workspace [sum(ctx) + pad_rows, 576], workspace_starts int32 [B])."""
+    ctx = wl.host(w.context_lens).astype(np.int64)
+    starts = np.zeros(len(ctx), np.int32)
+    starts[1:] = np.cumsum(ctx)[:-1]
+    total = int(ctx.sum())
+    ws = torch.zeros((total + pad_rows, 576), dtype=torch.bfloat16, device=DEV)
+    if total:
+        gather = getattr(kvq, "kvq_gather_upconvert_nvfp4_ds_mla" if fmt == "nvfp4" else
+                         "kvq_gather_upconvert_fp8_ds_mla")
+        gather(dcache, ws[:total], w.block_table.to(DEV), torch.from_numpy(starts).to(DEV),
+               torch.zeros(len(ctx), dtype=torch.int32, device=DEV), batch_size=len(ctx))
+    return ws, torch.from_numpy(starts).to(DEV)
+
+
+@pytest.mark.parametrize("fmt", sorted(PREFILL_FORMATS))
+@pytest.mark.parametrize("name,kw", PREFILL_CASES, ids=[c[0] for c in PREFILL_CASES])
+def test_workspace_prefill_equals_fused(kvq, oracle_mod, name, kw, fmt):
+    """Gather + attention over the workspace gives, bit for bit, what the
+    fused prefill reads straight from the cache; both against the oracle."""
+    w = wl.make_prefill(name, **kw)
+    cache = host_cache(oracle_mod, w.fill, fmt=fmt)
+    dcache = torch.from_numpy(cache).to(DEV)
+    q = w.q.to(DEV)
+    ws, starts = gather_workspace(kvq, w, dcache, fmt)
+    out, lse = kvq.kvq_prefill_mla_attention_workspace(q, w.query_start.to(DEV), w.context_lens.to(DEV), starts, ws,
+                                                       w.softmax_scale, w.max_query_len)
+    ref_out, ref_lse = getattr(kvq, PREFILL_FORMATS[fmt][1])(q, w.query_start.to(DEV), w.context_lens.to(DEV),
+                                                              w.block_table.to(DEV), dcache, w.softmax_scale,
+                                                              w.max_query_len)
+    torch.cuda.synchronize()
+    qs = wl.host(w.query_start)
+    rows = slice(int(qs[0]), int(qs[-1]))                 # tokens of some request
+    assert torch.equal(out[rows].view(torch.int16), ref_out[rows].view(torch.int16))
+    assert torch.equal(lse[rows].view(torch.int32), ref_lse[rows].view(torch.int32))
+    check_prefill(oracle_mod, cache, w, out, lse)
+
+
+def test_workspace_prefill_4k_and_padding(kvq, oracle_mod, threads):
+    """Contexts of 4096 and 4500 positions (the last tile of the second one
+    partial), the workspace longer than the contexts (zeroed rows past them)."""
+    w = wl.make_prefill("ws 4k", [4096, 4500], [2, 1], 128, 160, 64, 561)
+    cache = host_cache(oracle_mod, w.fill, threads)
+    ws, starts = gather_workspace(kvq, w, torch.from_numpy(cache).to(DEV), "nvfp4", pad_rows=100)
+    out, lse = kvq.kvq_prefill_mla_attention_workspace(w.q.to(DEV), w.query_start.to(DEV), w.context_lens.to(DEV),
+                                                       starts, ws, w.softmax_scale, w.max_query_len)
+    torch.cuda.synchronize()
+    check_prefill(oracle_mod, cache, w, out, lse, threads)
+
+
+def test_workspace_prefill_bad_ranges(kvq, oracle_mod):
+    """A request whose context runs past the workspace and one that starts
+    before it are skipped (KVQ_STATUS_BAD_BATCH, rows untouched); the third
+    is computed."""
+    w = wl.make_prefill("ws bad", [100, 90, 80], [2, 1, 2], 16, 12, 64, 562)
+    cache = host_cache(oracle_mod, w.fill)
+    ws, starts = gather_workspace(kvq, w, torch.from_numpy(cache).to(DEV), "nvfp4")
+    bad = starts.clone()
+    bad[0] = int(ws.shape[0]) - 50                    # 100 positions from 50 rows before the end
+    bad[1] = -1
+    T = w.num_tokens
+    out = torch.full((T, 16, 512), -7.0, dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((T, 16), -7.0, dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kvq.kvq_prefill_mla_attention_workspace(w.q.to(DEV), w.query_start.to(DEV), w.context_lens.to(DEV), bad, ws,
+                                            w.softmax_scale, w.max_query_len, out=out, lse=lse, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == kvq.STATUS_BAD_BATCH
+    assert torch.all(out[:3] == -7.0) and torch.all(lse[:3] == -7.0)
+    check_prefill(oracle_mod, cache, w, out, lse, requests=[2])
+
+
+@pytest.mark.parametrize("fmt", sorted(PREFILL_FORMATS))
+def test_workspace_prefill_full_size_equals_fused(kvq, oracle_mod, threads, fmt):
+    """The bench's prefill workloads (32 requests over 7k-34k positions of the
+    nvfp4 cache, 16 over the fp8 cache; 16 query tokens x 128 heads each):
+    gather + workspace attention equal to the fused prefill bit for bit."""
+    gather = wl.prefill_gather(DEV) if fmt == "nvfp4" else wl.fp8_gather(DEV)
+    w = wl.prefill_attention(gather, DEV)
+    cache = torch.from_numpy(host_cache(oracle_mod, gather.fill, threads, fmt)).to(DEV)
+    del gather
+    ws, starts = gather_workspace(kvq, w, cache, fmt)
+    out, lse = kvq.kvq_prefill_mla_attention_workspace(w.q, w.query_start, w.context_lens, starts, ws,
+                                                       w.softmax_scale, w.max_query_len)
+    ref_out, ref_lse = getattr(kvq, PREFILL_FORMATS[fmt][1])(w.q, w.query_start, w.context_lens, w.block_table,
+                                                              cache, w.softmax_scale, w.max_query_len)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32))
