@@ -1,7 +1,9 @@
 // kvq_attention.cu -- MLA attention read straight from the quantized paged
 // caches (352-byte nvfp4_ds_mla and 656-byte fp8_ds_mla entries), on the
 // fifth-generation tensor cores (tcgen05, accumulators in TMEM).  It is the
-// consumer that makes the bf16 workspace unnecessary, in two forms:
+// consumer that makes the bf16 workspace unnecessary, in two forms (and, as
+// a third key mode, the same dense prefill over a workspace that a gather
+// filled, its keys landed by the copy engine):
 //   - sparse decode: each token attends to its own top-k list of global slots
 //     (vLLM PR #51724, "Enable W4A16 DSA: NVFP4 DS-MLA KV cache format for the
 //     FlashMLA Sparse backend", "Key source snippets" (flashmla_sparse.py):
@@ -50,6 +52,11 @@
 //     reference maximum moves only when a tile exceeds it by 2^8), write P as
 //     bf16 into TMEM and rescale their O row when the reference moved; the
 //     denominator sums the bf16-rounded P.
+// Start-up: the query rows arrive by nine tensor-map copies (the own
+// dimensions through the idle key stages into TMEM); the epilogue writes each
+// output row by one bulk copy.  Split over the keys (small batches): a CTA
+// pair per (row block, key range) writes a normalised fp32 partial row and
+// its base-2 log-sum-exp, and combine_splits_kernel weighs the ranges.
 //
 // Every wait is bounded; on expiry (or when another role of the CTA gave up)
 // the CTA records KVQ_STATUS_TIMEOUT, stops issuing work, waits (with its own
