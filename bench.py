@@ -900,6 +900,39 @@ def run_prefill_only(query_len: int) -> int:
     return 0
 
 
+def run_workspace_prefill_only(query_len: int) -> int:
+    """Profiler hook: the case of run_prefill_only by the gather-then-attend
+    flow (the contexts gathered into a packed bf16 workspace, then the
+    prefill over it), 3 times."""
+    import fp8_quantized_paged_concat_gb300 as kvq
+    kvq.load_library()
+    dev = torch.device("cuda:0")
+    fill = wl.make_fill("prefill profiling fill 8192x64", 8192, 64, 1007, dev, rng="device")
+    cache = torch.zeros((8192, 64, 352), dtype=torch.uint8, device=dev)
+    kvq.kvq_write_nvfp4_ds_mla(fill.kv_c, fill.k_pe, cache, fill.slot_mapping)
+    g = np.random.Generator(np.random.PCG64(1007))
+    w = wl.make_prefill("prefill profiling case", g.integers(4096, 16384, 8, endpoint=True), [query_len] * 8, 128,
+                        8192, 64, 1007, dev, fill=fill, rng="device")
+    ctx = wl.host(w.context_lens).astype(np.int64)
+    starts = np.zeros(len(ctx), np.int32)
+    starts[1:] = np.cumsum(ctx)[:-1]
+    wst = torch.from_numpy(starts).to(dev)
+    ws = torch.empty((int(ctx.sum()), 576), dtype=torch.bfloat16, device=dev)
+    zeros = torch.zeros(len(ctx), dtype=torch.int32, device=dev)
+    for r in range(3):
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record()
+        kvq.kvq_gather_upconvert_nvfp4_ds_mla(cache, ws, w.block_table, wst, zeros, batch_size=len(ctx))
+        b.record()
+        kvq.kvq_prefill_mla_attention_workspace(w.q, w.query_start, w.context_lens, wst, ws, w.softmax_scale,
+                                                w.max_query_len)
+        c.record()
+        torch.cuda.synchronize()
+        print(f"gather {a.elapsed_time(b) * 1e3:.1f} us + prefill over the workspace q={query_len}: "
+              f"{b.elapsed_time(c) * 1e3:.1f} us", flush=True)
+    return 0
+
+
 def run_attention_only(tokens: int) -> int:
     """Profiler hook: the attention alone on a small cache (a few hundred MB)."""
     import fp8_quantized_paged_concat_gb300 as kvq
@@ -978,6 +1011,8 @@ def main(argv=None):
     p.add_argument("--attention-only", type=int, default=0, metavar="T",
                    help="profiler hook: T decode tokens of the sparse MLA attention (128 heads, top-2048 "
                         "over an 8192 x 64 cache), 3 launches, times printed; nothing else runs")
+    p.add_argument("--workspace-prefill-only", type=int, default=0, metavar="Q",
+                   help="profiler hook: the prefill case by gather + prefill over the workspace")
     p.add_argument("--prefill-only", type=int, default=0, metavar="Q",
                    help="profiler hook: the dense prefill alone, 8 requests with contexts of 4k-16k, Q new "
                         "tokens x 128 heads each, over an 8192 x 64 cache, 3 launches; nothing else runs")
@@ -991,6 +1026,8 @@ def main(argv=None):
         return run_kernel_only(args.kernel_only)
     if args.prefill_only > 0:
         return run_prefill_only(args.prefill_only)
+    if args.workspace_prefill_only > 0:
+        return run_workspace_prefill_only(args.workspace_prefill_only)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
