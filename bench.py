@@ -527,6 +527,29 @@ def time_extra(step: GpuStep):
                 "bound": "tensor", "peak_tflops": peak_tf, "peak": f"{peak_src} bf16 burst",
                 "frac": round(flops / us / 1e6 / peak_tf, 4), "gbs": round(nbytes / us / 1e3, 1),
                 "valid_slots": n_valid, "method": "CUDA events"}
+            if fmt == "nvfp4_ds_mla":
+                # the same batch as decoded early in a sequence: only the first
+                # 512 entries of each list are used (a 512-position context),
+                # the rest -1; the tiles past the last used entry are skipped
+                short = aw.indices.clone()
+                short[:, 512:] = -1
+                times = []
+                for r in range(8):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    fn(aw.q, short, cache, aw.softmax_scale, out=ao, lse=al)
+                    b.record()
+                    torch.cuda.synchronize()
+                    if r >= 2:
+                        times.append(a.elapsed_time(b))
+                us = statistics.median(times) * 1e3
+                n_short = int((short >= 0).sum())
+                flops_s = ATTN_FLOPS_PER_SLOT_HEAD * 128 * n_short
+                out[f"sparse_mla_attention_{fmt} T=4096 H=128 top-2048, 512 used"] = {
+                    "units": aw.num_tokens, "us": round(us, 2), "tflops": round(flops_s / us / 1e6, 1),
+                    "bound": "tensor", "peak_tflops": peak_tf, "peak": f"{peak_src} bf16 burst",
+                    "frac": round(flops_s / us / 1e6 / peak_tf, 4), "valid_slots": n_short, "method": "CUDA events"}
+                del short
             del aw, ao, al
         # a small decode batch: 8 tokens x 128 heads x top-2048 over the same
         # nvfp4 cache, one CTA pair per token (16 CTAs on the GPU) against

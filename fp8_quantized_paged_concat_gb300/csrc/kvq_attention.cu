@@ -108,7 +108,8 @@ constexpr uint32_t kBOff = kAOff + kAStages * kAStage;       // group B: 4 own-N
 constexpr uint32_t kBStage = 4 * kKBlock;
 constexpr uint32_t kMiscOff = kBOff + kBStages * kBStage;
 constexpr uint32_t kBiasOff = kMiscOff + 256;                // per softmax warp: 64 fp32 score biases
-constexpr uint32_t kSmemBytes = kBiasOff + kSoftmaxWarps * 256 + 1024;   // + alignment
+constexpr uint32_t kLastOff = kBiasOff + kSoftmaxWarps * 256;  // per warp: the last valid key (list search)
+constexpr uint32_t kSmemBytes = kLastOff + 64 + 1024;          // + alignment
 static_assert(kSmemBytes <= 232448, "shared memory budget of one sm_103a CTA");
 // The key stages (group A then group B, contiguous) are idle before the
 // first tile and after the last: they stage the own query dimensions on their
@@ -748,6 +749,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kMiscOff + 160);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kMiscOff + 164);
   const uint32_t q_full = bar0 + 168;    // the query rows' tensor-map loads
+  int* s_last = reinterpret_cast<int*>(smem + kMiscOff + 176);   // [13]: per warp, the last valid key
+  static_assert(176 + 4 * (kThreads / 32) <= 256, "the per-warp key bounds fit the flags area");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t half = blockIdx.x & 1;  // value columns [256 half, +256)
@@ -817,8 +820,25 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
     cp_async16(blk_base + sw128_offset(row, c), src, bytes);
   }
 
-  const int n_tiles = (blk.n_keys + kTile - 1) / kTile;
+  // Sparse lists often end in unused entries (a context shorter than the
+  // list): the tiles past the last valid key are skipped (they would add
+  // nothing; an out-of-range entry among them is still reported).  Each
+  // thread checks one of the last kThreads entries here; only a list whose
+  // last kThreads entries are all unused is searched further (below).  The
+  // first tile's loads go by the whole list.
   bool bad_index = false;
+  if constexpr (K == Keys::kSparse) {
+    const int j = blk.n_keys - 1 - static_cast<int>(threadIdx.x);
+    int last = -1;
+    if (j >= 0) {
+      const int32_t raw = __ldg(blk.idx + j);
+      if (raw_valid<K>(a, raw)) last = j;
+      else if (raw >= 0) bad_index = true;
+    }
+    last = __reduce_max_sync(0xffffffffu, last);
+    if (lane == 0) s_last[warp] = last;
+  }
+  const int n_tiles0 = (blk.n_keys + kTile - 1) / kTile;
   const bool is_softmax = warp < kSoftmaxWarps;
   const bool is_producer = warp >= kFirstProducerWarp && warp < kMmaWarp;
   // Producer row r of a tile, dimension block k of its parts (see below).
@@ -836,7 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
     cur = key_entry<K>(a, blk, key_raw<K>(a, blk, r), r, bad_index);
     raw_next = key_raw<K>(a, blk, kTile + r);
     raw_next2 = key_raw<K>(a, blk, 2 * kTile + r);
-    if (n_tiles > 0) {
+    if (n_tiles0 > 0) {
       load_part<F, true>(cur, a_nope0, k, ra);
       load_part<F, false>(cur, b_nope0, k, rb);
     }
@@ -849,6 +869,23 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *s_tmem;
+  int n_tiles = n_tiles0;
+  int last_key = -1;
+  if constexpr (K == Keys::kSparse) {
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) last_key = max(last_key, s_last[w]);
+    if (last_key < 0 && blk.n_keys > kThreads) {
+      // the last kThreads entries are all unused: search the rest of the list
+      int last = -1;
+      for (int j = threadIdx.x; j < blk.n_keys - kThreads; j += kThreads) {
+        const int32_t raw = __ldg(blk.idx + j);
+        if (raw_valid<K>(a, raw)) last = j;
+        else if (raw >= 0) bad_index = true;
+      }
+      last = __reduce_max_sync(0xffffffffu, last);
+      if (lane == 0) reinterpret_cast<volatile int*>(smem + kLastOff)[warp] = last;
+    }
+  }
   // The CTA's own 256 NoPE query dimensions: staging -> TMEM (softmax warp w:
   // lane = row 32 w + lane), once the tensor-map loads have landed.
   if (is_softmax && (!a.q_tma || warp_wait_or_abort(q_full, 0, s_abort))) {
@@ -870,6 +907,14 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
+  if constexpr (K == Keys::kSparse) {
+    if (last_key < 0 && blk.n_keys > kThreads) {
+#pragma unroll
+      for (int w = 0; w < kThreads / 32; ++w)
+        last_key = max(last_key, reinterpret_cast<volatile int*>(smem + kLastOff)[w]);
+    }
+    n_tiles = (last_key + kTile) / kTile;            // tiles up to the last valid key
+  }
 
   int mma_issued = 0;                    // MMA thread: any MMA issued
   float m = -INFINITY, l = 0.0f;         // softmax: reference max (base 2), partial sum of the row

@@ -777,3 +777,31 @@ def test_workspace_prefill_full_size_equals_fused(kvq, oracle_mod, threads, fmt)
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
     assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32))
+
+
+def test_trailing_unused_entries(kvq, oracle_mod):
+    """Lists that end in unused entries (a context shorter than the list):
+    the tiles past the last valid key are skipped.  Token 0 keeps 348 of 2048
+    entries and has an out-of-range slot among its unused tail (still
+    reported), token 1 keeps 300, token 2 none.  The result equals, bit for
+    bit, the one over the lists cut after entry 348, and the oracle's."""
+    w = wl.make_attention("trailing", 3, 128, 2048, 64, 64, 571, p_unused=0.1)
+    idx = wl.host(w.indices).copy()
+    idx[:, 348:] = -1
+    idx[1, 300:] = -1
+    idx[2, :] = -1
+    idx[0, 2000] = 64 * 64 + 5                        # past the cache
+    cache = host_cache(oracle_mod, w.fill)
+    dcache = torch.from_numpy(cache).to(DEV)
+    q = w.q.to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, lse = kvq.kvq_sparse_mla_attention_nvfp4_ds_mla(q, torch.from_numpy(idx).to(DEV), dcache, w.softmax_scale,
+                                                         status=status)
+    cut = np.ascontiguousarray(idx[:, :348])
+    out2, lse2 = kvq.kvq_sparse_mla_attention_nvfp4_ds_mla(q, torch.from_numpy(cut).to(DEV), dcache, w.softmax_scale)
+    torch.cuda.synchronize()
+    assert int(status.item()) == kvq.STATUS_BAD_INDEX
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
+    idx[0, 2000] = -1
+    check(oracle_mod, cache, w.q, idx, w.softmax_scale, out, lse)
