@@ -805,3 +805,39 @@ def test_trailing_unused_entries(kvq, oracle_mod):
     assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
     idx[0, 2000] = -1
     check(oracle_mod, cache, w.q, idx, w.softmax_scale, out, lse)
+
+
+def test_split_decode_on_a_side_stream_without_lse(kvq, oracle_mod):
+    """The split decode's three launches (range marks, partial rows, combine)
+    all go to the caller's stream: run on a side stream, no lse output,
+    read after that stream alone is synchronised."""
+    w = wl.make_attention("split side stream", 3, 64, 512, 16, 64, 581, p_unused=0.1)
+    cache = host_cache(oracle_mod, w.fill)
+    dcache = torch.from_numpy(cache).to(DEV)
+    q, idx = w.q.to(DEV), w.indices.to(DEV)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    out = torch.full((3, 64, 512), -7.0, dtype=torch.bfloat16, device=DEV)
+    with torch.cuda.stream(side):
+        kvq.kvq_sparse_mla_attention_split_nvfp4_ds_mla(q, idx, dcache, w.softmax_scale, num_splits=4, out=out,
+                                                        lse=False, stream=side)
+    side.synchronize()
+    _, lse_ref, _ = oracle_mod.sparse_mla_attention_nvfp4_ds_mla(wl.bf16_bits(w.q), wl.host(w.indices), cache,
+                                                                 w.softmax_scale)
+    check(oracle_mod, cache, w.q, wl.host(w.indices), w.softmax_scale, out,
+          torch.from_numpy(lse_ref.astype(np.float32)))
+
+
+def test_workspace_prefill_without_lse(kvq, oracle_mod):
+    w = wl.make_prefill("ws no lse", [300, 64], [3, 2], 32, 16, 64, 582)
+    cache = host_cache(oracle_mod, w.fill)
+    ws, starts = gather_workspace(kvq, w, torch.from_numpy(cache).to(DEV), "nvfp4")
+    out, none = kvq.kvq_prefill_mla_attention_workspace(w.q.to(DEV), w.query_start.to(DEV), w.context_lens.to(DEV),
+                                                        starts, ws, w.softmax_scale, w.max_query_len, lse=False)
+    ref_out, ref_lse = kvq.kvq_prefill_mla_attention_workspace(w.q.to(DEV), w.query_start.to(DEV),
+                                                               w.context_lens.to(DEV), starts, ws, w.softmax_scale,
+                                                               w.max_query_len)
+    torch.cuda.synchronize()
+    assert none is None
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    check_prefill(oracle_mod, cache, w, out, ref_lse)
