@@ -490,13 +490,15 @@ def test_dequant_per_head_random_cache_and_bad_slots(kvq, oracle_mod, layout):
     run_dequant(kvq, oracle_mod, w, cache, status_expected=kvq.STATUS_BAD_INDEX, layout=layout)
 
 
-def test_dequant_per_head_full_size(kvq, oracle_mod, threads):
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_dequant_per_head_full_size(kvq, oracle_mod, threads, layout):
     w = wl.per_head()
     T, H, D = w.key.shape
-    cache = np.zeros((w.num_pages, 2, w.block_size, H, kvq.nvfp4_full_dim(D)), np.uint8)
+    shape = (w.block_size, H) if layout == "NHD" else (H, w.block_size)
+    cache = np.zeros((w.num_pages, 2, *shape, kvq.nvfp4_full_dim(D)), np.uint8)
     oracle_mod.reshape_and_cache_nvfp4(wl.bf16_bits(w.key), wl.bf16_bits(w.value), wl.host(w.slot_mapping),
-                                       cache, threads=threads)
-    run_dequant(kvq, oracle_mod, w, cache, threads=threads)
+                                       cache, threads=threads, layout=layout)
+    run_dequant(kvq, oracle_mod, w, cache, threads=threads, layout=layout)
 
 
 # --------------------------------------------------------------------------
