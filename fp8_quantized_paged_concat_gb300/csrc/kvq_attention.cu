@@ -384,6 +384,21 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction (three-input max, sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// lo_acc += the bf16 in bits 15:0 of p, hi_acc += the one in bits 31:16, each
+// an fp32 addition of the exactly widened bf16 (mixed-precision add, one
+// instruction each: no shift or mask to widen the halves first).
+__device__ __forceinline__ void add_bf16x2(float& lo_acc, float& hi_acc, uint32_t p) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+      : "+f"(lo_acc), "+f"(hi_acc) : "r"(p));
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -430,18 +445,19 @@ __device__ __forceinline__ GroupTable group_table(uint32_t sf_code) {
 // the group's tables: one byte permute gathers the low (or high) bytes of
 // four values' products, two more interleave them into bf16 pairs.  A code's
 // sign bit is the top bit of a byte of x (odd values) or of x << 4 (even
-// values); a byte permute in sign-replicate mode spreads it over a byte and
-// it is XORed into bit 15 of its bf16 (so a negative scale byte still gives
-// the product's sign).  An exhaustive CPU emulation of this byte logic
-// against the exact products over every code and scale byte was run.
+// values); one byte permute in sign-replicate mode spreads the signs of four
+// values over four bytes, in the order of their high bytes, and the sign bits
+// are XORed into those high bytes before the interleave (so a negative scale
+// byte still gives the product's sign): 15 operations per 8 values.  An
+// exhaustive CPU emulation of the byte logic against the exact products over
+// every code and scale byte was run, and of this sign placement against the
+// earlier one (sign XORed into each bf16 pair after the interleave).
 __device__ __forceinline__ uint4 e2m1x8_bf16(uint32_t x, const GroupTable& t) {
   const uint32_t mag = x & 0x77777777u, mag_hi = mag >> 16, x4 = x << 4;
-  const uint32_t l0 = prmt(t.lo_a, t.lo_b, mag), h0 = prmt(t.hi_a, t.hi_b, mag);
-  const uint32_t l1 = prmt(t.lo_a, t.lo_b, mag_hi), h1 = prmt(t.hi_a, t.hi_b, mag_hi);
-  return make_uint4(prmt(l0, h0, 0x5140) ^ (prmt(x4, x, 0xC080) & 0x80008000u),
-                    prmt(l0, h0, 0x7362) ^ (prmt(x4, x, 0xD090) & 0x80008000u),
-                    prmt(l1, h1, 0x5140) ^ (prmt(x4, x, 0xE0A0) & 0x80008000u),
-                    prmt(l1, h1, 0x7362) ^ (prmt(x4, x, 0xF0B0) & 0x80008000u));
+  const uint32_t s0 = prmt(x, x4, 0x9D8C), s1 = prmt(x, x4, 0xBFAE);   // values 0-3, 4-7
+  const uint32_t l0 = prmt(t.lo_a, t.lo_b, mag), h0 = prmt(t.hi_a, t.hi_b, mag) ^ (s0 & 0x80808080u);
+  const uint32_t l1 = prmt(t.lo_a, t.lo_b, mag_hi), h1 = prmt(t.hi_a, t.hi_b, mag_hi) ^ (s1 & 0x80808080u);
+  return make_uint4(prmt(l0, h0, 0x5140), prmt(l0, h0, 0x7362), prmt(l1, h1, 0x5140), prmt(l1, h1, 0x7362));
 }
 
 // 16 e4m3 codes times their tile's fp32 scale -> 16 bf16, as the fp8 gather
@@ -958,11 +974,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
         s[i + 1] = y0.y;
         s[i + 2] = y1.x;
         s[i + 3] = y1.y;
-        mx[(i >> 1) & 7] = fmaxf(mx[(i >> 1) & 7], fmaxf(y0.x, y0.y));
-        mx[((i >> 1) + 1) & 7] = fmaxf(mx[((i >> 1) + 1) & 7], fmaxf(y1.x, y1.y));
+        mx[(i >> 1) & 7] = fmax3(mx[(i >> 1) & 7], y0.x, y0.y);
+        mx[((i >> 1) + 1) & 7] = fmax3(mx[((i >> 1) + 1) & 7], y1.x, y1.y);
       }
-      const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float tmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
       // Lazy rescaling: the reference max moves only when the tile's max
       // exceeds it by more than 2^8 (weights stay below 256 otherwise).
       const bool grow = tmax > m + kRescaleLog2;
@@ -977,7 +992,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
       for (int i = 0; i < 32; ++i) {
         const float2 d = fadd2(make_float2(s[2 * i], s[2 * i + 1]), make_float2(-m_use, -m_use));
         pk[i] = pack_bf16x2(ex2(d.x), ex2(d.y));
-        ps[i & 3] = fadd2(ps[i & 3], make_float2(bf16_lo(pk[i]), bf16_hi(pk[i])));
+        add_bf16x2(ps[i & 3].x, ps[i & 3].y, pk[i]);
       }
       const float2 p01 = fadd2(ps[0], ps[1]), p23 = fadd2(ps[2], ps[3]);
       const float2 psum2 = fadd2(p01, p23);
