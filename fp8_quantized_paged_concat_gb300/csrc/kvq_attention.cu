@@ -430,9 +430,8 @@ struct GroupTable {
   uint32_t lo_a, lo_b, hi_a, hi_b;       // low / high bytes of products 0-3 and 4-7
 };
 
-__device__ __forceinline__ GroupTable group_table(uint32_t sf_code) {
-  const uint32_t sf = __float_as_uint(e4m3_to_float(sf_code)) >> 16;   // exact bf16
-  const uint32_t sf2 = sf | (sf << 16);
+__device__ __forceinline__ GroupTable group_table(float sf_f32) {
+  const uint32_t sf2 = prmt(__float_as_uint(sf_f32), 0u, 0x3232);       // its bf16 (exact) in both halves
   const uint32_t t0 = bf16x2_mul(0x3F000000u, sf2);   // (0, 0.5) * sf
   const uint32_t t1 = bf16x2_mul(0x3FC03F80u, sf2);   // (1, 1.5) * sf
   const uint32_t t2 = bf16x2_mul(0x40404000u, sf2);   // (2, 3) * sf
@@ -705,12 +704,17 @@ __device__ __forceinline__ void load_part(const uint8_t* p, int nope0, int k, Pa
 // key decodes to zeros.
 template <Entry F, bool kRope>
 __device__ __forceinline__ void decode_part(bool valid, const PartRegs<F, kRope>& e, uint4 (&v)[kRope ? 10 : 8]) {
+  float2 sf01, sf23;                     // nvfp4: the 4 group scales, exact
+  if constexpr (F == Entry::kNvfp4) {
+    sf01 = __half22float2(e4m3x2_to_half2(e.sf));
+    sf23 = __half22float2(e4m3x2_to_half2(e.sf >> 16));
+  }
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     v[2 * g] = v[2 * g + 1] = make_uint4(0, 0, 0, 0);
     if (valid) {
       if constexpr (F == Entry::kNvfp4) {
-        const GroupTable t = group_table((e.sf >> (8 * g)) & 0xffu);
+        const GroupTable t = group_table(g == 0 ? sf01.x : g == 1 ? sf01.y : g == 2 ? sf23.x : sf23.y);
         const uint4& c = e.code[g >> 1];
         v[2 * g] = e2m1x8_bf16((g & 1) ? c.z : c.x, t);
         v[2 * g + 1] = e2m1x8_bf16((g & 1) ? c.w : c.y, t);
@@ -738,11 +742,15 @@ __device__ __forceinline__ void decode_part(bool valid, const PartRegs<F, kRope>
 template <bool kRope>
 __device__ __forceinline__ void write_part(uint32_t blk, uint32_t rope_blk, uint32_t r, int k,
                                            const uint4 (&v)[kRope ? 10 : 8]) {
+  // blocks are 1024-byte aligned: row r's chunk c is at (blk + 128 r + 16 (r % 8)) XOR 16 c
+  const uint32_t row = r * 128u + ((r & 7u) << 4);
+  const uint32_t b = blk + row;
 #pragma unroll
-  for (int c = 0; c < 8; ++c) st_shared16(blk + sw128_offset(r, c), v[c]);
+  for (int c = 0; c < 8; ++c) st_shared16(b ^ (static_cast<uint32_t>(c) << 4), v[c]);
   if constexpr (kRope) {
-    st_shared16(rope_blk + sw128_offset(r, 2 * k), v[8]);
-    st_shared16(rope_blk + sw128_offset(r, 2 * k + 1), v[9]);
+    const uint32_t rb = rope_blk + row;
+    st_shared16(rb ^ (static_cast<uint32_t>(2 * k) << 4), v[8]);
+    st_shared16(rb ^ (static_cast<uint32_t>(2 * k + 1) << 4), v[9]);
   }
 }
 
