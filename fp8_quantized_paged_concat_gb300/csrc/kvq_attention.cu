@@ -674,12 +674,17 @@ template <bool kRope> struct PartRegs<Entry::kFp8, kRope> {
   uint4 rope[2];                         // group A: 16 bf16 RoPE values
 };
 
-// Issues the loads of this thread's share of one key's entry (p = nullptr:
-// nothing to load): NoPE dimensions nope0 .. nope0 + 63 and, with kRope, the
-// RoPE dimensions 16 k .. 16 k + 15.
+// Issues the loads of this thread's share of one key's entry: NoPE
+// dimensions nope0 .. nope0 + 63 and, with kRope, the RoPE dimensions
+// 16 k .. 16 k + 15.  For p = nullptr (an unused key) the registers are
+// zeroed instead: zero codes and a zero scale decode to zeros, so the decode
+// needs no per-value select.
 template <Entry F, bool kRope>
 __device__ __forceinline__ void load_part(const uint8_t* p, int nope0, int k, PartRegs<F, kRope>& e) {
-  if (p == nullptr) return;
+  if (p == nullptr) {
+    e = PartRegs<F, kRope>{};
+    return;
+  }
   if constexpr (F == Entry::kNvfp4) {
     const uint4* c = reinterpret_cast<const uint4*>(p + nope0 / 2);
     e.code[0] = __ldg(c);
@@ -700,10 +705,10 @@ __device__ __forceinline__ void load_part(const uint8_t* p, int nope0, int k, Pa
 }
 
 // Decodes this thread's share of a key row into registers: chunks 2g, 2g + 1
-// hold NoPE group g and, with kRope, v[8], v[9] the RoPE values.  An unused
-// key decodes to zeros.
+// hold NoPE group g and, with kRope, v[8], v[9] the RoPE values (an unused
+// key's zeroed registers decode to zeros).
 template <Entry F, bool kRope>
-__device__ __forceinline__ void decode_part(bool valid, const PartRegs<F, kRope>& e, uint4 (&v)[kRope ? 10 : 8]) {
+__device__ __forceinline__ void decode_part(const PartRegs<F, kRope>& e, uint4 (&v)[kRope ? 10 : 8]) {
   float2 sf01, sf23;                     // nvfp4: the 4 group scales, exact
   if constexpr (F == Entry::kNvfp4) {
     sf01 = __half22float2(e4m3x2_to_half2(e.sf));
@@ -711,28 +716,22 @@ __device__ __forceinline__ void decode_part(bool valid, const PartRegs<F, kRope>
   }
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
-    v[2 * g] = v[2 * g + 1] = make_uint4(0, 0, 0, 0);
-    if (valid) {
-      if constexpr (F == Entry::kNvfp4) {
-        const GroupTable t = group_table(g == 0 ? sf01.x : g == 1 ? sf01.y : g == 2 ? sf23.x : sf23.y);
-        const uint4& c = e.code[g >> 1];
-        v[2 * g] = e2m1x8_bf16((g & 1) ? c.z : c.x, t);
-        v[2 * g + 1] = e2m1x8_bf16((g & 1) ? c.w : c.y, t);
-      } else {
-        e4m3x16_scaled(e.code[g], e.sc, v[2 * g], v[2 * g + 1]);
-      }
+    if constexpr (F == Entry::kNvfp4) {
+      const GroupTable t = group_table(g == 0 ? sf01.x : g == 1 ? sf01.y : g == 2 ? sf23.x : sf23.y);
+      const uint4& c = e.code[g >> 1];
+      v[2 * g] = e2m1x8_bf16((g & 1) ? c.z : c.x, t);
+      v[2 * g + 1] = e2m1x8_bf16((g & 1) ? c.w : c.y, t);
+    } else {
+      e4m3x16_scaled(e.code[g], e.sc, v[2 * g], v[2 * g + 1]);
     }
   }
   if constexpr (kRope) {
-    v[8] = v[9] = make_uint4(0, 0, 0, 0);
-    if (valid) {
-      if constexpr (F == Entry::kNvfp4) {
-        v[8] = e4m3x8_bf16(make_uint2(e.rope.x, e.rope.y));
-        v[9] = e4m3x8_bf16(make_uint2(e.rope.z, e.rope.w));
-      } else {
-        v[8] = e.rope[0];                              // bf16 as stored
-        v[9] = e.rope[1];
-      }
+    if constexpr (F == Entry::kNvfp4) {
+      v[8] = e4m3x8_bf16(make_uint2(e.rope.x, e.rope.y));
+      v[9] = e4m3x8_bf16(make_uint2(e.rope.z, e.rope.w));
+    } else {
+      v[8] = e.rope[0];                                  // bf16 as stored
+      v[9] = e.rope[1];
     }
   }
 }
@@ -1086,7 +1085,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
         // group A: decoded into registers, then stored once stage t % kAStages
         // is free (the group-A K-steps of tile t - kAStages are done)
         uint4 va[10];
-        decode_part<F, true>(cur != nullptr, ra, va);
+        decode_part<F, true>(ra, va);
         const int sa = t % kAStages;
         if (t >= kAStages && !warp_wait_or_abort(a_empty0 + 8 * sa, (t / kAStages - 1) & 1, s_abort)) break;
         const uint32_t astage = base + kAOff + sa * kAStage;
@@ -1101,7 +1100,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
         if (t + 1 < n_tiles) load_part<F, true>(next, a_nope0, k, ra);
         // group B: stage t % kBStages is free once P V of tile t - kBStages is done
         uint4 vb[8];
-        decode_part<F, false>(cur != nullptr, rb, vb);
+        decode_part<F, false>(rb, vb);
         const int sb = t % kBStages;
         if (t >= kBStages && !warp_wait_or_abort(b_empty0 + 8 * sb, (t / kBStages - 1) & 1, s_abort)) break;
         write_part<false>(base + kBOff + sb * kBStage + k * kKBlock, 0, r, k, vb);
