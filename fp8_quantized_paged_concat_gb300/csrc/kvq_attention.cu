@@ -1111,6 +1111,23 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
         cur = next;
         raw_next = raw_next2;
         raw_next2 = key_raw<K>(a, blk, (t + 3) * kTile + r);
+        if constexpr (F == Entry::kFp8) {
+          // 656-byte entries: the lines of the entry two tiles ahead are asked
+          // into L2 now (the four lanes of a row take one line each, then the
+          // rest), so that next tile's register loads of it find them there.
+          // The nvfp4 entries' loads are already covered; their prefetch
+          // only costs issue slots.
+          if (t + 2 < n_tiles && raw_valid<K>(a, raw_next)) {
+            bool unused = false;
+            const uint8_t* p2 = key_entry<K>(a, blk, raw_next, (t + 2) * kTile + r, unused);
+            constexpr int kBytes = KVQ_FP8_DS_MLA_ENTRY_BYTES;
+#pragma unroll
+            for (int o = 0; o < kBytes + 127; o += 512) {
+              const int off = o + 128 * k;
+              if (off < kBytes + 127) prefetch_l2_line(p2 + (off < kBytes ? off : kBytes - 1));
+            }
+          }
+        }
       }
     }
   } else if (lane == 0) {
