@@ -1111,12 +1111,13 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attention_kernel(const Attent
         cur = next;
         raw_next = raw_next2;
         raw_next2 = key_raw<K>(a, blk, (t + 3) * kTile + r);
-        if constexpr (F == Entry::kFp8) {
-          // 656-byte entries: the lines of the entry two tiles ahead are asked
-          // into L2 now (the four lanes of a row take one line each, then the
-          // rest), so that next tile's register loads of it find them there.
-          // The nvfp4 entries' loads are already covered; their prefetch
-          // only costs issue slots.
+        if constexpr (F == Entry::kFp8 && K == Keys::kSparse) {
+          // Scattered 656-byte entries: the lines of the entry two tiles ahead
+          // are asked into L2 now (the four lanes of a row take one line
+          // each, then the rest), so that next tile's register loads of it
+          // find them there.  The nvfp4 entries' loads, and a dense prefill's
+          // consecutive entries of one block, are already covered; there the
+          // prefetch only costs issue slots.
           if (t + 2 < n_tiles && raw_valid<K>(a, raw_next)) {
             bool unused = false;
             const uint8_t* p2 = key_entry<K>(a, blk, raw_next, (t + 2) * kTile + r, unused);
