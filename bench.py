@@ -956,23 +956,30 @@ def run_workspace_prefill_only(query_len: int) -> int:
     return 0
 
 
-def run_attention_only(tokens: int) -> int:
-    """Profiler hook: the attention alone on a small cache (a few hundred MB)."""
+def run_attention_only(tokens: int, fmt: str = "nvfp4_ds_mla") -> int:
+    """Profiler hook: the attention alone on a small cache (a few hundred MB)
+    of either entry format."""
     import fp8_quantized_paged_concat_gb300 as kvq
     kvq.load_library()
     dev = torch.device("cuda:0")
-    fill = wl.make_fill("attention profiling fill 8192x64", 8192, 64, 1006, dev, rng="device")
-    cache = torch.zeros((8192, 64, 352), dtype=torch.uint8, device=dev)
-    kvq.kvq_write_nvfp4_ds_mla(fill.kv_c, fill.k_pe, cache, fill.slot_mapping)
+    entry = 352 if fmt == "nvfp4_ds_mla" else 656
+    fill = wl.make_fill("attention profiling fill 8192x64", 8192, 64, 1006, dev, entry_bytes=entry, rng="device")
+    cache = torch.zeros((8192, 64, entry), dtype=torch.uint8, device=dev)
+    if fmt == "nvfp4_ds_mla":
+        kvq.kvq_write_nvfp4_ds_mla(fill.kv_c, fill.k_pe, cache, fill.slot_mapping)
+        attend = kvq.kvq_sparse_mla_attention_nvfp4_ds_mla
+    else:
+        kvq.kvq_write_fp8_ds_mla(fill.kv_c, fill.k_pe, cache, fill.slot_mapping)
+        attend = kvq.kvq_sparse_mla_attention_fp8_ds_mla
     w = wl.make_attention("attention profiling case", tokens, 128, 2048, 8192, 64, 1006, dev, p_unused=0.1,
                           fill=fill, rng="device")
     for r in range(3):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        kvq.kvq_sparse_mla_attention_nvfp4_ds_mla(w.q, w.indices, cache, w.softmax_scale)
+        attend(w.q, w.indices, cache, w.softmax_scale)
         b.record()
         torch.cuda.synchronize()
-        print(f"sparse_mla_attention T={tokens}: {a.elapsed_time(b) * 1e3:.1f} us", flush=True)
+        print(f"sparse_mla_attention {fmt} T={tokens}: {a.elapsed_time(b) * 1e3:.1f} us", flush=True)
     return 0
 
 
@@ -1034,6 +1041,8 @@ def main(argv=None):
     p.add_argument("--attention-only", type=int, default=0, metavar="T",
                    help="profiler hook: T decode tokens of the sparse MLA attention (128 heads, top-2048 "
                         "over an 8192 x 64 cache), 3 launches, times printed; nothing else runs")
+    p.add_argument("--attention-fp8-only", type=int, default=0, metavar="T",
+                   help="profiler hook: the same over a fp8_ds_mla cache of 8192 x 64 656-byte entries")
     p.add_argument("--workspace-prefill-only", type=int, default=0, metavar="Q",
                    help="profiler hook: the prefill case by gather + prefill over the workspace")
     p.add_argument("--prefill-only", type=int, default=0, metavar="Q",
@@ -1045,6 +1054,8 @@ def main(argv=None):
     args = p.parse_args(argv)
     if args.attention_only > 0:
         return run_attention_only(args.attention_only)
+    if args.attention_fp8_only > 0:
+        return run_attention_only(args.attention_fp8_only, "fp8_ds_mla")
     if args.kernel_only:
         return run_kernel_only(args.kernel_only)
     if args.prefill_only > 0:
